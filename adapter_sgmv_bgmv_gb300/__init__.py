@@ -1,0 +1,271 @@
+"""GB300 (sm_103a) heterogeneous multi-LoRA delta: y_i += s_k (x_i A_k) B_k over a
+batch whose rows are grouped by adapter id, with paged adapter storage, released
+rows skipped, and an in-place merge / unmerge of W +/- s A B.
+
+Every step runs in the CUDA kernels of ``liblora.so`` behind the C ABI declared in
+``include/lora.h``; this module only marshals torch tensors (device memory and
+streams) and numpy id arrays into those calls, under the same names.  Importing it
+without the built library raises: there is no other implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import numpy as np
+import torch
+
+from . import _lib
+
+__all__ = ["LoraError", "Context", "AdapterTable", "lora_plan_build", "lora_shrink",
+           "lora_expand", "lora_fused", "lora_merge", "lora_unmerge", "lora_tune_shape",
+           "KIND_ROWS_FUSED", "KIND_SHRINK", "KIND_EXPAND", "KIND_TILE_FUSED", "KIND_MERGE",
+           "library_path"]
+
+KIND_ROWS_FUSED, KIND_SHRINK, KIND_EXPAND, KIND_TILE_FUSED, KIND_MERGE = range(5)
+ERROR_NAMES = {0: "LORA_OK", -1: "LORA_E_INVAL", -2: "LORA_E_RANK", -3: "LORA_E_ADAPTER",
+               -4: "LORA_E_NOT_RESIDENT", -5: "LORA_E_PAGE", -6: "LORA_E_CUDA",
+               -7: "LORA_E_TIMEOUT", -8: "LORA_E_NOMEM", -9: "LORA_E_CAPACITY",
+               -10: "LORA_E_UNSUPPORTED", -11: "LORA_E_IO"}
+
+_L = _lib.load()
+
+
+def library_path() -> str:
+    return _lib.LIB_PATH
+
+
+class LoraError(RuntimeError):
+    def __init__(self, code: int, detail: str = ""):
+        self.code = code
+        self.name = ERROR_NAMES.get(code, str(code))
+        msg = f"{self.name}: {_L.lora_strerror(code).decode()}"
+        if detail:
+            msg += f" ({detail})"
+        super().__init__(msg)
+
+
+def _check(rc: int, ctx: "Context | None" = None) -> int:
+    if rc < 0:
+        detail = ""
+        if rc == -6 and ctx is not None and ctx.handle:
+            detail = (_L.lora_last_cuda_error(ctx.handle) or b"").decode()
+        raise LoraError(rc, detail)
+    return rc
+
+
+def _stream(stream, device) -> int:
+    if stream is None:
+        return torch.cuda.current_stream(device).cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _dev_ptr(t: torch.Tensor, what: str) -> int:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{what} must be a CUDA tensor")
+    return t.data_ptr()
+
+
+def _ids(ids) -> np.ndarray:
+    a = np.ascontiguousarray(np.asarray(ids), dtype=np.int32)
+    if a.ndim != 1:
+        raise ValueError("ids must be one-dimensional")
+    return a
+
+
+def _rows(t: torch.Tensor, what: str):
+    """(pointer, row stride in elements, columns) of a 2-D row-major 16-bit tensor."""
+    if t.dim() != 2 or t.element_size() != 2 or t.stride(1) != 1:
+        raise ValueError(f"{what} must be a 2-D row-major bf16 tensor")
+    return _dev_ptr(t, what), t.stride(0), t.shape[1]
+
+
+class Context:
+    """A library context on one device (plan staging buffers, status word, tile table)."""
+
+    def __init__(self, device: int = 0, max_rows: int = 1 << 16, max_rank: int = 64):
+        """device = -1: host-only context (plans and tile tables, no launches)."""
+        if isinstance(device, int) and device < 0:
+            self.device, idx = None, -1
+        else:
+            self.device = torch.device("cuda", device) if isinstance(device, int) else torch.device(device)
+            idx = self.device.index or 0
+        h = ctypes.c_void_p()
+        _check(_L.lora_ctx_create(idx, int(max_rows), int(max_rank), ctypes.byref(h)))
+        self.handle = h.value
+
+    def close(self):
+        if self.handle:
+            _L.lora_ctx_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def tiles_load(self, path: str):
+        _check(_L.lora_tiles_load(self.handle, path.encode()), self)
+
+    def tiles_save(self, path: str):
+        _check(_L.lora_tiles_save(self.handle, path.encode()), self)
+
+    def tiles_count(self) -> int:
+        return int(_L.lora_tiles_count(self.handle))
+
+    def sync_status(self, stream=None) -> int:
+        """Synchronize and read back the device status word (raises on a timeout)."""
+        return _check(_L.lora_sync_status(self.handle, _stream(stream, self.device)), self)
+
+    def profile_begin(self):
+        """Start bracketing every kernel launch with CUDA events."""
+        _check(_L.lora_profile_begin(self.handle), self)
+
+    def profile_end(self):
+        """Stop; returns {family: (device ms, launches)} for row / tile / merge kernels."""
+        ms = (ctypes.c_double * 3)()
+        n = (ctypes.c_int64 * 3)()
+        _check(_L.lora_profile_end(self.handle, ms, n), self)
+        return {name: (ms[i], int(n[i])) for i, name in enumerate(("rows", "tile", "merge"))}
+
+    def last_path(self):
+        """(path bits, launches) of the last call: 1 row-gather, 2 tensor-core tile,
+        4 merge."""
+        n = ctypes.c_int()
+        p = _L.lora_last_path(self.handle, ctypes.byref(n))
+        return p, n.value
+
+
+class AdapterTable:
+    """Registered adapter table over caller-owned device pools of bf16 pages.
+
+    a_pool / b_pool: CUDA tensors [n_pages, page_width] (bf16 or 16-bit ints); may be
+    the same tensor.  rank, scale: [n_adapters]; a_pages, b_pages: [n_adapters,
+    max_rank] page ids (-1 = not resident).  The pools are kept referenced here so
+    they outlive the table."""
+
+    def __init__(self, ctx: Context, a_pool: torch.Tensor, b_pool: torch.Tensor, rank, scale,
+                 a_pages, b_pages):
+        self.ctx = ctx
+        self.a_pool, self.b_pool = a_pool, b_pool
+        for t, nm in ((a_pool, "a_pool"), (b_pool, "b_pool")):
+            if t.dim() != 2 or t.element_size() != 2 or not t.is_contiguous():
+                raise ValueError(f"{nm} must be a contiguous 2-D 16-bit tensor")
+        self.rank = np.ascontiguousarray(rank, dtype=np.int32)
+        self.scale = np.ascontiguousarray(scale, dtype=np.float32)
+        self.a_pages = np.ascontiguousarray(a_pages, dtype=np.int32)
+        self.b_pages = np.ascontiguousarray(b_pages, dtype=np.int32)
+        n_adapters, max_rank = self.a_pages.shape
+        self.n_adapters, self.max_rank = n_adapters, max_rank
+        h = ctypes.c_void_p()
+        if ctx.device is None:      # host-only context: pools are never dereferenced
+            pa, pb = a_pool.data_ptr(), b_pool.data_ptr()
+        else:
+            pa, pb = _dev_ptr(a_pool, "a_pool"), _dev_ptr(b_pool, "b_pool")
+        _check(_L.lora_table_create(
+            ctx.handle, pa, a_pool.shape[0], a_pool.shape[1],
+            pb, b_pool.shape[0], b_pool.shape[1], n_adapters, max_rank,
+            self.rank.ctypes.data, self.scale.ctypes.data, self.a_pages.ctypes.data,
+            self.b_pages.ctypes.data, ctypes.byref(h)), ctx)
+        self.handle = h.value
+
+    def close(self):
+        if getattr(self, "handle", None):
+            _L.lora_table_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def lora_plan_build(ctx: Context, table: AdapterTable, ids) -> dict:
+    """Host-side grouping of one batch (copies of the context's plan arrays)."""
+    ids = _ids(ids)
+    v = _lib.PlanView()
+    _check(_L.lora_plan_build(ctx.handle, table.handle, ids.ctypes.data, ids.shape[0],
+                              ctypes.byref(v)), ctx)
+
+    def arr(p, n):
+        return np.ctypeslib.as_array(p, shape=(n,)).copy() if n > 0 else np.zeros(0, np.int32)
+    return {"active_rows": arr(v.active_rows, v.n_active), "perm": arr(v.perm, v.n_active),
+            "seg_offsets": arr(v.seg_offsets, v.n_segments + 1),
+            "seg_adapter": arr(v.seg_adapter, v.n_segments),
+            "row_items": int(v.row_items), "tile_items": int(v.tile_items),
+            "rows_per_item": int(v.rows_per_item)}
+
+
+def lora_shrink(ctx: Context, table: AdapterTable, ids, x: torch.Tensor, v: torch.Tensor,
+                stream=None):
+    """v[i, :r_k] = x_i A_k (fp32) for rows with ids[i] >= 0."""
+    ids = _ids(ids)
+    px, ldx, d_in = _rows(x, "x")
+    if v.dtype != torch.float32 or v.dim() != 2 or v.stride(1) != 1:
+        raise ValueError("v must be a 2-D row-major float32 tensor")
+    _check(_L.lora_shrink(ctx.handle, table.handle, ids.ctypes.data, ids.shape[0], px, ldx,
+                          d_in, _dev_ptr(v, "v"), v.stride(0), _stream(stream, ctx.device)), ctx)
+
+
+def lora_expand(ctx: Context, table: AdapterTable, ids, v: torch.Tensor, y: torch.Tensor,
+                stream=None):
+    """y_i <- bf16(y_i + s_k v_i B_k) in place for rows with ids[i] >= 0."""
+    ids = _ids(ids)
+    py, ldy, d_out = _rows(y, "y")
+    if v.dtype != torch.float32 or v.dim() != 2 or v.stride(1) != 1:
+        raise ValueError("v must be a 2-D row-major float32 tensor")
+    _check(_L.lora_expand(ctx.handle, table.handle, ids.ctypes.data, ids.shape[0],
+                          _dev_ptr(v, "v"), v.stride(0), py, ldy, d_out,
+                          _stream(stream, ctx.device)), ctx)
+
+
+def lora_fused(ctx: Context, table: AdapterTable, ids, x: torch.Tensor, y: torch.Tensor,
+               stream=None):
+    """y_i <- bf16(y_i + s_k (x_i A_k) B_k) in place for rows with ids[i] >= 0."""
+    ids = _ids(ids)
+    px, ldx, d_in = _rows(x, "x")
+    py, ldy, d_out = _rows(y, "y")
+    _check(_L.lora_fused(ctx.handle, table.handle, ids.ctypes.data, ids.shape[0], px, ldx,
+                         d_in, py, ldy, d_out, _stream(stream, ctx.device)), ctx)
+
+
+def lora_merge(ctx: Context, table: AdapterTable, adapter: int, W: torch.Tensor, stream=None):
+    """W <- bf16(W + s_k A_k B_k) in place (W is [d_in, d_out] row-major)."""
+    pw, ldw, d_out = _rows(W, "W")
+    _check(_L.lora_merge(ctx.handle, table.handle, int(adapter), pw, ldw, W.shape[0], d_out,
+                         _stream(stream, ctx.device)), ctx)
+
+
+def lora_unmerge(ctx: Context, table: AdapterTable, adapter: int, W: torch.Tensor, stream=None):
+    """W <- bf16(W - s_k A_k B_k) in place."""
+    pw, ldw, d_out = _rows(W, "W")
+    _check(_L.lora_unmerge(ctx.handle, table.handle, int(adapter), pw, ldw, W.shape[0], d_out,
+                           _stream(stream, ctx.device)), ctx)
+
+
+def lora_tune_shape(ctx: Context, table: AdapterTable, kind: int, ids, x: torch.Tensor,
+                    y: torch.Tensor, iters: int = 20, stream=None) -> float:
+    """Offline search for one shape (see include/lora.h); returns the best time in us
+    and keeps the winning configuration in the context's table.  For KIND_MERGE, x is
+    W, y is ignored and ids[0] is the adapter."""
+    ids = _ids(ids)
+    px, ldx, d_in = _rows(x, "x")
+    if kind == KIND_MERGE:
+        py, ldy, d_out = px, ldx, d_in
+        d_in = x.shape[0]
+    else:
+        py, ldy, d_out = _rows(y, "y")
+    best = ctypes.c_float()
+    _check(_L.lora_tune_shape(ctx.handle, table.handle, int(kind), ids.ctypes.data,
+                              ids.shape[0], px, ldx, d_in, py, ldy, d_out, int(iters),
+                              ctypes.byref(best), _stream(stream, ctx.device)), ctx)
+    return float(best.value)

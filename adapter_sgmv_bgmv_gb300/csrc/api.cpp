@@ -1,0 +1,752 @@
+// C ABI of the multi-LoRA delta library (declared in include/lora.h): argument
+// checks, the host plan, staging of the plan to the device, kernel selection
+// through the shape -> configuration table, and launches on the caller's stream.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <string>
+#include <vector>
+
+#include "../../include/lora.h"
+#include "internal.h"
+#include "plan.h"
+#include "tiles.h"
+
+namespace lora {
+cudaError_t launch_merge_simt(const MergeParams &p, cudaStream_t stream);
+cudaError_t launch_merge_tc(const MergeParams &p, int n_split, cudaStream_t stream);
+bool merge_tc_supported(int d_in, int d_out, int rank);
+}  // namespace lora
+
+using namespace lora;
+
+namespace {
+
+constexpr int kSlots = 8;
+constexpr int kSms = 152;
+
+struct Slot {
+    uint8_t *host = nullptr;   // pinned
+    uint8_t *dev = nullptr;
+    size_t cap = 0;
+    cudaEvent_t ev = nullptr;
+    bool pending = false;
+};
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+inline int round_up8(int64_t v) { return int((v + 7) / 8 * 8); }
+
+}  // namespace
+
+struct lora_ctx {
+    int device = 0;
+    int64_t max_rows = 0;
+    int max_rank = 0;
+    unsigned *d_status = nullptr;
+    Slot slots[kSlots];
+    int next_slot = 0;
+    Plan plan;
+    TileTable tiles;
+    char cuda_err[256] = {0};
+    int last_path = 0;
+    int last_launches = 0;
+    // Per-launch CUDA-event timing (lora_profile_begin / lora_profile_end).
+    struct ProfEv {
+        cudaEvent_t a = nullptr, b = nullptr;
+        int family = 0;
+    };
+    bool prof = false;
+    std::vector<ProfEv> prof_ev;
+    size_t prof_used = 0;
+    RowsParamsInline inline_args;   // staging of in-parameter plans
+};
+
+struct lora_table {
+    lora_ctx *ctx = nullptr;
+    const uint16_t *a_pool = nullptr;
+    const uint16_t *b_pool = nullptr;
+    int64_t a_n_pages = 0, b_n_pages = 0;
+    int a_pw = 0, b_pw = 0;
+    int n_adapters = 0, max_rank = 0;
+    std::vector<int32_t> rank, a_pages, b_pages;
+    std::vector<float> scale;
+    std::vector<int8_t> status;        // per adapter: LORA_OK or the error a reference gets
+    int32_t *d_rank = nullptr, *d_a_pages = nullptr, *d_b_pages = nullptr;
+    float *d_scale = nullptr;
+};
+
+namespace {
+
+int cuda_fail(lora_ctx *ctx, cudaError_t e)
+{
+    if (ctx)
+        std::snprintf(ctx->cuda_err, sizeof ctx->cuda_err, "%s: %s", cudaGetErrorName(e),
+                      cudaGetErrorString(e));
+    return LORA_E_CUDA;
+}
+
+#define CUDA_TRY(ctx, expr)                          \
+    do {                                             \
+        cudaError_t _e = (expr);                     \
+        if (_e != cudaSuccess)                       \
+            return cuda_fail((ctx), _e);             \
+    } while (0)
+
+int use_device(lora_ctx *ctx)
+{
+    if (ctx->device < 0)
+        return LORA_E_UNSUPPORTED;   // host-only context
+    int cur = -1;
+    CUDA_TRY(ctx, cudaGetDevice(&cur));
+    if (cur != ctx->device)
+        CUDA_TRY(ctx, cudaSetDevice(ctx->device));
+    return LORA_OK;
+}
+
+// Take the next staging slot with room for `bytes`; waits for the slot's previous
+// upload/launches to finish before reusing its buffers.
+int acquire_slot(lora_ctx *ctx, size_t bytes, Slot **out)
+{
+    Slot &s = ctx->slots[ctx->next_slot];
+    ctx->next_slot = (ctx->next_slot + 1) % kSlots;
+    if (s.pending) {
+        CUDA_TRY(ctx, cudaEventSynchronize(s.ev));
+        s.pending = false;
+    }
+    if (bytes > s.cap) {
+        size_t cap = std::max(bytes, s.cap * 2);
+        cap = (cap + 255) & ~size_t(255);
+        if (s.host)
+            cudaFreeHost(s.host);
+        if (s.dev)
+            cudaFree(s.dev);
+        s.host = nullptr;
+        s.dev = nullptr;
+        s.cap = 0;
+        if (cudaMallocHost(reinterpret_cast<void **>(&s.host), cap) != cudaSuccess)
+            return LORA_E_NOMEM;
+        if (cudaMalloc(reinterpret_cast<void **>(&s.dev), cap) != cudaSuccess)
+            return LORA_E_NOMEM;
+        s.cap = cap;
+    }
+    *out = &s;
+    return LORA_OK;
+}
+
+int release_slot(lora_ctx *ctx, Slot *s, cudaStream_t stream)
+{
+    CUDA_TRY(ctx, cudaEventRecord(s->ev, stream));
+    s->pending = true;
+    return LORA_OK;
+}
+
+// Bracket one kernel launch with events when profiling is on.  Returns the slot.
+long prof_start(lora_ctx *ctx, int family, cudaStream_t stream)
+{
+    if (!ctx->prof)
+        return -1;
+    if (ctx->prof_used == ctx->prof_ev.size()) {
+        lora_ctx::ProfEv e;
+        if (cudaEventCreate(&e.a) != cudaSuccess || cudaEventCreate(&e.b) != cudaSuccess)
+            return -1;
+        ctx->prof_ev.push_back(e);
+    }
+    lora_ctx::ProfEv &e = ctx->prof_ev[ctx->prof_used];
+    e.family = family;
+    if (cudaEventRecord(e.a, stream) != cudaSuccess)
+        return -1;
+    return long(ctx->prof_used++);
+}
+
+void prof_stop(lora_ctx *ctx, long slot, cudaStream_t stream)
+{
+    if (slot >= 0)
+        cudaEventRecord(ctx->prof_ev[size_t(slot)].b, stream);
+}
+
+// Per-adapter status computed once when the table is registered.
+int8_t adapter_status(const lora_table *t, int k)
+{
+    const int r = t->rank[size_t(k)];
+    if (r < 8 || r > t->max_rank || r > LORA_MAX_RANK || (r % 8) != 0)
+        return LORA_E_RANK;
+    for (int j = 0; j < r; ++j) {
+        const int32_t pa = t->a_pages[size_t(k) * t->max_rank + j];
+        const int32_t pb = t->b_pages[size_t(k) * t->max_rank + j];
+        if (pa == -1 || pb == -1)
+            return LORA_E_NOT_RESIDENT;
+        if (pa < -1 || pb < -1 || pa >= t->a_n_pages || pb >= t->b_n_pages)
+            return LORA_E_PAGE;
+    }
+    return LORA_OK;
+}
+
+// Rows-kernel launch shape: cluster size C and rows per item R.
+struct RowsCfg {
+    int cluster;
+    int rows;
+};
+
+RowsCfg default_rows_cfg(int64_t n_act, int64_t n_seg, int d_in, int d_out)
+{
+    RowsCfg c{1, 1};
+    // rows per item: about the mean segment length, at most 16
+    const int64_t mean = n_seg > 0 ? ceil_div(n_act, n_seg) : 1;
+    while (c.rows < 16 && c.rows < mean)
+        c.rows <<= 1;
+    // cluster: enough CTAs to cover the GPU twice, slices of at least 128 elements
+    int64_t items = 0;
+    if (n_seg > 0)
+        items = std::max<int64_t>(n_seg, ceil_div(n_act, c.rows));
+    const int dmax = std::max(d_in, d_out);
+    while (c.cluster < 8 && items * c.cluster < 2 * kSms && dmax / (2 * c.cluster) >= 128)
+        c.cluster <<= 1;
+    return c;
+}
+
+int rows_launch_params(lora_ctx *ctx, int mode, RowsCfg cfg, int d_in, int d_out,
+                       int rank_alloc, RowsParams &p, size_t &smem)
+{
+    for (;; cfg.cluster <<= 1) {
+        if (cfg.cluster > 16)
+            return LORA_E_UNSUPPORTED;
+        p.cluster = cfg.cluster;
+        p.slice_in = std::max(8, round_up8(ceil_div(d_in, cfg.cluster)));
+        p.slice_out = std::max(8, round_up8(ceil_div(d_out, cfg.cluster)));
+        p.rows_alloc = cfg.rows;
+        p.rank_alloc = rank_alloc;
+        smem = rows_smem_bytes(mode, p.slice_in, p.slice_out, p.rows_alloc, p.rank_alloc);
+        if (smem <= size_t(rows_max_smem()))
+            return LORA_OK;
+    }
+    (void)ctx;
+}
+
+// Validate the pieces every delta call shares and build the plan.
+int prepare(lora_ctx *ctx, const lora_table *t, const int32_t *ids, int64_t n)
+{
+    if (!ctx || !t || t->ctx != ctx || n < 0 || (n > 0 && !ids))
+        return LORA_E_INVAL;
+    if (n > ctx->max_rows)
+        return LORA_E_CAPACITY;
+    int rc = plan_group(ctx->plan, ids, n, t->n_adapters);
+    if (rc != LORA_OK)
+        return rc;
+    for (int32_t k : ctx->plan.seg_adapter) {
+        const int8_t st = t->status[size_t(k)];
+        if (st != LORA_OK)
+            return st;
+        if (t->rank[size_t(k)] > ctx->max_rank)
+            return LORA_E_RANK;
+    }
+    return LORA_OK;
+}
+
+bool stride_ok(const void *p, int64_t ld, int d)
+{
+    return p && aligned16(p) && d > 0 && (d % 8) == 0 && ld >= d && (ld % 8) == 0;
+}
+
+RowsCfg choose_rows_cfg(const lora_ctx *ctx, int kind, int64_t n_act, int64_t n_seg, int d_in,
+                        int d_out, int rank)
+{
+    RowsCfg cfg = default_rows_cfg(n_act, n_seg, d_in, d_out);
+    TileCfg tc;
+    if (ctx->tiles.lookup(TileKey{kind, pow2_bucket(n_act), d_in, d_out, rank}, tc) &&
+        tc[0] >= 1 && tc[0] <= 16 && (tc[0] & (tc[0] - 1)) == 0 && tc[1] >= 1 && tc[1] <= 64) {
+        cfg.cluster = tc[0];
+        cfg.rows = tc[1];
+    }
+    return cfg;
+}
+
+// Stage items + perm and launch the row-gather kernel for the row items of the
+// current plan (cut with cfg.rows rows per item).
+int run_rows(lora_ctx *ctx, const lora_table *t, int mode, RowsCfg cfg, const void *x,
+             int64_t ldx, int d_in, float *v, int64_t ldv, void *y, int64_t ldy, int d_out,
+             cudaStream_t stream)
+{
+    Plan &pl = ctx->plan;
+    if (pl.row_items.empty())
+        return LORA_OK;
+    cfg.rows = std::max(1, pl.row_max_rows);
+    RowsParams p{};
+    size_t smem = 0;
+    int rc = rows_launch_params(ctx, mode, cfg, d_in, d_out, pl.row_max_rank, p, smem);
+    if (rc != LORA_OK)
+        return rc;
+
+    const size_t items_bytes = pl.row_items.size() * sizeof(RowItem);
+    const size_t perm_bytes = pl.perm.size() * sizeof(int32_t);
+    const bool in_params = pl.row_items.size() <= size_t(kInlineItems) &&
+                           pl.perm.size() <= size_t(kInlinePerm);
+    Slot *slot = nullptr;
+    if (!in_params) {
+        rc = acquire_slot(ctx, items_bytes + perm_bytes + 16, &slot);
+        if (rc != LORA_OK)
+            return rc;
+        std::memcpy(slot->host, pl.row_items.data(), items_bytes);
+        std::memcpy(slot->host + items_bytes, pl.perm.data(), perm_bytes);
+        CUDA_TRY(ctx, cudaMemcpyAsync(slot->dev, slot->host, items_bytes + perm_bytes,
+                                      cudaMemcpyHostToDevice, stream));
+    }
+
+    p.x = static_cast<const uint16_t *>(x);
+    p.ldx = ldx;
+    p.y = static_cast<uint16_t *>(y);
+    p.ldy = ldy;
+    p.v = v;
+    p.ldv = ldv;
+    p.a_pool = t->a_pool;
+    p.a_pw = t->a_pw;
+    p.b_pool = t->b_pool;
+    p.b_pw = t->b_pw;
+    p.a_pages = t->d_a_pages;
+    p.b_pages = t->d_b_pages;
+    p.rank = t->d_rank;
+    p.scale = t->d_scale;
+    p.items = in_params ? nullptr : reinterpret_cast<const RowItem *>(slot->dev);
+    p.perm = in_params ? nullptr : reinterpret_cast<const int32_t *>(slot->dev + items_bytes);
+    p.status = ctx->d_status;
+    p.max_rank = t->max_rank;
+    p.d_in = d_in;
+    p.d_out = d_out;
+    p.n_items = int(pl.row_items.size());
+    const long ev = prof_start(ctx, 0, stream);
+    if (in_params) {
+        RowsParamsInline &a = ctx->inline_args;
+        a.p = p;
+        std::memcpy(a.items, pl.row_items.data(), items_bytes);
+        std::memcpy(a.perm, pl.perm.data(), perm_bytes);
+        CUDA_TRY(ctx, launch_rows_inline(mode, a, smem, stream));
+    } else {
+        CUDA_TRY(ctx, launch_rows(mode, p, smem, stream));
+    }
+    prof_stop(ctx, ev, stream);
+    ctx->last_path |= 1;
+    ctx->last_launches += 1;
+    return slot ? release_slot(ctx, slot, stream) : LORA_OK;
+}
+
+int delta_call(lora_ctx *ctx, const lora_table *t, int mode, const int32_t *ids, int64_t n,
+               const void *x, int64_t ldx, int d_in, float *v, int64_t ldv, void *y,
+               int64_t ldy, int d_out, cudaStream_t stream)
+{
+    if (ctx)
+        ctx->last_path = ctx->last_launches = 0;
+    int rc = prepare(ctx, t, ids, n);
+    if (rc != LORA_OK)
+        return rc;
+    Plan &pl = ctx->plan;
+    if (pl.active.empty())
+        return LORA_OK;
+    if (mode != kExpand) {
+        if (!stride_ok(x, ldx, d_in) || d_in > t->a_pw)
+            return LORA_E_INVAL;
+    }
+    if (mode != kShrink) {
+        if (!stride_ok(y, ldy, d_out) || d_out > t->b_pw)
+            return LORA_E_INVAL;
+    }
+    if (mode != kFused) {
+        if (!v || (reinterpret_cast<uintptr_t>(v) & 3u) || ldv < 1)
+            return LORA_E_INVAL;
+        int32_t rmax = 0;
+        for (int32_t k : pl.seg_adapter)
+            rmax = std::max(rmax, t->rank[size_t(k)]);
+        if (ldv < rmax)
+            return LORA_E_INVAL;
+    }
+    rc = use_device(ctx);
+    if (rc != LORA_OK)
+        return rc;
+    const int kind = mode == kShrink ? kKindShrink : mode == kExpand ? kKindExpand : kKindRowsFused;
+    int32_t rmax = 0;
+    for (int32_t k : pl.seg_adapter)
+        rmax = std::max(rmax, t->rank[size_t(k)]);
+    const RowsCfg cfg = choose_rows_cfg(ctx, kind, int64_t(pl.active.size()),
+                                        int64_t(pl.seg_adapter.size()), d_in, d_out, rmax);
+    plan_items(pl, t->rank.data(), cfg.rows, 0);
+    return run_rows(ctx, t, mode, cfg, x, ldx, d_in, v, ldv, y, ldy, d_out, stream);
+}
+
+int merge_call(lora_ctx *ctx, const lora_table *t, int adapter, void *W, int64_t ldw,
+               int d_in, int d_out, float sign, cudaStream_t stream)
+{
+    if (ctx)
+        ctx->last_path = ctx->last_launches = 0;
+    if (!ctx || !t || t->ctx != ctx)
+        return LORA_E_INVAL;
+    if (adapter < 0 || adapter >= t->n_adapters)
+        return LORA_E_ADAPTER;
+    if (t->status[size_t(adapter)] != LORA_OK)
+        return t->status[size_t(adapter)];
+    if (!stride_ok(W, ldw, d_out) || d_in <= 0 || d_in > t->a_pw || d_out > t->b_pw)
+        return LORA_E_INVAL;
+    int rc = use_device(ctx);
+    if (rc != LORA_OK)
+        return rc;
+    MergeParams p{};
+    p.W = static_cast<uint16_t *>(W);
+    p.ldw = ldw;
+    p.a_pool = t->a_pool;
+    p.a_pw = t->a_pw;
+    p.b_pool = t->b_pool;
+    p.b_pw = t->b_pw;
+    p.a_pages = t->d_a_pages + size_t(adapter) * t->max_rank;
+    p.b_pages = t->d_b_pages + size_t(adapter) * t->max_rank;
+    p.status = ctx->d_status;
+    p.d_in = d_in;
+    p.d_out = d_out;
+    p.rank = t->rank[size_t(adapter)];
+    p.scale = sign * t->scale[size_t(adapter)];
+    const long ev = prof_start(ctx, 2, stream);
+    CUDA_TRY(ctx, launch_merge_simt(p, stream));
+    prof_stop(ctx, ev, stream);
+    ctx->last_path = 4;
+    ctx->last_launches = 1;
+    return LORA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int lora_version(void) { return 1; }
+
+const char *lora_strerror(int code)
+{
+    switch (code) {
+    case LORA_OK: return "ok";
+    case LORA_E_INVAL: return "invalid argument (null/misaligned pointer, size or stride)";
+    case LORA_E_RANK: return "unsupported rank (multiple of 8 in [8, max_rank] required)";
+    case LORA_E_ADAPTER: return "adapter id out of range";
+    case LORA_E_NOT_RESIDENT: return "referenced adapter is not resident (page id -1)";
+    case LORA_E_PAGE: return "page id beyond the pool";
+    case LORA_E_CUDA: return "CUDA runtime error";
+    case LORA_E_TIMEOUT: return "a bounded device-side wait expired";
+    case LORA_E_NOMEM: return "allocation failed";
+    case LORA_E_CAPACITY: return "more rows than the context was created for";
+    case LORA_E_UNSUPPORTED: return "shape not supported by the kernels";
+    case LORA_E_IO: return "tile-table file could not be read or written";
+    default: return "unknown status";
+    }
+}
+
+const char *lora_last_cuda_error(const lora_ctx *ctx) { return ctx ? ctx->cuda_err : ""; }
+
+int lora_ctx_create(int device, int64_t max_rows, int max_rank, lora_ctx **out)
+{
+    if (!out || max_rows < 0 || max_rank < 8 || max_rank > LORA_MAX_RANK || (max_rank % 8) ||
+        device < -1)
+        return LORA_E_INVAL;
+    *out = nullptr;
+    if (device == -1) {
+        // Host-only context: plans and tile tables, no device state, no launches.
+        lora_ctx *h = new (std::nothrow) lora_ctx();
+        if (!h)
+            return LORA_E_NOMEM;
+        h->device = -1;
+        h->max_rows = max_rows;
+        h->max_rank = max_rank;
+        *out = h;
+        return LORA_OK;
+    }
+    int ndev = 0;
+    if (cudaGetDeviceCount(&ndev) != cudaSuccess || device < 0 || device >= ndev)
+        return LORA_E_CUDA;
+    cudaDeviceProp prop{};
+    if (cudaGetDeviceProperties(&prop, device) != cudaSuccess)
+        return LORA_E_CUDA;
+    if (prop.major != 10 || prop.minor != 3)
+        return LORA_E_UNSUPPORTED;   // built for sm_103a only
+    lora_ctx *ctx = new (std::nothrow) lora_ctx();
+    if (!ctx)
+        return LORA_E_NOMEM;
+    ctx->device = device;
+    ctx->max_rows = max_rows;
+    ctx->max_rank = max_rank;
+    int prev = 0;
+    cudaGetDevice(&prev);
+    if (cudaSetDevice(device) != cudaSuccess ||
+        cudaMalloc(reinterpret_cast<void **>(&ctx->d_status), 16) != cudaSuccess ||
+        cudaMemset(ctx->d_status, 0, 16) != cudaSuccess) {
+        lora_ctx_destroy(ctx);
+        cudaSetDevice(prev);
+        return LORA_E_CUDA;
+    }
+    for (Slot &s : ctx->slots) {
+        if (cudaEventCreateWithFlags(&s.ev, cudaEventDisableTiming) != cudaSuccess) {
+            lora_ctx_destroy(ctx);
+            cudaSetDevice(prev);
+            return LORA_E_CUDA;
+        }
+    }
+    cudaSetDevice(prev);
+    *out = ctx;
+    return LORA_OK;
+}
+
+int lora_ctx_destroy(lora_ctx *ctx)
+{
+    if (!ctx)
+        return LORA_E_INVAL;
+    if (ctx->device < 0) {
+        delete ctx;
+        return LORA_OK;
+    }
+    int prev = 0;
+    cudaGetDevice(&prev);
+    cudaSetDevice(ctx->device);
+    for (auto &e : ctx->prof_ev) {
+        cudaEventDestroy(e.a);
+        cudaEventDestroy(e.b);
+    }
+    for (Slot &s : ctx->slots) {
+        if (s.ev) {
+            if (s.pending)
+                cudaEventSynchronize(s.ev);
+            cudaEventDestroy(s.ev);
+        }
+        if (s.host)
+            cudaFreeHost(s.host);
+        if (s.dev)
+            cudaFree(s.dev);
+    }
+    if (ctx->d_status)
+        cudaFree(ctx->d_status);
+    cudaSetDevice(prev);
+    delete ctx;
+    return LORA_OK;
+}
+
+int lora_table_create(lora_ctx *ctx, const void *a_pool, int64_t a_n_pages, int a_page_width,
+                      const void *b_pool, int64_t b_n_pages, int b_page_width, int n_adapters,
+                      int max_rank, const int32_t *rank_host, const float *scale_host,
+                      const int32_t *a_pages_host, const int32_t *b_pages_host,
+                      lora_table **out)
+{
+    if (!out)
+        return LORA_E_INVAL;
+    *out = nullptr;
+    if (!ctx || !a_pool || !b_pool || !aligned16(a_pool) || !aligned16(b_pool) ||
+        a_n_pages <= 0 || b_n_pages <= 0 || a_page_width <= 0 || b_page_width <= 0 ||
+        (a_page_width % 8) || (b_page_width % 8) || n_adapters <= 0 || max_rank < 8 ||
+        max_rank > LORA_MAX_RANK || !rank_host || !scale_host || !a_pages_host || !b_pages_host)
+        return LORA_E_INVAL;
+    lora_table *t = new (std::nothrow) lora_table();
+    if (!t)
+        return LORA_E_NOMEM;
+    t->ctx = ctx;
+    t->a_pool = static_cast<const uint16_t *>(a_pool);
+    t->b_pool = static_cast<const uint16_t *>(b_pool);
+    t->a_n_pages = a_n_pages;
+    t->b_n_pages = b_n_pages;
+    t->a_pw = a_page_width;
+    t->b_pw = b_page_width;
+    t->n_adapters = n_adapters;
+    t->max_rank = max_rank;
+    const size_t np = size_t(n_adapters) * size_t(max_rank);
+    t->rank.assign(rank_host, rank_host + n_adapters);
+    t->scale.assign(scale_host, scale_host + n_adapters);
+    t->a_pages.assign(a_pages_host, a_pages_host + np);
+    t->b_pages.assign(b_pages_host, b_pages_host + np);
+    t->status.resize(size_t(n_adapters));
+    for (int k = 0; k < n_adapters; ++k)
+        t->status[size_t(k)] = adapter_status(t, k);
+    // Device copies; pages of adapters that cannot be used are zeroed so that no
+    // kernel could ever form an address from them.
+    if (ctx->device < 0) {
+        *out = t;   // host-only: bookkeeping without device copies
+        return LORA_OK;
+    }
+    std::vector<int32_t> ap(t->a_pages), bp(t->b_pages);
+    for (int k = 0; k < n_adapters; ++k)
+        if (t->status[size_t(k)] != LORA_OK)
+            for (int j = 0; j < max_rank; ++j)
+                ap[size_t(k) * max_rank + j] = bp[size_t(k) * max_rank + j] = 0;
+    int prev = 0;
+    cudaGetDevice(&prev);
+    bool okk = cudaSetDevice(ctx->device) == cudaSuccess &&
+               cudaMalloc(reinterpret_cast<void **>(&t->d_rank), sizeof(int32_t) * n_adapters) == cudaSuccess &&
+               cudaMalloc(reinterpret_cast<void **>(&t->d_scale), sizeof(float) * n_adapters) == cudaSuccess &&
+               cudaMalloc(reinterpret_cast<void **>(&t->d_a_pages), sizeof(int32_t) * np) == cudaSuccess &&
+               cudaMalloc(reinterpret_cast<void **>(&t->d_b_pages), sizeof(int32_t) * np) == cudaSuccess &&
+               cudaMemcpy(t->d_rank, rank_host, sizeof(int32_t) * n_adapters, cudaMemcpyHostToDevice) == cudaSuccess &&
+               cudaMemcpy(t->d_scale, scale_host, sizeof(float) * n_adapters, cudaMemcpyHostToDevice) == cudaSuccess &&
+               cudaMemcpy(t->d_a_pages, ap.data(), sizeof(int32_t) * np, cudaMemcpyHostToDevice) == cudaSuccess &&
+               cudaMemcpy(t->d_b_pages, bp.data(), sizeof(int32_t) * np, cudaMemcpyHostToDevice) == cudaSuccess;
+    cudaSetDevice(prev);
+    if (!okk) {
+        lora_table_destroy(t);
+        return LORA_E_CUDA;
+    }
+    *out = t;
+    return LORA_OK;
+}
+
+int lora_table_destroy(lora_table *t)
+{
+    if (!t)
+        return LORA_E_INVAL;
+    if (!t->ctx || t->ctx->device < 0) {
+        delete t;
+        return LORA_OK;
+    }
+    int prev = 0;
+    cudaGetDevice(&prev);
+    cudaSetDevice(t->ctx->device);
+    // Launches that read the table may still be queued: wait for the device first.
+    cudaDeviceSynchronize();
+    cudaFree(t->d_rank);
+    cudaFree(t->d_scale);
+    cudaFree(t->d_a_pages);
+    cudaFree(t->d_b_pages);
+    cudaSetDevice(prev);
+    delete t;
+    return LORA_OK;
+}
+
+int lora_plan_build(lora_ctx *ctx, const lora_table *t, const int32_t *ids, int64_t n,
+                    lora_plan_view *out)
+{
+    if (!out)
+        return LORA_E_INVAL;
+    int rc = prepare(ctx, t, ids, n);
+    if (rc != LORA_OK)
+        return rc;
+    Plan &pl = ctx->plan;
+    const RowsCfg cfg = default_rows_cfg(int64_t(pl.active.size()),
+                                         int64_t(pl.seg_adapter.size()), t->a_pw, t->b_pw);
+    plan_items(pl, t->rank.data(), cfg.rows, 0);
+    out->n_active = int64_t(pl.active.size());
+    out->active_rows = pl.active.data();
+    out->perm = pl.perm.data();
+    out->n_segments = int64_t(pl.seg_adapter.size());
+    out->seg_offsets = pl.seg_offsets.data();
+    out->seg_adapter = pl.seg_adapter.data();
+    out->row_items = int64_t(pl.row_items.size());
+    out->tile_items = int64_t(pl.tile_items.size());
+    out->rows_per_item = cfg.rows;
+    return LORA_OK;
+}
+
+int lora_shrink(lora_ctx *ctx, const lora_table *t, const int32_t *ids, int64_t n,
+                const void *x, int64_t ldx, int d_in, float *v, int64_t ldv, void *stream)
+{
+    return delta_call(ctx, t, kShrink, ids, n, x, ldx, d_in, v, ldv, nullptr, 0, 8,
+                      static_cast<cudaStream_t>(stream));
+}
+
+int lora_expand(lora_ctx *ctx, const lora_table *t, const int32_t *ids, int64_t n,
+                const float *v, int64_t ldv, void *y, int64_t ldy, int d_out, void *stream)
+{
+    return delta_call(ctx, t, kExpand, ids, n, nullptr, 0, 8, const_cast<float *>(v), ldv, y,
+                      ldy, d_out, static_cast<cudaStream_t>(stream));
+}
+
+int lora_fused(lora_ctx *ctx, const lora_table *t, const int32_t *ids, int64_t n,
+               const void *x, int64_t ldx, int d_in, void *y, int64_t ldy, int d_out,
+               void *stream)
+{
+    return delta_call(ctx, t, kFused, ids, n, x, ldx, d_in, nullptr, 0, y, ldy, d_out,
+                      static_cast<cudaStream_t>(stream));
+}
+
+int lora_merge(lora_ctx *ctx, const lora_table *t, int adapter, void *W, int64_t ldw, int d_in,
+               int d_out, void *stream)
+{
+    return merge_call(ctx, t, adapter, W, ldw, d_in, d_out, +1.f,
+                      static_cast<cudaStream_t>(stream));
+}
+
+int lora_unmerge(lora_ctx *ctx, const lora_table *t, int adapter, void *W, int64_t ldw,
+                 int d_in, int d_out, void *stream)
+{
+    return merge_call(ctx, t, adapter, W, ldw, d_in, d_out, -1.f,
+                      static_cast<cudaStream_t>(stream));
+}
+
+int lora_tiles_load(lora_ctx *ctx, const char *path)
+{
+    if (!ctx || !path)
+        return LORA_E_INVAL;
+    return ctx->tiles.load(path);
+}
+
+int lora_tiles_save(const lora_ctx *ctx, const char *path)
+{
+    if (!ctx || !path)
+        return LORA_E_INVAL;
+    return ctx->tiles.save(path);
+}
+
+int64_t lora_tiles_count(const lora_ctx *ctx) { return ctx ? int64_t(ctx->tiles.map.size()) : -1; }
+
+int lora_sync_status(lora_ctx *ctx, void *stream)
+{
+    if (!ctx)
+        return LORA_E_INVAL;
+    int rc = use_device(ctx);
+    if (rc != LORA_OK)
+        return rc;
+    CUDA_TRY(ctx, cudaStreamSynchronize(static_cast<cudaStream_t>(stream)));
+    unsigned word = 0;
+    CUDA_TRY(ctx, cudaMemcpy(&word, ctx->d_status, sizeof word, cudaMemcpyDeviceToHost));
+    if (word != 0) {
+        CUDA_TRY(ctx, cudaMemset(ctx->d_status, 0, sizeof word));
+        return LORA_E_TIMEOUT;
+    }
+    return LORA_OK;
+}
+
+int lora_profile_begin(lora_ctx *ctx)
+{
+    if (!ctx)
+        return LORA_E_INVAL;
+    ctx->prof = true;
+    ctx->prof_used = 0;
+    return LORA_OK;
+}
+
+int lora_profile_end(lora_ctx *ctx, double *ms, int64_t *launches)
+{
+    if (!ctx || !ms || !launches)
+        return LORA_E_INVAL;
+    ctx->prof = false;
+    for (int f = 0; f < 3; ++f) {
+        ms[f] = 0.0;
+        launches[f] = 0;
+    }
+    for (size_t i = 0; i < ctx->prof_used; ++i) {
+        lora_ctx::ProfEv &e = ctx->prof_ev[i];
+        CUDA_TRY(ctx, cudaEventSynchronize(e.b));
+        float t = 0.f;
+        CUDA_TRY(ctx, cudaEventElapsedTime(&t, e.a, e.b));
+        ms[e.family] += double(t);
+        launches[e.family] += 1;
+    }
+    ctx->prof_used = 0;
+    return LORA_OK;
+}
+
+int lora_last_path(const lora_ctx *ctx, int *n_launches)
+{
+    if (!ctx)
+        return LORA_E_INVAL;
+    if (n_launches)
+        *n_launches = ctx->last_launches;
+    return ctx->last_path;
+}
+
+int lora_tune_shape(lora_ctx *, const lora_table *, int, const int32_t *, int64_t, const void *,
+                    int64_t, int, void *, int64_t, int, int, float *, void *)
+{
+    return LORA_E_UNSUPPORTED;
+}
+
+}  // extern "C"

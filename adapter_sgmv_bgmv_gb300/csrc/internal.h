@@ -1,0 +1,91 @@
+// Host-side structures shared by the C-ABI layer and the kernel launchers.
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace lora {
+
+// One work item of the row-gather kernel: `nrows` consecutive entries of the
+// by-adapter permutation starting at `p0`, all on adapter `adapter`.
+struct RowItem {
+    int32_t adapter;
+    int32_t p0;
+    int32_t nrows;
+    int32_t pad;
+};
+
+// One tile of the tensor-core kernel: rows [row0, row0 + nrows) of x / y (a run of
+// consecutive rows that share one adapter), nrows <= 128.
+struct TileItem {
+    int32_t adapter;
+    int32_t row0;
+    int32_t nrows;
+    int32_t pad;
+};
+
+enum Mode : int { kShrink = 0, kExpand = 1, kFused = 2 };
+
+// Everything a row-gather launch needs (passed by value as the kernel parameter).
+struct RowsParams {
+    const uint16_t *x;
+    int64_t ldx;
+    uint16_t *y;
+    int64_t ldy;
+    float *v;
+    int64_t ldv;
+    const uint16_t *a_pool;
+    int64_t a_pw;
+    const uint16_t *b_pool;
+    int64_t b_pw;
+    const int32_t *a_pages;   // device copy, [n_adapters * max_rank]
+    const int32_t *b_pages;
+    const int32_t *rank;      // device copy, [n_adapters]
+    const float *scale;       // device copy, [n_adapters]
+    const RowItem *items;
+    const int32_t *perm;
+    unsigned *status;
+    int max_rank;
+    int d_in;
+    int d_out;
+    int n_items;
+    int cluster;              // CTAs per item (split of d_in and of d_out)
+    int slice_in;             // elements of d_in per CTA (multiple of 8)
+    int slice_out;            // elements of d_out per CTA (multiple of 8)
+    int rows_alloc;           // shared-memory rows per item (>= every item's nrows)
+    int rank_alloc;           // shared-memory rank slots (>= every item's rank)
+};
+
+// Small plans travel inside the kernel parameter block (no separate upload).
+constexpr int kInlineItems = 256;
+constexpr int kInlinePerm = 512;
+struct RowsParamsInline {
+    RowsParams p;
+    RowItem items[kInlineItems];
+    int32_t perm[kInlinePerm];
+};
+
+size_t rows_smem_bytes(int mode, int slice_in, int slice_out, int rows_alloc, int rank_alloc);
+cudaError_t launch_rows(int mode, const RowsParams &p, size_t smem, cudaStream_t stream);
+cudaError_t launch_rows_inline(int mode, const RowsParamsInline &a, size_t smem,
+                               cudaStream_t stream);
+int rows_max_smem();
+
+// Tensor-core kernels (defined in tc_*.cu).
+struct MergeParams {
+    uint16_t *W;
+    int64_t ldw;
+    const uint16_t *a_pool;
+    int64_t a_pw;
+    const uint16_t *b_pool;
+    int64_t b_pw;
+    const int32_t *a_pages;   // host-resolved page ids of this adapter, device copy
+    const int32_t *b_pages;
+    unsigned *status;
+    int d_in;
+    int d_out;
+    int rank;
+    float scale;              // signed
+    int n_split;              // column groups per 128-row block
+};
+
+}  // namespace lora

@@ -1,0 +1,545 @@
+#!/usr/bin/env python3
+"""Throughput of the heterogeneous multi-LoRA delta on one GB300 (or N replicas).
+
+Default workload: the Llama-7B-shaped decode batch (64 single-token requests,
+d_in = d_out = 4096, rank 16); one step = one lora_fused call on the heterogeneous
+batch (64 distinct adapters) plus one on the homogeneous batch (all rows on one
+adapter), 128 tokens.  Inputs rotate over enough copies that one pass over them is
+several times the 129 MB L2, so every step reads cold HBM.
+
+Prints one JSON line (rank 0).  `--impl reference` times the CPU oracle instead,
+on a bounded sample of the same workload.  `--all` prints one line per workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = ("multi-LoRA delta tokens/s and µs/call; % of HBM (decode) / TC (prefill) "
+          "roofline")
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+DEFAULT_CONFIG = "llama7b_decode"
+CONFIGS = ("llama7b_decode", "tiny_decode", "slora_prefill", "valora_prefill", "valora_merge",
+           "lorazor_decode")
+
+
+# --------------------------------------------------------------------------- peaks
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            d = json.load(fh)
+        hbm = float(d.get("hbm_gbs") or d.get("hbm_GBps"))
+        tc = float(d.get("bf16_tflops"))
+        tcs = float(d.get("bf16_tflops_sustained", tc))
+        return {"hbm_gbs": hbm, "bf16_tflops": tc, "bf16_tflops_sustained": tcs,
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": FALLBACK_BF16_TFLOPS,
+                "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# --------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples of this GPU's clocks and throttle reasons every 200 ms."""
+
+    FIELDS = ("index,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str | None):
+        self.uuid = uuid
+        self.rows = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 10:
+                self.rows.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0: float, t1: float):
+        rows = [p for (t, p) in self.rows if (self.uuid is None or p[1] == self.uuid)]
+        window = [p for (t, p) in self.rows if t0 <= t <= t1 and (self.uuid is None or p[1] == self.uuid)]
+        use = window or rows
+        if not use:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(p[2]) for p in use if num(p[2]) is not None]
+        mx = [num(p[3]) for p in use if num(p[3]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in use for i in range(4) if p[6 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(use), "in_timed_window": bool(window)}
+
+
+# --------------------------------------------------------------------------- workloads
+
+def alg_bytes_delta(case, ids):
+    """Algorithmic bytes of one fused call: x read, y read + write, the A and B pages
+    of every distinct active adapter, and the plan (items + permutation)."""
+    ids = np.asarray(ids)
+    act = ids[ids >= 0]
+    n_act = int(act.size)
+    d_in, d_out = case["d_in"], case["d_out"]
+    distinct = np.unique(act)
+    ab = int(sum(2 * int(case["rank"][k]) * (d_in + d_out) for k in distinct))
+    return 2 * n_act * d_in + 4 * n_act * d_out + ab + 4 * n_act + 16 * len(distinct)
+
+
+def flops_delta(case, ids):
+    ids = np.asarray(ids)
+    act = ids[ids >= 0]
+    return int(sum(2 * int(case["rank"][k]) * (case["d_in"] + case["d_out"]) for k in act))
+
+
+class Bench:
+    """Device-resident rotating copies of one workload and the per-step calls."""
+
+    def __init__(self, name: str, L, torch, ctx):
+        self.name, self.L, self.torch, self.ctx = name, L, torch, ctx
+        self.calls = []          # list of (case_key, ids) per step, for delta workloads
+        if name == "llama7b_decode":
+            het = workloads.make("llama7b_decode_het", seed=0)
+            hom = workloads.make("llama7b_decode_hom", seed=0)
+            self.cases = {"het": het, "hom": hom}
+            self.steps_ids = [[("het", het["ids"]), ("hom", hom["ids"])]]
+            self.workload = ("Llama-7B projection 4096x4096, 64 requests x 1 token, rank 16, "
+                             "bf16; per step one call with 64 distinct adapters (heterogeneous) "
+                             "+ one call with all rows on one adapter (homogeneous)")
+        elif name == "lorazor_decode":
+            c = workloads.make("lorazor_decode", seed=0)
+            self.cases = {"main": c}
+            self.steps_ids = [[("main", workloads.lorazor_ids(c, t))] for t in range(100)]
+            self.workload = ("70B projection 8192x8192, 256 requests x 1 token, 512 resident "
+                             "rank-16 adapters (Zipf 1.0) in shuffled 8192-wide pages; step t "
+                             "releases 128+t rows (t = 0..99, cycled)")
+        elif name in ("tiny_decode", "slora_prefill", "valora_prefill"):
+            c = workloads.make(name, seed=0)
+            self.cases = {"main": c}
+            self.steps_ids = [[("main", c["ids"])]]
+            self.workload = {
+                "tiny_decode": "d=256, 16 requests x 1 token, 4 rank-8 adapters",
+                "slora_prefill": ("S-LoRA prefill 4096x4096, 8 requests with log-normal "
+                                  "lengths (%d tokens), ranks in {8,16,32,64}, 8 of 1000 "
+                                  "adapters resident in shuffled 4096-wide pages" % c["n"]),
+                "valora_prefill": ("Qwen-VL-7B MLP up-proj 4096->11008, 16 requests x "
+                                   "(1024 visual + 32 text) tokens, 4 rank-64 adapters, Zipf 1.2"),
+            }[name]
+        elif name == "valora_merge":
+            c = workloads.make("valora_merge", seed=0)
+            self.cases = {"main": c}
+            self.steps_ids = None
+            self.workload = "merge then unmerge of a rank-64 adapter into W 4096x11008 bf16"
+        else:
+            raise KeyError(name)
+        self.is_merge = name == "valora_merge"
+        self._upload()
+
+    # ---- device data, rotated so that one pass over the sets exceeds L2
+    def _unique_bytes_per_step(self):
+        if self.is_merge:
+            c = self.cases["main"]
+            return 2 * c["d_in"] * c["d_out"]
+        tot = 0
+        for key, ids in self.steps_ids[0]:
+            tot += alg_bytes_delta(self.cases[key], ids)
+        return tot
+
+    def _upload(self):
+        torch, L = self.torch, self.L
+        from tests.gpu_util import to_dev
+        per = max(1, self._unique_bytes_per_step())
+        self.n_sets = int(min(32, max(1, math.ceil(3 * L2_BYTES / per))))
+        self.sets = []
+        base = {}
+        for key, c in self.cases.items():
+            d = {"a_pool": to_dev(c["a_pool"])}
+            d["b_pool"] = d["a_pool"] if c["b_pool"] is c["a_pool"] else to_dev(c["b_pool"])
+            if self.is_merge:
+                d["W"] = to_dev(c["W"])
+            else:
+                d["x"] = to_dev(c["x"])
+                d["y"] = to_dev(c["y"])
+            base[key] = d
+        for s in range(self.n_sets):
+            st = {}
+            for key, c in self.cases.items():
+                b = base[key]
+                if s == 0:
+                    d = dict(b)
+                else:
+                    d = {"a_pool": b["a_pool"].clone()}
+                    d["b_pool"] = d["a_pool"] if b["b_pool"] is b["a_pool"] else b["b_pool"].clone()
+                    for f in ("x", "y", "W"):
+                        if f in b:
+                            d[f] = b[f].clone()
+                d["table"] = L.AdapterTable(self.ctx, d["a_pool"], d["b_pool"], c["rank"],
+                                            c["scale"], c["a_pages"], c["b_pages"])
+                st[key] = d
+            self.sets.append(st)
+        torch.cuda.synchronize()
+
+    # ---- one step
+    def step(self, i: int, stream):
+        L = self.L
+        st = self.sets[i % self.n_sets]
+        if self.is_merge:
+            d = st["main"]
+            k = self.cases["main"]["merge_adapter"]
+            L.lora_merge(self.ctx, d["table"], k, d["W"], stream)
+            L.lora_unmerge(self.ctx, d["table"], k, d["W"], stream)
+            return
+        for key, ids in self.steps_ids[i % len(self.steps_ids)]:
+            d = st[key]
+            L.lora_fused(self.ctx, d["table"], ids, d["x"], d["y"], stream)
+
+    def tokens_per_step(self, i: int) -> int:
+        if self.is_merge:
+            return 0
+        return sum(int((np.asarray(ids) >= 0).sum()) for _, ids in self.steps_ids[i % len(self.steps_ids)])
+
+    def launches_per_step(self) -> int:
+        return 2 if (self.is_merge or self.name == "llama7b_decode") else 1
+
+    def alg_bytes_step(self, i: int) -> int:
+        if self.is_merge:
+            c = self.cases["main"]
+            r = int(c["rank"][c["merge_adapter"]])
+            return 2 * (4 * c["d_in"] * c["d_out"] + 2 * r * (c["d_in"] + c["d_out"]))
+        return sum(alg_bytes_delta(self.cases[k], ids) for k, ids in self.steps_ids[i % len(self.steps_ids)])
+
+    def flops_step(self, i: int) -> int:
+        if self.is_merge:
+            c = self.cases["main"]
+            r = int(c["rank"][c["merge_adapter"]])
+            return 2 * 2 * c["d_in"] * c["d_out"] * r
+        return sum(flops_delta(self.cases[k], ids) for k, ids in self.steps_ids[i % len(self.steps_ids)])
+
+    # ---- end to end through host buffers
+    def e2e_setup(self):
+        torch = self.torch
+        self.host = {}
+        for key, c in self.cases.items():
+            if self.is_merge:
+                self.host[key] = {"W": torch.from_numpy(c["W"].view(np.int16)).pin_memory()}
+            else:
+                self.host[key] = {
+                    "x": torch.from_numpy(c["x"].view(np.int16)).pin_memory(),
+                    "y": torch.from_numpy(c["y"].view(np.int16)).pin_memory(),
+                    "y_out": torch.empty(c["y"].shape, dtype=torch.int16).pin_memory()}
+
+    def e2e_step(self, i: int, stream):
+        st = self.sets[i % self.n_sets]
+        L = self.L
+        h2d = d2h = 0
+        if self.is_merge:
+            d, h = st["main"], self.host["main"]
+            d["W"].view(self.torch.int16).copy_(h["W"], non_blocking=True)
+            k = self.cases["main"]["merge_adapter"]
+            L.lora_merge(self.ctx, d["table"], k, d["W"], stream)
+            L.lora_unmerge(self.ctx, d["table"], k, d["W"], stream)
+            h["W"].copy_(d["W"].view(self.torch.int16), non_blocking=True)
+            nb = h["W"].numel() * 2
+            return nb, nb
+        for key, ids in self.steps_ids[i % len(self.steps_ids)]:
+            d, h = st[key], self.host[key]
+            d["x"].view(self.torch.int16).copy_(h["x"], non_blocking=True)
+            d["y"].view(self.torch.int16).copy_(h["y"], non_blocking=True)
+            L.lora_fused(self.ctx, d["table"], ids, d["x"], d["y"], stream)
+            h["y_out"].copy_(d["y"].view(self.torch.int16), non_blocking=True)
+            h2d += (h["x"].numel() + h["y"].numel()) * 2 + 4 * len(ids)
+            d2h += h["y_out"].numel() * 2
+        return h2d, d2h
+
+
+# --------------------------------------------------------------------------- oracle leg
+
+def oracle_sample(name: str, budget_s: float, nthreads: int):
+    """Time the CPU oracle on a bounded sample of the workload: whole calls of the
+    step (or rows of them) until about `budget_s` seconds have been spent.
+    Returns (tokens or calls processed, seconds, sample description)."""
+    import oracle
+    if name == "valora_merge":
+        c = workloads.make("valora_merge", seed=0)
+        t = oracle.Table.from_case(c)
+        rows_per = 16
+        done = 0
+        t0 = time.perf_counter()
+        while time.perf_counter() - t0 < budget_s:
+            rows = np.arange(done, done + rows_per) % c["d_in"]
+            oracle.merge(t, c["merge_adapter"], c["W"], +1, nthreads=nthreads, rows=rows)
+            done += rows_per
+        dt = time.perf_counter() - t0
+        # one call = all d_in rows of W
+        return done / c["d_in"], dt, f"merge of {done} W rows (of {c['d_in']} per call)"
+    if name == "llama7b_decode":
+        parts = [workloads.make("llama7b_decode_het", seed=0),
+                 workloads.make("llama7b_decode_hom", seed=0)]
+    elif name == "lorazor_decode":
+        c = workloads.make("lorazor_decode", seed=0)
+        parts = [dict(c, ids=workloads.lorazor_ids(c, 0))]
+    else:
+        parts = [workloads.make(name, seed=0)]
+    tables = [oracle.Table.from_case(p) for p in parts]
+    done_tok = 0
+    t0 = time.perf_counter()
+    chunk = 64
+    q = 0
+    while time.perf_counter() - t0 < budget_s:
+        p, t = parts[q % len(parts)], tables[q % len(parts)]
+        act = np.flatnonzero(p["ids"] >= 0)
+        start = (q // len(parts)) * chunk % max(1, len(act))
+        rows = act[start:start + chunk]
+        oracle.fused_rows(t, p["ids"], p["x"], p["y"], rows, nthreads=nthreads)
+        done_tok += len(rows)
+        q += 1
+    dt = time.perf_counter() - t0
+    return done_tok, dt, f"{done_tok} active rows of the workload's calls, {chunk}-row chunks"
+
+
+# --------------------------------------------------------------------------- main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default=DEFAULT_CONFIG, choices=CONFIGS)
+    ap.add_argument("--all", action="store_true", help="one line per workload")
+    ap.add_argument("--cpu-budget", type=float, default=12.0,
+                    help="seconds of oracle time for the cpu_baseline")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--tiles", default=os.path.join(ROOT, "adapter_sgmv_bgmv_gb300", "tiles.tbl"))
+    args = ap.parse_args()
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        return run_reference(args)
+
+    import torch
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    import adapter_sgmv_bgmv_gb300 as L
+    ctx = L.Context(local, max_rows=1 << 15, max_rank=64)
+    if os.path.exists(args.tiles):
+        ctx.tiles_load(args.tiles)
+    names = list(CONFIGS) if args.all else [args.config]
+    for name in names:
+        line = run_one(name, args, L, torch, ctx, dist, world, rank, local)
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+    ctx.close()
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def default_steps(name):
+    return {"llama7b_decode": 20000, "tiny_decode": 20000, "lorazor_decode": 10000,
+            "slora_prefill": 2000, "valora_prefill": 500, "valora_merge": 1000}[name]
+
+
+def run_one(name, args, L, torch, ctx, dist, world, rank, local):
+    K = args.steps if args.steps is not None else default_steps(name)
+    W = max(3, args.warmup)
+    b = Bench(name, L, torch, ctx)
+    stream = torch.cuda.current_stream()
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(local).uuid)
+        if not uuid.startswith("GPU-"):
+            uuid = "GPU-" + uuid
+    except Exception:
+        uuid = None
+    clocks = ClockSampler(uuid)
+    clocks.start()
+    for i in range(W):
+        b.step(i, stream)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ctx.profile_begin()
+    t_wall0 = time.time()
+    ev0.record(stream)
+    for i in range(K):
+        b.step(W + i, stream)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    prof = ctx.profile_end()
+    ms = ev0.elapsed_time(ev1)
+    if dist is not None:
+        import torch.distributed as d
+        tt = torch.tensor([ms], device="cuda")
+        d.all_reduce(tt, op=d.ReduceOp.MAX)
+        ms = float(tt.item())
+        d.barrier()
+    clocks.stop()
+    clk = clocks.summary(t_wall0, t_wall1)
+
+    tokens = sum(b.tokens_per_step(W + i) for i in range(K))
+    bytes_total = sum(b.alg_bytes_step(W + i) for i in range(K))
+    flops_total = sum(b.flops_step(W + i) for i in range(K))
+    pk = peaks()
+    fam = "merge" if b.is_merge else "rows"
+    k_ms, k_n = prof[fam]
+    if k_n == 0:   # nothing of that family ran: take the other one
+        fam = max(prof, key=lambda f: prof[f][1])
+        k_ms, k_n = prof[fam]
+    launches = sum(n for (_, n) in prof.values())
+    kern_s_total = sum(m for (m, _) in prof.values()) / 1e3
+    per_launch_s = (k_ms / 1e3) / max(1, k_n)
+    bytes_per_launch = bytes_total / max(1, launches)
+    achieved_gbs = bytes_per_launch / per_launch_s / 1e9 if per_launch_s > 0 else None
+    sec = ms / 1e3
+    if b.is_merge:
+        value = 2 * K * world / sec
+        unit = "merge+unmerge calls/s"
+    else:
+        value = tokens * world / sec
+        unit = "tokens/s"
+    line = {
+        "metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": K,
+        "warmup": W, "ms_per_step": ms / K, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": b.workload, "name": name,
+                   "l2": f"inputs rotate over {b.n_sets} device copies "
+                         f"({b.n_sets * b._unique_bytes_per_step() / 1e6:.0f} MB touched per pass "
+                         f"> 129 MB L2)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "us_per_call": {"kernel": 1e3 * k_ms / max(1, k_n),
+                        "host_call": 1e6 * sec / max(1, K * b.launches_per_step())},
+        "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": pk["hbm_gbs"],
+                     "unit": "GB/s",
+                     "frac": (achieved_gbs / pk["hbm_gbs"]) if achieved_gbs else None,
+                     "traffic": None, "peak_source": pk["source"],
+                     "kernel": "k_rows_inline<fused>" if not b.is_merge else "merge",
+                     "alg_bytes_per_launch": bytes_per_launch,
+                     "tflops": flops_total / max(1e-12, kern_s_total) / 1e12},
+        "gpu_launches": launches,
+        "clocks": clk,
+    }
+    # end to end through pinned host buffers
+    b.e2e_setup()
+    Ke = min(K, 2000)
+    for i in range(3):
+        b.e2e_step(i, stream)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    h2d = d2h = 0
+    for i in range(Ke):
+        hb, db = b.e2e_step(i, stream)
+        h2d, d2h = hb, db
+    e1.record(stream)
+    torch.cuda.synchronize()
+    es = e0.elapsed_time(e1) / 1e3
+    if b.is_merge:
+        e2e_val = 2 * Ke * world / es
+    else:
+        e2e_val = sum(b.tokens_per_step(i) for i in range(Ke)) * world / es
+    line["e2e"] = {"value": e2e_val, "unit": unit, "h2d_bytes_per_step": h2d,
+                   "d2h_bytes_per_step": d2h}
+    if rank == 0 and world == 1 and not args.no_cpu:
+        nthreads = os.cpu_count() or 1
+        done, dt, desc = oracle_sample(name, args.cpu_budget, nthreads)
+        line["cpu_baseline"] = {"value": done / dt * (2 if b.is_merge else 1),
+                                "unit": unit, "cores": nthreads, "kind": "oracle",
+                                "sample": desc + f", {dt:.1f} s"}
+    return line
+
+
+def run_reference(args):
+    """The oracle as the reference arm: each step is a bounded sample of the
+    workload, so that the whole run ends within a few minutes."""
+    name = args.config
+    K = args.steps if args.steps is not None else 20
+    W = max(3, args.warmup) if args.warmup is not None else 3
+    nthreads = os.cpu_count() or 1
+    per_step = max(0.05, min(2.0, 150.0 / max(1, K + W)))
+    for _ in range(W):
+        oracle_sample(name, per_step / 4, nthreads)
+    done = 0.0
+    tot = 0.0
+    for _ in range(K):
+        d, dt, desc = oracle_sample(name, per_step, nthreads)
+        done += d
+        tot += dt
+    is_merge = name == "valora_merge"
+    unit = "merge+unmerge calls/s" if is_merge else "tokens/s"
+    value = done / tot * (2 if is_merge else 1)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": unit, "n_gpus": 1,
+            "steps": K, "warmup": W, "ms_per_step": 1e3 * tot / K, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": name, "name": name, "parallelism": "host cores"},
+            "cpu_baseline": {"value": value, "unit": unit, "cores": nthreads, "kind": "oracle",
+                             "sample": f"each step: about {per_step:.2f} s of the oracle on "
+                                       f"the workload's rows ({desc.split(',')[0]} in the last)"},
+            "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

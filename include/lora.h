@@ -1,0 +1,190 @@
+/*
+ * lora.h -- C ABI of the GB300 (sm_103a) heterogeneous multi-LoRA delta library.
+ *
+ * The operation (Punica in "BEE-30060 Multi-LoRA serving", Background; S-LoRA page,
+ * Batching, formula 2): for a batch of n rows (tokens) where row i uses adapter
+ * k = ids[i],
+ *
+ *     y_i  <-  y_i + s_k * (x_i . A_k) . B_k        (rows with ids[i] == -1 untouched)
+ *
+ * with x_i a row vector of d_in, A_k a d_in x r_k matrix, B_k an r_k x d_out matrix
+ * and s_k the adapter's scale.  Rows are grouped into segments by adapter id
+ * (Punica: requests grouped by adapter identity) and released rows (id -1) take no
+ * part in the launch (LoRazor page: active-row-aware kernels).  The merge mode
+ * switch applies W <- W +/- s_k A_k B_k in place (VaLoRA blog, section 4.4.1).
+ *
+ * Adapter storage (S-LoRA page, Unified Paging: a rank-R weight takes R pages of one
+ * hidden-size vector): column j of A_k is the contiguous vector
+ *     a_pool + a_pages[k * max_rank + j] * a_page_width      (d_in elements used)
+ * and row j of B_k is
+ *     b_pool + b_pages[k * max_rank + j] * b_page_width      (d_out elements used).
+ * a_pool and b_pool may be the same unified pool.  Unpaged (contiguous) storage is
+ * the special case a_pages[k][j] = offset_k + j.
+ *
+ * Conventions for every call:
+ *  - Return value: LORA_OK (0) or a negative LORA_E_* code.  Arguments are checked
+ *    on the host before anything is launched; on error nothing is launched and no
+ *    caller memory is written.
+ *  - Element type: bf16 (bit pattern in 16 bits) for x, y, W and the pools; fp32
+ *    for v and scales; int32 for ids and page ids.  Matrices are row-major with a
+ *    row stride given in elements (ld*).
+ *  - Pointers named *_host are host memory; every other data pointer is device
+ *    memory of the context's device, owned by the caller (the library never frees
+ *    it).  Device pointers and row strides must be 16-byte aligned (ld* and widths
+ *    multiples of 8 elements).
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls are
+ *    asynchronous on that stream; ids are read on the host during the call and
+ *    need not outlive it.  A context is not thread-safe.
+ *  - Ranks must be multiples of 8 in [8, LORA_MAX_RANK].
+ */
+#ifndef LORA_H
+#define LORA_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define LORA_MAX_RANK 128
+
+enum {
+    LORA_OK = 0,
+    LORA_E_INVAL = -1,        /* null / misaligned pointer, bad size or stride      */
+    LORA_E_RANK = -2,         /* rank not a multiple of 8, or outside [8, max_rank] */
+    LORA_E_ADAPTER = -3,      /* adapter id >= n_adapters, or < -1                  */
+    LORA_E_NOT_RESIDENT = -4, /* a referenced adapter has a page id of -1           */
+    LORA_E_PAGE = -5,         /* a page id >= the pool's page count                 */
+    LORA_E_CUDA = -6,         /* CUDA runtime error; see lora_last_cuda_error()     */
+    LORA_E_TIMEOUT = -7,      /* a bounded device-side wait expired                 */
+    LORA_E_NOMEM = -8,        /* host or device allocation inside the library failed*/
+    LORA_E_CAPACITY = -9,     /* n exceeds the context's max_rows                   */
+    LORA_E_UNSUPPORTED = -10, /* shape beyond what the kernels handle, or not sm_103 */
+    LORA_E_IO = -11           /* tile-table file could not be read or written       */
+};
+
+typedef struct lora_ctx lora_ctx;
+typedef struct lora_table lora_table;
+
+/* Host view of the last plan built by lora_plan_build (arrays owned by the context,
+ * valid until the next call on it).  Bookkeeping of the grouping step:
+ *   active_rows  ascending row indices i with ids[i] >= 0            [n_active]
+ *   perm         active rows stably sorted by adapter id (ascending) [n_active]
+ *   seg_offsets  segment s is perm[seg_offsets[s] .. seg_offsets[s+1])  [n_segments+1]
+ *   seg_adapter  adapter id of segment s                              [n_segments]
+ *   row_items    work items of the row-gather (decode) kernel, each at most
+ *                rows_per_item consecutive entries of one segment of perm
+ *   tile_items   128-row tiles of the tensor-core (prefill) kernel             */
+typedef struct {
+    int64_t n_active;
+    const int32_t *active_rows;
+    const int32_t *perm;
+    int64_t n_segments;
+    const int32_t *seg_offsets;
+    const int32_t *seg_adapter;
+    int64_t row_items;
+    int64_t tile_items;
+    int64_t rows_per_item;
+} lora_plan_view;
+
+/* Create a context on `device` for batches of at most max_rows rows and adapters
+ * of rank <= max_rank.  Allocates small pinned staging buffers, device plan
+ * buffers and a device status word (owned by the context).  device = -1 makes a
+ * host-only context: plans, tables and tile files work, every launching call
+ * returns LORA_E_UNSUPPORTED.  Fails with LORA_E_UNSUPPORTED on a device other
+ * than compute capability 10.3. */
+int lora_ctx_create(int device, int64_t max_rows, int max_rank, lora_ctx **out);
+int lora_ctx_destroy(lora_ctx *ctx);
+
+/* Register an adapter table.  The pools stay caller-owned device memory and must
+ * outlive the table; rank_host, scale_host, a_pages_host and b_pages_host
+ * ([n_adapters], [n_adapters], [n_adapters * max_rank] x2, page id -1 = not
+ * resident) are copied.  Entries j >= rank[k] of the page arrays are ignored.
+ * Per-adapter problems (bad rank, non-resident or out-of-range pages) are not
+ * errors here: they are reported by the calls that reference that adapter. */
+int lora_table_create(lora_ctx *ctx, const void *a_pool, int64_t a_n_pages,
+                      int a_page_width, const void *b_pool, int64_t b_n_pages,
+                      int b_page_width, int n_adapters, int max_rank,
+                      const int32_t *rank_host, const float *scale_host,
+                      const int32_t *a_pages_host, const int32_t *b_pages_host,
+                      lora_table **out);
+int lora_table_destroy(lora_table *table);
+
+/* Host-only: build the plan for ids_host[n] and expose it (for inspection). */
+int lora_plan_build(lora_ctx *ctx, const lora_table *table, const int32_t *ids_host,
+                    int64_t n, lora_plan_view *out);
+
+/* Shrink: v[i, j] = sum_{c < d_in} x[i, c] * A_k[c, j] for j < r_k (fp32 out).
+ * x [n, ldx] bf16, v [n, ldv] fp32 (ldv >= max rank referenced).  Columns j >= r_k
+ * and rows with id -1 are not written. */
+int lora_shrink(lora_ctx *ctx, const lora_table *table, const int32_t *ids_host,
+                int64_t n, const void *x, int64_t ldx, int d_in, float *v,
+                int64_t ldv, void *stream);
+
+/* Expand: y[i, o] = bf16(y[i, o] + s_k * sum_{j < r_k} v[i, j] * B_k[j, o]).
+ * v [n, ldv] fp32, y [n, ldy] bf16 updated in place; rows with id -1 untouched. */
+int lora_expand(lora_ctx *ctx, const lora_table *table, const int32_t *ids_host,
+                int64_t n, const float *v, int64_t ldv, void *y, int64_t ldy,
+                int d_out, void *stream);
+
+/* Fused: y_i <- y_i + s_k (x_i A_k) B_k, one bf16 rounding per output element.
+ * x_i . A_k never leaves the chip in the row-gather kernel; the tensor-core tile
+ * kernel keeps it in fp32 tensor memory and rounds it once to bf16 as an MMA
+ * operand.  Rows with id -1 untouched. */
+int lora_fused(lora_ctx *ctx, const lora_table *table, const int32_t *ids_host,
+               int64_t n, const void *x, int64_t ldx, int d_in, void *y, int64_t ldy,
+               int d_out, void *stream);
+
+/* Merge / unmerge (mode switch): W[c, o] = bf16(W[c, o] +/- s_k sum_j A_k[c, j]
+ * B_k[j, o]) in place, W [d_in, ldw] bf16 row-major.  Unmerge after merge restores
+ * W to within two bf16 rounding steps (not bit-exactly). */
+int lora_merge(lora_ctx *ctx, const lora_table *table, int adapter, void *W,
+               int64_t ldw, int d_in, int d_out, void *stream);
+int lora_unmerge(lora_ctx *ctx, const lora_table *table, int adapter, void *W,
+                 int64_t ldw, int d_in, int d_out, void *stream);
+
+/* Shape -> tile-configuration table (VaLoRA blog, section 4.3.2: an offline
+ * search stores the best tiling per input shape in a hash table that the runtime
+ * looks up).  Lines of the text file are
+ *     kind m_bucket d_in d_out rank  cfg0 cfg1 cfg2 cfg3
+ * kind: 0 row-gather fused, 1 shrink, 2 expand, 3 tile fused, 4 merge.
+ * Unknown shapes use a built-in default; a lookup never fails. */
+int lora_tiles_load(lora_ctx *ctx, const char *path);
+int lora_tiles_save(const lora_ctx *ctx, const char *path);
+int64_t lora_tiles_count(const lora_ctx *ctx);
+
+/* Offline search for one shape: times every pruned candidate configuration of
+ * `kind` on caller-provided buffers (same meaning as for the matching call; for
+ * kind 4, `x` is W and `ids_host` names the adapter in its first entry), keeps the
+ * fastest in the context's table and returns its time in *best_us.  Writes y / W
+ * (results are the call's result applied several times). */
+int lora_tune_shape(lora_ctx *ctx, const lora_table *table, int kind,
+                    const int32_t *ids_host, int64_t n, const void *x, int64_t ldx,
+                    int d_in, void *y, int64_t ldy, int d_out, int iters,
+                    float *best_us, void *stream);
+
+/* Synchronize `stream`, then read and clear the device status word: LORA_OK or
+ * LORA_E_TIMEOUT if a kernel's bounded wait expired since the last check. */
+int lora_sync_status(lora_ctx *ctx, void *stream);
+
+/* Per-launch timing: between lora_profile_begin and lora_profile_end every kernel
+ * launch of the context is bracketed by CUDA events on its stream.  _end
+ * synchronizes on those events and returns, per kernel family (0 row-gather,
+ * 1 tensor-core tile, 2 merge), the summed device time in ms[] and the launch count
+ * in launches[] (arrays of 3). */
+int lora_profile_begin(lora_ctx *ctx);
+int lora_profile_end(lora_ctx *ctx, double *ms, int64_t *launches);
+
+/* Which kernel the last delta call launched: 0 none, 1 row-gather, 2 tensor-core
+ * tile, 3 both; and how many kernels it launched. */
+int lora_last_path(const lora_ctx *ctx, int *n_launches);
+
+const char *lora_strerror(int code);
+const char *lora_last_cuda_error(const lora_ctx *ctx);
+int lora_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LORA_H */

@@ -1,0 +1,130 @@
+"""The C ABI without a GPU: the library loads, exports every function include/lora.h
+declares, and its host-only parts (status strings, plan, tile-table files) work."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "lora.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(lora_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_calls():
+    names = declared_functions()
+    for required in ("lora_shrink", "lora_expand", "lora_fused", "lora_merge", "lora_unmerge",
+                     "lora_table_create", "lora_plan_build", "lora_tiles_load"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol():
+    import adapter_sgmv_bgmv_gb300 as L
+    lib = ctypes.CDLL(L.library_path())
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+    assert lib.lora_version() >= 1
+
+
+def test_status_strings_and_no_gpu_context():
+    import adapter_sgmv_bgmv_gb300 as L
+    assert L._L.lora_strerror(0) == b"ok"
+    for code in range(-11, 0):
+        assert L._L.lora_strerror(code) != b"unknown status"
+    if not torch.cuda.is_available():
+        with pytest.raises(L.LoraError):
+            L.Context(0)
+
+
+def _host_table(n_adapters=6, ranks=(8, 16, 8, 24, 8, 8), pw=64):
+    import adapter_sgmv_bgmv_gb300 as L
+    ctx = L.Context(-1, max_rows=4096, max_rank=64)
+    mr = 32
+    ap = np.full((n_adapters, mr), -1, np.int32)
+    bp = np.full((n_adapters, mr), -1, np.int32)
+    nxt = 0
+    for k, r in enumerate(ranks):
+        ap[k, :r] = np.arange(nxt, nxt + r)
+        bp[k, :r] = np.arange(nxt + r, nxt + 2 * r)
+        nxt += 2 * r
+    pool = torch.zeros((nxt, pw), dtype=torch.bfloat16)
+    t = L.AdapterTable(ctx, pool, pool, np.array(ranks, np.int32),
+                       np.full(n_adapters, 2.0, np.float32), ap, bp)
+    return ctx, t
+
+
+def _numpy_plan(ids, n_adapters):
+    active = np.flatnonzero(ids >= 0).astype(np.int32)
+    perm = active[np.argsort(ids[active], kind="stable")].astype(np.int32)
+    counts = np.bincount(ids[active], minlength=n_adapters)
+    seg_adapter = np.flatnonzero(counts).astype(np.int32)
+    seg_offsets = np.concatenate([[0], np.cumsum(counts[seg_adapter])]).astype(np.int32)
+    return active, perm, seg_offsets, seg_adapter
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_library_plan_is_bit_exact_against_numpy(seed):
+    import adapter_sgmv_bgmv_gb300 as L
+    ctx, t = _host_table()
+    rng = np.random.default_rng(100 + seed)
+    n = int(rng.integers(0, 2000))
+    ids = rng.integers(-1, 6, n).astype(np.int32)
+    if seed == 3:
+        ids[:] = -1
+    if seed == 5:
+        ids[:] = 2
+    p = L.lora_plan_build(ctx, t, ids)
+    a, pm, so, sa = _numpy_plan(ids, 6)
+    np.testing.assert_array_equal(p["active_rows"], a)
+    np.testing.assert_array_equal(p["perm"], pm)
+    np.testing.assert_array_equal(p["seg_offsets"], so)
+    np.testing.assert_array_equal(p["seg_adapter"], sa)
+    R = p["rows_per_item"]
+    assert 1 <= R <= 64
+    lens = np.diff(so)
+    assert p["row_items"] + p["tile_items"] >= 1 or len(a) == 0
+    assert p["row_items"] == int(np.sum((lens + R - 1) // R))
+    # page accounting of the table: adapter k holds 2 r_k pages, r_k (d_in + d_out) values
+    ranks = np.array([8, 16, 8, 24, 8, 8])
+    assert (t.a_pages >= 0).sum(axis=1).tolist() == ranks.tolist()
+    assert ((t.a_pages >= 0).sum(axis=1) + (t.b_pages >= 0).sum(axis=1)).tolist() == (2 * ranks).tolist()
+
+
+def test_library_plan_errors_on_host():
+    import adapter_sgmv_bgmv_gb300 as L
+    ctx, t = _host_table()
+    with pytest.raises(L.LoraError) as e:
+        L.lora_plan_build(ctx, t, np.array([0, 6], np.int32))
+    assert e.value.name == "LORA_E_ADAPTER"
+    with pytest.raises(L.LoraError) as e:
+        L.lora_plan_build(ctx, t, np.zeros(5000, np.int32))
+    assert e.value.name == "LORA_E_CAPACITY"
+    x = torch.zeros((4, 64), dtype=torch.bfloat16)
+    with pytest.raises((L.LoraError, TypeError)):
+        L.lora_fused(ctx, t, np.zeros(4, np.int32), x, x)   # host-only: no launches
+
+
+def test_tile_table_file_round_trip(tmp_path):
+    import adapter_sgmv_bgmv_gb300 as L
+    ctx, _ = _host_table()
+    f = tmp_path / "tiles.tbl"
+    f.write_text("# comment\n0 64 4096 4096 16 8 1 0 0\n4 4096 4096 11008 64 2 0 0 0\n\n")
+    ctx.tiles_load(str(f))
+    assert ctx.tiles_count() == 2
+    out = tmp_path / "out.tbl"
+    ctx.tiles_save(str(out))
+    rows = sorted(l for l in out.read_text().splitlines() if not l.startswith("#"))
+    assert rows == ["0 64 4096 4096 16 8 1 0 0", "4 4096 4096 11008 64 2 0 0 0"]
+    bad = tmp_path / "bad.tbl"
+    bad.write_text("0 64 4096\n")
+    with pytest.raises(L.LoraError):
+        ctx.tiles_load(str(bad))
+    with pytest.raises(L.LoraError):
+        ctx.tiles_load(str(tmp_path / "missing.tbl"))
