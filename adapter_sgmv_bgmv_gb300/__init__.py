@@ -10,6 +10,7 @@ without the built library raises: there is no other implementation.
 from __future__ import annotations
 
 import ctypes
+import weakref
 
 import numpy as np
 import torch
@@ -92,11 +93,16 @@ class Context:
             self.device = torch.device("cuda", device) if isinstance(device, int) else torch.device(device)
             idx = self.device.index or 0
         h = ctypes.c_void_p()
+        self.handle = None
+        self._tables = weakref.WeakSet()
         _check(_L.lora_ctx_create(idx, int(max_rows), int(max_rank), ctypes.byref(h)))
         self.handle = h.value
 
     def close(self):
+        """Destroy the context and every table registered with it."""
         if self.handle:
+            for t in list(self._tables):
+                t.close()
             _L.lora_ctx_destroy(self.handle)
             self.handle = None
 
@@ -176,6 +182,7 @@ class AdapterTable:
             self.rank.ctypes.data, self.scale.ctypes.data, self.a_pages.ctypes.data,
             self.b_pages.ctypes.data, ctypes.byref(h)), ctx)
         self.handle = h.value
+        ctx._tables.add(self)
 
     def close(self):
         if getattr(self, "handle", None):

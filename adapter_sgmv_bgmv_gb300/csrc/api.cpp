@@ -66,7 +66,8 @@ struct lora_ctx {
 };
 
 struct lora_table {
-    lora_ctx *ctx = nullptr;
+    lora_ctx *ctx = nullptr;           // the context it was registered with (not owned)
+    int device = -1;                   // device of the device copies (-1: host-only)
     const uint16_t *a_pool = nullptr;
     const uint16_t *b_pool = nullptr;
     int64_t a_n_pages = 0, b_n_pages = 0;
@@ -100,6 +101,7 @@ int use_device(lora_ctx *ctx)
 {
     if (ctx->device < 0)
         return LORA_E_UNSUPPORTED;   // host-only context
+    (void)cudaGetLastError();        // drop a stale error left by an unrelated call
     int cur = -1;
     CUDA_TRY(ctx, cudaGetDevice(&cur));
     if (cur != ctx->device)
@@ -542,6 +544,7 @@ int lora_table_create(lora_ctx *ctx, const void *a_pool, int64_t a_n_pages, int 
     if (!t)
         return LORA_E_NOMEM;
     t->ctx = ctx;
+    t->device = ctx->device;
     t->a_pool = static_cast<const uint16_t *>(a_pool);
     t->b_pool = static_cast<const uint16_t *>(b_pool);
     t->a_n_pages = a_n_pages;
@@ -593,13 +596,14 @@ int lora_table_destroy(lora_table *t)
 {
     if (!t)
         return LORA_E_INVAL;
-    if (!t->ctx || t->ctx->device < 0) {
+    // Only the table's own fields are used here: the context may already be gone.
+    if (t->device < 0) {
         delete t;
         return LORA_OK;
     }
     int prev = 0;
     cudaGetDevice(&prev);
-    cudaSetDevice(t->ctx->device);
+    cudaSetDevice(t->device);
     // Launches that read the table may still be queued: wait for the device first.
     cudaDeviceSynchronize();
     cudaFree(t->d_rank);

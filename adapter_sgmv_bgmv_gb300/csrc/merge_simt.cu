@@ -100,9 +100,12 @@ cudaError_t launch_merge_simt(const MergeParams &p, cudaStream_t stream)
             return e;
         configured = true;
     }
-    dim3 grid((p.d_out + kColsTile - 1) / kColsTile, (p.d_in + kRowsTile - 1) / kRowsTile);
-    k_merge_simt<<<grid, kThreads, smem, stream>>>(p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((p.d_out + kColsTile - 1) / kColsTile, (p.d_in + kRowsTile - 1) / kRowsTile);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    return cudaLaunchKernelEx(&cfg, k_merge_simt, p);
 }
 
 }  // namespace lora
