@@ -68,18 +68,23 @@ def _dev_ptr(t: torch.Tensor, what: str) -> int:
     return t.data_ptr()
 
 
-def _ids(ids) -> np.ndarray:
-    a = np.ascontiguousarray(np.asarray(ids), dtype=np.int32)
-    if a.ndim != 1:
+def _ids(ids):
+    """(int32 contiguous array, its address, length)."""
+    if not (isinstance(ids, np.ndarray) and ids.dtype == np.int32 and ids.flags.c_contiguous):
+        ids = np.ascontiguousarray(np.asarray(ids), dtype=np.int32)
+    if ids.ndim != 1:
         raise ValueError("ids must be one-dimensional")
-    return a
+    return ids, ids.__array_interface__["data"][0], ids.shape[0]
 
 
 def _rows(t: torch.Tensor, what: str):
-    """(pointer, row stride in elements, columns) of a 2-D row-major 16-bit tensor."""
-    if t.dim() != 2 or t.element_size() != 2 or t.stride(1) != 1:
+    """(pointer, row stride in elements, columns) of a 2-D row-major 16-bit CUDA tensor."""
+    st = t.stride()
+    if len(st) != 2 or st[1] != 1 or t.element_size() != 2 or not t.is_cuda:
+        if not isinstance(t, torch.Tensor) or not t.is_cuda:
+            raise TypeError(f"{what} must be a CUDA tensor")
         raise ValueError(f"{what} must be a 2-D row-major bf16 tensor")
-    return _dev_ptr(t, what), t.stride(0), t.shape[1]
+    return t.data_ptr(), st[0], t.shape[1]
 
 
 class Context:
@@ -198,10 +203,9 @@ class AdapterTable:
 
 def lora_plan_build(ctx: Context, table: AdapterTable, ids) -> dict:
     """Host-side grouping of one batch (copies of the context's plan arrays)."""
-    ids = _ids(ids)
+    ids, pid, n = _ids(ids)
     v = _lib.PlanView()
-    _check(_L.lora_plan_build(ctx.handle, table.handle, ids.ctypes.data, ids.shape[0],
-                              ctypes.byref(v)), ctx)
+    _check(_L.lora_plan_build(ctx.handle, table.handle, pid, n, ctypes.byref(v)), ctx)
 
     def arr(p, n):
         return np.ctypeslib.as_array(p, shape=(n,)).copy() if n > 0 else np.zeros(0, np.int32)
@@ -215,34 +219,35 @@ def lora_plan_build(ctx: Context, table: AdapterTable, ids) -> dict:
 def lora_shrink(ctx: Context, table: AdapterTable, ids, x: torch.Tensor, v: torch.Tensor,
                 stream=None):
     """v[i, :r_k] = x_i A_k (fp32) for rows with ids[i] >= 0."""
-    ids = _ids(ids)
+    ids, pid, n = _ids(ids)
     px, ldx, d_in = _rows(x, "x")
     if v.dtype != torch.float32 or v.dim() != 2 or v.stride(1) != 1:
         raise ValueError("v must be a 2-D row-major float32 tensor")
-    _check(_L.lora_shrink(ctx.handle, table.handle, ids.ctypes.data, ids.shape[0], px, ldx,
-                          d_in, _dev_ptr(v, "v"), v.stride(0), _stream(stream, ctx.device)), ctx)
+    _check(_L.lora_shrink(ctx.handle, table.handle, pid, n, px, ldx, d_in, _dev_ptr(v, "v"),
+                          v.stride(0), _stream(stream, ctx.device)), ctx)
 
 
 def lora_expand(ctx: Context, table: AdapterTable, ids, v: torch.Tensor, y: torch.Tensor,
                 stream=None):
     """y_i <- bf16(y_i + s_k v_i B_k) in place for rows with ids[i] >= 0."""
-    ids = _ids(ids)
+    ids, pid, n = _ids(ids)
     py, ldy, d_out = _rows(y, "y")
     if v.dtype != torch.float32 or v.dim() != 2 or v.stride(1) != 1:
         raise ValueError("v must be a 2-D row-major float32 tensor")
-    _check(_L.lora_expand(ctx.handle, table.handle, ids.ctypes.data, ids.shape[0],
-                          _dev_ptr(v, "v"), v.stride(0), py, ldy, d_out,
-                          _stream(stream, ctx.device)), ctx)
+    _check(_L.lora_expand(ctx.handle, table.handle, pid, n, _dev_ptr(v, "v"), v.stride(0), py,
+                          ldy, d_out, _stream(stream, ctx.device)), ctx)
 
 
 def lora_fused(ctx: Context, table: AdapterTable, ids, x: torch.Tensor, y: torch.Tensor,
                stream=None):
     """y_i <- bf16(y_i + s_k (x_i A_k) B_k) in place for rows with ids[i] >= 0."""
-    ids = _ids(ids)
+    ids, pid, n = _ids(ids)
     px, ldx, d_in = _rows(x, "x")
     py, ldy, d_out = _rows(y, "y")
-    _check(_L.lora_fused(ctx.handle, table.handle, ids.ctypes.data, ids.shape[0], px, ldx,
-                         d_in, py, ldy, d_out, _stream(stream, ctx.device)), ctx)
+    rc = _L.lora_fused(ctx.handle, table.handle, pid, n, px, ldx, d_in, py, ldy, d_out,
+                       _stream(stream, ctx.device))
+    if rc:
+        _check(rc, ctx)
 
 
 def lora_merge(ctx: Context, table: AdapterTable, adapter: int, W: torch.Tensor, stream=None):
@@ -264,7 +269,7 @@ def lora_tune_shape(ctx: Context, table: AdapterTable, kind: int, ids, x: torch.
     """Offline search for one shape (see include/lora.h); returns the best time in us
     and keeps the winning configuration in the context's table.  For KIND_MERGE, x is
     W, y is ignored and ids[0] is the adapter."""
-    ids = _ids(ids)
+    ids, pid, n = _ids(ids)
     px, ldx, d_in = _rows(x, "x")
     if kind == KIND_MERGE:
         py, ldy, d_out = px, ldx, d_in
@@ -272,7 +277,7 @@ def lora_tune_shape(ctx: Context, table: AdapterTable, kind: int, ids, x: torch.
     else:
         py, ldy, d_out = _rows(y, "y")
     best = ctypes.c_float()
-    _check(_L.lora_tune_shape(ctx.handle, table.handle, int(kind), ids.ctypes.data,
-                              ids.shape[0], px, ldx, d_in, py, ldy, d_out, int(iters),
+    _check(_L.lora_tune_shape(ctx.handle, table.handle, int(kind), pid, n, px, ldx, d_in, py,
+                              ldy, d_out, int(iters),
                               ctypes.byref(best), _stream(stream, ctx.device)), ctx)
     return float(best.value)

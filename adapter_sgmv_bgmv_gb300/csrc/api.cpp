@@ -193,39 +193,49 @@ struct RowsCfg {
     int rows;
 };
 
-RowsCfg default_rows_cfg(int64_t n_act, int64_t n_seg, int d_in, int d_out)
+size_t rows_smem_for(int mode, int cluster, int rows, int rank, int d_in, int d_out)
+{
+    const int si = std::max(8, round_up8(ceil_div(d_in, cluster)));
+    const int so = std::max(8, round_up8(ceil_div(d_out, cluster)));
+    return rows_smem_bytes(mode, si, so, rows, rank, cluster);
+}
+
+// Default launch shape when the tile table has no entry: items of at most 4 rows,
+// then the smallest cluster that puts two CTAs' worth of work on every SM, grown
+// further while one CTA would need more than half an SM's shared memory.
+RowsCfg default_rows_cfg(int mode, int64_t n_act, int64_t n_seg, int d_in, int d_out, int rank)
 {
     RowsCfg c{1, 1};
-    // rows per item: about the mean segment length, at most 16
     const int64_t mean = n_seg > 0 ? ceil_div(n_act, n_seg) : 1;
-    while (c.rows < 16 && c.rows < mean)
+    while (c.rows < 4 && c.rows < mean)
         c.rows <<= 1;
-    // cluster: enough CTAs to cover the GPU twice, slices of at least 128 elements
-    int64_t items = 0;
-    if (n_seg > 0)
-        items = std::max<int64_t>(n_seg, ceil_div(n_act, c.rows));
-    const int dmax = std::max(d_in, d_out);
-    while (c.cluster < 8 && items * c.cluster < 2 * kSms && dmax / (2 * c.cluster) >= 128)
+    const int64_t items = n_seg > 0 ? std::max<int64_t>(n_seg, ceil_div(n_act, c.rows)) : 0;
+    const int dmin = std::min(d_in, d_out);
+    const int cmax = rows_max_cluster();
+    while (c.cluster < cmax && items * c.cluster < 2 * kSms && dmin / (2 * c.cluster) >= 128)
+        c.cluster <<= 1;
+    while (c.cluster < cmax &&
+           rows_smem_for(mode, c.cluster, c.rows, rank, d_in, d_out) > size_t(110 * 1024))
         c.cluster <<= 1;
     return c;
 }
 
-int rows_launch_params(lora_ctx *ctx, int mode, RowsCfg cfg, int d_in, int d_out,
-                       int rank_alloc, RowsParams &p, size_t &smem)
+int rows_launch_params(int mode, RowsCfg cfg, int d_in, int d_out, int rank_alloc, RowsParams &p,
+                       size_t &smem)
 {
     for (;; cfg.cluster <<= 1) {
-        if (cfg.cluster > 16)
+        if (cfg.cluster > rows_max_cluster())
             return LORA_E_UNSUPPORTED;
         p.cluster = cfg.cluster;
         p.slice_in = std::max(8, round_up8(ceil_div(d_in, cfg.cluster)));
         p.slice_out = std::max(8, round_up8(ceil_div(d_out, cfg.cluster)));
         p.rows_alloc = cfg.rows;
         p.rank_alloc = rank_alloc;
-        smem = rows_smem_bytes(mode, p.slice_in, p.slice_out, p.rows_alloc, p.rank_alloc);
+        smem = rows_smem_bytes(mode, p.slice_in, p.slice_out, p.rows_alloc, p.rank_alloc,
+                               p.cluster);
         if (smem <= size_t(rows_max_smem()))
             return LORA_OK;
     }
-    (void)ctx;
 }
 
 // Validate the pieces every delta call shares and build the plan.
@@ -253,10 +263,10 @@ bool stride_ok(const void *p, int64_t ld, int d)
     return p && aligned16(p) && d > 0 && (d % 8) == 0 && ld >= d && (ld % 8) == 0;
 }
 
-RowsCfg choose_rows_cfg(const lora_ctx *ctx, int kind, int64_t n_act, int64_t n_seg, int d_in,
-                        int d_out, int rank)
+RowsCfg choose_rows_cfg(const lora_ctx *ctx, int mode, int kind, int64_t n_act, int64_t n_seg,
+                        int d_in, int d_out, int rank)
 {
-    RowsCfg cfg = default_rows_cfg(n_act, n_seg, d_in, d_out);
+    RowsCfg cfg = default_rows_cfg(mode, n_act, n_seg, d_in, d_out, rank);
     TileCfg tc;
     if (ctx->tiles.lookup(TileKey{kind, pow2_bucket(n_act), d_in, d_out, rank}, tc) &&
         tc[0] >= 1 && tc[0] <= 16 && (tc[0] & (tc[0] - 1)) == 0 && tc[1] >= 1 && tc[1] <= 64) {
@@ -278,7 +288,7 @@ int run_rows(lora_ctx *ctx, const lora_table *t, int mode, RowsCfg cfg, const vo
     cfg.rows = std::max(1, pl.row_max_rows);
     RowsParams p{};
     size_t smem = 0;
-    int rc = rows_launch_params(ctx, mode, cfg, d_in, d_out, pl.row_max_rank, p, smem);
+    int rc = rows_launch_params(mode, cfg, d_in, d_out, pl.row_max_rank, p, smem);
     if (rc != LORA_OK)
         return rc;
 
@@ -370,9 +380,9 @@ int delta_call(lora_ctx *ctx, const lora_table *t, int mode, const int32_t *ids,
     int32_t rmax = 0;
     for (int32_t k : pl.seg_adapter)
         rmax = std::max(rmax, t->rank[size_t(k)]);
-    const RowsCfg cfg = choose_rows_cfg(ctx, kind, int64_t(pl.active.size()),
+    const RowsCfg cfg = choose_rows_cfg(ctx, mode, kind, int64_t(pl.active.size()),
                                         int64_t(pl.seg_adapter.size()), d_in, d_out, rmax);
-    plan_items(pl, t->rank.data(), cfg.rows, 0);
+    plan_items(pl, t->rank.data(), t->scale.data(), cfg.rows, 0);
     return run_rows(ctx, t, mode, cfg, x, ldx, d_in, v, ldv, y, ldy, d_out, stream);
 }
 
@@ -624,9 +634,10 @@ int lora_plan_build(lora_ctx *ctx, const lora_table *t, const int32_t *ids, int6
     if (rc != LORA_OK)
         return rc;
     Plan &pl = ctx->plan;
-    const RowsCfg cfg = default_rows_cfg(int64_t(pl.active.size()),
-                                         int64_t(pl.seg_adapter.size()), t->a_pw, t->b_pw);
-    plan_items(pl, t->rank.data(), cfg.rows, 0);
+    const RowsCfg cfg = default_rows_cfg(kFused, int64_t(pl.active.size()),
+                                         int64_t(pl.seg_adapter.size()), t->a_pw, t->b_pw,
+                                         pl.max_rank > 0 ? pl.max_rank : 8);
+    plan_items(pl, t->rank.data(), t->scale.data(), cfg.rows, 0);
     out->n_active = int64_t(pl.active.size());
     out->active_rows = pl.active.data();
     out->perm = pl.perm.data();

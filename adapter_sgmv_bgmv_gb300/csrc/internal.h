@@ -6,13 +6,16 @@
 namespace lora {
 
 // One work item of the row-gather kernel: `nrows` consecutive entries of the
-// by-adapter permutation starting at `p0`, all on adapter `adapter`.
+// by-adapter permutation starting at `p0`, all on adapter `adapter` of rank `rank`
+// and scale `scale` (carried here so the kernel needs no lookup before its copies).
 struct RowItem {
     int32_t adapter;
     int32_t p0;
-    int32_t nrows;
-    int32_t pad;
+    int16_t nrows;
+    int16_t rank;
+    float scale;
 };
+static_assert(sizeof(RowItem) == 16, "RowItem is one 16-byte load");
 
 // One tile of the tensor-core kernel: rows [row0, row0 + nrows) of x / y (a run of
 // consecutive rows that share one adapter), nrows <= 128.
@@ -64,7 +67,9 @@ struct RowsParamsInline {
     int32_t perm[kInlinePerm];
 };
 
-size_t rows_smem_bytes(int mode, int slice_in, int slice_out, int rows_alloc, int rank_alloc);
+size_t rows_smem_bytes(int mode, int slice_in, int slice_out, int rows_alloc, int rank_alloc,
+                       int cluster);
+int rows_max_cluster();
 cudaError_t launch_rows(int mode, const RowsParams &p, size_t smem, cudaStream_t stream);
 cudaError_t launch_rows_inline(int mode, const RowsParamsInline &a, size_t smem,
                                cudaStream_t stream);

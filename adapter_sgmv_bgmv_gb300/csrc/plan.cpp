@@ -47,7 +47,8 @@ int plan_group(Plan &pl, const int32_t *ids, int64_t n, int n_adapters)
     return LORA_OK;
 }
 
-void plan_items(Plan &pl, const int32_t *rank, int rows_per_item, int tile_min_run)
+void plan_items(Plan &pl, const int32_t *rank, const float *scale, int rows_per_item,
+                int tile_min_run)
 {
     pl.row_items.clear();
     pl.tile_items.clear();
@@ -64,7 +65,7 @@ void plan_items(Plan &pl, const int32_t *rank, int rows_per_item, int tile_min_r
         auto flush_rows = [&](int32_t from, int32_t to) {
             for (int32_t p = from; p < to; p += rows_per_item) {
                 const int32_t m = std::min(rows_per_item, to - p);
-                pl.row_items.push_back(RowItem{k, p, m, 0});
+                pl.row_items.push_back(RowItem{k, p, int16_t(m), int16_t(r), scale[k]});
                 pl.row_max_rows = std::max(pl.row_max_rows, m);
                 pl.row_active += m;
             }

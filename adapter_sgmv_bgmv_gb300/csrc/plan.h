@@ -32,6 +32,7 @@ int plan_group(Plan &pl, const int32_t *ids, int64_t n, int n_adapters);
 // Cut segments into work items.  Runs of consecutive rows of at least
 // `tile_min_run` rows go to 128-row tiles (tile_min_run <= 0: none do); everything
 // else goes to row items of at most `rows_per_item` rows.
-void plan_items(Plan &pl, const int32_t *rank, int rows_per_item, int tile_min_run);
+void plan_items(Plan &pl, const int32_t *rank, const float *scale, int rows_per_item,
+                int tile_min_run);
 
 }  // namespace lora

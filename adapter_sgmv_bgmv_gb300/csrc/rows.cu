@@ -5,19 +5,20 @@
 // cluster of `cluster` CTAs.  CTA c of the cluster owns the c-th slice of d_in for
 // the shrink and the c-th slice of d_out for the expand:
 //
-//   1. one warp issues bulk (TMA) copies of its slice of every page of A_k and of
-//      every gathered x row (barrier 0), then of B_k and of the y rows (barrier 1),
-//      so the whole working set of the CTA is in flight at once;
+//   1. warp 0 issues bulk (TMA) copies: lane i < nrows fetches x row i and y row i,
+//      lane j < r reads page j of A_k / B_k from the page table and fetches its
+//      slice, so the CTA's whole working set is in flight after one dependent load;
 //   2. shrink: partial v[i, j] over the CTA's d_in slice, warp-per-page dot
 //      products with 128-bit shared loads and a warp-shuffle reduction;
-//   3. the partial sums are combined through distributed shared memory in a fixed
-//      rank order (every CTA of the cluster gets identical v);
+//   3. each CTA pushes its partial v into a per-source slot of every peer's shared
+//      memory (distributed shared memory stores), one cluster barrier, then every
+//      CTA sums the slots in rank order (all CTAs get identical v);
 //   4. expand: y[i, o] = bf16(y[i, o] + s_k * sum_j v[i, j] B_k[j, o]) for the CTA's
 //      d_out slice, 128-bit stores straight to the gathered rows.
 //
 // Released rows (id -1) are in no item, so they cost no CTA and are never touched
 // (LoRazor page: the launch follows the active rows).  Modes: shrink-only writes v
-// (fp32) and skips 4; expand-only reads v and skips 1-3 for x/A.
+// (fp32) and skips 4; expand-only reads v, skips 1-3 for x/A and needs no cluster.
 #include <cuda_runtime.h>
 
 #include "internal.h"
@@ -29,22 +30,60 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
+constexpr int kMaxCluster = 16;
 
 __host__ __device__ inline size_t align16(size_t v) { return (v + 15) & ~size_t(15); }
 
 __host__ __device__ inline size_t carve(int mode, int si, int so, int rows, int ranks,
-                                        size_t off[7])
+                                        int cluster, size_t off[7])
 {
     size_t o = 0;
     const bool has_in = mode != kExpand, has_out = mode != kShrink;
-    off[0] = o; o += has_in ? align16(size_t(ranks) * si * 2) : 0;    // A slice
-    off[1] = o; o += has_in ? align16(size_t(rows) * si * 2) : 0;     // x rows
-    off[2] = o; o += has_out ? align16(size_t(ranks) * so * 2) : 0;   // B slice
-    off[3] = o; o += has_out ? align16(size_t(rows) * so * 2) : 0;   // y rows
-    off[4] = o; o += align16(size_t(rows) * ranks * 4);               // partial v
-    off[5] = o; o += align16(size_t(rows) * ranks * 4);               // v
-    off[6] = o; o += 16;                                              // 2 mbarriers
+    off[0] = o; o += has_in ? align16(size_t(ranks) * si * 2) : 0;          // A slice
+    off[1] = o; o += has_in ? align16(size_t(rows) * si * 2) : 0;           // x rows
+    off[2] = o; o += has_out ? align16(size_t(ranks) * so * 2) : 0;         // B slice
+    off[3] = o; o += has_out ? align16(size_t(rows) * so * 2) : 0;          // y rows
+    off[4] = o; o += has_in ? align16(size_t(cluster) * rows * ranks * 4) : 0;  // pushed partials
+    off[5] = o; o += align16(size_t(rows) * ranks * 4);                     // v
+    off[6] = o; o += 16;                                                    // 2 mbarriers
     return o;
+}
+
+__device__ __forceinline__ void st_dsmem_f32(float *local, uint32_t rank, float v)
+{
+    uint32_t ra;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_u32(local)), "r"(rank));
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(ra), "f"(v) : "memory");
+}
+
+__device__ __forceinline__ void cluster_arrive_relaxed()
+{
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+
+// Expand of `ROWS` rows starting at i0 for 8 output columns at vector q:
+// acc[u][e] = sum_j v[i0+u, j] * B[j, 8q+e].
+template <int ROWS>
+__device__ __forceinline__ void expand_vec(const uint16_t *sB, int slice_out, const float *vsum,
+                                           int RA, int r, int i0, int q, float acc[ROWS][8])
+{
+#pragma unroll
+    for (int u = 0; u < ROWS; ++u)
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            acc[u][e] = 0.f;
+#pragma unroll 4
+    for (int j = 0; j < r; ++j) {
+        float bf[8];
+        unpack8(reinterpret_cast<const uint4 *>(sB + size_t(j) * slice_out)[q], bf);
+#pragma unroll
+        for (int u = 0; u < ROWS; ++u) {
+            const float vv = vsum[(i0 + u) * RA + j];
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                acc[u][e] = fmaf(vv, bf[e], acc[u][e]);
+        }
+    }
 }
 
 template <int MODE>
@@ -52,27 +91,29 @@ __device__ __forceinline__ void rows_body(const RowsParams &p, const RowItem *it
                                           const int32_t *perm)
 {
     extern __shared__ __align__(128) uint8_t smem[];
+    const int C = p.cluster;
     size_t off[7];
-    carve(MODE, p.slice_in, p.slice_out, p.rows_alloc, p.rank_alloc, off);
+    carve(MODE, p.slice_in, p.slice_out, p.rows_alloc, p.rank_alloc, C, off);
     uint16_t *sA = reinterpret_cast<uint16_t *>(smem + off[0]);
     uint16_t *sX = reinterpret_cast<uint16_t *>(smem + off[1]);
     uint16_t *sB = reinterpret_cast<uint16_t *>(smem + off[2]);
     uint16_t *sY = reinterpret_cast<uint16_t *>(smem + off[3]);
-    float *vpart = reinterpret_cast<float *>(smem + off[4]);
+    float *vin = reinterpret_cast<float *>(smem + off[4]);
     float *vsum = reinterpret_cast<float *>(smem + off[5]);
     const uint32_t bar0 = smem_u32(smem + off[6]);
     const uint32_t bar1 = bar0 + 8;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int C = p.cluster;
+    const bool clustered = (MODE != kExpand) && C > 1;
     const int item_id = blockIdx.x / C;
-    const uint32_t crank = (C > 1) ? cluster_ctarank() : 0u;
+    const uint32_t crank = clustered ? cluster_ctarank() : uint32_t(blockIdx.x % C);
     const RowItem it = items[item_id];
     const int k = it.adapter;
-    const int r = p.rank[k];
+    const int r = it.rank;
     const int nrows = it.nrows;
-    const float s = p.scale[k];
+    const float s = it.scale;
     const int RA = p.rank_alloc;
+    const int RW = p.rows_alloc;
 
     const int in0 = int(crank) * p.slice_in;
     const int in_len = max(0, min(p.d_in - in0, p.slice_in));
@@ -85,69 +126,69 @@ __device__ __forceinline__ void rows_body(const RowsParams &p, const RowItem *it
         fence_mbar_init();
     }
     __syncthreads();
+    if (clustered)
+        cluster_arrive_relaxed();   // "started"; waited on before the first remote store
 
-    // ---- 1. issue every copy this CTA needs
+    // ---- 1. copies (one dependent load: the page ids)
     if (warp == 0) {
+        const uint32_t in_bytes = uint32_t(in_len) * 2u, out_bytes = uint32_t(out_len) * 2u;
+        if (lane == 0) {
+            if (MODE != kExpand)
+                mbar_arrive_expect_tx(bar0, uint32_t(r + nrows) * in_bytes);
+            if (MODE != kShrink)
+                mbar_arrive_expect_tx(bar1, uint32_t(r + nrows) * out_bytes);
+        }
+        __syncwarp();
         const int32_t *ap = p.a_pages + size_t(k) * p.max_rank;
         const int32_t *bp = p.b_pages + size_t(k) * p.max_rank;
-        if (MODE != kExpand) {
-            if (lane == 0)
-                mbar_arrive_expect_tx(bar0, uint32_t(r + nrows) * uint32_t(in_len) * 2u);
-            __syncwarp();
-            if (in_len > 0) {
-                for (int q = lane; q < r + nrows; q += 32) {
-                    const uint16_t *src;
-                    uint16_t *dst;
-                    if (q < r) {
-                        src = p.a_pool + int64_t(ap[q]) * p.a_pw + in0;
-                        dst = sA + size_t(q) * p.slice_in;
-                    } else {
-                        const int row = perm[it.p0 + (q - r)];
-                        src = p.x + int64_t(row) * p.ldx + in0;
-                        dst = sX + size_t(q - r) * p.slice_in;
-                    }
-                    bulk_g2s(smem_u32(dst), src, uint32_t(in_len) * 2u, bar0);
-                }
+        for (int q = lane; q < r || q < nrows; q += 32) {
+            int32_t pa = 0, pb = 0, row = 0;
+            if (q < r) {
+                if (MODE != kExpand)
+                    pa = ap[q];
+                if (MODE != kShrink)
+                    pb = bp[q];
             }
-        }
-        if (MODE != kShrink) {
-            if (lane == 0)
-                mbar_arrive_expect_tx(bar1, uint32_t(r + nrows) * uint32_t(out_len) * 2u);
-            __syncwarp();
-            if (out_len > 0) {
-                for (int q = lane; q < r + nrows; q += 32) {
-                    const uint16_t *src;
-                    uint16_t *dst;
-                    if (q < r) {
-                        src = p.b_pool + int64_t(bp[q]) * p.b_pw + out0;
-                        dst = sB + size_t(q) * p.slice_out;
-                    } else {
-                        const int row = perm[it.p0 + (q - r)];
-                        src = p.y + int64_t(row) * p.ldy + out0;
-                        dst = sY + size_t(q - r) * p.slice_out;
-                    }
-                    bulk_g2s(smem_u32(dst), src, uint32_t(out_len) * 2u, bar1);
-                }
+            if (q < nrows)
+                row = perm[it.p0 + q];
+            if (q < nrows) {
+                if (MODE != kExpand && in_bytes)
+                    bulk_g2s(smem_u32(sX + size_t(q) * p.slice_in),
+                             p.x + int64_t(row) * p.ldx + in0, in_bytes, bar0);
+                if (MODE != kShrink && out_bytes)
+                    bulk_g2s(smem_u32(sY + size_t(q) * p.slice_out),
+                             p.y + int64_t(row) * p.ldy + out0, out_bytes, bar1);
+            }
+            if (q < r) {
+                if (MODE != kExpand && in_bytes)
+                    bulk_g2s(smem_u32(sA + size_t(q) * p.slice_in),
+                             p.a_pool + int64_t(pa) * p.a_pw + in0, in_bytes, bar0);
+                if (MODE != kShrink && out_bytes)
+                    bulk_g2s(smem_u32(sB + size_t(q) * p.slice_out),
+                             p.b_pool + int64_t(pb) * p.b_pw + out0, out_bytes, bar1);
             }
         }
     }
 
     bool ok = true;
 
-    // ---- 2./3. shrink and cluster reduction
+    // ---- 2./3. shrink and cluster exchange
     if (MODE != kExpand) {
         ok = mbar_wait_bounded(bar0, 0, p.status, kDevTimeoutLoad) && ok;
         const int nvec = in_len >> 3;
+        if (clustered)
+            cluster_wait_acquire();  // every peer has started: its shared memory exists
         for (int j = warp; j < r; j += kWarps) {
             const uint4 *a = reinterpret_cast<const uint4 *>(sA + size_t(j) * p.slice_in);
             for (int i0 = 0; i0 < nrows; i0 += 4) {
                 float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                const int nr = min(4, nrows - i0);
                 for (int q = lane; q < nvec; q += 32) {
                     float af[8];
                     unpack8(a[q], af);
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
-                        if (i0 + u < nrows) {
+                        if (u < nr) {
                             float xf[8];
                             unpack8(reinterpret_cast<const uint4 *>(
                                         sX + size_t(i0 + u) * p.slice_in)[q], xf);
@@ -159,27 +200,28 @@ __device__ __forceinline__ void rows_body(const RowsParams &p, const RowItem *it
                 }
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
-                    const float t = warp_sum(acc[u]);
-                    if (lane == 0 && i0 + u < nrows)
-                        vpart[(i0 + u) * RA + j] = t;
+                    if (u < nr) {
+                        const float t = warp_sum(acc[u]);
+                        const int slot = (i0 + u) * RA + j;
+                        if (!clustered) {
+                            if (lane == 0)
+                                vsum[slot] = t;
+                        } else if (lane < C) {
+                            // lane c delivers this partial to CTA c's slot for our rank
+                            st_dsmem_f32(vin + (size_t(crank) * RW) * RA + slot, uint32_t(lane), t);
+                        }
+                    }
                 }
             }
         }
-        if (C > 1) {
-            cluster_sync();   // partial sums of every CTA are visible cluster-wide
+        if (clustered) {
+            cluster_sync();   // all partials delivered to every CTA
             for (int q = tid; q < nrows * r; q += kThreads) {
                 const int i = q / r, j = q - (q / r) * r;
                 float acc = 0.f;
                 for (int c = 0; c < C; ++c)
-                    acc += ld_dsmem_f32(vpart + i * RA + j, uint32_t(c));
+                    acc += vin[(size_t(c) * RW + i) * RA + j];
                 vsum[i * RA + j] = acc;
-            }
-            cluster_arrive_release();   // peers may leave once everyone has read
-        } else {
-            __syncthreads();
-            for (int q = tid; q < nrows * r; q += kThreads) {
-                const int i = q / r, j = q - (q / r) * r;
-                vsum[i * RA + j] = vpart[i * RA + j];
             }
         }
         __syncthreads();
@@ -203,30 +245,36 @@ __device__ __forceinline__ void rows_body(const RowsParams &p, const RowItem *it
     if (MODE != kShrink) {
         ok = mbar_wait_bounded(bar1, 0, p.status, kDevTimeoutLoad) && ok;
         const int nvo = out_len >> 3;
-        const int ngroups = (nrows + 3) >> 2;
-        for (int w = tid; w < nvo * ngroups; w += kThreads) {
-            const int q = w % nvo;
-            const int i0 = (w / nvo) * 4;
-            float acc[4][8];
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
+        if (nrows == 1) {
+            const int row = perm[it.p0];
+            for (int q = tid; q < nvo; q += kThreads) {
+                float acc[1][8];
+                expand_vec<1>(sB, p.slice_out, vsum, RA, r, 0, q, acc);
+                float yf[8];
+                unpack8(reinterpret_cast<const uint4 *>(sY)[q], yf);
 #pragma unroll
                 for (int e = 0; e < 8; ++e)
-                    acc[u][e] = 0.f;
-            for (int j = 0; j < r; ++j) {
-                float bf[8];
-                unpack8(reinterpret_cast<const uint4 *>(sB + size_t(j) * p.slice_out)[q], bf);
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const float vv = (i0 + u < nrows) ? vsum[(i0 + u) * RA + j] : 0.f;
+                    yf[e] = fmaf(s, acc[0][e], yf[e]);
+                if (ok)
+                    *reinterpret_cast<uint4 *>(p.y + int64_t(row) * p.ldy + out0 + 8 * q) = pack8(yf);
+            }
+        } else {
+            const int ngroups = (nrows + 1) >> 1;
+            for (int w = tid; w < nvo * ngroups; w += kThreads) {
+                const int q = w % nvo;
+                const int i0 = (w / nvo) * 2;
+                float acc[2][8];
+                if (i0 + 1 < nrows) {
+                    expand_vec<2>(sB, p.slice_out, vsum, RA, r, i0, q, acc);
+                } else {
+                    float a1[1][8];
+                    expand_vec<1>(sB, p.slice_out, vsum, RA, r, i0, q, a1);
 #pragma unroll
                     for (int e = 0; e < 8; ++e)
-                        acc[u][e] = fmaf(vv, bf[e], acc[u][e]);
+                        acc[0][e] = a1[0][e];
                 }
-            }
-            if (ok) {
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
+                for (int u = 0; u < 2; ++u) {
                     if (i0 + u < nrows) {
                         float yf[8];
                         unpack8(reinterpret_cast<const uint4 *>(
@@ -235,8 +283,9 @@ __device__ __forceinline__ void rows_body(const RowsParams &p, const RowItem *it
                         for (int e = 0; e < 8; ++e)
                             yf[e] = fmaf(s, acc[u][e], yf[e]);
                         const int row = perm[it.p0 + i0 + u];
-                        *reinterpret_cast<uint4 *>(p.y + int64_t(row) * p.ldy + out0 + 8 * q) =
-                            pack8(yf);
+                        if (ok)
+                            *reinterpret_cast<uint4 *>(p.y + int64_t(row) * p.ldy + out0 + 8 * q) =
+                                pack8(yf);
                     }
                 }
             }
@@ -251,8 +300,6 @@ __device__ __forceinline__ void rows_body(const RowsParams &p, const RowItem *it
         if (MODE != kShrink)
             mbar_wait_bounded(bar1, 0, nullptr, 0);
     }
-    if (MODE != kExpand && C > 1)
-        cluster_wait_acquire();   // keep this CTA's shared memory alive for its peers
 }
 
 template <int MODE>
@@ -295,7 +342,7 @@ cudaError_t launch_mode(const RowsParams &p, const Arg &arg, size_t smem, cudaSt
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = unsigned(p.cluster);
+    attr[0].val.clusterDim.x = (MODE == kExpand) ? 1u : unsigned(p.cluster);
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
@@ -309,11 +356,13 @@ cudaError_t launch_mode(const RowsParams &p, const Arg &arg, size_t smem, cudaSt
 }  // namespace
 
 int rows_max_smem() { return 227 * 1024; }
+int rows_max_cluster() { return kMaxCluster; }
 
-size_t rows_smem_bytes(int mode, int slice_in, int slice_out, int rows_alloc, int rank_alloc)
+size_t rows_smem_bytes(int mode, int slice_in, int slice_out, int rows_alloc, int rank_alloc,
+                       int cluster)
 {
     size_t off[7];
-    return carve(mode, slice_in, slice_out, rows_alloc, rank_alloc, off);
+    return carve(mode, slice_in, slice_out, rows_alloc, rank_alloc, cluster, off);
 }
 
 cudaError_t launch_rows(int mode, const RowsParams &p, size_t smem, cudaStream_t stream)
