@@ -63,6 +63,7 @@ struct lora_ctx {
     std::vector<ProfEv> prof_ev;
     size_t prof_used = 0;
     RowsParamsInline inline_args;   // staging of in-parameter plans
+    int merge_path = 0;             // 0 auto (tensor cores when supported), 1 CUDA cores
 };
 
 struct lora_table {
@@ -417,7 +418,10 @@ int merge_call(lora_ctx *ctx, const lora_table *t, int adapter, void *W, int64_t
     p.rank = t->rank[size_t(adapter)];
     p.scale = sign * t->scale[size_t(adapter)];
     const long ev = prof_start(ctx, 2, stream);
-    CUDA_TRY(ctx, launch_merge_simt(p, stream));
+    if (merge_tc_supported(d_in, d_out, p.rank) && ctx->merge_path != 1)
+        CUDA_TRY(ctx, launch_merge_tc(p, 0, stream));
+    else
+        CUDA_TRY(ctx, launch_merge_simt(p, stream));
     prof_stop(ctx, ev, stream);
     ctx->last_path = 4;
     ctx->last_launches = 1;
