@@ -20,9 +20,11 @@ from . import _lib
 __all__ = ["LoraError", "Context", "AdapterTable", "lora_plan_build", "lora_shrink",
            "lora_expand", "lora_fused", "lora_merge", "lora_unmerge", "lora_tune_shape",
            "KIND_ROWS_FUSED", "KIND_SHRINK", "KIND_EXPAND", "KIND_TILE_FUSED", "KIND_MERGE",
+           "OPT_TILE_PATH", "OPT_MERGE_KERNEL", "OPT_TILE_MIN_RUN",
            "library_path"]
 
 KIND_ROWS_FUSED, KIND_SHRINK, KIND_EXPAND, KIND_TILE_FUSED, KIND_MERGE = range(5)
+OPT_TILE_PATH, OPT_MERGE_KERNEL, OPT_TILE_MIN_RUN = 1, 2, 3
 ERROR_NAMES = {0: "LORA_OK", -1: "LORA_E_INVAL", -2: "LORA_E_RANK", -3: "LORA_E_ADAPTER",
                -4: "LORA_E_NOT_RESIDENT", -5: "LORA_E_PAGE", -6: "LORA_E_CUDA",
                -7: "LORA_E_TIMEOUT", -8: "LORA_E_NOMEM", -9: "LORA_E_CAPACITY",
@@ -136,6 +138,11 @@ class Context:
         """Synchronize and read back the device status word (raises on a timeout)."""
         return _check(_L.lora_sync_status(self.handle, _stream(stream, self.device)), self)
 
+    def set_option(self, option: int, value: int):
+        """LORA_OPT_* (see include/lora.h): OPT_TILE_PATH, OPT_MERGE_KERNEL,
+        OPT_TILE_MIN_RUN."""
+        _check(_L.lora_ctx_set_option(self.handle, int(option), int(value)), self)
+
     def profile_begin(self):
         """Start bracketing every kernel launch with CUDA events."""
         _check(_L.lora_profile_begin(self.handle), self)
@@ -213,7 +220,7 @@ def lora_plan_build(ctx: Context, table: AdapterTable, ids) -> dict:
             "seg_offsets": arr(v.seg_offsets, v.n_segments + 1),
             "seg_adapter": arr(v.seg_adapter, v.n_segments),
             "row_items": int(v.row_items), "tile_items": int(v.tile_items),
-            "rows_per_item": int(v.rows_per_item)}
+            "rows_per_item": int(v.rows_per_item), "tile_min_run": int(v.tile_min_run)}
 
 
 def lora_shrink(ctx: Context, table: AdapterTable, ids, x: torch.Tensor, v: torch.Tensor,

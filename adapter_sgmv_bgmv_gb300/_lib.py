@@ -18,7 +18,8 @@ class PlanView(ctypes.Structure):
                 ("perm", ctypes.POINTER(ctypes.c_int32)), ("n_segments", I64),
                 ("seg_offsets", ctypes.POINTER(ctypes.c_int32)),
                 ("seg_adapter", ctypes.POINTER(ctypes.c_int32)),
-                ("row_items", I64), ("tile_items", I64), ("rows_per_item", I64)]
+                ("row_items", I64), ("tile_items", I64), ("rows_per_item", I64),
+                ("tile_min_run", I64)]
 
 
 SIGNATURES = {
@@ -42,6 +43,7 @@ SIGNATURES = {
     "lora_sync_status": ([P, P], I),
     "lora_last_path": ([P, ctypes.POINTER(I)], I),
     "lora_profile_begin": ([P], I),
+    "lora_ctx_set_option": ([P, I, I], I),
     "lora_profile_end": ([P, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(I64)], I),
 }
 

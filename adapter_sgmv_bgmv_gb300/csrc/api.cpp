@@ -64,6 +64,10 @@ struct lora_ctx {
     size_t prof_used = 0;
     RowsParamsInline inline_args;   // staging of in-parameter plans
     int merge_path = 0;             // 0 auto (tensor cores when supported), 1 CUDA cores
+    int tile_path = 1;              // 1: long same-adapter runs use the tensor-core tiles
+    int tile_min_run_override = 0;  // > 0: fixed minimum run for the tile path
+    uint8_t *vtiles = nullptr;      // fused tile path: per-tile V between its two kernels
+    size_t vtiles_cap = 0;
 };
 
 struct lora_table {
@@ -345,6 +349,85 @@ int run_rows(lora_ctx *ctx, const lora_table *t, int mode, RowsCfg cfg, const vo
     return slot ? release_slot(ctx, slot, stream) : LORA_OK;
 }
 
+// Minimum run of consecutive same-adapter rows that goes to the tensor-core tile
+// kernels (shorter runs use the row-gather kernel); 0 disables the tile path.
+int tile_min_run(const lora_ctx *ctx, int64_t n_act, int d_in, int d_out, int rank)
+{
+    if (ctx->tile_min_run_override > 0)
+        return ctx->tile_min_run_override;
+    TileCfg tc;
+    if (ctx->tiles.lookup(TileKey{kKindTileFused, pow2_bucket(n_act), d_in, d_out, rank}, tc))
+        return tc[0];
+    return 64;
+}
+
+int run_tiles(lora_ctx *ctx, const lora_table *t, int mode, const void *x, int64_t ldx, int d_in,
+              float *v, int64_t ldv, void *y, int64_t ldy, int d_out, int64_t n,
+              cudaStream_t stream)
+{
+    Plan &pl = ctx->plan;
+    if (pl.tile_items.empty())
+        return LORA_OK;
+    const size_t items_bytes = pl.tile_items.size() * sizeof(TileItem);
+    Slot *slot = nullptr;
+    int rc = acquire_slot(ctx, items_bytes + 16, &slot);
+    if (rc != LORA_OK)
+        return rc;
+    std::memcpy(slot->host, pl.tile_items.data(), items_bytes);
+    CUDA_TRY(ctx, cudaMemcpyAsync(slot->dev, slot->host, items_bytes, cudaMemcpyHostToDevice, stream));
+    if (mode == kFused) {
+        const size_t need = pl.tile_items.size() * size_t(kVTileBytes);
+        if (need > ctx->vtiles_cap) {
+            // Grows once to the largest tile count seen; later calls reuse it.
+            if (ctx->vtiles) {
+                CUDA_TRY(ctx, cudaStreamSynchronize(stream));
+                cudaFree(ctx->vtiles);
+                ctx->vtiles = nullptr;
+                ctx->vtiles_cap = 0;
+            }
+            if (cudaMalloc(reinterpret_cast<void **>(&ctx->vtiles), need) != cudaSuccess)
+                return LORA_E_NOMEM;
+            ctx->vtiles_cap = need;
+        }
+    }
+    TileParams p{};
+    p.x = static_cast<const uint16_t *>(x);
+    p.ldx = ldx;
+    p.y = static_cast<uint16_t *>(y);
+    p.ldy = ldy;
+    p.a_pool = t->a_pool;
+    p.a_pw = t->a_pw;
+    p.b_pool = t->b_pool;
+    p.b_pw = t->b_pw;
+    p.a_pages = t->d_a_pages;
+    p.b_pages = t->d_b_pages;
+    p.items = reinterpret_cast<const TileItem *>(slot->dev);
+    p.vtiles = reinterpret_cast<uint16_t *>(ctx->vtiles);
+    p.v = v;
+    p.ldv = ldv;
+    p.status = ctx->d_status;
+    p.max_rank = t->max_rank;
+    p.n_rows = int(n);
+    p.d_in = d_in;
+    p.d_out = d_out;
+    p.n_items = int(pl.tile_items.size());
+    p.vmode = mode == kFused ? 0 : 1;
+    if (mode != kExpand) {
+        const long ev = prof_start(ctx, 1, stream);
+        CUDA_TRY(ctx, launch_shrink_tc(p, stream));
+        prof_stop(ctx, ev, stream);
+        ctx->last_launches += 1;
+    }
+    if (mode != kShrink) {
+        const long ev = prof_start(ctx, 1, stream);
+        CUDA_TRY(ctx, launch_expand_tc(p, stream));
+        prof_stop(ctx, ev, stream);
+        ctx->last_launches += 1;
+    }
+    ctx->last_path |= 2;
+    return release_slot(ctx, slot, stream);
+}
+
 int delta_call(lora_ctx *ctx, const lora_table *t, int mode, const int32_t *ids, int64_t n,
                const void *x, int64_t ldx, int d_in, float *v, int64_t ldv, void *y,
                int64_t ldy, int d_out, cudaStream_t stream)
@@ -381,9 +464,21 @@ int delta_call(lora_ctx *ctx, const lora_table *t, int mode, const int32_t *ids,
     int32_t rmax = 0;
     for (int32_t k : pl.seg_adapter)
         rmax = std::max(rmax, t->rank[size_t(k)]);
-    const RowsCfg cfg = choose_rows_cfg(ctx, mode, kind, int64_t(pl.active.size()),
-                                        int64_t(pl.seg_adapter.size()), d_in, d_out, rmax);
-    plan_items(pl, t->rank.data(), t->scale.data(), cfg.rows, 0);
+    const int64_t n_act = int64_t(pl.active.size());
+    const int min_run = (ctx->tile_path && tile_tc_supported(d_in, d_out, rmax))
+                            ? tile_min_run(ctx, n_act, d_in, d_out, rmax)
+                            : 0;
+    // Rows-kernel shape from the rows that stay on it (approximated by all rows when
+    // the tile path is off).
+    RowsCfg cfg = choose_rows_cfg(ctx, mode, kind, n_act, int64_t(pl.seg_adapter.size()), d_in,
+                                  d_out, rmax);
+    plan_items(pl, t->rank.data(), t->scale.data(), cfg.rows, min_run);
+    if (!pl.tile_items.empty() && pl.row_active > 0 && pl.row_active < n_act)
+        cfg = choose_rows_cfg(ctx, mode, kind, pl.row_active, int64_t(pl.row_items.size()), d_in,
+                              d_out, pl.row_max_rank);
+    rc = run_tiles(ctx, t, mode, x, ldx, d_in, v, ldv, y, ldy, d_out, n, stream);
+    if (rc != LORA_OK)
+        return rc;
     return run_rows(ctx, t, mode, cfg, x, ldx, d_in, v, ldv, y, ldy, d_out, stream);
 }
 
@@ -535,6 +630,8 @@ int lora_ctx_destroy(lora_ctx *ctx)
     }
     if (ctx->d_status)
         cudaFree(ctx->d_status);
+    if (ctx->vtiles)
+        cudaFree(ctx->vtiles);
     cudaSetDevice(prev);
     delete ctx;
     return LORA_OK;
@@ -638,10 +735,16 @@ int lora_plan_build(lora_ctx *ctx, const lora_table *t, const int32_t *ids, int6
     if (rc != LORA_OK)
         return rc;
     Plan &pl = ctx->plan;
-    const RowsCfg cfg = default_rows_cfg(kFused, int64_t(pl.active.size()),
-                                         int64_t(pl.seg_adapter.size()), t->a_pw, t->b_pw,
-                                         pl.max_rank > 0 ? pl.max_rank : 8);
-    plan_items(pl, t->rank.data(), t->scale.data(), cfg.rows, 0);
+    int32_t rmax = 8;
+    for (int32_t k : pl.seg_adapter)
+        rmax = std::max(rmax, t->rank[size_t(k)]);
+    const int64_t n_act = int64_t(pl.active.size());
+    const int min_run = (ctx->tile_path && tile_tc_supported(t->a_pw, t->b_pw, rmax))
+                            ? tile_min_run(ctx, n_act, t->a_pw, t->b_pw, rmax)
+                            : 0;
+    const RowsCfg cfg = choose_rows_cfg(ctx, kFused, kKindRowsFused, n_act,
+                                        int64_t(pl.seg_adapter.size()), t->a_pw, t->b_pw, rmax);
+    plan_items(pl, t->rank.data(), t->scale.data(), cfg.rows, min_run);
     out->n_active = int64_t(pl.active.size());
     out->active_rows = pl.active.data();
     out->perm = pl.perm.data();
@@ -651,6 +754,7 @@ int lora_plan_build(lora_ctx *ctx, const lora_table *t, const int32_t *ids, int6
     out->row_items = int64_t(pl.row_items.size());
     out->tile_items = int64_t(pl.tile_items.size());
     out->rows_per_item = cfg.rows;
+    out->tile_min_run = min_run;
     return LORA_OK;
 }
 
@@ -721,6 +825,26 @@ int lora_sync_status(lora_ctx *ctx, void *stream)
         return LORA_E_TIMEOUT;
     }
     return LORA_OK;
+}
+
+int lora_ctx_set_option(lora_ctx *ctx, int option, int value)
+{
+    if (!ctx)
+        return LORA_E_INVAL;
+    switch (option) {
+    case LORA_OPT_TILE_PATH: ctx->tile_path = value ? 1 : 0; return LORA_OK;
+    case LORA_OPT_MERGE_KERNEL:
+        if (value < 0 || value > 1)
+            return LORA_E_INVAL;
+        ctx->merge_path = value;
+        return LORA_OK;
+    case LORA_OPT_TILE_MIN_RUN:
+        if (value < 0)
+            return LORA_E_INVAL;
+        ctx->tile_min_run_override = value;
+        return LORA_OK;
+    default: return LORA_E_INVAL;
+    }
 }
 
 int lora_profile_begin(lora_ctx *ctx)

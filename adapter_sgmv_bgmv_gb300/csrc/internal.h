@@ -17,14 +17,16 @@ struct RowItem {
 };
 static_assert(sizeof(RowItem) == 16, "RowItem is one 16-byte load");
 
-// One tile of the tensor-core kernel: rows [row0, row0 + nrows) of x / y (a run of
-// consecutive rows that share one adapter), nrows <= 128.
+// One tile of the tensor-core kernels: rows [row0, row0 + nrows) of x / y (a run of
+// consecutive rows that share adapter `adapter`), nrows <= 128.
 struct TileItem {
     int32_t adapter;
     int32_t row0;
-    int32_t nrows;
-    int32_t pad;
+    int16_t nrows;
+    int16_t rank;
+    float scale;
 };
+static_assert(sizeof(TileItem) == 16, "TileItem is one 16-byte load");
 
 enum Mode : int { kShrink = 0, kExpand = 1, kFused = 2 };
 
@@ -75,7 +77,37 @@ cudaError_t launch_rows_inline(int mode, const RowsParamsInline &a, size_t smem,
                                cudaStream_t stream);
 int rows_max_smem();
 
-// Tensor-core kernels (defined in tc_*.cu).
+// Tensor-core tile kernels (tile_tc.cu).  V travels between them as bf16 tiles of
+// 128 rows x 128 ranks in the layout the expand MMA reads (32 KB per tile).
+constexpr int kVTileBytes = 128 * 128 * 2;
+struct TileParams {
+    const uint16_t *x;
+    int64_t ldx;
+    uint16_t *y;
+    int64_t ldy;
+    const uint16_t *a_pool;
+    int64_t a_pw;
+    const uint16_t *b_pool;
+    int64_t b_pw;
+    const int32_t *a_pages;
+    const int32_t *b_pages;
+    const TileItem *items;
+    uint16_t *vtiles;         // fused: per-tile V in MMA layout
+    float *v;                 // shrink / expand only: fp32 rows [n, ldv]
+    int64_t ldv;
+    unsigned *status;
+    int max_rank;
+    int n_rows;               // rows of x / y (tensor-map extent)
+    int d_in;
+    int d_out;
+    int n_items;
+    int vmode;                // 0: V tiles (fused), 1: fp32 v rows
+};
+cudaError_t launch_shrink_tc(const TileParams &p, cudaStream_t stream);
+cudaError_t launch_expand_tc(const TileParams &p, cudaStream_t stream);
+bool tile_tc_supported(int d_in, int d_out, int rank);
+
+// Tensor-core merge (merge_tc.cu).
 struct MergeParams {
     uint16_t *W;
     int64_t ldw;

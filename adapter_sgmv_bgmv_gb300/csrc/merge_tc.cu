@@ -156,7 +156,8 @@ __global__ void __launch_bounds__(kThreads) k_merge_tc(const __grid_constant__ M
     __syncthreads();
     if (tid == 0 && ok) {
         tc::tma_store_2d(&args.tmW, o0, c0, sW);
-        tc::tma_store_2d(&args.tmW, o0 + 64, c0, sW + kBM * 128);
+        if (o0 + 64 < p.d_out)   // a box wholly right of d_out is not stored
+            tc::tma_store_2d(&args.tmW, o0 + 64, c0, sW + kBM * 128);
         tc::bulk_commit();
         tc::bulk_wait_read0();
     }

@@ -74,7 +74,9 @@ typedef struct lora_table lora_table;
  *   seg_adapter  adapter id of segment s                              [n_segments]
  *   row_items    work items of the row-gather (decode) kernel, each at most
  *                rows_per_item consecutive entries of one segment of perm
- *   tile_items   128-row tiles of the tensor-core (prefill) kernel             */
+ *   tile_items   tiles of at most 128 consecutive rows of one adapter for the
+ *                tensor-core kernels: every maximal run of consecutive row indices
+ *                inside a segment that is at least tile_min_run long (0: no tiles) */
 typedef struct {
     int64_t n_active;
     const int32_t *active_rows;
@@ -85,6 +87,7 @@ typedef struct {
     int64_t row_items;
     int64_t tile_items;
     int64_t rows_per_item;
+    int64_t tile_min_run;
 } lora_plan_view;
 
 /* Create a context on `device` for batches of at most max_rows rows and adapters
@@ -166,6 +169,16 @@ int lora_tune_shape(lora_ctx *ctx, const lora_table *table, int kind,
 /* Synchronize `stream`, then read and clear the device status word: LORA_OK or
  * LORA_E_TIMEOUT if a kernel's bounded wait expired since the last check. */
 int lora_sync_status(lora_ctx *ctx, void *stream);
+
+/* Context options (all default to the fastest choice):
+ *   LORA_OPT_TILE_PATH     1 (default) route runs of >= tile_min_run consecutive
+ *                          same-adapter rows to the tensor-core tile kernels; 0 keeps
+ *                          every row on the row-gather kernel
+ *   LORA_OPT_MERGE_KERNEL  0 (default) tensor-core merge where supported; 1 CUDA cores
+ *   LORA_OPT_TILE_MIN_RUN  > 0 fixes the minimum run length; 0 uses the tile table
+ *                          (default 64) */
+enum { LORA_OPT_TILE_PATH = 1, LORA_OPT_MERGE_KERNEL = 2, LORA_OPT_TILE_MIN_RUN = 3 };
+int lora_ctx_set_option(lora_ctx *ctx, int option, int value);
 
 /* Per-launch timing: between lora_profile_begin and lora_profile_end every kernel
  * launch of the context is bracketed by CUDA events on its stream.  _end

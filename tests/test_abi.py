@@ -80,6 +80,8 @@ def test_library_plan_is_bit_exact_against_numpy(seed):
         ids[:] = -1
     if seed == 5:
         ids[:] = 2
+    if seed == 6:
+        ids[50:400] = 1                        # one long run among short ones
     p = L.lora_plan_build(ctx, t, ids)
     a, pm, so, sa = _numpy_plan(ids, 6)
     np.testing.assert_array_equal(p["active_rows"], a)
@@ -88,9 +90,24 @@ def test_library_plan_is_bit_exact_against_numpy(seed):
     np.testing.assert_array_equal(p["seg_adapter"], sa)
     R = p["rows_per_item"]
     assert 1 <= R <= 64
-    lens = np.diff(so)
-    assert p["row_items"] + p["tile_items"] >= 1 or len(a) == 0
-    assert p["row_items"] == int(np.sum((lens + R - 1) // R))
+    # independent item count: runs of consecutive rows inside each segment that are
+    # at least tile_min_run long become 128-row tiles, the rest R-row items
+    m = p["tile_min_run"]
+    n_tiles = n_rows = 0
+    for s in range(len(sa)):
+        seg = pm[so[s]:so[s + 1]]
+        breaks = np.flatnonzero(np.diff(seg) != 1) + 1
+        runs = np.split(seg, breaks)
+        pending = 0
+        for run in runs:
+            if m > 0 and len(run) >= m:
+                n_rows += (pending + R - 1) // R
+                pending = 0
+                n_tiles += (len(run) + 127) // 128
+            else:
+                pending += len(run)
+        n_rows += (pending + R - 1) // R
+    assert p["tile_items"] == n_tiles and p["row_items"] == n_rows
     # page accounting of the table: adapter k holds 2 r_k pages, r_k (d_in + d_out) values
     ranks = np.array([8, 16, 8, 24, 8, 8])
     assert (t.a_pages >= 0).sum(axis=1).tolist() == ranks.tolist()

@@ -180,3 +180,71 @@ def test_host_side_errors_launch_nothing(ctx):
     with pytest.raises(L.LoraError) as e:
         L.lora_fused(ctx, t3, np.array([1], np.int32), x[:1], y[:1])
     assert e.value.name == "LORA_E_RANK"
+
+
+# ------------------------------------------------------------------ tensor-core tiles
+
+TILE_CASES = {
+    # one adapter, 300 consecutive rows: tiles of 128, 128 and 44 rows; d_in not a
+    # multiple of the 64-wide K block, d_out not a multiple of the 128-wide N chunk
+    "ragged_single_run": dict(seed=51, n=300, d_in=200, d_out=136, n_adapters=1, ranks=[24],
+                              ids=np.zeros(300, np.int32)),
+    # runs of several adapters cut by released rows, mixed ranks (pads 8 -> 16, 40 -> 48)
+    "runs_with_releases": dict(seed=52, n=700, d_in=256, d_out=384, n_adapters=3,
+                               ranks=[8, 40, 64], paged=True,
+                               ids=np.concatenate([np.full(150, 0), np.full(3, -1),
+                                                   np.full(260, 2), np.full(17, 1),
+                                                   np.full(200, 1), np.full(70, 0)]).astype(np.int32)),
+}
+
+
+def _tile_check(ctx, c, tile_path: bool):
+    ctx.set_option(L.OPT_TILE_PATH, 1 if tile_path else 0)
+    try:
+        got = run_fused(ctx, c)
+        path, launches = ctx.last_path()
+    finally:
+        ctx.set_option(L.OPT_TILE_PATH, 1)
+    ref = oracle.fused(oracle.Table.from_case(c), c["ids"], c["x"], c["y"], nthreads=8)
+    assert_parity(got, ref, REL_FROB, MAX_ABS_RMS, f"tile_path={tile_path}")
+    rel = c["ids"] < 0
+    np.testing.assert_array_equal(got[rel], c["y"][rel])
+    return path
+
+
+@pytest.mark.parametrize("name", sorted(TILE_CASES))
+def test_tile_kernels_match_oracle(ctx, name):
+    c = workloads.small(**TILE_CASES[name])
+    assert _tile_check(ctx, c, True) & 2          # the tensor-core tiles ran
+    assert _tile_check(ctx, c, False) == 1        # row-gather only
+
+
+def test_tile_kernels_rank_128():
+    big = L.Context(0, max_rows=4096, max_rank=128)
+    c = workloads.small(seed=53, n=256, d_in=320, d_out=512, n_adapters=2, ranks=[128, 96],
+                        ids=np.repeat(np.array([0, 1], np.int32), 128))
+    assert _tile_check(big, c, True) & 2
+    big.close()
+
+
+def test_tile_shrink_and_expand_match_oracle(ctx):
+    c = workloads.small(seed=54, n=400, d_in=192, d_out=256, n_adapters=2, ranks=[32, 16],
+                        ids=np.repeat(np.array([1, 0], np.int32), 200))
+    table = upload_table(ctx, c)
+    t = oracle.Table.from_case(c)
+    v_ref = oracle.shrink(t, c["ids"], c["x"])
+    v = torch.full((c["n"], 64), float("nan"), device="cuda")
+    L.lora_shrink(ctx, table, c["ids"], to_dev(c["x"]), v)
+    ctx.sync_status()
+    assert ctx.last_path()[0] & 2
+    vg = v.cpu().numpy()
+    np.testing.assert_array_equal(np.isnan(vg), np.isnan(v_ref))
+    m = ~np.isnan(v_ref)
+    assert np.abs(vg[m] - v_ref[m]).max() <= 1e-3 * np.sqrt(np.mean(v_ref[m] ** 2))
+    v0 = np.where(np.isnan(v_ref), 0, v_ref).astype(np.float32)
+    y = to_dev(c["y"])
+    L.lora_expand(ctx, table, c["ids"], torch.from_numpy(v0).cuda(), y)
+    ctx.sync_status()
+    assert ctx.last_path()[0] & 2
+    assert_parity(from_dev(y), oracle.expand(t, c["ids"], v0, c["y"]), REL_FROB, MAX_ABS_RMS,
+                  "tile expand")
