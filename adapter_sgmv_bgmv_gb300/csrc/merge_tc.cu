@@ -130,6 +130,7 @@ __global__ void __launch_bounds__(kThreads) k_merge_tc(const __grid_constant__ M
     bool ok = mbar_wait_bounded(bar_mma, 0, p.status, kDevTimeoutMma);
     tc::fence_after_sync();
     ok = mbar_wait_bounded(bar_w, 0, p.status, kDevTimeoutLoad) && ok;
+    ok = __syncthreads_and(ok);         // converged, one decision for the whole CTA
 
     if (ok) {
         const int row = warp * 32 + lane;   // TMEM lane == tile row
@@ -168,6 +169,7 @@ __global__ void __launch_bounds__(kThreads) k_merge_tc(const __grid_constant__ M
     }
     __syncthreads();
     if (warp == 0) {
+        __syncwarp();
         tc::fence_after_sync();
         tc::tmem_dealloc(tmem, kTmemCols);
     }

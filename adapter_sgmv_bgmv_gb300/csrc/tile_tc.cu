@@ -164,6 +164,7 @@ __global__ void __launch_bounds__(kShrinkThreads, 1) k_shrink_tc(const __grid_co
 
         // Epilogue: this warp reads TMEM lanes 32*(warp%4) .. +31.
         ok = mbar_wait_bounded(done, 0, p.status, kDevTimeoutMma) && ok;
+        ok = __all_sync(0xffffffffu, ok);   // warp converged and agreed before tcgen05.ld
         tc::fence_after_sync();
         const int row = 32 * (warp & 3) + lane;
         float v[16];
@@ -195,6 +196,7 @@ __global__ void __launch_bounds__(kShrinkThreads, 1) k_shrink_tc(const __grid_co
     tc::fence_before_sync();
     __syncthreads();
     if (warp == 1) {
+        __syncwarp();
         tc::fence_after_sync();
         tc::tmem_dealloc(tmem, ncols);
     }
@@ -293,6 +295,8 @@ __global__ void __launch_bounds__(kExpandThreads) k_expand_tc(const __grid_const
     ok = mbar_wait_bounded(bar_mma, 0, p.status, kDevTimeoutMma) && ok;
     tc::fence_after_sync();
     ok = mbar_wait_bounded(bar_in, 0, p.status, kDevTimeoutLoad) && ok;
+    ok = __all_sync(0xffffffffu, ok);
+    ok = __syncthreads_and(ok);         // one decision for the whole CTA
 
     if (ok) {
         const int row = warp * 32 + lane;
@@ -346,6 +350,7 @@ __global__ void __launch_bounds__(kExpandThreads) k_expand_tc(const __grid_const
     tc::fence_before_sync();
     __syncthreads();
     if (warp == 0) {
+        __syncwarp();
         tc::fence_after_sync();
         tc::tmem_dealloc(tmem, kBN);
     }
