@@ -358,7 +358,7 @@ int tile_min_run(const lora_ctx *ctx, int64_t n_act, int d_in, int d_out, int ra
     TileCfg tc;
     if (ctx->tiles.lookup(TileKey{kKindTileFused, pow2_bucket(n_act), d_in, d_out, rank}, tc))
         return tc[0];
-    return 64;
+    return 128;
 }
 
 int run_tiles(lora_ctx *ctx, const lora_table *t, int mode, const void *x, int64_t ldx, int d_in,
@@ -412,6 +412,7 @@ int run_tiles(lora_ctx *ctx, const lora_table *t, int mode, const void *x, int64
     p.d_out = d_out;
     p.n_items = int(pl.tile_items.size());
     p.vmode = mode == kFused ? 0 : 1;
+    p.max_tile_rank = pl.tile_max_rank;
     if (mode != kExpand) {
         const long ev = prof_start(ctx, 1, stream);
         CUDA_TRY(ctx, launch_shrink_tc(p, stream));

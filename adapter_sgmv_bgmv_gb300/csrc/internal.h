@@ -77,9 +77,10 @@ cudaError_t launch_rows_inline(int mode, const RowsParamsInline &a, size_t smem,
                                cudaStream_t stream);
 int rows_max_smem();
 
-// Tensor-core tile kernels (tile_tc.cu).  V travels between them as bf16 tiles of
-// 128 rows x 128 ranks in the layout the expand MMA reads (32 KB per tile).
-constexpr int kVTileBytes = 128 * 128 * 2;
+// Tensor-core tile kernels (tile_tc.cu).  V travels between them as a pair of bf16
+// tiles (v = hi + lo, each 128 rows x up to 128 ranks) in the layout the expand MMA
+// reads: 16 KB per 64 ranks, hi atoms first, 64 KB per tile at most.
+constexpr int kVTileBytes = 128 * 128 * 2 * 2;
 struct TileParams {
     const uint16_t *x;
     int64_t ldx;
@@ -102,6 +103,7 @@ struct TileParams {
     int d_out;
     int n_items;
     int vmode;                // 0: V tiles (fused), 1: fp32 v rows
+    int max_tile_rank;        // largest rank among the items (sizes shared memory)
 };
 cudaError_t launch_shrink_tc(const TileParams &p, cudaStream_t stream);
 cudaError_t launch_expand_tc(const TileParams &p, cudaStream_t stream);

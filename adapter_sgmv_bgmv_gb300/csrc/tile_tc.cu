@@ -12,14 +12,16 @@
 //   warp 1   issues the tcgen05 MMAs (M = 128, N = r, K = 64 per stage) into a TMEM
 //            accumulator and frees each stage with tcgen05.commit;
 //   warps 2-5 finally read V from TMEM (row t = lane t) and write it either as a
-//            bf16 tile already in the expand MMA's operand layout, or as fp32 rows.
+//            pair of bf16 tiles hi = bf16(v), lo = bf16(v - hi) already in the expand
+//            MMA's operand layout, or as fp32 rows.
 //
 // k_expand_tc, one CTA per (tile, 128-column chunk of d_out):
 //   y[rows, n0:n0+128] = bf16(y + s_k * V . B_k[:, n0:n0+128])
-//   one bulk copy brings the V tile, TMA brings the y tile, all threads stage B_k's
-//   r x 128 block (N-major, from the pages), one thread issues the K = r MMAs into
-//   TMEM; the epilogue adds s * acc to the y tile in shared memory and stores it with
-//   TMA when all 128 rows belong to the tile, else row by row.
+//   one bulk copy brings the V tiles, TMA brings the y tile, all threads stage B_k's
+//   r x 128 block (N-major, from the pages), one thread issues the MMAs
+//   acc = V_hi . B + V_lo . B (K = r each) into TMEM, so v enters with about 16
+//   significant bits; the epilogue adds s * acc to the y tile in shared memory and
+//   stores it with TMA when all 128 rows belong to the tile, else row by row.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -54,10 +56,13 @@ constexpr uint32_t shrink_smem_bytes()
     return 1024u + kStages * kStage + 2u * kStages * 8u + 64u + 4u * 128u;
 }
 
-__host__ __device__ inline uint32_t expand_smem_bytes()
+// 64-rank atom columns of one V half (hi or lo) for a padded rank.
+__host__ __device__ inline int v_atoms(int rp) { return (rp + 63) / 64; }
+
+__host__ __device__ inline uint32_t expand_smem_bytes(int rp)
 {
-    return 1024u + uint32_t(kVTileBytes) /* V, up to 128 ranks */ +
-           128u * kBN * 2u /* B, up to 128 ranks */ + uint32_t(kTM) * kBN * 2u /* y */ + 64u;
+    return 1024u + 2u * uint32_t(v_atoms(rp)) * (kTM * 128u) /* V hi + lo */ +
+           uint32_t(rp) * kBN * 2u /* B */ + uint32_t(kTM) * kBN * 2u /* y */ + 64u;
 }
 
 // ---------------------------------------------------------------------- shrink
@@ -173,14 +178,23 @@ __global__ void __launch_bounds__(kShrinkThreads, 1) k_shrink_tc(const __grid_co
             if (!ok)
                 continue;
             if (p.vmode == 0) {
-                // bf16, K-major 128-byte-swizzled: 64 ranks per 16 KB atom column
+                // bf16 hi and lo, K-major 128-byte-swizzled: 64 ranks per 16 KB atom
                 uint8_t *tile = reinterpret_cast<uint8_t *>(p.vtiles) +
-                                size_t(blockIdx.x) * kVTileBytes + (c16 >> 2) * (kTM * 128);
+                                size_t(blockIdx.x) * kVTileBytes;
+                uint8_t *hi = tile + (c16 >> 2) * (kTM * 128);
+                uint8_t *lo = tile + (v_atoms(rp) + (c16 >> 2)) * (kTM * 128);
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
-                    const uint32_t chunk = uint32_t((c16 & 3) * 2 + h);
-                    *reinterpret_cast<uint4 *>(tile + tc::sw128(uint32_t(row), chunk)) =
-                        pack8(v + 8 * h);
+                    const uint32_t off = tc::sw128(uint32_t(row), uint32_t((c16 & 3) * 2 + h));
+                    float rem[8];
+                    const uint4 hv = pack8(v + 8 * h);
+                    float back[8];
+                    unpack8(hv, back);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        rem[e] = v[8 * h + e] - back[e];
+                    *reinterpret_cast<uint4 *>(hi + off) = hv;
+                    *reinterpret_cast<uint4 *>(lo + off) = pack8(rem);
                 }
             } else if (row < it.nrows) {
                 float *dst = p.v + int64_t(it.row0 + row) * p.ldv + 16 * c16;
@@ -211,13 +225,6 @@ __global__ void __launch_bounds__(kExpandThreads) k_expand_tc(const __grid_const
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t *gbase = smem_raw + (base - raw);
-    const uint32_t sV = base;                          // up to 2 atom columns x 16 KB
-    const uint32_t sB = sV + kVTileBytes;              // rp * 256 B
-    const uint32_t sY = sB + 128u * kBN * 2u;          // 2 boxes x 16 KB
-    const uint32_t bar_in = sY + kTM * kBN * 2u;
-    const uint32_t bar_mma = bar_in + 8;
-    const uint32_t tmem_slot = bar_in + 16;
-
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int n_chunks = (p.d_out + kBN - 1) / kBN;
     const int item = blockIdx.x / n_chunks;
@@ -225,6 +232,13 @@ __global__ void __launch_bounds__(kExpandThreads) k_expand_tc(const __grid_const
     const TileItem it = p.items[item];
     const int r = it.rank, rp = rank_pad16(r);
     const uint32_t lbo = uint32_t(rp / 8) * 1024u;     // N-atom stride of the B operand
+    const int atoms = v_atoms(rp);
+    const uint32_t sV = base;                          // hi atoms, then lo atoms
+    const uint32_t sB = sV + 2u * atoms * (kTM * 128); // rp * 256 B
+    const uint32_t sY = sB + uint32_t(rp) * kBN * 2u;  // 2 boxes x 16 KB
+    const uint32_t bar_in = sY + kTM * kBN * 2u;
+    const uint32_t bar_mma = bar_in + 8;
+    const uint32_t tmem_slot = bar_in + 16;
 
     if (tid == 0) {
         mbar_init(bar_in, 1);
@@ -238,7 +252,7 @@ __global__ void __launch_bounds__(kExpandThreads) k_expand_tc(const __grid_const
     tc::fence_after_sync();
     const uint32_t tmem = *reinterpret_cast<const uint32_t *>(gbase + (tmem_slot - base));
 
-    const uint32_t v_bytes = rp <= 64 ? uint32_t(kTM * 128) : uint32_t(kVTileBytes);
+    const uint32_t v_bytes = 2u * atoms * (kTM * 128);
     if (tid == 0) {
         mbar_arrive_expect_tx(bar_in, uint32_t(kTM) * kBN * 2u + (p.vmode == 0 ? v_bytes : 0u));
         tc::tma_load_2d(sY, &args.map, n0, it.row0, bar_in);
@@ -260,17 +274,24 @@ __global__ void __launch_bounds__(kExpandThreads) k_expand_tc(const __grid_const
         *reinterpret_cast<uint4 *>(gbase + (sB - base) + off) = vb;
     }
     if (p.vmode == 1) {
-        // V from fp32 rows: row t of the tile, ranks rounded once to bf16.
+        // V from fp32 rows: row t of the tile, split into bf16 hi + lo.
         const int row = tid;
         for (int c = 0; c < rp / 8; ++c) {
-            float f[8];
+            float f[8], back[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 const int j = 8 * c + e;
                 f[e] = (row < it.nrows && j < r) ? p.v[int64_t(it.row0 + row) * p.ldv + j] : 0.f;
             }
-            *reinterpret_cast<uint4 *>(gbase + (sV - base) + (c >> 3) * (kTM * 128) +
-                                       tc::sw128(uint32_t(row), uint32_t(c & 7))) = pack8(f);
+            const uint4 hv = pack8(f);
+            unpack8(hv, back);
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                f[e] -= back[e];
+            const uint32_t off = tc::sw128(uint32_t(row), uint32_t(c & 7));
+            *reinterpret_cast<uint4 *>(gbase + (sV - base) + (c >> 3) * (kTM * 128) + off) = hv;
+            *reinterpret_cast<uint4 *>(gbase + (sV - base) + (atoms + (c >> 3)) * (kTM * 128) +
+                                       off) = pack8(f);
         }
     }
     tc::fence_proxy_async_smem();
@@ -283,11 +304,14 @@ __global__ void __launch_bounds__(kExpandThreads) k_expand_tc(const __grid_const
         ok = mbar_wait_bounded(bar_in, 0, p.status, kDevTimeoutLoad);
         if (ok) {
             const uint32_t idesc = tc::idesc_bf16(kTM, kBN, 0, 1);
-            for (int kk = 0; kk < rp / 16; ++kk) {
-                const uint64_t dv = tc::smem_desc_sw128(
-                    sV + uint32_t(kk >> 2) * (kTM * 128) + uint32_t(kk & 3) * 32u, 16u, 1024u);
-                const uint64_t db = tc::smem_desc_sw128(sB + uint32_t(kk) * 2048u, lbo, 1024u);
-                tc::mma_bf16(tmem, dv, db, idesc, kk > 0 ? 1u : 0u);
+            for (int part = 0; part < 2; ++part) {       // V_hi . B, then + V_lo . B
+                const uint32_t vp = sV + uint32_t(part * atoms) * (kTM * 128);
+                for (int kk = 0; kk < rp / 16; ++kk) {
+                    const uint64_t dv = tc::smem_desc_sw128(
+                        vp + uint32_t(kk >> 2) * (kTM * 128) + uint32_t(kk & 3) * 32u, 16u, 1024u);
+                    const uint64_t db = tc::smem_desc_sw128(sB + uint32_t(kk) * 2048u, lbo, 1024u);
+                    tc::mma_bf16(tmem, dv, db, idesc, (part > 0 || kk > 0) ? 1u : 0u);
+                }
             }
         }
         tc::mma_commit(bar_mma);
@@ -396,7 +420,7 @@ cudaError_t launch_expand_tc(const TileParams &p, cudaStream_t stream)
     static bool configured = false;
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(k_expand_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             int(expand_smem_bytes()));
+                                             int(expand_smem_bytes(128)));
         if (e != cudaSuccess)
             return e;
         configured = true;
@@ -405,7 +429,7 @@ cudaError_t launch_expand_tc(const TileParams &p, cudaStream_t stream)
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(unsigned(p.n_items) * unsigned(n_chunks));
     cfg.blockDim = dim3(kExpandThreads);
-    cfg.dynamicSmemBytes = expand_smem_bytes();
+    cfg.dynamicSmemBytes = expand_smem_bytes(rank_pad16(p.max_tile_rank));
     cfg.stream = stream;
     return cudaLaunchKernelEx(&cfg, k_expand_tc, args);
 }

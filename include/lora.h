@@ -132,8 +132,9 @@ int lora_expand(lora_ctx *ctx, const lora_table *table, const int32_t *ids_host,
 
 /* Fused: y_i <- y_i + s_k (x_i A_k) B_k, one bf16 rounding per output element.
  * x_i . A_k never leaves the chip in the row-gather kernel; the tensor-core tile
- * kernel keeps it in fp32 tensor memory and rounds it once to bf16 as an MMA
- * operand.  Rows with id -1 untouched. */
+ * kernels accumulate it in fp32 tensor memory and hand it to the expand as a pair
+ * of bf16 operands (hi + lo, about 16 significant bits) through a context-owned
+ * scratch that stays in L2.  Rows with id -1 untouched. */
 int lora_fused(lora_ctx *ctx, const lora_table *table, const int32_t *ids_host,
                int64_t n, const void *x, int64_t ldx, int d_in, void *y, int64_t ldy,
                int d_out, void *stream);
@@ -176,7 +177,7 @@ int lora_sync_status(lora_ctx *ctx, void *stream);
  *                          every row on the row-gather kernel
  *   LORA_OPT_MERGE_KERNEL  0 (default) tensor-core merge where supported; 1 CUDA cores
  *   LORA_OPT_TILE_MIN_RUN  > 0 fixes the minimum run length; 0 uses the tile table
- *                          (default 64) */
+ *                          (default 128) */
 enum { LORA_OPT_TILE_PATH = 1, LORA_OPT_MERGE_KERNEL = 2, LORA_OPT_TILE_MIN_RUN = 3 };
 int lora_ctx_set_option(lora_ctx *ctx, int option, int value);
 

@@ -233,7 +233,7 @@ def test_tile_shrink_and_expand_match_oracle(ctx):
     table = upload_table(ctx, c)
     t = oracle.Table.from_case(c)
     v_ref = oracle.shrink(t, c["ids"], c["x"])
-    v = torch.full((c["n"], 64), float("nan"), device="cuda")
+    v = torch.full((c["n"], v_ref.shape[1]), float("nan"), device="cuda")
     L.lora_shrink(ctx, table, c["ids"], to_dev(c["x"]), v)
     ctx.sync_status()
     assert ctx.last_path()[0] & 2
