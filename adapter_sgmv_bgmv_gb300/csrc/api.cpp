@@ -66,8 +66,8 @@ struct lora_ctx {
     int merge_path = 0;             // 0 auto (tensor cores when supported), 1 CUDA cores
     int tile_path = 1;              // 1: long same-adapter runs use the tensor-core tiles
     int tile_min_run_override = 0;  // > 0: fixed minimum run for the tile path
-    uint8_t *vtiles = nullptr;      // fused tile path: per-tile V between its two kernels
-    size_t vtiles_cap = 0;
+    uint8_t *vparts = nullptr;      // fused tile path: partial V between its two kernels
+    size_t vparts_cap = 0;
 };
 
 struct lora_table {
@@ -375,19 +375,26 @@ int run_tiles(lora_ctx *ctx, const lora_table *t, int mode, const void *x, int64
         return rc;
     std::memcpy(slot->host, pl.tile_items.data(), items_bytes);
     CUDA_TRY(ctx, cudaMemcpyAsync(slot->dev, slot->host, items_bytes, cudaMemcpyHostToDevice, stream));
+    // K-split of the fused shrink: about two CTAs per SM over all tiles, each CTA
+    // keeping at least 4 K blocks of 64.
+    int ksplit = 1;
     if (mode == kFused) {
-        const size_t need = pl.tile_items.size() * size_t(kVTileBytes);
-        if (need > ctx->vtiles_cap) {
-            // Grows once to the largest tile count seen; later calls reuse it.
-            if (ctx->vtiles) {
+        const int64_t tiles = int64_t(pl.tile_items.size());
+        const int nkb = (d_in + 63) / 64;
+        while (ksplit < 8 && tiles * ksplit * 2 <= 2 * kSms && nkb / (ksplit * 2) >= 4)
+            ksplit *= 2;
+        const size_t need = size_t(tiles) * size_t(ksplit) * size_t(kVPartBytes);
+        if (need > ctx->vparts_cap) {
+            // Grows to the largest need seen; later calls reuse it.
+            if (ctx->vparts) {
                 CUDA_TRY(ctx, cudaStreamSynchronize(stream));
-                cudaFree(ctx->vtiles);
-                ctx->vtiles = nullptr;
-                ctx->vtiles_cap = 0;
+                cudaFree(ctx->vparts);
+                ctx->vparts = nullptr;
+                ctx->vparts_cap = 0;
             }
-            if (cudaMalloc(reinterpret_cast<void **>(&ctx->vtiles), need) != cudaSuccess)
+            if (cudaMalloc(reinterpret_cast<void **>(&ctx->vparts), need) != cudaSuccess)
                 return LORA_E_NOMEM;
-            ctx->vtiles_cap = need;
+            ctx->vparts_cap = need;
         }
     }
     TileParams p{};
@@ -402,7 +409,8 @@ int run_tiles(lora_ctx *ctx, const lora_table *t, int mode, const void *x, int64
     p.a_pages = t->d_a_pages;
     p.b_pages = t->d_b_pages;
     p.items = reinterpret_cast<const TileItem *>(slot->dev);
-    p.vtiles = reinterpret_cast<uint16_t *>(ctx->vtiles);
+    p.vparts = reinterpret_cast<float *>(ctx->vparts);
+    p.ksplit = ksplit;
     p.v = v;
     p.ldv = ldv;
     p.status = ctx->d_status;
@@ -631,8 +639,8 @@ int lora_ctx_destroy(lora_ctx *ctx)
     }
     if (ctx->d_status)
         cudaFree(ctx->d_status);
-    if (ctx->vtiles)
-        cudaFree(ctx->vtiles);
+    if (ctx->vparts)
+        cudaFree(ctx->vparts);
     cudaSetDevice(prev);
     delete ctx;
     return LORA_OK;

@@ -77,10 +77,10 @@ cudaError_t launch_rows_inline(int mode, const RowsParamsInline &a, size_t smem,
                                cudaStream_t stream);
 int rows_max_smem();
 
-// Tensor-core tile kernels (tile_tc.cu).  V travels between them as a pair of bf16
-// tiles (v = hi + lo, each 128 rows x up to 128 ranks) in the layout the expand MMA
-// reads: 16 KB per 64 ranks, hi atoms first, 64 KB per tile at most.
-constexpr int kVTileBytes = 128 * 128 * 2 * 2;
+// Tensor-core tile kernels (tile_tc.cu, stream_tc.cu).  In the fused call the shrink
+// splits K over `ksplit` CTAs per tile; each writes its fp32 partial V (128 rows x
+// r_pad) into its own 64 KB slot of a scratch that the expand sums in order.
+constexpr int kVPartBytes = 128 * 128 * 4;
 struct TileParams {
     const uint16_t *x;
     int64_t ldx;
@@ -93,7 +93,7 @@ struct TileParams {
     const int32_t *a_pages;
     const int32_t *b_pages;
     const TileItem *items;
-    uint16_t *vtiles;         // fused: per-tile V in MMA layout
+    float *vparts;            // fused: [n_items][ksplit] partial V slots
     float *v;                 // shrink / expand only: fp32 rows [n, ldv]
     int64_t ldv;
     unsigned *status;
@@ -104,6 +104,7 @@ struct TileParams {
     int n_items;
     int vmode;                // 0: V tiles (fused), 1: fp32 v rows
     int max_tile_rank;        // largest rank among the items (sizes shared memory)
+    int ksplit;               // fused: K-split of the shrink (1..8)
 };
 cudaError_t launch_shrink_tc(const TileParams &p, cudaStream_t stream);
 cudaError_t launch_expand_tc(const TileParams &p, cudaStream_t stream);
