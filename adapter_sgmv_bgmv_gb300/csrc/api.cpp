@@ -66,6 +66,8 @@ struct lora_ctx {
     int merge_path = 0;             // 0 auto (tensor cores when supported), 1 CUDA cores
     int tile_path = 1;              // 1: long same-adapter runs use the tensor-core tiles
     int tile_min_run_override = 0;  // > 0: fixed minimum run for the tile path
+    int force_cluster = 0;          // > 0 while tuning: row-kernel cluster width
+    int force_rows = 0;             // > 0 while tuning: rows per item
     uint8_t *vparts = nullptr;      // fused tile path: partial V between its two kernels
     size_t vparts_cap = 0;
 };
@@ -272,6 +274,8 @@ RowsCfg choose_rows_cfg(const lora_ctx *ctx, int mode, int kind, int64_t n_act, 
                         int d_in, int d_out, int rank)
 {
     RowsCfg cfg = default_rows_cfg(mode, n_act, n_seg, d_in, d_out, rank);
+    if (ctx->force_cluster > 0 && ctx->force_rows > 0)
+        return RowsCfg{ctx->force_cluster, ctx->force_rows};
     TileCfg tc;
     if (ctx->tiles.lookup(TileKey{kind, pow2_bucket(n_act), d_in, d_out, rank}, tc) &&
         tc[0] >= 1 && tc[0] <= 16 && (tc[0] & (tc[0] - 1)) == 0 && tc[1] >= 1 && tc[1] <= 64) {
@@ -521,8 +525,13 @@ int merge_call(lora_ctx *ctx, const lora_table *t, int adapter, void *W, int64_t
     p.d_out = d_out;
     p.rank = t->rank[size_t(adapter)];
     p.scale = sign * t->scale[size_t(adapter)];
+    int path = ctx->merge_path;
+    TileCfg tcfg;
+    if (path == 0 && ctx->tiles.lookup(TileKey{kKindMerge, pow2_bucket(d_in), d_in, d_out, p.rank},
+                                       tcfg))
+        path = tcfg[0];
     const long ev = prof_start(ctx, 2, stream);
-    if (merge_tc_supported(d_in, d_out, p.rank) && ctx->merge_path != 1)
+    if (merge_tc_supported(d_in, d_out, p.rank) && path != 1)
         CUDA_TRY(ctx, launch_merge_tc(p, 0, stream));
     else
         CUDA_TRY(ctx, launch_merge_simt(p, stream));
@@ -895,10 +904,126 @@ int lora_last_path(const lora_ctx *ctx, int *n_launches)
     return ctx->last_path;
 }
 
-int lora_tune_shape(lora_ctx *, const lora_table *, int, const int32_t *, int64_t, const void *,
-                    int64_t, int, void *, int64_t, int, int, float *, void *)
+int lora_tune_shape(lora_ctx *ctx, const lora_table *t, int kind, const int32_t *ids, int64_t n,
+                    const void *x, int64_t ldx, int d_in, void *y, int64_t ldy, int d_out,
+                    int iters, float *best_us, void *stream_ptr)
 {
-    return LORA_E_UNSUPPORTED;
+    if (!ctx || !t || !best_us || iters < 1 || kind < 0 || kind > 4 || !ids || n < 1)
+        return LORA_E_INVAL;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+    int rc = use_device(ctx);
+    if (rc != LORA_OK)
+        return rc;
+    // One candidate: warm up twice, then the mean of `iters` timed calls.
+    cudaEvent_t e0, e1;
+    CUDA_TRY(ctx, cudaEventCreate(&e0));
+    CUDA_TRY(ctx, cudaEventCreate(&e1));
+    auto call = [&]() -> int {
+        switch (kind) {
+        case kKindShrink: return LORA_E_UNSUPPORTED;
+        case kKindExpand: return LORA_E_UNSUPPORTED;
+        case kKindMerge: return lora_merge(ctx, t, ids[0], y, ldy, d_in, d_out, stream);
+        default: return lora_fused(ctx, t, ids, n, x, ldx, d_in, y, ldy, d_out, stream);
+        }
+    };
+    auto time_it = [&](float &us) -> int {
+        for (int w = 0; w < 2; ++w) {
+            int r2 = call();
+            if (r2 != LORA_OK)
+                return r2;
+        }
+        if (cudaEventRecord(e0, stream) != cudaSuccess)
+            return LORA_E_CUDA;
+        for (int i = 0; i < iters; ++i) {
+            int r2 = call();
+            if (r2 != LORA_OK)
+                return r2;
+        }
+        if (cudaEventRecord(e1, stream) != cudaSuccess || cudaEventSynchronize(e1) != cudaSuccess)
+            return LORA_E_CUDA;
+        float ms = 0.f;
+        cudaEventElapsedTime(&ms, e0, e1);
+        us = 1000.f * ms / float(iters);
+        return LORA_OK;
+    };
+    // The key of the shape, as the runtime will look it up.
+    rc = prepare(ctx, t, ids, n);
+    if (rc != LORA_OK) {
+        cudaEventDestroy(e0);
+        cudaEventDestroy(e1);
+        return rc;
+    }
+    int32_t rmax = 8;
+    for (int32_t k : ctx->plan.seg_adapter)
+        rmax = std::max(rmax, t->rank[size_t(k)]);
+    if (kind == kKindMerge)
+        rmax = t->rank[size_t(ids[0])];
+    const int64_t n_act = int64_t(ctx->plan.active.size());
+    const TileKey key{kind, kind == kKindMerge ? pow2_bucket(d_in) : pow2_bucket(n_act),
+                      d_in, d_out, rmax};
+    float best = -1.f;
+    TileCfg best_cfg{0, 0, 0, 0};
+    const int saved_tile = ctx->tile_path, saved_merge = ctx->merge_path,
+              saved_run = ctx->tile_min_run_override;
+    if (kind == kKindRowsFused) {
+        // Pruned space (VaLoRA blog 4.3.2: hardware limits and dimensions that are
+        // multiples of the tile): power-of-two cluster widths whose slices are at
+        // least 64 elements and fit shared memory, rows per item up to the longest
+        // segment.
+        ctx->tile_path = 0;
+        const int seg_max = ctx->plan.max_seg_len;
+        for (int C = 1; C <= rows_max_cluster(); C *= 2) {
+            if (C > 1 && std::min(d_in, d_out) / C < 64)
+                break;
+            for (int R = 1; R <= 16; R *= 2) {
+                if (R > 1 && R / 2 >= seg_max)
+                    break;
+                if (rows_smem_for(kFused, C, R, rmax, d_in, d_out) > size_t(rows_max_smem()))
+                    continue;
+                ctx->force_cluster = C;
+                ctx->force_rows = R;
+                float us = 0.f;
+                if (time_it(us) == LORA_OK && (best < 0.f || us < best)) {
+                    best = us;
+                    best_cfg = TileCfg{C, R, 0, 0};
+                }
+            }
+        }
+        ctx->force_cluster = ctx->force_rows = 0;
+    } else if (kind == kKindTileFused) {
+        const int runs[] = {32, 64, 128, 256, 512, 1 << 30};
+        for (int m : runs) {
+            ctx->tile_min_run_override = m;
+            float us = 0.f;
+            if (time_it(us) == LORA_OK && (best < 0.f || us < best)) {
+                best = us;
+                best_cfg = TileCfg{m, 0, 0, 0};
+            }
+        }
+    } else if (kind == kKindMerge) {
+        for (int path = 0; path <= 1; ++path) {
+            ctx->merge_path = path;
+            float us = 0.f;
+            if (time_it(us) == LORA_OK && (best < 0.f || us < best)) {
+                best = us;
+                best_cfg = TileCfg{path, 0, 0, 0};
+            }
+        }
+    } else {
+        rc = LORA_E_UNSUPPORTED;
+    }
+    ctx->tile_path = saved_tile;
+    ctx->merge_path = saved_merge;
+    ctx->tile_min_run_override = saved_run;
+    cudaEventDestroy(e0);
+    cudaEventDestroy(e1);
+    if (rc != LORA_OK)
+        return rc;
+    if (best < 0.f)
+        return LORA_E_UNSUPPORTED;
+    ctx->tiles.put(key, best_cfg);
+    *best_us = best;
+    return LORA_OK;
 }
 
 }  // extern "C"

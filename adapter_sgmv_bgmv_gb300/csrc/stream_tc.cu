@@ -36,7 +36,7 @@ namespace {
 
 constexpr int kTM = 128;
 constexpr int kBN = 128;
-constexpr int kThreads = 128;
+constexpr int kThreads = 192;
 constexpr uint32_t kBox = kTM * 128;          // one 64-column TMA box of 128 rows
 constexpr uint32_t kTile = 2 * kBox;          // 128 x 128 bf16
 
@@ -67,9 +67,19 @@ __host__ __device__ inline uint32_t stage_bytes(int rp) { return uint32_t(rp) * 
 
 __host__ __device__ inline uint32_t stream_smem_bytes(int left, int rp, int stages)
 {
-    return 1024u + left_bytes(left, rp) + uint32_t(stages) * stage_bytes(rp) + 128u;
+    return 1024u + left_bytes(left, rp) + uint32_t(stages) * stage_bytes(rp) + 128u;   // + barriers
 }
 
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Warp roles: warp 0 producer (B chunks by cp.async, y / W tiles by TMA) running up
+// to NS chunks ahead; warp 1 MMA issuer (two TMEM accumulators, so the MMAs of
+// chunk i + 1 overlap the epilogue of chunk i); warps 2-5 stage the left operand,
+// then run the epilogue and the stores, releasing a stage once its store has read
+// shared memory.
 __global__ void __launch_bounds__(kThreads) k_stream_tc(const __grid_constant__ StreamArgs a)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -116,133 +126,87 @@ __global__ void __launch_bounds__(kThreads) k_stream_tc(const __grid_constant__ 
     const uint32_t sL = base;
     const uint32_t sStage0 = sL + left_bytes(a.left, rp);
     const uint32_t sBar = sStage0 + uint32_t(NS) * stage_bytes(rp);
-    const uint32_t bar_left = sBar, bar_mma = sBar + 8, bar_y0 = sBar + 16;   // + 8 per stage (<= 4)
-    const uint32_t tmem_slot = sBar + 64;
+    // barriers: left, full[4], empty[4], tfull[2], tempty[2]
+    const uint32_t bar_left = sBar;
+    const uint32_t full0 = sBar + 8, empty0 = sBar + 40;
+    const uint32_t tfull0 = sBar + 72, tempty0 = sBar + 88;
+    const uint32_t tmem_slot = sBar + 104;
     const uint32_t lbo_b = uint32_t(rp / 8) * 1024u;   // N-atom stride of B (and M-atom of A)
     auto stage_b = [&](int c) { return sStage0 + uint32_t(c % NS) * stage_bytes(rp); };
     auto stage_t = [&](int c) { return stage_b(c) + uint32_t(rp) * kBN * 2u; };
+    const bool full_rows = (a.left == kLeftAPages) || nrows == kTM;
 
     if (tid == 0) {
         mbar_init(bar_left, 1);
-        mbar_init(bar_mma, 1);
-        for (int s = 0; s < NS; ++s)
-            mbar_init(bar_y0 + 8 * s, 1);
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(full0 + 8 * s, 2);       // producer lane 0 (B done) + TMA tx
+            mbar_init(empty0 + 8 * s, 1);      // epilogue store has read the stage
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(tfull0 + 8 * b, 1);      // MMA commit
+            mbar_init(tempty0 + 8 * b, 4);     // one arrive per epilogue warp
+        }
         fence_mbar_init();
     }
-    if (warp == 0)
-        tc::tmem_alloc(tmem_slot, kBN);
+    if (warp == 1)
+        tc::tmem_alloc(tmem_slot, 2 * kBN);
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = *reinterpret_cast<const uint32_t *>(gbase + (tmem_slot - base));
-
-    // ---- left operand (once)
     const int atoms = v_atoms(rp);
-    if (a.left != kLeftAPages) {
-        const int row = tid;
-        const int KS = a.left == kLeftVParts ? a.p.ksplit : 1;
-        for (int c = 0; c < rp / 8; ++c) {
-            float f[8], back[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-                f[e] = 0.f;
-            if (a.left == kLeftVParts) {
-                for (int ks = 0; ks < KS; ++ks) {
-                    const float *src = a.p.vparts + (size_t(blk) * KS + ks) * (kVPartBytes / 4) +
-                                       size_t(row) * rp + 8 * c;
-                    const float4 lo4 = *reinterpret_cast<const float4 *>(src);
-                    const float4 hi4 = *reinterpret_cast<const float4 *>(src + 4);
-                    f[0] += lo4.x; f[1] += lo4.y; f[2] += lo4.z; f[3] += lo4.w;
-                    f[4] += hi4.x; f[5] += hi4.y; f[6] += hi4.z; f[7] += hi4.w;
-                }
-            } else {
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const int j = 8 * c + e;
-                    f[e] = (row < nrows && j < r) ? a.p.v[int64_t(row0 + row) * a.p.ldv + j] : 0.f;
-                }
-            }
-            const uint4 hv = pack8(f);
-            unpack8(hv, back);
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-                f[e] -= back[e];
-            const uint32_t off = tc::sw128(uint32_t(row), uint32_t(c & 7));
-            *reinterpret_cast<uint4 *>(gbase + (sL - base) + (c >> 3) * kBox + off) = hv;
-            *reinterpret_cast<uint4 *>(gbase + (sL - base) + (atoms + (c >> 3)) * kBox + off) =
-                pack8(f);
-        }
-        if (tid == 0)
-            mbar_arrive(bar_left);
-    } else {
-        // A_k rows c0..c0+127, column j = page j: M-major, 64-row atoms.
-        for (int q = tid; q < rp * 16; q += kThreads) {
-            const int j = q >> 4, c16 = q & 15;
-            const int c = row0 + 8 * c16;
-            const bool valid = j < r && c + 8 <= a.m.d_in;
-            const uint32_t off = uint32_t(c16 >> 3) * lbo_b + uint32_t(j >> 3) * 1024u +
-                                 tc::sw128(uint32_t(j & 7), uint32_t(c16 & 7));
-            tc::cp_async16(sL + off,
-                           valid ? a.m.a_pool + int64_t(a.m.a_pages[j]) * a.m.a_pw + c : a.m.a_pool,
-                           valid ? 16u : 0u);
-        }
-        tc::cp_async_commit();   // waited together with the first B block
-        if (tid == 0)
-            mbar_arrive(bar_left);
-    }
-
-    // ---- prefetch of chunk c into its stage: B by every thread, the tile by TMA
-    auto prefetch = [&](int c) {
-        const int n0 = (ch0 + c) * kBN;
-        const uint32_t sb = stage_b(c);
-        for (int q = tid; q < rp * 16; q += kThreads) {
-            const int j = q >> 4, c16 = q & 15;
-            const int col = n0 + 8 * c16;
-            const bool valid = j < r && col + 8 <= d_out;
-            const uint32_t off = uint32_t(c16 >> 3) * lbo_b + uint32_t(j >> 3) * 1024u +
-                                 tc::sw128(uint32_t(j & 7), uint32_t(c16 & 7));
-            tc::cp_async16(sb + off, valid ? b_pool + int64_t(b_pages[j]) * b_pw + col : b_pool,
-                           valid ? 16u : 0u);
-        }
-        tc::cp_async_commit();
-        if (tid == 0) {
-            tc::bulk_wait_read0();   // the store that last used this stage has read it
-            const uint32_t bar = bar_y0 + 8u * uint32_t(c % NS);
-            mbar_arrive_expect_tx(bar, kTile);
-            tc::tma_load_2d(stage_t(c), &a.map, n0, row0, bar);
-            tc::tma_load_2d(stage_t(c) + kBox, &a.map, n0 + 64, row0, bar);
-        }
-    };
-
-    for (int c = 0; c < NS - 1 && c < nch; ++c)
-        prefetch(c);
-
     bool ok = true;
-    const bool full_rows = (a.left == kLeftAPages) || nrows == kTM;
-    const uint32_t idesc = tc::idesc_bf16(kTM, kBN, a.left == kLeftAPages ? 1 : 0, 1);
-#pragma unroll 1
-    for (int i = 0; i < nch; ++i) {
-        // B of chunk i (and the left operand on the first pass) is in shared memory
-        {
-            const int allow = min(NS - 2, nch - 1 - i);   // newer B groups already issued
-            if (allow >= 2)
-                tc::cp_async_wait<2>();
-            else if (allow == 1)
-                tc::cp_async_wait<1>();
-            else
-                tc::cp_async_wait<0>();
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        for (int i = 0; i < nch; ++i) {
+            const int s = i % NS, u = i / NS;
+            if (u > 0)
+                ok = mbar_wait_bounded(empty0 + 8 * s, uint32_t((u - 1) & 1), status,
+                                       kDevTimeoutPipe) && ok;
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok)
+                break;
+            const int n0 = (ch0 + i) * kBN;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(full0 + 8 * s, kTile);
+                tc::tma_load_2d(stage_t(i), &a.map, n0, row0, full0 + 8 * s);
+                tc::tma_load_2d(stage_t(i) + kBox, &a.map, n0 + 64, row0, full0 + 8 * s);
+            }
+            const uint32_t sb = stage_b(i);
+            for (int q = lane; q < rp * 16; q += 32) {
+                const int j = q >> 4, c16 = q & 15;
+                const int col = n0 + 8 * c16;
+                const bool valid = j < r && col + 8 <= d_out;
+                const uint32_t off = uint32_t(c16 >> 3) * lbo_b + uint32_t(j >> 3) * 1024u +
+                                     tc::sw128(uint32_t(j & 7), uint32_t(c16 & 7));
+                tc::cp_async16(sb + off, valid ? b_pool + int64_t(b_pages[j]) * b_pw + col : b_pool,
+                               valid ? 16u : 0u);
+            }
+            tc::cp_async_commit();
+            tc::cp_async_wait<0>();
+            tc::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(full0 + 8 * s);
         }
-        tc::fence_proxy_async_smem();
-        tc::fence_before_sync();
-        __syncthreads();
-        tc::fence_after_sync();
-        if (tid == 0) {
-            bool go = ok;
-            if (i == 0)
-                go = mbar_wait_bounded(bar_left, 0, status, kDevTimeoutLoad) && go;
-            if (go) {
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            ok = mbar_wait_bounded(bar_left, 0, status, kDevTimeoutLoad);
+            const uint32_t idesc = tc::idesc_bf16(kTM, kBN, a.left == kLeftAPages ? 1 : 0, 1);
+            const int parts = a.left == kLeftAPages ? 1 : 2;
+            for (int i = 0; i < nch && ok; ++i) {
+                const int s = i % NS, b = i & 1;
+                ok = mbar_wait_bounded(full0 + 8 * s, uint32_t((i / NS) & 1), status, kDevTimeoutLoad);
+                if (ok && i >= 2)
+                    ok = mbar_wait_bounded(tempty0 + 8 * b, uint32_t(((i >> 1) - 1) & 1), status,
+                                           kDevTimeoutPipe);
+                if (!ok)
+                    break;
+                tc::fence_after_sync();
                 const uint32_t sb = stage_b(i);
-                const int parts = a.left == kLeftAPages ? 1 : 2;
+                const uint32_t d = tmem + uint32_t(b * kBN);
                 for (int part = 0; part < parts; ++part) {
                     for (int kk = 0; kk < rp / 16; ++kk) {
                         uint64_t dl;
@@ -253,27 +217,87 @@ __global__ void __launch_bounds__(kThreads) k_stream_tc(const __grid_constant__ 
                                                          uint32_t(kk & 3) * 32u,
                                                      16u, 1024u);
                         const uint64_t db = tc::smem_desc_sw128(sb + uint32_t(kk) * 2048u, lbo_b, 1024u);
-                        tc::mma_bf16(tmem, dl, db, idesc, (part > 0 || kk > 0) ? 1u : 0u);
+                        tc::mma_bf16(d, dl, db, idesc, (part > 0 || kk > 0) ? 1u : 0u);
                     }
                 }
+                tc::mma_commit(tfull0 + 8 * b);
             }
-            tc::mma_commit(bar_mma);
-            ok = go;
         }
-        if (i + NS - 1 < nch)
-            prefetch(i + NS - 1);
-        ok = mbar_wait_bounded(bar_mma, uint32_t(i & 1), status, kDevTimeoutMma) && ok;
-        tc::fence_after_sync();
-        ok = mbar_wait_bounded(bar_y0 + 8u * uint32_t(i % NS), uint32_t((i / NS) & 1), status,
-                               kDevTimeoutLoad) && ok;
-        ok = __syncthreads_and(ok);
-        const uint32_t st = stage_t(i);
-        if (ok) {
-            const int row = warp * 32 + lane;
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ left operand
+        const int et = tid - 64;                 // 0..127
+        if (a.left != kLeftAPages) {
+            const int row = et;
+            const int KS = a.left == kLeftVParts ? a.p.ksplit : 1;
+            for (int c = 0; c < rp / 8; ++c) {
+                float f[8], back[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    f[e] = 0.f;
+                if (a.left == kLeftVParts) {
+                    for (int ks = 0; ks < KS; ++ks) {
+                        const float *src = a.p.vparts + (size_t(blk) * KS + ks) * (kVPartBytes / 4) +
+                                           size_t(row) * rp + 8 * c;
+                        const float4 lo4 = *reinterpret_cast<const float4 *>(src);
+                        const float4 hi4 = *reinterpret_cast<const float4 *>(src + 4);
+                        f[0] += lo4.x; f[1] += lo4.y; f[2] += lo4.z; f[3] += lo4.w;
+                        f[4] += hi4.x; f[5] += hi4.y; f[6] += hi4.z; f[7] += hi4.w;
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const int j = 8 * c + e;
+                        f[e] = (row < nrows && j < r) ? a.p.v[int64_t(row0 + row) * a.p.ldv + j] : 0.f;
+                    }
+                }
+                const uint4 hv = pack8(f);
+                unpack8(hv, back);
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    f[e] -= back[e];
+                const uint32_t off = tc::sw128(uint32_t(row), uint32_t(c & 7));
+                *reinterpret_cast<uint4 *>(gbase + (sL - base) + (c >> 3) * kBox + off) = hv;
+                *reinterpret_cast<uint4 *>(gbase + (sL - base) + (atoms + (c >> 3)) * kBox + off) =
+                    pack8(f);
+            }
+            tc::fence_proxy_async_smem();
+        } else {
+            // A_k rows row0..row0+127, column j = page j: M-major, 64-row atoms.
+            for (int q = et; q < rp * 16; q += 128) {
+                const int j = q >> 4, c16 = q & 15;
+                const int c = row0 + 8 * c16;
+                const bool valid = j < r && c + 8 <= a.m.d_in;
+                const uint32_t off = uint32_t(c16 >> 3) * lbo_b + uint32_t(j >> 3) * 1024u +
+                                     tc::sw128(uint32_t(j & 7), uint32_t(c16 & 7));
+                tc::cp_async16(sL + off,
+                               valid ? a.m.a_pool + int64_t(a.m.a_pages[j]) * a.m.a_pw + c : a.m.a_pool,
+                               valid ? 16u : 0u);
+            }
+            tc::cp_async_commit();
+            tc::cp_async_wait<0>();
+            tc::fence_proxy_async_smem();
+        }
+        named_bar_sync(1, 128);
+        if (et == 0)
+            mbar_arrive(bar_left);
+
+        // ------------------------------------------------------------ epilogue
+        const int q4 = warp & 3;                  // TMEM lanes 32*q4 .. 32*q4+31
+        const int row = 32 * q4 + lane;
+        for (int i = 0; i < nch; ++i) {
+            const int s = i % NS, b = i & 1;
+            ok = mbar_wait_bounded(tfull0 + 8 * b, uint32_t((i >> 1) & 1), status, kDevTimeoutMma) && ok;
+            ok = mbar_wait_bounded(full0 + 8 * s, uint32_t((i / NS) & 1), status, kDevTimeoutLoad) && ok;
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok)
+                break;
+            tc::fence_after_sync();
+            const uint32_t st = stage_t(i);
 #pragma unroll 1
             for (int cc = 0; cc < kBN / 32; ++cc) {
                 float acc[32];
-                tc::tmem_ld32(tmem + (uint32_t(warp * 32) << 16) + uint32_t(cc * 32), acc);
+                tc::tmem_ld32(tmem + (uint32_t(32 * q4) << 16) + uint32_t(b * kBN + cc * 32), acc);
                 uint8_t *box = gbase + (st - base) + (cc >> 1) * kBox;
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
@@ -287,48 +311,49 @@ __global__ void __launch_bounds__(kThreads) k_stream_tc(const __grid_constant__ 
                     *ptr = pack8(t);
                 }
             }
-        }
-        tc::fence_proxy_async_smem();
-        tc::fence_before_sync();
-        __syncthreads();
-        if (!ok)
-            break;
-        const int n0 = (ch0 + i) * kBN;
-        if (full_rows) {
-            if (tid == 0) {
-                tc::tma_store_2d(&a.map, n0, row0, st);
-                if (n0 + 64 < d_out)   // a box wholly right of the matrix is not stored
-                    tc::tma_store_2d(&a.map, n0 + 64, row0, st + kBox);
-                tc::bulk_commit();
-            }
-        } else {
-            const int c16 = lane & 15;
-            const int col = n0 + 8 * c16;
-            for (int rr = warp * 2 + (lane >> 4); rr < nrows; rr += 8) {
-                if (col + 8 <= d_out) {
-                    const uint4 val = *reinterpret_cast<const uint4 *>(
-                        gbase + (st - base) + (c16 >> 3) * kBox +
-                        tc::sw128(uint32_t(rr), uint32_t(c16 & 7)));
-                    *reinterpret_cast<uint4 *>(a.p.y + int64_t(row0 + rr) * a.p.ldy + col) = val;
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(tempty0 + 8 * b);      // this warp is done with accumulator b
+            tc::fence_proxy_async_smem();
+            named_bar_sync(1, 128);
+            const int n0 = (ch0 + i) * kBN;
+            if (full_rows) {
+                if (et == 0) {
+                    tc::tma_store_2d(&a.map, n0, row0, st);
+                    if (n0 + 64 < d_out)   // a box wholly right of the matrix is not stored
+                        tc::tma_store_2d(&a.map, n0 + 64, row0, st + kBox);
+                    tc::bulk_commit();
+                    // release the previous chunk's stage once its store has read it
+                    tc::bulk_wait_read1();
+                    if (i > 0)
+                        mbar_arrive(empty0 + 8 * ((i - 1) % NS));
                 }
+            } else {
+                const int c16 = lane & 15;
+                const int col = n0 + 8 * c16;
+                for (int rr = (warp - 2) * 2 + (lane >> 4); rr < nrows; rr += 8) {
+                    if (col + 8 <= d_out) {
+                        const uint4 val = *reinterpret_cast<const uint4 *>(
+                            gbase + (st - base) + (c16 >> 3) * kBox +
+                            tc::sw128(uint32_t(rr), uint32_t(c16 & 7)));
+                        *reinterpret_cast<uint4 *>(a.p.y + int64_t(row0 + rr) * a.p.ldy + col) = val;
+                    }
+                }
+                named_bar_sync(1, 128);
+                if (et == 0)
+                    mbar_arrive(empty0 + 8 * s);
             }
         }
-    }
-    if (tid == 0)
-        tc::bulk_wait0();
-    tc::cp_async_wait<0>();
-    if (!ok) {
-        // leave nothing running on this CTA's shared memory or TMEM
-        mbar_wait_bounded(bar_mma, 0, nullptr, 0, 1000000ull);
-        for (int s = 0; s < NS; ++s)
-            mbar_wait_bounded(bar_y0 + 8 * s, 0, nullptr, 0, 1000000ull);
+        if (et == 0)
+            tc::bulk_wait0();
     }
     tc::fence_before_sync();
     __syncthreads();
-    if (warp == 0) {
+    if (warp == 1) {
         __syncwarp();
         tc::fence_after_sync();
-        tc::tmem_dealloc(tmem, kBN);
+        tc::tmem_dealloc(tmem, 2 * kBN);
     }
 }
 

@@ -178,6 +178,12 @@ __device__ __forceinline__ void bulk_wait_read0()
 
 __device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
+// All but the most recent bulk group have finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read1()
+{
+    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+
 // Byte offset of 16-byte chunk `chunk` (0..7) of row `row` inside a 1024-byte,
 // 1024-aligned 128-byte-swizzle atom of 8 rows x 128 bytes.
 __host__ __device__ constexpr uint32_t sw128(uint32_t row, uint32_t chunk)

@@ -157,11 +157,16 @@ int lora_tiles_load(lora_ctx *ctx, const char *path);
 int lora_tiles_save(const lora_ctx *ctx, const char *path);
 int64_t lora_tiles_count(const lora_ctx *ctx);
 
-/* Offline search for one shape: times every pruned candidate configuration of
- * `kind` on caller-provided buffers (same meaning as for the matching call; for
- * kind 4, `x` is W and `ids_host` names the adapter in its first entry), keeps the
- * fastest in the context's table and returns its time in *best_us.  Writes y / W
- * (results are the call's result applied several times). */
+/* Offline search for one shape (VaLoRA blog, section 4.3.2): times every
+ * candidate of a pruned configuration space with CUDA events (two warm-up calls,
+ * then the mean of `iters` calls), keeps the fastest in the context's table under
+ * the key the runtime looks up, and returns its time in *best_us.
+ *   kind 0 (row-gather fused): cluster width x rows per item;
+ *   kind 3 (tile fused):       minimum run length routed to the tensor-core tiles;
+ *   kind 4 (merge):            tensor-core or CUDA-core kernel; `y` is W
+ *                              [d_in, ldy], ids_host[0] names the adapter, x unused.
+ * Kinds 1 and 2 return LORA_E_UNSUPPORTED.  The buffers are updated by every
+ * timed call (y receives the delta 2 + iters times per candidate). */
 int lora_tune_shape(lora_ctx *ctx, const lora_table *table, int kind,
                     const int32_t *ids_host, int64_t n, const void *x, int64_t ldx,
                     int d_in, void *y, int64_t ldy, int d_out, int iters,
