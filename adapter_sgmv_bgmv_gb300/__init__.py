@@ -18,7 +18,7 @@ import torch
 from . import _lib
 
 __all__ = ["LoraError", "Context", "AdapterTable", "lora_plan_build", "lora_shrink",
-           "lora_expand", "lora_fused", "lora_merge", "lora_unmerge", "lora_tune_shape",
+           "lora_expand", "lora_fused", "PreparedFused", "lora_merge", "lora_unmerge", "lora_tune_shape",
            "KIND_ROWS_FUSED", "KIND_SHRINK", "KIND_EXPAND", "KIND_TILE_FUSED", "KIND_MERGE",
            "OPT_TILE_PATH", "OPT_MERGE_KERNEL", "OPT_TILE_MIN_RUN",
            "library_path"]
@@ -143,16 +143,22 @@ class Context:
         OPT_TILE_MIN_RUN."""
         _check(_L.lora_ctx_set_option(self.handle, int(option), int(value)), self)
 
-    def profile_begin(self):
-        """Start bracketing every kernel launch with CUDA events."""
-        _check(_L.lora_profile_begin(self.handle), self)
+    def profile_begin(self, every: int = 1):
+        """Start bracketing every `every`-th kernel launch with CUDA events."""
+        _check(_L.lora_profile_begin(self.handle, int(every)), self)
 
     def profile_end(self):
-        """Stop; returns {family: (device ms, launches)} for row / tile / merge kernels."""
-        ms = (ctypes.c_double * 3)()
-        n = (ctypes.c_int64 * 3)()
+        """Stop; returns {family: (device ms, launches)} for the row-gather, tile shrink,
+        merge and streaming expand kernels."""
+        ms = (ctypes.c_double * 4)()
+        n = (ctypes.c_int64 * 4)()
         _check(_L.lora_profile_end(self.handle, ms, n), self)
-        return {name: (ms[i], int(n[i])) for i, name in enumerate(("rows", "tile", "merge"))}
+        return {name: (ms[i], int(n[i]))
+                for i, name in enumerate(("rows", "shrink", "merge", "expand"))}
+
+    def launch_count(self) -> int:
+        """Kernels launched by this context so far."""
+        return int(_L.lora_launch_count(self.handle))
 
     def last_path(self):
         """(path bits, launches) of the last call: 1 row-gather, 2 tensor-core tile,
@@ -255,6 +261,28 @@ def lora_fused(ctx: Context, table: AdapterTable, ids, x: torch.Tensor, y: torch
                        _stream(stream, ctx.device))
     if rc:
         _check(rc, ctx)
+
+
+class PreparedFused:
+    """lora_fused with fixed x, y, table and stream (a decode loop's persistent
+    buffers): the pointer / stride / stream marshalling happens once, each call only
+    converts the ids and makes the C call."""
+
+    def __init__(self, ctx: Context, table: AdapterTable, x: torch.Tensor, y: torch.Tensor,
+                 stream=None):
+        px, ldx, d_in = _rows(x, "x")
+        py, ldy, d_out = _rows(y, "y")
+        self._keep = (ctx, table, x, y)
+        self._ctx = ctx
+        self._fn = _L.lora_fused
+        self._head = (ctx.handle, table.handle)
+        self._tail = (px, ldx, d_in, py, ldy, d_out, _stream(stream, ctx.device))
+
+    def __call__(self, ids):
+        ids, pid, n = _ids(ids)
+        rc = self._fn(*self._head, pid, n, *self._tail)
+        if rc:
+            _check(rc, self._ctx)
 
 
 def lora_merge(ctx: Context, table: AdapterTable, adapter: int, W: torch.Tensor, stream=None):

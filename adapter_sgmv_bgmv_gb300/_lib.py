@@ -42,7 +42,8 @@ SIGNATURES = {
     "lora_tune_shape": ([P, P, I, P, I64, P, I64, I, P, I64, I, I, ctypes.POINTER(F), P], I),
     "lora_sync_status": ([P, P], I),
     "lora_last_path": ([P, ctypes.POINTER(I)], I),
-    "lora_profile_begin": ([P], I),
+    "lora_launch_count": ([P], I64),
+    "lora_profile_begin": ([P, I], I),
     "lora_ctx_set_option": ([P, I, I], I),
     "lora_profile_end": ([P, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(I64)], I),
 }

@@ -63,6 +63,10 @@ struct lora_ctx {
     std::vector<ProfEv> prof_ev;
     size_t prof_used = 0;
     RowsParamsInline inline_args;   // staging of in-parameter plans
+    RowsParamsInlineSmall inline_small;
+    int64_t launches_total = 0;     // every kernel launched by this context
+    int prof_every = 1;             // bracket one launch in this many
+    int64_t prof_seen = 0;
     int merge_path = 0;             // 0 auto (tensor cores when supported), 1 CUDA cores
     int tile_path = 1;              // 1: long same-adapter runs use the tensor-core tiles
     int tile_min_run_override = 0;  // > 0: fixed minimum run for the tile path
@@ -157,6 +161,8 @@ int release_slot(lora_ctx *ctx, Slot *s, cudaStream_t stream)
 long prof_start(lora_ctx *ctx, int family, cudaStream_t stream)
 {
     if (!ctx->prof)
+        return -1;
+    if ((ctx->prof_seen++ % ctx->prof_every) != 0)
         return -1;
     if (ctx->prof_used == ctx->prof_ev.size()) {
         lora_ctx::ProfEv e;
@@ -302,16 +308,16 @@ int run_rows(lora_ctx *ctx, const lora_table *t, int mode, RowsCfg cfg, const vo
         return rc;
 
     const size_t items_bytes = pl.row_items.size() * sizeof(RowItem);
-    const size_t perm_bytes = pl.perm.size() * sizeof(int32_t);
+    const size_t perm_bytes = pl.row_perm.size() * sizeof(int32_t);
     const bool in_params = pl.row_items.size() <= size_t(kInlineItems) &&
-                           pl.perm.size() <= size_t(kInlinePerm);
+                           pl.row_perm.size() <= size_t(kInlinePerm);
     Slot *slot = nullptr;
     if (!in_params) {
         rc = acquire_slot(ctx, items_bytes + perm_bytes + 16, &slot);
         if (rc != LORA_OK)
             return rc;
         std::memcpy(slot->host, pl.row_items.data(), items_bytes);
-        std::memcpy(slot->host + items_bytes, pl.perm.data(), perm_bytes);
+        std::memcpy(slot->host + items_bytes, pl.row_perm.data(), perm_bytes);
         CUDA_TRY(ctx, cudaMemcpyAsync(slot->dev, slot->host, items_bytes + perm_bytes,
                                       cudaMemcpyHostToDevice, stream));
     }
@@ -338,11 +344,17 @@ int run_rows(lora_ctx *ctx, const lora_table *t, int mode, RowsCfg cfg, const vo
     p.d_out = d_out;
     p.n_items = int(pl.row_items.size());
     const long ev = prof_start(ctx, 0, stream);
-    if (in_params) {
+    if (in_params && pl.row_items.size() <= 64 && pl.row_perm.size() <= 128) {
+        RowsParamsInlineSmall &a = ctx->inline_small;
+        a.p = p;
+        std::memcpy(a.items, pl.row_items.data(), items_bytes);
+        std::memcpy(a.perm, pl.row_perm.data(), perm_bytes);
+        CUDA_TRY(ctx, launch_rows_inline_small(mode, a, smem, stream));
+    } else if (in_params) {
         RowsParamsInline &a = ctx->inline_args;
         a.p = p;
         std::memcpy(a.items, pl.row_items.data(), items_bytes);
-        std::memcpy(a.perm, pl.perm.data(), perm_bytes);
+        std::memcpy(a.perm, pl.row_perm.data(), perm_bytes);
         CUDA_TRY(ctx, launch_rows_inline(mode, a, smem, stream));
     } else {
         CUDA_TRY(ctx, launch_rows(mode, p, smem, stream));
@@ -350,6 +362,7 @@ int run_rows(lora_ctx *ctx, const lora_table *t, int mode, RowsCfg cfg, const vo
     prof_stop(ctx, ev, stream);
     ctx->last_path |= 1;
     ctx->last_launches += 1;
+        ctx->launches_total += 1;
     return slot ? release_slot(ctx, slot, stream) : LORA_OK;
 }
 
@@ -374,11 +387,15 @@ int run_tiles(lora_ctx *ctx, const lora_table *t, int mode, const void *x, int64
         return LORA_OK;
     const size_t items_bytes = pl.tile_items.size() * sizeof(TileItem);
     Slot *slot = nullptr;
-    int rc = acquire_slot(ctx, items_bytes + 16, &slot);
+    int rc = LORA_OK;
+    const TileItem *d_items = nullptr;
+    rc = acquire_slot(ctx, items_bytes + 16, &slot);
     if (rc != LORA_OK)
         return rc;
     std::memcpy(slot->host, pl.tile_items.data(), items_bytes);
-    CUDA_TRY(ctx, cudaMemcpyAsync(slot->dev, slot->host, items_bytes, cudaMemcpyHostToDevice, stream));
+    CUDA_TRY(ctx, cudaMemcpyAsync(slot->dev, slot->host, items_bytes, cudaMemcpyHostToDevice,
+                                  stream));
+    d_items = reinterpret_cast<const TileItem *>(slot->dev);
     // K-split of the fused shrink: about two CTAs per SM over all tiles, each CTA
     // keeping at least 4 K blocks of 64.
     int ksplit = 1;
@@ -412,7 +429,7 @@ int run_tiles(lora_ctx *ctx, const lora_table *t, int mode, const void *x, int64
     p.b_pw = t->b_pw;
     p.a_pages = t->d_a_pages;
     p.b_pages = t->d_b_pages;
-    p.items = reinterpret_cast<const TileItem *>(slot->dev);
+    p.items = d_items;
     p.vparts = reinterpret_cast<float *>(ctx->vparts);
     p.ksplit = ksplit;
     p.v = v;
@@ -430,15 +447,17 @@ int run_tiles(lora_ctx *ctx, const lora_table *t, int mode, const void *x, int64
         CUDA_TRY(ctx, launch_shrink_tc(p, stream));
         prof_stop(ctx, ev, stream);
         ctx->last_launches += 1;
+        ctx->launches_total += 1;
     }
     if (mode != kShrink) {
-        const long ev = prof_start(ctx, 1, stream);
+        const long ev = prof_start(ctx, 3, stream);
         CUDA_TRY(ctx, launch_expand_tc(p, stream));
         prof_stop(ctx, ev, stream);
         ctx->last_launches += 1;
+        ctx->launches_total += 1;
     }
     ctx->last_path |= 2;
-    return release_slot(ctx, slot, stream);
+    return slot ? release_slot(ctx, slot, stream) : LORA_OK;
 }
 
 int delta_call(lora_ctx *ctx, const lora_table *t, int mode, const int32_t *ids, int64_t n,
@@ -538,6 +557,7 @@ int merge_call(lora_ctx *ctx, const lora_table *t, int adapter, void *W, int64_t
     prof_stop(ctx, ev, stream);
     ctx->last_path = 4;
     ctx->last_launches = 1;
+    ctx->launches_total += 1;
     return LORA_OK;
 }
 
@@ -599,6 +619,15 @@ int lora_ctx_create(int device, int64_t max_rows, int max_rank, lora_ctx **out)
     ctx->device = device;
     ctx->max_rows = max_rows;
     ctx->max_rank = max_rank;
+    // Plans up to max_rows never grow these again.
+    Plan &pl = ctx->plan;
+    pl.active.reserve(size_t(max_rows));
+    pl.perm.reserve(size_t(max_rows));
+    pl.seg_offsets.reserve(size_t(max_rows) + 1);
+    pl.seg_adapter.reserve(size_t(max_rows));
+    pl.row_items.reserve(size_t(max_rows));
+    pl.row_perm.reserve(size_t(max_rows));
+    pl.tile_items.reserve(size_t(max_rows) / 64 + 64);
     int prev = 0;
     cudaGetDevice(&prev);
     if (cudaSetDevice(device) != cudaSuccess ||
@@ -688,6 +717,10 @@ int lora_table_create(lora_ctx *ctx, const void *a_pool, int64_t a_n_pages, int 
     t->a_pages.assign(a_pages_host, a_pages_host + np);
     t->b_pages.assign(b_pages_host, b_pages_host + np);
     t->status.resize(size_t(n_adapters));
+    if (ctx->plan.count.capacity() < size_t(n_adapters)) {
+        ctx->plan.count.reserve(size_t(n_adapters));
+        ctx->plan.cursor.reserve(size_t(n_adapters));
+    }
     for (int k = 0; k < n_adapters; ++k)
         t->status[size_t(k)] = adapter_status(t, k);
     // Device copies; pages of adapters that cannot be used are zeroed so that no
@@ -865,12 +898,14 @@ int lora_ctx_set_option(lora_ctx *ctx, int option, int value)
     }
 }
 
-int lora_profile_begin(lora_ctx *ctx)
+int lora_profile_begin(lora_ctx *ctx, int every)
 {
-    if (!ctx)
+    if (!ctx || every < 1)
         return LORA_E_INVAL;
     ctx->prof = true;
     ctx->prof_used = 0;
+    ctx->prof_every = every;
+    ctx->prof_seen = 0;
     return LORA_OK;
 }
 
@@ -879,7 +914,7 @@ int lora_profile_end(lora_ctx *ctx, double *ms, int64_t *launches)
     if (!ctx || !ms || !launches)
         return LORA_E_INVAL;
     ctx->prof = false;
-    for (int f = 0; f < 3; ++f) {
+    for (int f = 0; f < 4; ++f) {
         ms[f] = 0.0;
         launches[f] = 0;
     }
@@ -894,6 +929,8 @@ int lora_profile_end(lora_ctx *ctx, double *ms, int64_t *launches)
     ctx->prof_used = 0;
     return LORA_OK;
 }
+
+int64_t lora_launch_count(const lora_ctx *ctx) { return ctx ? ctx->launches_total : -1; }
 
 int lora_last_path(const lora_ctx *ctx, int *n_launches)
 {

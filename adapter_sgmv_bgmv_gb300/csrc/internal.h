@@ -60,14 +60,18 @@ struct RowsParams {
     int rank_alloc;           // shared-memory rank slots (>= every item's rank)
 };
 
-// Small plans travel inside the kernel parameter block (no separate upload).
+// Small plans travel inside the kernel parameter block (no separate upload), in
+// one of two sizes so that a decode batch does not ship an oversized block.
 constexpr int kInlineItems = 256;
 constexpr int kInlinePerm = 512;
-struct RowsParamsInline {
+template <int NI, int NP>
+struct RowsParamsInlineT {
     RowsParams p;
-    RowItem items[kInlineItems];
-    int32_t perm[kInlinePerm];
+    RowItem items[NI];
+    int32_t perm[NP];
 };
+using RowsParamsInline = RowsParamsInlineT<kInlineItems, kInlinePerm>;
+using RowsParamsInlineSmall = RowsParamsInlineT<64, 128>;
 
 size_t rows_smem_bytes(int mode, int slice_in, int slice_out, int rows_alloc, int rank_alloc,
                        int cluster);
@@ -75,6 +79,8 @@ int rows_max_cluster();
 cudaError_t launch_rows(int mode, const RowsParams &p, size_t smem, cudaStream_t stream);
 cudaError_t launch_rows_inline(int mode, const RowsParamsInline &a, size_t smem,
                                cudaStream_t stream);
+cudaError_t launch_rows_inline_small(int mode, const RowsParamsInlineSmall &a, size_t smem,
+                                     cudaStream_t stream);
 int rows_max_smem();
 
 // Tensor-core tile kernels (tile_tc.cu, stream_tc.cu).  In the fused call the shrink

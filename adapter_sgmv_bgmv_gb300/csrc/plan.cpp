@@ -51,6 +51,7 @@ void plan_items(Plan &pl, const int32_t *rank, const float *scale, int rows_per_
                 int tile_min_run)
 {
     pl.row_items.clear();
+    pl.row_perm.clear();
     pl.tile_items.clear();
     pl.max_rank = pl.tile_max_rank = pl.row_max_rank = pl.row_max_rows = 0;
     pl.row_active = pl.tile_active = 0;
@@ -65,7 +66,10 @@ void plan_items(Plan &pl, const int32_t *rank, const float *scale, int rows_per_
         auto flush_rows = [&](int32_t from, int32_t to) {
             for (int32_t p = from; p < to; p += rows_per_item) {
                 const int32_t m = std::min(rows_per_item, to - p);
-                pl.row_items.push_back(RowItem{k, p, int16_t(m), int16_t(r), scale[k]});
+                const int32_t q0 = int32_t(pl.row_perm.size());
+                for (int32_t u = 0; u < m; ++u)
+                    pl.row_perm.push_back(pl.perm[size_t(p + u)]);
+                pl.row_items.push_back(RowItem{k, q0, int16_t(m), int16_t(r), scale[k]});
                 pl.row_max_rows = std::max(pl.row_max_rows, m);
                 pl.row_active += m;
             }

@@ -13,7 +13,8 @@ struct Plan {
     std::vector<int32_t> perm;         // active rows stably sorted by adapter id
     std::vector<int32_t> seg_offsets;  // [n_seg + 1]
     std::vector<int32_t> seg_adapter;  // [n_seg]
-    std::vector<RowItem> row_items;
+    std::vector<RowItem> row_items;    // p0 indexes row_perm
+    std::vector<int32_t> row_perm;     // the perm entries of the row items only
     std::vector<TileItem> tile_items;
     std::vector<int32_t> count;        // scratch, [n_adapters]
     std::vector<int32_t> cursor;       // scratch, [n_adapters]

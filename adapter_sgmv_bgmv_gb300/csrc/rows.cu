@@ -309,8 +309,8 @@ __global__ void __launch_bounds__(kThreads) k_rows(const __grid_constant__ RowsP
 }
 
 // Same kernel with the plan (items and permutation) in the parameter block.
-template <int MODE>
-__global__ void __launch_bounds__(kThreads) k_rows_inline(const __grid_constant__ RowsParamsInline a)
+template <int MODE, typename Inline>
+__global__ void __launch_bounds__(kThreads) k_rows_inline(const __grid_constant__ Inline a)
 {
     rows_body<MODE>(a.p, a.items, a.perm);
 }
@@ -330,7 +330,11 @@ cudaError_t launch_mode(const RowsParams &p, const Arg &arg, size_t smem, cudaSt
 {
     static bool configured = false;
     if (!configured) {
-        cudaError_t e = INLINE ? configure(k_rows_inline<MODE>) : configure(k_rows<MODE>);
+        cudaError_t e;
+        if constexpr (INLINE)
+            e = configure(k_rows_inline<MODE, Arg>);
+        else
+            e = configure(k_rows<MODE>);
         if (e != cudaSuccess)
             return e;
         configured = true;
@@ -348,7 +352,7 @@ cudaError_t launch_mode(const RowsParams &p, const Arg &arg, size_t smem, cudaSt
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     if constexpr (INLINE)
-        return cudaLaunchKernelEx(&cfg, k_rows_inline<MODE>, arg);
+        return cudaLaunchKernelEx(&cfg, k_rows_inline<MODE, Arg>, arg);
     else
         return cudaLaunchKernelEx(&cfg, k_rows<MODE>, arg);
 }
@@ -376,6 +380,16 @@ cudaError_t launch_rows(int mode, const RowsParams &p, size_t smem, cudaStream_t
 
 cudaError_t launch_rows_inline(int mode, const RowsParamsInline &a, size_t smem,
                                cudaStream_t stream)
+{
+    switch (mode) {
+    case kShrink: return launch_mode<kShrink, true>(a.p, a, smem, stream);
+    case kExpand: return launch_mode<kExpand, true>(a.p, a, smem, stream);
+    default: return launch_mode<kFused, true>(a.p, a, smem, stream);
+    }
+}
+
+cudaError_t launch_rows_inline_small(int mode, const RowsParamsInlineSmall &a, size_t smem,
+                                     cudaStream_t stream)
 {
     switch (mode) {
     case kShrink: return launch_mode<kShrink, true>(a.p, a, smem, stream);

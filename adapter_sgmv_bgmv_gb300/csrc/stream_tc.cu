@@ -159,37 +159,49 @@ __global__ void __launch_bounds__(kThreads) k_stream_tc(const __grid_constant__ 
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
-        for (int i = 0; i < nch; ++i) {
-            const int s = i % NS, u = i / NS;
-            if (u > 0)
-                ok = mbar_wait_bounded(empty0 + 8 * s, uint32_t((u - 1) & 1), status,
-                                       kDevTimeoutPipe) && ok;
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok)
-                break;
-            const int n0 = (ch0 + i) * kBN;
-            if (lane == 0) {
-                mbar_arrive_expect_tx(full0 + 8 * s, kTile);
-                tc::tma_load_2d(stage_t(i), &a.map, n0, row0, full0 + 8 * s);
-                tc::tma_load_2d(stage_t(i) + kBox, &a.map, n0 + 64, row0, full0 + 8 * s);
+        // The y / W tile of chunk i goes out by TMA at once; B of chunk i by
+        // cp.async, and chunk i's "full" arrival is made one chunk later, once that
+        // B group has landed, so the warp never waits on its own copies.
+        for (int i = 0; i <= nch; ++i) {
+            if (i < nch) {
+                const int s = i % NS, u = i / NS;
+                if (u > 0)
+                    ok = mbar_wait_bounded(empty0 + 8 * s, uint32_t((u - 1) & 1), status,
+                                           kDevTimeoutPipe) && ok;
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok)
+                    break;
+                const int n0 = (ch0 + i) * kBN;
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(full0 + 8 * s, kTile);
+                    tc::tma_load_2d(stage_t(i), &a.map, n0, row0, full0 + 8 * s);
+                    tc::tma_load_2d(stage_t(i) + kBox, &a.map, n0 + 64, row0, full0 + 8 * s);
+                }
+                const uint32_t sb = stage_b(i);
+                for (int q = lane; q < rp * 16; q += 32) {
+                    const int j = q >> 4, c16 = q & 15;
+                    const int col = n0 + 8 * c16;
+                    const bool valid = j < r && col + 8 <= d_out;
+                    const uint32_t off = uint32_t(c16 >> 3) * lbo_b + uint32_t(j >> 3) * 1024u +
+                                         tc::sw128(uint32_t(j & 7), uint32_t(c16 & 7));
+                    tc::cp_async16(sb + off,
+                                   valid ? b_pool + int64_t(b_pages[j]) * b_pw + col : b_pool,
+                                   valid ? 16u : 0u);
+                }
+                tc::cp_async_commit();
             }
-            const uint32_t sb = stage_b(i);
-            for (int q = lane; q < rp * 16; q += 32) {
-                const int j = q >> 4, c16 = q & 15;
-                const int col = n0 + 8 * c16;
-                const bool valid = j < r && col + 8 <= d_out;
-                const uint32_t off = uint32_t(c16 >> 3) * lbo_b + uint32_t(j >> 3) * 1024u +
-                                     tc::sw128(uint32_t(j & 7), uint32_t(c16 & 7));
-                tc::cp_async16(sb + off, valid ? b_pool + int64_t(b_pages[j]) * b_pw + col : b_pool,
-                               valid ? 16u : 0u);
+            if (i > 0) {
+                if (i < nch)
+                    tc::cp_async_wait<1>();     // B of chunk i - 1 has landed
+                else
+                    tc::cp_async_wait<0>();
+                tc::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(full0 + 8 * ((i - 1) % NS));
             }
-            tc::cp_async_commit();
-            tc::cp_async_wait<0>();
-            tc::fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(full0 + 8 * s);
         }
+        tc::cp_async_wait<0>();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
@@ -324,10 +336,9 @@ __global__ void __launch_bounds__(kThreads) k_stream_tc(const __grid_constant__ 
                     if (n0 + 64 < d_out)   // a box wholly right of the matrix is not stored
                         tc::tma_store_2d(&a.map, n0 + 64, row0, st + kBox);
                     tc::bulk_commit();
-                    // release the previous chunk's stage once its store has read it
-                    tc::bulk_wait_read1();
-                    if (i > 0)
-                        mbar_arrive(empty0 + 8 * ((i - 1) % NS));
+                    // release the stage as soon as the store has read it
+                    tc::bulk_wait_read0();
+                    mbar_arrive(empty0 + 8 * s);
                 }
             } else {
                 const int c16 = lane & 15;

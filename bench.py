@@ -222,6 +222,9 @@ class Bench:
                             d[f] = b[f].clone()
                 d["table"] = L.AdapterTable(self.ctx, d["a_pool"], d["b_pool"], c["rank"],
                                             c["scale"], c["a_pages"], c["b_pages"])
+                if not self.is_merge:
+                    d["call"] = L.PreparedFused(self.ctx, d["table"], d["x"], d["y"],
+                                                torch.cuda.current_stream())
                 st[key] = d
             self.sets.append(st)
         torch.cuda.synchronize()
@@ -237,8 +240,7 @@ class Bench:
             L.lora_unmerge(self.ctx, d["table"], k, d["W"], stream)
             return
         for key, ids in self.steps_ids[i % len(self.steps_ids)]:
-            d = st[key]
-            L.lora_fused(self.ctx, d["table"], ids, d["x"], d["y"], stream)
+            st[key]["call"](ids)
 
     def tokens_per_step(self, i: int) -> int:
         if self.is_merge:
@@ -357,6 +359,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0,
                     help="seconds of oracle time for the cpu_baseline")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--profile-every", type=int, default=8,
+                    help="bracket one kernel launch in N with CUDA events (roofline timing)")
     ap.add_argument("--tiles", default=os.path.join(ROOT, "adapter_sgmv_bgmv_gb300", "tiles.tbl"))
     args = ap.parse_args()
 
@@ -391,6 +395,20 @@ def main():
     return 0
 
 
+def aggregate_ranks(ms: float, tokens: int, dist, device):
+    """Replicas only: every rank times its own copy of the workload; the job's time is
+    the slowest rank's and its throughput is the sum of all ranks' units over that
+    time.  Returns (max ms, total units, world size)."""
+    if dist is None or not dist.is_initialized():
+        return ms, tokens, 1
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    u = torch.tensor([float(tokens)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), int(u.item()), dist.get_world_size()
+
+
 def default_steps(name):
     return {"llama7b_decode": 20000, "tiny_decode": 20000, "lorazor_decode": 10000,
             "slora_prefill": 2000, "valora_prefill": 500, "valora_merge": 1000}[name]
@@ -417,7 +435,8 @@ def run_one(name, args, L, torch, ctx, dist, world, rank, local):
         dist.barrier()
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
-    ctx.profile_begin()
+    ctx.profile_begin(args.profile_every)
+    n_launch0 = ctx.launch_count()
     t_wall0 = time.time()
     ev0.record(stream)
     for i in range(K):
@@ -426,36 +445,33 @@ def run_one(name, args, L, torch, ctx, dist, world, rank, local):
     torch.cuda.synchronize()
     t_wall1 = time.time()
     prof = ctx.profile_end()
+    n_launched = ctx.launch_count() - n_launch0
     ms = ev0.elapsed_time(ev1)
+    tokens_local = sum(b.tokens_per_step(W + i) for i in range(K))
+    ms, tokens_all, _ = aggregate_ranks(ms, tokens_local, dist, "cuda")
     if dist is not None:
-        import torch.distributed as d
-        tt = torch.tensor([ms], device="cuda")
-        d.all_reduce(tt, op=d.ReduceOp.MAX)
-        ms = float(tt.item())
-        d.barrier()
+        dist.barrier()
     clocks.stop()
     clk = clocks.summary(t_wall0, t_wall1)
 
-    tokens = sum(b.tokens_per_step(W + i) for i in range(K))
     bytes_total = sum(b.alg_bytes_step(W + i) for i in range(K))
     flops_total = sum(b.flops_step(W + i) for i in range(K))
     pk = peaks()
-    fam = "merge" if b.is_merge else "rows"
-    k_ms, k_n = prof[fam]
-    if k_n == 0:   # nothing of that family ran: take the other one
-        fam = max(prof, key=lambda f: prof[f][1])
-        k_ms, k_n = prof[fam]
     launches = sum(n for (_, n) in prof.values())
     kern_s_total = sum(m for (m, _) in prof.values()) / 1e3
-    per_launch_s = (k_ms / 1e3) / max(1, k_n)
-    bytes_per_launch = bytes_total / max(1, launches)
-    achieved_gbs = bytes_per_launch / per_launch_s / 1e9 if per_launch_s > 0 else None
+    # All kernels of the path are HBM-bound: the roofline is taken over every
+    # launch of the timed region (algorithmic bytes / summed kernel time).
+    achieved_gbs = bytes_total / kern_s_total / 1e9 if kern_s_total > 0 else None
+    per_kernel = {f: round(1e3 * m / n, 3) for f, (m, n) in prof.items() if n}
+    kernel_names = {"rows": "k_rows_inline<fused>", "shrink": "k_shrink_tc",
+                    "expand": "k_stream_tc(expand)", "merge": "k_stream_tc(merge)"}
+    dominant = max(prof, key=lambda f: prof[f][0])
     sec = ms / 1e3
     if b.is_merge:
         value = 2 * K * world / sec
         unit = "merge+unmerge calls/s"
     else:
-        value = tokens * world / sec
+        value = tokens_all / sec
         unit = "tokens/s"
     line = {
         "metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": K,
@@ -466,16 +482,18 @@ def run_one(name, args, L, torch, ctx, dist, world, rank, local):
                          f"({b.n_sets * b._unique_bytes_per_step() / 1e6:.0f} MB touched per pass "
                          f"> 129 MB L2)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-        "us_per_call": {"kernel": 1e3 * k_ms / max(1, k_n),
-                        "host_call": 1e6 * sec / max(1, K * b.launches_per_step())},
+        "us_per_call": {"kernel": 1e6 * kern_s_total / max(1, K * b.launches_per_step()),
+                        "host_call": 1e6 * sec / max(1, K * b.launches_per_step()),
+                        "per_kernel_launch": per_kernel},
         "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": pk["hbm_gbs"],
                      "unit": "GB/s",
                      "frac": (achieved_gbs / pk["hbm_gbs"]) if achieved_gbs else None,
                      "traffic": None, "peak_source": pk["source"],
-                     "kernel": "k_rows_inline<fused>" if not b.is_merge else "merge",
-                     "alg_bytes_per_launch": bytes_per_launch,
+                     "kernel": kernel_names[dominant],
+                     "scope": "all launches of the timed region",
+                     "alg_bytes_per_call": bytes_total / max(1, K * b.launches_per_step()),
                      "tflops": flops_total / max(1e-12, kern_s_total) / 1e12},
-        "gpu_launches": launches,
+        "gpu_launches": n_launched,
         "clocks": clk,
     }
     # end to end through pinned host buffers

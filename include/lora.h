@@ -186,13 +186,17 @@ int lora_sync_status(lora_ctx *ctx, void *stream);
 enum { LORA_OPT_TILE_PATH = 1, LORA_OPT_MERGE_KERNEL = 2, LORA_OPT_TILE_MIN_RUN = 3 };
 int lora_ctx_set_option(lora_ctx *ctx, int option, int value);
 
-/* Per-launch timing: between lora_profile_begin and lora_profile_end every kernel
- * launch of the context is bracketed by CUDA events on its stream.  _end
+/* Per-launch timing: between lora_profile_begin and lora_profile_end every
+ * `every`-th kernel launch of the context (every >= 1) is bracketed by CUDA events
+ * on its stream.  _end
  * synchronizes on those events and returns, per kernel family (0 row-gather,
- * 1 tensor-core tile, 2 merge), the summed device time in ms[] and the launch count
- * in launches[] (arrays of 3). */
-int lora_profile_begin(lora_ctx *ctx);
+ * 1 tensor-core tile shrink, 2 merge, 3 tensor-core streaming expand), the summed
+ * device time in ms[] and the launch count in launches[] (arrays of 4). */
+int lora_profile_begin(lora_ctx *ctx, int every);
 int lora_profile_end(lora_ctx *ctx, double *ms, int64_t *launches);
+
+/* Kernels launched by this context since it was created. */
+int64_t lora_launch_count(const lora_ctx *ctx);
 
 /* Which kernel the last delta call launched: 0 none, 1 row-gather, 2 tensor-core
  * tile, 3 both; and how many kernels it launched. */
