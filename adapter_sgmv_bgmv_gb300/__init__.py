@@ -18,7 +18,7 @@ import torch
 from . import _lib
 
 __all__ = ["LoraError", "Context", "AdapterTable", "lora_plan_build", "lora_shrink",
-           "lora_expand", "lora_fused", "PreparedFused", "lora_merge", "lora_unmerge", "lora_tune_shape",
+           "lora_expand", "lora_fused", "lora_fused_noalloc", "PreparedFused", "lora_merge", "lora_unmerge", "lora_tune_shape",
            "KIND_ROWS_FUSED", "KIND_SHRINK", "KIND_EXPAND", "KIND_TILE_FUSED", "KIND_MERGE",
            "OPT_TILE_PATH", "OPT_MERGE_KERNEL", "OPT_TILE_MIN_RUN",
            "library_path"]
@@ -261,6 +261,18 @@ def lora_fused(ctx: Context, table: AdapterTable, ids, x: torch.Tensor, y: torch
                        _stream(stream, ctx.device))
     if rc:
         _check(rc, ctx)
+
+
+def lora_fused_noalloc(ctx: Context, table: AdapterTable, ids, x: torch.Tensor, y: torch.Tensor,
+                       stream=None):
+    """lora_fused for callers that must not allocate while it runs: scratch is a fixed
+    4 MB device array inside the library; raises LORA_E_CAPACITY beyond its limits
+    (see include/lora.h)."""
+    ids, pid, n = _ids(ids)
+    px, ldx, d_in = _rows(x, "x")
+    py, ldy, d_out = _rows(y, "y")
+    _check(_L.lora_fused_noalloc(ctx.handle, table.handle, pid, n, px, ldx, d_in, py, ldy, d_out,
+                                 _stream(stream, ctx.device)), ctx)
 
 
 class PreparedFused:

@@ -34,6 +34,7 @@ SIGNATURES = {
     "lora_shrink": ([P, P, P, I64, P, I64, I, P, I64, P], I),
     "lora_expand": ([P, P, P, I64, P, I64, P, I64, I, P], I),
     "lora_fused": ([P, P, P, I64, P, I64, I, P, I64, I, P], I),
+    "lora_fused_noalloc": ([P, P, P, I64, P, I64, I, P, I64, I, P], I),
     "lora_merge": ([P, P, I, P, I64, I, I, P], I),
     "lora_unmerge": ([P, P, I, P, I64, I, I, P], I),
     "lora_tiles_load": ([P, ctypes.c_char_p], I),

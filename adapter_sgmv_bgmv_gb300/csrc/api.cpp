@@ -380,7 +380,7 @@ int tile_min_run(const lora_ctx *ctx, int64_t n_act, int d_in, int d_out, int ra
 
 int run_tiles(lora_ctx *ctx, const lora_table *t, int mode, const void *x, int64_t ldx, int d_in,
               float *v, int64_t ldv, void *y, int64_t ldy, int d_out, int64_t n,
-              cudaStream_t stream)
+              cudaStream_t stream, const NoAllocScratch *fixed = nullptr)
 {
     Plan &pl = ctx->plan;
     if (pl.tile_items.empty())
@@ -389,23 +389,29 @@ int run_tiles(lora_ctx *ctx, const lora_table *t, int mode, const void *x, int64
     Slot *slot = nullptr;
     int rc = LORA_OK;
     const TileItem *d_items = nullptr;
-    rc = acquire_slot(ctx, items_bytes + 16, &slot);
-    if (rc != LORA_OK)
-        return rc;
-    std::memcpy(slot->host, pl.tile_items.data(), items_bytes);
-    CUDA_TRY(ctx, cudaMemcpyAsync(slot->dev, slot->host, items_bytes, cudaMemcpyHostToDevice,
-                                  stream));
-    d_items = reinterpret_cast<const TileItem *>(slot->dev);
+    if (fixed) {
+        CUDA_TRY(ctx, noalloc_put_items(pl.tile_items.data(), int(pl.tile_items.size()), stream));
+        d_items = fixed->items;
+    } else {
+        rc = acquire_slot(ctx, items_bytes + 16, &slot);
+        if (rc != LORA_OK)
+            return rc;
+        std::memcpy(slot->host, pl.tile_items.data(), items_bytes);
+        CUDA_TRY(ctx, cudaMemcpyAsync(slot->dev, slot->host, items_bytes, cudaMemcpyHostToDevice,
+                                      stream));
+        d_items = reinterpret_cast<const TileItem *>(slot->dev);
+    }
     // K-split of the fused shrink: about two CTAs per SM over all tiles, each CTA
     // keeping at least 4 K blocks of 64.
     int ksplit = 1;
     if (mode == kFused) {
         const int64_t tiles = int64_t(pl.tile_items.size());
         const int nkb = (d_in + 63) / 64;
-        while (ksplit < 8 && tiles * ksplit * 2 <= 2 * kSms && nkb / (ksplit * 2) >= 4)
+        while (ksplit < 8 && tiles * ksplit * 2 <= 2 * kSms && nkb / (ksplit * 2) >= 4 &&
+               (!fixed || tiles * ksplit * 2 <= kNoAllocSlots))
             ksplit *= 2;
         const size_t need = size_t(tiles) * size_t(ksplit) * size_t(kVPartBytes);
-        if (need > ctx->vparts_cap) {
+        if (!fixed && need > ctx->vparts_cap) {
             // Grows to the largest need seen; later calls reuse it.
             if (ctx->vparts) {
                 CUDA_TRY(ctx, cudaStreamSynchronize(stream));
@@ -430,7 +436,7 @@ int run_tiles(lora_ctx *ctx, const lora_table *t, int mode, const void *x, int64
     p.a_pages = t->d_a_pages;
     p.b_pages = t->d_b_pages;
     p.items = d_items;
-    p.vparts = reinterpret_cast<float *>(ctx->vparts);
+    p.vparts = fixed ? fixed->vparts : reinterpret_cast<float *>(ctx->vparts);
     p.ksplit = ksplit;
     p.v = v;
     p.ldv = ldv;
@@ -829,6 +835,53 @@ int lora_fused(lora_ctx *ctx, const lora_table *t, const int32_t *ids, int64_t n
 {
     return delta_call(ctx, t, kFused, ids, n, x, ldx, d_in, nullptr, 0, y, ldy, d_out,
                       static_cast<cudaStream_t>(stream));
+}
+
+int lora_fused_noalloc(lora_ctx *ctx, const lora_table *t, const int32_t *ids, int64_t n,
+                       const void *x, int64_t ldx, int d_in, void *y, int64_t ldy, int d_out,
+                       void *stream_ptr)
+{
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+    if (ctx)
+        ctx->last_path = ctx->last_launches = 0;
+    int rc = prepare(ctx, t, ids, n);
+    if (rc != LORA_OK)
+        return rc;
+    Plan &pl = ctx->plan;
+    if (pl.active.empty())
+        return LORA_OK;
+    if (!stride_ok(x, ldx, d_in) || d_in > t->a_pw || !stride_ok(y, ldy, d_out) || d_out > t->b_pw)
+        return LORA_E_INVAL;
+    rc = use_device(ctx);
+    if (rc != LORA_OK)
+        return rc;
+    int32_t rmax = 0;
+    for (int32_t k : pl.seg_adapter)
+        rmax = std::max(rmax, t->rank[size_t(k)]);
+    const int64_t n_act = int64_t(pl.active.size());
+    const int min_run = (ctx->tile_path && tile_tc_supported(d_in, d_out, rmax))
+                            ? tile_min_run(ctx, n_act, d_in, d_out, rmax)
+                            : 0;
+    RowsCfg cfg = choose_rows_cfg(ctx, kFused, kKindRowsFused, n_act,
+                                  int64_t(pl.seg_adapter.size()), d_in, d_out, rmax);
+    plan_items(pl, t->rank.data(), t->scale.data(), cfg.rows, min_run);
+    // Everything must fit the fixed arrays and the launch parameter block.
+    if (pl.tile_items.size() > size_t(kNoAllocSlots) ||
+        pl.row_items.size() > size_t(kInlineItems) || pl.row_perm.size() > size_t(kInlinePerm))
+        return LORA_E_CAPACITY;
+    if (!pl.tile_items.empty() && pl.row_active > 0 && pl.row_active < n_act)
+        cfg = choose_rows_cfg(ctx, kFused, kKindRowsFused, pl.row_active,
+                              int64_t(pl.row_items.size()), d_in, d_out, pl.row_max_rank);
+    NoAllocScratch fixed{};
+    if (noalloc_scratch(ctx->device, &fixed) != 0)
+        return LORA_E_CUDA;
+    const bool prof = ctx->prof;
+    ctx->prof = false;   // the event pool could grow
+    rc = run_tiles(ctx, t, kFused, x, ldx, d_in, nullptr, 0, y, ldy, d_out, n, stream, &fixed);
+    if (rc == LORA_OK)
+        rc = run_rows(ctx, t, kFused, cfg, x, ldx, d_in, nullptr, 0, y, ldy, d_out, stream);
+    ctx->prof = prof;
+    return rc;
 }
 
 int lora_merge(lora_ctx *ctx, const lora_table *t, int adapter, void *W, int64_t ldw, int d_in,

@@ -112,6 +112,16 @@ struct TileParams {
     int max_tile_rank;        // largest rank among the items (sizes shared memory)
     int ksplit;               // fused: K-split of the shrink (1..8)
 };
+// Fixed scratch of lora_fused_noalloc (noalloc.cu): device addresses of the
+// file-scope arrays on one device, looked up once per device.
+constexpr int kNoAllocSlots = 64;
+struct NoAllocScratch {
+    float *vparts;            // kNoAllocSlots slots of kVPartBytes
+    TileItem *items;          // kNoAllocSlots entries
+};
+int noalloc_scratch(int device, NoAllocScratch *out);
+cudaError_t noalloc_put_items(const TileItem *items, int n, cudaStream_t stream);
+
 cudaError_t launch_shrink_tc(const TileParams &p, cudaStream_t stream);
 cudaError_t launch_expand_tc(const TileParams &p, cudaStream_t stream);
 bool tile_tc_supported(int d_in, int d_out, int rank);

@@ -139,6 +139,28 @@ int lora_fused(lora_ctx *ctx, const lora_table *table, const int32_t *ids_host,
                int64_t n, const void *x, int64_t ldx, int d_in, void *y, int64_t ldy,
                int d_out, void *stream);
 
+/* Fused delta that allocates nothing.  Same operation, arguments and results as
+ * lora_fused (within the same tolerance; the two may pick different summation
+ * orders), for callers that must not allocate device or pinned memory while they
+ * run: code paths that forbid cudaMalloc / cudaFree, or that run inside a
+ * pre-sized memory budget.  There is no counterpart of this entry point on the
+ * pages.  The context and the table are created beforehand (those calls do
+ * allocate); this call then only launches kernels.  Its tensor-core scratch is a
+ * fixed 4 MB file-scope device array (64 partial slots of 128 x 128 fp32) that
+ * every GPU loading the library holds until the process exits.  Limits (else
+ * LORA_E_CAPACITY, nothing launched): at most 64 tiles of up to 128 consecutive
+ * same-adapter rows, at most 256 row-gather work items and 512 active rows outside
+ * those tiles, n <= the context's max_rows.  The first call on a device looks up
+ * the array's device address (a runtime call, no allocation) and should come
+ * before any stream capture.  Every call shares the array: calls that overlap on
+ * the GPU (different streams, or one stream and a capture replay) race on it;
+ * calls in order on one stream do not.  Nothing in it needs clearing: every slot a
+ * call reads is written by the same call first.  Profiling (lora_profile_begin) is
+ * ignored for this call. */
+int lora_fused_noalloc(lora_ctx *ctx, const lora_table *table, const int32_t *ids_host,
+                       int64_t n, const void *x, int64_t ldx, int d_in, void *y, int64_t ldy,
+                       int d_out, void *stream);
+
 /* Merge / unmerge (mode switch): W[c, o] = bf16(W[c, o] +/- s_k sum_j A_k[c, j]
  * B_k[j, o]) in place, W [d_in, ldw] bf16 row-major.  Unmerge after merge restores
  * W to within two bf16 rounding steps (not bit-exactly). */
