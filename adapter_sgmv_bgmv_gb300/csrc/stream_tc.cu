@@ -36,7 +36,8 @@ namespace {
 
 constexpr int kTM = 128;
 constexpr int kBN = 128;
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;          // producer, MMA, 8 epilogue warps
+constexpr int kEpi = 256;
 constexpr uint32_t kBox = kTM * 128;          // one 64-column TMA box of 128 rows
 constexpr uint32_t kTile = 2 * kBox;          // 128 x 128 bf16
 
@@ -77,9 +78,11 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads)
 
 // Warp roles: warp 0 producer (B chunks by cp.async, y / W tiles by TMA) running up
 // to NS chunks ahead; warp 1 MMA issuer (two TMEM accumulators, so the MMAs of
-// chunk i + 1 overlap the epilogue of chunk i); warps 2-5 stage the left operand,
-// then run the epilogue and the stores, releasing a stage once its store has read
-// shared memory.
+// chunk i + 1 overlap the epilogue of chunk i); warps 2-9 stage the left operand,
+// then run the epilogue (warp w reads TMEM lanes 32*(w%4).. and one 64-column half
+// of the chunk, both TMEM loads in flight before one wait) and the stores; a stage
+// is released one chunk later, once its store has read shared memory, so that wait
+// stays off the critical path.
 __global__ void __launch_bounds__(kThreads) k_stream_tc(const __grid_constant__ StreamArgs a)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -144,7 +147,7 @@ __global__ void __launch_bounds__(kThreads) k_stream_tc(const __grid_constant__ 
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(tfull0 + 8 * b, 1);      // MMA commit
-            mbar_init(tempty0 + 8 * b, 4);     // one arrive per epilogue warp
+            mbar_init(tempty0 + 8 * b, kEpi / 32);   // one arrive per epilogue warp
         }
         fence_mbar_init();
     }
@@ -238,8 +241,8 @@ __global__ void __launch_bounds__(kThreads) k_stream_tc(const __grid_constant__ 
         __syncwarp();
     } else {
         // ------------------------------------------------------------ left operand
-        const int et = tid - 64;                 // 0..127
-        if (a.left != kLeftAPages) {
+        const int et = tid - 64;                 // 0..255
+        if (a.left != kLeftAPages && et < kTM) {
             const int row = et;
             const int KS = a.left == kLeftVParts ? a.p.ksplit : 1;
             for (int c = 0; c < rp / 8; ++c) {
@@ -274,9 +277,9 @@ __global__ void __launch_bounds__(kThreads) k_stream_tc(const __grid_constant__ 
                     pack8(f);
             }
             tc::fence_proxy_async_smem();
-        } else {
+        } else if (a.left == kLeftAPages) {
             // A_k rows row0..row0+127, column j = page j: M-major, 64-row atoms.
-            for (int q = et; q < rp * 16; q += 128) {
+            for (int q = et; q < rp * 16; q += kEpi) {
                 const int j = q >> 4, c16 = q & 15;
                 const int c = row0 + 8 * c16;
                 const bool valid = j < r && c + 8 <= a.m.d_in;
@@ -290,12 +293,13 @@ __global__ void __launch_bounds__(kThreads) k_stream_tc(const __grid_constant__ 
             tc::cp_async_wait<0>();
             tc::fence_proxy_async_smem();
         }
-        named_bar_sync(1, 128);
+        named_bar_sync(1, kEpi);
         if (et == 0)
             mbar_arrive(bar_left);
 
         // ------------------------------------------------------------ epilogue
         const int q4 = warp & 3;                  // TMEM lanes 32*q4 .. 32*q4+31
+        const int half = (warp - 2) >> 2;         // columns 64*half .. 64*half+63
         const int row = 32 * q4 + lane;
         for (int i = 0; i < nch; ++i) {
             const int s = i % NS, b = i & 1;
@@ -306,29 +310,32 @@ __global__ void __launch_bounds__(kThreads) k_stream_tc(const __grid_constant__ 
                 break;
             tc::fence_after_sync();
             const uint32_t st = stage_t(i);
-#pragma unroll 1
-            for (int cc = 0; cc < kBN / 32; ++cc) {
-                float acc[32];
-                tc::tmem_ld32(tmem + (uint32_t(32 * q4) << 16) + uint32_t(b * kBN + cc * 32), acc);
-                uint8_t *box = gbase + (st - base) + (cc >> 1) * kBox;
+            uint32_t acc[2][32];
+            const uint32_t ta = tmem + (uint32_t(32 * q4) << 16) + uint32_t(b * kBN + 64 * half);
+            tc::tmem_ld32_nowait(ta, acc[0]);
+            tc::tmem_ld32_nowait(ta + 32, acc[1]);
+            tc::tmem_wait_ld();
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(tempty0 + 8 * b);      // accumulator b is free for chunk i + 2
+            uint8_t *box = gbase + (st - base) + half * kBox;   // the 64-column TMA box
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     uint4 *ptr = reinterpret_cast<uint4 *>(
-                        box + tc::sw128(uint32_t(row), uint32_t((cc & 1) * 4 + q)));
+                        box + tc::sw128(uint32_t(row), uint32_t(cc * 4 + q)));
                     float t[8];
                     unpack8(*ptr, t);
 #pragma unroll
                     for (int e = 0; e < 8; ++e)
-                        t[e] = fmaf(scale, acc[q * 8 + e], t[e]);
+                        t[e] = fmaf(scale, __uint_as_float(acc[cc][q * 8 + e]), t[e]);
                     *ptr = pack8(t);
                 }
             }
-            tc::fence_before_sync();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(tempty0 + 8 * b);      // this warp is done with accumulator b
             tc::fence_proxy_async_smem();
-            named_bar_sync(1, 128);
+            named_bar_sync(1, kEpi);
             const int n0 = (ch0 + i) * kBN;
             if (full_rows) {
                 if (et == 0) {
@@ -336,14 +343,15 @@ __global__ void __launch_bounds__(kThreads) k_stream_tc(const __grid_constant__ 
                     if (n0 + 64 < d_out)   // a box wholly right of the matrix is not stored
                         tc::tma_store_2d(&a.map, n0 + 64, row0, st + kBox);
                     tc::bulk_commit();
-                    // release the stage as soon as the store has read it
-                    tc::bulk_wait_read0();
-                    mbar_arrive(empty0 + 8 * s);
+                    // the previous chunk's store has read its stage by now, usually
+                    tc::bulk_wait_read1();
+                    if (i > 0)
+                        mbar_arrive(empty0 + 8 * ((i - 1) % NS));
                 }
             } else {
                 const int c16 = lane & 15;
                 const int col = n0 + 8 * c16;
-                for (int rr = (warp - 2) * 2 + (lane >> 4); rr < nrows; rr += 8) {
+                for (int rr = (warp - 2) * 2 + (lane >> 4); rr < nrows; rr += kEpi / 16) {
                     if (col + 8 <= d_out) {
                         const uint4 val = *reinterpret_cast<const uint4 *>(
                             gbase + (st - base) + (c16 >> 3) * kBox +
@@ -351,7 +359,7 @@ __global__ void __launch_bounds__(kThreads) k_stream_tc(const __grid_constant__ 
                         *reinterpret_cast<uint4 *>(a.p.y + int64_t(row0 + rr) * a.p.ldy + col) = val;
                     }
                 }
-                named_bar_sync(1, 128);
+                named_bar_sync(1, kEpi);
                 if (et == 0)
                     mbar_arrive(empty0 + 8 * s);
             }

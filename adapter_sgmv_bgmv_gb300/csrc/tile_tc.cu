@@ -30,10 +30,26 @@ namespace {
 
 constexpr int kTM = 128;                       // rows per tile
 constexpr int kKB = 64;                        // K elements per stage (one 128-byte row)
-constexpr int kStages = 5;
+constexpr int kMaxStages = 8;
 constexpr uint32_t kXStage = kTM * 128;        // 16 KB
-constexpr uint32_t kAStage = 128 * 128;        // up to 128 ranks x 128 B
-constexpr uint32_t kStage = kXStage + kAStage;
+
+// Stage ring of the launch, sized by its largest padded rank: X block + A block,
+// as many stages (<= 8) as fit in about 200 KB.
+struct ShrinkRing {
+    uint32_t a_stage, stage;
+    int stages;
+};
+__host__ __device__ inline ShrinkRing shrink_ring(int max_rank)
+{
+    ShrinkRing g;
+    const int rpm = (max_rank + 15) & ~15;
+    g.a_stage = uint32_t(rpm) * 128u;
+    g.stage = (kXStage + g.a_stage + 1023u) & ~1023u;
+    g.stages = int((200u * 1024u) / g.stage);
+    if (g.stages > kMaxStages)
+        g.stages = kMaxStages;
+    return g;
+}
 constexpr int kShrinkThreads = 192;
 constexpr int kProducers = 128;                // warps 2..5
 
@@ -44,9 +60,10 @@ struct TileArgs {
 
 __host__ __device__ inline int rank_pad16(int r) { return (r + 15) & ~15; }
 
-constexpr uint32_t shrink_smem_bytes()
+__host__ __device__ inline uint32_t shrink_smem_bytes(int max_rank)
 {
-    return 1024u + kStages * kStage + 2u * kStages * 8u + 64u + 4u * 128u;
+    const ShrinkRing g = shrink_ring(max_rank);
+    return 1024u + uint32_t(g.stages) * g.stage + 2u * kMaxStages * 8u + 64u + 4u * 128u;
 }
 
 
@@ -60,9 +77,12 @@ __global__ void __launch_bounds__(kShrinkThreads, 1) k_shrink_tc(const __grid_co
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t *gbase = smem_raw + (base - raw);
-    const uint32_t full0 = base + kStages * kStage;
-    const uint32_t empty0 = full0 + kStages * 8;
-    const uint32_t done = empty0 + kStages * 8;
+    const ShrinkRing ring = shrink_ring(p.max_tile_rank);
+    const int kStages = ring.stages;
+    const uint32_t kStage = ring.stage;
+    const uint32_t full0 = base + uint32_t(kStages) * kStage;
+    const uint32_t empty0 = full0 + kMaxStages * 8;
+    const uint32_t done = empty0 + kMaxStages * 8;
     const uint32_t tmem_slot = done + 8;
     int32_t *s_pages = reinterpret_cast<int32_t *>(gbase + (tmem_slot + 64 - base));
 
@@ -104,7 +124,8 @@ __global__ void __launch_bounds__(kShrinkThreads, 1) k_shrink_tc(const __grid_co
                 if (!ok)
                     break;
                 mbar_arrive_expect_tx(full0 + 8 * s, kXStage);
-                tc::tma_load_2d(base + s * kStage, &args.map, (kb0 + kb) * kKB, it.row0, full0 + 8 * s);
+                tc::tma_load_2d(base + uint32_t(s) * kStage, &args.map, (kb0 + kb) * kKB, it.row0,
+                                full0 + 8 * s);
             }
         }
     } else if (warp == 1) {
@@ -116,7 +137,7 @@ __global__ void __launch_bounds__(kShrinkThreads, 1) k_shrink_tc(const __grid_co
                 if (!ok)
                     break;
                 tc::fence_after_sync();
-                const uint32_t xs = base + s * kStage, as = xs + kXStage;
+                const uint32_t xs = base + uint32_t(s) * kStage, as = xs + kXStage;
 #pragma unroll
                 for (int k4 = 0; k4 < kKB / 16; ++k4) {
                     const uint64_t da = tc::smem_desc_sw128(xs + 32u * k4, 16u, 1024u);
@@ -136,7 +157,7 @@ __global__ void __launch_bounds__(kShrinkThreads, 1) k_shrink_tc(const __grid_co
             if (u > 0 && ok)
                 ok = mbar_wait_bounded(empty0 + 8 * s, (u - 1) & 1, p.status, kDevTimeoutPipe);
             if (ok) {
-                const uint32_t as = base + s * kStage + kXStage;
+                const uint32_t as = base + uint32_t(s) * kStage + kXStage;
                 for (int q = t; q < nchunks; q += kProducers) {
                     const int j = q >> 3, c = q & 7;
                     const int col = (kb0 + kb) * kKB + c * 8;
@@ -217,7 +238,7 @@ cudaError_t launch_shrink_tc(const TileParams &p, cudaStream_t stream)
     static bool configured = false;
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(k_shrink_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             int(shrink_smem_bytes()));
+                                             227 * 1024);
         if (e != cudaSuccess)
             return e;
         configured = true;
@@ -225,7 +246,7 @@ cudaError_t launch_shrink_tc(const TileParams &p, cudaStream_t stream)
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(unsigned(p.n_items) * unsigned(p.vmode == 0 ? p.ksplit : 1));
     cfg.blockDim = dim3(kShrinkThreads);
-    cfg.dynamicSmemBytes = shrink_smem_bytes();
+    cfg.dynamicSmemBytes = shrink_smem_bytes(p.max_tile_rank);
     cfg.stream = stream;
     return cudaLaunchKernelEx(&cfg, k_shrink_tc, args);
 }
