@@ -65,8 +65,8 @@ struct lora_ctx {
     RowsParamsInline inline_args;   // staging of in-parameter plans
     RowsParamsInlineSmall inline_small;
     int64_t launches_total = 0;     // every kernel launched by this context
-    int prof_every = 1;             // bracket one launch in this many
-    int64_t prof_seen = 0;
+    int prof_every = 1;             // bracket one launch in this many, per kernel family
+    int64_t prof_seen[4] = {0, 0, 0, 0};
     int merge_path = 0;             // 0 auto (tensor cores when supported), 1 CUDA cores
     int tile_path = 1;              // 1: long same-adapter runs use the tensor-core tiles
     int tile_min_run_override = 0;  // > 0: fixed minimum run for the tile path
@@ -162,7 +162,7 @@ long prof_start(lora_ctx *ctx, int family, cudaStream_t stream)
 {
     if (!ctx->prof)
         return -1;
-    if ((ctx->prof_seen++ % ctx->prof_every) != 0)
+    if ((ctx->prof_seen[family & 3]++ % ctx->prof_every) != 0)
         return -1;
     if (ctx->prof_used == ctx->prof_ev.size()) {
         lora_ctx::ProfEv e;
@@ -958,7 +958,8 @@ int lora_profile_begin(lora_ctx *ctx, int every)
     ctx->prof = true;
     ctx->prof_used = 0;
     ctx->prof_every = every;
-    ctx->prof_seen = 0;
+    for (int64_t &c : ctx->prof_seen)
+        c = 0;
     return LORA_OK;
 }
 

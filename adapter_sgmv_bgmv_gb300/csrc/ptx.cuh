@@ -131,6 +131,15 @@ __device__ __forceinline__ float ld_dsmem_f32(const float *local, uint32_t rank)
     return v;
 }
 
+// ---------------------------------------------------------------- programmatic launch
+
+// Wait until the preceding kernel in the stream has completed and its writes are
+// visible (returns at once when the launch has no programmatic predecessor).
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Allow the next kernel in the stream to start launching its CTAs.
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---------------------------------------------------------------- bf16 vectors
 
 __device__ __forceinline__ void unpack8(const uint4 &u, float f[8])

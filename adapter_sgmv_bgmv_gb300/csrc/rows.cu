@@ -129,9 +129,33 @@ __device__ __forceinline__ void rows_body(const RowsParams &p, const RowItem *it
     if (clustered)
         cluster_arrive_relaxed();   // "started"; waited on before the first remote store
 
-    // ---- 1. copies (one dependent load: the page ids)
+    // ---- 1. copies.  Page ids come from the table (written once, at registration),
+    // so they are read before waiting for the preceding kernel; everything it may
+    // have written (x, y, v, the pools) is touched only after the wait.
+    const uint32_t in_bytes = uint32_t(in_len) * 2u, out_bytes = uint32_t(out_len) * 2u;
+    int32_t pa0 = 0, pa1 = 0, pb0 = 0, pb1 = 0, pr0 = 0, pr1 = 0;
     if (warp == 0) {
-        const uint32_t in_bytes = uint32_t(in_len) * 2u, out_bytes = uint32_t(out_len) * 2u;
+        const int32_t *ap = p.a_pages + size_t(k) * p.max_rank;
+        const int32_t *bp = p.b_pages + size_t(k) * p.max_rank;
+        if (lane < r) {
+            if (MODE != kExpand)
+                pa0 = ap[lane];
+            if (MODE != kShrink)
+                pb0 = bp[lane];
+        }
+        if (lane + 32 < r) {
+            if (MODE != kExpand)
+                pa1 = ap[lane + 32];
+            if (MODE != kShrink)
+                pb1 = bp[lane + 32];
+        }
+        if (lane < nrows)
+            pr0 = perm[it.p0 + lane];
+        if (lane + 32 < nrows)
+            pr1 = perm[it.p0 + lane + 32];
+    }
+    grid_dep_wait();
+    if (warp == 0) {
         if (lane == 0) {
             if (MODE != kExpand)
                 mbar_arrive_expect_tx(bar0, uint32_t(r + nrows) * in_bytes);
@@ -142,15 +166,21 @@ __device__ __forceinline__ void rows_body(const RowsParams &p, const RowItem *it
         const int32_t *ap = p.a_pages + size_t(k) * p.max_rank;
         const int32_t *bp = p.b_pages + size_t(k) * p.max_rank;
         for (int q = lane; q < r || q < nrows; q += 32) {
-            int32_t pa = 0, pb = 0, row = 0;
-            if (q < r) {
-                if (MODE != kExpand)
-                    pa = ap[q];
-                if (MODE != kShrink)
-                    pb = bp[q];
+            const int h = q >> 5;
+            int32_t qa, qb, row;
+            if (h == 0) {
+                qa = pa0;
+                qb = pb0;
+                row = pr0;
+            } else if (h == 1) {
+                qa = pa1;
+                qb = pb1;
+                row = pr1;
+            } else {   // ranks or rows beyond 64 (rank 128): read them now
+                qa = (MODE != kExpand && q < r) ? ap[q] : 0;
+                qb = (MODE != kShrink && q < r) ? bp[q] : 0;
+                row = q < nrows ? perm[it.p0 + q] : 0;
             }
-            if (q < nrows)
-                row = perm[it.p0 + q];
             if (q < nrows) {
                 if (MODE != kExpand && in_bytes)
                     bulk_g2s(smem_u32(sX + size_t(q) * p.slice_in),
@@ -162,13 +192,14 @@ __device__ __forceinline__ void rows_body(const RowsParams &p, const RowItem *it
             if (q < r) {
                 if (MODE != kExpand && in_bytes)
                     bulk_g2s(smem_u32(sA + size_t(q) * p.slice_in),
-                             p.a_pool + int64_t(pa) * p.a_pw + in0, in_bytes, bar0);
+                             p.a_pool + int64_t(qa) * p.a_pw + in0, in_bytes, bar0);
                 if (MODE != kShrink && out_bytes)
                     bulk_g2s(smem_u32(sB + size_t(q) * p.slice_out),
-                             p.b_pool + int64_t(pb) * p.b_pw + out0, out_bytes, bar1);
+                             p.b_pool + int64_t(qb) * p.b_pw + out0, out_bytes, bar1);
             }
         }
     }
+    grid_dep_launch();
 
     bool ok = true;
 
@@ -344,13 +375,16 @@ cudaError_t launch_mode(const RowsParams &p, const Arg &arg, size_t smem, cudaSt
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = (MODE == kExpand) ? 1u : unsigned(p.cluster);
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    // May start while the previous kernel of the stream drains (see grid_dep_wait).
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     if constexpr (INLINE)
         return cudaLaunchKernelEx(&cfg, k_rows_inline<MODE, Arg>, arg);
     else
