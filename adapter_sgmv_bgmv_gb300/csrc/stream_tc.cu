@@ -40,6 +40,7 @@ constexpr int kThreads = 320;          // producer, MMA, 8 epilogue warps
 constexpr int kEpi = 256;
 constexpr uint32_t kBox = kTM * 128;          // one 64-column TMA box of 128 rows
 constexpr uint32_t kTile = 2 * kBox;          // 128 x 128 bf16
+constexpr int kPrefetch = 8;                  // chunks pulled into L2 ahead of their load
 
 enum Left : int { kLeftVParts = 0, kLeftVRows = 1, kLeftAPages = 2 };
 
@@ -164,7 +165,19 @@ __global__ void __launch_bounds__(kThreads) k_stream_tc(const __grid_constant__ 
         // ------------------------------------------------------------ producer
         // The y / W tile of chunk i goes out by TMA at once; B of chunk i by
         // cp.async, and chunk i's "full" arrival is made one chunk later, once that
-        // B group has landed, so the warp never waits on its own copies.
+        // B group has landed, so the warp never waits on its own copies.  Tiles
+        // kPrefetch chunks ahead are pulled into L2 first: the loads into shared
+        // memory then see L2 latency, and DRAM sees many more requests in flight
+        // than the stage ring could hold.
+        auto prefetch_l2 = [&](int c) {
+            const int n0 = (ch0 + c) * kBN;
+            tc::tma_prefetch_2d(&a.map, n0, row0);
+            if (n0 + 64 < d_out)
+                tc::tma_prefetch_2d(&a.map, n0 + 64, row0);
+        };
+        if (lane == 0)
+            for (int c = 0; c < kPrefetch && c < nch; ++c)
+                prefetch_l2(c);
         for (int i = 0; i <= nch; ++i) {
             if (i < nch) {
                 const int s = i % NS, u = i / NS;
@@ -176,6 +189,8 @@ __global__ void __launch_bounds__(kThreads) k_stream_tc(const __grid_constant__ 
                     break;
                 const int n0 = (ch0 + i) * kBN;
                 if (lane == 0) {
+                    if (i + kPrefetch < nch)
+                        prefetch_l2(i + kPrefetch);
                     mbar_arrive_expect_tx(full0 + 8 * s, kTile);
                     tc::tma_load_2d(stage_t(i), &a.map, n0, row0, full0 + 8 * s);
                     tc::tma_load_2d(stage_t(i) + kBox, &a.map, n0 + 64, row0, full0 + 8 * s);
