@@ -433,6 +433,7 @@ int run_tiles(lora_ctx *ctx, const lora_table *t, int mode, const void *x, int64
     p.a_pw = t->a_pw;
     p.b_pool = t->b_pool;
     p.b_pw = t->b_pw;
+    p.b_n_pages = t->b_n_pages;
     p.a_pages = t->d_a_pages;
     p.b_pages = t->d_b_pages;
     p.items = d_items;
@@ -543,6 +544,7 @@ int merge_call(lora_ctx *ctx, const lora_table *t, int adapter, void *W, int64_t
     p.a_pw = t->a_pw;
     p.b_pool = t->b_pool;
     p.b_pw = t->b_pw;
+    p.b_n_pages = t->b_n_pages;
     p.a_pages = t->d_a_pages + size_t(adapter) * t->max_rank;
     p.b_pages = t->d_b_pages + size_t(adapter) * t->max_rank;
     p.status = ctx->d_status;

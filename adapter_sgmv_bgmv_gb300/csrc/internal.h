@@ -96,6 +96,7 @@ struct TileParams {
     int64_t a_pw;
     const uint16_t *b_pool;
     int64_t b_pw;
+    int64_t b_n_pages;        // rows of the B pool (tensor-map extent of the page gather)
     const int32_t *a_pages;
     const int32_t *b_pages;
     const TileItem *items;
@@ -134,6 +135,7 @@ struct MergeParams {
     int64_t a_pw;
     const uint16_t *b_pool;
     int64_t b_pw;
+    int64_t b_n_pages;        // rows of the B pool (tensor-map extent of the page gather)
     const int32_t *a_pages;   // host-resolved page ids of this adapter, device copy
     const int32_t *b_pages;
     unsigned *status;

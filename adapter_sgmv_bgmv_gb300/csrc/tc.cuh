@@ -181,13 +181,18 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
-// Bring a tile into L2 ahead of its load (no shared memory, no completion).
-__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *map, int x, int y)
+// Four rows (arbitrary row coordinates r0..r3, e.g. page ids) of one box-wide column
+// slice into four consecutive 128-byte rows of shared memory; the map's box is one
+// row high.  The 128-byte swizzle follows the destination address, so rows 4..7 of
+// an 8-row swizzle atom go to atom + 512.
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap *map, int x, int r0,
+                                            int r1, int r2, int r3, uint32_t bar)
 {
-    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
-                     reinterpret_cast<uint64_t>(map)),
-                 "r"(x), "r"(y)
-                 : "memory");
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar)
+        : "memory");
 }
 
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, int x, int y, uint32_t src)

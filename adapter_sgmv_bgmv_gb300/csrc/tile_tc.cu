@@ -117,15 +117,8 @@ __global__ void __launch_bounds__(kShrinkThreads, 1) k_shrink_tc(const __grid_co
     bool ok = true;
     if (warp == 0) {
         if (lane == 0) {
-            // X blocks kPrefetch ahead are pulled into L2 first (see the streaming
-            // kernel): the ring's loads then see L2 latency.
-            constexpr int kPrefetch = 8;
-            for (int kb = 0; kb < kPrefetch && kb < nkb; ++kb)
-                tc::tma_prefetch_2d(&args.map, (kb0 + kb) * kKB, it.row0);
             for (int kb = 0; kb < nkb && ok; ++kb) {
                 const int s = kb % kStages, u = kb / kStages;
-                if (kb + kPrefetch < nkb)
-                    tc::tma_prefetch_2d(&args.map, (kb0 + kb + kPrefetch) * kKB, it.row0);
                 if (u > 0)
                     ok = mbar_wait_bounded(empty0 + 8 * s, (u - 1) & 1, p.status, kDevTimeoutPipe);
                 if (!ok)
