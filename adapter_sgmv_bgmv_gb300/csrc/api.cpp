@@ -433,6 +433,7 @@ int run_tiles(lora_ctx *ctx, const lora_table *t, int mode, const void *x, int64
     p.a_pw = t->a_pw;
     p.b_pool = t->b_pool;
     p.b_pw = t->b_pw;
+    p.a_n_pages = t->a_n_pages;
     p.b_n_pages = t->b_n_pages;
     p.a_pages = t->d_a_pages;
     p.b_pages = t->d_b_pages;

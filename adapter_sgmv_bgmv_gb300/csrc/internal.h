@@ -96,7 +96,8 @@ struct TileParams {
     int64_t a_pw;
     const uint16_t *b_pool;
     int64_t b_pw;
-    int64_t b_n_pages;        // rows of the B pool (tensor-map extent of the page gather)
+    int64_t a_n_pages;        // rows of the A pool (tensor-map extent of the page gather)
+    int64_t b_n_pages;        // rows of the B pool
     const int32_t *a_pages;
     const int32_t *b_pages;
     const TileItem *items;

@@ -29,7 +29,7 @@
 //     add s * acc to the tile in shared memory and store it: whole 128-row boxes by
 //     TMA when every row belongs to the block, else 8-row boxes (one swizzle atom
 //     each) over the block's rows and the last < 8 rows by the epilogue threads.
-//     A stage is released one chunk later, once its store has read shared memory.
+//     A stage is released as soon as its store has read shared memory.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -399,10 +399,15 @@ __global__ void __launch_bounds__(kThreads) k_stream_tc(const __grid_constant__ 
                             tc::tma_store_2d(&a.map8, n0 + 64 * h, bk.row0 + r8, src + uint32_t(r8) * 128u);
                 }
                 tc::bulk_commit();
-                // the previous chunk's store has read its stage by now, usually
-                tc::bulk_wait_read1();
-                if (i > 0)
-                    mbar_arrive(empty0 + 8 * ((i - 1) % NS));
+            }
+            // The stage goes back to the producer once its store has read it (and,
+            // in a tile with a ragged end, once the threads storing the last rows
+            // have): a stage held longer is one load fewer in flight.
+            if (!full_rows && rows8 < bk.nrows)
+                named_bar_sync(1, kEpi);
+            if (et == 0 && ok) {
+                tc::bulk_wait_read0();
+                mbar_arrive(empty0 + 8 * s);
             }
         }
         if (et == 0)

@@ -5,16 +5,19 @@
 //
 // k_shrink_tc, ksplit CTAs per tile, CTA s covering the s-th share of the K blocks:
 //   V[128 x r] (+)= X_tile[128 x K_s] . A_k[K_s x r]
-//   warp 0   TMA-loads X K-blocks (128 rows x 64, 128-byte swizzle) into a ring of
-//            stages;
-//   warps 2-5 stage the matching A_k block from the pages (row j of the MMA's
-//            K-major B operand = page j of A_k) with 16-byte cp.async, ranks padded
-//            to 16 with zeros;
+//   warp 0   fills a ring of stages by TMA alone: per K block the X block (128 rows
+//            x 64, 128-byte swizzle) and the matching A_k block -- row j of the
+//            MMA's K-major B operand is a 64-element slice of page j of A_k, so
+//            tile::gather4 drops four pages at a time straight into the swizzled
+//            layout (rank padding repeats page 0) -- all counted on one barrier;
 //   warp 1   issues the tcgen05 MMAs (M = 128, N = r, K = 64 per stage) into a TMEM
 //            accumulator and frees each stage with tcgen05.commit;
-//   warps 2-5 finally read V from TMEM (row t = lane t) and write it as fp32: into
-//            the CTA's partial slot (fused call; the expand sums the slots in order)
-//            or into the caller's v rows (shrink-only call, one CTA per tile).
+//   warps 2-5 read V from TMEM (row t = lane t) and write it as fp32: into the
+//            CTA's partial slot (fused call; the expand sums the slots in order;
+//            padded rank columns written as zeros) or into the caller's v rows
+//            (shrink-only call, one CTA per tile).
+// Shared memory is sized for two CTAs per SM, so the ksplit x tiles grid (at most
+// two per SM by construction) is resident in one wave.
 //
 // The expand side is the streaming kernel in stream_tc.cu.
 #include <cuda.h>
@@ -31,10 +34,11 @@ namespace {
 constexpr int kTM = 128;                       // rows per tile
 constexpr int kKB = 64;                        // K elements per stage (one 128-byte row)
 constexpr int kMaxStages = 8;
+constexpr int kMaxRank = 128;
 constexpr uint32_t kXStage = kTM * 128;        // 16 KB
+constexpr uint32_t kRingBudget = 100u * 1024u; // two CTAs per SM
 
-// Stage ring of the launch, sized by its largest padded rank: X block + A block,
-// as many stages (<= 8) as fit in about 200 KB.
+// Stage ring of the launch, sized by its largest padded rank: X block + A block.
 struct ShrinkRing {
     uint32_t a_stage, stage;
     int stages;
@@ -45,16 +49,16 @@ __host__ __device__ inline ShrinkRing shrink_ring(int max_rank)
     const int rpm = (max_rank + 15) & ~15;
     g.a_stage = uint32_t(rpm) * 128u;
     g.stage = (kXStage + g.a_stage + 1023u) & ~1023u;
-    g.stages = int((200u * 1024u) / g.stage);
+    g.stages = int(kRingBudget / g.stage);
     if (g.stages > kMaxStages)
         g.stages = kMaxStages;
     return g;
 }
 constexpr int kShrinkThreads = 192;
-constexpr int kProducers = 128;                // warps 2..5
 
 struct TileArgs {
-    CUtensorMap map;                           // x (shrink) or y (expand)
+    CUtensorMap map;                           // x, 64 x 128 boxes
+    CUtensorMap amap;                          // the A pool, rows = pages, 64 x 1 boxes
     TileParams p;
 };
 
@@ -63,14 +67,12 @@ __host__ __device__ inline int rank_pad16(int r) { return (r + 15) & ~15; }
 __host__ __device__ inline uint32_t shrink_smem_bytes(int max_rank)
 {
     const ShrinkRing g = shrink_ring(max_rank);
-    return 1024u + uint32_t(g.stages) * g.stage + 2u * kMaxStages * 8u + 64u + 4u * 128u;
+    return 1024u + uint32_t(g.stages) * g.stage + 2u * kMaxStages * 8u + 64u + 4u * kMaxRank;
 }
-
-
 
 // ---------------------------------------------------------------------- shrink
 
-__global__ void __launch_bounds__(kShrinkThreads, 1) k_shrink_tc(const __grid_constant__ TileArgs args)
+__global__ void __launch_bounds__(kShrinkThreads, 2) k_shrink_tc(const __grid_constant__ TileArgs args)
 {
     const TileParams &p = args.p;
     extern __shared__ uint8_t smem_raw[];
@@ -99,14 +101,14 @@ __global__ void __launch_bounds__(kShrinkThreads, 1) k_shrink_tc(const __grid_co
 
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(full0 + 8 * s, kProducers + 1);
-            mbar_init(empty0 + 8 * s, 1);
+            mbar_init(full0 + 8 * s, 1);       // producer's expect-tx; X + A bytes
+            mbar_init(empty0 + 8 * s, 1);      // MMA commit
         }
         mbar_init(done, 1);
         fence_mbar_init();
     }
-    if (tid < r)
-        s_pages[tid] = p.a_pages[size_t(it.adapter) * p.max_rank + tid];
+    if (tid < rp)   // rank padding repeats page 0; its V columns are zeroed below
+        s_pages[tid] = p.a_pages[size_t(it.adapter) * p.max_rank + (tid < r ? tid : 0)];
     if (warp == 1)
         tc::tmem_alloc(tmem_slot, ncols);
     tc::fence_before_sync();
@@ -116,16 +118,25 @@ __global__ void __launch_bounds__(kShrinkThreads, 1) k_shrink_tc(const __grid_co
 
     bool ok = true;
     if (warp == 0) {
-        if (lane == 0) {
-            for (int kb = 0; kb < nkb && ok; ++kb) {
-                const int s = kb % kStages, u = kb / kStages;
-                if (u > 0)
-                    ok = mbar_wait_bounded(empty0 + 8 * s, (u - 1) & 1, p.status, kDevTimeoutPipe);
-                if (!ok)
-                    break;
-                mbar_arrive_expect_tx(full0 + 8 * s, kXStage);
-                tc::tma_load_2d(base + uint32_t(s) * kStage, &args.map, (kb0 + kb) * kKB, it.row0,
-                                full0 + 8 * s);
+        const int quads = rp / 4;
+        for (int kb = 0; kb < nkb; ++kb) {
+            const int s = kb % kStages, u = kb / kStages;
+            if (u > 0)
+                ok = mbar_wait_bounded(empty0 + 8 * s, (u - 1) & 1, p.status, kDevTimeoutPipe) && ok;
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok)
+                break;
+            const uint32_t xs = base + uint32_t(s) * kStage, as = xs + kXStage;
+            const int k0 = (kb0 + kb) * kKB;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(full0 + 8 * s, kXStage + uint32_t(rp) * 128u);
+                tc::tma_load_2d(xs, &args.map, k0, it.row0, full0 + 8 * s);
+            }
+            __syncwarp();
+            for (int q = lane; q < quads; q += 32) {
+                const int j = 4 * q;
+                tc::tma_gather4(as + uint32_t(j) * 128u, &args.amap, k0, s_pages[j], s_pages[j + 1],
+                                s_pages[j + 2], s_pages[j + 3], full0 + 8 * s);
             }
         }
     } else if (warp == 1) {
@@ -148,39 +159,10 @@ __global__ void __launch_bounds__(kShrinkThreads, 1) k_shrink_tc(const __grid_co
             }
             tc::mma_commit(done);
         }
+        __syncwarp();
     } else {
-        // A producers: 16-byte chunks of the r_pad x 64 block of A_k^T for each stage.
-        const int t = tid - 64;
-        const int nchunks = rp * 8;
-        for (int kb = 0; kb < nkb; ++kb) {
-            const int s = kb % kStages, u = kb / kStages;
-            if (u > 0 && ok)
-                ok = mbar_wait_bounded(empty0 + 8 * s, (u - 1) & 1, p.status, kDevTimeoutPipe);
-            if (ok) {
-                const uint32_t as = base + uint32_t(s) * kStage + kXStage;
-                for (int q = t; q < nchunks; q += kProducers) {
-                    const int j = q >> 3, c = q & 7;
-                    const int col = (kb0 + kb) * kKB + c * 8;
-                    const bool valid = j < r && col + 8 <= p.d_in;
-                    const uint16_t *src = valid ? p.a_pool + int64_t(s_pages[j]) * p.a_pw + col
-                                                : p.a_pool;
-                    tc::cp_async16(as + tc::sw128(uint32_t(j), uint32_t(c)), src, valid ? 16u : 0u);
-                }
-            }
-            tc::cp_async_commit();
-            if (kb >= 2) {
-                tc::cp_async_wait<2>();
-                tc::fence_proxy_async_smem();
-                mbar_arrive(full0 + 8 * ((kb - 2) % kStages));
-            }
-        }
-        tc::cp_async_wait<0>();
-        tc::fence_proxy_async_smem();
-        for (int kb = nkb - 2 < 0 ? 0 : nkb - 2; kb < nkb; ++kb)
-            mbar_arrive(full0 + 8 * (kb % kStages));
-
         // Epilogue: this warp reads TMEM lanes 32*(warp%4) .. +31.
-        ok = mbar_wait_bounded(done, 0, p.status, kDevTimeoutMma) && ok;
+        ok = mbar_wait_bounded(done, 0, p.status, kDevTimeoutMma);
         ok = __all_sync(0xffffffffu, ok);   // warp converged and agreed before tcgen05.ld
         tc::fence_after_sync();
         const int row = 32 * (warp & 3) + lane;
@@ -189,11 +171,10 @@ __global__ void __launch_bounds__(kShrinkThreads, 1) k_shrink_tc(const __grid_co
             tc::tmem_ld16(tmem + (uint32_t(32 * (warp & 3)) << 16) + uint32_t(16 * c16), v);
             if (!ok)
                 continue;
-            if (nkb == 0) {   // this CTA's share of K is empty: its partial is zero
 #pragma unroll
-                for (int e = 0; e < 16; ++e)
+            for (int e = 0; e < 16; ++e)   // an empty K share, or a padded rank column
+                if (nkb == 0 || 16 * c16 + e >= r)
                     v[e] = 0.f;
-            }
             if (p.vmode == 0) {
                 // fp32 partial, row-major with row stride rp, in this CTA's slot
                 float *dst = p.vparts + size_t(blockIdx.x) * (kVPartBytes / 4) + size_t(row) * rp +
@@ -233,7 +214,9 @@ cudaError_t launch_shrink_tc(const TileParams &p, cudaStream_t stream)
     TileArgs args;
     args.p = p;
     if (!encode_bf16_2d(&args.map, p.x, uint64_t(p.d_in), uint64_t(p.n_rows), uint64_t(p.ldx) * 2u,
-                        kKB, kTM, true))
+                        kKB, kTM, true) ||
+        !encode_bf16_2d(&args.amap, p.a_pool, uint64_t(p.d_in), uint64_t(p.a_n_pages),
+                        uint64_t(p.a_pw) * 2u, kKB, 1, true))
         return cudaErrorInvalidValue;
     static bool configured = false;
     if (!configured) {
