@@ -74,6 +74,9 @@ struct lora_ctx {
     int force_rows = 0;             // > 0 while tuning: rows per item
     uint8_t *vparts = nullptr;      // fused tile path: partial V between its two kernels
     size_t vparts_cap = 0;
+    uint8_t *dense = nullptr;       // dense adapter rows of a call (dense.cu)
+    size_t dense_cap = 0;
+    std::vector<int32_t> slot_of;   // adapter -> slot while a call's slots are assigned
 };
 
 struct lora_table {
@@ -87,6 +90,7 @@ struct lora_table {
     std::vector<int32_t> rank, a_pages, b_pages;
     std::vector<float> scale;
     std::vector<int8_t> status;        // per adapter: LORA_OK or the error a reference gets
+    std::vector<uint8_t> a_contig, b_contig;   // per adapter: pages j < rank are p0 + j
     int32_t *d_rank = nullptr, *d_a_pages = nullptr, *d_b_pages = nullptr;
     float *d_scale = nullptr;
 };
@@ -378,6 +382,105 @@ int tile_min_run(const lora_ctx *ctx, int64_t n_act, int d_in, int d_out, int ra
     return 128;
 }
 
+// Row matrices of a tensor-core call over n_slots adapters (dense.cu): the pools
+// when every adapter's pages are consecutive and its rank a multiple of 16 (no
+// padding rows to zero), else a dense copy with one rp-row slot per adapter.
+struct RowMats {
+    const uint16_t *a = nullptr, *b = nullptr;
+    int64_t a_ld = 0, a_nrows = 0, b_ld = 0, b_nrows = 0;
+    bool staged = false;
+    int rp = 0;
+};
+
+int setup_rows(lora_ctx *ctx, const lora_table *t, const int32_t *adapters, int n_slots,
+               int d_in, int d_out, bool need_a, bool need_b, const NoAllocScratch *fixed,
+               cudaStream_t stream, RowMats *m, int32_t *a_base, int32_t *b_base)
+{
+    bool direct = true;
+    int rmax = 0;
+    for (int s = 0; s < n_slots; ++s) {
+        const size_t k = size_t(adapters[s]);
+        rmax = std::max(rmax, t->rank[k]);
+        if ((t->rank[k] % 16) != 0 || (need_a && !t->a_contig[k]) || (need_b && !t->b_contig[k]))
+            direct = false;
+    }
+    if (direct) {
+        m->a = t->a_pool;
+        m->a_ld = t->a_pw;
+        m->a_nrows = t->a_n_pages;
+        m->b = t->b_pool;
+        m->b_ld = t->b_pw;
+        m->b_nrows = t->b_n_pages;
+        for (int s = 0; s < n_slots; ++s) {
+            a_base[s] = t->a_pages[size_t(adapters[s]) * t->max_rank];
+            b_base[s] = t->b_pages[size_t(adapters[s]) * t->max_rank];
+        }
+        return LORA_OK;
+    }
+    const int rp = (rmax + 15) & ~15;
+    const size_t a_bytes = need_a ? (size_t(n_slots) * rp * size_t(d_in) * 2u + 255u) & ~size_t(255) : 0;
+    const size_t bytes = a_bytes + (need_b ? size_t(n_slots) * rp * size_t(d_out) * 2u : 0);
+    uint8_t *buf = nullptr;
+    if (fixed) {
+        if (bytes > kNoAllocDenseBytes)
+            return LORA_E_CAPACITY;
+        buf = reinterpret_cast<uint8_t *>(fixed->dense);
+    } else {
+        if (bytes > ctx->dense_cap) {
+            // Grows to the largest need seen; later calls reuse it.
+            if (ctx->dense) {
+                CUDA_TRY(ctx, cudaStreamSynchronize(stream));
+                cudaFree(ctx->dense);
+                ctx->dense = nullptr;
+                ctx->dense_cap = 0;
+            }
+            if (cudaMalloc(reinterpret_cast<void **>(&ctx->dense), bytes) != cudaSuccess)
+                return LORA_E_NOMEM;
+            ctx->dense_cap = bytes;
+        }
+        buf = ctx->dense;
+    }
+    m->staged = true;
+    m->rp = rp;
+    m->a = reinterpret_cast<const uint16_t *>(buf);
+    m->a_ld = d_in;
+    m->a_nrows = int64_t(n_slots) * rp;
+    m->b = reinterpret_cast<const uint16_t *>(buf + a_bytes);
+    m->b_ld = d_out;
+    m->b_nrows = int64_t(n_slots) * rp;
+    for (int s = 0; s < n_slots; ++s)
+        a_base[s] = b_base[s] = s * rp;
+    return LORA_OK;
+}
+
+// The copies setup_rows asked for (a no-op for the pools themselves).
+int run_staging(lora_ctx *ctx, const lora_table *t, const RowMats &m, const int32_t *adapters,
+                int n_slots, int d_in, int d_out, bool need_a, bool need_b, cudaStream_t stream)
+{
+    if (!m.staged)
+        return LORA_OK;
+    for (int s0 = 0; s0 < n_slots; s0 += kStageSlots) {
+        StageArgs sa{};
+        sa.max_rank = t->max_rank;
+        sa.rp = m.rp;
+        sa.n_slots = std::min(kStageSlots, n_slots - s0);
+        for (int s = 0; s < sa.n_slots; ++s) {
+            sa.adapter[s] = adapters[s0 + s];
+            sa.rank[s] = t->rank[size_t(adapters[s0 + s])];
+        }
+        if (need_a)
+            sa.side[0] = StageSide{t->a_pool, t->a_pw, t->d_a_pages,
+                                   const_cast<uint16_t *>(m.a) + int64_t(s0) * m.rp * d_in, d_in};
+        if (need_b)
+            sa.side[1] = StageSide{t->b_pool, t->b_pw, t->d_b_pages,
+                                   const_cast<uint16_t *>(m.b) + int64_t(s0) * m.rp * d_out, d_out};
+        CUDA_TRY(ctx, launch_stage_rows(sa, stream));
+        ctx->last_launches += 1;
+        ctx->launches_total += 1;
+    }
+    return LORA_OK;
+}
+
 int run_tiles(lora_ctx *ctx, const lora_table *t, int mode, const void *x, int64_t ldx, int d_in,
               float *v, int64_t ldv, void *y, int64_t ldy, int d_out, int64_t n,
               cudaStream_t stream, const NoAllocScratch *fixed = nullptr)
@@ -385,9 +488,35 @@ int run_tiles(lora_ctx *ctx, const lora_table *t, int mode, const void *x, int64
     Plan &pl = ctx->plan;
     if (pl.tile_items.empty())
         return LORA_OK;
+    // The call's adapters (slots, in order of first tile) and their row matrices.
+    const bool need_a = mode != kExpand, need_b = mode != kShrink;
+    if (ctx->slot_of.size() < size_t(t->n_adapters))
+        ctx->slot_of.resize(size_t(t->n_adapters), -1);
+    std::vector<int32_t> &slots = pl.slot_adapter;
+    slots.clear();
+    for (const TileItem &it : pl.tile_items)
+        if (ctx->slot_of[size_t(it.adapter)] < 0) {
+            ctx->slot_of[size_t(it.adapter)] = int32_t(slots.size());
+            slots.push_back(it.adapter);
+        }
+    const int n_slots = int(slots.size());
+    pl.slot_a_base.resize(slots.size());
+    pl.slot_b_base.resize(slots.size());
+    RowMats mats;
+    int rc = setup_rows(ctx, t, slots.data(), n_slots, d_in, d_out, need_a, need_b, fixed, stream,
+                        &mats, pl.slot_a_base.data(), pl.slot_b_base.data());
+    if (rc == LORA_OK)
+        for (TileItem &it : pl.tile_items) {
+            const int32_t sidx = ctx->slot_of[size_t(it.adapter)];
+            it.a_row = pl.slot_a_base[size_t(sidx)];
+            it.b_row = pl.slot_b_base[size_t(sidx)];
+        }
+    for (int32_t k : slots)
+        ctx->slot_of[size_t(k)] = -1;
+    if (rc != LORA_OK)
+        return rc;
     const size_t items_bytes = pl.tile_items.size() * sizeof(TileItem);
     Slot *slot = nullptr;
-    int rc = LORA_OK;
     const TileItem *d_items = nullptr;
     if (fixed) {
         CUDA_TRY(ctx, noalloc_put_items(pl.tile_items.data(), int(pl.tile_items.size()), stream));
@@ -429,14 +558,12 @@ int run_tiles(lora_ctx *ctx, const lora_table *t, int mode, const void *x, int64
     p.ldx = ldx;
     p.y = static_cast<uint16_t *>(y);
     p.ldy = ldy;
-    p.a_pool = t->a_pool;
-    p.a_pw = t->a_pw;
-    p.b_pool = t->b_pool;
-    p.b_pw = t->b_pw;
-    p.a_n_pages = t->a_n_pages;
-    p.b_n_pages = t->b_n_pages;
-    p.a_pages = t->d_a_pages;
-    p.b_pages = t->d_b_pages;
+    p.a_rows = mats.a;
+    p.a_ld = mats.a_ld;
+    p.a_nrows = mats.a_nrows;
+    p.b_rows = mats.b;
+    p.b_ld = mats.b_ld;
+    p.b_nrows = mats.b_nrows;
     p.items = d_items;
     p.vparts = fixed ? fixed->vparts : reinterpret_cast<float *>(ctx->vparts);
     p.ksplit = ksplit;
@@ -450,8 +577,12 @@ int run_tiles(lora_ctx *ctx, const lora_table *t, int mode, const void *x, int64
     p.n_items = int(pl.tile_items.size());
     p.vmode = mode == kFused ? 0 : 1;
     p.max_tile_rank = pl.tile_max_rank;
+    // The dense copy (if any) is timed with the kernel that first reads it.
     if (mode != kExpand) {
         const long ev = prof_start(ctx, 1, stream);
+        rc = run_staging(ctx, t, mats, slots.data(), n_slots, d_in, d_out, need_a, need_b, stream);
+        if (rc != LORA_OK)
+            return rc;
         CUDA_TRY(ctx, launch_shrink_tc(p, stream));
         prof_stop(ctx, ev, stream);
         ctx->last_launches += 1;
@@ -459,6 +590,11 @@ int run_tiles(lora_ctx *ctx, const lora_table *t, int mode, const void *x, int64
     }
     if (mode != kShrink) {
         const long ev = prof_start(ctx, 3, stream);
+        if (mode == kExpand) {
+            rc = run_staging(ctx, t, mats, slots.data(), n_slots, d_in, d_out, need_a, need_b, stream);
+            if (rc != LORA_OK)
+                return rc;
+        }
         CUDA_TRY(ctx, launch_expand_tc(p, stream));
         prof_stop(ctx, ev, stream);
         ctx->last_launches += 1;
@@ -558,14 +694,32 @@ int merge_call(lora_ctx *ctx, const lora_table *t, int adapter, void *W, int64_t
     if (path == 0 && ctx->tiles.lookup(TileKey{kKindMerge, pow2_bucket(d_in), d_in, d_out, p.rank},
                                        tcfg))
         path = tcfg[0];
+    const bool tc = merge_tc_supported(d_in, d_out, p.rank) && path != 1;
+    RowMats mats;
+    if (tc) {
+        rc = setup_rows(ctx, t, &adapter, 1, d_in, d_out, true, true, nullptr, stream, &mats,
+                        &p.a_row, &p.b_row);
+        if (rc != LORA_OK)
+            return rc;
+        p.a_rows = mats.a;
+        p.a_ld = mats.a_ld;
+        p.a_nrows = mats.a_nrows;
+        p.b_rows = mats.b;
+        p.b_ld = mats.b_ld;
+        p.b_nrows = mats.b_nrows;
+    }
     const long ev = prof_start(ctx, 2, stream);
-    if (merge_tc_supported(d_in, d_out, p.rank) && path != 1)
+    if (tc) {
+        rc = run_staging(ctx, t, mats, &adapter, 1, d_in, d_out, true, true, stream);
+        if (rc != LORA_OK)
+            return rc;
         CUDA_TRY(ctx, launch_merge_tc(p, 0, stream));
-    else
+    } else {
         CUDA_TRY(ctx, launch_merge_simt(p, stream));
+    }
     prof_stop(ctx, ev, stream);
     ctx->last_path = 4;
-    ctx->last_launches = 1;
+    ctx->last_launches += 1;
     ctx->launches_total += 1;
     return LORA_OK;
 }
@@ -688,6 +842,8 @@ int lora_ctx_destroy(lora_ctx *ctx)
         cudaFree(ctx->d_status);
     if (ctx->vparts)
         cudaFree(ctx->vparts);
+    if (ctx->dense)
+        cudaFree(ctx->dense);
     cudaSetDevice(prev);
     delete ctx;
     return LORA_OK;
@@ -730,8 +886,21 @@ int lora_table_create(lora_ctx *ctx, const void *a_pool, int64_t a_n_pages, int 
         ctx->plan.count.reserve(size_t(n_adapters));
         ctx->plan.cursor.reserve(size_t(n_adapters));
     }
-    for (int k = 0; k < n_adapters; ++k)
+    t->a_contig.assign(size_t(n_adapters), 0);
+    t->b_contig.assign(size_t(n_adapters), 0);
+    for (int k = 0; k < n_adapters; ++k) {
         t->status[size_t(k)] = adapter_status(t, k);
+        if (t->status[size_t(k)] != LORA_OK)
+            continue;
+        const int32_t *pa = &t->a_pages[size_t(k) * max_rank], *pb = &t->b_pages[size_t(k) * max_rank];
+        bool ca = true, cb = true;
+        for (int j = 1; j < t->rank[size_t(k)]; ++j) {
+            ca = ca && pa[j] == pa[0] + j;
+            cb = cb && pb[j] == pb[0] + j;
+        }
+        t->a_contig[size_t(k)] = ca;
+        t->b_contig[size_t(k)] = cb;
+    }
     // Device copies; pages of adapters that cannot be used are zeroed so that no
     // kernel could ever form an address from them.
     if (ctx->device < 0) {

@@ -1,0 +1,57 @@
+// Dense adapter rows for the tensor-core kernels.
+//
+// The tile shrink, the streaming expand and the merge read an adapter block per K
+// block / column chunk.  From a row matrix in which the adapter's pages are
+// consecutive rows, that block is one TMA box (or three: 64 + 32 + 16 rows); page
+// by page it would be one gather per four pages, and the TMA unit issues those
+// too slowly to keep up with the x / y streams.  When every adapter of a call has
+// consecutive pages of a rank that is a multiple of 16, the pools are used as they
+// are.  Otherwise this kernel copies the call's adapters (S-LoRA's unified pool
+// holds them in arbitrary pages) into a dense scratch, one slot of rp rows per
+// adapter, the rows beyond its rank zero.
+#include <cuda_runtime.h>
+
+#include "internal.h"
+
+namespace lora {
+
+namespace {
+
+constexpr int kStageThreads = 128;
+
+// One CTA per destination row: blockIdx.x = slot * rp + j, blockIdx.y = side.
+__global__ void __launch_bounds__(kStageThreads) k_stage_rows(const __grid_constant__ StageArgs a)
+{
+    const StageSide &sd = a.side[blockIdx.y];
+    if (!sd.dst)
+        return;
+    const int row = int(blockIdx.x);
+    const int slot = row / a.rp, j = row - slot * a.rp;
+    const int nv = sd.width / 8;
+    uint4 *dst = reinterpret_cast<uint4 *>(sd.dst + int64_t(row) * sd.width);
+    if (j < a.rank[slot]) {
+        const int32_t page = sd.pages[int64_t(a.adapter[slot]) * a.max_rank + j];
+        const uint4 *src = reinterpret_cast<const uint4 *>(sd.pool + int64_t(page) * sd.pw);
+        for (int q = threadIdx.x; q < nv; q += kStageThreads)
+            dst[q] = src[q];
+    } else {
+        const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+        for (int q = threadIdx.x; q < nv; q += kStageThreads)
+            dst[q] = z;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_stage_rows(const StageArgs &a, cudaStream_t stream)
+{
+    if (a.n_slots <= 0 || a.n_slots > kStageSlots || a.rp <= 0)
+        return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(a.n_slots * a.rp), 2u);
+    cfg.blockDim = dim3(kStageThreads);
+    cfg.stream = stream;
+    return cudaLaunchKernelEx(&cfg, k_stage_rows, a);
+}
+
+}  // namespace lora

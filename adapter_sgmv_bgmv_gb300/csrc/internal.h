@@ -25,8 +25,11 @@ struct TileItem {
     int16_t nrows;
     int16_t rank;
     float scale;
+    int32_t a_row;            // row of page 0 of A_k in the A row matrix (pages j: a_row + j)
+    int32_t b_row;            // row of page 0 of B_k in the B row matrix
+    int32_t pad[2];
 };
-static_assert(sizeof(TileItem) == 16, "TileItem is one 16-byte load");
+static_assert(sizeof(TileItem) == 32, "TileItem is two 16-byte loads");
 
 enum Mode : int { kShrink = 0, kExpand = 1, kFused = 2 };
 
@@ -92,14 +95,16 @@ struct TileParams {
     int64_t ldx;
     uint16_t *y;
     int64_t ldy;
-    const uint16_t *a_pool;
-    int64_t a_pw;
-    const uint16_t *b_pool;
-    int64_t b_pw;
-    int64_t a_n_pages;        // rows of the A pool (tensor-map extent of the page gather)
-    int64_t b_n_pages;        // rows of the B pool
-    const int32_t *a_pages;
-    const int32_t *b_pages;
+    // Row matrices of the adapters' pages: row a_row + j holds page j of A_k (its
+    // first d_in elements are read), row b_row + j page j of B_k (first d_out).
+    // Either the pools themselves (every adapter's pages consecutive) or a dense
+    // copy made for the call, rank-padded with zero rows.
+    const uint16_t *a_rows;
+    int64_t a_ld;             // row stride, elements
+    int64_t a_nrows;          // rows (tensor-map extent)
+    const uint16_t *b_rows;
+    int64_t b_ld;
+    int64_t b_nrows;
     const TileItem *items;
     float *vparts;            // fused: [n_items][ksplit] partial V slots
     float *v;                 // shrink / expand only: fp32 rows [n, ldv]
@@ -117,12 +122,34 @@ struct TileParams {
 // Fixed scratch of lora_fused_noalloc (noalloc.cu): device addresses of the
 // file-scope arrays on one device, looked up once per device.
 constexpr int kNoAllocSlots = 64;
+constexpr size_t kNoAllocDenseBytes = size_t(8) << 20;
 struct NoAllocScratch {
     float *vparts;            // kNoAllocSlots slots of kVPartBytes
     TileItem *items;          // kNoAllocSlots entries
+    uint16_t *dense;          // kNoAllocDenseBytes of dense adapter rows
 };
 int noalloc_scratch(int device, NoAllocScratch *out);
 cudaError_t noalloc_put_items(const TileItem *items, int n, cudaStream_t stream);
+
+// Dense adapter rows (dense.cu): for slot s and j < rp, row s*rp + j of dst gets
+// the first `width` elements of page j of the slot's adapter, zeros for j >= rank.
+constexpr int kStageSlots = 128;           // slots per launch
+struct StageSide {
+    const uint16_t *pool;
+    int64_t pw;
+    const int32_t *pages;     // device page table [n_adapters * max_rank]
+    uint16_t *dst;            // [n_slots * rp][width]
+    int width;
+};
+struct StageArgs {
+    StageSide side[2];        // A, B (side with dst == nullptr skipped)
+    int max_rank;
+    int rp;
+    int n_slots;
+    int32_t adapter[kStageSlots];
+    int32_t rank[kStageSlots];
+};
+cudaError_t launch_stage_rows(const StageArgs &a, cudaStream_t stream);
 
 cudaError_t launch_shrink_tc(const TileParams &p, cudaStream_t stream);
 cudaError_t launch_expand_tc(const TileParams &p, cudaStream_t stream);
@@ -139,6 +166,12 @@ struct MergeParams {
     int64_t b_n_pages;        // rows of the B pool (tensor-map extent of the page gather)
     const int32_t *a_pages;   // host-resolved page ids of this adapter, device copy
     const int32_t *b_pages;
+    // Row matrices as in TileParams (tensor-core merge), with this adapter's rows.
+    const uint16_t *a_rows;
+    int64_t a_ld, a_nrows;
+    const uint16_t *b_rows;
+    int64_t b_ld, b_nrows;
+    int32_t a_row, b_row;
     unsigned *status;
     int d_in;
     int d_out;

@@ -12,9 +12,11 @@ namespace lora {
 
 namespace {
 
-// 64 slots of one tile-part each: 64 x 64 KB = 4 MB of partial V, plus the list.
+// 64 slots of one tile-part each: 64 x 64 KB = 4 MB of partial V, the list, and
+// 8 MB for the dense adapter rows of a call whose adapters need copying.
 static __device__ __align__(256) float g_noalloc_vparts[kNoAllocSlots * (kVPartBytes / 4)];
 static __device__ __align__(256) TileItem g_noalloc_items[kNoAllocSlots];
+static __device__ __align__(256) uint16_t g_noalloc_dense[kNoAllocDenseBytes / 2];
 
 struct ItemsArg {
     TileItem items[kNoAllocSlots];
@@ -49,15 +51,17 @@ int noalloc_scratch(int device, NoAllocScratch *out)
             return -1;
         if (prev != device && cudaSetDevice(device) != cudaSuccess)
             return -1;
-        void *v = nullptr, *it = nullptr;
+        void *v = nullptr, *it = nullptr, *dn = nullptr;
         const cudaError_t e1 = cudaGetSymbolAddress(&v, g_noalloc_vparts);
         const cudaError_t e2 = cudaGetSymbolAddress(&it, g_noalloc_items);
+        const cudaError_t e3 = cudaGetSymbolAddress(&dn, g_noalloc_dense);
         if (prev != device)
             cudaSetDevice(prev);
-        if (e1 != cudaSuccess || e2 != cudaSuccess || !v || !it)
+        if (e1 != cudaSuccess || e2 != cudaSuccess || e3 != cudaSuccess || !v || !it || !dn)
             return -1;
         g_scratch[device].vparts = static_cast<float *>(v);
         g_scratch[device].items = static_cast<TileItem *>(it);
+        g_scratch[device].dense = static_cast<uint16_t *>(dn);
         g_ready[device] = true;
     }
     *out = g_scratch[device];

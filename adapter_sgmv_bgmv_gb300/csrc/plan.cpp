@@ -88,7 +88,7 @@ void plan_items(Plan &pl, const int32_t *rank, const float *scale, int rows_per_
                     for (int32_t p = q; p < t; p += 128) {
                         const int32_t m = std::min(128, t - p);
                         pl.tile_items.push_back(
-                            TileItem{k, pl.perm[size_t(p)], int16_t(m), int16_t(r), scale[k]});
+                            TileItem{k, pl.perm[size_t(p)], int16_t(m), int16_t(r), scale[k], -1, -1, {0, 0}});
                         pl.tile_active += m;
                     }
                     pl.tile_max_rank = std::max(pl.tile_max_rank, r);

@@ -16,6 +16,9 @@ struct Plan {
     std::vector<RowItem> row_items;    // p0 indexes row_perm
     std::vector<int32_t> row_perm;     // the perm entries of the row items only
     std::vector<TileItem> tile_items;
+    std::vector<int32_t> slot_adapter; // the tile items' adapters, in order of first tile
+    std::vector<int32_t> slot_a_base;  // first row of each slot in the A / B row matrices
+    std::vector<int32_t> slot_b_base;
     std::vector<int32_t> count;        // scratch, [n_adapters]
     std::vector<int32_t> cursor;       // scratch, [n_adapters]
     int32_t max_seg_len = 0;

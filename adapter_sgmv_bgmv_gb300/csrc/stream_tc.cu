@@ -15,21 +15,25 @@
 // crosses a block boundary now and then.  Per CTA:
 //   - warp 0 (producer) fills a ring of NS stages by TMA alone: per chunk the
 //     128 x 128 y / W tile (two 64-column boxes, 128-byte swizzle) and B_k's r x 128
-//     block, gathered four pages at a time (tile::gather4) straight into the MMA's
-//     N-major swizzled layout, all counted on the stage's one barrier -- so the
-//     producer never waits on its own copies;
+//     block from the B row matrix (dense.cu: pages as consecutive rows; per 64-column
+//     half one to three boxes of 64 / 32 / 16 rows, landing in the MMA's N-major
+//     swizzled layout), all counted on the stage's one barrier -- so the producer
+//     never waits on its own copies;
 //   - warp 1 (MMA) issues M = 128, N = 128, K = r MMAs per chunk into one of two
 //     TMEM accumulators, so the MMAs of chunk i + 1 overlap the epilogue of chunk i;
 //   - warps 2-9 (epilogue) stage the left operand each time the CTA enters a block
 //     -- V as the in-order sum of the shrink's fp32 partials or from the caller's
 //     fp32 rows, split into bf16 hi = bf16(v) and lo = bf16(v - hi) (about 16
-//     significant bits; the MMAs run on both), or A_k's 128 x r slice from the pages
-//     (M-major) -- then per chunk read the accumulator (warp w: TMEM lanes
+//     significant bits; the MMAs run on both), or A_k's 128 x r slice (M-major; one
+//     thread loads it by TMA from the A row matrix) -- then per chunk read the
+//     accumulator (warp w: TMEM lanes
 //     32*(w%4).., one 64-column half; both TMEM loads in flight before one wait),
-//     add s * acc to the tile in shared memory and store it: whole 128-row boxes by
-//     TMA when every row belongs to the block, else 8-row boxes (one swizzle atom
-//     each) over the block's rows and the last < 8 rows by the epilogue threads.
-//     A stage is released as soon as its store has read shared memory.
+//     add s * acc to its own row of the tile in shared memory (and store that row
+//     itself if it is one of a ragged block's last < 8 rows), then arrive on the
+//     stage's "tile ready" barrier -- no barrier among the epilogue warps per chunk;
+//   - warp 10 (store) stores each ready tile by TMA -- whole 128-row boxes when
+//     every row belongs to the block, else 8-row boxes (one swizzle atom each) --
+//     and hands the stage back to the producer as soon as the store has read it.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -45,19 +49,19 @@ namespace {
 
 constexpr int kTM = 128;
 constexpr int kBN = 128;
-constexpr int kThreads = 320;                 // producer, MMA, 8 epilogue warps
+constexpr int kThreads = 352;                 // producer, MMA, 8 epilogue warps, store
 constexpr int kEpi = 256;
 constexpr uint32_t kBox = kTM * 128;          // one 64-column TMA box of 128 rows
 constexpr uint32_t kTile = 2 * kBox;          // 128 x 128 bf16
 constexpr int kMaxStages = 4;
-constexpr int kMaxRank = 128;                 // page-id slots per operand
 
 enum Left : int { kLeftVParts = 0, kLeftVRows = 1, kLeftAPages = 2 };
 
 struct StreamArgs {
     CUtensorMap map;                          // y (expand) or W (merge), 128-row boxes
     CUtensorMap map8;                         // the same tensor, 8-row boxes
-    CUtensorMap bmap;                         // the B pool, rows = pages, 64 x 1 boxes
+    CUtensorMap bmap[3];                      // the B row matrix, 64 x 16 / 32 / 64 boxes
+    CUtensorMap amap[3];                      // merge: the A row matrix, same boxes
     TileParams p;                             // expand: items; merge: unused fields
     MergeParams m;                            // merge only
     int left;
@@ -71,7 +75,7 @@ struct StreamArgs {
 __host__ __device__ inline int rank_pad16(int r) { return (r + 15) & ~15; }
 __host__ __device__ inline int v_atoms(int rp) { return (rp + 63) / 64; }
 
-// Shared memory: [left operand][stage s: B | tile] x NS [barriers][page ids of B, of A]
+// Shared memory: [left operand][stage s: B | tile] x NS [barriers]
 __host__ __device__ inline uint32_t left_bytes(int left, int rp)
 {
     return left == kLeftAPages ? uint32_t(rp) * kTM * 2u               // A: rp x 128, M-major
@@ -82,7 +86,7 @@ __host__ __device__ inline uint32_t stage_bytes(int rp) { return uint32_t(rp) * 
 
 __host__ __device__ inline uint32_t stream_smem_bytes(int left, int rp, int stages)
 {
-    return 1024u + left_bytes(left, rp) + uint32_t(stages) * stage_bytes(rp) + 128u + 1024u;
+    return 1024u + left_bytes(left, rp) + uint32_t(stages) * stage_bytes(rp) + 192u;   // + barriers
 }
 
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads)
@@ -94,7 +98,7 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads)
 struct Block {
     int r, rp, row0, nrows;
     float scale;
-    const int32_t *b_pages;
+    int a_row, b_row;                         // first rows in the A / B row matrices
 };
 
 __device__ __forceinline__ Block block_info(const StreamArgs &a, int blk)
@@ -105,14 +109,16 @@ __device__ __forceinline__ Block block_info(const StreamArgs &a, int blk)
         b.row0 = blk * kTM;
         b.nrows = min(kTM, a.m.d_in - b.row0);
         b.scale = a.m.scale;
-        b.b_pages = a.m.b_pages;
+        b.a_row = a.m.a_row;
+        b.b_row = a.m.b_row;
     } else {
         const TileItem it = a.p.items[blk];
         b.r = it.rank;
         b.row0 = it.row0;
         b.nrows = it.nrows;
         b.scale = it.scale;
-        b.b_pages = a.p.b_pages + size_t(it.adapter) * a.p.max_rank;
+        b.a_row = it.a_row;
+        b.b_row = it.b_row;
     }
     b.rp = rank_pad16(b.r);
     return b;
@@ -138,15 +144,11 @@ __global__ void __launch_bounds__(kThreads) k_stream_tc(const __grid_constant__ 
     const uint32_t sL = base;
     const uint32_t sStage0 = sL + left_bytes(a.left, a.rp_max);
     const uint32_t sBar = sStage0 + uint32_t(NS) * stage_bytes(a.rp_max);
-    // barriers: left, full[4], empty[4], tfull[2], tempty[2]
+    // barriers: left, full[4], empty[4], tready[4], tfull[2], tempty[2]
     const uint32_t bar_left = sBar;
-    const uint32_t full0 = sBar + 8, empty0 = sBar + 40;
-    const uint32_t tfull0 = sBar + 72, tempty0 = sBar + 88;
-    const uint32_t tmem_slot = sBar + 104;
-    // The current block's page ids, read once per block: a page id loaded per copy
-    // would put a dependent global load in front of every cp.async.
-    int32_t *s_bpg = reinterpret_cast<int32_t *>(gbase + (sBar + 128u - base));
-    int32_t *s_apg = s_bpg + kMaxRank;
+    const uint32_t full0 = sBar + 8, empty0 = sBar + 40, tready0 = sBar + 72;
+    const uint32_t tfull0 = sBar + 104, tempty0 = sBar + 120;
+    const uint32_t tmem_slot = sBar + 136;
     auto stage_b = [&](int i) { return sStage0 + uint32_t(i % NS) * stage_bytes(a.rp_max); };
     auto stage_t = [&](int i) { return stage_b(i) + uint32_t(a.rp_max) * kBN * 2u; };
 
@@ -155,6 +157,7 @@ __global__ void __launch_bounds__(kThreads) k_stream_tc(const __grid_constant__ 
         for (int s = 0; s < NS; ++s) {
             mbar_init(full0 + 8 * s, 1);       // producer's expect-tx; tile + B bytes
             mbar_init(empty0 + 8 * s, 1);      // the stage's store has read it
+            mbar_init(tready0 + 8 * s, kEpi / 32);   // one arrive per epilogue warp
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(tfull0 + 8 * b, 1);      // MMA commit
@@ -162,8 +165,6 @@ __global__ void __launch_bounds__(kThreads) k_stream_tc(const __grid_constant__ 
         }
         fence_mbar_init();
     }
-    if (merge && tid < a.m.rank)       // one adapter for the whole launch
-        s_apg[tid] = a.m.a_pages[tid];
     if (warp == 1)
         tc::tmem_alloc(tmem_slot, 2 * kBN);
     tc::fence_before_sync();
@@ -174,48 +175,39 @@ __global__ void __launch_bounds__(kThreads) k_stream_tc(const __grid_constant__ 
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
-        // Rank padding (rows r..rp-1 of B) repeats page 0: it meets zero columns of
-        // the left operand.  A 64-column half of B that lies wholly right of d_out
-        // is not gathered; its accumulator columns are never stored.
-        int cur_blk = -1;
-        Block bk{};
-        for (int i = 0; i < nch; ++i) {
-            const int s = i % NS, u = i / NS;
-            if (u > 0)
-                ok = mbar_wait_bounded(empty0 + 8 * s, uint32_t((u - 1) & 1), status,
-                                       kDevTimeoutPipe) && ok;
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok)
-                break;
-            const int g = g0 + i, blk = g / a.n_chunks;
-            if (blk != cur_blk) {
-                bk = block_info(a, blk);
-                cur_blk = blk;
-                // gathers already issued took their page ids when issued
-                for (int j = lane; j < bk.rp; j += 32)
-                    s_bpg[j] = bk.b_pages[j < bk.r ? j : 0];
-                __syncwarp();
-            }
-            const int n0 = (g - blk * a.n_chunks) * kBN;
-            const int halves = n0 + 64 < d_out ? 2 : 1;
-            if (lane == 0) {
+        // A 64-column half of B that lies wholly right of d_out is not loaded; its
+        // accumulator columns are never stored.
+        if (lane == 0) {
+            int cur_blk = -1;
+            Block bk{};
+            for (int i = 0; i < nch && ok; ++i) {
+                const int s = i % NS, u = i / NS;
+                if (u > 0)
+                    ok = mbar_wait_bounded(empty0 + 8 * s, uint32_t((u - 1) & 1), status,
+                                           kDevTimeoutPipe);
+                if (!ok)
+                    break;
+                const int g = g0 + i, blk = g / a.n_chunks;
+                if (blk != cur_blk) {
+                    bk = block_info(a, blk);
+                    cur_blk = blk;
+                }
+                const int n0 = (g - blk * a.n_chunks) * kBN;
+                const int halves = n0 + 64 < d_out ? 2 : 1;
                 mbar_arrive_expect_tx(full0 + 8 * s,
                                       kTile + uint32_t(halves) * uint32_t(bk.rp) * 128u);
                 tc::tma_load_2d(stage_t(i), &a.map, n0, bk.row0, full0 + 8 * s);
                 tc::tma_load_2d(stage_t(i) + kBox, &a.map, n0 + 64, bk.row0, full0 + 8 * s);
-            }
-            __syncwarp();
-            const uint32_t sb = stage_b(i);
-            const uint32_t lbo_b = uint32_t(bk.rp / 8) * 1024u;   // N-atom stride of B
-            const int quads = bk.rp / 4;
-            for (int q = lane; q < halves * quads; q += 32) {
-                const int h = q / quads, j = 4 * (q - h * quads);
-                tc::tma_gather4(sb + uint32_t(h) * lbo_b + uint32_t(j >> 3) * 1024u +
-                                    uint32_t(j & 7) * 128u,
-                                &a.bmap, n0 + 64 * h, s_bpg[j], s_bpg[j + 1], s_bpg[j + 2],
-                                s_bpg[j + 3], full0 + 8 * s);
+                const uint32_t sb = stage_b(i);
+                const uint32_t lbo_b = uint32_t(bk.rp) * 128u;   // N-atom stride of B
+                for (int h = 0; h < halves; ++h)
+                    tc::for_row_boxes(bk.rp, [&](int off, int m) {
+                        tc::tma_load_2d(sb + uint32_t(h) * lbo_b + uint32_t(off) * 128u,
+                                        &a.bmap[m], n0 + 64 * h, bk.b_row + off, full0 + 8 * s);
+                    });
             }
         }
+        __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
@@ -262,11 +254,50 @@ __global__ void __launch_bounds__(kThreads) k_stream_tc(const __grid_constant__ 
             }
         }
         __syncwarp();
+    } else if (warp == 10) {
+        // ------------------------------------------------------------ store
+        if (lane == 0) {
+            int cur_blk = -1;
+            Block bk{};
+            for (int i = 0; i < nch && ok; ++i) {
+                const int s = i % NS;
+                ok = mbar_wait_bounded(tready0 + 8 * s, uint32_t((i / NS) & 1), status,
+                                       kDevTimeoutPipe);
+                if (!ok)
+                    break;
+                const int g = g0 + i, blk = g / a.n_chunks;
+                if (blk != cur_blk) {
+                    bk = block_info(a, blk);
+                    cur_blk = blk;
+                }
+                const int n0 = (g - blk * a.n_chunks) * kBN;
+                const bool full_rows = merge || bk.nrows == kTM;
+                const int rows8 = full_rows ? kTM : (bk.nrows & ~7);
+                const uint32_t st = stage_t(i);
+                for (int h = 0; h < 2; ++h) {
+                    if (h == 1 && n0 + 64 >= d_out)   // a box wholly right of the matrix
+                        break;
+                    const uint32_t src = st + uint32_t(h) * kBox;
+                    if (full_rows)
+                        tc::tma_store_2d(&a.map, n0 + 64 * h, bk.row0, src);
+                    else
+                        for (int r8 = 0; r8 < rows8; r8 += 8)
+                            tc::tma_store_2d(&a.map8, n0 + 64 * h, bk.row0 + r8,
+                                             src + uint32_t(r8) * 128u);
+                }
+                tc::bulk_commit();
+                tc::bulk_wait_read0();
+                mbar_arrive(empty0 + 8 * s);
+            }
+            tc::bulk_wait0();
+        }
+        __syncwarp();
     } else {
         // ------------------------------------------------------------ epilogue
-        // Every epilogue thread runs the same sequence of named barriers whatever
-        // happens: after a failed (timed-out) wait a warp skips its work, never the
-        // barriers, so no other warp is left waiting on it.
+        // Every epilogue thread runs the same sequence of named barriers (one per
+        // block, for the left operand) whatever happens: after a failed (timed-out)
+        // wait a warp skips its work, never the barriers, so no other warp is left
+        // waiting on it.
         const int et = tid - 64;                 // 0..255
         const int q4 = warp & 3;                  // TMEM lanes 32*q4 .. 32*q4+31
         const int half = (warp - 2) >> 2;         // columns 64*half .. 64*half+63
@@ -320,27 +351,27 @@ __global__ void __launch_bounds__(kThreads) k_stream_tc(const __grid_constant__ 
                                                    off) = pack8(f);
                     }
                     tc::fence_proxy_async_smem();
-                } else if (ok && merge) {
-                    // A_k rows row0..row0+127, column j = page j: M-major, 64-row atoms.
-                    const uint32_t lbo_a = uint32_t(bk.rp / 8) * 1024u;
-                    for (int q = et; q < bk.rp * 16; q += kEpi) {
-                        const int j = q >> 4, c16 = q & 15;
-                        const int c = bk.row0 + 8 * c16;
-                        const bool valid = j < bk.r && c + 8 <= a.m.d_in;
-                        const uint32_t off = uint32_t(c16 >> 3) * lbo_a + uint32_t(j >> 3) * 1024u +
-                                             tc::sw128(uint32_t(j & 7), uint32_t(c16 & 7));
-                        tc::cp_async16(sL + off,
-                                       valid ? a.m.a_pool + int64_t(s_apg[j]) * a.m.a_pw + c
-                                             : a.m.a_pool,
-                                       valid ? 16u : 0u);
-                    }
-                    tc::cp_async_commit();
-                    tc::cp_async_wait<0>();
-                    tc::fence_proxy_async_smem();
                 }
                 named_bar_sync(1, kEpi);
-                if (et == 0)
+                if (et == 0 && merge) {
+                    // A_k rows row0..row0+127 (M-major: page j of A_k is row j of the
+                    // operand, 64 M values per 128-byte row), one 64-row half at a time;
+                    // a half wholly below d_in is not loaded (its rows are not stored).
+                    const int halves = bk.row0 + 64 < a.m.d_in ? 2 : 1;
+                    const uint32_t lbo_a = uint32_t(bk.rp) * 128u;
+                    if (ok) {
+                        mbar_arrive_expect_tx(bar_left, uint32_t(halves) * uint32_t(bk.rp) * 128u);
+                        for (int h = 0; h < halves; ++h)
+                            tc::for_row_boxes(bk.rp, [&](int off, int m) {
+                                tc::tma_load_2d(sL + uint32_t(h) * lbo_a + uint32_t(off) * 128u,
+                                                &a.amap[m], bk.row0 + 64 * h, bk.a_row + off, bar_left);
+                            });
+                    } else {
+                        mbar_arrive(bar_left);
+                    }
+                } else if (et == 0) {
                     mbar_arrive(bar_left);
+                }
             }
             if (ok)
                 ok = mbar_wait_bounded(tfull0 + 8 * b, uint32_t((i >> 1) & 1), status, kDevTimeoutMma);
@@ -375,46 +406,22 @@ __global__ void __launch_bounds__(kThreads) k_stream_tc(const __grid_constant__ 
                     }
                 }
                 tc::fence_proxy_async_smem();
-            }
-            named_bar_sync(1, kEpi);
-            const int n0 = (g - blk * a.n_chunks) * kBN;
-            const bool full_rows = merge || bk.nrows == kTM;
-            const int rows8 = full_rows ? kTM : (bk.nrows & ~7);
-            if (ok && row >= rows8 && row < bk.nrows) {
-                // one of the block's last (< 8) rows: this thread's 64 columns of it
-                const int col = n0 + 64 * half;
-                for (int c = 0; c < 8 && col + 8 * c + 8 <= d_out; ++c)
-                    *reinterpret_cast<uint4 *>(a.p.y + int64_t(bk.row0 + row) * a.p.ldy + col + 8 * c) =
-                        *reinterpret_cast<const uint4 *>(box + tc::sw128(uint32_t(row), uint32_t(c)));
-            }
-            if (et == 0 && ok) {
-                for (int h = 0; h < 2; ++h) {
-                    if (h == 1 && n0 + 64 >= d_out)   // a box wholly right of the matrix
-                        break;
-                    const uint32_t src = st + uint32_t(h) * kBox;
-                    if (full_rows)
-                        tc::tma_store_2d(&a.map, n0 + 64 * h, bk.row0, src);
-                    else
-                        for (int r8 = 0; r8 < rows8; r8 += 8)
-                            tc::tma_store_2d(&a.map8, n0 + 64 * h, bk.row0 + r8, src + uint32_t(r8) * 128u);
+                // one of a ragged block's last (< 8) rows: this thread wrote its 64
+                // columns of it and stores them (the TMA store covers 8-row boxes)
+                if (!merge && bk.nrows < kTM && row >= (bk.nrows & ~7) && row < bk.nrows) {
+                    const int col = (g - blk * a.n_chunks) * kBN + 64 * half;
+                    for (int c = 0; c < 8 && col + 8 * c + 8 <= d_out; ++c)
+                        *reinterpret_cast<uint4 *>(a.p.y + int64_t(bk.row0 + row) * a.p.ldy + col +
+                                                   8 * c) =
+                            *reinterpret_cast<const uint4 *>(box + tc::sw128(uint32_t(row),
+                                                                              uint32_t(c)));
                 }
-                tc::bulk_commit();
-            }
-            // The stage goes back to the producer once its store has read it (and,
-            // in a tile with a ragged end, once the threads storing the last rows
-            // have): a stage held longer is one load fewer in flight.
-            if (!full_rows && rows8 < bk.nrows)
-                named_bar_sync(1, kEpi);
-            if (et == 0 && ok) {
-                tc::bulk_wait_read0();
-                mbar_arrive(empty0 + 8 * s);
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(tready0 + 8 * s);
             }
         }
-        if (et == 0)
-            tc::bulk_wait0();
     }
-    if (!ok)
-        tc::cp_async_wait<0>();
     tc::fence_before_sync();
     __syncthreads();
     if (warp == 1) {
@@ -446,15 +453,13 @@ int device_sms()
 }
 
 cudaError_t launch_stream(StreamArgs &a, const void *tensor, uint64_t inner, uint64_t outer,
-                          uint64_t row_bytes, const void *b_pool, int64_t b_pw, int64_t b_pages,
-                          cudaStream_t stream)
+                          uint64_t row_bytes, cudaStream_t stream)
 {
     a.stages = pick_stages(a.left, a.rp_max);
     if (a.stages == 0)
         return cudaErrorInvalidValue;
     if (!encode_bf16_2d(&a.map, tensor, inner, outer, row_bytes, 64, kTM, true) ||
-        !encode_bf16_2d(&a.map8, tensor, inner, outer, row_bytes, 64, 8, true) ||
-        !encode_bf16_2d(&a.bmap, b_pool, inner, uint64_t(b_pages), uint64_t(b_pw) * 2u, 64, 1, true))
+        !encode_bf16_2d(&a.map8, tensor, inner, outer, row_bytes, 64, 8, true))
         return cudaErrorInvalidValue;
     // One CTA per SM (the shared memory holds no second one), each with an even
     // share of the chunks but at least two, so the pipeline has something to overlap.
@@ -486,8 +491,10 @@ cudaError_t launch_expand_tc(const TileParams &p, cudaStream_t stream)
     a.n_blocks = p.n_items;
     a.n_chunks = (p.d_out + kBN - 1) / kBN;
     a.rp_max = rank_pad16(p.max_tile_rank);
+    if (!encode_row_maps(a.bmap, p.b_rows, uint64_t(p.d_out), p.b_nrows, p.b_ld))
+        return cudaErrorInvalidValue;
     return launch_stream(a, p.y, uint64_t(p.d_out), uint64_t(p.n_rows), uint64_t(p.ldy) * 2u,
-                         p.b_pool, p.b_pw, p.b_n_pages, stream);
+                         stream);
 }
 
 bool merge_tc_supported(int d_in, int d_out, int rank)
@@ -504,8 +511,11 @@ cudaError_t launch_merge_tc(const MergeParams &p, int /*n_split*/, cudaStream_t 
     a.n_blocks = (p.d_in + kTM - 1) / kTM;
     a.n_chunks = (p.d_out + kBN - 1) / kBN;
     a.rp_max = rank_pad16(p.rank);
+    if (!encode_row_maps(a.bmap, p.b_rows, uint64_t(p.d_out), p.b_nrows, p.b_ld) ||
+        !encode_row_maps(a.amap, p.a_rows, uint64_t(p.d_in), p.a_nrows, p.a_ld))
+        return cudaErrorInvalidValue;
     return launch_stream(a, p.W, uint64_t(p.d_out), uint64_t(p.d_in), uint64_t(p.ldw) * 2u,
-                         p.b_pool, p.b_pw, p.b_n_pages, stream);
+                         stream);
 }
 
 }  // namespace lora

@@ -181,6 +181,18 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
+// Rows [0, rp) of an adapter block (rp a multiple of 16) as TMA boxes of 64, 32
+// and 16 rows: f(first row, map index 2 / 1 / 0) per box.
+template <typename F>
+__device__ __forceinline__ void for_row_boxes(int rp, F &&f)
+{
+    for (int off = 0; off < rp;) {
+        const int m = rp - off >= 64 ? 2 : rp - off >= 32 ? 1 : 0;
+        f(off, m);
+        off += 16 << m;
+    }
+}
+
 // Four rows (arbitrary row coordinates r0..r3, e.g. page ids) of one box-wide column
 // slice into four consecutive 128-byte rows of shared memory; the map's box is one
 // row high.  The 128-byte swizzle follows the destination address, so rows 4..7 of

@@ -7,14 +7,15 @@
 //   V[128 x r] (+)= X_tile[128 x K_s] . A_k[K_s x r]
 //   warp 0   fills a ring of stages by TMA alone: per K block the X block (128 rows
 //            x 64, 128-byte swizzle) and the matching A_k block -- row j of the
-//            MMA's K-major B operand is a 64-element slice of page j of A_k, so
-//            tile::gather4 drops four pages at a time straight into the swizzled
-//            layout (rank padding repeats page 0) -- all counted on one barrier;
+//            MMA's K-major B operand is a 64-element slice of page j of A_k, and in
+//            the A row matrix (dense.cu) the pages are consecutive rows, so the
+//            block is one to three boxes of 64 / 32 / 16 rows -- all counted on one
+//            barrier;
 //   warp 1   issues the tcgen05 MMAs (M = 128, N = r, K = 64 per stage) into a TMEM
 //            accumulator and frees each stage with tcgen05.commit;
 //   warps 2-5 read V from TMEM (row t = lane t) and write it as fp32: into the
 //            CTA's partial slot (fused call; the expand sums the slots in order;
-//            padded rank columns written as zeros) or into the caller's v rows
+//            rank-padding columns written as zeros) or into the caller's v rows
 //            (shrink-only call, one CTA per tile).
 // Shared memory is sized for two CTAs per SM, so the ksplit x tiles grid (at most
 // two per SM by construction) is resident in one wave.
@@ -34,7 +35,6 @@ namespace {
 constexpr int kTM = 128;                       // rows per tile
 constexpr int kKB = 64;                        // K elements per stage (one 128-byte row)
 constexpr int kMaxStages = 8;
-constexpr int kMaxRank = 128;
 constexpr uint32_t kXStage = kTM * 128;        // 16 KB
 constexpr uint32_t kRingBudget = 100u * 1024u; // two CTAs per SM
 
@@ -58,7 +58,7 @@ constexpr int kShrinkThreads = 192;
 
 struct TileArgs {
     CUtensorMap map;                           // x, 64 x 128 boxes
-    CUtensorMap amap;                          // the A pool, rows = pages, 64 x 1 boxes
+    CUtensorMap amap[3];                       // the A row matrix, 64 x 16 / 32 / 64 boxes
     TileParams p;
 };
 
@@ -67,7 +67,7 @@ __host__ __device__ inline int rank_pad16(int r) { return (r + 15) & ~15; }
 __host__ __device__ inline uint32_t shrink_smem_bytes(int max_rank)
 {
     const ShrinkRing g = shrink_ring(max_rank);
-    return 1024u + uint32_t(g.stages) * g.stage + 2u * kMaxStages * 8u + 64u + 4u * kMaxRank;
+    return 1024u + uint32_t(g.stages) * g.stage + 2u * kMaxStages * 8u + 64u;
 }
 
 // ---------------------------------------------------------------------- shrink
@@ -86,7 +86,6 @@ __global__ void __launch_bounds__(kShrinkThreads, 2) k_shrink_tc(const __grid_co
     const uint32_t empty0 = full0 + kMaxStages * 8;
     const uint32_t done = empty0 + kMaxStages * 8;
     const uint32_t tmem_slot = done + 8;
-    int32_t *s_pages = reinterpret_cast<int32_t *>(gbase + (tmem_slot + 64 - base));
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int KS = p.vmode == 0 ? p.ksplit : 1;
@@ -107,8 +106,6 @@ __global__ void __launch_bounds__(kShrinkThreads, 2) k_shrink_tc(const __grid_co
         mbar_init(done, 1);
         fence_mbar_init();
     }
-    if (tid < rp)   // rank padding repeats page 0; its V columns are zeroed below
-        s_pages[tid] = p.a_pages[size_t(it.adapter) * p.max_rank + (tid < r ? tid : 0)];
     if (warp == 1)
         tc::tmem_alloc(tmem_slot, ncols);
     tc::fence_before_sync();
@@ -118,27 +115,24 @@ __global__ void __launch_bounds__(kShrinkThreads, 2) k_shrink_tc(const __grid_co
 
     bool ok = true;
     if (warp == 0) {
-        const int quads = rp / 4;
-        for (int kb = 0; kb < nkb; ++kb) {
-            const int s = kb % kStages, u = kb / kStages;
-            if (u > 0)
-                ok = mbar_wait_bounded(empty0 + 8 * s, (u - 1) & 1, p.status, kDevTimeoutPipe) && ok;
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok)
-                break;
-            const uint32_t xs = base + uint32_t(s) * kStage, as = xs + kXStage;
-            const int k0 = (kb0 + kb) * kKB;
-            if (lane == 0) {
+        if (lane == 0) {
+            for (int kb = 0; kb < nkb && ok; ++kb) {
+                const int s = kb % kStages, u = kb / kStages;
+                if (u > 0)
+                    ok = mbar_wait_bounded(empty0 + 8 * s, (u - 1) & 1, p.status, kDevTimeoutPipe);
+                if (!ok)
+                    break;
+                const uint32_t xs = base + uint32_t(s) * kStage, as = xs + kXStage;
+                const int k0 = (kb0 + kb) * kKB;
                 mbar_arrive_expect_tx(full0 + 8 * s, kXStage + uint32_t(rp) * 128u);
                 tc::tma_load_2d(xs, &args.map, k0, it.row0, full0 + 8 * s);
-            }
-            __syncwarp();
-            for (int q = lane; q < quads; q += 32) {
-                const int j = 4 * q;
-                tc::tma_gather4(as + uint32_t(j) * 128u, &args.amap, k0, s_pages[j], s_pages[j + 1],
-                                s_pages[j + 2], s_pages[j + 3], full0 + 8 * s);
+                tc::for_row_boxes(rp, [&](int off, int m) {
+                    tc::tma_load_2d(as + uint32_t(off) * 128u, &args.amap[m], k0, it.a_row + off,
+                                    full0 + 8 * s);
+                });
             }
         }
+        __syncwarp();
     } else if (warp == 1) {
         if (lane == 0) {
             const uint32_t idesc = tc::idesc_bf16(kTM, rp, 0, 0);
@@ -215,8 +209,7 @@ cudaError_t launch_shrink_tc(const TileParams &p, cudaStream_t stream)
     args.p = p;
     if (!encode_bf16_2d(&args.map, p.x, uint64_t(p.d_in), uint64_t(p.n_rows), uint64_t(p.ldx) * 2u,
                         kKB, kTM, true) ||
-        !encode_bf16_2d(&args.amap, p.a_pool, uint64_t(p.d_in), uint64_t(p.a_n_pages),
-                        uint64_t(p.a_pw) * 2u, kKB, 1, true))
+        !encode_row_maps(args.amap, p.a_rows, uint64_t(p.d_in), p.a_nrows, p.a_ld))
         return cudaErrorInvalidValue;
     static bool configured = false;
     if (!configured) {

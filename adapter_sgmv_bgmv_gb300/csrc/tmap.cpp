@@ -4,6 +4,7 @@
 
 #include <cuda_runtime.h>
 
+#include <cstring>
 #include <mutex>
 
 namespace lora {
@@ -48,6 +49,22 @@ bool encode_bf16_2d(CUtensorMap *map, const void *base, uint64_t inner, uint64_t
                     swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
+}
+
+bool encode_row_maps(CUtensorMap maps[3], const void *base, uint64_t width, int64_t nrows,
+                     int64_t ld_elems)
+{
+    for (int m = 0; m < 3; ++m) {
+        const uint32_t rows = 16u << m;
+        if (int64_t(rows) > nrows) {
+            std::memset(&maps[m], 0, sizeof(CUtensorMap));
+            continue;
+        }
+        if (!encode_bf16_2d(&maps[m], base, width, uint64_t(nrows), uint64_t(ld_elems) * 2u, 64,
+                            rows, true))
+            return false;
+    }
+    return true;
 }
 
 }  // namespace lora

@@ -145,12 +145,15 @@ int lora_fused(lora_ctx *ctx, const lora_table *table, const int32_t *ids_host,
  * run: code paths that forbid cudaMalloc / cudaFree, or that run inside a
  * pre-sized memory budget.  There is no counterpart of this entry point on the
  * pages.  The context and the table are created beforehand (those calls do
- * allocate); this call then only launches kernels.  Its tensor-core scratch is a
- * fixed 4 MB file-scope device array (64 partial slots of 128 x 128 fp32) that
- * every GPU loading the library holds until the process exits.  Limits (else
- * LORA_E_CAPACITY, nothing launched): at most 64 tiles of up to 128 consecutive
- * same-adapter rows, at most 256 row-gather work items and 512 active rows outside
- * those tiles, n <= the context's max_rows.  The first call on a device looks up
+ * allocate); this call then only launches kernels.  Its tensor-core scratch is
+ * fixed file-scope device arrays that every GPU loading the library holds until
+ * the process exits: 4 MB of partial V (64 slots of 128 x 128 fp32) and 8 MB for
+ * the dense adapter rows of a call whose tile adapters do not sit in consecutive
+ * pages of a rank that is a multiple of 16 (slots x rank padded to 16 x (d_in +
+ * d_out) bf16).  Limits (else LORA_E_CAPACITY, nothing launched): at most 64
+ * tiles of up to 128 consecutive same-adapter rows, those 8 MB, at most 256
+ * row-gather work items and 512 active rows outside those tiles, n <= the
+ * context's max_rows.  The first call on a device looks up
  * the array's device address (a runtime call, no allocation) and should come
  * before any stream capture.  Every call shares the array: calls that overlap on
  * the GPU (different streams, or one stream and a capture replay) race on it;
