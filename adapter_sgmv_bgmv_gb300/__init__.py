@@ -149,7 +149,8 @@ class Context:
 
     def profile_end(self):
         """Stop; returns {family: (device ms, launches)} for the row-gather, tile shrink,
-        merge and streaming expand kernels."""
+        merge and streaming expand kernels: every launch made while profiling, and
+        their device time (the bracketed launches' mean times that count)."""
         ms = (ctypes.c_double * 4)()
         n = (ctypes.c_int64 * 4)()
         _check(_L.lora_profile_end(self.handle, ms, n), self)

@@ -6,6 +6,7 @@
 #include <algorithm>
 #include <cstdio>
 #include <cstring>
+#include <memory>
 #include <new>
 #include <string>
 #include <vector>
@@ -77,6 +78,7 @@ struct lora_ctx {
     uint8_t *dense = nullptr;       // dense adapter rows of a call (dense.cu)
     size_t dense_cap = 0;
     std::vector<int32_t> slot_of;   // adapter -> slot while a call's slots are assigned
+    std::unique_ptr<TileParams> tparams;   // launch parameters of the tile kernels
 };
 
 struct lora_table {
@@ -518,10 +520,10 @@ int run_tiles(lora_ctx *ctx, const lora_table *t, int mode, const void *x, int64
     const size_t items_bytes = pl.tile_items.size() * sizeof(TileItem);
     Slot *slot = nullptr;
     const TileItem *d_items = nullptr;
-    if (fixed) {
-        CUDA_TRY(ctx, noalloc_put_items(pl.tile_items.data(), int(pl.tile_items.size()), stream));
-        d_items = fixed->items;
-    } else {
+    const bool inl = pl.tile_items.size() <= size_t(kInlineTiles);
+    if (fixed && !inl)
+        return LORA_E_CAPACITY;
+    if (!inl) {
         rc = acquire_slot(ctx, items_bytes + 16, &slot);
         if (rc != LORA_OK)
             return rc;
@@ -553,7 +555,18 @@ int run_tiles(lora_ctx *ctx, const lora_table *t, int mode, const void *x, int64
             ctx->vparts_cap = need;
         }
     }
-    TileParams p{};
+    // TileParams carries the inline list (8 KB): one per context, reused.
+    if (!ctx->tparams) {
+        ctx->tparams.reset(new (std::nothrow) TileParams());
+        if (!ctx->tparams)
+            return LORA_E_NOMEM;
+    }
+    TileParams &p = *ctx->tparams;
+    p = TileParams{};
+    if (inl) {
+        p.items_inline = 1;
+        std::copy(pl.tile_items.begin(), pl.tile_items.end(), p.inl);
+    }
     p.x = static_cast<const uint16_t *>(x);
     p.ldx = ldx;
     p.y = static_cast<uint16_t *>(y);
@@ -1144,13 +1157,20 @@ int lora_profile_end(lora_ctx *ctx, double *ms, int64_t *launches)
         ms[f] = 0.0;
         launches[f] = 0;
     }
+    int64_t sampled[4] = {0, 0, 0, 0};
     for (size_t i = 0; i < ctx->prof_used; ++i) {
         lora_ctx::ProfEv &e = ctx->prof_ev[i];
         CUDA_TRY(ctx, cudaEventSynchronize(e.b));
         float t = 0.f;
         CUDA_TRY(ctx, cudaEventElapsedTime(&t, e.a, e.b));
         ms[e.family] += double(t);
-        launches[e.family] += 1;
+        sampled[e.family] += 1;
+    }
+    // The bracketed launches stand for all of their family: mean x count.
+    for (int f = 0; f < 4; ++f) {
+        launches[f] = ctx->prof_seen[f];
+        if (sampled[f] > 0)
+            ms[f] *= double(ctx->prof_seen[f]) / double(sampled[f]);
     }
     ctx->prof_used = 0;
     return LORA_OK;

@@ -12,6 +12,7 @@
 #include <cuda_runtime.h>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace lora {
 
@@ -23,6 +24,9 @@ constexpr int kStageThreads = 128;
 __global__ void __launch_bounds__(kStageThreads) k_stage_rows(const __grid_constant__ StageArgs a)
 {
     const StageSide &sd = a.side[blockIdx.y];
+    // Launched as a programmatic dependent; the previous kernels may still read
+    // the scratch, and the pools may be theirs to write.
+    grid_dep_wait();
     if (!sd.dst)
         return;
     const int row = int(blockIdx.x);
@@ -51,6 +55,11 @@ cudaError_t launch_stage_rows(const StageArgs &a, cudaStream_t stream)
     cfg.gridDim = dim3(unsigned(a.n_slots * a.rp), 2u);
     cfg.blockDim = dim3(kStageThreads);
     cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, k_stage_rows, a);
 }
 

@@ -90,6 +90,9 @@ int rows_max_smem();
 // splits K over `ksplit` CTAs per tile; each writes its fp32 partial V (128 rows x
 // r_pad) into its own 64 KB slot of a scratch that the expand sums in order.
 constexpr int kVPartBytes = 128 * 128 * 4;
+// Tile lists up to this long travel in the launch parameters (no copy in the
+// stream ahead of the kernels); longer ones are copied to the device.
+constexpr int kInlineTiles = 256;
 struct TileParams {
     const uint16_t *x;
     int64_t ldx;
@@ -105,7 +108,7 @@ struct TileParams {
     const uint16_t *b_rows;
     int64_t b_ld;
     int64_t b_nrows;
-    const TileItem *items;
+    const TileItem *items;    // device copy of the list, unless items_inline
     float *vparts;            // fused: [n_items][ksplit] partial V slots
     float *v;                 // shrink / expand only: fp32 rows [n, ldv]
     int64_t ldv;
@@ -118,18 +121,25 @@ struct TileParams {
     int vmode;                // 0: V tiles (fused), 1: fp32 v rows
     int max_tile_rank;        // largest rank among the items (sizes shared memory)
     int ksplit;               // fused: K-split of the shrink (1..8)
+    int items_inline;         // 1: the list is inl[0 .. n_items)
+    TileItem inl[kInlineTiles];
 };
+#ifdef __CUDACC__
+__device__ __forceinline__ TileItem tile_item(const TileParams &p, int i)
+{
+    return p.items_inline ? p.inl[i] : p.items[i];
+}
+#endif
 // Fixed scratch of lora_fused_noalloc (noalloc.cu): device addresses of the
 // file-scope arrays on one device, looked up once per device.
 constexpr int kNoAllocSlots = 64;
 constexpr size_t kNoAllocDenseBytes = size_t(8) << 20;
 struct NoAllocScratch {
     float *vparts;            // kNoAllocSlots slots of kVPartBytes
-    TileItem *items;          // kNoAllocSlots entries
     uint16_t *dense;          // kNoAllocDenseBytes of dense adapter rows
 };
+static_assert(kNoAllocSlots <= kInlineTiles, "a no-alloc tile list travels in the parameters");
 int noalloc_scratch(int device, NoAllocScratch *out);
-cudaError_t noalloc_put_items(const TileItem *items, int n, cudaStream_t stream);
 
 // Dense adapter rows (dense.cu): for slot s and j < rp, row s*rp + j of dst gets
 // the first `width` elements of page j of the slot's adapter, zeros for j >= rank.

@@ -112,7 +112,7 @@ __device__ __forceinline__ Block block_info(const StreamArgs &a, int blk)
         b.a_row = a.m.a_row;
         b.b_row = a.m.b_row;
     } else {
-        const TileItem it = a.p.items[blk];
+        const TileItem it = tile_item(a.p, blk);
         b.r = it.rank;
         b.row0 = it.row0;
         b.nrows = it.nrows;
@@ -171,6 +171,9 @@ __global__ void __launch_bounds__(kThreads) k_stream_tc(const __grid_constant__ 
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = *reinterpret_cast<const uint32_t *>(gbase + (tmem_slot - base));
+    // Launched as a programmatic dependent: everything above overlapped the previous
+    // kernel; y / W, V and the row matrices may be its to write.
+    grid_dep_wait();
     bool ok = true;
 
     if (warp == 0) {
@@ -206,6 +209,7 @@ __global__ void __launch_bounds__(kThreads) k_stream_tc(const __grid_constant__ 
                                         &a.bmap[m], n0 + 64 * h, bk.b_row + off, full0 + 8 * s);
                     });
             }
+            grid_dep_launch();   // every load issued: the next kernel may start its set-up
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -478,6 +482,11 @@ cudaError_t launch_stream(StreamArgs &a, const void *tensor, uint64_t inner, uin
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = stream_smem_bytes(a.left, a.rp_max, a.stages);
     cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, k_stream_tc, a);
 }
 

@@ -18,7 +18,10 @@
 //            rank-padding columns written as zeros) or into the caller's v rows
 //            (shrink-only call, one CTA per tile).
 // Shared memory is sized for two CTAs per SM, so the ksplit x tiles grid (at most
-// two per SM by construction) is resident in one wave.
+// two per SM by construction) is resident in one wave.  The kernel is launched as
+// a programmatic dependent of the one before it: barrier set-up and the TMEM
+// allocation overlap that kernel's tail, and the expand is released to start its
+// own set-up once every CTA has issued its last MMA.
 //
 // The expand side is the streaming kernel in stream_tc.cu.
 #include <cuda.h>
@@ -90,7 +93,7 @@ __global__ void __launch_bounds__(kShrinkThreads, 2) k_shrink_tc(const __grid_co
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int KS = p.vmode == 0 ? p.ksplit : 1;
     const int tile = blockIdx.x / KS, ks = blockIdx.x - (blockIdx.x / KS) * KS;
-    const TileItem it = p.items[tile];
+    const TileItem it = tile_item(p, tile);
     const int r = it.rank, rp = rank_pad16(r);
     const int nkb_all = (p.d_in + kKB - 1) / kKB;
     const int per = (nkb_all + KS - 1) / KS;
@@ -112,6 +115,9 @@ __global__ void __launch_bounds__(kShrinkThreads, 2) k_shrink_tc(const __grid_co
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = *reinterpret_cast<const uint32_t *>(gbase + (tmem_slot - base));
+    // Launched as a programmatic dependent: everything above overlapped the previous
+    // kernel; x, the row matrix and the partial slots may be its to write or read.
+    grid_dep_wait();
 
     bool ok = true;
     if (warp == 0) {
@@ -157,6 +163,8 @@ __global__ void __launch_bounds__(kShrinkThreads, 2) k_shrink_tc(const __grid_co
     } else {
         // Epilogue: this warp reads TMEM lanes 32*(warp%4) .. +31.
         ok = mbar_wait_bounded(done, 0, p.status, kDevTimeoutMma);
+        if (tid == 64)
+            grid_dep_launch();   // the expand may start its set-up on freed SMs
         ok = __all_sync(0xffffffffu, ok);   // warp converged and agreed before tcgen05.ld
         tc::fence_after_sync();
         const int row = 32 * (warp & 3) + lane;
@@ -224,6 +232,11 @@ cudaError_t launch_shrink_tc(const TileParams &p, cudaStream_t stream)
     cfg.blockDim = dim3(kShrinkThreads);
     cfg.dynamicSmemBytes = shrink_smem_bytes(p.max_tile_rank);
     cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, k_shrink_tc, args);
 }
 

@@ -133,6 +133,23 @@ def alg_bytes_delta(case, ids):
     return 2 * n_act * d_in + 4 * n_act * d_out + ab + 4 * n_act + 16 * len(distinct)
 
 
+def alg_bytes_split(case, ids, tiles: bool) -> dict:
+    """alg_bytes_delta split by the kernel family that moves each part: on the tile
+    path the shrink reads x and the A pages, the expand reads and writes y and reads
+    the B pages; on the row-gather path one kernel does all of it."""
+    ids = np.asarray(ids)
+    act = ids[ids >= 0]
+    n_act = int(act.size)
+    d_in, d_out = case["d_in"], case["d_out"]
+    distinct = np.unique(act)
+    a_b = int(sum(2 * int(case["rank"][k]) * d_in for k in distinct))
+    b_b = int(sum(2 * int(case["rank"][k]) * d_out for k in distinct))
+    plan = 4 * n_act + 16 * len(distinct)
+    if tiles:
+        return {"shrink": 2 * n_act * d_in + a_b + plan, "expand": 4 * n_act * d_out + b_b}
+    return {"rows": 2 * n_act * d_in + 4 * n_act * d_out + a_b + b_b + plan}
+
+
 def flops_delta(case, ids):
     ids = np.asarray(ids)
     act = ids[ids >= 0]
@@ -256,6 +273,26 @@ class Bench:
             r = int(c["rank"][c["merge_adapter"]])
             return 2 * (4 * c["d_in"] * c["d_out"] + 2 * r * (c["d_in"] + c["d_out"]))
         return sum(alg_bytes_delta(self.cases[k], ids) for k, ids in self.steps_ids[i % len(self.steps_ids)])
+
+    def learn_paths(self, stream):
+        """Which kernels each call of a step runs (one untimed call per case)."""
+        self.paths = {}
+        if self.is_merge:
+            return
+        for key, ids in self.steps_ids[0]:
+            self.sets[0][key]["call"](ids)
+            self.paths[key] = self.ctx.last_path()[0]
+        self.torch.cuda.synchronize()
+
+    def alg_bytes_family(self, i: int) -> dict:
+        if self.is_merge:
+            return {"merge": self.alg_bytes_step(i)}
+        out = {}
+        for k, ids in self.steps_ids[i % len(self.steps_ids)]:
+            tiles = bool(self.paths.get(k, 1) & 2) and not (self.paths.get(k, 1) & 1)
+            for f, v in alg_bytes_split(self.cases[k], ids, tiles).items():
+                out[f] = out.get(f, 0) + v
+        return out
 
     def flops_step(self, i: int) -> int:
         if self.is_merge:
@@ -430,6 +467,7 @@ def run_one(name, args, L, torch, ctx, dist, world, rank, local):
     clocks.start()
     for i in range(W):
         b.step(i, stream)
+    b.learn_paths(stream)
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
@@ -454,18 +492,29 @@ def run_one(name, args, L, torch, ctx, dist, world, rank, local):
     clocks.stop()
     clk = clocks.summary(t_wall0, t_wall1)
 
-    bytes_total = sum(b.alg_bytes_step(W + i) for i in range(K))
     flops_total = sum(b.flops_step(W + i) for i in range(K))
     pk = peaks()
-    launches = sum(n for (_, n) in prof.values())
     kern_s_total = sum(m for (m, _) in prof.values()) / 1e3
-    # All kernels of the path are HBM-bound: the roofline is taken over every
-    # launch of the timed region (algorithmic bytes / summed kernel time).
-    achieved_gbs = bytes_total / kern_s_total / 1e9 if kern_s_total > 0 else None
-    per_kernel = {f: round(1e3 * m / n, 3) for f, (m, n) in prof.items() if n}
+    # Per kernel family: launches, mean device time per launch (the profiler times
+    # one launch in `profile_every` per family and scales), algorithmic bytes it
+    # moves and the rate.  Every kernel of the path is HBM-bound; the roofline line
+    # is that of the family with the most device time.
+    fam_bytes = {}
+    for i in range(K):
+        for f, v in b.alg_bytes_family(W + i).items():
+            fam_bytes[f] = fam_bytes.get(f, 0) + v
+    per_family = {}
+    for f, (m, n) in prof.items():
+        if n and m > 0:
+            gbs = fam_bytes.get(f, 0) / (m / 1e3) / 1e9
+            per_family[f] = {"launches": n, "us_per_launch": round(1e3 * m / n, 3),
+                             "alg_bytes_per_launch": fam_bytes.get(f, 0) / n,
+                             "GB/s": round(gbs, 1), "frac": round(gbs / pk["hbm_gbs"], 4)}
+    per_kernel = {f: v["us_per_launch"] for f, v in per_family.items()}
     kernel_names = {"rows": "k_rows_inline<fused>", "shrink": "k_shrink_tc",
                     "expand": "k_stream_tc(expand)", "merge": "k_stream_tc(merge)"}
-    dominant = max(prof, key=lambda f: prof[f][0])
+    dominant = max(per_family, key=lambda f: prof[f][0])
+    achieved_gbs = per_family[dominant]["GB/s"]
     sec = ms / 1e3
     if b.is_merge:
         value = 2 * K * world / sec
@@ -482,16 +531,17 @@ def run_one(name, args, L, torch, ctx, dist, world, rank, local):
                          f"({b.n_sets * b._unique_bytes_per_step() / 1e6:.0f} MB touched per pass "
                          f"> 129 MB L2)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-        "us_per_call": {"kernel": 1e6 * kern_s_total / max(1, K * b.launches_per_step()),
-                        "host_call": 1e6 * sec / max(1, K * b.launches_per_step()),
+        "us_per_call": {"device": 1e6 * kern_s_total / max(1, K * b.launches_per_step()),
+                        "wall": 1e6 * sec / max(1, K * b.launches_per_step()),
                         "per_kernel_launch": per_kernel},
         "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": pk["hbm_gbs"],
                      "unit": "GB/s",
                      "frac": (achieved_gbs / pk["hbm_gbs"]) if achieved_gbs else None,
                      "traffic": None, "peak_source": pk["source"],
                      "kernel": kernel_names[dominant],
-                     "scope": "all launches of the timed region",
-                     "alg_bytes_per_call": bytes_total / max(1, K * b.launches_per_step()),
+                     "bytes_per_launch": per_family[dominant]["alg_bytes_per_launch"],
+                     "us_per_launch": per_family[dominant]["us_per_launch"],
+                     "per_family": per_family,
                      "tflops": flops_total / max(1e-12, kern_s_total) / 1e12},
         "gpu_launches": n_launched,
         "clocks": clk,

@@ -213,10 +213,12 @@ int lora_ctx_set_option(lora_ctx *ctx, int option, int value);
 
 /* Per-launch timing: between lora_profile_begin and lora_profile_end every
  * `every`-th kernel launch of the context (every >= 1) is bracketed by CUDA events
- * on its stream.  _end
- * synchronizes on those events and returns, per kernel family (0 row-gather,
- * 1 tensor-core tile shrink, 2 merge, 3 tensor-core streaming expand), the summed
- * device time in ms[] and the launch count in launches[] (arrays of 4). */
+ * on its stream.  _end synchronizes on those events and returns, per kernel
+ * family (0 row-gather, 1 tensor-core tile shrink, 2 merge, 3 tensor-core streaming
+ * expand), the number of launches made while profiling in launches[] and their
+ * device time in ms[] (arrays of 4): the mean of the bracketed launches times that
+ * number.  A call that first copies adapter pages into dense rows (dense.cu)
+ * counts the copy in the family of the kernel that reads it. */
 int lora_profile_begin(lora_ctx *ctx, int every);
 int lora_profile_end(lora_ctx *ctx, double *ms, int64_t *launches);
 
