@@ -68,3 +68,13 @@ def load(path: str = LIB_PATH):
         fn.restype = res
     _lib = lib
     return lib
+
+
+def untyped(name: str):
+    """A second foreign-function object for `name` with no argument types: called
+    with ctypes instances, it passes them as they are, without the per-argument
+    conversion that the typed object does on every call."""
+    lib = load()
+    fn = lib._FuncPtr((name, lib))
+    fn.restype = SIGNATURES[name][1]
+    return fn

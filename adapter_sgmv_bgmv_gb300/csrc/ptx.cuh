@@ -163,6 +163,24 @@ __device__ __forceinline__ uint4 pack8(const float f[8])
     return u;
 }
 
+// acc0 += sum over even e of a[e] b[e], acc1 += the odd ones, for 8 bf16 pairs:
+// mixed-precision FMA (bf16 multiplicands, fp32 accumulator, one rounding: the
+// same result as fmaf on the converted values), no conversion instructions.
+__device__ __forceinline__ void dot8_bf16(const uint4 &a, const uint4 &b, float &acc0, float &acc1)
+{
+    asm("{\n\t.reg .b16 a0, a1, a2, a3, a4, a5, a6, a7, b0, b1, b2, b3, b4, b5, b6, b7;\n\t"
+        "mov.b32 {a0, a1}, %2;\n\tmov.b32 {a2, a3}, %3;\n\t"
+        "mov.b32 {a4, a5}, %4;\n\tmov.b32 {a6, a7}, %5;\n\t"
+        "mov.b32 {b0, b1}, %6;\n\tmov.b32 {b2, b3}, %7;\n\t"
+        "mov.b32 {b4, b5}, %8;\n\tmov.b32 {b6, b7}, %9;\n\t"
+        "fma.rn.f32.bf16 %0, a0, b0, %0;\n\tfma.rn.f32.bf16 %1, a1, b1, %1;\n\t"
+        "fma.rn.f32.bf16 %0, a2, b2, %0;\n\tfma.rn.f32.bf16 %1, a3, b3, %1;\n\t"
+        "fma.rn.f32.bf16 %0, a4, b4, %0;\n\tfma.rn.f32.bf16 %1, a5, b5, %1;\n\t"
+        "fma.rn.f32.bf16 %0, a6, b6, %0;\n\tfma.rn.f32.bf16 %1, a7, b7, %1;\n\t}"
+        : "+f"(acc0), "+f"(acc1)
+        : "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w));
+}
+
 __device__ __forceinline__ float warp_sum(float v)
 {
 #pragma unroll

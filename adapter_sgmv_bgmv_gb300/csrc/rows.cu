@@ -8,11 +8,13 @@
 //   1. warp 0 issues bulk (TMA) copies: lane i < nrows fetches x row i and y row i,
 //      lane j < r reads page j of A_k / B_k from the page table and fetches its
 //      slice, so the CTA's whole working set is in flight after one dependent load;
-//   2. shrink: partial v[i, j] over the CTA's d_in slice, warp-per-page dot
-//      products with 128-bit shared loads and a warp-shuffle reduction;
-//   3. each CTA pushes its partial v into a per-source slot of every peer's shared
-//      memory (distributed shared memory stores), one cluster barrier, then every
-//      CTA sums the slots in rank order (all CTAs get identical v);
+//   2. shrink: partial v[i, j] over the CTA's d_in slice, half a warp per page (all
+//      pages of a rank <= 16 at once), 128-bit shared loads and a shuffle reduction,
+//      into the CTA's own shared memory;
+//   3. one cluster barrier, then every CTA reads all C partials with distributed
+//      shared memory loads and sums them in cluster-rank order (all CTAs get an
+//      identical v); a second barrier phase, waited on at exit, keeps each CTA's
+//      partial alive while its peers read it;
 //   4. expand: y[i, o] = bf16(y[i, o] + s_k * sum_j v[i, j] B_k[j, o]) for the CTA's
 //      d_out slice, 128-bit stores straight to the gathered rows.
 //
@@ -29,13 +31,12 @@ namespace lora {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
 constexpr int kMaxCluster = 16;
 
 __host__ __device__ inline size_t align16(size_t v) { return (v + 15) & ~size_t(15); }
 
 __host__ __device__ inline size_t carve(int mode, int si, int so, int rows, int ranks,
-                                        int cluster, size_t off[7])
+                                        int cluster, size_t off[8])
 {
     size_t o = 0;
     const bool has_in = mode != kExpand, has_out = mode != kShrink;
@@ -43,22 +44,11 @@ __host__ __device__ inline size_t carve(int mode, int si, int so, int rows, int 
     off[1] = o; o += has_in ? align16(size_t(rows) * si * 2) : 0;           // x rows
     off[2] = o; o += has_out ? align16(size_t(ranks) * so * 2) : 0;         // B slice
     off[3] = o; o += has_out ? align16(size_t(rows) * so * 2) : 0;          // y rows
-    off[4] = o; o += has_in ? align16(size_t(cluster) * rows * ranks * 4) : 0;  // pushed partials
+    off[4] = o; o += (has_in && cluster > 1) ? align16(size_t(rows) * ranks * 4) : 0;  // own partial
     off[5] = o; o += align16(size_t(rows) * ranks * 4);                     // v
-    off[6] = o; o += 16;                                                    // 2 mbarriers
+    off[6] = o; o += align16(size_t(rows) * 4);                             // the rows' indices
+    off[7] = o; o += 16;                                                    // 2 mbarriers
     return o;
-}
-
-__device__ __forceinline__ void st_dsmem_f32(float *local, uint32_t rank, float v)
-{
-    uint32_t ra;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_u32(local)), "r"(rank));
-    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(ra), "f"(v) : "memory");
-}
-
-__device__ __forceinline__ void cluster_arrive_relaxed()
-{
-    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 }
 
 // Expand of `ROWS` rows starting at i0 for 8 output columns at vector q:
@@ -87,12 +77,16 @@ __device__ __forceinline__ void expand_vec(const uint16_t *sB, int slice_out, co
 }
 
 template <int MODE>
-__device__ __forceinline__ void rows_body(const RowsParams &p, const RowItem *items,
+__device__ __forceinline__ void rows_body(const RowsParams &pin, const RowItem *items,
                                           const int32_t *perm)
 {
+    // A register copy of the parameters: read through the parameter block's
+    // address, every field would be loaded again after each asm statement that
+    // clobbers memory (barriers, cluster stores).
+    const RowsParams p = pin;
     extern __shared__ __align__(128) uint8_t smem[];
     const int C = p.cluster;
-    size_t off[7];
+    size_t off[8];
     carve(MODE, p.slice_in, p.slice_out, p.rows_alloc, p.rank_alloc, C, off);
     uint16_t *sA = reinterpret_cast<uint16_t *>(smem + off[0]);
     uint16_t *sX = reinterpret_cast<uint16_t *>(smem + off[1]);
@@ -100,7 +94,8 @@ __device__ __forceinline__ void rows_body(const RowsParams &p, const RowItem *it
     uint16_t *sY = reinterpret_cast<uint16_t *>(smem + off[3]);
     float *vin = reinterpret_cast<float *>(smem + off[4]);
     float *vsum = reinterpret_cast<float *>(smem + off[5]);
-    const uint32_t bar0 = smem_u32(smem + off[6]);
+    int32_t *s_rows = reinterpret_cast<int32_t *>(smem + off[6]);   // perm[it.p0 + i]
+    const uint32_t bar0 = smem_u32(smem + off[7]);
     const uint32_t bar1 = bar0 + 8;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -113,7 +108,6 @@ __device__ __forceinline__ void rows_body(const RowsParams &p, const RowItem *it
     const int nrows = it.nrows;
     const float s = it.scale;
     const int RA = p.rank_alloc;
-    const int RW = p.rows_alloc;
 
     const int in0 = int(crank) * p.slice_in;
     const int in_len = max(0, min(p.d_in - in0, p.slice_in));
@@ -126,8 +120,6 @@ __device__ __forceinline__ void rows_body(const RowsParams &p, const RowItem *it
         fence_mbar_init();
     }
     __syncthreads();
-    if (clustered)
-        cluster_arrive_relaxed();   // "started"; waited on before the first remote store
 
     // ---- 1. copies.  Page ids come from the table (written once, at registration),
     // so they are read before waiting for the preceding kernel; everything it may
@@ -153,6 +145,8 @@ __device__ __forceinline__ void rows_body(const RowsParams &p, const RowItem *it
             pr0 = perm[it.p0 + lane];
         if (lane + 32 < nrows)
             pr1 = perm[it.p0 + lane + 32];
+        for (int q = lane; q < nrows; q += 32)
+            s_rows[q] = q < 32 ? pr0 : q < 64 ? pr1 : perm[it.p0 + q];
     }
     grid_dep_wait();
     if (warp == 0) {
@@ -207,67 +201,72 @@ __device__ __forceinline__ void rows_body(const RowsParams &p, const RowItem *it
     if (MODE != kExpand) {
         ok = mbar_wait_bounded(bar0, 0, p.status, kDevTimeoutLoad) && ok;
         const int nvec = in_len >> 3;
-        if (clustered)
-            cluster_wait_acquire();  // every peer has started: its shared memory exists
-        for (int j = warp; j < r; j += kWarps) {
+        // Half a warp per page, all pages of a rank <= 16 at once: thread l16 of
+        // the half takes every 16th 8-element vector of the CTA's slice.
+        const int l16 = lane & 15;
+        const unsigned hmask = 0xffffu << (lane & 16);
+        for (int j = tid >> 4; j < r; j += kThreads / 16) {
             const uint4 *a = reinterpret_cast<const uint4 *>(sA + size_t(j) * p.slice_in);
             for (int i0 = 0; i0 < nrows; i0 += 4) {
-                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc2[4] = {0.f, 0.f, 0.f, 0.f};
                 const int nr = min(4, nrows - i0);
-                for (int q = lane; q < nvec; q += 32) {
-                    float af[8];
-                    unpack8(a[q], af);
+                for (int q = l16; q < nvec; q += 16) {
+                    const uint4 av = a[q];
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        if (u < nr) {
-                            float xf[8];
-                            unpack8(reinterpret_cast<const uint4 *>(
-                                        sX + size_t(i0 + u) * p.slice_in)[q], xf);
-#pragma unroll
-                            for (int e = 0; e < 8; ++e)
-                                acc[u] = fmaf(xf[e], af[e], acc[u]);
-                        }
-                    }
+                    for (int u = 0; u < 4; ++u)
+                        if (u < nr)
+                            dot8_bf16(reinterpret_cast<const uint4 *>(sX + size_t(i0 + u) * p.slice_in)[q],
+                                      av, acc[u], acc2[u]);
                 }
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
                     if (u < nr) {
-                        const float t = warp_sum(acc[u]);
+                        float t = acc[u] + acc2[u];
+#pragma unroll
+                        for (int o = 8; o > 0; o >>= 1)
+                            t += __shfl_xor_sync(hmask, t, o);
                         const int slot = (i0 + u) * RA + j;
-                        if (!clustered) {
-                            if (lane == 0)
-                                vsum[slot] = t;
-                        } else if (lane < C) {
-                            // lane c delivers this partial to CTA c's slot for our rank
-                            st_dsmem_f32(vin + (size_t(crank) * RW) * RA + slot, uint32_t(lane), t);
-                        }
+                        if (l16 == 0)
+                            (clustered ? vin : vsum)[slot] = t;
                     }
                 }
             }
         }
         if (clustered) {
-            cluster_sync();   // all partials delivered to every CTA
+            // Every CTA's partial is in its own shared memory: one cluster barrier,
+            // then each CTA reads all C partials (distributed shared memory loads, all
+            // issued before any add) and sums them in cluster-rank order, so every
+            // CTA holds the same v.  A second barrier phase, arrived at here and
+            // waited on before exit, keeps each CTA's memory alive while peers read it.
+            cluster_sync();
             for (int q = tid; q < nrows * r; q += kThreads) {
                 const int i = q / r, j = q - (q / r) * r;
+                float part[kMaxCluster];
+#pragma unroll
+                for (int c = 0; c < kMaxCluster; ++c)
+                    if (c < C)
+                        part[c] = ld_dsmem_f32(vin + i * RA + j, uint32_t(c));
                 float acc = 0.f;
-                for (int c = 0; c < C; ++c)
-                    acc += vin[(size_t(c) * RW + i) * RA + j];
+#pragma unroll
+                for (int c = 0; c < kMaxCluster; ++c)
+                    if (c < C)
+                        acc += part[c];
                 vsum[i * RA + j] = acc;
             }
+            cluster_arrive_release();
         }
         __syncthreads();
         if (MODE == kShrink && ok && crank == 0) {
             for (int q = tid; q < nrows * r; q += kThreads) {
                 const int i = q / r, j = q - (q / r) * r;
-                const int row = perm[it.p0 + i];
-                p.v[int64_t(row) * p.ldv + j] = vsum[i * RA + j];
+                p.v[int64_t(s_rows[i]) * p.ldv + j] = vsum[i * RA + j];
             }
         }
     } else {
+        __syncthreads();   // s_rows
         for (int q = tid; q < nrows * r; q += kThreads) {
             const int i = q / r, j = q - (q / r) * r;
-            const int row = perm[it.p0 + i];
-            vsum[i * RA + j] = p.v[int64_t(row) * p.ldv + j];
+            vsum[i * RA + j] = p.v[int64_t(s_rows[i]) * p.ldv + j];
         }
         __syncthreads();
     }
@@ -277,7 +276,7 @@ __device__ __forceinline__ void rows_body(const RowsParams &p, const RowItem *it
         ok = mbar_wait_bounded(bar1, 0, p.status, kDevTimeoutLoad) && ok;
         const int nvo = out_len >> 3;
         if (nrows == 1) {
-            const int row = perm[it.p0];
+            const int row = s_rows[0];
             for (int q = tid; q < nvo; q += kThreads) {
                 float acc[1][8];
                 expand_vec<1>(sB, p.slice_out, vsum, RA, r, 0, q, acc);
@@ -313,7 +312,7 @@ __device__ __forceinline__ void rows_body(const RowsParams &p, const RowItem *it
 #pragma unroll
                         for (int e = 0; e < 8; ++e)
                             yf[e] = fmaf(s, acc[u][e], yf[e]);
-                        const int row = perm[it.p0 + i0 + u];
+                        const int row = s_rows[i0 + u];
                         if (ok)
                             *reinterpret_cast<uint4 *>(p.y + int64_t(row) * p.ldy + out0 + 8 * q) =
                                 pack8(yf);
@@ -331,6 +330,8 @@ __device__ __forceinline__ void rows_body(const RowsParams &p, const RowItem *it
         if (MODE != kShrink)
             mbar_wait_bounded(bar1, 0, nullptr, 0);
     }
+    if (clustered)
+        cluster_wait_acquire();   // every peer has finished reading this CTA's partial
 }
 
 template <int MODE>
@@ -399,7 +400,7 @@ int rows_max_cluster() { return kMaxCluster; }
 size_t rows_smem_bytes(int mode, int slice_in, int slice_out, int rows_alloc, int rank_alloc,
                        int cluster)
 {
-    size_t off[7];
+    size_t off[8];
     return carve(mode, slice_in, slice_out, rows_alloc, rank_alloc, cluster, off);
 }
 

@@ -248,3 +248,21 @@ def test_tile_shrink_and_expand_match_oracle(ctx):
     assert ctx.last_path()[0] & 2
     assert_parity(from_dev(y), oracle.expand(t, c["ids"], v0, c["y"]), REL_FROB, MAX_ABS_RMS,
                   "tile expand")
+
+
+def test_prepared_fused_matches_lora_fused_and_reads_a_rewritten_ids_buffer(ctx):
+    """PreparedFused reuses its converted arguments when handed the same ids array
+    again: the array's new contents (rows released in place) must still be used."""
+    c = workloads.small(seed=81, n=48, d_in=256, d_out=384, n_adapters=3, ranks=[8, 16, 32])
+    table = upload_table(ctx, c)
+    x = to_dev(c["x"])
+    y_ref, y_got = to_dev(c["y"]), to_dev(c["y"])
+    call = L.PreparedFused(ctx, table, x, y_got)
+    ids = np.ascontiguousarray(c["ids"], np.int32).copy()
+    for step in range(3):
+        if step == 2:
+            ids[::3] = -1                       # the same buffer, rewritten in place
+        L.lora_fused(ctx, table, ids.copy(), x, y_ref)
+        call(ids)
+        ctx.sync_status()
+        np.testing.assert_array_equal(from_dev(y_got), from_dev(y_ref))
