@@ -79,6 +79,8 @@ struct lora_ctx {
     size_t dense_cap = 0;
     std::vector<int32_t> slot_of;   // adapter -> slot while a call's slots are assigned
     std::unique_ptr<TileParams> tparams;   // launch parameters of the tile kernels
+    uint8_t *flush = nullptr;       // lora_tune_shape: a buffer larger than L2, written
+                                    // before each timed call so that it starts cold
 };
 
 struct lora_table {
@@ -289,7 +291,7 @@ RowsCfg choose_rows_cfg(const lora_ctx *ctx, int mode, int kind, int64_t n_act, 
     if (ctx->force_cluster > 0 && ctx->force_rows > 0)
         return RowsCfg{ctx->force_cluster, ctx->force_rows};
     TileCfg tc;
-    if (ctx->tiles.lookup(TileKey{kind, pow2_bucket(n_act), d_in, d_out, rank}, tc) &&
+    if (ctx->tiles.lookup(TileKey{kind, pow2_bucket(n_act), pow2_bucket(n_seg), d_in, d_out, rank}, tc) &&
         tc[0] >= 1 && tc[0] <= 16 && (tc[0] & (tc[0] - 1)) == 0 && tc[1] >= 1 && tc[1] <= 64) {
         cfg.cluster = tc[0];
         cfg.rows = tc[1];
@@ -379,7 +381,7 @@ int tile_min_run(const lora_ctx *ctx, int64_t n_act, int d_in, int d_out, int ra
     if (ctx->tile_min_run_override > 0)
         return ctx->tile_min_run_override;
     TileCfg tc;
-    if (ctx->tiles.lookup(TileKey{kKindTileFused, pow2_bucket(n_act), d_in, d_out, rank}, tc))
+    if (ctx->tiles.lookup(TileKey{kKindTileFused, pow2_bucket(n_act), 0, d_in, d_out, rank}, tc))
         return tc[0];
     return 128;
 }
@@ -704,7 +706,7 @@ int merge_call(lora_ctx *ctx, const lora_table *t, int adapter, void *W, int64_t
     p.scale = sign * t->scale[size_t(adapter)];
     int path = ctx->merge_path;
     TileCfg tcfg;
-    if (path == 0 && ctx->tiles.lookup(TileKey{kKindMerge, pow2_bucket(d_in), d_in, d_out, p.rank},
+    if (path == 0 && ctx->tiles.lookup(TileKey{kKindMerge, pow2_bucket(d_in), 0, d_in, d_out, p.rank},
                                        tcfg))
         path = tcfg[0];
     const bool tc = merge_tc_supported(d_in, d_out, p.rank) && path != 1;
@@ -857,6 +859,8 @@ int lora_ctx_destroy(lora_ctx *ctx)
         cudaFree(ctx->vparts);
     if (ctx->dense)
         cudaFree(ctx->dense);
+    if (ctx->flush)
+        cudaFree(ctx->flush);
     cudaSetDevice(prev);
     delete ctx;
     return LORA_OK;
@@ -1197,7 +1201,12 @@ int lora_tune_shape(lora_ctx *ctx, const lora_table *t, int kind, const int32_t 
     int rc = use_device(ctx);
     if (rc != LORA_OK)
         return rc;
-    // One candidate: warm up twice, then the mean of `iters` timed calls.
+    // One candidate: warm up twice, then the median of `iters` calls, each timed
+    // alone and started with L2 cold (a 256 MB write first), as a serving step meets
+    // its adapters after the rest of the model has streamed through the cache.
+    constexpr size_t kFlushBytes = size_t(256) << 20;
+    if (!ctx->flush && cudaMalloc(reinterpret_cast<void **>(&ctx->flush), kFlushBytes) != cudaSuccess)
+        return LORA_E_NOMEM;
     cudaEvent_t e0, e1;
     CUDA_TRY(ctx, cudaEventCreate(&e0));
     CUDA_TRY(ctx, cudaEventCreate(&e1));
@@ -1215,18 +1224,23 @@ int lora_tune_shape(lora_ctx *ctx, const lora_table *t, int kind, const int32_t 
             if (r2 != LORA_OK)
                 return r2;
         }
-        if (cudaEventRecord(e0, stream) != cudaSuccess)
-            return LORA_E_CUDA;
+        std::vector<float> t_ms;
+        t_ms.reserve(size_t(iters));
         for (int i = 0; i < iters; ++i) {
+            if (cudaMemsetAsync(ctx->flush, i & 0xff, kFlushBytes, stream) != cudaSuccess ||
+                cudaEventRecord(e0, stream) != cudaSuccess)
+                return LORA_E_CUDA;
             int r2 = call();
             if (r2 != LORA_OK)
                 return r2;
+            if (cudaEventRecord(e1, stream) != cudaSuccess || cudaEventSynchronize(e1) != cudaSuccess)
+                return LORA_E_CUDA;
+            float ms = 0.f;
+            cudaEventElapsedTime(&ms, e0, e1);
+            t_ms.push_back(ms);
         }
-        if (cudaEventRecord(e1, stream) != cudaSuccess || cudaEventSynchronize(e1) != cudaSuccess)
-            return LORA_E_CUDA;
-        float ms = 0.f;
-        cudaEventElapsedTime(&ms, e0, e1);
-        us = 1000.f * ms / float(iters);
+        std::nth_element(t_ms.begin(), t_ms.begin() + iters / 2, t_ms.end());
+        us = 1000.f * t_ms[size_t(iters / 2)];
         return LORA_OK;
     };
     // The key of the shape, as the runtime will look it up.
@@ -1243,6 +1257,7 @@ int lora_tune_shape(lora_ctx *ctx, const lora_table *t, int kind, const int32_t 
         rmax = t->rank[size_t(ids[0])];
     const int64_t n_act = int64_t(ctx->plan.active.size());
     const TileKey key{kind, kind == kKindMerge ? pow2_bucket(d_in) : pow2_bucket(n_act),
+                      kind == kKindRowsFused ? pow2_bucket(int64_t(ctx->plan.seg_adapter.size())) : 0,
                       d_in, d_out, rmax};
     float best = -1.f;
     TileCfg best_cfg{0, 0, 0, 0};
@@ -1274,7 +1289,9 @@ int lora_tune_shape(lora_ctx *ctx, const lora_table *t, int kind, const int32_t 
         }
         ctx->force_cluster = ctx->force_rows = 0;
     } else if (kind == kKindTileFused) {
-        const int runs[] = {32, 64, 128, 256, 512, 1 << 30};
+        // Up to 256: a longer minimum would send prompt-length runs of a batch with
+        // mixed lengths to the row-gather kernel, which the tuned shape may not show.
+        const int runs[] = {32, 64, 128, 256};
         for (int m : runs) {
             ctx->tile_min_run_override = m;
             float us = 0.f;

@@ -1,11 +1,12 @@
 // Text form of the shape -> configuration table: one entry per line,
-//   kind m_bucket d_in d_out rank cfg0 cfg1 cfg2 cfg3
-// '#' starts a comment.
+//   kind m_bucket s_bucket d_in d_out rank cfg0 cfg1 cfg2 cfg3
+// '#' starts a comment.  Lines without s_bucket (nine fields) read it as 0.
 #include "tiles.h"
 
 #include <cstdio>
 #include <fstream>
 #include <sstream>
+#include <vector>
 
 #include "../../include/lora.h"
 
@@ -23,13 +24,21 @@ int TileTable::load(const std::string &path)
         if (hash != std::string::npos)
             line.resize(hash);
         std::istringstream ss(line);
-        TileKey k{};
-        TileCfg c{};
-        if (!(ss >> k.kind))
-            continue;   // blank line
-        if (!(ss >> k.m_bucket >> k.d_in >> k.d_out >> k.rank >> c[0] >> c[1] >> c[2] >> c[3]))
+        std::vector<int64_t> f;
+        int64_t v = 0;
+        while (ss >> v)
+            f.push_back(v);
+        if (!ss.eof())
+            return LORA_E_INVAL;   // a field that is not an integer
+        if (f.empty())
+            continue;              // blank line
+        if (f.size() == 9)
+            f.insert(f.begin() + 2, 0);
+        if (f.size() != 10)
             return LORA_E_INVAL;
-        if (k.kind < 0 || k.kind > 4 || k.m_bucket < 0)
+        TileKey k{int(f[0]), f[1], f[2], int(f[3]), int(f[4]), int(f[5])};
+        TileCfg c{int(f[6]), int(f[7]), int(f[8]), int(f[9])};
+        if (k.kind < 0 || k.kind > 4 || k.m_bucket < 0 || k.s_bucket < 0)
             return LORA_E_INVAL;
         fresh[k] = c;
     }
@@ -43,11 +52,12 @@ int TileTable::save(const std::string &path) const
     std::ofstream out(path);
     if (!out)
         return LORA_E_IO;
-    out << "# kind m_bucket d_in d_out rank cfg0 cfg1 cfg2 cfg3\n";
+    out << "# kind m_bucket s_bucket d_in d_out rank cfg0 cfg1 cfg2 cfg3\n";
     for (const auto &kv : map) {
         const TileKey &k = kv.first;
         const TileCfg &c = kv.second;
-        out << k.kind << ' ' << k.m_bucket << ' ' << k.d_in << ' ' << k.d_out << ' ' << k.rank
+        out << k.kind << ' ' << k.m_bucket << ' ' << k.s_bucket << ' ' << k.d_in << ' ' << k.d_out
+            << ' ' << k.rank
             << ' ' << c[0] << ' ' << c[1] << ' ' << c[2] << ' ' << c[3] << '\n';
     }
     return out ? LORA_OK : LORA_E_IO;

@@ -1,6 +1,8 @@
 // Shape -> launch-configuration table (VaLoRA blog, section 4.3.2: the best tiling
 // for each input shape is found offline, kept in a hash table and looked up at run
-// time).  Keys bucket the row count to the next power of two.
+// time).  Keys bucket the row count to the next power of two; row-gather keys also
+// bucket the number of distinct adapters (one segment per adapter), which decides
+// how many rows a work item can hold.
 #pragma once
 #include <array>
 #include <cstdint>
@@ -15,11 +17,12 @@ enum Kind : int { kKindRowsFused = 0, kKindShrink = 1, kKindExpand = 2, kKindTil
 struct TileKey {
     int kind;
     int64_t m_bucket;
+    int64_t s_bucket;         // row-gather kinds: distinct adapters, bucketed; else 0
     int d_in, d_out, rank;
     bool operator==(const TileKey &o) const
     {
-        return kind == o.kind && m_bucket == o.m_bucket && d_in == o.d_in && d_out == o.d_out &&
-               rank == o.rank;
+        return kind == o.kind && m_bucket == o.m_bucket && s_bucket == o.s_bucket &&
+               d_in == o.d_in && d_out == o.d_out && rank == o.rank;
     }
 };
 
@@ -27,7 +30,7 @@ struct TileKeyHash {
     size_t operator()(const TileKey &k) const
     {
         uint64_t h = 1469598103934665603ull;
-        const int64_t parts[5] = {k.kind, k.m_bucket, k.d_in, k.d_out, k.rank};
+        const int64_t parts[6] = {k.kind, k.m_bucket, k.s_bucket, k.d_in, k.d_out, k.rank};
         for (int64_t p : parts) {
             h ^= uint64_t(p);
             h *= 1099511628211ull;

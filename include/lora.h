@@ -175,16 +175,21 @@ int lora_unmerge(lora_ctx *ctx, const lora_table *table, int adapter, void *W,
 /* Shape -> tile-configuration table (VaLoRA blog, section 4.3.2: an offline
  * search stores the best tiling per input shape in a hash table that the runtime
  * looks up).  Lines of the text file are
- *     kind m_bucket d_in d_out rank  cfg0 cfg1 cfg2 cfg3
+ *     kind m_bucket s_bucket d_in d_out rank  cfg0 cfg1 cfg2 cfg3
  * kind: 0 row-gather fused, 1 shrink, 2 expand, 3 tile fused, 4 merge.
- * Unknown shapes use a built-in default; a lookup never fails. */
+ * m_bucket: active rows (merge: d_in) rounded up to a power of two; s_bucket:
+ * for kind 0 the number of distinct adapters, rounded up likewise, else 0.  A
+ * line with nine fields has no s_bucket (read as 0).  Unknown shapes use a
+ * built-in default; a lookup never fails. */
 int lora_tiles_load(lora_ctx *ctx, const char *path);
 int lora_tiles_save(const lora_ctx *ctx, const char *path);
 int64_t lora_tiles_count(const lora_ctx *ctx);
 
 /* Offline search for one shape (VaLoRA blog, section 4.3.2): times every
  * candidate of a pruned configuration space with CUDA events (two warm-up calls,
- * then the mean of `iters` calls), keeps the fastest in the context's table under
+ * then the median of `iters` calls, each timed alone after a 256 MB write that
+ * leaves L2 cold; the context allocates that buffer on its first search and frees
+ * it with the context), keeps the fastest in the context's table under
  * the key the runtime looks up, and returns its time in *best_us.
  *   kind 0 (row-gather fused): cluster width x rows per item;
  *   kind 3 (tile fused):       minimum run length routed to the tensor-core tiles;

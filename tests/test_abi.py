@@ -132,13 +132,17 @@ def test_tile_table_file_round_trip(tmp_path):
     import adapter_sgmv_bgmv_gb300 as L
     ctx, _ = _host_table()
     f = tmp_path / "tiles.tbl"
-    f.write_text("# comment\n0 64 4096 4096 16 8 1 0 0\n4 4096 4096 11008 64 2 0 0 0\n\n")
+    # one line with the adapter bucket, one without it (nine fields: bucket 0), and
+    # the same row shape again for a different number of adapters (a separate key)
+    f.write_text("# comment\n0 64 64 4096 4096 16 8 1 0 0\n4 4096 4096 11008 64 2 0 0 0\n"
+                 "0 64 1 4096 4096 16 16 4 0 0\n\n")
     ctx.tiles_load(str(f))
-    assert ctx.tiles_count() == 2
+    assert ctx.tiles_count() == 3
     out = tmp_path / "out.tbl"
     ctx.tiles_save(str(out))
     rows = sorted(l for l in out.read_text().splitlines() if not l.startswith("#"))
-    assert rows == ["0 64 4096 4096 16 8 1 0 0", "4 4096 4096 11008 64 2 0 0 0"]
+    assert rows == ["0 64 1 4096 4096 16 16 4 0 0", "0 64 64 4096 4096 16 8 1 0 0",
+                    "4 4096 0 4096 11008 64 2 0 0 0"]
     bad = tmp_path / "bad.tbl"
     bad.write_text("0 64 4096\n")
     with pytest.raises(L.LoraError):
