@@ -71,6 +71,7 @@ struct lora_ctx {
     int merge_path = 0;             // 0 auto (tensor cores when supported), 1 CUDA cores
     int tile_path = 1;              // 1: long same-adapter runs use the tensor-core tiles
     int tile_min_run_override = 0;  // > 0: fixed minimum run for the tile path
+    int early_pages = 0;            // LORA_OPT_EARLY_PAGES
     int force_cluster = 0;          // > 0 while tuning: row-kernel cluster width
     int force_rows = 0;             // > 0 while tuning: rows per item
     uint8_t *vparts = nullptr;      // fused tile path: partial V between its two kernels
@@ -351,6 +352,7 @@ int run_rows(lora_ctx *ctx, const lora_table *t, int mode, RowsCfg cfg, const vo
     p.d_in = d_in;
     p.d_out = d_out;
     p.n_items = int(pl.row_items.size());
+    p.early_pages = ctx->early_pages;
     const long ev = prof_start(ctx, 0, stream);
     if (in_params && pl.row_items.size() <= 64 && pl.row_perm.size() <= 128) {
         RowsParamsInlineSmall &a = ctx->inline_small;
@@ -1136,6 +1138,7 @@ int lora_ctx_set_option(lora_ctx *ctx, int option, int value)
             return LORA_E_INVAL;
         ctx->tile_min_run_override = value;
         return LORA_OK;
+    case LORA_OPT_EARLY_PAGES: ctx->early_pages = value ? 1 : 0; return LORA_OK;
     default: return LORA_E_INVAL;
     }
 }

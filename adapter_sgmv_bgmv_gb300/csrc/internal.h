@@ -60,6 +60,7 @@ struct RowsParams {
     int slice_in;             // elements of d_in per CTA (multiple of 8)
     int slice_out;            // elements of d_out per CTA (multiple of 8)
     int rows_alloc;           // shared-memory rows per item (>= every item's nrows)
+    int early_pages;          // 1: adapter page copies issued before the dependency wait
     int rank_alloc;           // shared-memory rank slots (>= every item's rank)
 };
 

@@ -126,9 +126,9 @@ __device__ __forceinline__ void rows_body(const RowsParams &pin, const RowItem *
     // have written (x, y, v, the pools) is touched only after the wait.
     const uint32_t in_bytes = uint32_t(in_len) * 2u, out_bytes = uint32_t(out_len) * 2u;
     int32_t pa0 = 0, pa1 = 0, pb0 = 0, pb1 = 0, pr0 = 0, pr1 = 0;
+    const int32_t *ap = p.a_pages + size_t(k) * p.max_rank;
+    const int32_t *bp = p.b_pages + size_t(k) * p.max_rank;
     if (warp == 0) {
-        const int32_t *ap = p.a_pages + size_t(k) * p.max_rank;
-        const int32_t *bp = p.b_pages + size_t(k) * p.max_rank;
         if (lane < r) {
             if (MODE != kExpand)
                 pa0 = ap[lane];
@@ -148,7 +148,21 @@ __device__ __forceinline__ void rows_body(const RowsParams &pin, const RowItem *
         for (int q = lane; q < nrows; q += 32)
             s_rows[q] = q < 32 ? pr0 : q < 64 ? pr1 : perm[it.p0 + q];
     }
-    grid_dep_wait();
+    // Adapter pages first (by lane j < r), then the rows (lane i < nrows); with
+    // early_pages the page copies go out before waiting for the preceding kernel
+    // (the pools are not that kernel's to write), overlapping its tail.
+    auto issue_pages = [&]() {
+        for (int q = lane; q < r; q += 32) {
+            const int32_t qa = q < 32 ? pa0 : q < 64 ? pa1 : (MODE != kExpand ? ap[q] : 0);
+            const int32_t qb = q < 32 ? pb0 : q < 64 ? pb1 : (MODE != kShrink ? bp[q] : 0);
+            if (MODE != kExpand && in_bytes)
+                bulk_g2s(smem_u32(sA + size_t(q) * p.slice_in),
+                         p.a_pool + int64_t(qa) * p.a_pw + in0, in_bytes, bar0);
+            if (MODE != kShrink && out_bytes)
+                bulk_g2s(smem_u32(sB + size_t(q) * p.slice_out),
+                         p.b_pool + int64_t(qb) * p.b_pw + out0, out_bytes, bar1);
+        }
+    };
     if (warp == 0) {
         if (lane == 0) {
             if (MODE != kExpand)
@@ -157,40 +171,21 @@ __device__ __forceinline__ void rows_body(const RowsParams &pin, const RowItem *
                 mbar_arrive_expect_tx(bar1, uint32_t(r + nrows) * out_bytes);
         }
         __syncwarp();
-        const int32_t *ap = p.a_pages + size_t(k) * p.max_rank;
-        const int32_t *bp = p.b_pages + size_t(k) * p.max_rank;
-        for (int q = lane; q < r || q < nrows; q += 32) {
-            const int h = q >> 5;
-            int32_t qa, qb, row;
-            if (h == 0) {
-                qa = pa0;
-                qb = pb0;
-                row = pr0;
-            } else if (h == 1) {
-                qa = pa1;
-                qb = pb1;
-                row = pr1;
-            } else {   // ranks or rows beyond 64 (rank 128): read them now
-                qa = (MODE != kExpand && q < r) ? ap[q] : 0;
-                qb = (MODE != kShrink && q < r) ? bp[q] : 0;
-                row = q < nrows ? perm[it.p0 + q] : 0;
-            }
-            if (q < nrows) {
-                if (MODE != kExpand && in_bytes)
-                    bulk_g2s(smem_u32(sX + size_t(q) * p.slice_in),
-                             p.x + int64_t(row) * p.ldx + in0, in_bytes, bar0);
-                if (MODE != kShrink && out_bytes)
-                    bulk_g2s(smem_u32(sY + size_t(q) * p.slice_out),
-                             p.y + int64_t(row) * p.ldy + out0, out_bytes, bar1);
-            }
-            if (q < r) {
-                if (MODE != kExpand && in_bytes)
-                    bulk_g2s(smem_u32(sA + size_t(q) * p.slice_in),
-                             p.a_pool + int64_t(qa) * p.a_pw + in0, in_bytes, bar0);
-                if (MODE != kShrink && out_bytes)
-                    bulk_g2s(smem_u32(sB + size_t(q) * p.slice_out),
-                             p.b_pool + int64_t(qb) * p.b_pw + out0, out_bytes, bar1);
-            }
+        if (p.early_pages)
+            issue_pages();
+    }
+    grid_dep_wait();
+    if (warp == 0) {
+        if (!p.early_pages)
+            issue_pages();
+        for (int q = lane; q < nrows; q += 32) {
+            const int row = s_rows[q];
+            if (MODE != kExpand && in_bytes)
+                bulk_g2s(smem_u32(sX + size_t(q) * p.slice_in), p.x + int64_t(row) * p.ldx + in0,
+                         in_bytes, bar0);
+            if (MODE != kShrink && out_bytes)
+                bulk_g2s(smem_u32(sY + size_t(q) * p.slice_out), p.y + int64_t(row) * p.ldy + out0,
+                         out_bytes, bar1);
         }
     }
     grid_dep_launch();

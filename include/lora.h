@@ -206,14 +206,24 @@ int lora_tune_shape(lora_ctx *ctx, const lora_table *table, int kind,
  * LORA_E_TIMEOUT if a kernel's bounded wait expired since the last check. */
 int lora_sync_status(lora_ctx *ctx, void *stream);
 
-/* Context options (all default to the fastest choice):
+/* Context options:
  *   LORA_OPT_TILE_PATH     1 (default) route runs of >= tile_min_run consecutive
  *                          same-adapter rows to the tensor-core tile kernels; 0 keeps
  *                          every row on the row-gather kernel
  *   LORA_OPT_MERGE_KERNEL  0 (default) tensor-core merge where supported; 1 CUDA cores
  *   LORA_OPT_TILE_MIN_RUN  > 0 fixes the minimum run length; 0 uses the tile table
- *                          (default 128) */
-enum { LORA_OPT_TILE_PATH = 1, LORA_OPT_MERGE_KERNEL = 2, LORA_OPT_TILE_MIN_RUN = 3 };
+ *                          (default 128)
+ *   LORA_OPT_EARLY_PAGES   0 (default) / 1.  The kernels are launched as programmatic
+ *                          dependents of the kernel before them in the stream and
+ *                          read nothing that kernel may write before it finishes.  With
+ *                          1 the row-gather kernel copies the adapter pages (A and B
+ *                          pools) before that wait, overlapping the previous kernel's
+ *                          tail.  The caller then guarantees that no kernel launched
+ *                          immediately before a delta call in the same stream writes
+ *                          the pools (this library's own kernels never do; a copy or a
+ *                          host-side wait in between is enough). */
+enum { LORA_OPT_TILE_PATH = 1, LORA_OPT_MERGE_KERNEL = 2, LORA_OPT_TILE_MIN_RUN = 3,
+       LORA_OPT_EARLY_PAGES = 4 };
 int lora_ctx_set_option(lora_ctx *ctx, int option, int value);
 
 /* Per-launch timing: between lora_profile_begin and lora_profile_end every

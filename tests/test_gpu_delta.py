@@ -266,3 +266,28 @@ def test_prepared_fused_matches_lora_fused_and_reads_a_rewritten_ids_buffer(ctx)
         call(ids)
         ctx.sync_status()
         np.testing.assert_array_equal(from_dev(y_got), from_dev(y_ref))
+
+
+@pytest.mark.parametrize("name", ["llama7b_decode_het", "llama7b_decode_hom"])
+def test_early_page_copies_change_nothing(ctx, name):
+    """LORA_OPT_EARLY_PAGES only moves the adapter-page copies ahead of the wait for
+    the previous kernel: results are bit-identical with the option off, and within
+    the bar of the oracle."""
+    c = workloads.make(name, seed=5)
+    table = upload_table(ctx, c)
+    x = to_dev(c["x"])
+    got = {}
+    for early in (0, 1):
+        ctx.set_option(L.OPT_EARLY_PAGES, early)
+        try:
+            y = to_dev(c["y"])
+            for _ in range(3):          # back to back, so the overlap actually happens
+                y.copy_(to_dev(c["y"]))
+                L.lora_fused(ctx, table, c["ids"], x, y)
+            ctx.sync_status()
+            got[early] = from_dev(y)
+        finally:
+            ctx.set_option(L.OPT_EARLY_PAGES, 0)
+    np.testing.assert_array_equal(got[1], got[0])
+    ref = oracle.fused(oracle.Table.from_case(c), c["ids"], c["x"], c["y"], nthreads=8)
+    assert_parity(got[1], ref, REL_FROB, MAX_ABS_RMS, name)
