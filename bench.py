@@ -13,6 +13,8 @@ on a bounded sample of the same workload.  `--all` prints one line per workload.
 from __future__ import annotations
 
 import argparse
+import ctypes
+import glob
 import json
 import math
 import os
@@ -133,6 +135,17 @@ def alg_bytes_delta(case, ids):
     return 2 * n_act * d_in + 4 * n_act * d_out + ab + 4 * n_act + 16 * len(distinct)
 
 
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) of the
+# dominant kernel family, from the ncu captures summarised in profiles/ (taken on
+# the kernels as they are now; a change to one of these kernels voids its entry).
+# Configurations without a capture report null.
+MEASURED_TRAFFIC = {
+    ("llama7b_decode", "rows"): (17.88e6 + 1.36e6) / 2,   # profiles/rows_llama7b_decode.md
+    ("valora_prefill", "expand"): 725.30e6,                # profiles/stream_tile_valora_prefill.md
+    ("valora_merge", "merge"): 123.00e6,                   # profiles/stream_merge_valora.md
+}
+
+
 def alg_bytes_split(case, ids, tiles: bool) -> dict:
     """alg_bytes_delta split by the kernel family that moves each part: on the tile
     path the shrink reads x and the A pages, the expand reads and writes y and reads
@@ -225,24 +238,40 @@ class Bench:
                 d["x"] = to_dev(c["x"])
                 d["y"] = to_dev(c["y"])
             base[key] = d
+        # Per set, the step's activations sit in one block, every x first and every y
+        # after it, so that the end-to-end loop copies a step in with one copy and
+        # reads its result back with another.
+        keys = list(self.cases)
+        fields = [] if self.is_merge else [(k, "x") for k in keys] + [(k, "y") for k in keys]
+        self.blk_elems = sum(base[k][f].numel() for k, f in fields)
+        self.y_offset = sum(base[k]["x"].numel() for k in keys) if not self.is_merge else 0
         for s in range(self.n_sets):
             st = {}
+            blk = torch.empty(max(1, self.blk_elems), dtype=torch.bfloat16, device="cuda")
+            views, off = {}, 0
+            for k, f in fields:
+                t = base[k][f]
+                views[(k, f)] = blk[off:off + t.numel()].view(t.shape)
+                views[(k, f)].copy_(t)
+                off += t.numel()
             for key, c in self.cases.items():
                 b = base[key]
                 if s == 0:
-                    d = dict(b)
+                    d = {"a_pool": b["a_pool"], "b_pool": b["b_pool"]}
                 else:
                     d = {"a_pool": b["a_pool"].clone()}
                     d["b_pool"] = d["a_pool"] if b["b_pool"] is b["a_pool"] else b["b_pool"].clone()
-                    for f in ("x", "y", "W"):
-                        if f in b:
-                            d[f] = b[f].clone()
+                if self.is_merge:
+                    d["W"] = b["W"] if s == 0 else b["W"].clone()
+                else:
+                    d["x"], d["y"] = views[(key, "x")], views[(key, "y")]
                 d["table"] = L.AdapterTable(self.ctx, d["a_pool"], d["b_pool"], c["rank"],
                                             c["scale"], c["a_pages"], c["b_pages"])
                 if not self.is_merge:
                     d["call"] = L.PreparedFused(self.ctx, d["table"], d["x"], d["y"],
                                                 torch.cuda.current_stream())
                 st[key] = d
+            st["_blk"] = blk
             self.sets.append(st)
         torch.cuda.synchronize()
 
@@ -304,39 +333,126 @@ class Bench:
 
     # ---- end to end through host buffers
     def e2e_setup(self):
+        """Pinned host copies of a step's inputs (one block, laid out as on the
+        device), per device set a pinned result buffer and three events, and two
+        copy streams.  The loop issues its copies and event operations through the
+        CUDA runtime with arguments built here, so a step costs the host little more
+        than the library calls themselves."""
         torch = self.torch
-        self.host = {}
-        for key, c in self.cases.items():
-            if self.is_merge:
-                self.host[key] = {"W": torch.from_numpy(c["W"].view(np.int16)).pin_memory()}
-            else:
-                self.host[key] = {
-                    "x": torch.from_numpy(c["x"].view(np.int16)).pin_memory(),
-                    "y": torch.from_numpy(c["y"].view(np.int16)).pin_memory(),
-                    "y_out": torch.empty(c["y"].shape, dtype=torch.int16).pin_memory()}
+        if self.is_merge:
+            w = self.cases["main"]["W"]
+            self.host_in = torch.from_numpy(w.view(np.int16).reshape(-1)).pin_memory()
+            self.out_elems = w.size
+        else:
+            parts = [self.cases[k]["x"] for k in self.cases] + [self.cases[k]["y"] for k in self.cases]
+            self.host_in = torch.from_numpy(
+                np.concatenate([p.view(np.int16).reshape(-1) for p in parts])).pin_memory()
+            self.out_elems = self.blk_elems - self.y_offset
+        self.host_out = [torch.empty(self.out_elems, dtype=torch.int16).pin_memory()
+                         for _ in range(self.n_sets)]
+        self.s_in, self.s_out = torch.cuda.Stream(), torch.cuda.Stream()
+        rt = _runtime()
+        self.rt = rt
+        V, S = ctypes.c_void_p, ctypes.c_size_t
+        in_bytes, out_bytes = self.host_in.numel() * 2, self.out_elems * 2
+        s_in, s_out = V(self.s_in.cuda_stream), V(self.s_out.cuda_stream)
+        s_comp = V(torch.cuda.current_stream().cuda_stream)
+        self.e2e_ops = []
+        for k in range(self.n_sets):
+            ev = []
+            for _ in range(3):
+                e = V()
+                _rt_check(rt.cudaEventCreateWithFlags(ctypes.byref(e), 2))   # no timing
+                ev.append(e)
+            blk = self._dev_block(self.sets[k])
+            dev_in, dev_out = V(blk.data_ptr()), V(blk.data_ptr() + 2 * self.y_offset)
+            self.e2e_ops.append({
+                "refill_wait": (s_in, ev[2], 0),
+                "copy_in": (dev_in, V(self.host_in.data_ptr()), S(in_bytes), 1, s_in),
+                "rec_in": (ev[0], s_in), "wait_in": (s_comp, ev[0], 0),
+                "rec_c": (ev[1], s_comp), "wait_c": (s_out, ev[1], 0),
+                "copy_out": (V(self.host_out[k].data_ptr()), dev_out, S(out_bytes), 2, s_out),
+                "rec_out": (ev[2], s_out), "drain": (s_comp, ev[2], 0)})
+        self.used = [False] * self.n_sets
+        self.e2e_bytes = (in_bytes, out_bytes)
+
+    def _dev_block(self, st):
+        if self.is_merge:
+            return st["main"]["W"]
+        return st["_blk"]
 
     def e2e_step(self, i: int, stream):
-        st = self.sets[i % self.n_sets]
-        L = self.L
-        h2d = d2h = 0
+        """One step end to end, pipelined with its neighbours: step i's inputs are
+        copied in on one stream while step i-1 computes and step i-2's result is read
+        back on another.  A device set is refilled only after its previous result
+        has been read back."""
+        k = i % self.n_sets
+        st, op, rt = self.sets[k], self.e2e_ops[k], self.rt
+        if self.used[k]:
+            _rt_check(rt.cudaStreamWaitEvent(*op["refill_wait"]))
+        self.used[k] = True
+        _rt_check(rt.cudaMemcpyAsync(*op["copy_in"]))
+        _rt_check(rt.cudaEventRecord(*op["rec_in"]))
+        _rt_check(rt.cudaStreamWaitEvent(*op["wait_in"]))
+        h2d = self.e2e_bytes[0]
         if self.is_merge:
-            d, h = st["main"], self.host["main"]
-            d["W"].view(self.torch.int16).copy_(h["W"], non_blocking=True)
-            k = self.cases["main"]["merge_adapter"]
-            L.lora_merge(self.ctx, d["table"], k, d["W"], stream)
-            L.lora_unmerge(self.ctx, d["table"], k, d["W"], stream)
-            h["W"].copy_(d["W"].view(self.torch.int16), non_blocking=True)
-            nb = h["W"].numel() * 2
-            return nb, nb
-        for key, ids in self.steps_ids[i % len(self.steps_ids)]:
-            d, h = st[key], self.host[key]
-            d["x"].view(self.torch.int16).copy_(h["x"], non_blocking=True)
-            d["y"].view(self.torch.int16).copy_(h["y"], non_blocking=True)
-            L.lora_fused(self.ctx, d["table"], ids, d["x"], d["y"], stream)
-            h["y_out"].copy_(d["y"].view(self.torch.int16), non_blocking=True)
-            h2d += (h["x"].numel() + h["y"].numel()) * 2 + 4 * len(ids)
-            d2h += h["y_out"].numel() * 2
-        return h2d, d2h
+            d = st["main"]
+            a = self.cases["main"]["merge_adapter"]
+            self.L.lora_merge(self.ctx, d["table"], a, d["W"], stream)
+            self.L.lora_unmerge(self.ctx, d["table"], a, d["W"], stream)
+        else:
+            for key, ids in self.steps_ids[i % len(self.steps_ids)]:
+                st[key]["call"](ids)
+                h2d += 4 * len(ids)
+        _rt_check(rt.cudaEventRecord(*op["rec_c"]))
+        _rt_check(rt.cudaStreamWaitEvent(*op["wait_c"]))
+        _rt_check(rt.cudaMemcpyAsync(*op["copy_out"]))
+        _rt_check(rt.cudaEventRecord(*op["rec_out"]))
+        return h2d, self.e2e_bytes[1]
+
+    def e2e_drain(self, stream):
+        """Make the compute stream wait for every read-back issued so far."""
+        for k in range(self.n_sets):
+            if self.used[k]:
+                _rt_check(self.rt.cudaStreamWaitEvent(*self.e2e_ops[k]["drain"]))
+
+
+class _RuntimeFns:
+    pass
+
+
+_RT = None
+
+
+def _runtime():
+    """The CUDA runtime's copy / event / stream-wait entry points, each a foreign
+    function without argument types (called with ready-made ctypes objects)."""
+    global _RT
+    if _RT is not None:
+        return _RT
+    import ctypes.util
+    cands = ["/usr/local/cuda/lib64/libcudart.so", ctypes.util.find_library("cudart")]
+    cands += sorted(glob.glob(os.path.join(os.path.dirname(np.__file__), "..", "nvidia", "*", "lib",
+                                           "libcudart.so*")))
+    for path in cands:
+        if path and os.path.exists(path):
+            lib = ctypes.CDLL(path)
+            break
+    else:
+        raise RuntimeError("no CUDA runtime library found for the end-to-end loop")
+    rt = _RuntimeFns()
+    for name in ("cudaMemcpyAsync", "cudaEventRecord", "cudaStreamWaitEvent",
+                 "cudaEventCreateWithFlags"):
+        fn = lib._FuncPtr((name, lib))
+        fn.restype = ctypes.c_int
+        setattr(rt, name, fn)
+    _RT = rt
+    return rt
+
+
+def _rt_check(rc: int):
+    if rc != 0:
+        raise RuntimeError(f"CUDA runtime call failed with error {rc}")
 
 
 # --------------------------------------------------------------------------- oracle leg
@@ -549,7 +665,8 @@ def run_one(name, args, L, torch, ctx, dist, world, rank, local):
         "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": pk["hbm_gbs"],
                      "unit": "GB/s",
                      "frac": (achieved_gbs / pk["hbm_gbs"]) if achieved_gbs else None,
-                     "traffic": None, "peak_source": pk["source"],
+                     "traffic": MEASURED_TRAFFIC.get((name, dominant)),
+                     "peak_source": pk["source"],
                      "kernel": kernel_names[dominant],
                      "bytes_per_launch": per_family[dominant]["alg_bytes_per_launch"],
                      "us_per_launch": per_family[dominant]["us_per_launch"],
@@ -566,11 +683,14 @@ def run_one(name, args, L, torch, ctx, dist, world, rank, local):
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
+    e0.record(b.s_in)            # the first thing of the timed region is a copy in
+    stream.wait_event(e0)
+    b.s_out.wait_event(e0)
     h2d = d2h = 0
     for i in range(Ke):
         hb, db = b.e2e_step(i, stream)
         h2d, d2h = hb, db
+    b.e2e_drain(stream)          # ... and the last is a read back
     e1.record(stream)
     torch.cuda.synchronize()
     es = e0.elapsed_time(e1) / 1e3
