@@ -20,8 +20,17 @@ def ctx():
     c.close()
 
 
+@pytest.mark.parametrize("kernel", [0, 1], ids=["tensor_cores", "cuda_cores"])
 @pytest.mark.parametrize("shape", [(96, 80, [16, 8]), (200, 264, [64, 32]), (128, 256, [8, 24])])
-def test_merge_small_full(ctx, shape):
+def test_merge_small_full(ctx, shape, kernel):
+    ctx.set_option(L.OPT_MERGE_KERNEL, kernel)
+    try:
+        _merge_small_full(ctx, shape)
+    finally:
+        ctx.set_option(L.OPT_MERGE_KERNEL, 0)
+
+
+def _merge_small_full(ctx, shape):
     d_in, d_out, ranks = shape
     c = workloads.small(seed=41, n=1, d_in=d_in, d_out=d_out, n_adapters=len(ranks),
                         ranks=ranks, paged=True)
