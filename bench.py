@@ -513,6 +513,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0,
                     help="seconds of oracle time for the cpu_baseline")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--cpu-threads", type=int, default=0,
+                    help="host threads for the oracle (0: every core)")
     ap.add_argument("--no-early-pages", action="store_true",
                     help="keep the adapter-page copies behind the dependency wait")
     ap.add_argument("--profile-every", type=int, default=8,
@@ -701,7 +703,7 @@ def run_one(name, args, L, torch, ctx, dist, world, rank, local):
     line["e2e"] = {"value": e2e_val, "unit": unit, "h2d_bytes_per_step": h2d,
                    "d2h_bytes_per_step": d2h}
     if rank == 0 and world == 1 and not args.no_cpu:
-        nthreads = os.cpu_count() or 1
+        nthreads = args.cpu_threads or os.cpu_count() or 1
         done, dt, desc = oracle_sample(name, args.cpu_budget, nthreads)
         line["cpu_baseline"] = {"value": done / dt * (2 if b.is_merge else 1),
                                 "unit": unit, "cores": nthreads, "kind": "oracle",
@@ -715,7 +717,7 @@ def run_reference(args):
     name = args.config
     K = args.steps if args.steps is not None else 20
     W = max(3, args.warmup) if args.warmup is not None else 3
-    nthreads = os.cpu_count() or 1
+    nthreads = args.cpu_threads or os.cpu_count() or 1
     per_step = max(0.05, min(2.0, 150.0 / max(1, K + W)))
     for _ in range(W):
         oracle_sample(name, per_step / 4, nthreads)
