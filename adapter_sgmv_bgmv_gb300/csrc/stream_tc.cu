@@ -21,12 +21,15 @@
 //     never waits on its own copies;
 //   - warp 1 (MMA) issues M = 128, N = 128, K = r MMAs per chunk into one of two
 //     TMEM accumulators, so the MMAs of chunk i + 1 overlap the epilogue of chunk i;
-//   - warps 2-9 (epilogue) stage the left operand each time the CTA enters a block
-//     -- V as the in-order sum of the shrink's fp32 partials or from the caller's
-//     fp32 rows, split into bf16 hi = bf16(v) and lo = bf16(v - hi) (about 16
-//     significant bits; the MMAs run on both), or A_k's 128 x r slice (M-major; one
-//     thread loads it by TMA from the A row matrix) -- then per chunk read the
-//     accumulator (warp w: TMEM lanes
+//   - warps 11-14 (left) stage the left operand of each block of the CTA's share --
+//     V as the in-order sum of the shrink's fp32 partials or from the caller's fp32
+//     rows, split into bf16 hi = bf16(v) and lo = bf16(v - hi) (about 16 significant
+//     bits; the MMAs run on both), or A_k's 128 x r slice (M-major; one thread loads
+//     it by TMA from the A row matrix) -- into one of two buffers, so the next
+//     block's operand is ready before the current block ends (one buffer when a
+//     second would cost a stage); the MMA warp frees a buffer with a commit after
+//     the block's last MMA;
+//   - warps 2-9 (epilogue) per chunk read the accumulator (warp w: TMEM lanes
 //     32*(w%4).., one 64-column half; both TMEM loads in flight before one wait),
 //     add s * acc to its own row of the tile in shared memory (and store that row
 //     itself if it is one of a ragged block's last < 8 rows), then arrive on the
@@ -49,8 +52,10 @@ namespace {
 
 constexpr int kTM = 128;
 constexpr int kBN = 128;
-constexpr int kThreads = 352;                 // producer, MMA, 8 epilogue warps, store
+constexpr int kThreads = 480;                 // producer, MMA, 8 epilogue, store, 4 left
 constexpr int kEpi = 256;
+constexpr int kLeftWarp0 = 11;                // warps 11..14 stage the left operand
+constexpr int kLeftThreads = 128;
 constexpr uint32_t kBox = kTM * 128;          // one 64-column TMA box of 128 rows
 constexpr uint32_t kTile = 2 * kBox;          // 128 x 128 bf16
 constexpr int kMaxStages = 4;
@@ -70,12 +75,13 @@ struct StreamArgs {
     int ctas;                                 // the chunk sequence is split over these
     int rp_max;                               // padded rank that sizes the layout
     int stages;
+    int nbuf;                                 // left-operand buffers (2: next block staged ahead)
 };
 
 __host__ __device__ inline int rank_pad16(int r) { return (r + 15) & ~15; }
 __host__ __device__ inline int v_atoms(int rp) { return (rp + 63) / 64; }
 
-// Shared memory: [left operand][stage s: B | tile] x NS [barriers]
+// Shared memory: [left operand] x nbuf [stage s: B | tile] x NS [barriers]
 __host__ __device__ inline uint32_t left_bytes(int left, int rp)
 {
     return left == kLeftAPages ? uint32_t(rp) * kTM * 2u               // A: rp x 128, M-major
@@ -84,9 +90,10 @@ __host__ __device__ inline uint32_t left_bytes(int left, int rp)
 
 __host__ __device__ inline uint32_t stage_bytes(int rp) { return uint32_t(rp) * kBN * 2u + kTile; }
 
-__host__ __device__ inline uint32_t stream_smem_bytes(int left, int rp, int stages)
+__host__ __device__ inline uint32_t stream_smem_bytes(int left, int rp, int stages, int nbuf)
 {
-    return 1024u + left_bytes(left, rp) + uint32_t(stages) * stage_bytes(rp) + 192u;   // + barriers
+    return 1024u + uint32_t(nbuf) * left_bytes(left, rp) + uint32_t(stages) * stage_bytes(rp) +
+           192u;   // + barriers
 }
 
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads)
@@ -140,20 +147,23 @@ __global__ void __launch_bounds__(kThreads) k_stream_tc(const __grid_constant__ 
     const bool merge = a.left == kLeftAPages;
     const int d_out = merge ? a.m.d_out : a.p.d_out;
     unsigned *status = merge ? a.m.status : a.p.status;
-    const int NS = a.stages;
-    const uint32_t sL = base;
-    const uint32_t sStage0 = sL + left_bytes(a.left, a.rp_max);
+    const int NS = a.stages, NB = a.nbuf;
+    const uint32_t sL = base, LB = left_bytes(a.left, a.rp_max);
+    const uint32_t sStage0 = sL + uint32_t(NB) * LB;
     const uint32_t sBar = sStage0 + uint32_t(NS) * stage_bytes(a.rp_max);
-    // barriers: left, full[4], empty[4], tready[4], tfull[2], tempty[2]
-    const uint32_t bar_left = sBar;
+    // barriers: full[4], empty[4], tready[4], tfull[2], tempty[2], lfull[2], lempty[2]
     const uint32_t full0 = sBar + 8, empty0 = sBar + 40, tready0 = sBar + 72;
     const uint32_t tfull0 = sBar + 104, tempty0 = sBar + 120;
     const uint32_t tmem_slot = sBar + 136;
+    const uint32_t lfull0 = sBar + 144, lempty0 = sBar + 160;
     auto stage_b = [&](int i) { return sStage0 + uint32_t(i % NS) * stage_bytes(a.rp_max); };
     auto stage_t = [&](int i) { return stage_b(i) + uint32_t(a.rp_max) * kBN * 2u; };
 
     if (tid == 0) {
-        mbar_init(bar_left, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(lfull0 + 8 * b, 1);      // left warps (or their TMA bytes)
+            mbar_init(lempty0 + 8 * b, 1);     // MMA commit after a block's last MMA
+        }
         for (int s = 0; s < NS; ++s) {
             mbar_init(full0 + 8 * s, 1);       // producer's expect-tx; tile + B bytes
             mbar_init(empty0 + 8 * s, 1);      // the stage's store has read it
@@ -218,15 +228,22 @@ __global__ void __launch_bounds__(kThreads) k_stream_tc(const __grid_constant__ 
             const uint32_t idesc = tc::idesc_bf16(kTM, kBN, merge ? 1 : 0, 1);
             const int parts = merge ? 1 : 2;
             int cur_blk = -1, seg = -1;
+            uint32_t sLb = sL;
             Block bk{};
             for (int i = 0; i < nch && ok; ++i) {
                 const int s = i % NS, b = i & 1;
                 const int blk = (g0 + i) / a.n_chunks;
-                if (blk != cur_blk) {              // wait for the new block's left operand
+                if (blk != cur_blk) {
+                    // The previous block's buffer is free once its MMAs complete; then
+                    // wait for the new block's left operand.
+                    if (seg >= 0)
+                        tc::mma_commit(lempty0 + 8 * (seg % NB));
                     bk = block_info(a, blk);
                     cur_blk = blk;
                     ++seg;
-                    ok = mbar_wait_bounded(bar_left, uint32_t(seg & 1), status, kDevTimeoutLoad);
+                    sLb = sL + uint32_t(seg % NB) * LB;
+                    ok = mbar_wait_bounded(lfull0 + 8 * (seg % NB), uint32_t((seg / NB) & 1), status,
+                                           kDevTimeoutLoad);
                 }
                 if (ok)
                     ok = mbar_wait_bounded(full0 + 8 * s, uint32_t((i / NS) & 1), status,
@@ -245,9 +262,9 @@ __global__ void __launch_bounds__(kThreads) k_stream_tc(const __grid_constant__ 
                     for (int kk = 0; kk < bk.rp / 16; ++kk) {
                         uint64_t dl;
                         if (merge)
-                            dl = tc::smem_desc_sw128(sL + uint32_t(kk) * 2048u, lbo, 1024u);
+                            dl = tc::smem_desc_sw128(sLb + uint32_t(kk) * 2048u, lbo, 1024u);
                         else
-                            dl = tc::smem_desc_sw128(sL + uint32_t(part * atoms + (kk >> 2)) * kBox +
+                            dl = tc::smem_desc_sw128(sLb + uint32_t(part * atoms + (kk >> 2)) * kBox +
                                                          uint32_t(kk & 3) * 32u,
                                                      16u, 1024u);
                         const uint64_t db = tc::smem_desc_sw128(sb + uint32_t(kk) * 2048u, lbo, 1024u);
@@ -258,6 +275,81 @@ __global__ void __launch_bounds__(kThreads) k_stream_tc(const __grid_constant__ 
             }
         }
         __syncwarp();
+    } else if (warp >= kLeftWarp0) {
+        // ------------------------------------------------------------ left operand
+        // One block after another of this CTA's share, into buffer seg % NB once the
+        // MMAs of the block that last used it have completed (with two buffers, the
+        // next block's operand is ready before the current block's last chunk).
+        // Every left thread runs the same sequence of named barriers whatever
+        // happens: after a failed wait it skips the work, never the barrier.
+        const int vr = tid - 32 * kLeftWarp0;   // 0..127: row of V
+        const int blk0 = nch > 0 ? g0 / a.n_chunks : 0;
+        const int nseg = nch > 0 ? (g0 + nch - 1) / a.n_chunks - blk0 + 1 : 0;
+        for (int seg = 0; seg < nseg; ++seg) {
+            const int blk = blk0 + seg, buf = seg % NB;
+            const Block bk = block_info(a, blk);
+            if (ok && seg >= NB)
+                ok = mbar_wait_bounded(lempty0 + 8 * buf, uint32_t((seg / NB - 1) & 1), status,
+                                       kDevTimeoutPipe);
+            ok = __all_sync(0xffffffffu, ok);
+            const uint32_t sLb = sL + uint32_t(buf) * LB;
+            if (ok && !merge) {
+                // V row vr as bf16 hi = bf16(v) and lo = bf16(v - hi), K-major atoms
+                const int KS = a.left == kLeftVParts ? a.p.ksplit : 1;
+                const int atoms = v_atoms(bk.rp);
+                for (int c = 0; c < bk.rp / 8; ++c) {
+                    float f[8], back[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        f[e] = 0.f;
+                    if (a.left == kLeftVParts) {
+                        for (int ks = 0; ks < KS; ++ks) {
+                            const float *src = a.p.vparts + (size_t(blk) * KS + ks) * (kVPartBytes / 4) +
+                                               size_t(vr) * bk.rp + 8 * c;
+                            const float4 lo4 = *reinterpret_cast<const float4 *>(src);
+                            const float4 hi4 = *reinterpret_cast<const float4 *>(src + 4);
+                            f[0] += lo4.x; f[1] += lo4.y; f[2] += lo4.z; f[3] += lo4.w;
+                            f[4] += hi4.x; f[5] += hi4.y; f[6] += hi4.z; f[7] += hi4.w;
+                        }
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const int j = 8 * c + e;
+                            f[e] = (vr < bk.nrows && j < bk.r) ? a.p.v[int64_t(bk.row0 + vr) * a.p.ldv + j]
+                                                               : 0.f;
+                        }
+                    }
+                    const uint4 hv = pack8(f);
+                    unpack8(hv, back);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        f[e] -= back[e];
+                    const uint32_t off = tc::sw128(uint32_t(vr), uint32_t(c & 7));
+                    *reinterpret_cast<uint4 *>(gbase + (sLb - base) + (c >> 3) * kBox + off) = hv;
+                    *reinterpret_cast<uint4 *>(gbase + (sLb - base) + (atoms + (c >> 3)) * kBox + off) =
+                        pack8(f);
+                }
+                tc::fence_proxy_async_smem();
+            }
+            named_bar_sync(1, kLeftThreads);
+            if (vr == 0) {
+                if (ok && merge) {
+                    // A_k rows row0..row0+127 (M-major: page j of A_k is row j of the
+                    // operand, 64 M values per 128-byte row), one 64-row half at a time;
+                    // a half wholly below d_in is not loaded (its rows are not stored).
+                    const int halves = bk.row0 + 64 < a.m.d_in ? 2 : 1;
+                    const uint32_t lbo_a = uint32_t(bk.rp) * 128u;
+                    mbar_arrive_expect_tx(lfull0 + 8 * buf, uint32_t(halves) * uint32_t(bk.rp) * 128u);
+                    for (int h = 0; h < halves; ++h)
+                        tc::for_row_boxes(bk.rp, [&](int off, int m) {
+                            tc::tma_load_2d(sLb + uint32_t(h) * lbo_a + uint32_t(off) * 128u, &a.amap[m],
+                                            bk.row0 + 64 * h, bk.a_row + off, lfull0 + 8 * buf);
+                        });
+                } else {
+                    mbar_arrive(lfull0 + 8 * buf);
+                }
+            }
+        }
     } else if (warp == 10) {
         // ------------------------------------------------------------ store
         if (lane == 0) {
@@ -298,11 +390,6 @@ __global__ void __launch_bounds__(kThreads) k_stream_tc(const __grid_constant__ 
         __syncwarp();
     } else {
         // ------------------------------------------------------------ epilogue
-        // Every epilogue thread runs the same sequence of named barriers (one per
-        // block, for the left operand) whatever happens: after a failed (timed-out)
-        // wait a warp skips its work, never the barriers, so no other warp is left
-        // waiting on it.
-        const int et = tid - 64;                 // 0..255
         const int q4 = warp & 3;                  // TMEM lanes 32*q4 .. 32*q4+31
         const int half = (warp - 2) >> 2;         // columns 64*half .. 64*half+63
         const int row = 32 * q4 + lane;
@@ -312,70 +399,8 @@ __global__ void __launch_bounds__(kThreads) k_stream_tc(const __grid_constant__ 
             const int s = i % NS, b = i & 1;
             const int g = g0 + i, blk = g / a.n_chunks;
             if (blk != cur_blk) {
-                // Left operand of the new block.  This thread has seen the commit of
-                // every MMA of the previous block, so the buffer is free.
                 bk = block_info(a, blk);
                 cur_blk = blk;
-                if (ok && !merge && et < kTM) {
-                    const int vr = et;
-                    const int KS = a.left == kLeftVParts ? a.p.ksplit : 1;
-                    const int atoms = v_atoms(bk.rp);
-                    for (int c = 0; c < bk.rp / 8; ++c) {
-                        float f[8], back[8];
-#pragma unroll
-                        for (int e = 0; e < 8; ++e)
-                            f[e] = 0.f;
-                        if (a.left == kLeftVParts) {
-                            for (int ks = 0; ks < KS; ++ks) {
-                                const float *src = a.p.vparts +
-                                                   (size_t(blk) * KS + ks) * (kVPartBytes / 4) +
-                                                   size_t(vr) * bk.rp + 8 * c;
-                                const float4 lo4 = *reinterpret_cast<const float4 *>(src);
-                                const float4 hi4 = *reinterpret_cast<const float4 *>(src + 4);
-                                f[0] += lo4.x; f[1] += lo4.y; f[2] += lo4.z; f[3] += lo4.w;
-                                f[4] += hi4.x; f[5] += hi4.y; f[6] += hi4.z; f[7] += hi4.w;
-                            }
-                        } else {
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) {
-                                const int j = 8 * c + e;
-                                f[e] = (vr < bk.nrows && j < bk.r)
-                                           ? a.p.v[int64_t(bk.row0 + vr) * a.p.ldv + j]
-                                           : 0.f;
-                            }
-                        }
-                        const uint4 hv = pack8(f);
-                        unpack8(hv, back);
-#pragma unroll
-                        for (int e = 0; e < 8; ++e)
-                            f[e] -= back[e];
-                        const uint32_t off = tc::sw128(uint32_t(vr), uint32_t(c & 7));
-                        *reinterpret_cast<uint4 *>(gbase + (sL - base) + (c >> 3) * kBox + off) = hv;
-                        *reinterpret_cast<uint4 *>(gbase + (sL - base) + (atoms + (c >> 3)) * kBox +
-                                                   off) = pack8(f);
-                    }
-                    tc::fence_proxy_async_smem();
-                }
-                named_bar_sync(1, kEpi);
-                if (et == 0 && merge) {
-                    // A_k rows row0..row0+127 (M-major: page j of A_k is row j of the
-                    // operand, 64 M values per 128-byte row), one 64-row half at a time;
-                    // a half wholly below d_in is not loaded (its rows are not stored).
-                    const int halves = bk.row0 + 64 < a.m.d_in ? 2 : 1;
-                    const uint32_t lbo_a = uint32_t(bk.rp) * 128u;
-                    if (ok) {
-                        mbar_arrive_expect_tx(bar_left, uint32_t(halves) * uint32_t(bk.rp) * 128u);
-                        for (int h = 0; h < halves; ++h)
-                            tc::for_row_boxes(bk.rp, [&](int off, int m) {
-                                tc::tma_load_2d(sL + uint32_t(h) * lbo_a + uint32_t(off) * 128u,
-                                                &a.amap[m], bk.row0 + 64 * h, bk.a_row + off, bar_left);
-                            });
-                    } else {
-                        mbar_arrive(bar_left);
-                    }
-                } else if (et == 0) {
-                    mbar_arrive(bar_left);
-                }
             }
             if (ok)
                 ok = mbar_wait_bounded(tfull0 + 8 * b, uint32_t((i >> 1) & 1), status, kDevTimeoutMma);
@@ -435,12 +460,20 @@ __global__ void __launch_bounds__(kThreads) k_stream_tc(const __grid_constant__ 
     }
 }
 
-int pick_stages(int left, int rp)
+// Stages and left-operand buffers: as many stages as fit beside one buffer, and a
+// second buffer (the next block's operand staged during the current block) only if
+// it costs no stage -- a stage fewer lowered the expand's bandwidth more than the
+// prefetch saved at a CTA's one or two block changes.  False if two stages do not fit.
+bool pick_layout(int left, int rp, int &stages, int &nbuf)
 {
-    for (int ns = kMaxStages; ns >= 2; --ns)
-        if (stream_smem_bytes(left, rp, ns) <= 227u * 1024u)
-            return ns;
-    return 0;
+    stages = 0;
+    for (int ns = kMaxStages; ns >= 2 && !stages; --ns)
+        if (stream_smem_bytes(left, rp, ns, 1) <= 227u * 1024u)
+            stages = ns;
+    if (!stages)
+        return false;
+    nbuf = stream_smem_bytes(left, rp, stages, 2) <= 227u * 1024u ? 2 : 1;
+    return true;
 }
 
 int device_sms()
@@ -459,8 +492,7 @@ int device_sms()
 cudaError_t launch_stream(StreamArgs &a, const void *tensor, uint64_t inner, uint64_t outer,
                           uint64_t row_bytes, cudaStream_t stream)
 {
-    a.stages = pick_stages(a.left, a.rp_max);
-    if (a.stages == 0)
+    if (!pick_layout(a.left, a.rp_max, a.stages, a.nbuf))
         return cudaErrorInvalidValue;
     if (!encode_bf16_2d(&a.map, tensor, inner, outer, row_bytes, 64, kTM, true) ||
         !encode_bf16_2d(&a.map8, tensor, inner, outer, row_bytes, 64, 8, true))
@@ -480,7 +512,7 @@ cudaError_t launch_stream(StreamArgs &a, const void *tensor, uint64_t inner, uin
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(unsigned(a.ctas));
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = stream_smem_bytes(a.left, a.rp_max, a.stages);
+    cfg.dynamicSmemBytes = stream_smem_bytes(a.left, a.rp_max, a.stages, a.nbuf);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -508,8 +540,9 @@ cudaError_t launch_expand_tc(const TileParams &p, cudaStream_t stream)
 
 bool merge_tc_supported(int d_in, int d_out, int rank)
 {
+    int ns = 0, nb = 0;
     return rank >= 8 && rank <= 128 && d_in > 0 && d_out > 0 &&
-           pick_stages(kLeftAPages, rank_pad16(rank)) > 0;
+           pick_layout(kLeftAPages, rank_pad16(rank), ns, nb);
 }
 
 cudaError_t launch_merge_tc(const MergeParams &p, int /*n_split*/, cudaStream_t stream)
