@@ -294,40 +294,67 @@ __global__ void __launch_bounds__(kThreads) k_stream_tc(const __grid_constant__ 
             ok = __all_sync(0xffffffffu, ok);
             const uint32_t sLb = sL + uint32_t(buf) * LB;
             if (ok && !merge) {
-                // V row vr as bf16 hi = bf16(v) and lo = bf16(v - hi), K-major atoms
+                // V row vr as bf16 hi = bf16(v) and lo = bf16(v - hi), K-major atoms.
+                // Four 8-column groups at a time: all their loads are issued (read-only
+                // path) before anything is summed or stored, so a group of four costs
+                // one round trip per K-split share instead of one per group.
                 const int KS = a.left == kLeftVParts ? a.p.ksplit : 1;
-                const int atoms = v_atoms(bk.rp);
-                for (int c = 0; c < bk.rp / 8; ++c) {
-                    float f[8], back[8];
+                const int atoms = v_atoms(bk.rp), nc = bk.rp / 8;
+                for (int c0 = 0; c0 < nc; c0 += 4) {
+                    float f[4][8];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        f[e] = 0.f;
+                    for (int u = 0; u < 4; ++u)
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            f[u][e] = 0.f;
                     if (a.left == kLeftVParts) {
                         for (int ks = 0; ks < KS; ++ks) {
-                            const float *src = a.p.vparts + (size_t(blk) * KS + ks) * (kVPartBytes / 4) +
-                                               size_t(vr) * bk.rp + 8 * c;
-                            const float4 lo4 = *reinterpret_cast<const float4 *>(src);
-                            const float4 hi4 = *reinterpret_cast<const float4 *>(src + 4);
-                            f[0] += lo4.x; f[1] += lo4.y; f[2] += lo4.z; f[3] += lo4.w;
-                            f[4] += hi4.x; f[5] += hi4.y; f[6] += hi4.z; f[7] += hi4.w;
+                            const float4 *src = reinterpret_cast<const float4 *>(
+                                a.p.vparts + (size_t(blk) * KS + ks) * (kVPartBytes / 4) +
+                                size_t(vr) * bk.rp + 8 * c0);
+                            float4 t[8];
+#pragma unroll
+                            for (int u = 0; u < 4; ++u)
+                                if (c0 + u < nc) {
+                                    t[2 * u] = __ldg(src + 2 * u);
+                                    t[2 * u + 1] = __ldg(src + 2 * u + 1);
+                                }
+#pragma unroll
+                            for (int u = 0; u < 4; ++u)
+                                if (c0 + u < nc) {
+                                    f[u][0] += t[2 * u].x; f[u][1] += t[2 * u].y;
+                                    f[u][2] += t[2 * u].z; f[u][3] += t[2 * u].w;
+                                    f[u][4] += t[2 * u + 1].x; f[u][5] += t[2 * u + 1].y;
+                                    f[u][6] += t[2 * u + 1].z; f[u][7] += t[2 * u + 1].w;
+                                }
                         }
                     } else {
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            const int j = 8 * c + e;
-                            f[e] = (vr < bk.nrows && j < bk.r) ? a.p.v[int64_t(bk.row0 + vr) * a.p.ldv + j]
-                                                               : 0.f;
-                        }
-                    }
-                    const uint4 hv = pack8(f);
-                    unpack8(hv, back);
+                        for (int u = 0; u < 4; ++u)
 #pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        f[e] -= back[e];
-                    const uint32_t off = tc::sw128(uint32_t(vr), uint32_t(c & 7));
-                    *reinterpret_cast<uint4 *>(gbase + (sLb - base) + (c >> 3) * kBox + off) = hv;
-                    *reinterpret_cast<uint4 *>(gbase + (sLb - base) + (atoms + (c >> 3)) * kBox + off) =
-                        pack8(f);
+                            for (int e = 0; e < 8; ++e) {
+                                const int j = 8 * (c0 + u) + e;
+                                f[u][e] = (c0 + u < nc && vr < bk.nrows && j < bk.r)
+                                              ? __ldg(a.p.v + int64_t(bk.row0 + vr) * a.p.ldv + j)
+                                              : 0.f;
+                            }
+                    }
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int c = c0 + u;
+                        if (c >= nc)
+                            break;
+                        float back[8];
+                        const uint4 hv = pack8(f[u]);
+                        unpack8(hv, back);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            f[u][e] -= back[e];
+                        const uint32_t off = tc::sw128(uint32_t(vr), uint32_t(c & 7));
+                        *reinterpret_cast<uint4 *>(gbase + (sLb - base) + (c >> 3) * kBox + off) = hv;
+                        *reinterpret_cast<uint4 *>(gbase + (sLb - base) + (atoms + (c >> 3)) * kBox + off) =
+                            pack8(f[u]);
+                    }
                 }
                 tc::fence_proxy_async_smem();
             }
