@@ -8,7 +8,8 @@
 // consecutive pages of a rank that is a multiple of 16, the pools are used as they
 // are.  Otherwise this kernel copies the call's adapters (S-LoRA's unified pool
 // holds them in arbitrary pages) into a dense scratch, one slot of rp rows per
-// adapter, the rows beyond its rank zero.
+// adapter: its rank's rows, then zeros up to the rank rounded up to 16 (the rows
+// the tensor-core kernels read); the slot's rows beyond those are left unwritten.
 #include <cuda_runtime.h>
 
 #include "internal.h"
@@ -19,6 +20,7 @@ namespace lora {
 namespace {
 
 constexpr int kStageThreads = 128;
+constexpr int kPerThread = 8;                 // 16-byte vectors per thread per pass
 
 // One CTA per destination row: blockIdx.x = slot * rp + j, blockIdx.y = side.
 __global__ void __launch_bounds__(kStageThreads) k_stage_rows(const __grid_constant__ StageArgs a)
@@ -31,14 +33,33 @@ __global__ void __launch_bounds__(kStageThreads) k_stage_rows(const __grid_const
         return;
     const int row = int(blockIdx.x);
     const int slot = row / a.rp, j = row - slot * a.rp;
+    const int rank = a.rank[slot];
+    if (j >= ((rank + 15) & ~15))   // the kernels read a slot's rank rounded up to 16 rows
+        return;
     const int nv = sd.width / 8;
     uint4 *dst = reinterpret_cast<uint4 *>(sd.dst + int64_t(row) * sd.width);
-    if (j < a.rank[slot]) {
+    if (j < rank) {
         const int32_t page = sd.pages[int64_t(a.adapter[slot]) * a.max_rank + j];
         const uint4 *src = reinterpret_cast<const uint4 *>(sd.pool + int64_t(page) * sd.pw);
-        for (int q = threadIdx.x; q < nv; q += kStageThreads)
-            dst[q] = src[q];
+        // All of a pass's loads are in flight before its first store (a row of up to
+        // 8192 elements is one pass), so a row costs one round trip, not one per vector.
+        for (int q0 = 0; q0 < nv; q0 += kPerThread * kStageThreads) {
+            uint4 v[kPerThread];
+#pragma unroll
+            for (int e = 0; e < kPerThread; ++e) {
+                const int q = q0 + e * kStageThreads + int(threadIdx.x);
+                if (q < nv)
+                    v[e] = __ldg(src + q);
+            }
+#pragma unroll
+            for (int e = 0; e < kPerThread; ++e) {
+                const int q = q0 + e * kStageThreads + int(threadIdx.x);
+                if (q < nv)
+                    dst[q] = v[e];
+            }
+        }
     } else {
+        // Rank padding: zero, since the expand and the merge multiply these rows.
         const uint4 z = make_uint4(0u, 0u, 0u, 0u);
         for (int q = threadIdx.x; q < nv; q += kStageThreads)
             dst[q] = z;
