@@ -22,13 +22,17 @@
 //   - warp 1 (MMA) issues M = 128, N = 128, K = r MMAs per chunk into one of two
 //     TMEM accumulators, so the MMAs of chunk i + 1 overlap the epilogue of chunk i;
 //   - warps 11-14 (left) stage the left operand of each block of the CTA's share --
-//     V as the in-order sum of the shrink's fp32 partials or from the caller's fp32
-//     rows, split into bf16 hi = bf16(v) and lo = bf16(v - hi) (about 16 significant
-//     bits; the MMAs run on both), or A_k's 128 x r slice (M-major; one thread loads
-//     it by TMA from the A row matrix) -- into one of two buffers, so the next
-//     block's operand is ready before the current block ends (one buffer when a
-//     second would cost a stage); the MMA warp frees a buffer with a commit after
-//     the block's last MMA;
+//     V as the in-order sum of the shrink's fp32 partials (coalesced loads, up to 16
+//     in flight per thread) or from the caller's fp32 rows, split into bf16
+//     hi = bf16(v) and lo = bf16(v - hi) (about 16 significant bits; the MMAs run on
+//     both), or A_k's 128 x r slice (M-major; one thread loads it by TMA from the A
+//     row matrix) -- into one of two buffers, so the next block's operand is ready
+//     before the current block ends (one buffer when a second would cost a stage);
+//     the MMA warp frees a buffer with a commit after the block's last MMA.  The
+//     producer holds the first block's third tile until its V is staged (V's loads
+//     then do not queue behind a full ring of tile loads), and when its share runs
+//     on into another block it fetches that block's partials into L2 as it issues
+//     the current block's last chunk;
 //   - warps 2-9 (epilogue) per chunk read the accumulator (warp w: TMEM lanes
 //     32*(w%4).., one 64-column half; both TMEM loads in flight before one wait),
 //     add s * acc to its own row of the tile in shared memory (and store that row
@@ -59,6 +63,8 @@ constexpr int kLeftThreads = 128;
 constexpr uint32_t kBox = kTM * 128;          // one 64-column TMA box of 128 rows
 constexpr uint32_t kTile = 2 * kBox;          // 128 x 128 bf16
 constexpr int kMaxStages = 4;
+constexpr int kGateChunk = 2;                 // chunks of the first block issued before its V
+constexpr int kShortShare = 24;               // chunks per CTA up to which two left buffers win
 
 enum Left : int { kLeftVParts = 0, kLeftVRows = 1, kLeftAPages = 2 };
 
@@ -131,6 +137,98 @@ __device__ __forceinline__ Block block_info(const StreamArgs &a, int blk)
     return b;
 }
 
+// Left operand of block blk from the shrink's K-split partials: V as bf16 hi = bf16(v)
+// and lo = bf16(v - hi) in K-major 128-byte-swizzled atoms at `dst`, v the in-order
+// sum of the ks shares.  A share's partial is 128 rows x rp floats, row-major: piece
+// pc (16 bytes) is columns 4 (pc % (rp/4)) .. + 3 of row pc / (rp/4), half of a
+// 16-byte chunk of the operand.  Thread vr (0..127) takes pieces vr, vr + 128, ..., so
+// each load instruction of a warp reads 512 contiguous bytes.
+__device__ __forceinline__ void store_v_piece(uint8_t *dst, int atoms, int q4, int pc, float4 v)
+{
+    const int row = pc / q4, col = 4 * (pc - row * q4), c = col >> 3;
+    const __nv_bfloat162 h01 = __floats2bfloat162_rn(v.x, v.y);
+    const __nv_bfloat162 h23 = __floats2bfloat162_rn(v.z, v.w);
+    const float2 b01 = __bfloat1622float2(h01), b23 = __bfloat1622float2(h23);
+    const __nv_bfloat162 l01 = __floats2bfloat162_rn(v.x - b01.x, v.y - b01.y);
+    const __nv_bfloat162 l23 = __floats2bfloat162_rn(v.z - b23.x, v.w - b23.y);
+    const uint32_t off = tc::sw128(uint32_t(row), uint32_t(c & 7)) + 8u * uint32_t((col >> 2) & 1);
+    *reinterpret_cast<uint2 *>(dst + (c >> 3) * kBox + off) =
+        make_uint2(*reinterpret_cast<const uint32_t *>(&h01), *reinterpret_cast<const uint32_t *>(&h23));
+    *reinterpret_cast<uint2 *>(dst + (atoms + (c >> 3)) * kBox + off) =
+        make_uint2(*reinterpret_cast<const uint32_t *>(&l01), *reinterpret_cast<const uint32_t *>(&l23));
+}
+
+__device__ __forceinline__ void add4(float4 &a, const float4 &b)
+{
+    a.x += b.x;
+    a.y += b.y;
+    a.z += b.z;
+    a.w += b.w;
+}
+
+// Up to two shares: eight pieces of each in flight at once, summed in place.
+__device__ __forceinline__ void stage_v_parts2(const StreamArgs &a, int blk, int rp, int vr, uint8_t *dst)
+{
+    const int KS = a.p.ksplit, atoms = v_atoms(rp), q4 = rp / 4;
+    const float4 *part =
+        reinterpret_cast<const float4 *>(a.p.vparts + size_t(blk) * KS * (kVPartBytes / 4)) + vr;
+    for (int j0 = 0; j0 < q4; j0 += 8) {
+        float4 t0[8], t1[8];
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj)
+            if (j0 + jj < q4) {
+                t0[jj] = __ldg(part + 128 * (j0 + jj));
+                if (KS == 2)
+                    t1[jj] = __ldg(part + kVPartBytes / 16 + 128 * (j0 + jj));
+            }
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj)
+            if (j0 + jj < q4) {
+                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);   // 0 + p0 (+ p1): the shares' order
+                add4(v, t0[jj]);
+                if (KS == 2)
+                    add4(v, t1[jj]);
+                store_v_piece(dst, atoms, q4, vr + 128 * (j0 + jj), v);
+            }
+    }
+}
+
+// Any number of shares: four shares x four pieces in flight per batch.
+__device__ __forceinline__ void stage_v_parts4(const StreamArgs &a, int blk, int rp, int vr, uint8_t *dst)
+{
+    const int KS = a.p.ksplit, atoms = v_atoms(rp), q4 = rp / 4;
+    const float4 *part =
+        reinterpret_cast<const float4 *>(a.p.vparts + size_t(blk) * KS * (kVPartBytes / 4)) + vr;
+    for (int j0 = 0; j0 < q4; j0 += 4) {
+        float4 acc[4];
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj)
+            acc[jj] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int ks0 = 0; ks0 < KS; ks0 += 4) {
+            float4 t[4][4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj)
+                    if (ks0 + q < KS)
+                        t[q][jj] = __ldg(part + size_t(ks0 + q) * (kVPartBytes / 16) + 128 * (j0 + jj));
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj)
+                    if (ks0 + q < KS)
+                        add4(acc[jj], t[q][jj]);
+        }
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj)
+            store_v_piece(dst, atoms, q4, vr + 128 * (j0 + jj), acc[jj]);
+    }
+}
+
+// kWide: the K-split has at most two shares and V is staged 16 loads deep per thread
+// (stage_v_parts2); otherwise four shares x four pieces (stage_v_parts4).  Two
+// instantiations, since one kernel holding both would spill.
+template <bool kWide>
 __global__ void __launch_bounds__(kThreads) k_stream_tc(const __grid_constant__ StreamArgs a)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -198,6 +296,12 @@ __global__ void __launch_bounds__(kThreads) k_stream_tc(const __grid_constant__ 
                 if (u > 0)
                     ok = mbar_wait_bounded(empty0 + 8 * s, uint32_t((u - 1) & 1), status,
                                            kDevTimeoutPipe);
+                // Two chunks of the first block go out at once; the rest wait until its
+                // V is staged, so that the tiles' loads do not queue ahead of V's.  (Only
+                // within the first block: the first V is staged whatever the producer
+                // does, so this wait always ends.)
+                if (ok && i == kGateChunk && !merge && (g0 + i) / a.n_chunks == g0 / a.n_chunks)
+                    ok = mbar_wait_bounded(lfull0, 0u, status, kDevTimeoutLoad);
                 if (!ok)
                     break;
                 const int g = g0 + i, blk = g / a.n_chunks;
@@ -218,6 +322,15 @@ __global__ void __launch_bounds__(kThreads) k_stream_tc(const __grid_constant__ 
                         tc::tma_load_2d(sb + uint32_t(h) * lbo_b + uint32_t(off) * 128u,
                                         &a.bmap[m], n0 + 64 * h, bk.b_row + off, full0 + 8 * s);
                     });
+                // The block's last chunk, and the share goes on into the next block: the
+                // next block's partials (long since evicted from L2 by the tile stream)
+                // are fetched into L2 now, so that their staging hits L2.
+                if (a.left == kLeftVParts && i + 1 < nch && (g + 1) / a.n_chunks != blk) {
+                    const int rpn = rank_pad16(tile_item(a.p, blk + 1).rank);
+                    for (int ks = 0; ks < a.p.ksplit; ++ks)
+                        tc::prefetch_l2(a.p.vparts + (size_t(blk + 1) * a.p.ksplit + ks) * (kVPartBytes / 4),
+                                        uint32_t(kTM * rpn * 4));
+                }
             }
             grid_dep_launch();   // every load issued: the next kernel may start its set-up
         }
@@ -282,7 +395,7 @@ __global__ void __launch_bounds__(kThreads) k_stream_tc(const __grid_constant__ 
         // next block's operand is ready before the current block's last chunk).
         // Every left thread runs the same sequence of named barriers whatever
         // happens: after a failed wait it skips the work, never the barrier.
-        const int vr = tid - 32 * kLeftWarp0;   // 0..127: row of V
+        const int vr = tid - 32 * kLeftWarp0;   // 0..127: a row of V, or a lane over V's pieces
         const int blk0 = nch > 0 ? g0 / a.n_chunks : 0;
         const int nseg = nch > 0 ? (g0 + nch - 1) / a.n_chunks - blk0 + 1 : 0;
         for (int seg = 0; seg < nseg; ++seg) {
@@ -293,52 +406,27 @@ __global__ void __launch_bounds__(kThreads) k_stream_tc(const __grid_constant__ 
                                        kDevTimeoutPipe);
             ok = __all_sync(0xffffffffu, ok);
             const uint32_t sLb = sL + uint32_t(buf) * LB;
-            if (ok && !merge) {
-                // V row vr as bf16 hi = bf16(v) and lo = bf16(v - hi), K-major atoms.
-                // Four 8-column groups at a time: all their loads are issued (read-only
-                // path) before anything is summed or stored, so a group of four costs
-                // one round trip per K-split share instead of one per group.
-                const int KS = a.left == kLeftVParts ? a.p.ksplit : 1;
+            if (ok && a.left == kLeftVParts) {
+                uint8_t *dst = gbase + (sLb - base);
+                if (kWide)
+                    stage_v_parts2(a, blk, bk.rp, vr, dst);
+                else
+                    stage_v_parts4(a, blk, bk.rp, vr, dst);
+                tc::fence_proxy_async_smem();
+            } else if (ok && !merge) {
+                // V row vr from the caller's fp32 rows (row stride ldv), as hi / lo.
                 const int atoms = v_atoms(bk.rp), nc = bk.rp / 8;
                 for (int c0 = 0; c0 < nc; c0 += 4) {
                     float f[4][8];
 #pragma unroll
                     for (int u = 0; u < 4; ++u)
 #pragma unroll
-                        for (int e = 0; e < 8; ++e)
-                            f[u][e] = 0.f;
-                    if (a.left == kLeftVParts) {
-                        for (int ks = 0; ks < KS; ++ks) {
-                            const float4 *src = reinterpret_cast<const float4 *>(
-                                a.p.vparts + (size_t(blk) * KS + ks) * (kVPartBytes / 4) +
-                                size_t(vr) * bk.rp + 8 * c0);
-                            float4 t[8];
-#pragma unroll
-                            for (int u = 0; u < 4; ++u)
-                                if (c0 + u < nc) {
-                                    t[2 * u] = __ldg(src + 2 * u);
-                                    t[2 * u + 1] = __ldg(src + 2 * u + 1);
-                                }
-#pragma unroll
-                            for (int u = 0; u < 4; ++u)
-                                if (c0 + u < nc) {
-                                    f[u][0] += t[2 * u].x; f[u][1] += t[2 * u].y;
-                                    f[u][2] += t[2 * u].z; f[u][3] += t[2 * u].w;
-                                    f[u][4] += t[2 * u + 1].x; f[u][5] += t[2 * u + 1].y;
-                                    f[u][6] += t[2 * u + 1].z; f[u][7] += t[2 * u + 1].w;
-                                }
+                        for (int e = 0; e < 8; ++e) {
+                            const int j = 8 * (c0 + u) + e;
+                            f[u][e] = (c0 + u < nc && vr < bk.nrows && j < bk.r)
+                                          ? __ldg(a.p.v + int64_t(bk.row0 + vr) * a.p.ldv + j)
+                                          : 0.f;
                         }
-                    } else {
-#pragma unroll
-                        for (int u = 0; u < 4; ++u)
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) {
-                                const int j = 8 * (c0 + u) + e;
-                                f[u][e] = (c0 + u < nc && vr < bk.nrows && j < bk.r)
-                                              ? __ldg(a.p.v + int64_t(bk.row0 + vr) * a.p.ldv + j)
-                                              : 0.f;
-                            }
-                    }
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
                         const int c = c0 + u;
@@ -528,14 +616,25 @@ cudaError_t launch_stream(StreamArgs &a, const void *tensor, uint64_t inner, uin
     // share of the chunks but at least two, so the pipeline has something to overlap.
     const int64_t total = int64_t(a.n_blocks) * a.n_chunks;
     a.ctas = int(std::max<int64_t>(1, std::min<int64_t>(device_sms(), total / 2)));
+    // Short shares (a few chunks per CTA, so the first V and a block change weigh
+    // more than a stage of streaming): two left buffers even at the cost of a stage.
+    if (a.left != kLeftAPages && a.nbuf == 1 && total / a.ctas <= kShortShare)
+        for (int ns = kMaxStages; ns >= 2; --ns)
+            if (stream_smem_bytes(a.left, a.rp_max, ns, 2) <= 227u * 1024u) {
+                a.stages = ns;
+                a.nbuf = 2;
+                break;
+            }
     static bool configured = false;
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(k_stream_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             227 * 1024);
-        if (e != cudaSuccess)
-            return e;
+        for (auto *k : {k_stream_tc<false>, k_stream_tc<true>}) {
+            cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+            if (e != cudaSuccess)
+                return e;
+        }
         configured = true;
     }
+    const bool wide = a.left == kLeftVParts && a.p.ksplit <= 2;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(unsigned(a.ctas));
     cfg.blockDim = dim3(kThreads);
@@ -546,7 +645,7 @@ cudaError_t launch_stream(StreamArgs &a, const void *tensor, uint64_t inner, uin
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, k_stream_tc, a);
+    return wide ? cudaLaunchKernelEx(&cfg, k_stream_tc<true>, a) : cudaLaunchKernelEx(&cfg, k_stream_tc<false>, a);
 }
 
 }  // namespace

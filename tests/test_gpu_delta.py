@@ -227,6 +227,17 @@ def test_tile_kernels_rank_128():
     big.close()
 
 
+def test_tile_kernels_eight_way_k_split(ctx):
+    # nine tiles at d_in = 4096: the fused shrink splits K eight ways (the launcher
+    # doubles the split while tiles x split stays within two CTAs per SM and each CTA
+    # keeps at least four 64-wide K blocks), so the expand sums eight partials per
+    # tile, two batches of four shares; ragged last tiles (88 and 16 rows) and a
+    # ragged last column chunk (d_out = 384 + 72)
+    c = workloads.small(seed=55, n=1000, d_in=4096, d_out=456, n_adapters=2, ranks=[64, 16],
+                        ids=np.repeat(np.array([0, 1], np.int32), [600, 400]))
+    assert _tile_check(ctx, c, True) & 2
+
+
 def test_tile_shrink_and_expand_match_oracle(ctx):
     c = workloads.small(seed=54, n=400, d_in=192, d_out=256, n_adapters=2, ranks=[32, 16],
                         ids=np.repeat(np.array([1, 0], np.int32), 200))
