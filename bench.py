@@ -141,8 +141,8 @@ def alg_bytes_delta(case, ids):
 # Configurations without a capture report null.
 MEASURED_TRAFFIC = {
     ("llama7b_decode", "rows"): (17.88e6 + 1.36e6) / 2,   # profiles/rows_llama7b_decode.md
-    ("valora_prefill", "expand"): 724.81e6,                # profiles/stream_tile_valora_prefill.md
-    ("valora_merge", "merge"): 123.13e6,                   # profiles/stream_merge_valora.md
+    ("valora_prefill", "expand"): 725.66e6,                # profiles/stream_tile_valora_prefill.md
+    ("valora_merge", "merge"): 123.15e6,                   # profiles/stream_merge_valora.md
 }
 
 
