@@ -76,8 +76,9 @@ struct lora_ctx {
     int force_rows = 0;             // > 0 while tuning: rows per item
     uint8_t *vparts = nullptr;      // fused tile path: partial V between its two kernels
     size_t vparts_cap = 0;
-    uint8_t *dense = nullptr;       // dense adapter rows of a call (dense.cu)
-    size_t dense_cap = 0;
+    uint8_t *dense = nullptr;       // dense adapter rows of a call (dense.cu): two halves,
+    size_t dense_cap = 0;           //   of dense_cap bytes each, used by turns
+    int dense_turn = 0;
     std::vector<int32_t> slot_of;   // adapter -> slot while a call's slots are assigned
     std::unique_ptr<TileParams> tparams;   // launch parameters of the tile kernels
     uint8_t *flush = nullptr;       // lora_tune_shape: a buffer larger than L2, written
@@ -395,6 +396,7 @@ struct RowMats {
     const uint16_t *a = nullptr, *b = nullptr;
     int64_t a_ld = 0, a_nrows = 0, b_ld = 0, b_nrows = 0;
     bool staged = false;
+    bool early = false;             // the copy may run before the previous kernel ends
     int rp = 0;
 };
 
@@ -440,11 +442,15 @@ int setup_rows(lora_ctx *ctx, const lora_table *t, const int32_t *adapters, int 
                 ctx->dense = nullptr;
                 ctx->dense_cap = 0;
             }
-            if (cudaMalloc(reinterpret_cast<void **>(&ctx->dense), bytes) != cudaSuccess)
+            if (cudaMalloc(reinterpret_cast<void **>(&ctx->dense), 2 * bytes) != cudaSuccess)
                 return LORA_E_NOMEM;
             ctx->dense_cap = bytes;
         }
-        buf = ctx->dense;
+        // Consecutive staged calls use the two halves in turn, so a call's copy may
+        // run while the previous call's kernels still read theirs (early staging).
+        ctx->dense_turn ^= 1;
+        buf = ctx->dense + size_t(ctx->dense_turn) * ctx->dense_cap;
+        m->early = ctx->early_pages != 0;
     }
     m->staged = true;
     m->rp = rp;
@@ -469,6 +475,7 @@ int run_staging(lora_ctx *ctx, const lora_table *t, const RowMats &m, const int3
         StageArgs sa{};
         sa.max_rank = t->max_rank;
         sa.rp = m.rp;
+        sa.early = m.early ? 1 : 0;
         sa.n_slots = std::min(kStageSlots, n_slots - s0);
         for (int s = 0; s < sa.n_slots; ++s) {
             sa.adapter[s] = adapters[s0 + s];

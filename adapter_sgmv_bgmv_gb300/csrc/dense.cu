@@ -22,13 +22,10 @@ namespace {
 constexpr int kStageThreads = 128;
 constexpr int kPerThread = 8;                 // 16-byte vectors per thread per pass
 
-// One CTA per destination row: blockIdx.x = slot * rp + j, blockIdx.y = side.
-__global__ void __launch_bounds__(kStageThreads) k_stage_rows(const __grid_constant__ StageArgs a)
+// Destination row blockIdx.x = slot * rp + j of side blockIdx.y.
+__device__ __forceinline__ void stage_row(const StageArgs &a)
 {
     const StageSide &sd = a.side[blockIdx.y];
-    // Launched as a programmatic dependent; the previous kernels may still read
-    // the scratch, and the pools may be theirs to write.
-    grid_dep_wait();
     if (!sd.dst)
         return;
     const int row = int(blockIdx.x);
@@ -64,6 +61,21 @@ __global__ void __launch_bounds__(kStageThreads) k_stage_rows(const __grid_const
         for (int q = threadIdx.x; q < nv; q += kStageThreads)
             dst[q] = z;
     }
+}
+
+// One CTA per destination row.  Launched as a programmatic dependent of the kernel
+// before it: by default it waits for that kernel first (the pools may be its to
+// write).  Early (the caller's guarantee that the kernel just before writes no pool
+// or page table; the scratch half is not the one the previous call reads), it copies
+// first and waits after -- still before it ends, so that the kernels after it keep
+// the stream's order.
+__global__ void __launch_bounds__(kStageThreads) k_stage_rows(const __grid_constant__ StageArgs a)
+{
+    if (!a.early)
+        grid_dep_wait();
+    stage_row(a);
+    if (a.early)
+        grid_dep_wait();
 }
 
 }  // namespace

@@ -157,6 +157,7 @@ struct StageArgs {
     int max_rank;
     int rp;
     int n_slots;
+    int early;                // copy before waiting for the previous kernel (dense.cu)
     int32_t adapter[kStageSlots];
     int32_t rank[kStageSlots];
 };

@@ -226,7 +226,10 @@ class Bench:
         torch, L = self.torch, self.L
         from tests.gpu_util import to_dev
         per = max(1, self._unique_bytes_per_step())
-        self.n_sets = int(min(32, max(1, math.ceil(3 * L2_BYTES / per))))
+        # enough sets that a pass touches > 3 x L2, and at least two, so that the end
+        # to end loop can copy one step's inputs in while the previous result is read
+        # back (a set is refilled only after its result has left the device)
+        self.n_sets = int(min(32, max(2, math.ceil(3 * L2_BYTES / per))))
         self.sets = []
         base = {}
         for key, c in self.cases.items():

@@ -218,10 +218,14 @@ int lora_sync_status(lora_ctx *ctx, void *stream);
  *                          read nothing that kernel may write before it finishes.  With
  *                          1 the row-gather kernel copies the adapter pages (A and B
  *                          pools) before that wait, overlapping the previous kernel's
- *                          tail.  The caller then guarantees that no kernel launched
- *                          immediately before a delta call in the same stream writes
- *                          the pools (this library's own kernels never do; a copy or a
- *                          host-side wait in between is enough). */
+ *                          tail, and so does the tensor-core path's copy of scattered
+ *                          adapters into dense rows (it writes the half of its
+ *                          double-buffered scratch that the previous staged call does
+ *                          not read, and still waits before it ends).  The caller then
+ *                          guarantees that no kernel launched immediately before a
+ *                          delta, merge or unmerge call in the same stream writes the
+ *                          pools or page tables (this library's own kernels never do; a
+ *                          copy or a host-side wait in between is enough). */
 enum { LORA_OPT_TILE_PATH = 1, LORA_OPT_MERGE_KERNEL = 2, LORA_OPT_TILE_MIN_RUN = 3,
        LORA_OPT_EARLY_PAGES = 4 };
 int lora_ctx_set_option(lora_ctx *ctx, int option, int value);
