@@ -18,7 +18,7 @@ import torch
 from . import _lib
 
 __all__ = ["LoraError", "Context", "AdapterTable", "lora_plan_build", "lora_shrink",
-           "lora_expand", "lora_fused", "lora_fused_noalloc", "PreparedFused", "lora_merge", "lora_unmerge", "lora_tune_shape",
+           "lora_expand", "lora_fused", "lora_fused_noalloc", "PreparedFused", "lora_merge", "lora_unmerge", "lora_page_in", "lora_tune_shape",
            "KIND_ROWS_FUSED", "KIND_SHRINK", "KIND_EXPAND", "KIND_TILE_FUSED", "KIND_MERGE",
            "OPT_TILE_PATH", "OPT_MERGE_KERNEL", "OPT_TILE_MIN_RUN", "OPT_EARLY_PAGES",
            "library_path"]
@@ -321,6 +321,26 @@ def lora_unmerge(ctx: Context, table: AdapterTable, adapter: int, W: torch.Tenso
     """W <- bf16(W - s_k A_k B_k) in place."""
     pw, ldw, d_out = _rows(W, "W")
     _check(_L.lora_unmerge(ctx.handle, table.handle, int(adapter), pw, ldw, W.shape[0], d_out,
+                           _stream(stream, ctx.device)), ctx)
+
+
+def lora_page_in(ctx: Context, table: AdapterTable, adapter: int, host_a: torch.Tensor,
+                 host_b: torch.Tensor, stream=None):
+    """Copy adapter `adapter`'s A and B into its pages of the table's pools, on
+    `stream` (asynchronous).  host_a: [rank, d_in] and host_b: [rank, d_out] bf16 (or
+    their 16-bit images) in page-locked CPU memory, contiguous; row j of host_a is
+    column j of A_k, row j of host_b is row j of B_k.  Keep both alive and unchanged
+    until the stream has passed the call (see include/lora.h)."""
+    r = int(table.rank[int(adapter)]) if 0 <= int(adapter) < table.n_adapters else -1
+    for name, h in (("host_a", host_a), ("host_b", host_b)):
+        if not isinstance(h, torch.Tensor) or h.device.type != "cpu" or not h.is_pinned():
+            raise ValueError(f"{name} must be a page-locked CPU tensor")
+        if h.dim() != 2 or not h.is_contiguous() or h.element_size() != 2:
+            raise ValueError(f"{name} must be a contiguous 2-D 16-bit tensor")
+        if r >= 0 and h.shape[0] != r:
+            raise ValueError(f"{name} has {h.shape[0]} rows, adapter {adapter} has rank {r}")
+    _check(_L.lora_page_in(ctx.handle, table.handle, int(adapter), host_a.data_ptr(),
+                           host_a.shape[1], host_b.data_ptr(), host_b.shape[1],
                            _stream(stream, ctx.device)), ctx)
 
 

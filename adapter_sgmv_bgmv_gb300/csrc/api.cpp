@@ -72,6 +72,9 @@ struct lora_ctx {
     int tile_path = 1;              // 1: long same-adapter runs use the tensor-core tiles
     int tile_min_run_override = 0;  // > 0: fixed minimum run for the tile path
     int early_pages = 0;            // LORA_OPT_EARLY_PAGES
+    int call_early = 0;             // early page copies for the call in progress
+    cudaStream_t pool_write_stream = nullptr;   // stream of the last page-in ...
+    bool pool_write_pending = false;            // ... and no delta / merge launch after it yet
     int force_cluster = 0;          // > 0 while tuning: row-kernel cluster width
     int force_rows = 0;             // > 0 while tuning: rows per item
     uint8_t *vparts = nullptr;      // fused tile path: partial V between its two kernels
@@ -132,6 +135,23 @@ int use_device(lora_ctx *ctx)
 
 // Take the next staging slot with room for `bytes`; waits for the slot's previous
 // upload/launches to finish before reusing its buffers.
+// Early page copies for the call about to launch: the option, unless the kernel just
+// before on this stream may be a page-in, which writes the pools.
+void begin_call(lora_ctx *ctx, cudaStream_t stream)
+{
+    ctx->call_early = ctx->early_pages && !(ctx->pool_write_pending && ctx->pool_write_stream == stream);
+}
+
+// A launch of a delta / merge call: after it, the stream's previous kernel is no
+// longer a page-in.
+void count_launch(lora_ctx *ctx, cudaStream_t stream)
+{
+    ctx->last_launches += 1;
+    ctx->launches_total += 1;
+    if (ctx->pool_write_pending && ctx->pool_write_stream == stream)
+        ctx->pool_write_pending = false;
+}
+
 int acquire_slot(lora_ctx *ctx, size_t bytes, Slot **out)
 {
     Slot &s = ctx->slots[ctx->next_slot];
@@ -353,7 +373,7 @@ int run_rows(lora_ctx *ctx, const lora_table *t, int mode, RowsCfg cfg, const vo
     p.d_in = d_in;
     p.d_out = d_out;
     p.n_items = int(pl.row_items.size());
-    p.early_pages = ctx->early_pages;
+    p.early_pages = ctx->call_early;
     const long ev = prof_start(ctx, 0, stream);
     if (in_params && pl.row_items.size() <= 64 && pl.row_perm.size() <= 128) {
         RowsParamsInlineSmall &a = ctx->inline_small;
@@ -372,8 +392,7 @@ int run_rows(lora_ctx *ctx, const lora_table *t, int mode, RowsCfg cfg, const vo
     }
     prof_stop(ctx, ev, stream);
     ctx->last_path |= 1;
-    ctx->last_launches += 1;
-        ctx->launches_total += 1;
+    count_launch(ctx, stream);
     return slot ? release_slot(ctx, slot, stream) : LORA_OK;
 }
 
@@ -450,7 +469,7 @@ int setup_rows(lora_ctx *ctx, const lora_table *t, const int32_t *adapters, int 
         // run while the previous call's kernels still read theirs (early staging).
         ctx->dense_turn ^= 1;
         buf = ctx->dense + size_t(ctx->dense_turn) * ctx->dense_cap;
-        m->early = ctx->early_pages != 0;
+        m->early = ctx->call_early != 0;
     }
     m->staged = true;
     m->rp = rp;
@@ -488,8 +507,7 @@ int run_staging(lora_ctx *ctx, const lora_table *t, const RowMats &m, const int3
             sa.side[1] = StageSide{t->b_pool, t->b_pw, t->d_b_pages,
                                    const_cast<uint16_t *>(m.b) + int64_t(s0) * m.rp * d_out, d_out};
         CUDA_TRY(ctx, launch_stage_rows(sa, stream));
-        ctx->last_launches += 1;
-        ctx->launches_total += 1;
+        count_launch(ctx, stream);
     }
     return LORA_OK;
 }
@@ -609,8 +627,7 @@ int run_tiles(lora_ctx *ctx, const lora_table *t, int mode, const void *x, int64
             return rc;
         CUDA_TRY(ctx, launch_shrink_tc(p, stream));
         prof_stop(ctx, ev, stream);
-        ctx->last_launches += 1;
-        ctx->launches_total += 1;
+        count_launch(ctx, stream);
     }
     if (mode != kShrink) {
         const long ev = prof_start(ctx, 3, stream);
@@ -621,8 +638,7 @@ int run_tiles(lora_ctx *ctx, const lora_table *t, int mode, const void *x, int64
         }
         CUDA_TRY(ctx, launch_expand_tc(p, stream));
         prof_stop(ctx, ev, stream);
-        ctx->last_launches += 1;
-        ctx->launches_total += 1;
+        count_launch(ctx, stream);
     }
     ctx->last_path |= 2;
     return slot ? release_slot(ctx, slot, stream) : LORA_OK;
@@ -632,8 +648,10 @@ int delta_call(lora_ctx *ctx, const lora_table *t, int mode, const int32_t *ids,
                const void *x, int64_t ldx, int d_in, float *v, int64_t ldv, void *y,
                int64_t ldy, int d_out, cudaStream_t stream)
 {
-    if (ctx)
+    if (ctx) {
         ctx->last_path = ctx->last_launches = 0;
+        begin_call(ctx, stream);
+    }
     int rc = prepare(ctx, t, ids, n);
     if (rc != LORA_OK)
         return rc;
@@ -685,8 +703,10 @@ int delta_call(lora_ctx *ctx, const lora_table *t, int mode, const int32_t *ids,
 int merge_call(lora_ctx *ctx, const lora_table *t, int adapter, void *W, int64_t ldw,
                int d_in, int d_out, float sign, cudaStream_t stream)
 {
-    if (ctx)
+    if (ctx) {
         ctx->last_path = ctx->last_launches = 0;
+        begin_call(ctx, stream);
+    }
     if (!ctx || !t || t->ctx != ctx)
         return LORA_E_INVAL;
     if (adapter < 0 || adapter >= t->n_adapters)
@@ -743,8 +763,7 @@ int merge_call(lora_ctx *ctx, const lora_table *t, int adapter, void *W, int64_t
     }
     prof_stop(ctx, ev, stream);
     ctx->last_path = 4;
-    ctx->last_launches += 1;
-    ctx->launches_total += 1;
+    count_launch(ctx, stream);
     return LORA_OK;
 }
 
@@ -1040,8 +1059,10 @@ int lora_fused_noalloc(lora_ctx *ctx, const lora_table *t, const int32_t *ids, i
                        void *stream_ptr)
 {
     cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
-    if (ctx)
+    if (ctx) {
         ctx->last_path = ctx->last_launches = 0;
+        begin_call(ctx, stream);
+    }
     int rc = prepare(ctx, t, ids, n);
     if (rc != LORA_OK)
         return rc;
@@ -1094,6 +1115,63 @@ int lora_unmerge(lora_ctx *ctx, const lora_table *t, int adapter, void *W, int64
 {
     return merge_call(ctx, t, adapter, W, ldw, d_in, d_out, -1.f,
                       static_cast<cudaStream_t>(stream));
+}
+
+int lora_page_in(lora_ctx *ctx, const lora_table *t, int adapter, const void *host_a, int d_in,
+                 const void *host_b, int d_out, void *stream_ptr)
+{
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+    if (ctx)
+        ctx->last_path = ctx->last_launches = 0;
+    if (!ctx || !t || t->ctx != ctx)
+        return LORA_E_INVAL;
+    if (adapter < 0 || adapter >= t->n_adapters)
+        return LORA_E_ADAPTER;
+    if (t->status[size_t(adapter)] != LORA_OK)
+        return t->status[size_t(adapter)];
+    if (!host_a || !host_b || !aligned16(host_a) || !aligned16(host_b) || d_in <= 0 || d_out <= 0 ||
+        (d_in % 8) || (d_out % 8) || d_in > t->a_pw || d_out > t->b_pw)
+        return LORA_E_INVAL;
+    int rc = use_device(ctx);
+    if (rc != LORA_OK)
+        return rc;
+    // Both buffers must be page-locked host memory mapped into the device's address
+    // space: the kernel reads them directly.  Anything else is refused here, before
+    // any launch.
+    const void *dev_src[2] = {nullptr, nullptr};
+    const void *host[2] = {host_a, host_b};
+    for (int side = 0; side < 2; ++side) {
+        cudaPointerAttributes at{};
+        if (cudaPointerGetAttributes(&at, host[side]) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return LORA_E_INVAL;
+        }
+        if (at.type != cudaMemoryTypeHost || !at.devicePointer)
+            return LORA_E_INVAL;
+        dev_src[side] = at.devicePointer;
+    }
+    const int r = t->rank[size_t(adapter)];
+    PageInArgs a{};
+    a.rank = r;
+    a.side[0].host = static_cast<const uint16_t *>(dev_src[0]);
+    a.side[0].pool = const_cast<uint16_t *>(t->a_pool);
+    a.side[0].pw = t->a_pw;
+    a.side[0].width = d_in;
+    a.side[1].host = static_cast<const uint16_t *>(dev_src[1]);
+    a.side[1].pool = const_cast<uint16_t *>(t->b_pool);
+    a.side[1].pw = t->b_pw;
+    a.side[1].width = d_out;
+    for (int j = 0; j < r; ++j) {
+        a.side[0].page[j] = t->a_pages[size_t(adapter) * t->max_rank + j];
+        a.side[1].page[j] = t->b_pages[size_t(adapter) * t->max_rank + j];
+    }
+    CUDA_TRY(ctx, launch_page_in(a, stream));
+    ctx->last_path = 8;
+    ctx->last_launches = 1;
+    ctx->launches_total += 1;
+    ctx->pool_write_stream = stream;
+    ctx->pool_write_pending = true;
+    return LORA_OK;
 }
 
 int lora_tiles_load(lora_ctx *ctx, const char *path)

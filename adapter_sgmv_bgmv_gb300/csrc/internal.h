@@ -163,6 +163,22 @@ struct StageArgs {
 };
 cudaError_t launch_stage_rows(const StageArgs &a, cudaStream_t stream);
 
+// Adapter page-in (pagein.cu): rows j < rank of `host` (device-mapped page-locked
+// host memory, `width` elements each) to pool page page[j], for A and for B.
+constexpr int kPageInMaxRank = 128;
+struct PageInSide {
+    const uint16_t *host;     // device address of the host rows [rank][width]
+    uint16_t *pool;
+    int64_t pw;               // pool page width, elements
+    int width;                // elements copied per page (<= pw, multiple of 8)
+    int32_t page[kPageInMaxRank];
+};
+struct PageInArgs {
+    PageInSide side[2];       // A, B
+    int rank;
+};
+cudaError_t launch_page_in(const PageInArgs &a, cudaStream_t stream);
+
 cudaError_t launch_shrink_tc(const TileParams &p, cudaStream_t stream);
 cudaError_t launch_expand_tc(const TileParams &p, cudaStream_t stream);
 bool tile_tc_supported(int d_in, int d_out, int rank);

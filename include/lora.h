@@ -172,6 +172,27 @@ int lora_merge(lora_ctx *ctx, const lora_table *table, int adapter, void *W,
 int lora_unmerge(lora_ctx *ctx, const lora_table *table, int adapter, void *W,
                  int64_t ldw, int d_in, int d_out, void *stream);
 
+/* Adapter page-in (S-LoRA: adapters kept in host memory are brought into the unified
+ * pool when a batch needs them, overlapped with compute; VaLoRA, section 4.4.1: only
+ * A and B move): copies adapter `adapter`'s A and B from host memory into its pages
+ * of the table's pools, asynchronously on `stream`.
+ *   host_a  rank[adapter] rows of d_in bf16, row j = page j of A_k (column j of A_k)
+ *   host_b  rank[adapter] rows of d_out bf16, row j = page j of B_k (row j of B_k)
+ * Both rows-by-width blocks are contiguous, 16-byte aligned and page-locked
+ * (cudaHostAlloc, or cudaHostRegister'ed): one kernel reads them directly over the
+ * CPU-GPU link and writes the pool pages, so they must stay valid and unchanged
+ * until the stream has passed the call.  d_in <= the A page width, d_out <= the B
+ * page width, both multiples of 8; the rest of each page is left as it is.  The
+ * pools are written (they are the caller's device memory, registered with the
+ * table): the copy starts after every earlier kernel of the stream; a delta or
+ * merge call that reads the adapter on another stream must be ordered after it
+ * (an event).  With LORA_OPT_EARLY_PAGES, the next delta or merge call on the same
+ * stream takes no early page copies.  Errors (nothing launched): LORA_E_INVAL (a
+ * bad argument, or a buffer that is not page-locked host memory), LORA_E_ADAPTER,
+ * or the adapter's own problem (LORA_E_RANK, LORA_E_NOT_RESIDENT, LORA_E_PAGE). */
+int lora_page_in(lora_ctx *ctx, const lora_table *table, int adapter, const void *host_a,
+                 int d_in, const void *host_b, int d_out, void *stream);
+
 /* Shape -> tile-configuration table (VaLoRA blog, section 4.3.2: an offline
  * search stores the best tiling per input shape in a hash table that the runtime
  * looks up).  Lines of the text file are
@@ -244,8 +265,9 @@ int lora_profile_end(lora_ctx *ctx, double *ms, int64_t *launches);
 /* Kernels launched by this context since it was created. */
 int64_t lora_launch_count(const lora_ctx *ctx);
 
-/* Which kernel the last delta call launched: 0 none, 1 row-gather, 2 tensor-core
- * tile, 3 both; and how many kernels it launched. */
+/* Which kernel the last call launched: 0 none, 1 row-gather, 2 tensor-core tile,
+ * 3 both (delta calls), 4 merge / unmerge, 8 page-in; and how many kernels it
+ * launched. */
 int lora_last_path(const lora_ctx *ctx, int *n_launches);
 
 const char *lora_strerror(int code);

@@ -114,6 +114,30 @@ def test_library_plan_is_bit_exact_against_numpy(seed):
     assert ((t.a_pages >= 0).sum(axis=1) + (t.b_pages >= 0).sum(axis=1)).tolist() == (2 * ranks).tolist()
 
 
+def test_page_in_checks_its_arguments_before_anything_else():
+    """lora_page_in on a host-only context: argument errors first, then
+    LORA_E_UNSUPPORTED (no device, nothing launched)."""
+    import adapter_sgmv_bgmv_gb300 as L
+    ctx, t = _host_table()
+    a = np.zeros((8, 64), np.uint16)
+    b = np.zeros((8, 64), np.uint16)
+
+    def call(adapter, d_in, d_out):
+        rc = L._L.lora_page_in(ctx.handle, t.handle, adapter, a.ctypes.data, d_in,
+                               b.ctypes.data, d_out, None)
+        return L.ERROR_NAMES[rc]
+
+    assert call(99, 64, 64) == "LORA_E_ADAPTER"
+    assert call(-1, 64, 64) == "LORA_E_ADAPTER"
+    assert call(0, 12, 64) == "LORA_E_INVAL"      # not a multiple of 8
+    assert call(0, 64, 72) == "LORA_E_INVAL"      # wider than a page
+    assert call(0, 0, 64) == "LORA_E_INVAL"
+    assert call(0, 64, 64) == "LORA_E_UNSUPPORTED"
+    with pytest.raises(ValueError):               # the binding wants page-locked tensors
+        L.lora_page_in(ctx, t, 0, torch.zeros((8, 64), dtype=torch.int16),
+                       torch.zeros((8, 64), dtype=torch.int16))
+
+
 def test_library_plan_errors_on_host():
     import adapter_sgmv_bgmv_gb300 as L
     ctx, t = _host_table()
