@@ -18,7 +18,7 @@ import torch
 from . import _lib
 
 __all__ = ["LoraError", "Context", "AdapterTable", "lora_plan_build", "lora_shrink",
-           "lora_expand", "lora_fused", "lora_fused_noalloc", "PreparedFused", "lora_merge", "lora_unmerge", "lora_page_in", "lora_tune_shape",
+           "lora_expand", "lora_fused", "lora_fused_noalloc", "PreparedFused", "lora_merge", "lora_unmerge", "lora_page_in", "lora_fused_device_ids", "lora_tune_shape",
            "KIND_ROWS_FUSED", "KIND_SHRINK", "KIND_EXPAND", "KIND_TILE_FUSED", "KIND_MERGE",
            "OPT_TILE_PATH", "OPT_MERGE_KERNEL", "OPT_TILE_MIN_RUN", "OPT_EARLY_PAGES",
            "library_path"]
@@ -262,6 +262,21 @@ def lora_fused(ctx: Context, table: AdapterTable, ids, x: torch.Tensor, y: torch
                        _stream(stream, ctx.device))
     if rc:
         _check(rc, ctx)
+
+
+def lora_fused_device_ids(ctx: Context, table: AdapterTable, ids: torch.Tensor, x: torch.Tensor,
+                          y: torch.Tensor, stream=None):
+    """lora_fused with the ids in device memory (a CUDA int32 tensor [n], -1 =
+    released): planned on the GPU, nothing read on the host, graph-capturable.  An
+    id the table cannot serve leaves its row unchanged and shows up as
+    LORA_E_ADAPTER at the next sync_status (see include/lora.h)."""
+    if not isinstance(ids, torch.Tensor) or not ids.is_cuda or ids.dtype != torch.int32 or \
+            ids.dim() != 1 or not ids.is_contiguous():
+        raise ValueError("ids must be a contiguous 1-D int32 CUDA tensor")
+    px, ldx, d_in = _rows(x, "x")
+    py, ldy, d_out = _rows(y, "y")
+    _check(_L.lora_fused_device_ids(ctx.handle, table.handle, ids.data_ptr(), ids.shape[0], px,
+                                    ldx, d_in, py, ldy, d_out, _stream(stream, ctx.device)), ctx)
 
 
 def lora_fused_noalloc(ctx: Context, table: AdapterTable, ids, x: torch.Tensor, y: torch.Tensor,

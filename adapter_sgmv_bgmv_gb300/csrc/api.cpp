@@ -13,6 +13,7 @@
 
 #include "../../include/lora.h"
 #include "internal.h"
+#include "status.h"
 #include "plan.h"
 #include "tiles.h"
 
@@ -48,6 +49,7 @@ struct lora_ctx {
     int64_t max_rows = 0;
     int max_rank = 0;
     unsigned *d_status = nullptr;
+    uint8_t *d_dplan = nullptr;     // device-side plan: items [max_rows], perm [max_rows], count
     Slot slots[kSlots];
     int next_slot = 0;
     Plan plan;
@@ -102,6 +104,8 @@ struct lora_table {
     std::vector<uint8_t> a_contig, b_contig;   // per adapter: pages j < rank are p0 + j
     int32_t *d_rank = nullptr, *d_a_pages = nullptr, *d_b_pages = nullptr;
     float *d_scale = nullptr;
+    uint8_t *d_ok = nullptr;           // per adapter: 1 when its status is LORA_OK
+    int rank_max_ok = 0;               // largest rank among the adapters it can serve
 };
 
 namespace {
@@ -838,7 +842,8 @@ int lora_ctx_create(int device, int64_t max_rows, int max_rank, lora_ctx **out)
     cudaGetDevice(&prev);
     if (cudaSetDevice(device) != cudaSuccess ||
         cudaMalloc(reinterpret_cast<void **>(&ctx->d_status), 16) != cudaSuccess ||
-        cudaMemset(ctx->d_status, 0, 16) != cudaSuccess) {
+        cudaMemset(ctx->d_status, 0, 16) != cudaSuccess ||
+        cudaMalloc(reinterpret_cast<void **>(&ctx->d_dplan), size_t(max_rows) * 20 + 64) != cudaSuccess) {
         lora_ctx_destroy(ctx);
         cudaSetDevice(prev);
         return LORA_E_CUDA;
@@ -883,6 +888,8 @@ int lora_ctx_destroy(lora_ctx *ctx)
     }
     if (ctx->d_status)
         cudaFree(ctx->d_status);
+    if (ctx->d_dplan)
+        cudaFree(ctx->d_dplan);
     if (ctx->vparts)
         cudaFree(ctx->vparts);
     if (ctx->dense)
@@ -953,10 +960,16 @@ int lora_table_create(lora_ctx *ctx, const void *a_pool, int64_t a_n_pages, int 
         return LORA_OK;
     }
     std::vector<int32_t> ap(t->a_pages), bp(t->b_pages);
-    for (int k = 0; k < n_adapters; ++k)
-        if (t->status[size_t(k)] != LORA_OK)
+    std::vector<uint8_t> okv(size_t(n_adapters), 0);
+    for (int k = 0; k < n_adapters; ++k) {
+        if (t->status[size_t(k)] != LORA_OK) {
             for (int j = 0; j < max_rank; ++j)
                 ap[size_t(k) * max_rank + j] = bp[size_t(k) * max_rank + j] = 0;
+        } else {
+            okv[size_t(k)] = 1;
+            t->rank_max_ok = std::max(t->rank_max_ok, t->rank[size_t(k)]);
+        }
+    }
     int prev = 0;
     cudaGetDevice(&prev);
     bool okk = cudaSetDevice(ctx->device) == cudaSuccess &&
@@ -967,7 +980,9 @@ int lora_table_create(lora_ctx *ctx, const void *a_pool, int64_t a_n_pages, int 
                cudaMemcpy(t->d_rank, rank_host, sizeof(int32_t) * n_adapters, cudaMemcpyHostToDevice) == cudaSuccess &&
                cudaMemcpy(t->d_scale, scale_host, sizeof(float) * n_adapters, cudaMemcpyHostToDevice) == cudaSuccess &&
                cudaMemcpy(t->d_a_pages, ap.data(), sizeof(int32_t) * np, cudaMemcpyHostToDevice) == cudaSuccess &&
-               cudaMemcpy(t->d_b_pages, bp.data(), sizeof(int32_t) * np, cudaMemcpyHostToDevice) == cudaSuccess;
+               cudaMemcpy(t->d_b_pages, bp.data(), sizeof(int32_t) * np, cudaMemcpyHostToDevice) == cudaSuccess &&
+               cudaMalloc(reinterpret_cast<void **>(&t->d_ok), size_t(n_adapters)) == cudaSuccess &&
+               cudaMemcpy(t->d_ok, okv.data(), size_t(n_adapters), cudaMemcpyHostToDevice) == cudaSuccess;
     cudaSetDevice(prev);
     if (!okk) {
         lora_table_destroy(t);
@@ -995,6 +1010,7 @@ int lora_table_destroy(lora_table *t)
     cudaFree(t->d_scale);
     cudaFree(t->d_a_pages);
     cudaFree(t->d_b_pages);
+    cudaFree(t->d_ok);
     cudaSetDevice(prev);
     delete t;
     return LORA_OK;
@@ -1103,6 +1119,83 @@ int lora_fused_noalloc(lora_ctx *ctx, const lora_table *t, const int32_t *ids, i
     return rc;
 }
 
+int lora_fused_device_ids(lora_ctx *ctx, const lora_table *t, const int32_t *ids_dev, int64_t n,
+                          const void *x, int64_t ldx, int d_in, void *y, int64_t ldy, int d_out,
+                          void *stream_ptr)
+{
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+    if (ctx) {
+        ctx->last_path = ctx->last_launches = 0;
+        begin_call(ctx, stream);
+    }
+    if (!ctx || !t || t->ctx != ctx || n < 0 || n > ctx->max_rows ||
+        (n > 0 && (!ids_dev || (reinterpret_cast<uintptr_t>(ids_dev) & 3u))))
+        return LORA_E_INVAL;
+    if (t->n_adapters > kDevPlanMaxAdapters)
+        return LORA_E_UNSUPPORTED;
+    if (n == 0)
+        return LORA_OK;
+    if (!stride_ok(x, ldx, d_in) || d_in > t->a_pw || !stride_ok(y, ldy, d_out) || d_out > t->b_pw)
+        return LORA_E_INVAL;
+    int rc = use_device(ctx);
+    if (rc != LORA_OK)
+        return rc;
+    if (t->rank_max_ok == 0)
+        return LORA_E_ADAPTER;   // no adapter of the table can be served
+    // Launch shape from what the host knows: the batch size and the table.  Every
+    // row may be on its own adapter, so the grid has room for n items; the surplus
+    // clusters leave as soon as they read the plan's count.
+    const int64_t n_seg = std::min<int64_t>(n, t->n_adapters);
+    RowsCfg cfg = choose_rows_cfg(ctx, kFused, kKindRowsFused, n, n_seg, d_in, d_out, t->rank_max_ok);
+    RowsParams p{};
+    size_t smem = 0;
+    rc = rows_launch_params(kFused, cfg, d_in, d_out, t->rank_max_ok, p, smem);
+    if (rc != LORA_OK)
+        return rc;
+    RowItem *items = reinterpret_cast<RowItem *>(ctx->d_dplan);
+    int32_t *perm = reinterpret_cast<int32_t *>(ctx->d_dplan + size_t(ctx->max_rows) * sizeof(RowItem));
+    int32_t *count = reinterpret_cast<int32_t *>(ctx->d_dplan + size_t(ctx->max_rows) * 20);
+    DevPlanArgs pa{};
+    pa.ids = ids_dev;
+    pa.n = int(n);
+    pa.rank = t->d_rank;
+    pa.scale = t->d_scale;
+    pa.ok = t->d_ok;
+    pa.n_adapters = t->n_adapters;
+    pa.rows_per_item = p.rows_alloc;
+    pa.items = items;
+    pa.perm = perm;
+    pa.n_items = count;
+    pa.status = ctx->d_status;
+    CUDA_TRY(ctx, launch_plan_dev(pa, stream));
+    count_launch(ctx, stream);
+    p.x = static_cast<const uint16_t *>(x);
+    p.ldx = ldx;
+    p.y = static_cast<uint16_t *>(y);
+    p.ldy = ldy;
+    p.a_pool = t->a_pool;
+    p.a_pw = t->a_pw;
+    p.b_pool = t->b_pool;
+    p.b_pw = t->b_pw;
+    p.a_pages = t->d_a_pages;
+    p.b_pages = t->d_b_pages;
+    p.rank = t->d_rank;
+    p.scale = t->d_scale;
+    p.items = items;
+    p.perm = perm;
+    p.n_items_dev = count;
+    p.status = ctx->d_status;
+    p.max_rank = t->max_rank;
+    p.d_in = d_in;
+    p.d_out = d_out;
+    p.n_items = int(n);
+    p.early_pages = 0;   // the plan comes from the kernel before: nothing is read ahead of it
+    CUDA_TRY(ctx, launch_rows(kFused, p, smem, stream));
+    count_launch(ctx, stream);
+    ctx->last_path = 1;
+    return LORA_OK;
+}
+
 int lora_merge(lora_ctx *ctx, const lora_table *t, int adapter, void *W, int64_t ldw, int d_in,
                int d_out, void *stream)
 {
@@ -1202,7 +1295,7 @@ int lora_sync_status(lora_ctx *ctx, void *stream)
     CUDA_TRY(ctx, cudaMemcpy(&word, ctx->d_status, sizeof word, cudaMemcpyDeviceToHost));
     if (word != 0) {
         CUDA_TRY(ctx, cudaMemset(ctx->d_status, 0, sizeof word));
-        return LORA_E_TIMEOUT;
+        return word == kDevBadId ? LORA_E_ADAPTER : LORA_E_TIMEOUT;
     }
     return LORA_OK;
 }

@@ -62,6 +62,8 @@ struct RowsParams {
     int rows_alloc;           // shared-memory rows per item (>= every item's nrows)
     int early_pages;          // 1: adapter page copies issued before the dependency wait
     int rank_alloc;           // shared-memory rank slots (>= every item's rank)
+    const int32_t *n_items_dev;   // device-side plan: the item count (items past it idle),
+                                  // read after the wait for the kernel that wrote the plan
 };
 
 // Small plans travel inside the kernel parameter block (no separate upload), in
@@ -178,6 +180,24 @@ struct PageInArgs {
     int rank;
 };
 cudaError_t launch_page_in(const PageInArgs &a, cudaStream_t stream);
+
+// Device-side plan (devplan.cu) of a row-gather call over device-resident ids.
+constexpr int kDevPlanMaxAdapters = 16384;
+struct DevPlanArgs {
+    const int32_t *ids;       // [n], device
+    int n;
+    const int32_t *rank;      // table's device copies
+    const float *scale;
+    const uint8_t *ok;        // 1: the table can serve the adapter
+    int n_adapters;
+    int rows_per_item;
+    RowItem *items;           // [n] out
+    int32_t *perm;            // [n] out
+    int32_t *n_items;         // out
+    unsigned *status;
+};
+size_t dev_plan_smem_bytes(int n_adapters);
+cudaError_t launch_plan_dev(const DevPlanArgs &a, cudaStream_t stream);
 
 cudaError_t launch_shrink_tc(const TileParams &p, cudaStream_t stream);
 cudaError_t launch_expand_tc(const TileParams &p, cudaStream_t stream);

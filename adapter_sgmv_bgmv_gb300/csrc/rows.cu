@@ -102,6 +102,14 @@ __device__ __forceinline__ void rows_body(const RowsParams &pin, const RowItem *
     const bool clustered = (MODE != kExpand) && C > 1;
     const int item_id = blockIdx.x / C;
     const uint32_t crank = clustered ? cluster_ctarank() : uint32_t(blockIdx.x % C);
+    if (p.n_items_dev) {
+        // A device-side plan is the previous kernel's output: wait for it before
+        // reading it.  Clusters past its item count have nothing to do (a cluster
+        // shares its item, so all its CTAs leave together, before any barrier).
+        grid_dep_wait();
+        if (item_id >= *p.n_items_dev)
+            return;
+    }
     const RowItem it = items[item_id];
     const int k = it.adapter;
     const int r = it.rank;

@@ -12,7 +12,8 @@ enum DeviceStatus : unsigned {
     kDevTimeoutLoad = 1,   // a copy into shared memory did not complete in time
     kDevTimeoutMma = 2,    // a tensor-core commit did not arrive in time
     kDevTimeoutPipe = 3,   // a producer/consumer pipeline slot was not released
-    kDevBadShape = 4       // a kernel found a size it cannot handle (skipped)
+    kDevBadShape = 4,      // a kernel found a size it cannot handle (skipped)
+    kDevBadId = 5          // a device-resident adapter id the table cannot serve (row skipped)
 };
 
 }  // namespace lora

@@ -164,6 +164,27 @@ int lora_fused_noalloc(lora_ctx *ctx, const lora_table *table, const int32_t *id
                        int64_t n, const void *x, int64_t ldx, int d_in, void *y, int64_t ldy,
                        int d_out, void *stream);
 
+/* lora_fused with the adapter ids in device memory (ids_dev: int32 [n], 16-byte
+ * alignment not needed, 4-byte alignment required; -1 = released row), for decode
+ * batches whose ids are produced on the GPU.  LoRazor article: the operator's work
+ * follows the rows still active -- here the active rows are found on the device:
+ * a one-CTA plan kernel counts the rows per adapter, lays out the row-gather work
+ * items (at most R rows of one adapter each) and the by-adapter permutation in
+ * context scratch, and the row-gather kernel reads them after waiting for it; its
+ * grid has room for n items and the clusters past the plan's count leave at once.
+ * The call reads nothing on the host, copies nothing and allocates nothing, so it
+ * can be captured in a CUDA graph (and replayed with new ids written in place).
+ * Row-gather kernel only (no tensor-core tiles): meant for decode-sized batches.
+ * Results are those of lora_fused on the same ids, element for element.  An id
+ * outside [-1, n_adapters) or an adapter the table cannot serve leaves its row
+ * unchanged and makes the next lora_sync_status return LORA_E_ADAPTER (the host
+ * never sees the ids, so the call itself cannot).  Errors before any launch:
+ * LORA_E_INVAL (arguments, n > max_rows), LORA_E_UNSUPPORTED (more than 16384
+ * adapters in the table), LORA_E_ADAPTER (the table can serve no adapter). */
+int lora_fused_device_ids(lora_ctx *ctx, const lora_table *table, const int32_t *ids_dev,
+                          int64_t n, const void *x, int64_t ldx, int d_in, void *y,
+                          int64_t ldy, int d_out, void *stream);
+
 /* Merge / unmerge (mode switch): W[c, o] = bf16(W[c, o] +/- s_k sum_j A_k[c, j]
  * B_k[j, o]) in place, W [d_in, ldw] bf16 row-major.  Unmerge after merge restores
  * W to within two bf16 rounding steps (not bit-exactly). */

@@ -138,6 +138,29 @@ def test_page_in_checks_its_arguments_before_anything_else():
                        torch.zeros((8, 64), dtype=torch.int16))
 
 
+def test_device_ids_call_checks_its_arguments_on_the_host():
+    """lora_fused_device_ids never reads the ids on the host; its own arguments are
+    still checked before anything else, and a host-only context launches nothing."""
+    import adapter_sgmv_bgmv_gb300 as L
+    ctx, t = _host_table()
+    ids = np.zeros(4, np.int32)
+    x = np.zeros((4, 64), np.uint16)
+    y = np.zeros((4, 64), np.uint16)
+
+    def call(n, ids_ptr=ids.ctypes.data, ld=64, d=64):
+        rc = L._L.lora_fused_device_ids(ctx.handle, t.handle, ids_ptr, n, x.ctypes.data, ld, d,
+                                        y.ctypes.data, ld, d, None)
+        return L.ERROR_NAMES[rc]
+
+    assert call(4, ids_ptr=None) == "LORA_E_INVAL"
+    assert call(4, ids_ptr=ids.ctypes.data + 2) == "LORA_E_INVAL"   # misaligned ids
+    assert call(5000) == "LORA_E_INVAL"                              # > max_rows
+    assert call(-1) == "LORA_E_INVAL"
+    assert call(0) == "LORA_OK"                                      # nothing to do
+    assert call(4, d=72) == "LORA_E_INVAL"                           # wider than a page
+    assert call(4) == "LORA_E_UNSUPPORTED"                           # no device
+
+
 def test_library_plan_errors_on_host():
     import adapter_sgmv_bgmv_gb300 as L
     ctx, t = _host_table()
