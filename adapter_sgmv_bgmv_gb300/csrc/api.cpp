@@ -75,6 +75,7 @@ struct lora_ctx {
     int tile_min_run_override = 0;  // > 0: fixed minimum run for the tile path
     int early_pages = 0;            // LORA_OPT_EARLY_PAGES
     int call_early = 0;             // early page copies for the call in progress
+    int device_plan = 0;            // LORA_OPT_DEVICE_PLAN
     cudaStream_t pool_write_stream = nullptr;   // stream of the last page-in ...
     bool pool_write_pending = false;            // ... and no delta / merge launch after it yet
     int force_cluster = 0;          // > 0 while tuning: row-kernel cluster width
@@ -1144,14 +1145,45 @@ int lora_fused_device_ids(lora_ctx *ctx, const lora_table *t, const int32_t *ids
         return LORA_E_ADAPTER;   // no adapter of the table can be served
     // Launch shape from what the host knows: the batch size and the table.  Every
     // row may be on its own adapter, so the grid has room for n items; the surplus
-    // clusters leave as soon as they read the plan's count.
+    // clusters leave as soon as they read the plan's count (planned mode) or their
+    // row's id (direct mode: one row per cluster, no plan kernel).
     const int64_t n_seg = std::min<int64_t>(n, t->n_adapters);
     RowsCfg cfg = choose_rows_cfg(ctx, kFused, kKindRowsFused, n, n_seg, d_in, d_out, t->rank_max_ok);
+    if (!ctx->device_plan)
+        cfg.rows = 1;
     RowsParams p{};
     size_t smem = 0;
     rc = rows_launch_params(kFused, cfg, d_in, d_out, t->rank_max_ok, p, smem);
     if (rc != LORA_OK)
         return rc;
+    p.x = static_cast<const uint16_t *>(x);
+    p.ldx = ldx;
+    p.y = static_cast<uint16_t *>(y);
+    p.ldy = ldy;
+    p.a_pool = t->a_pool;
+    p.a_pw = t->a_pw;
+    p.b_pool = t->b_pool;
+    p.b_pw = t->b_pw;
+    p.a_pages = t->d_a_pages;
+    p.b_pages = t->d_b_pages;
+    p.rank = t->d_rank;
+    p.scale = t->d_scale;
+    p.status = ctx->d_status;
+    p.max_rank = t->max_rank;
+    p.d_in = d_in;
+    p.d_out = d_out;
+    p.n_items = int(n);
+    p.early_pages = 0;   // planned: the plan is the previous kernel's output
+    if (!ctx->device_plan) {
+        p.early_pages = ctx->call_early;   // ids and pages read ahead of the wait
+        p.ids_dev = ids_dev;
+        p.ok = t->d_ok;
+        p.n_adapters = t->n_adapters;
+        CUDA_TRY(ctx, launch_rows(kFused, p, smem, stream));
+        count_launch(ctx, stream);
+        ctx->last_path = 1;
+        return LORA_OK;
+    }
     RowItem *items = reinterpret_cast<RowItem *>(ctx->d_dplan);
     int32_t *perm = reinterpret_cast<int32_t *>(ctx->d_dplan + size_t(ctx->max_rows) * sizeof(RowItem));
     int32_t *count = reinterpret_cast<int32_t *>(ctx->d_dplan + size_t(ctx->max_rows) * 20);
@@ -1169,27 +1201,9 @@ int lora_fused_device_ids(lora_ctx *ctx, const lora_table *t, const int32_t *ids
     pa.status = ctx->d_status;
     CUDA_TRY(ctx, launch_plan_dev(pa, stream));
     count_launch(ctx, stream);
-    p.x = static_cast<const uint16_t *>(x);
-    p.ldx = ldx;
-    p.y = static_cast<uint16_t *>(y);
-    p.ldy = ldy;
-    p.a_pool = t->a_pool;
-    p.a_pw = t->a_pw;
-    p.b_pool = t->b_pool;
-    p.b_pw = t->b_pw;
-    p.a_pages = t->d_a_pages;
-    p.b_pages = t->d_b_pages;
-    p.rank = t->d_rank;
-    p.scale = t->d_scale;
     p.items = items;
     p.perm = perm;
     p.n_items_dev = count;
-    p.status = ctx->d_status;
-    p.max_rank = t->max_rank;
-    p.d_in = d_in;
-    p.d_out = d_out;
-    p.n_items = int(n);
-    p.early_pages = 0;   // the plan comes from the kernel before: nothing is read ahead of it
     CUDA_TRY(ctx, launch_rows(kFused, p, smem, stream));
     count_launch(ctx, stream);
     ctx->last_path = 1;
@@ -1317,6 +1331,7 @@ int lora_ctx_set_option(lora_ctx *ctx, int option, int value)
         ctx->tile_min_run_override = value;
         return LORA_OK;
     case LORA_OPT_EARLY_PAGES: ctx->early_pages = value ? 1 : 0; return LORA_OK;
+    case LORA_OPT_DEVICE_PLAN: ctx->device_plan = value ? 1 : 0; return LORA_OK;
     default: return LORA_E_INVAL;
     }
 }

@@ -64,6 +64,10 @@ struct RowsParams {
     int rank_alloc;           // shared-memory rank slots (>= every item's rank)
     const int32_t *n_items_dev;   // device-side plan: the item count (items past it idle),
                                   // read after the wait for the kernel that wrote the plan
+    const int32_t *ids_dev;       // direct mode: one row per item, item i = row i, its
+                                  // adapter read from here after the wait (no plan)
+    const uint8_t *ok;            // direct mode: 1 where the table can serve the adapter
+    int n_adapters;               // direct mode
 };
 
 // Small plans travel inside the kernel parameter block (no separate upload), in

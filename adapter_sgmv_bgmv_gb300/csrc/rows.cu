@@ -102,15 +102,41 @@ __device__ __forceinline__ void rows_body(const RowsParams &pin, const RowItem *
     const bool clustered = (MODE != kExpand) && C > 1;
     const int item_id = blockIdx.x / C;
     const uint32_t crank = clustered ? cluster_ctarank() : uint32_t(blockIdx.x % C);
-    if (p.n_items_dev) {
-        // A device-side plan is the previous kernel's output: wait for it before
-        // reading it.  Clusters past its item count have nothing to do (a cluster
-        // shares its item, so all its CTAs leave together, before any barrier).
-        grid_dep_wait();
-        if (item_id >= *p.n_items_dev)
+    const bool direct = p.ids_dev != nullptr;
+    RowItem it;
+    if (direct) {
+        // Device-resident ids, one row per cluster: item i is row i, of the adapter
+        // the ids give -- read after the wait for the previous kernel, unless early
+        // page copies are on (the caller's guarantee then covers the ids too: the
+        // kernel just before does not write them).  A released row has nothing to
+        // do; a row whose id the table cannot serve is left as it is and flagged.  A
+        // cluster shares its row, so all its CTAs leave together, before any barrier.
+        if (!p.early_pages)
+            grid_dep_wait();
+        const int ka = p.ids_dev[item_id];
+        if (ka == -1)
             return;
+        if (ka < -1 || ka >= p.n_adapters || !p.ok[ka]) {
+            if (crank == 0 && threadIdx.x == 0)
+                raise_status(p.status, kDevBadId);
+            return;
+        }
+        it.adapter = ka;
+        it.p0 = item_id;
+        it.nrows = 1;
+        it.rank = int16_t(p.rank[ka]);
+        it.scale = p.scale[ka];
+    } else {
+        if (p.n_items_dev) {
+            // A device-side plan is the previous kernel's output: wait for it before
+            // reading it.  Clusters past its item count have nothing to do (a cluster
+            // shares its item, so all its CTAs leave together, before any barrier).
+            grid_dep_wait();
+            if (item_id >= *p.n_items_dev)
+                return;
+        }
+        it = items[item_id];
     }
-    const RowItem it = items[item_id];
     const int k = it.adapter;
     const int r = it.rank;
     const int nrows = it.nrows;
@@ -150,7 +176,7 @@ __device__ __forceinline__ void rows_body(const RowsParams &pin, const RowItem *
                 pb1 = bp[lane + 32];
         }
         if (lane < nrows)
-            pr0 = perm[it.p0 + lane];
+            pr0 = direct ? it.p0 : perm[it.p0 + lane];
         if (lane + 32 < nrows)
             pr1 = perm[it.p0 + lane + 32];
         for (int q = lane; q < nrows; q += 32)

@@ -168,10 +168,13 @@ int lora_fused_noalloc(lora_ctx *ctx, const lora_table *table, const int32_t *id
  * alignment not needed, 4-byte alignment required; -1 = released row), for decode
  * batches whose ids are produced on the GPU.  LoRazor article: the operator's work
  * follows the rows still active -- here the active rows are found on the device:
- * a one-CTA plan kernel counts the rows per adapter, lays out the row-gather work
- * items (at most R rows of one adapter each) and the by-adapter permutation in
- * context scratch, and the row-gather kernel reads them after waiting for it; its
- * grid has room for n items and the clusters past the plan's count leave at once.
+ * by default each row-gather cluster takes one row and reads its adapter id
+ * itself (after waiting for the kernel that wrote the ids); with
+ * LORA_OPT_DEVICE_PLAN = 1 a one-CTA plan kernel first counts the rows per adapter,
+ * lays out work items (at most R rows of one adapter each) and the by-adapter
+ * permutation in context scratch, which the row-gather kernel reads after waiting
+ * for it.  Either way the grid has room for n items and the idle clusters leave at
+ * once.
  * The call reads nothing on the host, copies nothing and allocates nothing, so it
  * can be captured in a CUDA graph (and replayed with new ids written in place).
  * Row-gather kernel only (no tensor-core tiles): meant for decode-sized batches.
@@ -267,9 +270,17 @@ int lora_sync_status(lora_ctx *ctx, void *stream);
  *                          guarantees that no kernel launched immediately before a
  *                          delta, merge or unmerge call in the same stream writes the
  *                          pools or page tables (this library's own kernels never do; a
- *                          copy or a host-side wait in between is enough). */
+ *                          copy or a host-side wait in between is enough).
+ *                          For lora_fused_device_ids in its default mode the guarantee
+ *                          covers the device ids as well: with 1 the kernel reads them
+ *                          (and copies the pages they select) before the wait.
+ *   LORA_OPT_DEVICE_PLAN   lora_fused_device_ids: 0 (default) one row per row-gather
+ *                          cluster, its adapter read from the device ids by the kernel
+ *                          itself (one launch); 1 a plan kernel first groups the rows by
+ *                          adapter into items of several rows (two launches, fewer
+ *                          re-reads of a shared adapter). */
 enum { LORA_OPT_TILE_PATH = 1, LORA_OPT_MERGE_KERNEL = 2, LORA_OPT_TILE_MIN_RUN = 3,
-       LORA_OPT_EARLY_PAGES = 4 };
+       LORA_OPT_EARLY_PAGES = 4, LORA_OPT_DEVICE_PLAN = 5 };
 int lora_ctx_set_option(lora_ctx *ctx, int option, int value);
 
 /* Per-launch timing: between lora_profile_begin and lora_profile_end every

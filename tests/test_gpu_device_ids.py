@@ -25,7 +25,10 @@ def _bucket(m: int) -> int:
     return b
 
 
-def _context(tmp_path, c, ids, cluster=4, rows=2):
+MODES = [0, 1]   # LORA_OPT_DEVICE_PLAN: one row per cluster / a plan kernel first
+
+
+def _context(tmp_path, c, ids, mode=0, cluster=4, rows=2):
     """A context whose tile table gives the host-planned call (keyed by its active
     rows, distinct adapters and their largest rank) and the device-planned call
     (keyed by n, min(n, adapters) and the table's largest rank) the same shape."""
@@ -44,6 +47,7 @@ def _context(tmp_path, c, ids, cluster=4, rows=2):
     ctx = L.Context(0, max_rows=4096, max_rank=64)
     ctx.tiles_load(str(path))
     ctx.set_option(L.OPT_TILE_PATH, 0)
+    ctx.set_option(L.OPT_DEVICE_PLAN, mode)
     return ctx
 
 
@@ -69,11 +73,12 @@ CASES = {
 }
 
 
+@pytest.mark.parametrize("mode", MODES)
 @pytest.mark.parametrize("name", sorted(CASES))
-def test_device_ids_match_host_ids_bit_for_bit(tmp_path, name):
+def test_device_ids_match_host_ids_bit_for_bit(tmp_path, name, mode):
     c, ids = CASES[name]()
     ids = c["ids"] if ids is None else ids
-    ctx = _context(tmp_path, c, ids)
+    ctx = _context(tmp_path, c, ids, mode)
     table = upload_table(ctx, c)
     got_host, got_dev = _both(ctx, table, c, ids)
     np.testing.assert_array_equal(got_dev, got_host)
@@ -85,11 +90,14 @@ def test_device_ids_match_host_ids_bit_for_bit(tmp_path, name):
     ctx.close()
 
 
-def test_device_ids_in_a_cuda_graph_replayed_with_new_ids(tmp_path):
+@pytest.mark.parametrize("early", [0, 1])
+@pytest.mark.parametrize("mode", MODES)
+def test_device_ids_in_a_cuda_graph_replayed_with_new_ids(tmp_path, mode, early):
     c = workloads.make("llama7b_decode_het", seed=4)
     rng = np.random.default_rng(72)
     id_sets = [c["ids"]] + [rng.integers(-1, len(c["rank"]), c["n"]).astype(np.int32) for _ in range(3)]
-    ctx = _context(tmp_path, c, c["ids"])
+    ctx = _context(tmp_path, c, c["ids"], mode)
+    ctx.set_option(L.OPT_EARLY_PAGES, early)   # the ids are rewritten by a copy, not a kernel
     table = upload_table(ctx, c)
     x = to_dev(c["x"])
     y0 = to_dev(c["y"])
@@ -116,13 +124,14 @@ def test_device_ids_in_a_cuda_graph_replayed_with_new_ids(tmp_path):
     ctx.close()
 
 
-def test_bad_device_ids_leave_their_rows_and_surface_at_sync(tmp_path):
+@pytest.mark.parametrize("mode", MODES)
+def test_bad_device_ids_leave_their_rows_and_surface_at_sync(tmp_path, mode):
     c = workloads.small(seed=73, n=64, d_in=256, d_out=256, n_adapters=4, ranks=[8, 16, 8, 16])
     ids = c["ids"].copy()
     bad = ids.copy()
     bad[5] = 4                                        # past the table
     bad[9] = -7                                       # below -1
-    ctx = _context(tmp_path, c, ids)
+    ctx = _context(tmp_path, c, ids, mode)
     table = upload_table(ctx, c)
     x = to_dev(c["x"])
     y = to_dev(c["y"])
