@@ -28,13 +28,18 @@
  *  - Element type: bf16 (bit pattern in 16 bits) for x, y, W and the pools; fp32
  *    for v and scales; int32 for ids and page ids.  Matrices are row-major with a
  *    row stride given in elements (ld*).
- *  - Pointers named *_host are host memory; every other data pointer is device
- *    memory of the context's device, owned by the caller (the library never frees
- *    it).  Device pointers and row strides must be 16-byte aligned (ld* and widths
- *    multiples of 8 elements).
+ *  - Pointers named *_host (and lora_page_in's host_a / host_b) are host memory;
+ *    every other data pointer is device memory of the context's device, owned by
+ *    the caller (the library never frees it).  Device pointers and row strides
+ *    must be 16-byte aligned (ld* and widths multiples of 8 elements).
  *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls are
  *    asynchronous on that stream; ids are read on the host during the call and
- *    need not outlive it.  A context is not thread-safe.
+ *    need not outlive it (lora_fused_device_ids excepted: its ids stay on the
+ *    device and must stay valid until the stream has passed the call).  A context
+ *    is not thread-safe, and its scratch (partial V, dense adapter rows, the
+ *    device-side plan) is shared by its calls: calls of one context that could
+ *    overlap on the GPU (different streams) must be ordered by events; page-in
+ *    uses no scratch.
  *  - Ranks must be multiples of 8 in [8, LORA_MAX_RANK].
  */
 #ifndef LORA_H
