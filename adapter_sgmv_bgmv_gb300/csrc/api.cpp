@@ -1179,7 +1179,9 @@ int lora_fused_device_ids(lora_ctx *ctx, const lora_table *t, const int32_t *ids
         p.ids_dev = ids_dev;
         p.ok = t->d_ok;
         p.n_adapters = t->n_adapters;
+        const long ev = prof_start(ctx, 0, stream);
         CUDA_TRY(ctx, launch_rows(kFused, p, smem, stream));
+        prof_stop(ctx, ev, stream);
         count_launch(ctx, stream);
         ctx->last_path = 1;
         return LORA_OK;
@@ -1204,7 +1206,9 @@ int lora_fused_device_ids(lora_ctx *ctx, const lora_table *t, const int32_t *ids
     p.items = items;
     p.perm = perm;
     p.n_items_dev = count;
+    const long ev = prof_start(ctx, 0, stream);
     CUDA_TRY(ctx, launch_rows(kFused, p, smem, stream));
+    prof_stop(ctx, ev, stream);
     count_launch(ctx, stream);
     ctx->last_path = 1;
     return LORA_OK;

@@ -39,6 +39,7 @@ FALLBACK_BF16_TFLOPS = 1900.0
 DEFAULT_CONFIG = "llama7b_decode"
 CONFIGS = ("llama7b_decode", "tiny_decode", "slora_prefill", "valora_prefill", "valora_merge",
            "lorazor_decode")
+DEVICE_IDS_CONFIGS = ("llama7b_decode", "tiny_decode", "lorazor_decode")
 
 
 # --------------------------------------------------------------------------- peaks
@@ -172,8 +173,13 @@ def flops_delta(case, ids):
 class Bench:
     """Device-resident rotating copies of one workload and the per-step calls."""
 
-    def __init__(self, name: str, L, torch, ctx):
+    def __init__(self, name: str, L, torch, ctx, device_ids: bool = False):
         self.name, self.L, self.torch, self.ctx = name, L, torch, ctx
+        if device_ids and name not in DEVICE_IDS_CONFIGS:
+            raise ValueError(f"--device-ids applies to the decode workloads {DEVICE_IDS_CONFIGS}")
+        # decode through lora_fused_device_ids: every set holds its steps' ids in
+        # device memory (the end-to-end loop copies them in with the step's inputs)
+        self.device_ids = device_ids
         self.calls = []          # list of (case_key, ids) per step, for delta workloads
         if name == "llama7b_decode":
             het = workloads.make("llama7b_decode_het", seed=0)
@@ -274,6 +280,11 @@ class Bench:
                     d["call"] = L.PreparedFused(self.ctx, d["table"], d["x"], d["y"],
                                                 torch.cuda.current_stream())
                 st[key] = d
+            if self.device_ids:
+                for t, calls in enumerate(self.steps_ids):
+                    for key, ids in calls:
+                        st[("ids", t, key)] = torch.from_numpy(
+                            np.ascontiguousarray(ids, np.int32)).cuda()
             st["_blk"] = blk
             self.sets.append(st)
         torch.cuda.synchronize()
@@ -288,7 +299,16 @@ class Bench:
             L.lora_merge(self.ctx, d["table"], k, d["W"], stream)
             L.lora_unmerge(self.ctx, d["table"], k, d["W"], stream)
             return
-        for key, ids in self.steps_ids[i % len(self.steps_ids)]:
+        t = i % len(self.steps_ids)
+        for key, ids in self.steps_ids[t]:
+            self._call(st, t, key, ids, stream)
+
+    def _call(self, st, t, key, ids, stream):
+        if self.device_ids:
+            d = st[key]
+            self.L.lora_fused_device_ids(self.ctx, d["table"], st[("ids", t, key)], d["x"], d["y"],
+                                         stream)
+        else:
             st[key]["call"](ids)
 
     def tokens_per_step(self, i: int) -> int:
@@ -313,7 +333,7 @@ class Bench:
         if self.is_merge:
             return
         for key, ids in self.steps_ids[0]:
-            self.sets[0][key]["call"](ids)
+            self._call(self.sets[0], 0, key, ids, self.torch.cuda.current_stream())
             self.paths[key] = self.ctx.last_path()[0]
         self.torch.cuda.synchronize()
 
@@ -353,6 +373,9 @@ class Bench:
             self.out_elems = self.blk_elems - self.y_offset
         self.host_out = [torch.empty(self.out_elems, dtype=torch.int16).pin_memory()
                          for _ in range(self.n_sets)]
+        if self.device_ids:
+            self.host_ids = {(t, key): torch.from_numpy(np.ascontiguousarray(ids, np.int32)).pin_memory()
+                             for t, calls in enumerate(self.steps_ids) for key, ids in calls}
         self.s_in, self.s_out = torch.cuda.Stream(), torch.cuda.Stream()
         rt = _runtime()
         self.rt = rt
@@ -395,6 +418,12 @@ class Bench:
             _rt_check(rt.cudaStreamWaitEvent(*op["refill_wait"]))
         self.used[k] = True
         _rt_check(rt.cudaMemcpyAsync(*op["copy_in"]))
+        t = 0 if self.is_merge else i % len(self.steps_ids)
+        if self.device_ids:
+            for key, _ in self.steps_ids[t]:
+                dev, host = st[("ids", t, key)], self.host_ids[(t, key)]
+                _rt_check(rt.cudaMemcpyAsync(ctypes.c_void_p(dev.data_ptr()), ctypes.c_void_p(host.data_ptr()),
+                                             ctypes.c_size_t(4 * host.numel()), 1, op["copy_in"][4]))
         _rt_check(rt.cudaEventRecord(*op["rec_in"]))
         _rt_check(rt.cudaStreamWaitEvent(*op["wait_in"]))
         h2d = self.e2e_bytes[0]
@@ -404,8 +433,8 @@ class Bench:
             self.L.lora_merge(self.ctx, d["table"], a, d["W"], stream)
             self.L.lora_unmerge(self.ctx, d["table"], a, d["W"], stream)
         else:
-            for key, ids in self.steps_ids[i % len(self.steps_ids)]:
-                st[key]["call"](ids)
+            for key, ids in self.steps_ids[t]:
+                self._call(st, t, key, ids, stream)
                 h2d += 4 * len(ids)
         _rt_check(rt.cudaEventRecord(*op["rec_c"]))
         _rt_check(rt.cudaStreamWaitEvent(*op["wait_c"]))
@@ -523,6 +552,8 @@ def main():
     ap.add_argument("--profile-every", type=int, default=8,
                     help="bracket one kernel launch in N with CUDA events (roofline timing)")
     ap.add_argument("--tiles", default=os.path.join(ROOT, "adapter_sgmv_bgmv_gb300", "tiles.tbl"))
+    ap.add_argument("--device-ids", action="store_true",
+                    help="decode workloads through lora_fused_device_ids (ids in device memory)")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -548,6 +579,8 @@ def main():
     # the adapter pools: the row-gather kernel may copy pages before its wait.
     ctx.set_option(L.OPT_EARLY_PAGES, 0 if args.no_early_pages else 1)
     names = list(CONFIGS) if args.all else [args.config]
+    if args.device_ids:
+        names = [n for n in names if n in DEVICE_IDS_CONFIGS]
     for name in names:
         line = run_one(name, args, L, torch, ctx, dist, world, rank, local)
         if rank == 0:
@@ -581,7 +614,7 @@ def default_steps(name):
 def run_one(name, args, L, torch, ctx, dist, world, rank, local):
     K = args.steps if args.steps is not None else default_steps(name)
     W = max(3, args.warmup)
-    b = Bench(name, L, torch, ctx)
+    b = Bench(name, L, torch, ctx, device_ids=args.device_ids)
     stream = torch.cuda.current_stream()
     uuid = None
     try:
@@ -650,7 +683,8 @@ def run_one(name, args, L, torch, ctx, dist, world, rank, local):
                              "alg_bytes_per_launch": fam_bytes.get(f, 0) / n,
                              "GB/s": round(gbs, 1), "frac": round(gbs / pk["hbm_gbs"], 4)}
     per_kernel = {f: v["us_per_launch"] for f, v in per_family.items()}
-    kernel_names = {"rows": "k_rows_inline<fused>", "shrink": "k_shrink_tc",
+    kernel_names = {"rows": "k_rows<fused> (device ids)" if b.device_ids else "k_rows_inline<fused>",
+                    "shrink": "k_shrink_tc",
                     "expand": "k_stream_tc(expand)", "merge": "k_stream_tc(merge)"}
     dominant = max(per_family, key=lambda f: prof[f][0])
     achieved_gbs = per_family[dominant]["GB/s"]
@@ -670,13 +704,13 @@ def run_one(name, args, L, torch, ctx, dist, world, rank, local):
                          f"({b.n_sets * b._unique_bytes_per_step() / 1e6:.0f} MB touched per pass "
                          f"> 129 MB L2)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "early_pages": not args.no_early_pages},
+                   "early_pages": not args.no_early_pages, "device_ids": b.device_ids},
         "us_per_call": {"device": 1e6 * sec / max(1, K * b.calls_per_step()),
                         "per_kernel_launch": per_kernel},
         "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": pk["hbm_gbs"],
                      "unit": "GB/s",
                      "frac": (achieved_gbs / pk["hbm_gbs"]) if achieved_gbs else None,
-                     "traffic": MEASURED_TRAFFIC.get((name, dominant)),
+                     "traffic": None if b.device_ids else MEASURED_TRAFFIC.get((name, dominant)),
                      "peak_source": pk["source"],
                      "kernel": kernel_names[dominant],
                      "bytes_per_launch": per_family[dominant]["alg_bytes_per_launch"],
