@@ -138,6 +138,11 @@ class Context:
         """Synchronize and read back the device status word (raises on a timeout)."""
         return _check(_L.lora_sync_status(self.handle, _stream(stream, self.device)), self)
 
+    def selftest_timeout(self, limit_us: int = 10000, stream=None):
+        """Launch a bounded wait that runs out (see include/lora.h): the next
+        sync_status raises LORA_E_TIMEOUT and the context stays usable."""
+        _check(_L.lora_selftest_timeout(self.handle, int(limit_us), _stream(stream, self.device)), self)
+
     def set_option(self, option: int, value: int):
         """LORA_OPT_* (see include/lora.h): OPT_TILE_PATH, OPT_MERGE_KERNEL,
         OPT_TILE_MIN_RUN, OPT_EARLY_PAGES, OPT_DEVICE_PLAN."""

@@ -39,6 +39,7 @@ SIGNATURES = {
     "lora_unmerge": ([P, P, I, P, I64, I, I, P], I),
     "lora_page_in": ([P, P, I, P, I, P, I, P], I),
     "lora_fused_device_ids": ([P, P, P, I64, P, I64, I, P, I64, I, P], I),
+    "lora_selftest_timeout": ([P, I64, P], I),
     "lora_tiles_load": ([P, ctypes.c_char_p], I),
     "lora_tiles_save": ([P, ctypes.c_char_p], I),
     "lora_tiles_count": ([P], I64),

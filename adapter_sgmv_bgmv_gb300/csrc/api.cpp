@@ -1285,6 +1285,19 @@ int lora_page_in(lora_ctx *ctx, const lora_table *t, int adapter, const void *ho
     return LORA_OK;
 }
 
+int lora_selftest_timeout(lora_ctx *ctx, int64_t limit_us, void *stream)
+{
+    if (!ctx || limit_us < 1 || limit_us > 1000000)
+        return LORA_E_INVAL;
+    int rc = use_device(ctx);
+    if (rc != LORA_OK)
+        return rc;
+    CUDA_TRY(ctx, launch_wait_selftest(ctx->d_status, uint64_t(limit_us) * 1000u,
+                                       static_cast<cudaStream_t>(stream)));
+    ctx->launches_total += 1;
+    return LORA_OK;
+}
+
 int lora_tiles_load(lora_ctx *ctx, const char *path)
 {
     if (!ctx || !path)

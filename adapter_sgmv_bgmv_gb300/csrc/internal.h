@@ -201,6 +201,7 @@ struct DevPlanArgs {
     unsigned *status;
 };
 size_t dev_plan_smem_bytes(int n_adapters);
+cudaError_t launch_wait_selftest(unsigned *status, uint64_t limit_ns, cudaStream_t stream);
 cudaError_t launch_plan_dev(const DevPlanArgs &a, cudaStream_t stream);
 
 cudaError_t launch_shrink_tc(const TileParams &p, cudaStream_t stream);

@@ -299,6 +299,14 @@ int lora_ctx_set_option(lora_ctx *ctx, int option, int value);
 int lora_profile_begin(lora_ctx *ctx, int every);
 int lora_profile_end(lora_ctx *ctx, double *ms, int64_t *launches);
 
+/* Failure-detection self-test: launches one thread that waits, for limit_us
+ * microseconds (1 .. 1e6), on a barrier nothing arrives on -- the bounded wait every
+ * kernel of this library uses -- so that the wait gives up, records a timeout in
+ * the status word and returns.  The next lora_sync_status on the stream then
+ * returns LORA_E_TIMEOUT (and clears the word); the context stays usable.  No
+ * trap, no fault: the kernel ends normally. */
+int lora_selftest_timeout(lora_ctx *ctx, int64_t limit_us, void *stream);
+
 /* Kernels launched by this context since it was created. */
 int64_t lora_launch_count(const lora_ctx *ctx);
 

@@ -159,6 +159,8 @@ def test_device_ids_call_checks_its_arguments_on_the_host():
     assert call(0) == "LORA_OK"                                      # nothing to do
     assert call(4, d=72) == "LORA_E_INVAL"                           # wider than a page
     assert call(4) == "LORA_E_UNSUPPORTED"                           # no device
+    assert L.ERROR_NAMES[L._L.lora_selftest_timeout(ctx.handle, 0, None)] == "LORA_E_INVAL"
+    assert L.ERROR_NAMES[L._L.lora_selftest_timeout(ctx.handle, 10, None)] == "LORA_E_UNSUPPORTED"
 
 
 def test_library_plan_errors_on_host():

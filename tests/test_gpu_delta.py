@@ -334,3 +334,19 @@ def test_early_staging_changes_nothing(ctx):
         np.testing.assert_array_equal(a, b)
     ref = oracle.fused(oracle.Table.from_case(c1), c1["ids"], c1["x"], c1["y"], nthreads=8)
     assert_parity(got[1][0], ref, REL_FROB, MAX_ABS_RMS, "early staging")
+
+
+def test_a_wait_that_runs_out_is_reported_and_the_context_stays_usable(ctx):
+    """Failure detection without a fault: a bounded wait on a barrier nothing arrives
+    on gives up after 10 ms, the status word records it, sync_status reports
+    LORA_E_TIMEOUT once, and the next call on the same context is exact."""
+    ctx.sync_status()
+    ctx.selftest_timeout(10000)
+    with pytest.raises(L.LoraError) as e:
+        ctx.sync_status()
+    assert e.value.name == "LORA_E_TIMEOUT"
+    ctx.sync_status()                                 # the word was cleared
+    c = workloads.make("tiny_decode", seed=9)
+    got = run_fused(ctx, c)
+    ref = oracle.fused(oracle.Table.from_case(c), c["ids"], c["x"], c["y"], nthreads=8)
+    assert_parity(got, ref, REL_FROB, MAX_ABS_RMS, "after a timed-out wait")
