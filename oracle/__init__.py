@@ -18,6 +18,12 @@ Functions and the passages they follow:
 * :func:`merge` -- W +/- s_k A_k B_k in place (VaLoRA blog, section 4.4.1 swift mode
   switch; S-LoRA page, Batching, formula 1).  Pinned by brute force and by
   merged == unmerged inference.
+* :func:`base_fused` -- y_i = x_i W + s_k (x_i A_k) B_k rounded once (x_i W alone for a
+  released row): the delta fused into the base projection (S-LoRA page, Batching,
+  formula 2; VaLoRA blog, C2, unmerged inference; LoRazor page: released rows keep
+  the backbone).  x W is a float64 library matmul, the adapter term is oracle_delta
+  in double.  Pinned by brute force, W = 0 reducing to :func:`fused`, all rows
+  released reducing to the dense product, and merged == unmerged inference.
 * :func:`plan` -- active rows and the stable by-adapter grouping (Punica grouping by
   adapter identity; LoRazor page, active-row-aware kernels).  Pinned bit-exactly by
   an independent numpy construction in the tests.
@@ -61,13 +67,16 @@ def bind(path: str):
     lib.oracle_expand.argtypes = table + [P, I64, P, I64, P, I64, I, I]
     lib.oracle_fused.argtypes = table + [P, I64, P, I64, I, P, I64, I, I]
     lib.oracle_merge.argtypes = table + [I, I, P, I64, I, I, I]
+    lib.oracle_delta.argtypes = table + [P, I64, P, I64, I, P, I64, I, I]
+    lib.oracle_round_bf16.argtypes = [P, P, I64]
     lib.oracle_plan.argtypes = [P, I64, I, P, P, P, P, P, P]
     lib.oracle_plan.restype = I
     lib.oracle_bf16_round.argtypes = [ctypes.c_double]
     lib.oracle_bf16_round.restype = ctypes.c_uint16
     lib.oracle_bf16_value.argtypes = [ctypes.c_uint16]
     lib.oracle_bf16_value.restype = ctypes.c_double
-    for f in (lib.oracle_shrink, lib.oracle_expand, lib.oracle_fused, lib.oracle_merge):
+    for f in (lib.oracle_shrink, lib.oracle_expand, lib.oracle_fused, lib.oracle_merge,
+              lib.oracle_delta, lib.oracle_round_bf16):
         f.restype = None
     return lib
 
@@ -156,6 +165,41 @@ def fused_rows(table: Table, ids, x, y_in, rows, nthreads: int = 1) -> np.ndarra
     rows = np.asarray(rows, dtype=np.int64)
     return fused(table, np.asarray(ids)[rows], np.asarray(x)[rows],
                  np.asarray(y_in)[rows], nthreads)
+
+
+def delta(table: Table, ids, x, d_out: int, nthreads: int = 1) -> np.ndarray:
+    """s_k (x_i A_k) B_k per row in double (zeros for released rows), unrounded."""
+    lib = _load()
+    ids = _c(ids, np.int32)
+    x = _c(x, np.uint16)
+    n, d_in = x.shape
+    out = np.empty((n, d_out), np.float64)
+    lib.oracle_delta(*table.args(), _ptr(ids), n, _ptr(x), d_in, d_in, _ptr(out), d_out,
+                     d_out, nthreads)
+    return out
+
+
+def round_bf16(v) -> np.ndarray:
+    """Nearest bf16 (ties to even) of every element of a float64 array (uint16 bits)."""
+    v = _c(v, np.float64)
+    out = np.empty(v.shape, np.uint16)
+    _load().oracle_round_bf16(_ptr(v), _ptr(out), v.size)
+    return out
+
+
+def base_fused(table: Table, ids, x, W, nthreads: int = 1, rows=None) -> np.ndarray:
+    """y_i = bf16(x_i W + s_k (x_i A_k) B_k), y_i = bf16(x_i W) for ids[i] == -1 (the base
+    projection with the adapter term, one rounding).  x [n, d_in], W [d_in, d_out] bf16
+    bits; rows: optionally a subset of the rows (returns those rows)."""
+    x = np.asarray(x, dtype=np.uint16)
+    ids = np.asarray(ids, dtype=np.int32)
+    if rows is not None:
+        rows = np.asarray(rows, dtype=np.int64)
+        x, ids = x[rows], ids[rows]
+    W = np.asarray(W, dtype=np.uint16)
+    base = bf16_to_f64(x) @ bf16_to_f64(W)          # float64 library matmul
+    base += delta(table, ids, x, W.shape[1], nthreads)
+    return round_bf16(base)
 
 
 def merge(table: Table, adapter: int, W, sign: int = +1, nthreads: int = 1,

@@ -15,6 +15,13 @@
  *   merge   W <- W +/- s_k * A_k . B_k (VaLoRA blog, section 4.4.1: Delta W is computed
  *           at run time from the stored A and B and added to / subtracted from the
  *           base weight in one go; S-LoRA page, Batching, "formula 1").
+ *   base    y_i = x_i . W + s_k * (x_i . A_k) . B_k, and y_i = x_i . W for a released
+ *           row (S-LoRA page, Batching: the batched base model xW plus the separately
+ *           computed xAB, "formula 2"; VaLoRA blog, C2: unmerged inference computes
+ *           x.W and the adapter term; LoRazor page: released rows keep the backbone).
+ *           The oracle supplies the adapter term in double (oracle_delta) and the
+ *           rounding (oracle_round_bf16); the product x.W is a library matmul in
+ *           float64 on the Python side, and the two are added before the one rounding.
  *   plan    active rows, stable grouping of active rows by adapter id
  *           (Punica: requests grouped by adapter identity; LoRazor page: rows of
  *           released adapters take no part in the LoRA operator).
@@ -203,7 +210,34 @@ static void expand_row(void *p, int64_t i)
     }
 }
 
-/* ---- fused: both factors, v kept in double ----------------------------- */
+/* ---- the adapter term of one row, unscaled, in double:
+ *      term[o] = sum_j v_j * B_k[j, o],  v_j = sum_c x[c] * A_k[c, j]
+ *      (both sums in ascending index order).  Returns 0, or -1 if out of memory. */
+
+static int adapter_term(const table_t *t, int k, const uint16_t *x_row, int d_in, int d_out,
+                        double *term)
+{
+    int r = t->rank[k];
+    double *v = (double *)malloc(sizeof(double) * (size_t)(r > 0 ? r : 1));
+    if (!v)
+        return -1;
+    for (int j = 0; j < r; ++j) {
+        double acc = 0.0;
+        for (int64_t col = 0; col < d_in; ++col)
+            acc += bf16_to_double(x_row[col]) * A_at(t, k, col, j);
+        v[j] = acc;
+    }
+    for (int64_t o = 0; o < d_out; ++o) {
+        double acc = 0.0;
+        for (int j = 0; j < r; ++j)
+            acc += v[j] * B_at(t, k, j, o);
+        term[o] = acc;
+    }
+    free(v);
+    return 0;
+}
+
+/* ---- fused: y[i, o] = bf16(y[i, o] + s_k * term[o]) -------------------- */
 
 typedef struct {
     table_t t;
@@ -222,25 +256,46 @@ static void fused_row(void *p, int64_t i)
     int k = c->ids[i];
     if (k < 0)
         return;
-    int r = c->t.rank[k];
-    double s = (double)c->t.scale[k];
-    double *v = (double *)malloc(sizeof(double) * (size_t)(r > 0 ? r : 1));
-    if (!v)
+    const double s_fused = (double)c->t.scale[k];
+    double *term = (double *)malloc(sizeof(double) * (size_t)(c->d_out > 0 ? c->d_out : 1));
+    if (!term)
         return;
-    for (int j = 0; j < r; ++j) {
-        double acc = 0.0;
-        for (int64_t col = 0; col < c->d_in; ++col)
-            acc += bf16_to_double(c->x[i * c->ldx + col]) * A_at(&c->t, k, col, j);
-        v[j] = acc;
+    if (adapter_term(&c->t, k, &c->x[i * c->ldx], c->d_in, c->d_out, term) == 0)
+        for (int64_t o = 0; o < c->d_out; ++o) {
+            uint16_t *yo = &c->y[i * c->ldy + o];
+            *yo = double_to_bf16(bf16_to_double(*yo) + s_fused * term[o]);
+        }
+    free(term);
+}
+
+/* ---- delta in double: out[i, o] = s_k * term[o], 0 for a released row (the
+ *      adapter term of the base projection, unrounded) -------------------- */
+
+typedef struct {
+    table_t t;
+    const int32_t *ids;
+    const uint16_t *x;
+    int64_t ldx;
+    int d_in;
+    double *out;
+    int64_t ldo;
+    int d_out;
+} delta_ctx;
+
+static void delta_row(void *p, int64_t i)
+{
+    delta_ctx *c = (delta_ctx *)p;
+    double *dst = &c->out[i * c->ldo];
+    int k = c->ids[i];
+    if (k < 0) {
+        for (int64_t o = 0; o < c->d_out; ++o)
+            dst[o] = 0.0;
+        return;
     }
-    for (int64_t o = 0; o < c->d_out; ++o) {
-        double acc = 0.0;
-        for (int j = 0; j < r; ++j)
-            acc += v[j] * B_at(&c->t, k, j, o);
-        uint16_t *yo = &c->y[i * c->ldy + o];
-        *yo = double_to_bf16(bf16_to_double(*yo) + s * acc);
-    }
-    free(v);
+    const double s_delta = (double)c->t.scale[k];
+    if (adapter_term(&c->t, k, &c->x[i * c->ldx], c->d_in, c->d_out, dst) == 0)
+        for (int64_t o = 0; o < c->d_out; ++o)
+            dst[o] *= s_delta;
 }
 
 /* ---- merge: W[c, o] = bf16(W[c, o] + sign * s_k * sum_j A_k[c, j] B_k[j, o]) */
@@ -298,6 +353,21 @@ void oracle_fused(TABLE_ARGS, const int32_t *ids, int64_t n, const uint16_t *x,
 {
     fused_ctx c = {TABLE_INIT, ids, x, ldx, d_in, y, ldy, d_out};
     for_rows(n, nthreads, fused_row, &c);
+}
+
+/* out [n, ldo] doubles: the adapter term s_k (x_i A_k) B_k of each row, unrounded. */
+void oracle_delta(TABLE_ARGS, const int32_t *ids, int64_t n, const uint16_t *x,
+                  int64_t ldx, int d_in, double *out, int64_t ldo, int d_out, int nthreads)
+{
+    delta_ctx c = {TABLE_INIT, ids, x, ldx, d_in, out, ldo, d_out};
+    for_rows(n, nthreads, delta_row, &c);
+}
+
+/* out[q] = nearest bf16 (ties to even) of v[q], q < count. */
+void oracle_round_bf16(const double *v, uint16_t *out, int64_t count)
+{
+    for (int64_t q = 0; q < count; ++q)
+        out[q] = double_to_bf16(v[q]);
 }
 
 /* sign = +1 merges the adapter into W, -1 takes it out again. */

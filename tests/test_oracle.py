@@ -293,3 +293,65 @@ def test_plan_rejects_out_of_range_ids():
         oracle.plan(np.array([0, 5], np.int32), 3)
     with pytest.raises(ValueError):
         oracle.plan(np.array([-2], np.int32), 3)
+
+
+# ---------------------------------------------------------------- base projection + delta
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_base_fused_is_nearest_bf16_of_float64_brute_force(seed):
+    """x W + s (x A) B per row by numpy float64 matmuls on gathered matrices (x W alone
+    for released rows): the oracle's output is the nearest bf16 of it."""
+    c = workloads.small(seed=90 + seed, n=11, d_in=48, d_out=40, n_adapters=3,
+                        ranks=[8, 16, 24], paged=bool(seed % 2), release_frac=0.25)
+    W = workloads.make_W(48, 40, seed=seed)
+    y = oracle.base_fused(oracle.Table.from_case(c), c["ids"], c["x"], W)
+    exact = f64(c["x"]) @ f64(W) + exact_delta(c)
+    assert_nearest_bf16(y, exact, slack=1e-6)
+
+
+def test_base_fused_closed_form_one_hot_adapter():
+    """x = [1, 2]; W = [[0.5, 1], [1, -1]] so x W = [2.5, -1]; a rank-8 adapter whose
+    A column 0 is e_1 (v_0 = x_1 = 2) and B row 0 is [1, 0.25], all else zero, s = 2:
+    the adapter term is 2 * 2 * [1, 0.25] = [4, 1], so y = [6.5, 0] exactly; a released
+    row gets x W alone."""
+    bf = lambda a: to_bf16_bits(np.asarray(a, np.float32))
+    a_pool = np.zeros((8, 2), np.uint16)
+    a_pool[0] = bf([0.0, 1.0])
+    b_pool = np.zeros((8, 2), np.uint16)
+    b_pool[0] = bf([1.0, 0.25])
+    pages = np.arange(8, dtype=np.int32).reshape(1, 8)
+    t = oracle.Table(a_pool, b_pool, np.array([8], np.int32), np.array([2.0], np.float32),
+                     pages, pages)
+    x = bf([[1.0, 2.0], [1.0, 2.0]])
+    W = bf([[0.5, 1.0], [1.0, -1.0]])
+    y = oracle.base_fused(t, np.array([0, -1], np.int32), x, W)
+    np.testing.assert_array_equal(f64(y), [[6.5, 0.0], [2.5, -1.0]])
+
+
+def test_base_fused_with_zero_base_is_the_delta_alone():
+    """W = 0: the base projection vanishes and the result is bit for bit the fused
+    delta on y_in = 0 (both round s (x A) B once)."""
+    c = workloads.small(seed=95, n=13, d_in=64, d_out=48, n_adapters=4, ranks=[8, 16, 32, 8],
+                        paged=True, release_frac=0.2, y_mode="zero")
+    t = oracle.Table.from_case(c)
+    y = oracle.base_fused(t, c["ids"], c["x"], np.zeros((64, 48), np.uint16))
+    np.testing.assert_array_equal(y, oracle.fused(t, c["ids"], c["x"], c["y"]))
+
+
+def test_base_fused_with_every_row_released_is_the_dense_product():
+    c = workloads.small(seed=96, n=9, d_in=56, d_out=32, n_adapters=2, ranks=[8, 8])
+    W = workloads.make_W(56, 32, seed=3)
+    y = oracle.base_fused(oracle.Table.from_case(c), np.full(9, -1, np.int32), c["x"], W)
+    assert_nearest_bf16(y, f64(c["x"]) @ f64(W), slack=1e-6)
+
+
+def test_base_fused_equals_merged_inference():
+    """Unmerged x W + s (x A) B against merged x (W + s A B) (VaLoRA blog, section 4.4:
+    the two modes compute the same layer)."""
+    c = workloads.small(seed=97, n=24, d_in=96, d_out=80, n_adapters=2, ranks=[16, 8],
+                        ids=np.ones(24, np.int32))
+    W = workloads.make_W(96, 80, seed=4)
+    t = oracle.Table.from_case(c)
+    y = oracle.base_fused(t, c["ids"], c["x"], W)
+    merged = f64(c["x"]) @ f64(oracle.merge(t, 1, W, +1))
+    assert_parity(y, to_bf16_bits(merged.astype(np.float32)), 5e-3, 2e-2, "merged vs unmerged")

@@ -13,22 +13,23 @@ from tests._helpers import adapter_mats, exact_delta, f64, parity_values
 SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
 
 MUTANTS = {
-    "expand_sign": ("*yo = double_to_bf16(bf16_to_double(*yo) + s * acc);\n    }\n    free(v);",
-                    "*yo = double_to_bf16(bf16_to_double(*yo) - s * acc);\n    }\n    free(v);"),
-    "dropped_last_input_term": (
-        "for (int64_t col = 0; col < c->d_in; ++col)\n            acc += bf16_to_double(c->x[i * c->ldx + col]) * A_at(&c->t, k, col, j);\n        v[j] = acc;",
-        "for (int64_t col = 0; col < c->d_in - 1; ++col)\n            acc += bf16_to_double(c->x[i * c->ldx + col]) * A_at(&c->t, k, col, j);\n        v[j] = acc;"),
-    "dropped_last_rank_term": ("acc += v[j] * B_at(&c->t, k, j, o);",
-                               "if (j < r - 1) acc += v[j] * B_at(&c->t, k, j, o);"),
-    "transposed_B_index": ("acc += v[j] * B_at(&c->t, k, j, o);",
-                           "acc += v[j] * B_at(&c->t, k, (int)(o % r), (int64_t)j);"),
+    "fused_sign": ("bf16_to_double(*yo) + s_fused * term[o]", "bf16_to_double(*yo) - s_fused * term[o]"),
+    "dropped_last_input_term": ("for (int64_t col = 0; col < d_in; ++col)",
+                                "for (int64_t col = 0; col < d_in - 1; ++col)"),
+    "dropped_last_rank_term": ("acc += v[j] * B_at(t, k, j, o);",
+                               "if (j < r - 1) acc += v[j] * B_at(t, k, j, o);"),
+    "transposed_B_index": ("acc += v[j] * B_at(t, k, j, o);",
+                           "acc += v[j] * B_at(t, k, (int)(o % r), (int64_t)j);"),
     "truncating_round": ("double units = rint(ldexp(a, -q));",
                          "double units = floor(ldexp(a, -q));"),
     "merge_ignores_sign": ("(sign < 0 ? -1.0 : 1.0)", "(sign < 0 ? 1.0 : 1.0)"),
     "unstable_grouping": ("int32_t row = active_rows[q];\n        perm",
                           "int32_t row = active_rows[na - 1 - q];\n        perm"),
-    "scale_dropped": ("double s = (double)c->t.scale[k];\n    double *v",
-                      "double s = 1.0;\n    double *v"),
+    "scale_dropped": ("const double s_fused = (double)c->t.scale[k];",
+                      "const double s_fused = 1.0;"),
+    "base_delta_scale_dropped": ("dst[o] *= s_delta;", "dst[o] *= 1.0;"),
+    "base_delta_on_released_rows": ("            dst[o] = 0.0;\n        return;",
+                                    "            dst[o] = 1.0;\n        return;"),
 }
 
 
@@ -56,6 +57,10 @@ def _pins_hold() -> bool:
             if r2 > 5e-3:
                 return False
         if oracle.bf16_round(1 + 3 * 2 ** -8) != 0x3F82 or oracle.bf16_round(1.9999) != 0x4000:
+            return False
+        yb = oracle.base_fused(t, c["ids"], c["x"], W[:40, :32])
+        rb, _ = parity_values(f64(yb), f64(c["x"]) @ f64(W[:40, :32]) + exact_delta(c))
+        if rb > 5e-3:
             return False
         ids = np.array([2, 0, 2, -1, 0, 1, 2], np.int32)
         if oracle.plan(ids, 3)["perm"].tolist() != [1, 4, 5, 0, 2, 6]:
