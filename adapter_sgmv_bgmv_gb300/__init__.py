@@ -28,7 +28,7 @@ OPT_TILE_PATH, OPT_MERGE_KERNEL, OPT_TILE_MIN_RUN, OPT_EARLY_PAGES, OPT_DEVICE_P
 ERROR_NAMES = {0: "LORA_OK", -1: "LORA_E_INVAL", -2: "LORA_E_RANK", -3: "LORA_E_ADAPTER",
                -4: "LORA_E_NOT_RESIDENT", -5: "LORA_E_PAGE", -6: "LORA_E_CUDA",
                -7: "LORA_E_TIMEOUT", -8: "LORA_E_NOMEM", -9: "LORA_E_CAPACITY",
-               -10: "LORA_E_UNSUPPORTED", -11: "LORA_E_IO"}
+               -10: "LORA_E_UNSUPPORTED", -11: "LORA_E_IO", -12: "LORA_E_NOTUNED"}
 
 _L = _lib.load()
 
@@ -133,6 +133,19 @@ class Context:
 
     def tiles_count(self) -> int:
         return int(_L.lora_tiles_count(self.handle))
+
+    def tile_status(self) -> str:
+        """"LORA_OK" if the last call found all its launch shapes in the tile table,
+        "LORA_E_NOTUNED" if it took a built-in default for one of them."""
+        return ERROR_NAMES[int(_L.lora_tile_status(self.handle))]
+
+    def tune(self, shapes_path: str, out_path: str | None = None, stream=None):
+        """lora_tune: the offline search over a shape file (see include/lora.h); the
+        winners go into this context's table, and to out_path if given."""
+        _check(_L.lora_tune(self.handle, shapes_path.encode(),
+                            out_path.encode() if out_path else None,
+                            _stream(stream, self.device) if self.device is not None else None),
+               self)
 
     def sync_status(self, stream=None) -> int:
         """Synchronize and read back the device status word (raises on a timeout)."""
@@ -286,9 +299,10 @@ def lora_fused_device_ids(ctx: Context, table: AdapterTable, ids: torch.Tensor, 
 
 def lora_fused_noalloc(ctx: Context, table: AdapterTable, ids, x: torch.Tensor, y: torch.Tensor,
                        stream=None):
-    """lora_fused for callers that must not allocate while it runs: scratch is a fixed
-    4 MB device array inside the library; raises LORA_E_CAPACITY beyond its limits
-    (see include/lora.h)."""
+    """lora_fused for callers that must not allocate while it runs: its scratch is
+    fixed device arrays inside the library (12 MB: 4 MB of partial V and 8 MB of
+    dense adapter rows, committed when a context is created); raises
+    LORA_E_CAPACITY beyond their limits (see include/lora.h)."""
     ids, pid, n = _ids(ids)
     px, ldx, d_in = _rows(x, "x")
     py, ldy, d_out = _rows(y, "y")
@@ -315,6 +329,13 @@ class PreparedFused:
                       ctypes.c_void_p(py), ctypes.c_int64(ldy), ctypes.c_int(d_out),
                       ctypes.c_void_p(_stream(stream, ctx.device)))
         self._last = None          # (ids object, its argument tuple)
+
+    def bind(self, ids):
+        """Convert and keep the arguments for this ids array without launching, so
+        that the first call with it costs no more than the later ones."""
+        arr, pid, n = _ids(ids)
+        if arr is ids:
+            self._last = (ids, self._head + (ctypes.c_void_p(pid), ctypes.c_int64(n)) + self._tail)
 
     def __call__(self, ids):
         last = self._last

@@ -43,6 +43,8 @@ SIGNATURES = {
     "lora_tiles_load": ([P, ctypes.c_char_p], I),
     "lora_tiles_save": ([P, ctypes.c_char_p], I),
     "lora_tiles_count": ([P], I64),
+    "lora_tile_status": ([P], I),
+    "lora_tune": ([P, ctypes.c_char_p, ctypes.c_char_p, P], I),
     "lora_tune_shape": ([P, P, I, P, I64, P, I64, I, P, I64, I, I, ctypes.POINTER(F), P], I),
     "lora_sync_status": ([P, P], I),
     "lora_last_path": ([P, ctypes.POINTER(I)], I),

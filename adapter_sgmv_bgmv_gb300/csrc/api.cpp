@@ -4,6 +4,9 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cctype>
+#include <cmath>
+#include <cstdlib>
 #include <cstdio>
 #include <cstring>
 #include <memory>
@@ -57,6 +60,7 @@ struct lora_ctx {
     char cuda_err[256] = {0};
     int last_path = 0;
     int last_launches = 0;
+    bool untuned = false;           // the last call took a built-in default launch shape
     // Per-launch CUDA-event timing (lora_profile_begin / lora_profile_end).
     struct ProfEv {
         cudaEvent_t a = nullptr, b = nullptr;
@@ -144,6 +148,7 @@ int use_device(lora_ctx *ctx)
 // before on this stream may be a page-in, which writes the pools.
 void begin_call(lora_ctx *ctx, cudaStream_t stream)
 {
+    ctx->untuned = false;
     ctx->call_early = ctx->early_pages && !(ctx->pool_write_pending && ctx->pool_write_stream == stream);
 }
 
@@ -311,10 +316,14 @@ bool stride_ok(const void *p, int64_t ld, int d)
     return p && aligned16(p) && d > 0 && (d % 8) == 0 && ld >= d && (ld % 8) == 0;
 }
 
+// *hit: whether the shape came from the table (or a forced tuning candidate) rather
+// than the built-in default.
 RowsCfg choose_rows_cfg(const lora_ctx *ctx, int mode, int kind, int64_t n_act, int64_t n_seg,
-                        int d_in, int d_out, int rank)
+                        int d_in, int d_out, int rank, bool *hit = nullptr)
 {
     RowsCfg cfg = default_rows_cfg(mode, n_act, n_seg, d_in, d_out, rank);
+    if (hit)
+        *hit = true;
     if (ctx->force_cluster > 0 && ctx->force_rows > 0)
         return RowsCfg{ctx->force_cluster, ctx->force_rows};
     TileCfg tc;
@@ -322,6 +331,8 @@ RowsCfg choose_rows_cfg(const lora_ctx *ctx, int mode, int kind, int64_t n_act, 
         tc[0] >= 1 && tc[0] <= 16 && (tc[0] & (tc[0] - 1)) == 0 && tc[1] >= 1 && tc[1] <= 64) {
         cfg.cluster = tc[0];
         cfg.rows = tc[1];
+    } else if (hit) {
+        *hit = false;
     }
     return cfg;
 }
@@ -403,13 +414,18 @@ int run_rows(lora_ctx *ctx, const lora_table *t, int mode, RowsCfg cfg, const vo
 
 // Minimum run of consecutive same-adapter rows that goes to the tensor-core tile
 // kernels (shorter runs use the row-gather kernel); 0 disables the tile path.
-int tile_min_run(const lora_ctx *ctx, int64_t n_act, int d_in, int d_out, int rank)
+int tile_min_run(const lora_ctx *ctx, int64_t n_act, int d_in, int d_out, int rank,
+                 bool *hit = nullptr)
 {
+    if (hit)
+        *hit = true;
     if (ctx->tile_min_run_override > 0)
         return ctx->tile_min_run_override;
     TileCfg tc;
     if (ctx->tiles.lookup(TileKey{kKindTileFused, pow2_bucket(n_act), 0, d_in, d_out, rank}, tc))
         return tc[0];
+    if (hit)
+        *hit = false;
     return 128;
 }
 
@@ -688,17 +704,21 @@ int delta_call(lora_ctx *ctx, const lora_table *t, int mode, const int32_t *ids,
     for (int32_t k : pl.seg_adapter)
         rmax = std::max(rmax, t->rank[size_t(k)]);
     const int64_t n_act = int64_t(pl.active.size());
+    bool hit_tiles = true, hit_rows = true;
     const int min_run = (ctx->tile_path && tile_tc_supported(d_in, d_out, rmax))
-                            ? tile_min_run(ctx, n_act, d_in, d_out, rmax)
+                            ? tile_min_run(ctx, n_act, d_in, d_out, rmax, &hit_tiles)
                             : 0;
     // Rows-kernel shape from the rows that stay on it (approximated by all rows when
     // the tile path is off).
     RowsCfg cfg = choose_rows_cfg(ctx, mode, kind, n_act, int64_t(pl.seg_adapter.size()), d_in,
-                                  d_out, rmax);
+                                  d_out, rmax, &hit_rows);
     plan_items(pl, t->rank.data(), t->scale.data(), cfg.rows, min_run);
     if (!pl.tile_items.empty() && pl.row_active > 0 && pl.row_active < n_act)
         cfg = choose_rows_cfg(ctx, mode, kind, pl.row_active, int64_t(pl.row_items.size()), d_in,
-                              d_out, pl.row_max_rank);
+                              d_out, pl.row_max_rank, &hit_rows);
+    // The minimum run is a tuned decision only where a run could reach a tile (the
+    // search's shortest candidate is 32 rows).
+    ctx->untuned = (!hit_tiles && pl.max_seg_len >= 32) || (!pl.row_items.empty() && !hit_rows);
     rc = run_tiles(ctx, t, mode, x, ldx, d_in, v, ldv, y, ldy, d_out, n, stream);
     if (rc != LORA_OK)
         return rc;
@@ -740,9 +760,12 @@ int merge_call(lora_ctx *ctx, const lora_table *t, int adapter, void *W, int64_t
     p.scale = sign * t->scale[size_t(adapter)];
     int path = ctx->merge_path;
     TileCfg tcfg;
-    if (path == 0 && ctx->tiles.lookup(TileKey{kKindMerge, pow2_bucket(d_in), 0, d_in, d_out, p.rank},
-                                       tcfg))
-        path = tcfg[0];
+    if (path == 0) {
+        if (ctx->tiles.lookup(TileKey{kKindMerge, pow2_bucket(d_in), 0, d_in, d_out, p.rank}, tcfg))
+            path = tcfg[0];
+        else
+            ctx->untuned = true;
+    }
     const bool tc = merge_tc_supported(d_in, d_out, p.rank) && path != 1;
     RowMats mats;
     if (tc) {
@@ -790,9 +813,10 @@ const char *lora_strerror(int code)
     case LORA_E_CUDA: return "CUDA runtime error";
     case LORA_E_TIMEOUT: return "a bounded device-side wait expired";
     case LORA_E_NOMEM: return "allocation failed";
-    case LORA_E_CAPACITY: return "more rows than the context was created for";
+    case LORA_E_CAPACITY: return "batch beyond the context's max_rows or a fixed scratch limit";
     case LORA_E_UNSUPPORTED: return "shape not supported by the kernels";
-    case LORA_E_IO: return "tile-table file could not be read or written";
+    case LORA_E_IO: return "tile-table or shape file could not be read or written";
+    case LORA_E_NOTUNED: return "information: a built-in default launch shape was used";
     default: return "unknown status";
     }
 }
@@ -855,6 +879,13 @@ int lora_ctx_create(int device, int64_t max_rows, int max_rank, lora_ctx **out)
             cudaSetDevice(prev);
             return LORA_E_CUDA;
         }
+    }
+    // lora_fused_noalloc's fixed scratch: loading the module that holds it commits
+    // its memory here, so that no lora_fused_noalloc call is the one that does.
+    if (noalloc_scratch(device, true, nullptr) != cudaSuccess) {
+        lora_ctx_destroy(ctx);
+        cudaSetDevice(prev);
+        return LORA_E_CUDA;
     }
     cudaSetDevice(prev);
     *out = ctx;
@@ -1095,11 +1126,12 @@ int lora_fused_noalloc(lora_ctx *ctx, const lora_table *t, const int32_t *ids, i
     for (int32_t k : pl.seg_adapter)
         rmax = std::max(rmax, t->rank[size_t(k)]);
     const int64_t n_act = int64_t(pl.active.size());
+    bool hit_tiles = true, hit_rows = true;
     const int min_run = (ctx->tile_path && tile_tc_supported(d_in, d_out, rmax))
-                            ? tile_min_run(ctx, n_act, d_in, d_out, rmax)
+                            ? tile_min_run(ctx, n_act, d_in, d_out, rmax, &hit_tiles)
                             : 0;
     RowsCfg cfg = choose_rows_cfg(ctx, kFused, kKindRowsFused, n_act,
-                                  int64_t(pl.seg_adapter.size()), d_in, d_out, rmax);
+                                  int64_t(pl.seg_adapter.size()), d_in, d_out, rmax, &hit_rows);
     plan_items(pl, t->rank.data(), t->scale.data(), cfg.rows, min_run);
     // Everything must fit the fixed arrays and the launch parameter block.
     if (pl.tile_items.size() > size_t(kNoAllocSlots) ||
@@ -1107,10 +1139,12 @@ int lora_fused_noalloc(lora_ctx *ctx, const lora_table *t, const int32_t *ids, i
         return LORA_E_CAPACITY;
     if (!pl.tile_items.empty() && pl.row_active > 0 && pl.row_active < n_act)
         cfg = choose_rows_cfg(ctx, kFused, kKindRowsFused, pl.row_active,
-                              int64_t(pl.row_items.size()), d_in, d_out, pl.row_max_rank);
+                              int64_t(pl.row_items.size()), d_in, d_out, pl.row_max_rank, &hit_rows);
+    // The minimum run is a tuned decision only where a run could reach a tile (the
+    // search's shortest candidate is 32 rows).
+    ctx->untuned = (!hit_tiles && pl.max_seg_len >= 32) || (!pl.row_items.empty() && !hit_rows);
     NoAllocScratch fixed{};
-    if (noalloc_scratch(ctx->device, &fixed) != 0)
-        return LORA_E_CUDA;
+    CUDA_TRY(ctx, noalloc_scratch(ctx->device, false, &fixed));
     const bool prof = ctx->prof;
     ctx->prof = false;   // the event pool could grow
     rc = run_tiles(ctx, t, kFused, x, ldx, d_in, nullptr, 0, y, ldy, d_out, n, stream, &fixed);
@@ -1148,7 +1182,10 @@ int lora_fused_device_ids(lora_ctx *ctx, const lora_table *t, const int32_t *ids
     // clusters leave as soon as they read the plan's count (planned mode) or their
     // row's id (direct mode: one row per cluster, no plan kernel).
     const int64_t n_seg = std::min<int64_t>(n, t->n_adapters);
-    RowsCfg cfg = choose_rows_cfg(ctx, kFused, kKindRowsFused, n, n_seg, d_in, d_out, t->rank_max_ok);
+    bool hit_rows = true;
+    RowsCfg cfg = choose_rows_cfg(ctx, kFused, kKindRowsFused, n, n_seg, d_in, d_out, t->rank_max_ok,
+                                  &hit_rows);
+    ctx->untuned = !hit_rows;
     if (!ctx->device_plan)
         cfg.rows = 1;
     RowsParams p{};
@@ -1313,6 +1350,13 @@ int lora_tiles_save(const lora_ctx *ctx, const char *path)
 }
 
 int64_t lora_tiles_count(const lora_ctx *ctx) { return ctx ? int64_t(ctx->tiles.map.size()) : -1; }
+
+int lora_tile_status(const lora_ctx *ctx)
+{
+    if (!ctx)
+        return LORA_E_INVAL;
+    return ctx->untuned ? LORA_E_NOTUNED : LORA_OK;
+}
 
 int lora_sync_status(lora_ctx *ctx, void *stream)
 {
@@ -1537,6 +1581,274 @@ int lora_tune_shape(lora_ctx *ctx, const lora_table *t, int kind, const int32_t 
     ctx->tiles.put(key, best_cfg);
     *best_us = best;
     return LORA_OK;
+}
+
+}  // extern "C"
+
+namespace {
+
+// ---------------------------------------------------------------- lora_tune: shape file
+
+struct TuneShape {
+    int kind = 0;             // kKindRowsFused, kKindTileFused or kKindMerge
+    int64_t n = 1;
+    int d_in = 0, d_out = 0, rank = 0, adapters = 1;
+    int64_t run = 0;          // rows per request; 0: ids cycle over the adapters
+    bool throughput = false;
+    std::string text;
+};
+
+// One shape per line: kind n d_in d_out rank adapters [run [objective]], kind one of
+// rows / tiles / merge, objective latency (default) or throughput (rows only); '#'
+// starts a comment.  Checked in full before anything runs.
+int parse_shapes(const char *path, int max_rank, std::vector<TuneShape> &out)
+{
+    std::FILE *f = std::fopen(path, "r");
+    if (!f)
+        return LORA_E_IO;
+    char buf[512];
+    int rc = LORA_OK;
+    while (rc == LORA_OK && std::fgets(buf, sizeof buf, f)) {
+        std::string line(buf);
+        const size_t hash = line.find('#');
+        if (hash != std::string::npos)
+            line.resize(hash);
+        std::vector<std::string> tok;
+        size_t i = 0;
+        while (i < line.size()) {
+            while (i < line.size() && std::isspace(static_cast<unsigned char>(line[i])))
+                ++i;
+            size_t j = i;
+            while (j < line.size() && !std::isspace(static_cast<unsigned char>(line[j])))
+                ++j;
+            if (j > i)
+                tok.push_back(line.substr(i, j - i));
+            i = j;
+        }
+        if (tok.empty())
+            continue;
+        if (tok.size() < 6 || tok.size() > 8) {
+            rc = LORA_E_INVAL;
+            break;
+        }
+        TuneShape sh;
+        if (tok[0] == "rows")
+            sh.kind = kKindRowsFused;
+        else if (tok[0] == "tiles")
+            sh.kind = kKindTileFused;
+        else if (tok[0] == "merge")
+            sh.kind = kKindMerge;
+        else
+            rc = LORA_E_INVAL;
+        int64_t v[7] = {0, 0, 0, 0, 0, 0, 0};
+        for (size_t q = 1; q < std::min<size_t>(tok.size(), 7) && rc == LORA_OK; ++q) {
+            char *end = nullptr;
+            v[q] = std::strtoll(tok[q].c_str(), &end, 10);
+            if (!end || *end != '\0')
+                rc = LORA_E_INVAL;
+        }
+        if (rc != LORA_OK)
+            break;
+        sh.n = v[1];
+        sh.d_in = int(v[2]);
+        sh.d_out = int(v[3]);
+        sh.rank = int(v[4]);
+        sh.adapters = int(v[5]);
+        sh.run = tok.size() > 6 ? v[6] : 0;
+        if (tok.size() > 7) {
+            if (tok[7] == "throughput")
+                sh.throughput = true;
+            else if (tok[7] != "latency")
+                rc = LORA_E_INVAL;
+        }
+        if (sh.n < 1 || sh.n > (int64_t(1) << 24) || v[2] < 8 || v[2] > 65536 || (v[2] % 8) ||
+            v[3] < 8 || v[3] > 65536 || (v[3] % 8) || sh.rank < 8 || (sh.rank % 8) ||
+            sh.rank > max_rank || sh.adapters < 1 || sh.adapters > 4096 || sh.run < 0 ||
+            (sh.throughput && sh.kind != kKindRowsFused))
+            rc = LORA_E_INVAL;
+        sh.text = tok[0];
+        for (size_t q = 1; q < tok.size(); ++q)
+            sh.text += " " + tok[q];
+        out.push_back(sh);
+    }
+    std::fclose(f);
+    return rc;
+}
+
+// Device buffers of one tuning shape, freed when it goes out of scope.
+struct TuneBuffers {
+    std::vector<void *> mem;
+    std::vector<lora_table *> tables;
+    ~TuneBuffers()
+    {
+        for (lora_table *t : tables)
+            lora_table_destroy(t);
+        for (void *p : mem)
+            cudaFree(p);
+    }
+    uint16_t *alloc(size_t elems)
+    {
+        void *p = nullptr;
+        if (cudaMalloc(&p, elems * 2) != cudaSuccess)
+            return nullptr;
+        mem.push_back(p);
+        return static_cast<uint16_t *>(p);
+    }
+};
+
+// Run one shape of lora_tune on synthetic data: values uniform with the variances of
+// the workloads (x and W unit / 1/d_in, A 1/d_in, B 1/r), filled on the device.
+int tune_one(lora_ctx *ctx, const TuneShape &sh, int index, cudaStream_t stream, float *best_us)
+{
+    const int na = sh.adapters, r = sh.rank;
+    const bool merge = sh.kind == kKindMerge;
+    const int64_t n = merge ? 1 : sh.n;
+    std::vector<int32_t> rank(size_t(na), r), pages(size_t(na) * r);
+    std::vector<float> scale(size_t(na), 16.f / float(r));
+    for (size_t i = 0; i < pages.size(); ++i)
+        pages[i] = int32_t(i);
+    std::vector<int32_t> ids(static_cast<size_t>(n));
+    for (int64_t i = 0; i < n; ++i)
+        ids[size_t(i)] = int32_t((sh.run > 0 ? i / sh.run : i) % na);
+    const size_t pool_a = size_t(na) * r * size_t(sh.d_in), pool_b = size_t(na) * r * size_t(sh.d_out);
+    const size_t act = merge ? size_t(sh.d_in) * size_t(sh.d_out) : size_t(n) * (sh.d_in + sh.d_out);
+    int sets = 1;
+    if (sh.throughput)   // inputs over a pass larger than L2, as a decode loop meets them
+        sets = int(std::min<size_t>(64, std::max<size_t>(2, ((size_t(256) << 20) + 2 * (pool_a + pool_b + act) - 1) /
+                                                               (2 * (pool_a + pool_b + act)))));
+    TuneBuffers b;
+    std::vector<uint16_t *> xs, ys;
+    const uint64_t seed0 = uint64_t(index) * 1000003ull;
+    for (int s = 0; s < sets; ++s) {
+        uint16_t *a = b.alloc(pool_a), *bb = b.alloc(pool_b);
+        uint16_t *x = merge ? nullptr : b.alloc(size_t(n) * sh.d_in);
+        uint16_t *y = b.alloc(merge ? size_t(sh.d_in) * sh.d_out : size_t(n) * sh.d_out);
+        if (!a || !bb || (!merge && !x) || !y)
+            return LORA_E_NOMEM;
+        const uint64_t sd = seed0 + uint64_t(s) * 16;
+        CUDA_TRY(ctx, launch_fill_bf16(a, pool_a, sd + 1, std::sqrt(3.f / float(sh.d_in)), stream));
+        CUDA_TRY(ctx, launch_fill_bf16(bb, pool_b, sd + 2, std::sqrt(3.f / float(r)), stream));
+        if (x)
+            CUDA_TRY(ctx, launch_fill_bf16(x, size_t(n) * sh.d_in, sd + 3, std::sqrt(3.f), stream));
+        CUDA_TRY(ctx, launch_fill_bf16(y, merge ? size_t(sh.d_in) * sh.d_out : size_t(n) * sh.d_out, sd + 4,
+                                       merge ? std::sqrt(3.f / float(sh.d_in)) : std::sqrt(3.f), stream));
+        lora_table *t = nullptr;
+        int rc = lora_table_create(ctx, a, int64_t(na) * r, sh.d_in, bb, int64_t(na) * r, sh.d_out, na, r,
+                                   rank.data(), scale.data(), pages.data(), pages.data(), &t);
+        if (rc != LORA_OK)
+            return rc;
+        b.tables.push_back(t);
+        xs.push_back(x);
+        ys.push_back(y);
+    }
+    CUDA_TRY(ctx, cudaStreamSynchronize(stream));
+    if (!sh.throughput) {
+        if (merge)
+            return lora_tune_shape(ctx, b.tables[0], kKindMerge, ids.data(), 1, ys[0], sh.d_out,
+                                   sh.d_in, ys[0], sh.d_out, sh.d_out, 31, best_us, stream);
+        return lora_tune_shape(ctx, b.tables[0], sh.kind, ids.data(), n, xs[0], sh.d_in, sh.d_in, ys[0],
+                               sh.d_out, sh.d_out, 31, best_us, stream);
+    }
+    // Throughput of back-to-back calls over the rotating sets, per candidate launch
+    // shape of the row-gather kernel (the space lora_tune_shape searches).
+    int seg_max = 0;
+    {
+        std::vector<int> cnt(size_t(na), 0);
+        for (int32_t k : ids)
+            seg_max = std::max(seg_max, ++cnt[size_t(k)]);
+    }
+    cudaEvent_t e0, e1;
+    CUDA_TRY(ctx, cudaEventCreate(&e0));
+    if (cudaEventCreate(&e1) != cudaSuccess) {
+        cudaEventDestroy(e0);
+        return LORA_E_CUDA;
+    }
+    const int saved_tile = ctx->tile_path;
+    ctx->tile_path = 0;
+    constexpr int kSteps = 1500;
+    float best = -1.f;
+    TileCfg best_cfg{0, 0, 0, 0};
+    int rc = LORA_OK;
+    for (int C = 1; C <= rows_max_cluster() && rc == LORA_OK; C *= 2) {
+        if (C > 1 && std::min(sh.d_in, sh.d_out) / C < 64)
+            break;
+        for (int R = 1; R <= 16 && rc == LORA_OK; R *= 2) {
+            if (R > 1 && R / 2 >= seg_max)
+                break;
+            if (rows_smem_for(kFused, C, R, r, sh.d_in, sh.d_out) > size_t(rows_max_smem()))
+                continue;
+            ctx->force_cluster = C;
+            ctx->force_rows = R;
+            for (int i = 0; i < 20 && rc == LORA_OK; ++i)
+                rc = lora_fused(ctx, b.tables[size_t(i % sets)], ids.data(), n, xs[size_t(i % sets)], sh.d_in,
+                                sh.d_in, ys[size_t(i % sets)], sh.d_out, sh.d_out, stream);
+            if (rc == LORA_OK && cudaEventRecord(e0, stream) != cudaSuccess)
+                rc = LORA_E_CUDA;
+            for (int i = 0; i < kSteps && rc == LORA_OK; ++i)
+                rc = lora_fused(ctx, b.tables[size_t(i % sets)], ids.data(), n, xs[size_t(i % sets)], sh.d_in,
+                                sh.d_in, ys[size_t(i % sets)], sh.d_out, sh.d_out, stream);
+            if (rc == LORA_OK &&
+                (cudaEventRecord(e1, stream) != cudaSuccess || cudaEventSynchronize(e1) != cudaSuccess))
+                rc = LORA_E_CUDA;
+            float ms = 0.f;
+            if (rc == LORA_OK && cudaEventElapsedTime(&ms, e0, e1) == cudaSuccess) {
+                const float us = 1000.f * ms / float(kSteps);
+                if (best < 0.f || us < best) {
+                    best = us;
+                    best_cfg = TileCfg{C, R, 0, 0};
+                }
+            }
+        }
+    }
+    ctx->force_cluster = ctx->force_rows = 0;
+    ctx->tile_path = saved_tile;
+    cudaEventDestroy(e0);
+    cudaEventDestroy(e1);
+    if (rc != LORA_OK)
+        return rc;
+    if (best < 0.f)
+        return LORA_E_UNSUPPORTED;
+    ctx->tiles.put(TileKey{kKindRowsFused, pow2_bucket(n), pow2_bucket(std::min<int64_t>(na, n)), sh.d_in,
+                           sh.d_out, r},
+                   best_cfg);
+    *best_us = best;
+    return LORA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int lora_tune(lora_ctx *ctx, const char *shapes_path, const char *out_path, void *stream_ptr)
+{
+    if (!ctx || !shapes_path)
+        return LORA_E_INVAL;
+    std::vector<TuneShape> shapes;
+    int rc = parse_shapes(shapes_path, ctx->max_rank, shapes);
+    if (rc != LORA_OK)
+        return rc;
+    rc = use_device(ctx);
+    if (rc != LORA_OK)
+        return rc;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+    std::vector<float> best(shapes.size(), 0.f);
+    for (size_t i = 0; i < shapes.size(); ++i) {
+        rc = tune_one(ctx, shapes[i], int(i), stream, &best[i]);
+        if (rc != LORA_OK)
+            return rc;
+    }
+    if (!out_path)
+        return LORA_OK;
+    rc = ctx->tiles.save(out_path);
+    if (rc != LORA_OK)
+        return rc;
+    std::FILE *f = std::fopen(out_path, "a");
+    if (!f)
+        return LORA_E_IO;
+    for (size_t i = 0; i < shapes.size(); ++i)
+        std::fprintf(f, "# tuned: %s -> %.3f us (%s)\n", shapes[i].text.c_str(), double(best[i]),
+                     shapes[i].throughput ? "back-to-back calls" : "cold single call, median");
+    return std::fclose(f) == 0 ? LORA_OK : LORA_E_IO;
 }
 
 }  // extern "C"

@@ -146,7 +146,10 @@ struct NoAllocScratch {
     uint16_t *dense;          // kNoAllocDenseBytes of dense adapter rows
 };
 static_assert(kNoAllocSlots <= kInlineTiles, "a no-alloc tile list travels in the parameters");
-int noalloc_scratch(int device, NoAllocScratch *out);
+// Looks the addresses up on the first call for `device` (with it current) or when
+// `refresh` is set, and caches them; loading the module that holds the arrays is
+// what commits their memory.
+cudaError_t noalloc_scratch(int device, bool refresh, NoAllocScratch *out);
 
 // Dense adapter rows (dense.cu): for slot s and j < rp, row s*rp + j of dst gets
 // the first `width` elements of page j of the slot's adapter, zeros for j >= rank.
@@ -203,6 +206,11 @@ struct DevPlanArgs {
 size_t dev_plan_smem_bytes(int n_adapters);
 cudaError_t launch_wait_selftest(unsigned *status, uint64_t limit_ns, cudaStream_t stream);
 cudaError_t launch_plan_dev(const DevPlanArgs &a, cudaStream_t stream);
+
+// Offline search (fill.cu): n bf16 values uniform in [-scale, scale) from a hash of
+// (seed, index).
+cudaError_t launch_fill_bf16(uint16_t *dst, uint64_t n, uint64_t seed, float scale,
+                             cudaStream_t stream);
 
 cudaError_t launch_shrink_tc(const TileParams &p, cudaStream_t stream);
 cudaError_t launch_expand_tc(const TileParams &p, cudaStream_t stream);

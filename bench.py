@@ -1,20 +1,30 @@
 #!/usr/bin/env python3
 """Throughput of the heterogeneous multi-LoRA delta on one GB300 (or N replicas).
 
-Default workload: the Llama-7B-shaped decode batch (64 single-token requests,
-d_in = d_out = 4096, rank 16); one step = one lora_fused call on the heterogeneous
-batch (64 distinct adapters) plus one on the homogeneous batch (all rows on one
-adapter), 128 tokens.  Inputs rotate over enough copies that one pass over them is
-several times the 129 MB L2, so every step reads cold HBM.
+Default workload (the line's headline): the VaLoRA-style vision prefill, the
+largest configuration -- Qwen-VL-7B MLP up-projection 4096 -> 11008, 16 requests x
+(1024 visual + 32 text) tokens, 4 rank-64 adapters with Zipf(1.2) popularity; one
+step = one lora_fused call over the 16,896 tokens.  Inputs rotate over enough
+device copies that one pass over them is several times the 129 MB L2, so every
+step reads cold HBM.
 
-Prints one JSON line (rank 0).  `--impl reference` times the CPU oracle instead,
-on a bounded sample of the same workload.  `--all` prints one line per workload.
+The same JSON line carries `per_config`: every other workload measured in the same
+run (tiny decode, the Llama-7B decode pair, S-LoRA prefill, the VaLoRA merge +
+unmerge, the LoRazor active-row decode with its microseconds-vs-active-rows curve),
+each with device and host microseconds per call, tokens/s, the dominant kernel's
+fraction of its roofline, the end-to-end rate and the oracle's rate on the host.
+
+`--impl reference` times the CPU oracle instead, on a bounded sample of the same
+workload.  `--all` prints one line per workload.  `--config NAME` makes NAME the
+headline.
 """
 from __future__ import annotations
 
 import argparse
 import ctypes
+import ctypes.util
 import glob
+import hashlib
 import json
 import math
 import os
@@ -36,10 +46,49 @@ METRIC = ("multi-LoRA delta tokens/s and µs/call; % of HBM (decode) / TC (prefi
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
-DEFAULT_CONFIG = "llama7b_decode"
-CONFIGS = ("llama7b_decode", "tiny_decode", "slora_prefill", "valora_prefill", "valora_merge",
+DEFAULT_CONFIG = "valora_prefill"
+CONFIGS = ("valora_prefill", "llama7b_decode", "tiny_decode", "slora_prefill", "valora_merge",
            "lorazor_decode")
 DEVICE_IDS_CONFIGS = ("llama7b_decode", "tiny_decode", "lorazor_decode")
+# Steps of a per_config entry (a fixed count, independent of --steps, sized so that
+# each timed region is a few tens to a few hundred milliseconds).
+PER_CONFIG_STEPS = {"llama7b_decode": 10000, "tiny_decode": 20000, "lorazor_decode": 10000,
+                    "slora_prefill": 2000, "valora_prefill": 500, "valora_merge": 1000}
+WORKLOAD_DESC = {
+    "valora_prefill": ("Qwen-VL-7B MLP up-proj 4096->11008, 16 requests x (1024 visual + 32 "
+                       "text) tokens = 16896, 4 rank-64 adapters (Zipf 1.2), contiguous storage"),
+    "llama7b_decode": ("Llama-7B projection 4096x4096, 64 requests x 1 token, rank 16; per step "
+                       "one call with 64 distinct adapters (heterogeneous) + one call with all "
+                       "rows on one adapter (homogeneous)"),
+    "tiny_decode": "d=256, 16 requests x 1 token, 4 rank-8 adapters, contiguous storage",
+    "slora_prefill": ("S-LoRA prefill 4096x4096, 8 requests with log-normal lengths (5353 "
+                      "tokens), ranks in {8,16,32,64}, 8 of 1000 adapters resident in shuffled "
+                      "4096-wide pages"),
+    "valora_merge": "merge then unmerge of a rank-64 adapter into W 4096x11008 bf16",
+    "lorazor_decode": ("70B projection 8192x8192, 256 requests x 1 token, 512 resident rank-16 "
+                       "adapters (Zipf 1.0) in shuffled 8192-wide pages; step t releases 128+t "
+                       "rows (t = 0..99, cycled)"),
+}
+# Source files of each kernel family: a DRAM-traffic figure measured by ncu holds only
+# while their contents are those it was measured on.
+FAMILY_SOURCES = {
+    "rows": ["rows.cu", "ptx.cuh"],
+    "shrink": ["tile_tc.cu", "dense.cu", "tc.cuh"],
+    "expand": ["stream_tc.cu", "tc.cuh"],
+    "merge": ["stream_tc.cu", "tc.cuh"],
+}
+KERNEL_NAMES = {"rows": "k_rows_inline<fused>", "shrink": "k_shrink_tc (+ k_stage_rows)",
+                "expand": "k_stream_tc(expand)", "merge": "k_stream_tc(merge)"}
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+
+
+def config_for(name: str, early_pages: bool = True, device_ids: bool = False) -> dict:
+    """The line's `config` (the same dict for both arms: a function of the workload)."""
+    return {"workload": WORKLOAD_DESC[name], "name": name,
+            "l2": "inputs rotate over device copies; one pass touches more than 3 x the "
+                  "129 MB L2 (no flush needed)",
+            "parallelism": "single GPU (replicas under torchrun)",
+            "early_pages": bool(early_pages), "device_ids": bool(device_ids)}
 
 
 # --------------------------------------------------------------------------- peaks
@@ -59,70 +108,158 @@ def peaks():
                 "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 
 
+def source_sha(family: str) -> str:
+    h = hashlib.sha256()
+    for f in FAMILY_SOURCES.get(family, []):
+        with open(os.path.join(ROOT, "adapter_sgmv_bgmv_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(name: str, family: str):
+    """DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) of this
+    workload's kernel family from the ncu figures kept in the traffic file, or None
+    when there is none or the kernel's sources changed since it was measured."""
+    try:
+        with open(TRAFFIC_FILE) as fh:
+            for line in fh:
+                f = line.split("#", 1)[0].split()
+                if len(f) >= 4 and f[0] == name and f[1] == family:
+                    return float(f[2]) if f[3] == source_sha(family) else None
+    except OSError:
+        pass
+    return None
+
+
 # --------------------------------------------------------------------------- clocks
 
 class ClockSampler:
-    """nvidia-smi samples of this GPU's clocks and throttle reasons every 200 ms."""
+    """SM clock, its maximum, power and the clock-event (throttle) reasons of this
+    GPU, read through NVML in this process every half millisecond while sampling is
+    on, so that even a timed region of a few milliseconds has samples; falls back to
+    nvidia-smi at 200 ms when NVML cannot be loaded."""
 
-    FIELDS = ("index,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
 
-    def __init__(self, uuid: str | None):
-        self.uuid = uuid
-        self.rows = []
+    def __init__(self, torch, index: int):
+        self.rows = []                # (t, sm_mhz, max_mhz, reasons bitmask, power W)
+        self.lib = self.dev = None
+        self.on = threading.Event()
+        self.stop_ev = threading.Event()
         self.proc = None
-        self.thread = None
-
-    def start(self):
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                raise OSError("nvmlInit")
+            dev = ctypes.c_void_p()
+            uuid = str(torch.cuda.get_device_properties(index).uuid)
+            if not uuid.startswith("GPU-"):
+                uuid = "GPU-" + uuid
+            if lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(dev)) != 0:
+                cnt = ctypes.c_uint()
+                if lib.nvmlDeviceGetCount_v2(ctypes.byref(cnt)) != 0 or cnt.value != 1 or \
+                        lib.nvmlDeviceGetHandleByIndex_v2(0, ctypes.byref(dev)) != 0:
+                    raise OSError("no NVML handle for this GPU")
+            self.reason_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                lib.nvmlDeviceGetCurrentClocksThrottleReasons
+            self.lib, self.dev = lib, dev
+            self.max_mhz = self._clock(lib.nvmlDeviceGetMaxClockInfo)
         except Exception:
-            self.proc = None
-            return
-        self.thread = threading.Thread(target=self._read, daemon=True)
+            self.lib = None
+        self.thread = threading.Thread(target=self._run, daemon=True)
         self.thread.start()
 
-    def _read(self):
-        for line in self.proc.stdout:
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) >= 10:
-                self.rows.append((time.time(), parts))
+    def _clock(self, fn):
+        v = ctypes.c_uint()
+        return v.value if fn(self.dev, 1, ctypes.byref(v)) == 0 else None   # 1: SM clock
 
-    def stop(self):
+    def _sample(self):
+        sm = self._clock(self.lib.nvmlDeviceGetClockInfo)
+        r = ctypes.c_ulonglong()
+        reasons = r.value if self.reason_fn(self.dev, ctypes.byref(r)) == 0 else 0
+        p = ctypes.c_uint()
+        power = p.value / 1000.0 if self.lib.nvmlDeviceGetPowerUsage(self.dev, ctypes.byref(p)) == 0 else None
+        self.rows.append((time.perf_counter(), sm, self.max_mhz, reasons, power))
+
+    def _run(self):
+        if self.lib is None:
+            self._run_smi()
+            return
+        while not self.stop_ev.is_set():
+            if self.on.wait(0.05):
+                self._sample()
+                time.sleep(0.0005)
+
+    def _run_smi(self):
+        q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+             "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+             "clocks_event_reasons.sw_power_cap")
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            return
+        bits = (0x8, 0x40, 0x20, 0x4)
+        for line in self.proc.stdout:
+            p = [x.strip() for x in line.split(",")]
+            if len(p) < 7:
+                continue
+            try:
+                mask = sum(b for b, v in zip(bits, p[3:7]) if v.lower().startswith("active"))
+                self.rows.append((time.perf_counter(), float(p[0]), float(p[1]), mask,
+                                  float(p[2]) if p[2].replace(".", "", 1).isdigit() else None))
+            except ValueError:
+                continue
+
+    def start(self):
+        """Begin sampling: one sample now (in this thread, so that even a region
+        shorter than the thread's first turn has one), then every half millisecond."""
+        if self.lib is not None:
+            self._sample()
+        self.on.set()
+
+    def pause(self):
+        """Stop sampling, with one last sample taken now, at the region's end."""
+        self.on.clear()
+        if self.lib is not None:
+            self._sample()
+
+    def close(self):
+        self.stop_ev.set()
+        self.on.set()
         if self.proc is not None:
             self.proc.terminate()
-            try:
-                self.proc.wait(timeout=5)
-            except Exception:
-                self.proc.kill()
-        if self.thread is not None:
-            self.thread.join(timeout=5)
+        self.thread.join(timeout=5)
 
-    def summary(self, t0: float, t1: float):
-        rows = [p for (t, p) in self.rows if (self.uuid is None or p[1] == self.uuid)]
-        window = [p for (t, p) in self.rows if t0 <= t <= t1 and (self.uuid is None or p[1] == self.uuid)]
-        use = window or rows
-        if not use:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+    def summary(self, t0: float, t1: float) -> dict:
+        win = [r for r in self.rows if t0 <= r[0] <= t1]
+        src = "nvml" if self.lib is not None else "nvidia-smi"
+        if not win:
+            # a region shorter than the sampling period: the samples nearest to it
+            near = sorted(self.rows, key=lambda r: min(abs(r[0] - t0), abs(r[0] - t1)))[:4]
+            if not near:
+                return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"],
+                        "samples": 0, "source": src}
+            out = self._stats(near)
+            out.update(in_timed_window=False, source=src)
+            return out
+        out = self._stats(win)
+        out.update(in_timed_window=True, source=src)
+        return out
 
-        def num(x):
-            try:
-                return float(x)
-            except ValueError:
-                return None
-        sm = [num(p[2]) for p in use if num(p[2]) is not None]
-        mx = [num(p[3]) for p in use if num(p[3]) is not None]
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for p in use for i in range(4) if p[6 + i].lower().startswith("active")})
+    def _stats(self, rows):
+        sm = [r[1] for r in rows if r[1] is not None]
+        mx = [r[2] for r in rows if r[2] is not None]
+        pw = [r[4] for r in rows if r[4] is not None]
+        reasons = sorted({name for r in rows for bit, name in self.REASONS.items() if r[3] & bit})
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
-                "samples": len(use), "in_timed_window": bool(window)}
+                "samples": len(rows), "power_w_max": max(pw) if pw else None}
 
 
-# --------------------------------------------------------------------------- workloads
+# --------------------------------------------------------------------------- algorithmic bytes
 
 def alg_bytes_delta(case, ids):
     """Algorithmic bytes of one fused call: x read, y read + write, the A and B pages
@@ -134,17 +271,6 @@ def alg_bytes_delta(case, ids):
     distinct = np.unique(act)
     ab = int(sum(2 * int(case["rank"][k]) * (d_in + d_out) for k in distinct))
     return 2 * n_act * d_in + 4 * n_act * d_out + ab + 4 * n_act + 16 * len(distinct)
-
-
-# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) of the
-# dominant kernel family, from the ncu captures summarised in profiles/ (taken on
-# the kernels as they are now; a change to one of these kernels voids its entry).
-# Configurations without a capture report null.
-MEASURED_TRAFFIC = {
-    ("llama7b_decode", "rows"): (17.88e6 + 1.36e6) / 2,   # profiles/rows_llama7b_decode.md
-    ("valora_prefill", "expand"): 725.71e6,                # profiles/stream_tile_valora_prefill.md
-    ("valora_merge", "merge"): 123.08e6,                   # profiles/stream_merge_valora.md
-}
 
 
 def alg_bytes_split(case, ids, tiles: bool) -> dict:
@@ -170,6 +296,8 @@ def flops_delta(case, ids):
     return int(sum(2 * int(case["rank"][k]) * (case["d_in"] + case["d_out"]) for k in act))
 
 
+# --------------------------------------------------------------------------- workload on the device
+
 class Bench:
     """Device-resident rotating copies of one workload and the per-step calls."""
 
@@ -180,41 +308,26 @@ class Bench:
         # decode through lora_fused_device_ids: every set holds its steps' ids in
         # device memory (the end-to-end loop copies them in with the step's inputs)
         self.device_ids = device_ids
-        self.calls = []          # list of (case_key, ids) per step, for delta workloads
         if name == "llama7b_decode":
             het = workloads.make("llama7b_decode_het", seed=0)
             hom = workloads.make("llama7b_decode_hom", seed=0)
             self.cases = {"het": het, "hom": hom}
             self.steps_ids = [[("het", het["ids"]), ("hom", hom["ids"])]]
-            self.workload = ("Llama-7B projection 4096x4096, 64 requests x 1 token, rank 16, "
-                             "bf16; per step one call with 64 distinct adapters (heterogeneous) "
-                             "+ one call with all rows on one adapter (homogeneous)")
         elif name == "lorazor_decode":
             c = workloads.make("lorazor_decode", seed=0)
             self.cases = {"main": c}
             self.steps_ids = [[("main", workloads.lorazor_ids(c, t))] for t in range(100)]
-            self.workload = ("70B projection 8192x8192, 256 requests x 1 token, 512 resident "
-                             "rank-16 adapters (Zipf 1.0) in shuffled 8192-wide pages; step t "
-                             "releases 128+t rows (t = 0..99, cycled)")
         elif name in ("tiny_decode", "slora_prefill", "valora_prefill"):
             c = workloads.make(name, seed=0)
             self.cases = {"main": c}
             self.steps_ids = [[("main", c["ids"])]]
-            self.workload = {
-                "tiny_decode": "d=256, 16 requests x 1 token, 4 rank-8 adapters",
-                "slora_prefill": ("S-LoRA prefill 4096x4096, 8 requests with log-normal "
-                                  "lengths (%d tokens), ranks in {8,16,32,64}, 8 of 1000 "
-                                  "adapters resident in shuffled 4096-wide pages" % c["n"]),
-                "valora_prefill": ("Qwen-VL-7B MLP up-proj 4096->11008, 16 requests x "
-                                   "(1024 visual + 32 text) tokens, 4 rank-64 adapters, Zipf 1.2"),
-            }[name]
         elif name == "valora_merge":
             c = workloads.make("valora_merge", seed=0)
             self.cases = {"main": c}
             self.steps_ids = None
-            self.workload = "merge then unmerge of a rank-64 adapter into W 4096x11008 bf16"
         else:
             raise KeyError(name)
+        self.workload = WORKLOAD_DESC[name]
         self.is_merge = name == "valora_merge"
         self._upload()
 
@@ -223,10 +336,7 @@ class Bench:
         if self.is_merge:
             c = self.cases["main"]
             return 2 * c["d_in"] * c["d_out"]
-        tot = 0
-        for key, ids in self.steps_ids[0]:
-            tot += alg_bytes_delta(self.cases[key], ids)
-        return tot
+        return sum(alg_bytes_delta(self.cases[key], ids) for key, ids in self.steps_ids[0])
 
     def _upload(self):
         torch, L = self.torch, self.L
@@ -287,6 +397,13 @@ class Bench:
                             np.ascontiguousarray(ids, np.int32)).cuda()
             st["_blk"] = blk
             self.sets.append(st)
+        # every set's call holds its arguments before the first step, so that no
+        # first call (argument conversion) falls inside a timed region
+        if not self.is_merge and not self.device_ids:
+            for st in self.sets:
+                for calls in self.steps_ids[:1]:
+                    for key, ids in calls:
+                        st[key]["call"].bind(ids)
         torch.cuda.synchronize()
 
     # ---- one step
@@ -303,6 +420,12 @@ class Bench:
         for key, ids in self.steps_ids[t]:
             self._call(st, t, key, ids, stream)
 
+    def step_on(self, set_idx: int, t: int, stream):
+        """The calls of step t (its ids) on device set set_idx."""
+        st = self.sets[set_idx % self.n_sets]
+        for key, ids in self.steps_ids[t]:
+            self._call(st, t, key, ids, stream)
+
     def _call(self, st, t, key, ids, stream):
         if self.device_ids:
             d = st[key]
@@ -310,6 +433,22 @@ class Bench:
                                          stream)
         else:
             st[key]["call"](ids)
+
+    def one_call(self, i: int, key: str, stream):
+        """One library call of step i's case `key` (merge: the merge alone)."""
+        st = self.sets[i % self.n_sets]
+        if self.is_merge:
+            d = st["main"]
+            self.L.lora_merge(self.ctx, d["table"], self.cases["main"]["merge_adapter"], d["W"],
+                              stream)
+            return
+        t = i % len(self.steps_ids)
+        for k, ids in self.steps_ids[t]:
+            if k == key:
+                self._call(st, t, k, ids, stream)
+
+    def call_keys(self):
+        return ["merge"] if self.is_merge else [k for k, _ in self.steps_ids[0]]
 
     def tokens_per_step(self, i: int) -> int:
         if self.is_merge:
@@ -448,6 +587,11 @@ class Bench:
             if self.used[k]:
                 _rt_check(self.rt.cudaStreamWaitEvent(*self.e2e_ops[k]["drain"]))
 
+    def release(self):
+        self.sets = []
+        self.torch.cuda.synchronize()
+        self.torch.cuda.empty_cache()
+
 
 class _RuntimeFns:
     pass
@@ -462,7 +606,6 @@ def _runtime():
     global _RT
     if _RT is not None:
         return _RT
-    import ctypes.util
     cands = ["/usr/local/cuda/lib64/libcudart.so", ctypes.util.find_library("cudart")]
     cands += sorted(glob.glob(os.path.join(os.path.dirname(np.__file__), "..", "nvidia", "*", "lib",
                                            "libcudart.so*")))
@@ -532,6 +675,249 @@ def oracle_sample(name: str, budget_s: float, nthreads: int):
     return done_tok, dt, f"{done_tok} active rows of the workload's calls, {chunk}-row chunks"
 
 
+# --------------------------------------------------------------------------- measurement
+
+def _events(torch):
+    return torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+
+def measure(name, K, W, args, L, torch, ctx, dist, world, local, clocks, cpu_budget,
+            extras: bool):
+    """Time K steps of one workload (after W warm-up steps) and gather the figures of
+    its JSON entry.  extras: repeats, single-call latencies, the LoRazor curve."""
+    b = Bench(name, L, torch, ctx, device_ids=args.device_ids)
+    stream = torch.cuda.current_stream()
+    for i in range(W):
+        b.step(i, stream)
+    b.learn_paths(stream)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    ev0, ev1 = _events(torch)
+    n_launch0 = ctx.launch_count()
+    t_s0 = time.perf_counter()
+    clocks.start()
+    t0 = time.perf_counter()
+    ev0.record(stream)
+    for i in range(K):
+        b.step(W + i, stream)
+    t_enq = time.perf_counter()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.perf_counter()
+    clocks.pause()
+    t_s1 = time.perf_counter()
+    n_launched = ctx.launch_count() - n_launch0
+    ms = ev0.elapsed_time(ev1)
+    calls = K * b.calls_per_step()
+    host_enqueue_us = 1e6 * (t_enq - t0) / max(1, calls)
+    clk = clocks.summary(t_s0, t_s1)   # the region and the samples at its two edges
+    # The per-family split comes from a second pass over the same steps with the
+    # profiler on, outside the timed region: a bracketed launch loses its overlap
+    # with its neighbours, which would otherwise slow the timed steps themselves.
+    ctx.profile_begin(args.profile_every)
+    for i in range(K):
+        b.step(W + i, stream)
+    torch.cuda.synchronize()
+    prof = ctx.profile_end()
+    tokens_local = sum(b.tokens_per_step(W + i) for i in range(K))
+    ms, tokens_all, _ = aggregate_ranks(ms, tokens_local, dist, "cuda")
+    pk = peaks()
+    # Per kernel family: launches, device time, algorithmic bytes it moves and the
+    # rate.  The profiling pass brackets one launch in `profile_every` per family
+    # with events; a bracket costs the launch its overlap with its neighbours (they
+    # are launched as programmatic dependents), so the bracketed times serve only to
+    # split the timed region's device time between the families.  A family's
+    # average launch duration is its share of the region divided by its launches
+    # (for a one-family workload: region time / launches).  Every kernel of the
+    # path is HBM-bound; the roofline line is that of the family with the most time.
+    fam_bytes = {}
+    for i in range(K):
+        for f, v in b.alg_bytes_family(W + i).items():
+            fam_bytes[f] = fam_bytes.get(f, 0) + v
+    bracketed = sum(m for (m, n) in prof.values() if n)
+    per_family = {}
+    for f, (m, n) in prof.items():
+        if n and m > 0:
+            share_s = (ms / 1e3) * (m / bracketed)
+            gbs = fam_bytes.get(f, 0) / share_s / 1e9
+            per_family[f] = {"kernel": KERNEL_NAMES[f], "launches": n,
+                             "us_per_launch": round(1e6 * share_s / n, 3),
+                             "us_per_launch_bracketed": round(1e3 * m / n, 3),
+                             "alg_bytes_per_launch": fam_bytes.get(f, 0) / n,
+                             "GB/s": round(gbs, 1), "frac": round(gbs / pk["hbm_gbs"], 4),
+                             "traffic": None if b.device_ids else measured_traffic(name, f)}
+    dominant = max(per_family, key=lambda f: prof[f][0])
+    achieved = per_family[dominant]["GB/s"]
+    flops_total = sum(b.flops_step(W + i) for i in range(K))
+    sec = ms / 1e3
+    if b.is_merge:
+        value, unit = 2 * K * world / sec, "merge+unmerge calls/s"
+    else:
+        value, unit = tokens_all / sec, "tokens/s"
+    out = {
+        "value": value, "unit": unit, "steps": K, "warmup": W, "ms_per_step": ms / K,
+        "us_per_call": {"device": 1e6 * sec / max(1, calls),
+                        "host_enqueue": round(host_enqueue_us, 3),
+                        "per_kernel_launch": {f: v["us_per_launch"] for f, v in per_family.items()}},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / pk["hbm_gbs"] if achieved else None,
+                     "traffic": per_family[dominant]["traffic"],
+                     "peak_source": pk["source"] + " (MEASURED_PEAKS.json hbm_gbs, STREAM-style copy)"
+                     if pk["source"] == "measured" else "fallback 6.8 TB/s",
+                     "kernel": KERNEL_NAMES[dominant],
+                     "bytes_per_launch": per_family[dominant]["alg_bytes_per_launch"],
+                     "us_per_launch": per_family[dominant]["us_per_launch"],
+                     "per_family": per_family,
+                     "tflops": flops_total / max(1e-12, sec) / 1e12},
+        "gpu_launches": n_launched,
+        "clocks": clk,
+        "l2_sets": b.n_sets,
+    }
+    if extras:
+        out["us_per_call"].update(per_call_stats(b, K, W, torch, ctx, stream))
+        if name == "lorazor_decode":
+            out["n_act_curve"] = lorazor_curve(b, torch, stream)
+    out["e2e"] = end_to_end(b, K, world, torch, stream)
+    if cpu_budget > 0 and world == 1 and not args.no_cpu:
+        nthreads = args.cpu_threads or os.cpu_count() or 1
+        done, dt, desc = oracle_sample(name, cpu_budget, nthreads)
+        out["cpu_baseline"] = {"value": done / dt * (2 if b.is_merge else 1), "unit": unit,
+                               "cores": nthreads, "kind": "oracle",
+                               "sample": desc + f", {dt:.1f} s"}
+    b.release()
+    return out
+
+
+def per_call_stats(b, K, W, torch, ctx, stream) -> dict:
+    """Median over five repeats of the K-step region (device µs per call), and per
+    call of a step: its device time alone after an L2 flush (CUDA events, median of
+    20) and its host time (call plus a stream synchronize, inputs already on the
+    device, plan and its upload included; median of 20)."""
+    reps = []
+    for _ in range(5):
+        e0, e1 = _events(torch)
+        e0.record(stream)
+        for i in range(K):
+            b.step(W + i, stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        reps.append(1e3 * e0.elapsed_time(e1) / (K * b.calls_per_step()))
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    single, host = {}, {}
+    for key in b.call_keys():
+        dev_us, host_us = [], []
+        for r in range(20):
+            flush.zero_()
+            e0, e1 = _events(torch)
+            e0.record(stream)
+            b.one_call(r, key, stream)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            dev_us.append(1e3 * e0.elapsed_time(e1))
+            flush.zero_()
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            b.one_call(r, key, stream)
+            stream.synchronize()
+            host_us.append(1e6 * (time.perf_counter() - t0))
+        single[key] = round(statistics.median(dev_us), 3)
+        host[key] = round(statistics.median(host_us), 3)
+    del flush
+    return {"device_median_of_5_repeats": round(statistics.median(reps), 3),
+            "single_call_cold_device": single, "single_call_host": host}
+
+
+def lorazor_curve(b, torch, stream) -> dict:
+    """Device µs of each of the 100 decode steps (20 back-to-back calls of that
+    step's ids over the rotating sets, after 3 untimed ones) against its active rows,
+    and the least-squares line through them: the time should follow the active rows
+    (the grid covers them alone), not the batch size."""
+    pts = []
+    for t in range(100):
+        for r in range(3):
+            b.step_on(r, t, stream)
+        e0, e1 = _events(torch)
+        e0.record(stream)
+        for r in range(20):
+            b.step_on(3 + r, t, stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        n_act = int((np.asarray(b.steps_ids[t][0][1]) >= 0).sum())
+        pts.append((n_act, 1e3 * e0.elapsed_time(e1) / 20))
+    x = np.array([p[0] for p in pts], np.float64)
+    y = np.array([p[1] for p in pts], np.float64)
+    slope, icpt = np.polyfit(x, y, 1)
+    fit = slope * x + icpt
+    r2 = 1.0 - float(np.sum((y - fit) ** 2) / max(1e-30, np.sum((y - y.mean()) ** 2)))
+    return {"points_n_act_us": [[int(a), round(float(u), 3)] for a, u in pts],
+            "slope_us_per_active_row": float(slope), "intercept_us": float(icpt), "r2": r2,
+            "us_at_n_act_128": float(slope * 128 + icpt), "us_at_n_act_29": float(slope * 29 + icpt),
+            "batch_rows": 256}
+
+
+def end_to_end(b, K, world, torch, stream) -> dict:
+    b.e2e_setup()
+    Ke = min(K, 2000)
+    for i in range(3):
+        b.e2e_step(i, stream)
+    torch.cuda.synchronize()
+    e0, e1 = _events(torch)
+    e0.record(b.s_in)            # the first thing of the timed region is a copy in
+    stream.wait_event(e0)
+    b.s_out.wait_event(e0)
+    h2d = d2h = 0
+    for i in range(Ke):
+        h2d, d2h = b.e2e_step(i, stream)
+    b.e2e_drain(stream)          # ... and the last is a read back
+    e1.record(stream)
+    torch.cuda.synchronize()
+    es = e0.elapsed_time(e1) / 1e3
+    if b.is_merge:
+        val, unit = 2 * Ke * world / es, "merge+unmerge calls/s"
+    else:
+        val, unit = sum(b.tokens_per_step(i) for i in range(Ke)) * world / es, "tokens/s"
+    return {"value": val, "unit": unit, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "steps": Ke}
+
+
+def aggregate_ranks(ms: float, tokens: int, dist, device):
+    """Replicas only: every rank times its own copy of the workload; the job's time is
+    the slowest rank's and its throughput is the sum of all ranks' units over that
+    time.  Returns (max ms, total units, world size)."""
+    if dist is None or not dist.is_initialized():
+        return ms, tokens, 1
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    u = torch.tensor([float(tokens)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), int(u.item()), dist.get_world_size()
+
+
+def default_steps(name):
+    return PER_CONFIG_STEPS[name]
+
+
+def headline_line(name, m, args, world):
+    line = {"metric": METRIC, "value": m["value"], "unit": m["unit"], "n_gpus": world,
+            "steps": m["steps"], "warmup": m["warmup"], "ms_per_step": m["ms_per_step"],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": config_for(name, not args.no_early_pages, args.device_ids)}
+    for k in ("us_per_call", "roofline", "gpu_launches", "clocks", "e2e", "cpu_baseline",
+              "l2_sets", "n_act_curve"):
+        if k in m:
+            line[k] = m[k]
+    return line
+
+
+def entry(name, m, args):
+    e = {"config": config_for(name, not args.no_early_pages, args.device_ids)}
+    e.update({k: v for k, v in m.items()})
+    return e
+
+
 # --------------------------------------------------------------------------- main
 
 def main():
@@ -542,8 +928,12 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default=DEFAULT_CONFIG, choices=CONFIGS)
     ap.add_argument("--all", action="store_true", help="one line per workload")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="the headline workload alone (no per_config entries)")
     ap.add_argument("--cpu-budget", type=float, default=12.0,
-                    help="seconds of oracle time for the cpu_baseline")
+                    help="seconds of oracle time for the headline's cpu_baseline")
+    ap.add_argument("--cpu-budget-per-config", type=float, default=3.0,
+                    help="seconds of oracle time for each per_config cpu_baseline")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-threads", type=int, default=0,
                     help="host threads for the oracle (0: every core)")
@@ -578,180 +968,41 @@ def main():
     # Every kernel the timed loop launches is this library's, none of which writes
     # the adapter pools: the row-gather kernel may copy pages before its wait.
     ctx.set_option(L.OPT_EARLY_PAGES, 0 if args.no_early_pages else 1)
-    names = list(CONFIGS) if args.all else [args.config]
-    if args.device_ids:
-        names = [n for n in names if n in DEVICE_IDS_CONFIGS]
-    for name in names:
-        line = run_one(name, args, L, torch, ctx, dist, world, rank, local)
+    clocks = ClockSampler(torch, local)
+    W = max(3, args.warmup)
+    if args.all:
+        names = [n for n in CONFIGS if not args.device_ids or n in DEVICE_IDS_CONFIGS]
+        for name in names:
+            K = args.steps if args.steps is not None else default_steps(name)
+            m = measure(name, K, W, args, L, torch, ctx, dist, world, local, clocks,
+                        args.cpu_budget, extras=True)
+            if rank == 0:
+                print(json.dumps(headline_line(name, m, args, world)), flush=True)
+    else:
+        name = args.config
+        if args.device_ids and name not in DEVICE_IDS_CONFIGS:
+            name = "llama7b_decode"
+        K = args.steps if args.steps is not None else default_steps(name)
+        m = measure(name, K, W, args, L, torch, ctx, dist, world, local, clocks,
+                    args.cpu_budget, extras=True)
+        line = headline_line(name, m, args, world)
+        if world == 1 and not args.no_per_config:
+            per = {}
+            others = [n for n in CONFIGS if n != name and
+                      (not args.device_ids or n in DEVICE_IDS_CONFIGS)]
+            for other in others:
+                mo = measure(other, PER_CONFIG_STEPS[other], W, args, L, torch, ctx, None, 1,
+                             local, clocks, args.cpu_budget_per_config, extras=True)
+                per[other] = entry(other, mo, args)
+            line["per_config"] = per
         if rank == 0:
             print(json.dumps(line), flush=True)
+    clocks.close()
     ctx.close()
     if dist is not None:
         dist.barrier()
         dist.destroy_process_group()
     return 0
-
-
-def aggregate_ranks(ms: float, tokens: int, dist, device):
-    """Replicas only: every rank times its own copy of the workload; the job's time is
-    the slowest rank's and its throughput is the sum of all ranks' units over that
-    time.  Returns (max ms, total units, world size)."""
-    if dist is None or not dist.is_initialized():
-        return ms, tokens, 1
-    import torch
-    t = torch.tensor([ms], dtype=torch.float64, device=device)
-    u = torch.tensor([float(tokens)], dtype=torch.float64, device=device)
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    dist.all_reduce(u, op=dist.ReduceOp.SUM)
-    return float(t.item()), int(u.item()), dist.get_world_size()
-
-
-def default_steps(name):
-    return {"llama7b_decode": 20000, "tiny_decode": 20000, "lorazor_decode": 10000,
-            "slora_prefill": 2000, "valora_prefill": 500, "valora_merge": 1000}[name]
-
-
-def run_one(name, args, L, torch, ctx, dist, world, rank, local):
-    K = args.steps if args.steps is not None else default_steps(name)
-    W = max(3, args.warmup)
-    b = Bench(name, L, torch, ctx, device_ids=args.device_ids)
-    stream = torch.cuda.current_stream()
-    uuid = None
-    try:
-        uuid = str(torch.cuda.get_device_properties(local).uuid)
-        if not uuid.startswith("GPU-"):
-            uuid = "GPU-" + uuid
-    except Exception:
-        uuid = None
-    clocks = ClockSampler(uuid)
-    clocks.start()
-    for i in range(W):
-        b.step(i, stream)
-    b.learn_paths(stream)
-    torch.cuda.synchronize()
-    if dist is not None:
-        dist.barrier()
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
-    n_launch0 = ctx.launch_count()
-    t_wall0 = time.time()
-    ev0.record(stream)
-    for i in range(K):
-        b.step(W + i, stream)
-    ev1.record(stream)
-    torch.cuda.synchronize()
-    t_wall1 = time.time()
-    n_launched = ctx.launch_count() - n_launch0
-    ms = ev0.elapsed_time(ev1)
-    # The per-family split comes from a second pass over the same steps with the
-    # profiler on, outside the timed region: a bracketed launch loses its overlap
-    # with its neighbours, which would otherwise slow the timed steps themselves.
-    ctx.profile_begin(args.profile_every)
-    for i in range(K):
-        b.step(W + i, stream)
-    torch.cuda.synchronize()
-    prof = ctx.profile_end()
-    tokens_local = sum(b.tokens_per_step(W + i) for i in range(K))
-    ms, tokens_all, _ = aggregate_ranks(ms, tokens_local, dist, "cuda")
-    if dist is not None:
-        dist.barrier()
-    clocks.stop()
-    clk = clocks.summary(t_wall0, t_wall1)
-
-    flops_total = sum(b.flops_step(W + i) for i in range(K))
-    pk = peaks()
-    # Per kernel family: launches, device time, algorithmic bytes it moves and the
-    # rate.  The profiling pass brackets one launch in `profile_every` per family
-    # with events; a bracket costs the launch its overlap with its neighbours (they
-    # are launched as programmatic dependents), so the bracketed times serve only to
-    # split the timed region's device time between the families.  A family's
-    # average launch duration is its share of the region divided by its launches
-    # (for a one-family workload: region time / launches).  Every kernel of the
-    # path is HBM-bound; the roofline line is that of the family with the most time.
-    fam_bytes = {}
-    for i in range(K):
-        for f, v in b.alg_bytes_family(W + i).items():
-            fam_bytes[f] = fam_bytes.get(f, 0) + v
-    bracketed = sum(m for (m, n) in prof.values() if n)
-    per_family = {}
-    for f, (m, n) in prof.items():
-        if n and m > 0:
-            share_s = (ms / 1e3) * (m / bracketed)
-            gbs = fam_bytes.get(f, 0) / share_s / 1e9
-            per_family[f] = {"launches": n, "us_per_launch": round(1e6 * share_s / n, 3),
-                             "us_per_launch_bracketed": round(1e3 * m / n, 3),
-                             "alg_bytes_per_launch": fam_bytes.get(f, 0) / n,
-                             "GB/s": round(gbs, 1), "frac": round(gbs / pk["hbm_gbs"], 4)}
-    per_kernel = {f: v["us_per_launch"] for f, v in per_family.items()}
-    kernel_names = {"rows": "k_rows<fused> (device ids)" if b.device_ids else "k_rows_inline<fused>",
-                    "shrink": "k_shrink_tc",
-                    "expand": "k_stream_tc(expand)", "merge": "k_stream_tc(merge)"}
-    dominant = max(per_family, key=lambda f: prof[f][0])
-    achieved_gbs = per_family[dominant]["GB/s"]
-    sec = ms / 1e3
-    if b.is_merge:
-        value = 2 * K * world / sec
-        unit = "merge+unmerge calls/s"
-    else:
-        value = tokens_all / sec
-        unit = "tokens/s"
-    line = {
-        "metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": K,
-        "warmup": W, "ms_per_step": ms / K, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": b.workload, "name": name,
-                   "l2": f"inputs rotate over {b.n_sets} device copies "
-                         f"({b.n_sets * b._unique_bytes_per_step() / 1e6:.0f} MB touched per pass "
-                         f"> 129 MB L2)",
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "early_pages": not args.no_early_pages, "device_ids": b.device_ids},
-        "us_per_call": {"device": 1e6 * sec / max(1, K * b.calls_per_step()),
-                        "per_kernel_launch": per_kernel},
-        "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": pk["hbm_gbs"],
-                     "unit": "GB/s",
-                     "frac": (achieved_gbs / pk["hbm_gbs"]) if achieved_gbs else None,
-                     "traffic": None if b.device_ids else MEASURED_TRAFFIC.get((name, dominant)),
-                     "peak_source": pk["source"],
-                     "kernel": kernel_names[dominant],
-                     "bytes_per_launch": per_family[dominant]["alg_bytes_per_launch"],
-                     "us_per_launch": per_family[dominant]["us_per_launch"],
-                     "per_family": per_family,
-                     "tflops": flops_total / max(1e-12, ms / 1e3) / 1e12},
-        "gpu_launches": n_launched,
-        "clocks": clk,
-    }
-    # end to end through pinned host buffers
-    b.e2e_setup()
-    Ke = min(K, 2000)
-    for i in range(3):
-        b.e2e_step(i, stream)
-    torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(b.s_in)            # the first thing of the timed region is a copy in
-    stream.wait_event(e0)
-    b.s_out.wait_event(e0)
-    h2d = d2h = 0
-    for i in range(Ke):
-        hb, db = b.e2e_step(i, stream)
-        h2d, d2h = hb, db
-    b.e2e_drain(stream)          # ... and the last is a read back
-    e1.record(stream)
-    torch.cuda.synchronize()
-    es = e0.elapsed_time(e1) / 1e3
-    if b.is_merge:
-        e2e_val = 2 * Ke * world / es
-    else:
-        e2e_val = sum(b.tokens_per_step(i) for i in range(Ke)) * world / es
-    line["e2e"] = {"value": e2e_val, "unit": unit, "h2d_bytes_per_step": h2d,
-                   "d2h_bytes_per_step": d2h}
-    if rank == 0 and world == 1 and not args.no_cpu:
-        nthreads = args.cpu_threads or os.cpu_count() or 1
-        done, dt, desc = oracle_sample(name, args.cpu_budget, nthreads)
-        line["cpu_baseline"] = {"value": done / dt * (2 if b.is_merge else 1),
-                                "unit": unit, "cores": nthreads, "kind": "oracle",
-                                "sample": desc + f", {dt:.1f} s"}
-    return line
 
 
 def run_reference(args):
@@ -776,7 +1027,7 @@ def run_reference(args):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": unit, "n_gpus": 1,
             "steps": K, "warmup": W, "ms_per_step": 1e3 * tot / K, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": name, "name": name, "parallelism": "host cores"},
+            "config": config_for(name, not args.no_early_pages, args.device_ids),
             "cpu_baseline": {"value": value, "unit": unit, "cores": nthreads, "kind": "oracle",
                              "sample": f"each step: about {per_step:.2f} s of the oracle on "
                                        f"the workload's rows ({desc.split(',')[0]} in the last)"},

@@ -65,7 +65,11 @@ enum {
     LORA_E_NOMEM = -8,        /* host or device allocation inside the library failed*/
     LORA_E_CAPACITY = -9,     /* n exceeds the context's max_rows                   */
     LORA_E_UNSUPPORTED = -10, /* shape beyond what the kernels handle, or not sm_103 */
-    LORA_E_IO = -11           /* tile-table file could not be read or written       */
+    LORA_E_IO = -11,          /* tile-table or shape file could not be read/written */
+    LORA_E_NOTUNED = -12      /* information only, never returned by a call that
+                                 computes: lora_tile_status() reports it when the last
+                                 call took a built-in default launch shape because the
+                                 tile table had no entry for its shape             */
 };
 
 typedef struct lora_ctx lora_ctx;
@@ -148,7 +152,8 @@ int lora_fused(lora_ctx *ctx, const lora_table *table, const int32_t *ids_host,
  * lora_fused (within the same tolerance; the two may pick different summation
  * orders), for callers that must not allocate device or pinned memory while they
  * run: code paths that forbid cudaMalloc / cudaFree, or that run inside a
- * pre-sized memory budget.  There is no counterpart of this entry point on the
+ * pre-sized memory budget, such as an allocator hook or a graph-building step that
+ * must not grow the device footprint.  There is no counterpart of this entry point on the
  * pages.  The context and the table are created beforehand (those calls do
  * allocate); this call then only launches kernels.  Its tensor-core scratch is
  * fixed file-scope device arrays that every GPU loading the library holds until
@@ -158,11 +163,13 @@ int lora_fused(lora_ctx *ctx, const lora_table *table, const int32_t *ids_host,
  * d_out) bf16).  Limits (else LORA_E_CAPACITY, nothing launched): at most 64
  * tiles of up to 128 consecutive same-adapter rows, those 8 MB, at most 256
  * row-gather work items and 512 active rows outside those tiles, n <= the
- * context's max_rows.  The first call on a device looks up
- * the array's device address (a runtime call, no allocation) and should come
- * before any stream capture.  Every call shares the array: calls that overlap on
- * the GPU (different streams, or one stream and a capture replay) race on it;
- * calls in order on one stream do not.  Nothing in it needs clearing: every slot a
+ * context's max_rows.  The arrays sit in a module of their own, which the CUDA
+ * runtime loads (committing their 12 MB) the first time it is touched on a device:
+ * lora_ctx_create does that and looks their device addresses up, so this call
+ * itself allocates nothing, also on its first use (a context created after a
+ * cudaDeviceReset looks the addresses up again).  Every call shares the arrays:
+ * calls that overlap on the GPU (different streams, or one stream and a capture
+ * replay) race on them; calls in order on one stream do not.  Nothing in it needs clearing: every slot a
  * call reads is written by the same call first.  Profiling (lora_profile_begin) is
  * ignored for this call. */
 int lora_fused_noalloc(lora_ctx *ctx, const lora_table *table, const int32_t *ids_host,
@@ -234,6 +241,31 @@ int lora_page_in(lora_ctx *ctx, const lora_table *table, int adapter, const void
 int lora_tiles_load(lora_ctx *ctx, const char *path);
 int lora_tiles_save(const lora_ctx *ctx, const char *path);
 int64_t lora_tiles_count(const lora_ctx *ctx);
+
+/* Whether the last delta, merge or unmerge call of the context found every launch
+ * shape it needed in the tile table: LORA_OK, or LORA_E_NOTUNED when at least one
+ * came from the built-in default (the call itself succeeded either way).  Read it
+ * after the call; the next call overwrites it.  LORA_E_INVAL for a null context. */
+int lora_tile_status(const lora_ctx *ctx);
+
+/* Offline search over a file of shapes (VaLoRA blog, section 4.3.2: every candidate
+ * tiling of each input shape is profiled offline and the best kept in the table the
+ * runtime looks up).  One shape per line of the text file at shapes_path:
+ *     kind n d_in d_out rank adapters [run [objective]]
+ * kind: rows (row-gather fused call), tiles (tensor-core fused call), merge; n rows
+ * (ignored for merge); `adapters` adapters of rank `rank`; run: rows per request,
+ * the ids being (i / run) % adapters (0, the default: i % adapters); objective:
+ * latency (default: lora_tune_shape's cold single-call median) or throughput (rows
+ * only: back-to-back calls over rotating copies of the inputs larger than L2).
+ * '#' starts a comment.  The whole file is checked before anything runs (LORA_E_IO
+ * if it cannot be read, LORA_E_INVAL for a malformed line or a rank above the
+ * context's max_rank).  Each shape then runs on device buffers the call allocates,
+ * fills with synthetic values (uniform, the variances of the workloads) on
+ * `stream`, and frees; the winners go into the context's table.  If out_path is not
+ * NULL the table is written there (lora_tiles_save format) followed by one comment
+ * line per shape with its best time.  A host-only context (device -1) parses the
+ * file and returns LORA_E_UNSUPPORTED. */
+int lora_tune(lora_ctx *ctx, const char *shapes_path, const char *out_path, void *stream);
 
 /* Offline search for one shape (VaLoRA blog, section 4.3.2): times every
  * candidate of a pruned configuration space with CUDA events (two warm-up calls,

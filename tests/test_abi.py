@@ -36,7 +36,7 @@ def test_library_exports_every_declared_symbol():
 def test_status_strings_and_no_gpu_context():
     import adapter_sgmv_bgmv_gb300 as L
     assert L._L.lora_strerror(0) == b"ok"
-    for code in range(-11, 0):
+    for code in range(-12, 0):
         assert L._L.lora_strerror(code) != b"unknown status"
     if not torch.cuda.is_available():
         with pytest.raises(L.LoraError):
@@ -198,3 +198,40 @@ def test_tile_table_file_round_trip(tmp_path):
         ctx.tiles_load(str(bad))
     with pytest.raises(L.LoraError):
         ctx.tiles_load(str(tmp_path / "missing.tbl"))
+
+
+def test_shape_file_of_the_offline_search_is_checked_before_anything_runs(tmp_path):
+    """lora_tune reads its shape file in full first: a missing file is LORA_E_IO, a
+    malformed line LORA_E_INVAL; a well-formed file on a host-only context parses
+    and stops at LORA_E_UNSUPPORTED (no launches), with no output file written."""
+    import adapter_sgmv_bgmv_gb300 as L
+    ctx = L.Context(-1, max_rows=4096, max_rank=64)
+    out = tmp_path / "out.tbl"
+    good = tmp_path / "good.shapes"
+    good.write_text("# kind n d_in d_out rank adapters run objective\n"
+                    "rows 64 4096 4096 16 64 0 throughput\n"
+                    "tiles 16896 4096 11008 64 4 1056\n\n"
+                    "merge 1 4096 11008 64 1   # merge ignores n\n")
+    with pytest.raises(L.LoraError) as e:
+        ctx.tune(str(good), str(out))
+    assert e.value.name == "LORA_E_UNSUPPORTED" and not out.exists()
+    with pytest.raises(L.LoraError) as e:
+        ctx.tune(str(tmp_path / "missing.shapes"), str(out))
+    assert e.value.name == "LORA_E_IO"
+    bad_lines = ["rows 64 4096 4096 16",                     # too few fields
+                 "conv 64 4096 4096 16 4",                   # unknown kind
+                 "rows 64 4096 4100 16 4",                   # width not a multiple of 8
+                 "rows 64 4096 4096 12 4",                   # rank not a multiple of 8
+                 "rows 64 4096 4096 128 4",                  # rank above the context's max
+                 "rows 64 4096 4096 16 4 0 fastest",         # unknown objective
+                 "tiles 512 4096 4096 16 4 128 throughput",  # throughput is for rows only
+                 "rows 6x4 4096 4096 16 4"]                  # not an integer
+    for line in bad_lines:
+        bad = tmp_path / "bad.shapes"
+        bad.write_text("rows 16 256 256 8 4\n" + line + "\n")
+        with pytest.raises(L.LoraError) as e:
+            ctx.tune(str(bad), str(out))
+        assert e.value.name == "LORA_E_INVAL", line
+    assert not out.exists()
+    assert ctx.tile_status() == "LORA_OK"
+    ctx.close()

@@ -55,3 +55,32 @@ def test_tune_merge_and_tiles():
     ref = oracle.fused(oracle.Table.from_case(p), p["ids"], p["x"], p["y"], nthreads=8)
     assert_parity(from_dev(y), ref, REL_FROB, MAX_ABS_RMS, "tuned tiles")
     ctx.close()
+
+
+def test_lora_tune_reads_a_shape_file_and_writes_the_table(tmp_path):
+    """The C driver of the offline search: one latency shape and one throughput shape
+    from a file, the table written with a comment per shape, and a fresh context that
+    loads it finds the tuned shapes (lora_tile_status LORA_OK) and stays exact."""
+    shapes = tmp_path / "s.shapes"
+    shapes.write_text("rows 16 256 256 8 4\nrows 64 256 256 8 4 0 throughput\n")
+    out = tmp_path / "t.tbl"
+    ctx = L.Context(0, max_rows=4096, max_rank=64)
+    ctx.tune(str(shapes), str(out))
+    text = out.read_text()
+    assert ctx.tiles_count() == 2 and text.count("# tuned:") == 2
+    fresh = L.Context(0, max_rows=4096, max_rank=64)
+    c = workloads.make("tiny_decode", seed=5)             # 16 rows, d=256, 4 rank-8 adapters
+    t = upload_table(fresh, c)
+    y = to_dev(c["y"])
+    L.lora_fused(fresh, t, c["ids"], to_dev(c["x"]), y)
+    assert fresh.tile_status() == "LORA_E_NOTUNED"        # empty table: the default shape
+    fresh.tiles_load(str(out))
+    y = to_dev(c["y"])
+    L.lora_fused(fresh, t, c["ids"], to_dev(c["x"]), y)
+    fresh.sync_status()
+    if len(np.unique(c["ids"])) == 4:                     # the tuned key (4 distinct adapters)
+        assert fresh.tile_status() == "LORA_OK"
+    ref = oracle.fused(oracle.Table.from_case(c), c["ids"], c["x"], c["y"])
+    assert_parity(from_dev(y), ref, REL_FROB, MAX_ABS_RMS, "after lora_tune")
+    fresh.close()
+    ctx.close()

@@ -1,12 +1,14 @@
 """lora_fused_noalloc: the fused delta for callers that must not allocate device or
-pinned memory while it runs (its scratch is a fixed array inside the library).
-It must give the same results as lora_fused, call after call, and leave the GPU's
-free memory unchanged.  Collected last on purpose: a failure here comes after every
-other test has run."""
+pinned memory while it runs (an allocator hook, a fixed memory budget): its
+scratch is fixed arrays inside the library, committed when the context is created.
+It must give the results of lora_fused and of the oracle, call after call, and
+leave the GPU's free memory unchanged from its very first call on.  Collected last
+on purpose: a failure here comes after every other test has run."""
 import numpy as np
 import pytest
 import torch
 
+import oracle
 import workloads
 from tests._helpers import assert_parity
 from tests.conftest import MAX_ABS_RMS, REL_FROB
@@ -25,40 +27,67 @@ def _case(seed):
                            ranks=[16, 32, 8, 64], paged=True, ids=ids)
 
 
-def test_noalloc_matches_fused_on_two_calls_and_allocates_nothing():
+def test_noalloc_matches_fused_and_oracle_on_two_calls_and_allocates_nothing():
     ctx = L.Context(0, max_rows=4096, max_rank=64)
     cases = [_case(71), _case(72)]
     tables = [upload_table(ctx, c) for c in cases]
     xs = [to_dev(c["x"]) for c in cases]
     y_ref = [to_dev(c["y"]) for c in cases]
     y_got = [to_dev(c["y"]) for c in cases]
-    warm = to_dev(cases[0]["y"])
     for c, t, x, y in zip(cases, tables, xs, y_ref):      # the existing entry point
         L.lora_fused(ctx, t, c["ids"], x, y)
-    L.lora_fused_noalloc(ctx, tables[0], cases[0]["ids"], xs[0], warm)   # first-call set-up
     torch.cuda.synchronize()
-    free_before = torch.cuda.mem_get_info()[0]
+    free_before = torch.cuda.mem_get_info()[0]            # before the first no-alloc call
     for c, t, x, y in zip(cases, tables, xs, y_got):      # two calls in a row
         L.lora_fused_noalloc(ctx, t, c["ids"], x, y)
         assert ctx.last_path()[0] == 3                    # tiles and row-gather both ran
     ctx.sync_status()
     assert torch.cuda.mem_get_info()[0] == free_before
     for k in range(2):
-        assert_parity(from_dev(y_got[k]), from_dev(y_ref[k]), REL_FROB, MAX_ABS_RMS, f"call {k}")
+        got = from_dev(y_got[k])
+        assert_parity(got, from_dev(y_ref[k]), REL_FROB, MAX_ABS_RMS, f"call {k} vs lora_fused")
+        ref = oracle.fused(oracle.Table.from_case(cases[k]), cases[k]["ids"], cases[k]["x"],
+                           cases[k]["y"], nthreads=8)
+        assert_parity(got, ref, REL_FROB, MAX_ABS_RMS, f"call {k} vs oracle")
         rel = cases[k]["ids"] < 0
-        np.testing.assert_array_equal(from_dev(y_got[k])[rel], cases[k]["y"][rel])
+        np.testing.assert_array_equal(got[rel], cases[k]["y"][rel])
     ctx.close()
 
 
-def test_noalloc_rejects_batches_beyond_its_fixed_scratch():
-    ctx = L.Context(0, max_rows=1 << 15, max_rank=64)
-    c = workloads.small(seed=73, n=65 * 128, d_in=64, d_out=64, n_adapters=1, ranks=[8],
-                        ids=np.zeros(65 * 128, np.int32))
+def _refused(ctx, c):
     t = upload_table(ctx, c)
     y = to_dev(c["y"])
     with pytest.raises(L.LoraError) as e:
         L.lora_fused_noalloc(ctx, t, c["ids"], to_dev(c["x"]), y)
     assert e.value.name == "LORA_E_CAPACITY"
+    assert ctx.last_path() == (0, 0)                      # nothing launched
     ctx.sync_status()
-    np.testing.assert_array_equal(from_dev(y), c["y"])
+    np.testing.assert_array_equal(from_dev(y), c["y"])    # nothing written
+
+
+def test_noalloc_rejects_more_tiles_than_its_partial_v_slots():
+    ctx = L.Context(0, max_rows=1 << 15, max_rank=64)
+    # 65 tiles of 128 rows: one more than the 64 partial-V slots
+    _refused(ctx, workloads.small(seed=73, n=65 * 128, d_in=64, d_out=64, n_adapters=1,
+                                  ranks=[8], ids=np.zeros(65 * 128, np.int32)))
+    ctx.close()
+
+
+def test_noalloc_rejects_dense_rows_beyond_its_fixed_array():
+    ctx = L.Context(0, max_rows=1 << 15, max_rank=64)
+    # nine rank-64 adapters in shuffled pages, 128 rows each: their dense rows take
+    # 9 x 64 x (4096 + 4096) x 2 B = 9 MB, past the 8 MB array
+    ids = np.repeat(np.arange(9, dtype=np.int32), 128)
+    _refused(ctx, workloads.small(seed=74, n=ids.size, d_in=4096, d_out=4096, n_adapters=9,
+                                  ranks=[64] * 9, paged=True, ids=ids))
+    ctx.close()
+
+
+def test_noalloc_rejects_more_scattered_rows_than_its_parameter_plan():
+    ctx = L.Context(0, max_rows=1 << 15, max_rank=64)
+    # 600 rows alternating between two adapters: no run reaches a tile, so all 600
+    # go to the row-gather kernel, past the 512 rows its in-parameter plan holds
+    ids = np.tile(np.array([0, 1], np.int32), 300)
+    _refused(ctx, workloads.small(seed=75, n=ids.size, d_in=64, d_out=64, n_adapters=2,
+                                  ranks=[8, 8], ids=ids))
     ctx.close()
