@@ -18,7 +18,7 @@ import torch
 from . import _lib
 
 __all__ = ["LoraError", "Context", "AdapterTable", "lora_plan_build", "lora_shrink",
-           "lora_expand", "lora_fused", "lora_fused_noalloc", "PreparedFused", "lora_merge", "lora_unmerge", "lora_page_in", "lora_fused_device_ids", "lora_tune_shape",
+           "lora_expand", "lora_fused", "lora_fused_noalloc", "lora_base_fused", "PreparedFused", "lora_merge", "lora_unmerge", "lora_page_in", "lora_fused_device_ids", "lora_tune_shape",
            "KIND_ROWS_FUSED", "KIND_SHRINK", "KIND_EXPAND", "KIND_TILE_FUSED", "KIND_MERGE",
            "OPT_TILE_PATH", "OPT_MERGE_KERNEL", "OPT_TILE_MIN_RUN", "OPT_EARLY_PAGES", "OPT_DEVICE_PLAN",
            "library_path"]
@@ -169,11 +169,11 @@ class Context:
         """Stop; returns {family: (device ms, launches)} for the row-gather, tile shrink,
         merge and streaming expand kernels: every launch made while profiling, and
         their device time (the bracketed launches' mean times that count)."""
-        ms = (ctypes.c_double * 4)()
-        n = (ctypes.c_int64 * 4)()
+        ms = (ctypes.c_double * 5)()
+        n = (ctypes.c_int64 * 5)()
         _check(_L.lora_profile_end(self.handle, ms, n), self)
         return {name: (ms[i], int(n[i]))
-                for i, name in enumerate(("rows", "shrink", "merge", "expand"))}
+                for i, name in enumerate(("rows", "shrink", "merge", "expand", "proj"))}
 
     def launch_count(self) -> int:
         """Kernels launched by this context so far."""
@@ -295,6 +295,21 @@ def lora_fused_device_ids(ctx: Context, table: AdapterTable, ids: torch.Tensor, 
     py, ldy, d_out = _rows(y, "y")
     _check(_L.lora_fused_device_ids(ctx.handle, table.handle, ids.data_ptr(), ids.shape[0], px,
                                     ldx, d_in, py, ldy, d_out, _stream(stream, ctx.device)), ctx)
+
+
+def lora_base_fused(ctx: Context, table: AdapterTable, ids, x: torch.Tensor, W: torch.Tensor,
+                    y: torch.Tensor, stream=None):
+    """y_i <- bf16(x_i W + s_k (x_i A_k) B_k) (x_i W alone for ids[i] == -1): the base
+    projection with the adapter term in one tensor-core GEMM; y is written, not read.
+    W is [d_in, d_out] row-major."""
+    ids, pid, n = _ids(ids)
+    px, ldx, d_in = _rows(x, "x")
+    pw, ldw, d_out = _rows(W, "W")
+    py, ldy, d_out_y = _rows(y, "y")
+    if W.shape[0] != d_in or d_out_y != d_out:
+        raise ValueError("shapes: x [n, d_in], W [d_in, d_out], y [n, d_out]")
+    _check(_L.lora_base_fused(ctx.handle, table.handle, pid, n, px, ldx, d_in, pw, ldw, py, ldy,
+                              d_out, _stream(stream, ctx.device)), ctx)
 
 
 def lora_fused_noalloc(ctx: Context, table: AdapterTable, ids, x: torch.Tensor, y: torch.Tensor,

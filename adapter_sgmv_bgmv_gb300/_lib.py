@@ -35,6 +35,7 @@ SIGNATURES = {
     "lora_expand": ([P, P, P, I64, P, I64, P, I64, I, P], I),
     "lora_fused": ([P, P, P, I64, P, I64, I, P, I64, I, P], I),
     "lora_fused_noalloc": ([P, P, P, I64, P, I64, I, P, I64, I, P], I),
+    "lora_base_fused": ([P, P, P, I64, P, I64, I, P, I64, P, I64, I, P], I),
     "lora_merge": ([P, P, I, P, I64, I, I, P], I),
     "lora_unmerge": ([P, P, I, P, I64, I, I, P], I),
     "lora_page_in": ([P, P, I, P, I, P, I, P], I),

@@ -32,6 +32,9 @@ namespace {
 
 constexpr int kSlots = 8;
 constexpr int kSms = 152;
+// Kernel families of the profiler: row-gather, tile shrink, merge, streaming
+// expand, base projection.
+constexpr int kFamilies = 5;
 
 struct Slot {
     uint8_t *host = nullptr;   // pinned
@@ -73,7 +76,7 @@ struct lora_ctx {
     RowsParamsInlineSmall inline_small;
     int64_t launches_total = 0;     // every kernel launched by this context
     int prof_every = 1;             // bracket one launch in this many, per kernel family
-    int64_t prof_seen[4] = {0, 0, 0, 0};
+    int64_t prof_seen[kFamilies] = {0, 0, 0, 0, 0};
     int merge_path = 0;             // 0 auto (tensor cores when supported), 1 CUDA cores
     int tile_path = 1;              // 1: long same-adapter runs use the tensor-core tiles
     int tile_min_run_override = 0;  // > 0: fixed minimum run for the tile path
@@ -84,6 +87,12 @@ struct lora_ctx {
     bool pool_write_pending = false;            // ... and no delta / merge launch after it yet
     int force_cluster = 0;          // > 0 while tuning: row-kernel cluster width
     int force_rows = 0;             // > 0 while tuning: rows per item
+    float *vrows = nullptr;         // lora_base_fused: the shrink's fp32 rows
+    size_t vrows_cap = 0;           //   (bytes)
+    uint8_t *brows = nullptr;       // lora_base_fused: dense B rows, when needed
+    size_t brows_cap = 0;
+    std::vector<int32_t> proj_mark, proj_off, proj_slots, proj_bbase;
+    std::vector<ProjTerm> proj_terms;
     uint8_t *vparts = nullptr;      // fused tile path: partial V between its two kernels
     size_t vparts_cap = 0;
     uint8_t *dense = nullptr;       // dense adapter rows of a call (dense.cu): two halves,
@@ -202,7 +211,7 @@ long prof_start(lora_ctx *ctx, int family, cudaStream_t stream)
 {
     if (!ctx->prof)
         return -1;
-    if ((ctx->prof_seen[family & 3]++ % ctx->prof_every) != 0)
+    if ((ctx->prof_seen[family % kFamilies]++ % ctx->prof_every) != 0)
         return -1;
     if (ctx->prof_used == ctx->prof_ev.size()) {
         lora_ctx::ProfEv e;
@@ -440,9 +449,33 @@ struct RowMats {
     int rp = 0;
 };
 
+// Bytes of the dense rows setup_rows would make for these adapters (0 when the
+// pools serve as they are).
+size_t dense_rows_bytes(const lora_table *t, const int32_t *adapters, int n_slots, int d_in,
+                        int d_out, bool need_a, bool need_b)
+{
+    bool direct = true;
+    int rmax = 0;
+    for (int s = 0; s < n_slots; ++s) {
+        const size_t k = size_t(adapters[s]);
+        rmax = std::max(rmax, t->rank[k]);
+        if ((t->rank[k] % 16) != 0 || (need_a && !t->a_contig[k]) || (need_b && !t->b_contig[k]))
+            direct = false;
+    }
+    if (direct)
+        return 0;
+    const int rp = (rmax + 15) & ~15;
+    const size_t a_bytes = need_a ? (size_t(n_slots) * rp * size_t(d_in) * 2u + 255u) & ~size_t(255) : 0;
+    return a_bytes + (need_b ? size_t(n_slots) * rp * size_t(d_out) * 2u : 0);
+}
+
+// own: a caller-sized buffer for the dense rows (instead of the context's two halves
+// or the fixed array), with room for dense_rows_bytes; its copy waits for the kernel
+// before it (no early staging).
 int setup_rows(lora_ctx *ctx, const lora_table *t, const int32_t *adapters, int n_slots,
                int d_in, int d_out, bool need_a, bool need_b, const NoAllocScratch *fixed,
-               cudaStream_t stream, RowMats *m, int32_t *a_base, int32_t *b_base)
+               cudaStream_t stream, RowMats *m, int32_t *a_base, int32_t *b_base,
+               uint8_t *own = nullptr)
 {
     bool direct = true;
     int rmax = 0;
@@ -469,7 +502,9 @@ int setup_rows(lora_ctx *ctx, const lora_table *t, const int32_t *adapters, int 
     const size_t a_bytes = need_a ? (size_t(n_slots) * rp * size_t(d_in) * 2u + 255u) & ~size_t(255) : 0;
     const size_t bytes = a_bytes + (need_b ? size_t(n_slots) * rp * size_t(d_out) * 2u : 0);
     uint8_t *buf = nullptr;
-    if (fixed) {
+    if (own) {
+        buf = own;
+    } else if (fixed) {
         if (bytes > kNoAllocDenseBytes)
             return LORA_E_CAPACITY;
         buf = reinterpret_cast<uint8_t *>(fixed->dense);
@@ -924,6 +959,10 @@ int lora_ctx_destroy(lora_ctx *ctx)
         cudaFree(ctx->d_dplan);
     if (ctx->vparts)
         cudaFree(ctx->vparts);
+    if (ctx->vrows)
+        cudaFree(ctx->vrows);
+    if (ctx->brows)
+        cudaFree(ctx->brows);
     if (ctx->dense)
         cudaFree(ctx->dense);
     if (ctx->flush)
@@ -1100,6 +1139,161 @@ int lora_fused(lora_ctx *ctx, const lora_table *t, const int32_t *ids, int64_t n
 {
     return delta_call(ctx, t, kFused, ids, n, x, ldx, d_in, nullptr, 0, y, ldy, d_out,
                       static_cast<cudaStream_t>(stream));
+}
+
+int lora_base_fused(lora_ctx *ctx, const lora_table *t, const int32_t *ids, int64_t n,
+                    const void *x, int64_t ldx, int d_in, const void *W, int64_t ldw, void *y,
+                    int64_t ldy, int d_out, void *stream_ptr)
+{
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+    if (ctx) {
+        ctx->last_path = ctx->last_launches = 0;
+        begin_call(ctx, stream);
+    }
+    int rc = prepare(ctx, t, ids, n);
+    if (rc != LORA_OK)
+        return rc;
+    if (n == 0)
+        return LORA_OK;
+    if (!stride_ok(x, ldx, d_in) || !stride_ok(W, ldw, d_out) || !stride_ok(y, ldy, d_out))
+        return LORA_E_INVAL;
+    const bool any_active = !ctx->plan.active.empty();
+    if (any_active && (d_in > t->a_pw || d_out > t->b_pw))
+        return LORA_E_INVAL;
+    rc = use_device(ctx);
+    if (rc != LORA_OK)
+        return rc;
+    int32_t rmax = 8;
+    for (int32_t k : ctx->plan.seg_adapter)
+        rmax = std::max(rmax, t->rank[size_t(k)]);
+    // 1. v = x A_k for the active rows (the shrink kernels) into fp32 scratch rows.
+    const int64_t ldv = rmax;
+    int path = 0;
+    bool untuned = false;
+    if (any_active) {
+        const size_t need = size_t(n) * size_t(ldv) * 4u;
+        if (need > ctx->vrows_cap) {
+            if (ctx->vrows) {
+                CUDA_TRY(ctx, cudaStreamSynchronize(stream));
+                cudaFree(ctx->vrows);
+                ctx->vrows = nullptr;
+                ctx->vrows_cap = 0;
+            }
+            if (cudaMalloc(reinterpret_cast<void **>(&ctx->vrows), need) != cudaSuccess)
+                return LORA_E_NOMEM;
+            ctx->vrows_cap = need;
+        }
+        rc = delta_call(ctx, t, kShrink, ids, n, x, ldx, d_in, ctx->vrows, ldv, nullptr, 0, 0,
+                        stream);
+        if (rc != LORA_OK)
+            return rc;
+        path = ctx->last_path;
+        untuned = ctx->untuned;
+    }
+    // 2. Per 128-row block, one term per adapter with rows in it (order of first row).
+    const int BM = proj_block_rows(), BN = proj_block_cols();
+    const int n_mblk = int(ceil_div(n, BM)), n_nblk = int(ceil_div(d_out, BN));
+    std::vector<int32_t> &mark = ctx->proj_mark, &off = ctx->proj_off, &slots = ctx->proj_slots;
+    std::vector<ProjTerm> &terms = ctx->proj_terms;
+    mark.assign(size_t(t->n_adapters), -1);
+    if (ctx->slot_of.size() < size_t(t->n_adapters))
+        ctx->slot_of.resize(size_t(t->n_adapters), -1);
+    off.assign(size_t(n_mblk) + 1, 0);
+    terms.clear();
+    slots.clear();
+    for (int m = 0; m < n_mblk; ++m) {
+        off[size_t(m)] = int32_t(terms.size());
+        const int64_t r1 = std::min<int64_t>(n, int64_t(m + 1) * BM);
+        for (int64_t i = int64_t(m) * BM; i < r1; ++i) {
+            const int32_t k = ids[i];
+            if (k < 0 || mark[size_t(k)] == m)
+                continue;
+            mark[size_t(k)] = m;
+            if (ctx->slot_of[size_t(k)] < 0) {
+                ctx->slot_of[size_t(k)] = int32_t(slots.size());
+                slots.push_back(k);
+            }
+            terms.push_back(ProjTerm{k, 0, t->rank[size_t(k)], t->scale[size_t(k)]});
+        }
+    }
+    off[size_t(n_mblk)] = int32_t(terms.size());
+    // 3. The B row matrix of those adapters: the pool itself, or dense rows in the
+    // call's own buffer (rank-padded with zero rows).
+    const int n_slots = int(slots.size());
+    RowMats mats;
+    ctx->proj_bbase.assign(size_t(n_slots), 0);
+    std::vector<int32_t> a_unused(size_t(n_slots) + 1, 0);
+    if (n_slots > 0) {
+        const size_t bytes = dense_rows_bytes(t, slots.data(), n_slots, d_in, d_out, false, true);
+        if (bytes > ctx->brows_cap) {
+            if (ctx->brows) {
+                CUDA_TRY(ctx, cudaStreamSynchronize(stream));
+                cudaFree(ctx->brows);
+                ctx->brows = nullptr;
+                ctx->brows_cap = 0;
+            }
+            if (cudaMalloc(reinterpret_cast<void **>(&ctx->brows), bytes) != cudaSuccess)
+                rc = LORA_E_NOMEM;
+            else
+                ctx->brows_cap = bytes;
+        }
+        if (rc == LORA_OK)
+            rc = setup_rows(ctx, t, slots.data(), n_slots, d_in, d_out, false, true, nullptr, stream,
+                            &mats, a_unused.data(), ctx->proj_bbase.data(), ctx->brows);
+        if (rc == LORA_OK)
+            for (ProjTerm &tm : terms)
+                tm.b_row = ctx->proj_bbase[size_t(ctx->slot_of[size_t(tm.adapter)])];
+    }
+    for (int32_t k : slots)
+        ctx->slot_of[size_t(k)] = -1;
+    if (rc != LORA_OK)
+        return rc;
+    // 4. Upload the block terms and the ids in one copy, stage B if needed, launch.
+    const size_t off_bytes = (size_t(n_mblk + 1) * 4u + 15u) & ~size_t(15);
+    const size_t terms_bytes = terms.size() * sizeof(ProjTerm);
+    const size_t ids_bytes = size_t(n) * 4u;
+    Slot *slot = nullptr;
+    rc = acquire_slot(ctx, off_bytes + terms_bytes + ids_bytes + 16, &slot);
+    if (rc != LORA_OK)
+        return rc;
+    std::memcpy(slot->host, off.data(), size_t(n_mblk + 1) * 4u);
+    std::memcpy(slot->host + off_bytes, terms.data(), terms_bytes);
+    std::memcpy(slot->host + off_bytes + terms_bytes, ids, ids_bytes);
+    CUDA_TRY(ctx, cudaMemcpyAsync(slot->dev, slot->host, off_bytes + terms_bytes + ids_bytes,
+                                  cudaMemcpyHostToDevice, stream));
+    const long ev = prof_start(ctx, 4, stream);
+    if (n_slots > 0) {
+        rc = run_staging(ctx, t, mats, slots.data(), n_slots, d_in, d_out, false, true, stream);
+        if (rc != LORA_OK)
+            return rc;
+    }
+    ProjParams p{};
+    p.x = static_cast<const uint16_t *>(x);
+    p.ldx = ldx;
+    p.W = static_cast<const uint16_t *>(W);
+    p.ldw = ldw;
+    p.y = static_cast<uint16_t *>(y);
+    p.ldy = ldy;
+    p.v = any_active ? ctx->vrows : nullptr;
+    p.ldv = ldv;
+    p.term_off = reinterpret_cast<const int32_t *>(slot->dev);
+    p.terms = reinterpret_cast<const ProjTerm *>(slot->dev + off_bytes);
+    p.ids = reinterpret_cast<const int32_t *>(slot->dev + off_bytes + terms_bytes);
+    p.b_rows = n_slots > 0 ? mats.b : nullptr;
+    p.b_ld = mats.b_ld;
+    p.b_nrows = mats.b_nrows;
+    p.status = ctx->d_status;
+    p.n = int(n);
+    p.d_in = d_in;
+    p.d_out = d_out;
+    p.n_mblk = n_mblk;
+    p.n_nblk = n_nblk;
+    CUDA_TRY(ctx, launch_proj_tc(p, stream));
+    prof_stop(ctx, ev, stream);
+    count_launch(ctx, stream);
+    ctx->last_path = path | 16;
+    ctx->untuned = untuned;
+    return release_slot(ctx, slot, stream);
 }
 
 int lora_fused_noalloc(lora_ctx *ctx, const lora_table *t, const int32_t *ids, int64_t n,
@@ -1414,11 +1608,11 @@ int lora_profile_end(lora_ctx *ctx, double *ms, int64_t *launches)
     if (!ctx || !ms || !launches)
         return LORA_E_INVAL;
     ctx->prof = false;
-    for (int f = 0; f < 4; ++f) {
+    for (int f = 0; f < kFamilies; ++f) {
         ms[f] = 0.0;
         launches[f] = 0;
     }
-    int64_t sampled[4] = {0, 0, 0, 0};
+    int64_t sampled[kFamilies] = {0, 0, 0, 0, 0};
     for (size_t i = 0; i < ctx->prof_used; ++i) {
         lora_ctx::ProfEv &e = ctx->prof_ev[i];
         CUDA_TRY(ctx, cudaEventSynchronize(e.b));
@@ -1428,7 +1622,7 @@ int lora_profile_end(lora_ctx *ctx, double *ms, int64_t *launches)
         sampled[e.family] += 1;
     }
     // The bracketed launches stand for all of their family: mean x count.
-    for (int f = 0; f < 4; ++f) {
+    for (int f = 0; f < kFamilies; ++f) {
         launches[f] = ctx->prof_seen[f];
         if (sampled[f] > 0)
             ms[f] *= double(ctx->prof_seen[f]) / double(sampled[f]);

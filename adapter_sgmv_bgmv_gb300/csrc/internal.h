@@ -207,6 +207,42 @@ size_t dev_plan_smem_bytes(int n_adapters);
 cudaError_t launch_wait_selftest(unsigned *status, uint64_t limit_ns, cudaStream_t stream);
 cudaError_t launch_plan_dev(const DevPlanArgs &a, cudaStream_t stream);
 
+// Base projection with the adapter term (proj_tc.cu): y = bf16(x W + s_k (x A_k) B_k).
+// One term per adapter with rows in a 128-row block; the block's terms are
+// terms[term_off[m] .. term_off[m + 1]).
+struct ProjTerm {
+    int32_t adapter;
+    int32_t b_row;            // row of page 0 of B_k in the B row matrix
+    int32_t rank;
+    float scale;
+};
+static_assert(sizeof(ProjTerm) == 16, "ProjTerm is one 16-byte load");
+struct ProjParams {
+    const uint16_t *x;
+    int64_t ldx;
+    const uint16_t *W;
+    int64_t ldw;
+    uint16_t *y;
+    int64_t ldy;
+    const float *v;           // the shrink's fp32 rows [n, ldv] (columns < rank used)
+    int64_t ldv;
+    const int32_t *ids;       // device copy of the call's ids [n]
+    const int32_t *term_off;  // [n_mblk + 1]
+    const ProjTerm *terms;
+    const uint16_t *b_rows;   // B row matrix (pages as consecutive rows, rank-padded)
+    int64_t b_ld;
+    int64_t b_nrows;
+    unsigned *status;
+    int n;
+    int d_in;
+    int d_out;
+    int n_mblk;               // 128-row blocks
+    int n_nblk;               // 256-column blocks
+};
+cudaError_t launch_proj_tc(const ProjParams &p, cudaStream_t stream);
+int proj_block_rows();
+int proj_block_cols();
+
 // Offline search (fill.cu): n bf16 values uniform in [-scale, scale) from a hash of
 // (seed, index).
 cudaError_t launch_fill_bf16(uint16_t *dst, uint64_t n, uint64_t seed, float scale,

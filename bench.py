@@ -48,12 +48,13 @@ FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 DEFAULT_CONFIG = "valora_prefill"
 CONFIGS = ("valora_prefill", "llama7b_decode", "tiny_decode", "slora_prefill", "valora_merge",
-           "lorazor_decode")
+           "lorazor_decode", "valora_base_fused")
 DEVICE_IDS_CONFIGS = ("llama7b_decode", "tiny_decode", "lorazor_decode")
 # Steps of a per_config entry (a fixed count, independent of --steps, sized so that
 # each timed region is a few tens to a few hundred milliseconds).
 PER_CONFIG_STEPS = {"llama7b_decode": 10000, "tiny_decode": 20000, "lorazor_decode": 10000,
-                    "slora_prefill": 2000, "valora_prefill": 500, "valora_merge": 1000}
+                    "slora_prefill": 2000, "valora_prefill": 500, "valora_merge": 1000,
+                    "valora_base_fused": 200}
 WORKLOAD_DESC = {
     "valora_prefill": ("Qwen-VL-7B MLP up-proj 4096->11008, 16 requests x (1024 visual + 32 "
                        "text) tokens = 16896, 4 rank-64 adapters (Zipf 1.2), contiguous storage"),
@@ -68,6 +69,9 @@ WORKLOAD_DESC = {
     "lorazor_decode": ("70B projection 8192x8192, 256 requests x 1 token, 512 resident rank-16 "
                        "adapters (Zipf 1.0) in shuffled 8192-wide pages; step t releases 128+t "
                        "rows (t = 0..99, cycled)"),
+    "valora_base_fused": ("the VaLoRA prefill through the base projection with the adapter term "
+                          "fused in: y = x W + s (x A) B, W 4096x11008 bf16, 16896 tokens, 4 "
+                          "rank-64 adapters (Zipf 1.2); y written once"),
 }
 # Source files of each kernel family: a DRAM-traffic figure measured by ncu holds only
 # while their contents are those it was measured on.
@@ -76,9 +80,11 @@ FAMILY_SOURCES = {
     "shrink": ["tile_tc.cu", "dense.cu", "tc.cuh"],
     "expand": ["stream_tc.cu", "tc.cuh"],
     "merge": ["stream_tc.cu", "tc.cuh"],
+    "proj": ["proj_tc.cu", "tc.cuh"],
 }
 KERNEL_NAMES = {"rows": "k_rows_inline<fused>", "shrink": "k_shrink_tc (+ k_stage_rows)",
-                "expand": "k_stream_tc(expand)", "merge": "k_stream_tc(merge)"}
+                "expand": "k_stream_tc(expand)", "merge": "k_stream_tc(merge)",
+                "proj": "k_proj_tc (base GEMM + adapter term)"}
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
 
 
@@ -321,6 +327,11 @@ class Bench:
             c = workloads.make(name, seed=0)
             self.cases = {"main": c}
             self.steps_ids = [[("main", c["ids"])]]
+        elif name == "valora_base_fused":
+            c = workloads.make("valora_prefill", seed=0)
+            c["W"] = workloads.make_W(c["d_in"], c["d_out"], seed=0)
+            self.cases = {"main": c}
+            self.steps_ids = [[("main", c["ids"])]]
         elif name == "valora_merge":
             c = workloads.make("valora_merge", seed=0)
             self.cases = {"main": c}
@@ -329,6 +340,7 @@ class Bench:
             raise KeyError(name)
         self.workload = WORKLOAD_DESC[name]
         self.is_merge = name == "valora_merge"
+        self.is_proj = name == "valora_base_fused"
         self._upload()
 
     # ---- device data, rotated so that one pass over the sets exceeds L2
@@ -336,6 +348,9 @@ class Bench:
         if self.is_merge:
             c = self.cases["main"]
             return 2 * c["d_in"] * c["d_out"]
+        if self.is_proj:
+            c = self.cases["main"]
+            return 2 * c["n"] * (c["d_in"] + c["d_out"]) + 2 * c["d_in"] * c["d_out"]
         return sum(alg_bytes_delta(self.cases[key], ids) for key, ids in self.steps_ids[0])
 
     def _upload(self):
@@ -356,6 +371,8 @@ class Bench:
             else:
                 d["x"] = to_dev(c["x"])
                 d["y"] = to_dev(c["y"])
+                if self.is_proj:
+                    d["W"] = to_dev(c["W"])
             base[key] = d
         # Per set, the step's activations sit in one block, every x first and every y
         # after it, so that the end-to-end loop copies a step in with one copy and
@@ -384,9 +401,11 @@ class Bench:
                     d["W"] = b["W"] if s == 0 else b["W"].clone()
                 else:
                     d["x"], d["y"] = views[(key, "x")], views[(key, "y")]
+                    if self.is_proj:
+                        d["W"] = b["W"] if s == 0 else b["W"].clone()
                 d["table"] = L.AdapterTable(self.ctx, d["a_pool"], d["b_pool"], c["rank"],
                                             c["scale"], c["a_pages"], c["b_pages"])
-                if not self.is_merge:
+                if not self.is_merge and not self.is_proj:
                     d["call"] = L.PreparedFused(self.ctx, d["table"], d["x"], d["y"],
                                                 torch.cuda.current_stream())
                 st[key] = d
@@ -399,7 +418,7 @@ class Bench:
             self.sets.append(st)
         # every set's call holds its arguments before the first step, so that no
         # first call (argument conversion) falls inside a timed region
-        if not self.is_merge and not self.device_ids:
+        if not self.is_merge and not self.is_proj and not self.device_ids:
             for st in self.sets:
                 for calls in self.steps_ids[:1]:
                     for key, ids in calls:
@@ -427,7 +446,10 @@ class Bench:
             self._call(st, t, key, ids, stream)
 
     def _call(self, st, t, key, ids, stream):
-        if self.device_ids:
+        if self.is_proj:
+            d = st[key]
+            self.L.lora_base_fused(self.ctx, d["table"], ids, d["x"], d["W"], d["y"], stream)
+        elif self.device_ids:
             d = st[key]
             self.L.lora_fused_device_ids(self.ctx, d["table"], st[("ids", t, key)], d["x"], d["y"],
                                          stream)
@@ -479,6 +501,14 @@ class Bench:
     def alg_bytes_family(self, i: int) -> dict:
         if self.is_merge:
             return {"merge": self.alg_bytes_step(i)}
+        if self.is_proj:
+            c = self.cases["main"]
+            ids = np.asarray(self.steps_ids[0][0][1])
+            sp = alg_bytes_split(c, ids, True)
+            n, d_in, d_out = c["n"], c["d_in"], c["d_out"]
+            b_pages = sp["expand"] - 4 * int((ids >= 0).sum()) * d_out
+            return {"shrink": sp["shrink"],
+                    "proj": 2 * n * d_in + 2 * d_in * d_out + 2 * n * d_out + b_pages}
         out = {}
         for k, ids in self.steps_ids[i % len(self.steps_ids)]:
             tiles = bool(self.paths.get(k, 1) & 2) and not (self.paths.get(k, 1) & 1)
@@ -486,7 +516,21 @@ class Bench:
                 out[f] = out.get(f, 0) + v
         return out
 
+    def flops_family(self, i: int) -> dict:
+        """Algorithmic flops per kernel family (the adapter term once, though the
+        tensor cores run it on both halves of s v)."""
+        if self.is_proj:
+            c = self.cases["main"]
+            ids = np.asarray(self.steps_ids[0][0][1])
+            act = ids[ids >= 0]
+            r = np.asarray(c["rank"])[act].astype(np.int64)
+            return {"shrink": int(2 * r.sum() * c["d_in"]),
+                    "proj": int(2 * c["n"] * c["d_in"] * c["d_out"] + 2 * r.sum() * c["d_out"])}
+        return {}
+
     def flops_step(self, i: int) -> int:
+        if self.is_proj:
+            return sum(self.flops_family(i).values())
         if self.is_merge:
             c = self.cases["main"]
             r = int(c["rank"][c["merge_adapter"]])
@@ -506,7 +550,11 @@ class Bench:
             self.host_in = torch.from_numpy(w.view(np.int16).reshape(-1)).pin_memory()
             self.out_elems = w.size
         else:
-            parts = [self.cases[k]["x"] for k in self.cases] + [self.cases[k]["y"] for k in self.cases]
+            # the step's inputs: x, and y where the call updates it in place (the base
+            # projection only writes y, so it copies x in alone)
+            parts = [self.cases[k]["x"] for k in self.cases]
+            if not self.is_proj:
+                parts += [self.cases[k]["y"] for k in self.cases]
             self.host_in = torch.from_numpy(
                 np.concatenate([p.view(np.int16).reshape(-1) for p in parts])).pin_memory()
             self.out_elems = self.blk_elems - self.y_offset
@@ -650,6 +698,18 @@ def oracle_sample(name: str, budget_s: float, nthreads: int):
         dt = time.perf_counter() - t0
         # one call = all d_in rows of W
         return done / c["d_in"], dt, f"merge of {done} W rows (of {c['d_in']} per call)"
+    if name == "valora_base_fused":
+        c = workloads.make("valora_prefill", seed=0)
+        W = workloads.make_W(c["d_in"], c["d_out"], seed=0)
+        t = oracle.Table.from_case(c)
+        done, chunk = 0, 512
+        t0 = time.perf_counter()
+        while time.perf_counter() - t0 < budget_s:
+            rows = np.arange(done, done + chunk) % c["n"]
+            oracle.base_fused(t, c["ids"], c["x"], W, nthreads=nthreads, rows=rows)
+            done += chunk
+        dt = time.perf_counter() - t0
+        return done, dt, f"{done} rows of the base projection with the adapter term, {chunk}-row chunks"
     if name == "llama7b_decode":
         parts = [workloads.make("llama7b_decode_het", seed=0),
                  workloads.make("llama7b_decode_hom", seed=0)]
@@ -735,22 +795,45 @@ def measure(name, K, W, args, L, torch, ctx, dist, world, local, clocks, cpu_bud
     for i in range(K):
         for f, v in b.alg_bytes_family(W + i).items():
             fam_bytes[f] = fam_bytes.get(f, 0) + v
+    fam_flops = {}
+    for i in range(K):
+        for f, v in b.flops_family(W + i).items():
+            fam_flops[f] = fam_flops.get(f, 0) + v
+    sec = ms / 1e3
+    # The base projection is a dense contraction: its roofline is the bf16 tensor
+    # peak (the sustained figure once the timed region runs for a quarter second or
+    # more, the burst figure below that); every other family is bound by HBM.
+    tc_peak = pk["bf16_tflops_sustained"] if sec >= 0.25 else pk["bf16_tflops"]
+    tc_src = "bf16_tflops_sustained" if sec >= 0.25 else "bf16_tflops"
     bracketed = sum(m for (m, n) in prof.values() if n)
     per_family = {}
     for f, (m, n) in prof.items():
         if n and m > 0:
-            share_s = (ms / 1e3) * (m / bracketed)
+            share_s = sec * (m / bracketed)
             gbs = fam_bytes.get(f, 0) / share_s / 1e9
-            per_family[f] = {"kernel": KERNEL_NAMES[f], "launches": n,
-                             "us_per_launch": round(1e6 * share_s / n, 3),
-                             "us_per_launch_bracketed": round(1e3 * m / n, 3),
-                             "alg_bytes_per_launch": fam_bytes.get(f, 0) / n,
-                             "GB/s": round(gbs, 1), "frac": round(gbs / pk["hbm_gbs"], 4),
-                             "traffic": None if b.device_ids else measured_traffic(name, f)}
+            e = {"kernel": KERNEL_NAMES[f], "launches": n,
+                 "us_per_launch": round(1e6 * share_s / n, 3),
+                 "us_per_launch_bracketed": round(1e3 * m / n, 3),
+                 "alg_bytes_per_launch": fam_bytes.get(f, 0) / n,
+                 "GB/s": round(gbs, 1), "frac": round(gbs / pk["hbm_gbs"], 4), "bound": "hbm",
+                 "traffic": None if b.device_ids else measured_traffic(name, f)}
+            if f == "proj":
+                tf = fam_flops.get(f, 0) / share_s / 1e12
+                e.update({"bound": "tensor", "alg_flops_per_launch": fam_flops.get(f, 0) / n,
+                          "TFLOP/s": round(tf, 1), "frac": round(tf / tc_peak, 4),
+                          "frac_of_hbm": round(gbs / pk["hbm_gbs"], 4)})
+            per_family[f] = e
     dominant = max(per_family, key=lambda f: prof[f][0])
-    achieved = per_family[dominant]["GB/s"]
+    dom = per_family[dominant]
+    if dom["bound"] == "tensor":
+        achieved, peak, unit_r = dom["TFLOP/s"], tc_peak, "TFLOP/s"
+        peak_src = (f"measured (MEASURED_PEAKS.json {tc_src}, cuBLAS bf16 GEMM)"
+                    if pk["source"] == "measured" else "fallback 1.9 PFLOP/s bf16")
+    else:
+        achieved, peak, unit_r = dom["GB/s"], pk["hbm_gbs"], "GB/s"
+        peak_src = ("measured (MEASURED_PEAKS.json hbm_gbs, STREAM-style copy)"
+                    if pk["source"] == "measured" else "fallback 6.8 TB/s")
     flops_total = sum(b.flops_step(W + i) for i in range(K))
-    sec = ms / 1e3
     if b.is_merge:
         value, unit = 2 * K * world / sec, "merge+unmerge calls/s"
     else:
@@ -760,11 +843,10 @@ def measure(name, K, W, args, L, torch, ctx, dist, world, local, clocks, cpu_bud
         "us_per_call": {"device": 1e6 * sec / max(1, calls),
                         "host_enqueue": round(host_enqueue_us, 3),
                         "per_kernel_launch": {f: v["us_per_launch"] for f, v in per_family.items()}},
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                     "frac": achieved / pk["hbm_gbs"] if achieved else None,
-                     "traffic": per_family[dominant]["traffic"],
-                     "peak_source": pk["source"] + " (MEASURED_PEAKS.json hbm_gbs, STREAM-style copy)"
-                     if pk["source"] == "measured" else "fallback 6.8 TB/s",
+        "roofline": {"bound": dom["bound"], "achieved": achieved, "peak": peak, "unit": unit_r,
+                     "frac": achieved / peak if achieved else None,
+                     "traffic": dom["traffic"],
+                     "peak_source": peak_src,
                      "kernel": KERNEL_NAMES[dominant],
                      "bytes_per_launch": per_family[dominant]["alg_bytes_per_launch"],
                      "us_per_launch": per_family[dominant]["us_per_launch"],

@@ -148,6 +148,24 @@ int lora_fused(lora_ctx *ctx, const lora_table *table, const int32_t *ids_host,
                int64_t n, const void *x, int64_t ldx, int d_in, void *y, int64_t ldy,
                int d_out, void *stream);
 
+/* Base projection with the adapter term fused into it (S-LoRA article, Batching: the
+ * batched base model x W plus the separately computed x A B, "formula 2"; VaLoRA
+ * blog, C2: the overhead of unmerged inference):
+ *     y_i = bf16( x_i . W + s_k (x_i . A_k) . B_k ),   k = ids[i] >= 0
+ *     y_i = bf16( x_i . W )                           ids[i] == -1 (released rows keep
+ *                                                     the backbone, LoRazor article)
+ * one bf16 rounding per output element.  x [n, ldx] bf16, W [d_in, ldw] bf16 (the
+ * base weight, row-major d_in x d_out, as for lora_merge), y [n, ldy] bf16 written
+ * (never read: every row of y is overwritten, released rows included).  The
+ * shrink kernels first write v = x_i A_k (fp32) into context scratch; then one
+ * tensor-core GEMM over 128 x 256 tiles accumulates x W and, in the same
+ * accumulator, the adapter terms of the tile's rows (s_k v as a pair of bf16
+ * operands, hi + lo, about 16 significant bits, times B_k).  Errors (nothing
+ * launched): as lora_fused, and LORA_E_INVAL for W. */
+int lora_base_fused(lora_ctx *ctx, const lora_table *table, const int32_t *ids_host,
+                    int64_t n, const void *x, int64_t ldx, int d_in, const void *W, int64_t ldw,
+                    void *y, int64_t ldy, int d_out, void *stream);
+
 /* Fused delta that allocates nothing.  Same operation, arguments and results as
  * lora_fused (within the same tolerance; the two may pick different summation
  * orders), for callers that must not allocate device or pinned memory while they
@@ -324,8 +342,8 @@ int lora_ctx_set_option(lora_ctx *ctx, int option, int value);
  * `every`-th kernel launch of the context (every >= 1) is bracketed by CUDA events
  * on its stream.  _end synchronizes on those events and returns, per kernel
  * family (0 row-gather, 1 tensor-core tile shrink, 2 merge, 3 tensor-core streaming
- * expand), the number of launches made while profiling in launches[] and their
- * device time in ms[] (arrays of 4): the mean of the bracketed launches times that
+ * expand, 4 base projection GEMM of lora_base_fused), the number of launches made
+ * while profiling in launches[] and their device time in ms[] (arrays of 5): the mean of the bracketed launches times that
  * number.  A call that first copies adapter pages into dense rows (dense.cu)
  * counts the copy in the family of the kernel that reads it. */
 int lora_profile_begin(lora_ctx *ctx, int every);
@@ -343,8 +361,9 @@ int lora_selftest_timeout(lora_ctx *ctx, int64_t limit_us, void *stream);
 int64_t lora_launch_count(const lora_ctx *ctx);
 
 /* Which kernel the last call launched: 0 none, 1 row-gather, 2 tensor-core tile,
- * 3 both (delta calls), 4 merge / unmerge, 8 page-in; and how many kernels it
- * launched. */
+ * 3 both (delta calls), 4 merge / unmerge, 8 page-in, 16 base projection GEMM (with
+ * the bits of the shrink kernels lora_base_fused launched before it); and how many
+ * kernels it launched. */
 int lora_last_path(const lora_ctx *ctx, int *n_launches);
 
 const char *lora_strerror(int code);
