@@ -908,12 +908,19 @@ int lora_ctx_create(int device, int64_t max_rows, int max_rank, lora_ctx **out)
         cudaSetDevice(prev);
         return LORA_E_CUDA;
     }
+    // Staging slots sized for any plan of up to max_rows rows (row items and the
+    // permutation, tile lists, base-projection terms and ids: at most 24 bytes a row
+    // and a little more), so that no call allocates in steady state.
+    const size_t slot_bytes = (size_t(max_rows) * 24u + 8192u + 255u) & ~size_t(255);
     for (Slot &s : ctx->slots) {
-        if (cudaEventCreateWithFlags(&s.ev, cudaEventDisableTiming) != cudaSuccess) {
+        if (cudaEventCreateWithFlags(&s.ev, cudaEventDisableTiming) != cudaSuccess ||
+            cudaMallocHost(reinterpret_cast<void **>(&s.host), slot_bytes) != cudaSuccess ||
+            cudaMalloc(reinterpret_cast<void **>(&s.dev), slot_bytes) != cudaSuccess) {
             lora_ctx_destroy(ctx);
             cudaSetDevice(prev);
             return LORA_E_CUDA;
         }
+        s.cap = slot_bytes;
     }
     // lora_fused_noalloc's fixed scratch: loading the module that holds it commits
     // its memory here, so that no lora_fused_noalloc call is the one that does.
@@ -1183,7 +1190,9 @@ int lora_base_fused(lora_ctx *ctx, const lora_table *t, const int32_t *ids, int6
                 return LORA_E_NOMEM;
             ctx->vrows_cap = need;
         }
-        rc = delta_call(ctx, t, kShrink, ids, n, x, ldx, d_in, ctx->vrows, ldv, nullptr, 0, 0,
+        // d_out: the call's, so that long runs take the tensor-core shrink and its
+        // launch shape comes from the tile table's entry for this shape
+        rc = delta_call(ctx, t, kShrink, ids, n, x, ldx, d_in, ctx->vrows, ldv, nullptr, 0, d_out,
                         stream);
         if (rc != LORA_OK)
             return rc;

@@ -9,8 +9,9 @@
 // accumulator, so y is written once and never read.)
 //
 // Persistent kernel, one CTA per SM, over the tiles (128-row block m, 256-column
-// block n) in row-major order (n fastest, so that the CTAs running at one time share
-// a few x blocks and sweep W, which stays in L2).  Per tile the accumulator (TMEM,
+// block n) in groups of 16 row blocks (row blocks fastest within a group, so that a
+// 256-column slice of W is fetched once per group and the group's x blocks stay in
+// L2).  Per tile the accumulator (TMEM,
 // 128 lanes x 256 fp32 columns, two of them so that one tile's epilogue overlaps the
 // next tile's MMAs) takes
 //   - the base: d_in / 64 stages of x block (128 x 64, K-major, 128-byte swizzle)
@@ -93,6 +94,21 @@ __device__ __forceinline__ bool named_bar_and(int id, int nthreads, bool v)
     return r != 0;
 }
 
+// Tile t of the launch: groups of kGroupM row blocks, each group swept over every
+// column block with its row blocks fastest, so that the CTAs running at one time
+// share a few x blocks and each 256-column slice of W is fetched from DRAM once per
+// group (x, W and y stay streaming; W is not assumed to stay in L2).
+constexpr int kGroupM = 16;
+__device__ __forceinline__ void tile_coords(const ProjParams &p, int t, int &m, int &nb)
+{
+    const int gsize = kGroupM * p.n_nblk;
+    const int g = t / gsize, local = t - g * gsize;
+    const int m0 = g * kGroupM;
+    const int gm = min(kGroupM, p.n_mblk - m0);
+    m = m0 + local % gm;
+    nb = local / gm;
+}
+
 // The stages of block m's adapter terms: for each term, hi then lo, each in chunks
 // of at most 64 of its padded rank.  f(term index, half, first column, K of stage).
 template <typename F>
@@ -161,7 +177,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_proj_tc(const __grid_constant__
         if (lane == 0) {
             uint32_t g = 0;
             for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
-                const int m = tile / p.n_nblk, n0 = (tile - m * p.n_nblk) * kBN, row0 = m * kBM;
+                int m, nb;
+                tile_coords(p, tile, m, nb);
+                const int n0 = nb * kBN, row0 = m * kBM;
                 const int natoms = min(4, (p.d_out - n0 + 63) / 64);   // 64-column boxes inside d_out
                 for (int kb = 0; kb < nkb && ok; ++kb, ++g) {
                     const int s = int(g % kNS);
@@ -211,7 +229,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_proj_tc(const __grid_constant__
             uint32_t g = 0;
             int lt = 0;
             for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x, ++lt) {
-                const int m = tile / p.n_nblk;
+                int m, nb;
+                tile_coords(p, tile, m, nb);
                 const int acc = lt & 1;
                 if (lt >= 2)
                     ok = mbar_wait_bounded(tempty0 + 8 * acc, ((lt >> 1) - 1) & 1, p.status,
@@ -256,7 +275,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_proj_tc(const __grid_constant__
         const int r_in = 32 * q4 + lane;               // this thread's row of the tile
         int lt = 0;
         for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++lt) {
-            const int m = tile / p.n_nblk, n0 = (tile - m * p.n_nblk) * kBN, row0 = m * kBM;
+            int m, nb;
+            tile_coords(p, tile, m, nb);
+            const int n0 = nb * kBN, row0 = m * kBM;
             const int acc = lt & 1;
             if (ok)
                 ok = mbar_wait_bounded(tfull0 + 8 * acc, (lt >> 1) & 1, p.status, kDevTimeoutMma);
@@ -304,7 +325,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_proj_tc(const __grid_constant__
         uint32_t g = 0;
         uint32_t uses[kNS] = {0, 0, 0, 0};   // adapter stages this thread has filled, per slot
         for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
-            const int m = tile / p.n_nblk, row0 = m * kBM;
+            int m, nb;
+            tile_coords(p, tile, m, nb);
+            const int row0 = m * kBM;
             const int row = row0 + vr;
             const int id = (p.ids && row < p.n) ? __ldg(p.ids + row) : -1;
             g += uint32_t(nkb);

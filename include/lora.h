@@ -100,8 +100,10 @@ typedef struct {
 } lora_plan_view;
 
 /* Create a context on `device` for batches of at most max_rows rows and adapters
- * of rank <= max_rank.  Allocates small pinned staging buffers, device plan
- * buffers and a device status word (owned by the context).  device = -1 makes a
+ * of rank <= max_rank.  Allocates eight pinned staging buffers of 24 * max_rows
+ * bytes (plus 8 KB) and their device copies (for the plans that do not travel in
+ * the launch parameters), device plan buffers and a device status word, all owned
+ * by the context, so that calls within max_rows allocate no staging memory.  device = -1 makes a
  * host-only context: plans, tables and tile files work, every launching call
  * returns LORA_E_UNSUPPORTED.  Fails with LORA_E_UNSUPPORTED on a device other
  * than compute capability 10.3. */
