@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cctype>
 #include <cmath>
 #include <cstdlib>
@@ -74,6 +75,27 @@ struct lora_ctx {
     size_t prof_used = 0;
     RowsParamsInline inline_args;   // staging of in-parameter plans
     RowsParamsInlineSmall inline_small;
+    // Launches of recent row-gather-only fused calls whose plan travelled in the
+    // parameters, by (table, shape, options, ids): a call repeating one of them (the
+    // same ids for every layer of a decode step) patches x and y and launches.
+    struct RowCacheEntry {
+        bool valid = false;
+        uint64_t table_sig = 0, tiles_gen = 0;
+        std::vector<int32_t> adapters;   // the plan's adapters (checked against the table)
+        int d_in = 0, d_out = 0;
+        int64_t n = 0;
+        std::vector<int32_t> ids;
+        bool small = true;
+        size_t smem = 0;
+        RowsParamsInlineSmall small_args;
+        std::unique_ptr<RowsParamsInline> big_args;
+        bool untuned = false;
+    };
+    RowCacheEntry rcache[4];
+    int rcache_next = 0;
+    bool rows_last_small = true;    // what run_rows launched last (in-parameter plans)
+    size_t rows_last_smem = 0;
+    bool rows_last_inline = false;
     int64_t launches_total = 0;     // every kernel launched by this context
     int prof_every = 1;             // bracket one launch in this many, per kernel family
     int64_t prof_seen[kFamilies] = {0, 0, 0, 0, 0};
@@ -106,6 +128,9 @@ struct lora_ctx {
 
 struct lora_table {
     lora_ctx *ctx = nullptr;           // the context it was registered with (not owned)
+    uint64_t serial = 0;               // unique per table created in this process
+    uint64_t sig = 0;                  // hash of what a row-gather plan depends on: adapter
+                                       // count, max rank, page widths, ranks, scales
     int device = -1;                   // device of the device copies (-1: host-only)
     const uint16_t *a_pool = nullptr;
     const uint16_t *b_pool = nullptr;
@@ -400,6 +425,9 @@ int run_rows(lora_ctx *ctx, const lora_table *t, int mode, RowsCfg cfg, const vo
     p.n_items = int(pl.row_items.size());
     p.early_pages = ctx->call_early;
     const long ev = prof_start(ctx, 0, stream);
+    ctx->rows_last_inline = in_params;
+    ctx->rows_last_smem = smem;
+    ctx->rows_last_small = in_params && pl.row_items.size() <= 64 && pl.row_perm.size() <= 128;
     if (in_params && pl.row_items.size() <= 64 && pl.row_perm.size() <= 128) {
         RowsParamsInlineSmall &a = ctx->inline_small;
         a.p = p;
@@ -700,6 +728,34 @@ int run_tiles(lora_ctx *ctx, const lora_table *t, int mode, const void *x, int64
     return slot ? release_slot(ctx, slot, stream) : LORA_OK;
 }
 
+// A repeat of a cached row-gather-only fused call: a table with the same signature
+// (ranks, scales, widths: a decode step's layers each have their own pools), the
+// same shape, options and ids (their contents).  Returns the entry or nullptr.
+lora_ctx::RowCacheEntry *rcache_find(lora_ctx *ctx, const lora_table *t, const int32_t *ids,
+                                     int64_t n, int d_in, int d_out)
+{
+    if (ctx->force_cluster > 0 || ctx->force_rows > 0)
+        return nullptr;
+    for (auto &e : ctx->rcache)
+        if (e.valid && e.table_sig == t->sig && e.n == n && e.d_in == d_in &&
+            e.d_out == d_out && e.tiles_gen == ctx->tiles.gen &&
+            std::memcmp(e.ids.data(), ids, size_t(n) * sizeof(int32_t)) == 0) {
+            // Same ranks and scales, possibly another table (another layer's pools):
+            // every adapter of the plan must be one this table can serve.
+            for (int32_t k : e.adapters)
+                if (t->status[size_t(k)] != LORA_OK)
+                    return nullptr;
+            return &e;
+        }
+    return nullptr;
+}
+
+void rcache_clear(lora_ctx *ctx)
+{
+    for (auto &e : ctx->rcache)
+        e.valid = false;
+}
+
 int delta_call(lora_ctx *ctx, const lora_table *t, int mode, const int32_t *ids, int64_t n,
                const void *x, int64_t ldx, int d_in, float *v, int64_t ldv, void *y,
                int64_t ldy, int d_out, cudaStream_t stream)
@@ -707,6 +763,42 @@ int delta_call(lora_ctx *ctx, const lora_table *t, int mode, const int32_t *ids,
     if (ctx) {
         ctx->last_path = ctx->last_launches = 0;
         begin_call(ctx, stream);
+    }
+    if (mode == kFused && ctx && t && t->ctx == ctx && n > 0 && ids && ctx->device >= 0) {
+        lora_ctx::RowCacheEntry *e = rcache_find(ctx, t, ids, n, d_in, d_out);
+        if (e) {
+            if (!stride_ok(x, ldx, d_in) || !stride_ok(y, ldy, d_out))
+                return LORA_E_INVAL;
+            int rc = use_device(ctx);
+            if (rc != LORA_OK)
+                return rc;
+            const long ev = prof_start(ctx, 0, stream);
+            auto patch = [&](RowsParams &q) {
+                q.x = static_cast<const uint16_t *>(x);
+                q.ldx = ldx;
+                q.y = static_cast<uint16_t *>(y);
+                q.ldy = ldy;
+                q.a_pool = t->a_pool;
+                q.b_pool = t->b_pool;
+                q.a_pages = t->d_a_pages;
+                q.b_pages = t->d_b_pages;
+                q.rank = t->d_rank;
+                q.scale = t->d_scale;
+                q.early_pages = ctx->call_early;
+            };
+            if (e->small) {
+                patch(e->small_args.p);
+                CUDA_TRY(ctx, launch_rows_inline_small(kFused, e->small_args, e->smem, stream));
+            } else {
+                patch(e->big_args->p);
+                CUDA_TRY(ctx, launch_rows_inline(kFused, *e->big_args, e->smem, stream));
+            }
+            prof_stop(ctx, ev, stream);
+            ctx->last_path = 1;
+            ctx->untuned = e->untuned;
+            count_launch(ctx, stream);
+            return LORA_OK;
+        }
     }
     int rc = prepare(ctx, t, ids, n);
     if (rc != LORA_OK)
@@ -757,7 +849,37 @@ int delta_call(lora_ctx *ctx, const lora_table *t, int mode, const int32_t *ids,
     rc = run_tiles(ctx, t, mode, x, ldx, d_in, v, ldv, y, ldy, d_out, n, stream);
     if (rc != LORA_OK)
         return rc;
-    return run_rows(ctx, t, mode, cfg, x, ldx, d_in, v, ldv, y, ldy, d_out, stream);
+    rc = run_rows(ctx, t, mode, cfg, x, ldx, d_in, v, ldv, y, ldy, d_out, stream);
+    // Keep the launch of a row-gather-only fused call whose plan travelled in the
+    // parameters, for the calls that repeat it.
+    if (rc == LORA_OK && mode == kFused && pl.tile_items.empty() && !pl.row_items.empty() &&
+        ctx->rows_last_inline && ctx->force_cluster == 0 && ctx->force_rows == 0) {
+        lora_ctx::RowCacheEntry &e = ctx->rcache[ctx->rcache_next];
+        ctx->rcache_next = (ctx->rcache_next + 1) % int(sizeof ctx->rcache / sizeof ctx->rcache[0]);
+        e.valid = false;
+        e.table_sig = t->sig;
+        e.adapters.assign(pl.seg_adapter.begin(), pl.seg_adapter.end());
+        e.tiles_gen = ctx->tiles.gen;
+        e.n = n;
+        e.d_in = d_in;
+        e.d_out = d_out;
+        e.ids.assign(ids, ids + n);
+        e.small = ctx->rows_last_small;
+        e.smem = ctx->rows_last_smem;
+        e.untuned = ctx->untuned;
+        if (e.small) {
+            e.small_args = ctx->inline_small;
+            e.valid = true;
+        } else {
+            if (!e.big_args)
+                e.big_args.reset(new (std::nothrow) RowsParamsInline());
+            if (e.big_args) {
+                *e.big_args = ctx->inline_args;
+                e.valid = true;
+            }
+        }
+    }
+    return rc;
 }
 
 int merge_call(lora_ctx *ctx, const lora_table *t, int adapter, void *W, int64_t ldw,
@@ -993,9 +1115,28 @@ int lora_table_create(lora_ctx *ctx, const void *a_pool, int64_t a_n_pages, int 
         (a_page_width % 8) || (b_page_width % 8) || n_adapters <= 0 || max_rank < 8 ||
         max_rank > LORA_MAX_RANK || !rank_host || !scale_host || !a_pages_host || !b_pages_host)
         return LORA_E_INVAL;
+    static std::atomic<uint64_t> serials{0};
     lora_table *t = new (std::nothrow) lora_table();
     if (!t)
         return LORA_E_NOMEM;
+    t->serial = ++serials;
+    {
+        // FNV-1a over the fields a row-gather plan and its launch shape depend on
+        // (not the pools or page ids: a cached launch patches those)
+        uint64_t h = 1469598103934665603ull;
+        auto mix = [&h](const void *d, size_t nb) {
+            const unsigned char *c = static_cast<const unsigned char *>(d);
+            for (size_t i = 0; i < nb; ++i) {
+                h ^= c[i];
+                h *= 1099511628211ull;
+            }
+        };
+        const int64_t head[4] = {n_adapters, max_rank, a_page_width, b_page_width};
+        mix(head, sizeof head);
+        mix(rank_host, size_t(n_adapters) * sizeof(int32_t));
+        mix(scale_host, size_t(n_adapters) * sizeof(float));
+        t->sig = h;
+    }
     t->ctx = ctx;
     t->device = ctx->device;
     t->a_pool = static_cast<const uint16_t *>(a_pool);
@@ -1582,6 +1723,7 @@ int lora_ctx_set_option(lora_ctx *ctx, int option, int value)
 {
     if (!ctx)
         return LORA_E_INVAL;
+    rcache_clear(ctx);
     switch (option) {
     case LORA_OPT_TILE_PATH: ctx->tile_path = value ? 1 : 0; return LORA_OK;
     case LORA_OPT_MERGE_KERNEL:

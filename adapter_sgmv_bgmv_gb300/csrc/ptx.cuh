@@ -121,6 +121,30 @@ __device__ __forceinline__ void cluster_sync()
     cluster_wait_acquire();
 }
 
+__device__ __forceinline__ void cluster_arrive_relaxed()
+{
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_cluster(uint32_t local_smem, uint32_t rank)
+{
+    uint32_t ra;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(local_smem), "r"(rank));
+    return ra;
+}
+
+// Asynchronous 16-byte store into a peer CTA's shared memory (cluster addresses of
+// the destination and of the peer's mbarrier): the bytes complete a transaction on
+// that mbarrier, which the peer waits on locally.
+__device__ __forceinline__ void st_async_v4(uint32_t remote_dst, float4 v, uint32_t remote_bar)
+{
+    asm volatile(
+        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];"
+        ::"r"(remote_dst), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(remote_bar)
+        : "memory");
+}
+
 // Read a float from the same shared-memory offset in CTA `rank` of the cluster.
 __device__ __forceinline__ float ld_dsmem_f32(const float *local, uint32_t rank)
 {

@@ -11,10 +11,14 @@
 //   2. shrink: partial v[i, j] over the CTA's d_in slice, half a warp per page (all
 //      pages of a rank <= 16 at once), 128-bit shared loads and a shuffle reduction,
 //      into the CTA's own shared memory;
-//   3. one cluster barrier, then every CTA reads all C partials with distributed
-//      shared memory loads and sums them in cluster-rank order (all CTAs get an
-//      identical v); a second barrier phase, waited on at exit, keeps each CTA's
-//      partial alive while its peers read it;
+//   3. every CTA pushes its partial into its C - 1 peers' shared memory with
+//      asynchronous remote stores (st.async) that complete bytes on the receiver's
+//      own mbarrier, waits on that mbarrier for the C - 1 partials addressed to it,
+//      and sums all C in cluster-rank order (all CTAs get an identical v).  The one
+//      cluster barrier (arrived at right after the mbarriers are set up, waited on
+//      before the first push) only makes every peer's mbarrier valid before anything
+//      is stored into it; no CTA leaves before all partials addressed to it have
+//      landed, so no barrier is needed at exit;
 //   4. expand: y[i, o] = bf16(y[i, o] + s_k * sum_j v[i, j] B_k[j, o]) for the CTA's
 //      d_out slice, 128-bit stores straight to the gathered rows.
 //
@@ -44,10 +48,11 @@ __host__ __device__ inline size_t carve(int mode, int si, int so, int rows, int 
     off[1] = o; o += has_in ? align16(size_t(rows) * si * 2) : 0;           // x rows
     off[2] = o; o += has_out ? align16(size_t(ranks) * so * 2) : 0;         // B slice
     off[3] = o; o += has_out ? align16(size_t(rows) * so * 2) : 0;          // y rows
-    off[4] = o; o += (has_in && cluster > 1) ? align16(size_t(rows) * ranks * 4) : 0;  // own partial
+    // own partial, then the C partials of the cluster (rank c at c * rows * ranks)
+    off[4] = o; o += (has_in && cluster > 1) ? align16(size_t(rows) * ranks * 4) * (1 + cluster) : 0;
     off[5] = o; o += align16(size_t(rows) * ranks * 4);                     // v
     off[6] = o; o += align16(size_t(rows) * 4);                             // the rows' indices
-    off[7] = o; o += 16;                                                    // 2 mbarriers
+    off[7] = o; o += 32;                                                    // 3 mbarriers
     return o;
 }
 
@@ -76,7 +81,9 @@ __device__ __forceinline__ void expand_vec(const uint16_t *sB, int slice_out, co
     }
 }
 
-template <int MODE>
+// DIRECT: the device-resident-ids mode (a kernel of its own, so that its id scan
+// costs the host-planned kernels no registers).
+template <int MODE, bool DIRECT>
 __device__ __forceinline__ void rows_body(const RowsParams &pin, const RowItem *items,
                                           const int32_t *perm)
 {
@@ -97,12 +104,13 @@ __device__ __forceinline__ void rows_body(const RowsParams &pin, const RowItem *
     int32_t *s_rows = reinterpret_cast<int32_t *>(smem + off[6]);   // perm[it.p0 + i]
     const uint32_t bar0 = smem_u32(smem + off[7]);
     const uint32_t bar1 = bar0 + 8;
+    const uint32_t xbar = bar0 + 16;              // the cluster's partials have landed
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const bool clustered = (MODE != kExpand) && C > 1;
     const int item_id = blockIdx.x / C;
     const uint32_t crank = clustered ? cluster_ctarank() : uint32_t(blockIdx.x % C);
-    const bool direct = p.ids_dev != nullptr;
+    constexpr bool direct = DIRECT;
     RowItem it;
     if (direct) {
         // Device-resident ids, one row per cluster: item i is row i, of the adapter
@@ -113,7 +121,8 @@ __device__ __forceinline__ void rows_body(const RowsParams &pin, const RowItem *
         // cluster shares its row, so all its CTAs leave together, before any barrier.
         if (!p.early_pages)
             grid_dep_wait();
-        const int ka = p.ids_dev[item_id];
+        const int row = item_id;
+        const int ka = p.ids_dev[row];
         if (ka == -1)
             return;
         if (ka < -1 || ka >= p.n_adapters || !p.ok[ka]) {
@@ -122,7 +131,7 @@ __device__ __forceinline__ void rows_body(const RowsParams &pin, const RowItem *
             return;
         }
         it.adapter = ka;
-        it.p0 = item_id;
+        it.p0 = row;
         it.nrows = 1;
         it.rank = int16_t(p.rank[ka]);
         it.scale = p.scale[ka];
@@ -148,12 +157,19 @@ __device__ __forceinline__ void rows_body(const RowsParams &pin, const RowItem *
     const int out0 = int(crank) * p.slice_out;
     const int out_len = max(0, min(p.d_out - out0, p.slice_out));
 
+    // The partials exchanged per CTA: nrows x RA floats, sent in 16-byte pieces.
+    const int xchunks = (nrows * RA + 3) >> 2;
     if (tid == 0) {
         mbar_init(bar0, 1);
         mbar_init(bar1, 1);
+        mbar_init(xbar, 1);
+        if (clustered)   // the C - 1 peers' partials (its own is copied locally)
+            mbar_arrive_expect_tx(xbar, uint32_t(C - 1) * uint32_t(xchunks) * 16u);
         fence_mbar_init();
     }
     __syncthreads();
+    if (clustered)
+        cluster_arrive_relaxed();   // this CTA's mbarriers are valid (waited on before the pushes)
 
     // ---- 1. copies.  Page ids come from the table (written once, at registration),
     // so they are read before waiting for the preceding kernel; everything it may
@@ -262,27 +278,34 @@ __device__ __forceinline__ void rows_body(const RowsParams &pin, const RowItem *
             }
         }
         if (clustered) {
-            // Every CTA's partial is in its own shared memory: one cluster barrier,
-            // then each CTA reads all C partials (distributed shared memory loads, all
-            // issued before any add) and sums them in cluster-rank order, so every
-            // CTA holds the same v.  A second barrier phase, arrived at here and
-            // waited on before exit, keeps each CTA's memory alive while peers read it.
-            cluster_sync();
+            // Push this CTA's partial into every peer of the cluster, at slot crank of
+            // their partials, once every peer's mbarrier is valid (and copy it into its
+            // own slot); then wait for the C - 1 partials addressed to this CTA and sum
+            // all C in cluster-rank order, so that every CTA holds the same v.
+            float *vall = vin + align16(size_t(p.rows_alloc) * RA * 4) / 4;
+            __syncthreads();                       // vin complete
+            cluster_wait_acquire();
+            const uint32_t dst0 = smem_u32(vall) + uint32_t(crank) * uint32_t(xchunks) * 16u;
+            for (int q = tid; q < C * xchunks; q += kThreads) {
+                const int c = q / xchunks, piece = q - c * xchunks;
+                const float4 val = reinterpret_cast<const float4 *>(vin)[piece];
+                if (c == int(crank))
+                    reinterpret_cast<float4 *>(vall)[size_t(c) * xchunks + piece] = val;
+                else
+                    st_async_v4(map_cluster(dst0 + uint32_t(piece) * 16u, uint32_t(c)), val,
+                                map_cluster(xbar, uint32_t(c)));
+            }
+            ok = mbar_wait_bounded(xbar, 0, p.status, kDevTimeoutLoad) && ok;
+            __syncthreads();                       // the local copy too
             for (int q = tid; q < nrows * r; q += kThreads) {
                 const int i = q / r, j = q - (q / r) * r;
-                float part[kMaxCluster];
-#pragma unroll
-                for (int c = 0; c < kMaxCluster; ++c)
-                    if (c < C)
-                        part[c] = ld_dsmem_f32(vin + i * RA + j, uint32_t(c));
                 float acc = 0.f;
 #pragma unroll
                 for (int c = 0; c < kMaxCluster; ++c)
                     if (c < C)
-                        acc += part[c];
+                        acc += vall[size_t(c) * (xchunks * 4) + i * RA + j];
                 vsum[i * RA + j] = acc;
             }
-            cluster_arrive_release();
         }
         __syncthreads();
         if (MODE == kShrink && ok && crank == 0) {
@@ -359,21 +382,19 @@ __device__ __forceinline__ void rows_body(const RowsParams &pin, const RowItem *
         if (MODE != kShrink)
             mbar_wait_bounded(bar1, 0, nullptr, 0);
     }
-    if (clustered)
-        cluster_wait_acquire();   // every peer has finished reading this CTA's partial
 }
 
-template <int MODE>
+template <int MODE, bool DIRECT>
 __global__ void __launch_bounds__(kThreads) k_rows(const __grid_constant__ RowsParams p)
 {
-    rows_body<MODE>(p, p.items, p.perm);
+    rows_body<MODE, DIRECT>(p, p.items, p.perm);
 }
 
 // Same kernel with the plan (items and permutation) in the parameter block.
 template <int MODE, typename Inline>
 __global__ void __launch_bounds__(kThreads) k_rows_inline(const __grid_constant__ Inline a)
 {
-    rows_body<MODE>(a.p, a.items, a.perm);
+    rows_body<MODE, false>(a.p, a.items, a.perm);
 }
 
 template <typename Kernel>
@@ -386,7 +407,7 @@ cudaError_t configure(Kernel k)
     return cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
 }
 
-template <int MODE, bool INLINE, typename Arg>
+template <int MODE, bool INLINE, typename Arg, bool DIRECT = false>
 cudaError_t launch_mode(const RowsParams &p, const Arg &arg, size_t smem, cudaStream_t stream)
 {
     static bool configured = false;
@@ -395,7 +416,7 @@ cudaError_t launch_mode(const RowsParams &p, const Arg &arg, size_t smem, cudaSt
         if constexpr (INLINE)
             e = configure(k_rows_inline<MODE, Arg>);
         else
-            e = configure(k_rows<MODE>);
+            e = configure(k_rows<MODE, DIRECT>);
         if (e != cudaSuccess)
             return e;
         configured = true;
@@ -418,7 +439,7 @@ cudaError_t launch_mode(const RowsParams &p, const Arg &arg, size_t smem, cudaSt
     if constexpr (INLINE)
         return cudaLaunchKernelEx(&cfg, k_rows_inline<MODE, Arg>, arg);
     else
-        return cudaLaunchKernelEx(&cfg, k_rows<MODE>, arg);
+        return cudaLaunchKernelEx(&cfg, k_rows<MODE, DIRECT>, arg);
 }
 
 }  // namespace
@@ -435,6 +456,8 @@ size_t rows_smem_bytes(int mode, int slice_in, int slice_out, int rows_alloc, in
 
 cudaError_t launch_rows(int mode, const RowsParams &p, size_t smem, cudaStream_t stream)
 {
+    if (p.ids_dev)   // device-resident ids: fused only
+        return launch_mode<kFused, false, RowsParams, true>(p, p, smem, stream);
     switch (mode) {
     case kShrink: return launch_mode<kShrink, false>(p, p, smem, stream);
     case kExpand: return launch_mode<kExpand, false>(p, p, smem, stream);

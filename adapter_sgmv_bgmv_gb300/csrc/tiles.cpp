@@ -44,6 +44,7 @@ int TileTable::load(const std::string &path)
     }
     for (auto &kv : fresh)
         map[kv.first] = kv.second;
+    ++gen;
     return LORA_OK;
 }
 

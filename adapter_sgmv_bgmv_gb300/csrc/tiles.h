@@ -51,7 +51,12 @@ struct TileTable {
         out = it->second;
         return true;
     }
-    void put(const TileKey &k, const TileCfg &c) { map[k] = c; }
+    void put(const TileKey &k, const TileCfg &c)
+    {
+        map[k] = c;
+        ++gen;
+    }
+    uint64_t gen = 0;                         // bumped by every change (put, load)
     int load(const std::string &path);        // LORA_OK / LORA_E_IO / LORA_E_INVAL
     int save(const std::string &path) const;
 };

@@ -1026,7 +1026,11 @@ def main():
     ap.add_argument("--tiles", default=os.path.join(ROOT, "adapter_sgmv_bgmv_gb300", "tiles.tbl"))
     ap.add_argument("--device-ids", action="store_true",
                     help="decode workloads through lora_fused_device_ids (ids in device memory)")
+    ap.add_argument("--probe", choices=PROBES, default=None,
+                    help="run one workload's call a few times for a profiler, print nothing")
     args = ap.parse_args()
+    if args.probe:
+        return run_probe(args.probe)
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -1084,6 +1088,82 @@ def main():
     if dist is not None:
         dist.barrier()
         dist.destroy_process_group()
+    return 0
+
+
+PROBES = ("valora", "slora", "llama_het", "llama_hom", "lorazor", "merge_tc", "merge_simt",
+          "proj", "page_in", "plan_dev", "device_ids")
+
+
+def run_probe(name: str) -> int:
+    """One workload's library call, a few times, on one set of device buffers (a
+    target for a profiler's capture of one kernel: `ncu -k regex:<kernel> -s 1 -c 1
+    python bench.py --probe <name>`).  Prints nothing; exits 0 when the calls and the
+    status check succeed."""
+    import torch
+    import adapter_sgmv_bgmv_gb300 as L
+    from tests.gpu_util import to_dev, upload_table
+    ctx = L.Context(0, max_rows=1 << 15, max_rank=64)
+    tiles = os.path.join(ROOT, "adapter_sgmv_bgmv_gb300", "tiles.tbl")
+    if os.path.exists(tiles):
+        ctx.tiles_load(tiles)
+    ctx.set_option(L.OPT_EARLY_PAGES, 1)
+
+    def n_sets(step_bytes):
+        # copies enough that a pass over them is more than 3 x L2: the call a profiler
+        # captures (the second) reads cold HBM, as in the timed loop
+        return int(min(16, max(2, math.ceil(3 * L2_BYTES / max(1, step_bytes)))))
+
+    def fused(case, ids):
+        sets = [(upload_table(ctx, case), to_dev(case["x"]), to_dev(case["y"]))
+                for _ in range(n_sets(alg_bytes_delta(case, ids)))]
+        for t, x, y in sets + sets[:1]:
+            L.lora_fused(ctx, t, ids, x, y)
+
+    if name in ("valora", "slora"):
+        c = workloads.make(f"{name}_prefill", seed=0)
+        fused(c, c["ids"])
+    elif name in ("llama_het", "llama_hom"):
+        c = workloads.make(f"llama7b_decode_{name[6:]}", seed=0)
+        fused(c, c["ids"])
+    elif name == "lorazor":
+        c = workloads.make("lorazor_decode", seed=0)
+        fused(c, workloads.lorazor_ids(c, 0))
+    elif name in ("merge_tc", "merge_simt"):
+        ctx.set_option(L.OPT_MERGE_KERNEL, 0 if name == "merge_tc" else 1)
+        c = workloads.make("valora_merge", seed=0)
+        sets = [(upload_table(ctx, c), to_dev(c["W"])) for _ in range(n_sets(4 * c["W"].size))]
+        for t, W in sets:
+            L.lora_merge(ctx, t, c["merge_adapter"], W)
+            L.lora_unmerge(ctx, t, c["merge_adapter"], W)
+    elif name == "proj":
+        c = workloads.make("valora_prefill", seed=0)
+        W = to_dev(workloads.make_W(c["d_in"], c["d_out"], seed=0))
+        t = upload_table(ctx, c)
+        x = to_dev(c["x"])
+        y = torch.empty((c["n"], c["d_out"]), dtype=torch.bfloat16, device="cuda")
+        for _ in range(3):
+            L.lora_base_fused(ctx, t, c["ids"], x, W, y)
+    elif name == "page_in":
+        c = workloads.small(seed=1, n=1, d_in=4096, d_out=4096, n_adapters=32, ranks=[64] * 32,
+                            paged=True)
+        t = upload_table(ctx, c)
+        ha = torch.zeros((64, 4096), dtype=torch.int16).pin_memory()
+        hb = torch.zeros((64, 4096), dtype=torch.int16).pin_memory()
+        for k in range(8):
+            L.lora_page_in(ctx, t, k, ha, hb)
+    elif name in ("plan_dev", "device_ids"):
+        ctx.set_option(L.OPT_DEVICE_PLAN, 1 if name == "plan_dev" else 0)
+        c = workloads.make("lorazor_decode", seed=0)
+        ids_h = workloads.lorazor_ids(c, 0)
+        ids = torch.from_numpy(np.ascontiguousarray(ids_h, np.int32)).cuda()
+        sets = [(upload_table(ctx, c), to_dev(c["x"]), to_dev(c["y"]))
+                for _ in range(n_sets(alg_bytes_delta(c, ids_h)))]
+        for t, x, y in sets + sets[:1]:
+            L.lora_fused_device_ids(ctx, t, ids, x, y)
+    torch.cuda.synchronize()
+    ctx.sync_status()
+    ctx.close()
     return 0
 
 

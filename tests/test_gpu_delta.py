@@ -350,3 +350,65 @@ def test_a_wait_that_runs_out_is_reported_and_the_context_stays_usable(ctx):
     got = run_fused(ctx, c)
     ref = oracle.fused(oracle.Table.from_case(c), c["ids"], c["x"], c["y"], nthreads=8)
     assert_parity(got, ref, REL_FROB, MAX_ABS_RMS, "after a timed-out wait")
+
+
+def test_repeated_ids_over_new_buffers_reuse_the_launch_and_stay_exact(ctx):
+    """A decode step applies one ids array to every layer, each with its own adapter
+    pools: the library keeps the launch of a row-gather call and, when a table with
+    the same ranks and scales, the same shape and the same ids come back, patches
+    the pools, x and y and launches.  Results must be bit-identical to a context
+    that plans every call -- across layers (each its own tables and x / y),
+    alternation between two batches, an option change and a tile-table reload in
+    between, and ids rewritten in place -- and a table that cannot serve an adapter
+    of the plan is refused, not served from the cache."""
+    import os
+    fresh = L.Context(0, max_rows=1 << 15, max_rank=64)
+    try:
+        rng = np.random.default_rng(5)
+        ids_het = np.ascontiguousarray(workloads.make("llama7b_decode_het", seed=11)["ids"],
+                                       np.int32).copy()
+        ids_hom = np.zeros(64, np.int32)
+        for layer in range(6):
+            # this layer's adapters: the same ranks and scales, new weights
+            het = workloads.make("llama7b_decode_het", seed=20 + layer)
+            hom = workloads.make("llama7b_decode_hom", seed=20 + layer)
+            xs = workloads.to_bf16_bits(rng.standard_normal((64, 4096), dtype=np.float32))
+            for case, ids_c in ((het, ids_het), (hom, ids_hom)):
+                t, f = upload_table(ctx, case), upload_table(fresh, case)
+                x = to_dev(xs)
+                y_a, y_b = to_dev(case["y"]), to_dev(case["y"])
+                L.lora_fused(ctx, t, ids_c, x, y_a)          # cached after the first layer
+                fresh.set_option(L.OPT_TILE_PATH, 1)         # clears the fresh context's cache
+                L.lora_fused(fresh, f, ids_c, x, y_b)
+                ctx.sync_status()
+                fresh.sync_status()
+                np.testing.assert_array_equal(from_dev(y_a), from_dev(y_b))
+                if layer in (0, 5):
+                    ref = oracle.fused(oracle.Table.from_case(case), ids_c, xs, case["y"], nthreads=8)
+                    assert_parity(from_dev(y_a), ref, REL_FROB, MAX_ABS_RMS, f"layer {layer}")
+            # both contexts always run the same configuration (a different cluster
+            # width would change the split-K summation order)
+            if layer == 2:
+                for c_ in (ctx, fresh):
+                    c_.set_option(L.OPT_EARLY_PAGES, 1)
+            if layer == 3:
+                tbl = os.path.join(os.path.dirname(L.__file__), "tiles.tbl")
+                if os.path.exists(tbl):
+                    for c_ in (ctx, fresh):
+                        c_.tiles_load(tbl)
+            if layer == 4:
+                ids_het[::5] = -1                            # the same buffer, new contents
+        # same ranks and scales, but adapter ids_hom[0] = 0 is not resident here
+        bad = workloads.make("llama7b_decode_hom", seed=99)
+        ap = bad["a_pages"].copy()
+        ap[0, 0] = -1
+        tb = upload_table(ctx, dict(bad, a_pages=ap))
+        y = to_dev(bad["y"])
+        with pytest.raises(L.LoraError) as e:
+            L.lora_fused(ctx, tb, ids_hom, to_dev(bad["x"]), y)
+        assert e.value.name == "LORA_E_NOT_RESIDENT"
+        ctx.sync_status()
+        np.testing.assert_array_equal(from_dev(y), bad["y"])
+    finally:
+        ctx.set_option(L.OPT_EARLY_PAGES, 0)
+        fresh.close()
