@@ -221,6 +221,11 @@ class AdapterTable:
         self.handle = h.value
         ctx._tables.add(self)
 
+    def invalidate(self, adapter: int = -1):
+        """The pages of `adapter` (-1: every adapter) were written outside lora_page_in:
+        the table's dense copy of them is stale (see include/lora.h)."""
+        _check(_L.lora_table_invalidate(self.handle, int(adapter)))
+
     def close(self):
         if getattr(self, "handle", None):
             _L.lora_table_destroy(self.handle)

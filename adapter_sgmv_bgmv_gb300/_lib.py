@@ -30,6 +30,7 @@ SIGNATURES = {
     "lora_ctx_destroy": ([P], I),
     "lora_table_create": ([P, P, I64, I, P, I64, I, I, I, P, P, P, P, ctypes.POINTER(P)], I),
     "lora_table_destroy": ([P], I),
+    "lora_table_invalidate": ([P, I], I),
     "lora_plan_build": ([P, P, P, I64, ctypes.POINTER(PlanView)], I),
     "lora_shrink": ([P, P, P, I64, P, I64, I, P, I64, P], I),
     "lora_expand": ([P, P, P, I64, P, I64, P, I64, I, P], I),

@@ -145,6 +145,14 @@ struct lora_table {
     float *d_scale = nullptr;
     uint8_t *d_ok = nullptr;           // per adapter: 1 when its status is LORA_OK
     int rank_max_ok = 0;               // largest rank among the adapters it can serve
+    // Dense rows of the adapters whose pages the tensor-core kernels cannot read as
+    // they are (scattered pages, or a rank not a multiple of 16): one slot of rp
+    // rows per adapter, full pages (widths a_pw / b_pw), copied once and kept until
+    // the adapter's pages change (lora_page_in, lora_table_invalidate).
+    uint16_t *dense_a = nullptr, *dense_b = nullptr;
+    int dense_cap = 0, dense_used = 0, dense_rp = 0;
+    std::vector<int32_t> dense_slot;   // adapter -> slot, -1 none
+    std::vector<uint8_t> dense_valid;  // adapter -> its slot holds its current pages
 };
 
 namespace {
@@ -475,6 +483,12 @@ struct RowMats {
     bool staged = false;
     bool early = false;             // the copy may run before the previous kernel ends
     int rp = 0;
+    // The copies to make: adapter stage_adapter[i] into slot stage_slot[i], widths and
+    // row strides of the destination (the per-call scratch: the call's widths; the
+    // table's cache: full pages).
+    std::vector<int32_t> stage_adapter, stage_slot;
+    int a_width = 0, b_width = 0;
+    bool stage_a = false, stage_b = false;
 };
 
 // Bytes of the dense rows setup_rows would make for these adapters (0 when the
@@ -497,14 +511,93 @@ size_t dense_rows_bytes(const lora_table *t, const int32_t *adapters, int n_slot
     return a_bytes + (need_b ? size_t(n_slots) * rp * size_t(d_out) * 2u : 0);
 }
 
+// The table's cache of dense rows, for the adapters of a tensor-core call: make
+// room (a grow copies the slots kept), give every adapter without a slot one, and
+// list the copies of the adapters whose slot is not current.  Returns
+// LORA_E_CAPACITY when the cache would pass kDenseCacheBytes (the call then stages
+// into per-call scratch).
+constexpr size_t kDenseCacheBytes = size_t(1) << 30;
+
+int cache_rows(lora_ctx *ctx, lora_table *t, const int32_t *adapters, int n_slots,
+               cudaStream_t stream, RowMats *m, int32_t *a_base, int32_t *b_base)
+{
+    if (t->dense_rp == 0)
+        t->dense_rp = (t->max_rank + 15) & ~15;
+    const int rp = t->dense_rp;
+    const size_t slot_bytes = size_t(rp) * (size_t(t->a_pw) + size_t(t->b_pw)) * 2u;
+    if (t->dense_slot.empty()) {
+        t->dense_slot.assign(size_t(t->n_adapters), -1);
+        t->dense_valid.assign(size_t(t->n_adapters), 0);
+    }
+    int need = t->dense_used;
+    for (int s = 0; s < n_slots; ++s)
+        if (t->dense_slot[size_t(adapters[s])] < 0)
+            ++need;
+    if (size_t(need) * slot_bytes > kDenseCacheBytes)
+        return LORA_E_CAPACITY;
+    if (need > t->dense_cap) {
+        int cap = std::max(16, t->dense_cap);
+        while (cap < need)
+            cap *= 2;
+        uint16_t *na = nullptr, *nb = nullptr;
+        if (cudaMalloc(reinterpret_cast<void **>(&na), size_t(cap) * rp * t->a_pw * 2u) != cudaSuccess)
+            return LORA_E_NOMEM;
+        if (cudaMalloc(reinterpret_cast<void **>(&nb), size_t(cap) * rp * t->b_pw * 2u) != cudaSuccess) {
+            cudaFree(na);
+            return LORA_E_NOMEM;
+        }
+        if (t->dense_used > 0) {
+            CUDA_TRY(ctx, cudaMemcpyAsync(na, t->dense_a, size_t(t->dense_used) * rp * t->a_pw * 2u,
+                                          cudaMemcpyDeviceToDevice, stream));
+            CUDA_TRY(ctx, cudaMemcpyAsync(nb, t->dense_b, size_t(t->dense_used) * rp * t->b_pw * 2u,
+                                          cudaMemcpyDeviceToDevice, stream));
+        }
+        // the old buffers may still be read by launches queued before this call
+        CUDA_TRY(ctx, cudaStreamSynchronize(stream));
+        cudaFree(t->dense_a);
+        cudaFree(t->dense_b);
+        t->dense_a = na;
+        t->dense_b = nb;
+        t->dense_cap = cap;
+    }
+    m->stage_adapter.clear();
+    m->stage_slot.clear();
+    for (int s = 0; s < n_slots; ++s) {
+        const size_t k = size_t(adapters[s]);
+        if (t->dense_slot[k] < 0)
+            t->dense_slot[k] = t->dense_used++;
+        if (!t->dense_valid[k]) {
+            m->stage_adapter.push_back(int32_t(k));
+            m->stage_slot.push_back(t->dense_slot[k]);
+            t->dense_valid[k] = 1;   // current once the copy queued below has run
+        }
+        a_base[s] = b_base[s] = t->dense_slot[k] * rp;
+    }
+    m->staged = !m->stage_adapter.empty();
+    m->early = false;                // the copy waits for the kernel before it
+    m->rp = rp;
+    m->a = t->dense_a;
+    m->a_ld = t->a_pw;
+    m->a_nrows = int64_t(t->dense_cap) * rp;
+    m->b = t->dense_b;
+    m->b_ld = t->b_pw;
+    m->b_nrows = int64_t(t->dense_cap) * rp;
+    m->a_width = t->a_pw;
+    m->b_width = t->b_pw;
+    m->stage_a = m->stage_b = true;  // a slot holds both sides
+    return LORA_OK;
+}
+
 // own: a caller-sized buffer for the dense rows (instead of the context's two halves
 // or the fixed array), with room for dense_rows_bytes; its copy waits for the kernel
 // before it (no early staging).
-int setup_rows(lora_ctx *ctx, const lora_table *t, const int32_t *adapters, int n_slots,
+int setup_rows(lora_ctx *ctx, const lora_table *tc, const int32_t *adapters, int n_slots,
                int d_in, int d_out, bool need_a, bool need_b, const NoAllocScratch *fixed,
                cudaStream_t stream, RowMats *m, int32_t *a_base, int32_t *b_base,
                uint8_t *own = nullptr)
 {
+    // The table's dense-row cache is the table's own state, kept across calls.
+    lora_table *t = const_cast<lora_table *>(tc);
     bool direct = true;
     int rmax = 0;
     for (int s = 0; s < n_slots; ++s) {
@@ -529,6 +622,19 @@ int setup_rows(lora_ctx *ctx, const lora_table *t, const int32_t *adapters, int 
     const int rp = (rmax + 15) & ~15;
     const size_t a_bytes = need_a ? (size_t(n_slots) * rp * size_t(d_in) * 2u + 255u) & ~size_t(255) : 0;
     const size_t bytes = a_bytes + (need_b ? size_t(n_slots) * rp * size_t(d_out) * 2u : 0);
+    if (!fixed && !own) {
+        int rc = cache_rows(ctx, t, adapters, n_slots, stream, m, a_base, b_base);
+        if (rc != LORA_E_CAPACITY)
+            return rc;   // served from the table's cache (or an error); else per call
+    }
+    m->stage_adapter.assign(adapters, adapters + n_slots);
+    m->stage_slot.resize(size_t(n_slots));
+    for (int s = 0; s < n_slots; ++s)
+        m->stage_slot[size_t(s)] = s;
+    m->a_width = d_in;
+    m->b_width = d_out;
+    m->stage_a = need_a;
+    m->stage_b = need_b;
     uint8_t *buf = nullptr;
     if (own) {
         buf = own;
@@ -569,27 +675,28 @@ int setup_rows(lora_ctx *ctx, const lora_table *t, const int32_t *adapters, int 
 }
 
 // The copies setup_rows asked for (a no-op for the pools themselves).
-int run_staging(lora_ctx *ctx, const lora_table *t, const RowMats &m, const int32_t *adapters,
-                int n_slots, int d_in, int d_out, bool need_a, bool need_b, cudaStream_t stream)
+int run_staging(lora_ctx *ctx, const lora_table *t, const RowMats &m, cudaStream_t stream)
 {
     if (!m.staged)
         return LORA_OK;
-    for (int s0 = 0; s0 < n_slots; s0 += kStageSlots) {
+    const int n = int(m.stage_adapter.size());
+    for (int s0 = 0; s0 < n; s0 += kStageSlots) {
         StageArgs sa{};
         sa.max_rank = t->max_rank;
         sa.rp = m.rp;
         sa.early = m.early ? 1 : 0;
-        sa.n_slots = std::min(kStageSlots, n_slots - s0);
+        sa.n_slots = std::min(kStageSlots, n - s0);
         for (int s = 0; s < sa.n_slots; ++s) {
-            sa.adapter[s] = adapters[s0 + s];
-            sa.rank[s] = t->rank[size_t(adapters[s0 + s])];
+            sa.adapter[s] = m.stage_adapter[size_t(s0 + s)];
+            sa.rank[s] = t->rank[size_t(sa.adapter[s])];
+            sa.dst_slot[s] = m.stage_slot[size_t(s0 + s)];
         }
-        if (need_a)
-            sa.side[0] = StageSide{t->a_pool, t->a_pw, t->d_a_pages,
-                                   const_cast<uint16_t *>(m.a) + int64_t(s0) * m.rp * d_in, d_in};
-        if (need_b)
-            sa.side[1] = StageSide{t->b_pool, t->b_pw, t->d_b_pages,
-                                   const_cast<uint16_t *>(m.b) + int64_t(s0) * m.rp * d_out, d_out};
+        if (m.stage_a)
+            sa.side[0] = StageSide{t->a_pool, t->a_pw, t->d_a_pages, const_cast<uint16_t *>(m.a),
+                                   m.a_width, m.a_ld};
+        if (m.stage_b)
+            sa.side[1] = StageSide{t->b_pool, t->b_pw, t->d_b_pages, const_cast<uint16_t *>(m.b),
+                                   m.b_width, m.b_ld};
         CUDA_TRY(ctx, launch_stage_rows(sa, stream));
         count_launch(ctx, stream);
     }
@@ -706,7 +813,7 @@ int run_tiles(lora_ctx *ctx, const lora_table *t, int mode, const void *x, int64
     // The dense copy (if any) is timed with the kernel that first reads it.
     if (mode != kExpand) {
         const long ev = prof_start(ctx, 1, stream);
-        rc = run_staging(ctx, t, mats, slots.data(), n_slots, d_in, d_out, need_a, need_b, stream);
+        rc = run_staging(ctx, t, mats, stream);
         if (rc != LORA_OK)
             return rc;
         CUDA_TRY(ctx, launch_shrink_tc(p, stream));
@@ -716,7 +823,7 @@ int run_tiles(lora_ctx *ctx, const lora_table *t, int mode, const void *x, int64
     if (mode != kShrink) {
         const long ev = prof_start(ctx, 3, stream);
         if (mode == kExpand) {
-            rc = run_staging(ctx, t, mats, slots.data(), n_slots, d_in, d_out, need_a, need_b, stream);
+            rc = run_staging(ctx, t, mats, stream);
             if (rc != LORA_OK)
                 return rc;
         }
@@ -939,7 +1046,7 @@ int merge_call(lora_ctx *ctx, const lora_table *t, int adapter, void *W, int64_t
     }
     const long ev = prof_start(ctx, 2, stream);
     if (tc) {
-        rc = run_staging(ctx, t, mats, &adapter, 1, d_in, d_out, true, true, stream);
+        rc = run_staging(ctx, t, mats, stream);
         if (rc != LORA_OK)
             return rc;
         CUDA_TRY(ctx, launch_merge_tc(p, 0, stream));
@@ -1211,6 +1318,19 @@ int lora_table_create(lora_ctx *ctx, const void *a_pool, int64_t a_n_pages, int 
     return LORA_OK;
 }
 
+int lora_table_invalidate(lora_table *t, int adapter)
+{
+    if (!t || adapter < -1 || adapter >= t->n_adapters)
+        return LORA_E_INVAL;
+    if (t->dense_valid.empty())
+        return LORA_OK;
+    if (adapter == -1)
+        std::fill(t->dense_valid.begin(), t->dense_valid.end(), uint8_t(0));
+    else
+        t->dense_valid[size_t(adapter)] = 0;
+    return LORA_OK;
+}
+
 int lora_table_destroy(lora_table *t)
 {
     if (!t)
@@ -1230,6 +1350,8 @@ int lora_table_destroy(lora_table *t)
     cudaFree(t->d_a_pages);
     cudaFree(t->d_b_pages);
     cudaFree(t->d_ok);
+    cudaFree(t->dense_a);
+    cudaFree(t->dense_b);
     cudaSetDevice(prev);
     delete t;
     return LORA_OK;
@@ -1413,7 +1535,7 @@ int lora_base_fused(lora_ctx *ctx, const lora_table *t, const int32_t *ids, int6
                                   cudaMemcpyHostToDevice, stream));
     const long ev = prof_start(ctx, 4, stream);
     if (n_slots > 0) {
-        rc = run_staging(ctx, t, mats, slots.data(), n_slots, d_in, d_out, false, true, stream);
+        rc = run_staging(ctx, t, mats, stream);
         if (rc != LORA_OK)
             return rc;
     }
@@ -1658,6 +1780,10 @@ int lora_page_in(lora_ctx *ctx, const lora_table *t, int adapter, const void *ho
         a.side[1].page[j] = t->b_pages[size_t(adapter) * t->max_rank + j];
     }
     CUDA_TRY(ctx, launch_page_in(a, stream));
+    // the adapter's dense rows (if the table keeps them) no longer match its pages
+    lora_table *tw = const_cast<lora_table *>(t);
+    if (!tw->dense_valid.empty())
+        tw->dense_valid[size_t(adapter)] = 0;
     ctx->last_path = 8;
     ctx->last_launches = 1;
     ctx->launches_total += 1;

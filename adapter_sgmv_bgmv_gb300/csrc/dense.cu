@@ -6,10 +6,12 @@
 // by page it would be one gather per four pages, and the TMA unit issues those
 // too slowly to keep up with the x / y streams.  When every adapter of a call has
 // consecutive pages of a rank that is a multiple of 16, the pools are used as they
-// are.  Otherwise this kernel copies the call's adapters (S-LoRA's unified pool
-// holds them in arbitrary pages) into a dense scratch, one slot of rp rows per
-// adapter: its rank's rows, then zeros up to the rank rounded up to 16 (the rows
-// the tensor-core kernels read); the slot's rows beyond those are left unwritten.
+// are.  Otherwise this kernel copies adapters (S-LoRA's unified pool holds them in
+// arbitrary pages) into dense rows, one slot of rp rows per adapter: its rank's
+// rows, then zeros up to the rank rounded up to 16 (the rows the tensor-core
+// kernels read); the slot's rows beyond those are left unwritten.  The slots are
+// the table's cache of dense rows (each adapter copied once, until its pages
+// change) or, where that cannot serve, a per-call scratch.
 #include <cuda_runtime.h>
 
 #include "internal.h"
@@ -22,7 +24,8 @@ namespace {
 constexpr int kStageThreads = 128;
 constexpr int kPerThread = 8;                 // 16-byte vectors per thread per pass
 
-// Destination row blockIdx.x = slot * rp + j of side blockIdx.y.
+// Row j of entry blockIdx.x / rp, side blockIdx.y: destination row
+// dst_slot[entry] * rp + j, of dst_ld elements.
 __device__ __forceinline__ void stage_row(const StageArgs &a)
 {
     const StageSide &sd = a.side[blockIdx.y];
@@ -34,7 +37,7 @@ __device__ __forceinline__ void stage_row(const StageArgs &a)
     if (j >= ((rank + 15) & ~15))   // the kernels read a slot's rank rounded up to 16 rows
         return;
     const int nv = sd.width / 8;
-    uint4 *dst = reinterpret_cast<uint4 *>(sd.dst + int64_t(row) * sd.width);
+    uint4 *dst = reinterpret_cast<uint4 *>(sd.dst + (int64_t(a.dst_slot[slot]) * a.rp + j) * sd.dst_ld);
     if (j < rank) {
         const int32_t page = sd.pages[int64_t(a.adapter[slot]) * a.max_rank + j];
         const uint4 *src = reinterpret_cast<const uint4 *>(sd.pool + int64_t(page) * sd.pw);

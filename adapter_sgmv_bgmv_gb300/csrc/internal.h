@@ -158,17 +158,19 @@ struct StageSide {
     const uint16_t *pool;
     int64_t pw;
     const int32_t *pages;     // device page table [n_adapters * max_rank]
-    uint16_t *dst;            // [n_slots * rp][width]
-    int width;
+    uint16_t *dst;            // rows of dst_ld elements; slot s at row s * rp
+    int width;                // elements copied per row (<= pw, <= dst_ld)
+    int64_t dst_ld;
 };
 struct StageArgs {
     StageSide side[2];        // A, B (side with dst == nullptr skipped)
     int max_rank;
     int rp;
-    int n_slots;
+    int n_slots;              // entries of this launch
     int early;                // copy before waiting for the previous kernel (dense.cu)
     int32_t adapter[kStageSlots];
     int32_t rank[kStageSlots];
+    int32_t dst_slot[kStageSlots];   // destination slot of entry s
 };
 cudaError_t launch_stage_rows(const StageArgs &a, cudaStream_t stream);
 

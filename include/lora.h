@@ -124,6 +124,18 @@ int lora_table_create(lora_ctx *ctx, const void *a_pool, int64_t a_n_pages,
                       lora_table **out);
 int lora_table_destroy(lora_table *table);
 
+/* The tensor-core kernels read an adapter as consecutive rows.  For an adapter whose
+ * pages are scattered in the pool (S-LoRA's unified paging), or whose rank is not a
+ * multiple of 16, the table keeps a dense copy of its pages (full pages, rank padded
+ * to 16 with zero rows, up to 1 GB per table; beyond that a call copies its adapters
+ * into per-call scratch), made by the first tensor-core call that needs it and used
+ * by every later one, so that a steady-state prefill call launches no copy.
+ * lora_page_in marks its adapter's copy stale.  A caller that writes pool pages in
+ * any other way must call this for the adapters it changed (adapter = -1: all)
+ * before the next call on the table; the next tensor-core call then copies them
+ * again.  Host-only; LORA_E_INVAL for a bad table or adapter. */
+int lora_table_invalidate(lora_table *table, int adapter);
+
 /* Host-only: build the plan for ids_host[n] and expose it (for inspection). */
 int lora_plan_build(lora_ctx *ctx, const lora_table *table, const int32_t *ids_host,
                     int64_t n, lora_plan_view *out);

@@ -412,3 +412,55 @@ def test_repeated_ids_over_new_buffers_reuse_the_launch_and_stay_exact(ctx):
     finally:
         ctx.set_option(L.OPT_EARLY_PAGES, 0)
         fresh.close()
+
+
+def test_scattered_adapters_are_copied_once_and_again_after_their_pages_change(ctx):
+    """S-LoRA's unified pool holds the adapters in scattered pages; the table keeps a
+    dense copy of them for the tensor-core kernels.  The first prefill call copies
+    them (three launches), later calls do not (two) and give the same bits; after a
+    page-in of new weights, and after lora_table_invalidate for pages written behind
+    the library's back, the next call copies again and matches the oracle on the new
+    weights."""
+    c = workloads.make("slora_prefill", seed=2)
+    table = upload_table(ctx, c)
+    x = to_dev(c["x"])
+    outs, launches = [], []
+    for _ in range(3):
+        y = to_dev(c["y"])
+        L.lora_fused(ctx, table, c["ids"], x, y)
+        launches.append(ctx.last_path()[1])
+        ctx.sync_status()
+        outs.append(from_dev(y))
+    assert launches[0] == launches[1] + 1 and launches[1] == launches[2] == 2, launches
+    np.testing.assert_array_equal(outs[1], outs[0])
+    np.testing.assert_array_equal(outs[2], outs[0])
+    rows = sample_rows(c, k=64)
+    ref = oracle.fused_rows(oracle.Table.from_case(c), c["ids"], c["x"], c["y"], rows, nthreads=8)
+    assert_parity(outs[0][rows], ref, REL_FROB, MAX_ABS_RMS, "first call")
+    # new weights for the first request's adapter, through lora_page_in
+    k = int(c["ids"][0])
+    r = int(c["rank"][k])
+    rng = np.random.default_rng(7)
+    new_a = workloads.to_bf16_bits(rng.standard_normal((r, 4096), dtype=np.float32) / 64)
+    new_b = workloads.to_bf16_bits(rng.standard_normal((r, 4096), dtype=np.float32) / 4)
+    ha = torch.from_numpy(new_a.view(np.int16)).pin_memory()
+    hb = torch.from_numpy(new_b.view(np.int16)).pin_memory()
+    L.lora_page_in(ctx, table, k, ha, hb)
+    c2 = dict(c, a_pool=c["a_pool"].copy())
+    c2["a_pool"][c["a_pages"][k, :r], :4096] = new_a
+    c2["a_pool"][c["b_pages"][k, :r], :4096] = new_b
+    c2["b_pool"] = c2["a_pool"]
+    y = to_dev(c["y"])
+    L.lora_fused(ctx, table, c["ids"], x, y)
+    assert ctx.last_path()[1] == 3                           # copied again
+    ctx.sync_status()
+    ref2 = oracle.fused_rows(oracle.Table.from_case(c2), c["ids"], c["x"], c["y"], rows, nthreads=8)
+    assert_parity(from_dev(y)[rows], ref2, REL_FROB, MAX_ABS_RMS, "after page-in")
+    # pages written by the caller: back to the original weights, then invalidate
+    table.a_pool.copy_(to_dev(c["a_pool"]))
+    table.invalidate(k)
+    y = to_dev(c["y"])
+    L.lora_fused(ctx, table, c["ids"], x, y)
+    assert ctx.last_path()[1] == 3
+    ctx.sync_status()
+    np.testing.assert_array_equal(from_dev(y), outs[0])
