@@ -113,8 +113,10 @@ struct lora_ctx {
     size_t vrows_cap = 0;           //   (bytes)
     uint8_t *brows = nullptr;       // lora_base_fused: dense B rows, when needed
     size_t brows_cap = 0;
+    uint16_t *aprep = nullptr;      // lora_base_fused: the prepared left operands
+    size_t aprep_cap = 0;
     std::vector<int32_t> proj_mark, proj_off, proj_slots, proj_bbase;
-    std::vector<ProjTerm> proj_terms;
+    std::vector<ProjChunk> proj_chunks;
     uint8_t *vparts = nullptr;      // fused tile path: partial V between its two kernels
     size_t vparts_cap = 0;
     uint8_t *dense = nullptr;       // dense adapter rows of a call (dense.cu): two halves,
@@ -1199,6 +1201,8 @@ int lora_ctx_destroy(lora_ctx *ctx)
         cudaFree(ctx->vrows);
     if (ctx->brows)
         cudaFree(ctx->brows);
+    if (ctx->aprep)
+        cudaFree(ctx->aprep);
     if (ctx->dense)
         cudaFree(ctx->dense);
     if (ctx->flush)
@@ -1411,6 +1415,26 @@ int lora_fused(lora_ctx *ctx, const lora_table *t, const int32_t *ids, int64_t n
                       static_cast<cudaStream_t>(stream));
 }
 
+// Grow a context-owned device buffer to `need` bytes (after the stream's work that
+// may still use the old one).
+static int grow_buffer(lora_ctx *ctx, cudaStream_t stream, void **buf, size_t *cap, size_t need)
+{
+    if (need <= *cap)
+        return LORA_OK;
+    if (*buf) {
+        CUDA_TRY(ctx, cudaStreamSynchronize(stream));
+        cudaFree(*buf);
+        *buf = nullptr;
+        *cap = 0;
+    }
+    if (cudaMalloc(buf, need) != cudaSuccess) {
+        cudaGetLastError();
+        return LORA_E_NOMEM;
+    }
+    *cap = need;
+    return LORA_OK;
+}
+
 int lora_base_fused(lora_ctx *ctx, const lora_table *t, const int32_t *ids, int64_t n,
                     const void *x, int64_t ldx, int d_in, const void *W, int64_t ldw, void *y,
                     int64_t ldy, int d_out, void *stream_ptr)
@@ -1436,45 +1460,23 @@ int lora_base_fused(lora_ctx *ctx, const lora_table *t, const int32_t *ids, int6
     int32_t rmax = 8;
     for (int32_t k : ctx->plan.seg_adapter)
         rmax = std::max(rmax, t->rank[size_t(k)]);
-    // 1. v = x A_k for the active rows (the shrink kernels) into fp32 scratch rows.
-    const int64_t ldv = rmax;
-    int path = 0;
-    bool untuned = false;
-    if (any_active) {
-        const size_t need = size_t(n) * size_t(ldv) * 4u;
-        if (need > ctx->vrows_cap) {
-            if (ctx->vrows) {
-                CUDA_TRY(ctx, cudaStreamSynchronize(stream));
-                cudaFree(ctx->vrows);
-                ctx->vrows = nullptr;
-                ctx->vrows_cap = 0;
-            }
-            if (cudaMalloc(reinterpret_cast<void **>(&ctx->vrows), need) != cudaSuccess)
-                return LORA_E_NOMEM;
-            ctx->vrows_cap = need;
-        }
-        // d_out: the call's, so that long runs take the tensor-core shrink and its
-        // launch shape comes from the tile table's entry for this shape
-        rc = delta_call(ctx, t, kShrink, ids, n, x, ldx, d_in, ctx->vrows, ldv, nullptr, 0, d_out,
-                        stream);
-        if (rc != LORA_OK)
-            return rc;
-        path = ctx->last_path;
-        untuned = ctx->untuned;
-    }
-    // 2. Per 128-row block, one term per adapter with rows in it (order of first row).
-    const int BM = proj_block_rows(), BN = proj_block_cols();
+    // (a multiple of 4 floats: the prep kernel reads a row's v as 16-byte vectors)
+    const int64_t ldv = (rmax + 3) & ~int64_t(3);
+
+    // 1. Per 256-row block, the adapters with rows in it (order of first row), each
+    //    cut into chunks of 64 columns of its padded rank.
+    const int BM = proj_block_rows(), BN = proj_block_cols(), CK = proj_chunk_cols();
     const int n_mblk = int(ceil_div(n, BM)), n_nblk = int(ceil_div(d_out, BN));
     std::vector<int32_t> &mark = ctx->proj_mark, &off = ctx->proj_off, &slots = ctx->proj_slots;
-    std::vector<ProjTerm> &terms = ctx->proj_terms;
+    std::vector<ProjChunk> &chunks = ctx->proj_chunks;
     mark.assign(size_t(t->n_adapters), -1);
     if (ctx->slot_of.size() < size_t(t->n_adapters))
         ctx->slot_of.resize(size_t(t->n_adapters), -1);
     off.assign(size_t(n_mblk) + 1, 0);
-    terms.clear();
+    chunks.clear();
     slots.clear();
     for (int m = 0; m < n_mblk; ++m) {
-        off[size_t(m)] = int32_t(terms.size());
+        off[size_t(m)] = int32_t(chunks.size());
         const int64_t r1 = std::min<int64_t>(n, int64_t(m + 1) * BM);
         for (int64_t i = int64_t(m) * BM; i < r1; ++i) {
             const int32_t k = ids[i];
@@ -1485,59 +1487,80 @@ int lora_base_fused(lora_ctx *ctx, const lora_table *t, const int32_t *ids, int6
                 ctx->slot_of[size_t(k)] = int32_t(slots.size());
                 slots.push_back(k);
             }
-            terms.push_back(ProjTerm{k, 0, t->rank[size_t(k)], t->scale[size_t(k)]});
+            const int32_t r = t->rank[size_t(k)], rp = (r + 15) & ~15;
+            for (int32_t c = 0; c < rp; c += CK)
+                chunks.push_back(ProjChunk{k, 0, r, t->scale[size_t(k)], m, c, std::min(CK, rp - c), 0});
         }
     }
-    off[size_t(n_mblk)] = int32_t(terms.size());
-    // 3. The B row matrix of those adapters: the pool itself, or dense rows in the
-    // call's own buffer (rank-padded with zero rows).
+    off[size_t(n_mblk)] = int32_t(chunks.size());
+    const int n_chunks = int(chunks.size());
+    // 2. The B row matrix of those adapters: the pool itself, or dense rows in the
+    //    context's own buffer (rank-padded with zero rows).
     const int n_slots = int(slots.size());
     RowMats mats;
     ctx->proj_bbase.assign(size_t(n_slots), 0);
     std::vector<int32_t> a_unused(size_t(n_slots) + 1, 0);
     if (n_slots > 0) {
         const size_t bytes = dense_rows_bytes(t, slots.data(), n_slots, d_in, d_out, false, true);
-        if (bytes > ctx->brows_cap) {
-            if (ctx->brows) {
-                CUDA_TRY(ctx, cudaStreamSynchronize(stream));
-                cudaFree(ctx->brows);
-                ctx->brows = nullptr;
-                ctx->brows_cap = 0;
-            }
-            if (cudaMalloc(reinterpret_cast<void **>(&ctx->brows), bytes) != cudaSuccess)
-                rc = LORA_E_NOMEM;
-            else
-                ctx->brows_cap = bytes;
-        }
+        rc = grow_buffer(ctx, stream, reinterpret_cast<void **>(&ctx->brows), &ctx->brows_cap, bytes);
         if (rc == LORA_OK)
             rc = setup_rows(ctx, t, slots.data(), n_slots, d_in, d_out, false, true, nullptr, stream,
                             &mats, a_unused.data(), ctx->proj_bbase.data(), ctx->brows);
         if (rc == LORA_OK)
-            for (ProjTerm &tm : terms)
-                tm.b_row = ctx->proj_bbase[size_t(ctx->slot_of[size_t(tm.adapter)])];
+            for (ProjChunk &ch : chunks)
+                ch.b_row = ctx->proj_bbase[size_t(ctx->slot_of[size_t(ch.adapter)])] + ch.c;
     }
     for (int32_t k : slots)
         ctx->slot_of[size_t(k)] = -1;
     if (rc != LORA_OK)
         return rc;
-    // 4. Upload the block terms and the ids in one copy, stage B if needed, launch.
+    // 3. Scratch: v rows, and the prepared left operands (per chunk 2 x 256 x 64 bf16).
+    if (any_active) {
+        rc = grow_buffer(ctx, stream, reinterpret_cast<void **>(&ctx->vrows), &ctx->vrows_cap,
+                         size_t(n) * size_t(ldv) * 4u);
+        if (rc == LORA_OK)
+            rc = grow_buffer(ctx, stream, reinterpret_cast<void **>(&ctx->aprep), &ctx->aprep_cap,
+                             size_t(n_chunks) * 2u * size_t(BM) * size_t(CK) * 2u);
+        if (rc != LORA_OK)
+            return rc;
+    }
+    // 4. Upload the block chunks and the ids in one copy, ahead of the shrink, so that
+    //    nothing stands between the shrink and the GEMM in the stream.
     const size_t off_bytes = (size_t(n_mblk + 1) * 4u + 15u) & ~size_t(15);
-    const size_t terms_bytes = terms.size() * sizeof(ProjTerm);
+    const size_t chunk_bytes = chunks.size() * sizeof(ProjChunk);
     const size_t ids_bytes = size_t(n) * 4u;
     Slot *slot = nullptr;
-    rc = acquire_slot(ctx, off_bytes + terms_bytes + ids_bytes + 16, &slot);
+    rc = acquire_slot(ctx, off_bytes + chunk_bytes + ids_bytes + 16, &slot);
     if (rc != LORA_OK)
         return rc;
     std::memcpy(slot->host, off.data(), size_t(n_mblk + 1) * 4u);
-    std::memcpy(slot->host + off_bytes, terms.data(), terms_bytes);
-    std::memcpy(slot->host + off_bytes + terms_bytes, ids, ids_bytes);
-    CUDA_TRY(ctx, cudaMemcpyAsync(slot->dev, slot->host, off_bytes + terms_bytes + ids_bytes,
+    std::memcpy(slot->host + off_bytes, chunks.data(), chunk_bytes);
+    std::memcpy(slot->host + off_bytes + chunk_bytes, ids, ids_bytes);
+    CUDA_TRY(ctx, cudaMemcpyAsync(slot->dev, slot->host, off_bytes + chunk_bytes + ids_bytes,
                                   cudaMemcpyHostToDevice, stream));
+    // 5. v = x A_k for the active rows (the shrink kernels) into the fp32 scratch rows;
+    //    d_out: the call's, so that long runs take the tensor-core shrink and its
+    //    launch shape comes from the tile table's entry for this shape.
+    int path = 0;
+    bool untuned = false;
+    if (any_active) {
+        rc = delta_call(ctx, t, kShrink, ids, n, x, ldx, d_in, ctx->vrows, ldv, nullptr, 0, d_out,
+                        stream);
+        if (rc != LORA_OK) {
+            release_slot(ctx, slot, stream);
+            return rc;
+        }
+        path = ctx->last_path;
+        untuned = ctx->untuned;
+    }
+    // 6. Stage B if needed, prepare the left operands, run the GEMM.
     const long ev = prof_start(ctx, 4, stream);
     if (n_slots > 0) {
         rc = run_staging(ctx, t, mats, stream);
-        if (rc != LORA_OK)
+        if (rc != LORA_OK) {
+            release_slot(ctx, slot, stream);
             return rc;
+        }
     }
     ProjParams p{};
     p.x = static_cast<const uint16_t *>(x);
@@ -1548,9 +1571,10 @@ int lora_base_fused(lora_ctx *ctx, const lora_table *t, const int32_t *ids, int6
     p.ldy = ldy;
     p.v = any_active ? ctx->vrows : nullptr;
     p.ldv = ldv;
-    p.term_off = reinterpret_cast<const int32_t *>(slot->dev);
-    p.terms = reinterpret_cast<const ProjTerm *>(slot->dev + off_bytes);
-    p.ids = reinterpret_cast<const int32_t *>(slot->dev + off_bytes + terms_bytes);
+    p.chunk_off = reinterpret_cast<const int32_t *>(slot->dev);
+    p.chunks = reinterpret_cast<const ProjChunk *>(slot->dev + off_bytes);
+    p.ids = reinterpret_cast<const int32_t *>(slot->dev + off_bytes + chunk_bytes);
+    p.a_prep = any_active ? ctx->aprep : nullptr;
     p.b_rows = n_slots > 0 ? mats.b : nullptr;
     p.b_ld = mats.b_ld;
     p.b_nrows = mats.b_nrows;
@@ -1560,6 +1584,11 @@ int lora_base_fused(lora_ctx *ctx, const lora_table *t, const int32_t *ids, int6
     p.d_out = d_out;
     p.n_mblk = n_mblk;
     p.n_nblk = n_nblk;
+    p.n_chunks = n_chunks;
+    if (n_chunks > 0) {
+        CUDA_TRY(ctx, launch_proj_prep(p, stream));
+        count_launch(ctx, stream);
+    }
     CUDA_TRY(ctx, launch_proj_tc(p, stream));
     prof_stop(ctx, ev, stream);
     count_launch(ctx, stream);

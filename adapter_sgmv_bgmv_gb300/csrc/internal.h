@@ -210,15 +210,19 @@ cudaError_t launch_wait_selftest(unsigned *status, uint64_t limit_ns, cudaStream
 cudaError_t launch_plan_dev(const DevPlanArgs &a, cudaStream_t stream);
 
 // Base projection with the adapter term (proj_tc.cu): y = bf16(x W + s_k (x A_k) B_k).
-// One term per adapter with rows in a 128-row block; the block's terms are
-// terms[term_off[m] .. term_off[m + 1]).
-struct ProjTerm {
+// The adapter terms of a 256-row block m are chunks[chunk_off[m] .. chunk_off[m + 1]):
+// one per adapter with rows in the block and 64 columns of its padded rank.
+struct ProjChunk {
     int32_t adapter;
-    int32_t b_row;            // row of page 0 of B_k in the B row matrix
+    int32_t b_row;            // the B row matrix's row of the chunk's first rank index
     int32_t rank;
     float scale;
+    int32_t m;                // the block
+    int32_t c;                // the chunk's first rank index (a multiple of 64)
+    int32_t kc;               // its K: min(64, padded rank - c), a multiple of 16
+    int32_t pad;
 };
-static_assert(sizeof(ProjTerm) == 16, "ProjTerm is one 16-byte load");
+static_assert(sizeof(ProjChunk) == 32, "ProjChunk is two 16-byte loads");
 struct ProjParams {
     const uint16_t *x;
     int64_t ldx;
@@ -226,11 +230,12 @@ struct ProjParams {
     int64_t ldw;
     uint16_t *y;
     int64_t ldy;
-    const float *v;           // the shrink's fp32 rows [n, ldv] (columns < rank used)
+    const float *v;           // the shrink's fp32 rows [n, ldv] (ldv a multiple of 4)
     int64_t ldv;
     const int32_t *ids;       // device copy of the call's ids [n]
-    const int32_t *term_off;  // [n_mblk + 1]
-    const ProjTerm *terms;
+    const int32_t *chunk_off; // [n_mblk + 1]
+    const ProjChunk *chunks;
+    uint16_t *a_prep;         // [n_chunks * 2 * 256, 64] bf16: per chunk hi, then lo
     const uint16_t *b_rows;   // B row matrix (pages as consecutive rows, rank-padded)
     int64_t b_ld;
     int64_t b_nrows;
@@ -238,12 +243,15 @@ struct ProjParams {
     int n;
     int d_in;
     int d_out;
-    int n_mblk;               // 128-row blocks
+    int n_mblk;               // 256-row blocks (one per CTA pair)
     int n_nblk;               // 256-column blocks
+    int n_chunks;
 };
+cudaError_t launch_proj_prep(const ProjParams &p, cudaStream_t stream);
 cudaError_t launch_proj_tc(const ProjParams &p, cudaStream_t stream);
 int proj_block_rows();
 int proj_block_cols();
+int proj_chunk_cols();
 
 // Offline search (fill.cu): n bf16 values uniform in [-scale, scale) from a hash of
 // (seed, index).

@@ -8,30 +8,41 @@
 // beside the base GEMM.  Here the adapter term is more K steps of the same
 // accumulator, so y is written once and never read.)
 //
-// Persistent kernel, one CTA per SM, over the tiles (128-row block m, 256-column
-// block n) in groups of 16 row blocks (row blocks fastest within a group, so that a
-// 256-column slice of W is fetched once per group and the group's x blocks stay in
-// L2).  Per tile the accumulator (TMEM,
-// 128 lanes x 256 fp32 columns, two of them so that one tile's epilogue overlaps the
-// next tile's MMAs) takes
-//   - the base: d_in / 64 stages of x block (128 x 64, K-major, 128-byte swizzle)
-//     times W block (64 x 256, N-major: four 64-column boxes);
-//   - then, for every adapter k with rows in block m, its term as stages of K <= 64:
-//     the left operand is s_k v (v = x A_k, the shrink's fp32 rows) split into bf16
-//     hi = bf16(s v) and lo = bf16(s v - hi) (about 16 significant bits; the MMAs
-//     run on both halves), with the rows of other adapters and released rows zero;
-//     the right operand is B_k's rows (N-major boxes from the B row matrix, whose
-//     rank-padding rows are zero).
+// k_proj_prep writes the left operand of every adapter stage before the GEMM runs:
+// per chunk (256-row block m, adapter k with rows in it, 64 columns c.. of its
+// padded rank) two 256 x 64 bf16 matrices, hi = bf16(s_k v) and lo = bf16(s_k v - hi)
+// (v = x A_k, the shrink's fp32 rows; hi + lo carries about 16 significant bits),
+// zero in the rows of other adapters, released rows, rows past n and columns past
+// the rank.  The GEMM then loads them by TMA like any other operand.
+//
+// k_proj_tc: persistent kernel over pairs of CTAs (clusters of two on neighbouring
+// SMs) that share one tcgen05 MMA of M = 256, N = 256 (cta_group::2): a pair owns
+// the tile (256-row block m, 256-column block n); CTA rank c of the pair loads rows
+// 128c .. 128c + 127 of the left operand and columns 128c .. 128c + 127 of the right
+// one into its own shared memory, and its TMEM holds those 128 rows of the 256 x 256
+// fp32 accumulator.  Against one CTA per 128 x 256 tile, every SM fills a third less
+// shared memory per MMA flop (32 KB per K block of 64 instead of 48 KB), and the
+// ring holds six stages.  Tiles go in groups of 8 row blocks (row blocks fastest
+// within a group, so that a 256-column slice of W is fetched once per group and the
+// group's x blocks stay in L2).  Per tile the accumulator (two of them, so that one
+// tile's epilogue overlaps the next tile's MMAs) takes
+//   - the base: d_in / 64 stages of x block (128 x 64 per CTA, K-major, 128-byte
+//     swizzle) times W block (64 x 128 per CTA, N-major: two 64-column boxes);
+//   - then, for every chunk of block m, two stages (hi, then lo) of K = the chunk's
+//     width: the prepared left operand times B_k's rows (N-major boxes from the B
+//     row matrix, whose rank-padding rows are zero).
 // Warps:
-//   0      producer: TMA loads of every stage into a ring of 4 (48 KB each), one
-//          barrier per stage (two arrivals: the producer's with the bytes, and a
-//          second one -- the producer's own for a base stage, the left-operand
-//          warps' for an adapter stage);
-//   1      MMA issuer: tcgen05.mma M = 128, N = 256, K = 16, frees each stage with
-//          tcgen05.commit, and hands each finished accumulator to the epilogue;
-//   2-5    epilogue: TMEM -> registers -> bf16 -> y rows (16-byte stores), then the
-//          accumulator goes back to the MMA warp;
-//   6-9    left operand of the adapter stages (thread = row of the block).
+//   0      producer (both CTAs): TMA loads of the CTA's halves of every stage into a
+//          ring of 6 (32 KB each); the bytes of both CTAs complete on rank 0's stage
+//          barrier, which rank 0's producer arms with the pair's byte count;
+//   1      rank 0 only, MMA issuer: tcgen05.mma M = 256, N = 256, K = 16; a commit
+//          multicast to both CTAs frees each stage, and another hands each finished
+//          accumulator to both CTAs' epilogues;
+//   2-5    epilogue (both CTAs): TMEM -> registers -> bf16 -> y rows (16-byte
+//          stores); the accumulator goes back to rank 0's MMA warp once all eight
+//          warps of the pair have read it.
+// The producer and the MMA warp read a block's chunk list for the next tile while
+// the current tile's base stages run, so that at a tile's end they go straight on.
 // Every wait is bounded (1 s); on expiry the status word records it, the stores are
 // skipped, and the kernel still ends.
 #include <cuda.h>
@@ -46,59 +57,37 @@ namespace lora {
 
 namespace {
 
-constexpr int kBM = 128;
-constexpr int kBN = 256;
+constexpr int kBM = 128;                            // rows per CTA
+constexpr int kPM = 2 * kBM;                        // rows per pair: the MMA's M
+constexpr int kBN = 256;                            // columns per tile: the MMA's N
+constexpr int kHN = kBN / 2;                        // columns of B in each CTA
 constexpr int kBK = 64;
-constexpr int kNS = 4;                              // stages in the ring
-constexpr uint32_t kAStage = kBM * kBK * 2;         // 16 KB: x block or one V half
+constexpr int kNS = 6;                              // stages in the ring
+constexpr uint32_t kAStage = kBM * kBK * 2;         // 16 KB: x block or a prepared half
 constexpr uint32_t kBAtom = kBK * 128;              // 8 KB: 64 K rows x 64 columns
-constexpr uint32_t kBStage = 4 * kBAtom;            // 32 KB: W block or B_k block
-constexpr uint32_t kStage = kAStage + kBStage;      // 48 KB
-constexpr int kThreads = 320;
-constexpr int kEpiWarp0 = 2;
-constexpr int kLeftWarp0 = 6;
+constexpr uint32_t kBStage = 2 * kBAtom;            // 16 KB: this CTA's 128 columns
+constexpr uint32_t kStage = kAStage + kBStage;      // 32 KB
+constexpr int kThreads = 192;
 constexpr uint32_t kTmemCols = 2 * kBN;             // two 256-column accumulators
 
 struct ProjArgs {
     CUtensorMap xmap;                               // x [n, d_in], 64 x 128 boxes
     CUtensorMap wmap;                               // W [d_in, d_out], 64 x 64 boxes
+    CUtensorMap amap;                               // prepared left operands, 64 x 128 boxes
     CUtensorMap bmap[3];                            // B row matrix, 64 x 16 / 32 / 64 boxes
     ProjParams p;
 };
 
-__host__ __device__ inline int rank_pad16(int r) { return (r + 15) & ~15; }
-
 __host__ __device__ inline uint32_t proj_smem_bytes()
 {
-    return 1024u + uint32_t(kNS) * kStage + 256u;   // + barriers (24 x 8 B + 4 x 8 B + 12 B)
-}
-
-__device__ __forceinline__ void named_bar_sync(int id, int nthreads)
-{
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
-
-// Named barrier over `nthreads` threads that also returns the AND of `v` over them,
-// so that every one of them takes the same branch afterwards.
-__device__ __forceinline__ bool named_bar_and(int id, int nthreads, bool v)
-{
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\t"
-        "setp.ne.u32 p, %1, 0;\n\t"
-        "bar.red.and.pred q, %2, %3, p;\n\t"
-        "selp.u32 %0, 1, 0, q;\n\t}"
-        : "=r"(r)
-        : "r"(uint32_t(v)), "r"(id), "r"(nthreads)
-        : "memory");
-    return r != 0;
+    return 1024u + uint32_t(kNS) * kStage + 256u;   // + barriers (2 x 6 x 8 B + 5 x 8 B + 4 B)
 }
 
 // Tile t of the launch: groups of kGroupM row blocks, each group swept over every
-// column block with its row blocks fastest, so that the CTAs running at one time
+// column block with its row blocks fastest, so that the pairs running at one time
 // share a few x blocks and each 256-column slice of W is fetched from DRAM once per
 // group (x, W and y stay streaming; W is not assumed to stay in L2).
-constexpr int kGroupM = 16;
+constexpr int kGroupM = 8;
 __device__ __forceinline__ void tile_coords(const ProjParams &p, int t, int &m, int &nb)
 {
     const int gsize = kGroupM * p.n_nblk;
@@ -109,22 +98,95 @@ __device__ __forceinline__ void tile_coords(const ProjParams &p, int t, int &m, 
     nb = local / gm;
 }
 
-// The stages of block m's adapter terms: for each term, hi then lo, each in chunks
-// of at most 64 of its padded rank.  f(term index, half, first column, K of stage).
-template <typename F>
-__device__ __forceinline__ void for_term_stages(const ProjParams &p, int m, F &&f)
+// The chunks of one row block as far as a warp holds them in registers: the range
+// [c0, c1) of the chunk list and its first two chunks (further ones, rare, are read
+// when they come).  Filled in two steps -- the range, then (once it has arrived)
+// the chunks -- so that the producer and the MMA warp can issue both loads for the
+// next tile while the current tile's base stages run.
+struct BlockChunks {
+    int c0, c1;
+    ProjChunk ch[2];
+};
+
+__device__ __forceinline__ ProjChunk load_chunk(const ProjParams &p, int i)
 {
-    const int t0 = __ldg(p.term_off + m), t1 = __ldg(p.term_off + m + 1);
-    for (int ti = t0; ti < t1; ++ti) {
-        const int rp = rank_pad16(p.terms[ti].rank);
+    const int4 *q = reinterpret_cast<const int4 *>(p.chunks + i);
+    const int4 u = __ldg(q), w = __ldg(q + 1);
+    return ProjChunk{u.x, u.y, u.z, __int_as_float(u.w), w.x, w.y, w.z, w.w};
+}
+
+__device__ __forceinline__ void block_chunks_range(const ProjParams &p, int m, BlockChunks &bc)
+{
+    bc.c0 = __ldg(p.chunk_off + m);
+    bc.c1 = __ldg(p.chunk_off + m + 1);
+}
+
+__device__ __forceinline__ void block_chunks_first(const ProjParams &p, BlockChunks &bc)
+{
+    if (bc.c1 > bc.c0)
+        bc.ch[0] = load_chunk(p, bc.c0);
+    if (bc.c1 > bc.c0 + 1)
+        bc.ch[1] = load_chunk(p, bc.c0 + 1);
+}
+
+// The adapter stages of a block: per chunk, hi then lo.  f(chunk index, chunk, half).
+template <typename F>
+__device__ __forceinline__ void for_chunk_stages(const ProjParams &p, const BlockChunks &bc, F &&f)
+{
+    for (int i = bc.c0; i < bc.c1; ++i) {
+        const ProjChunk ch = i == bc.c0 ? bc.ch[0] : i == bc.c0 + 1 ? bc.ch[1] : load_chunk(p, i);
         for (int half = 0; half < 2; ++half)
-            for (int c = 0; c < rp; c += kBK)
-                if (!f(ti, half, c, min(kBK, rp - c)))
-                    return;
+            if (!f(i, ch, half))
+                return;
     }
 }
 
-__global__ void __launch_bounds__(kThreads, 1) k_proj_tc(const __grid_constant__ ProjArgs a)
+// ------------------------------------------------------------------ prep
+
+// One CTA per chunk, thread t = row t of the chunk's 256-row block: the row's 64
+// values of s_k v[row, c .. c + 64) (zero unless the row is adapter k's and the
+// column below its rank) as bf16 hi into row 2 * chunk * 256 + t of the prepared
+// matrix and lo into row (2 * chunk + 1) * 256 + t.
+__global__ void __launch_bounds__(kPM) k_proj_prep(const __grid_constant__ ProjParams p)
+{
+    const int i = blockIdx.x, t = threadIdx.x;
+    const ProjChunk ch = load_chunk(p, i);
+    const int row = ch.m * kPM + t;
+    // v and the ids are the shrink's and the host copy's: wait for the kernel before.
+    grid_dep_wait();
+    const bool mine = row < p.n && __ldg(p.ids + row) == ch.adapter;
+    float4 v[16];
+    const float *vrow = p.v + int64_t(row) * p.ldv + ch.c;   // ldv: a multiple of 4
+#pragma unroll
+    for (int q = 0; q < 16; ++q)
+        v[q] = (mine && ch.c + 4 * q < ch.rank) ? __ldg(reinterpret_cast<const float4 *>(vrow) + q)
+                                                : make_float4(0.f, 0.f, 0.f, 0.f);
+    grid_dep_launch();
+    uint4 *hi = reinterpret_cast<uint4 *>(p.a_prep + (int64_t(2 * i) * kPM + t) * kBK);
+    uint4 *lo = reinterpret_cast<uint4 *>(p.a_prep + (int64_t(2 * i + 1) * kPM + t) * kBK);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        const float4 a = v[2 * q], b = v[2 * q + 1];
+        const float w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        float f[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            f[e] = (ch.c + 8 * q + e < ch.rank) ? ch.scale * w[e] : 0.f;
+        const uint4 h = pack8(f);
+        float back[8];
+        unpack8(h, back);
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            f[e] -= back[e];
+        hi[q] = h;
+        lo[q] = pack8(f);
+    }
+}
+
+// ------------------------------------------------------------------ GEMM
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    k_proj_tc(const __grid_constant__ ProjArgs a)
 {
     const ProjParams &p = a.p;
     extern __shared__ uint8_t smem_raw[];
@@ -132,91 +194,116 @@ __global__ void __launch_bounds__(kThreads, 1) k_proj_tc(const __grid_constant__
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t *gbase = smem_raw + (base - raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t crank = cluster_ctarank();          // 0 issues the pair's MMAs
+    const bool leader = crank == 0;
+    const int pair = int(blockIdx.x >> 1), npairs = int(gridDim.x >> 1);
 
     const uint32_t sBar = base + uint32_t(kNS) * kStage;
-    // barriers: full[4], empty[4], vgo[4], tfull[2], tempty[2], done; then the TMEM
-    // address.  vgo[s]: the producer found slot s free for an adapter stage, so the
-    // left-operand warps may write its A half.  (They cannot wait on empty[s]
-    // themselves: they skip the base stages, and a parity wait more than one phase
-    // ahead of the barrier would pass early.)
-    const uint32_t full0 = sBar, empty0 = sBar + 8 * kNS, vgo0 = sBar + 16 * kNS;
-    const uint32_t tfull0 = sBar + 24 * kNS;
+    // barriers: full[6], empty[6], tfull[2], tempty[2], done; then the TMEM address.
+    // full (rank 0's) counts both CTAs' bytes; empty and tfull get rank 0's commits
+    // in both CTAs; tempty (rank 0's) one arrival per epilogue warp of the pair.
+    const uint32_t full0 = sBar, empty0 = sBar + 8 * kNS;
+    const uint32_t tfull0 = sBar + 16 * kNS;
     const uint32_t tempty0 = tfull0 + 16, done = tempty0 + 16, tmem_slot = done + 8;
     auto stage_a = [&](int s) { return base + uint32_t(s) * kStage; };
     auto stage_b = [&](int s) { return base + uint32_t(s) * kStage + kAStage; };
+    // rank 0's copy of a barrier of this CTA's layout
+    auto at_leader = [&](uint32_t bar) { return map_cluster(bar, 0u); };
 
     if (tid == 0) {
         for (int s = 0; s < kNS; ++s) {
-            mbar_init(full0 + 8 * s, 2);
+            mbar_init(full0 + 8 * s, 1);
             mbar_init(empty0 + 8 * s, 1);
-            mbar_init(vgo0 + 8 * s, 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(tfull0 + 8 * b, 1);
-            mbar_init(tempty0 + 8 * b, 4);
+            mbar_init(tempty0 + 8 * b, 8);
         }
         mbar_init(done, 1);
         fence_mbar_init();
     }
     if (warp == 1)
-        tc::tmem_alloc(tmem_slot, kTmemCols);
+        tc::tmem_alloc_pair(tmem_slot, kTmemCols);
     tc::fence_before_sync();
     __syncthreads();
+    // Both CTAs' barriers are initialised and their TMEM allocated before anything
+    // is addressed across the pair.
+    cluster_sync();
     tc::fence_after_sync();
     const uint32_t tmem = *reinterpret_cast<const uint32_t *>(gbase + (tmem_slot - base));
-    // Launched as a programmatic dependent of the shrink that wrote v: everything
-    // above overlapped its tail.
+    // Launched as a programmatic dependent of the prep kernel: everything above
+    // overlapped its tail.
     grid_dep_wait();
 
     const int n_tiles = p.n_mblk * p.n_nblk;
     const int nkb = (p.d_in + kBK - 1) / kBK;
+    const int kpre = min(8, nkb - 1);   // base stage at which the next tile's chunks are read
     bool ok = true;
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
+        // Boxes that lie past n, d_out or the rank are loaded all the same (zero
+        // fill, full byte count), so that both CTAs' byte counts are fixed per stage.
         if (lane == 0) {
             uint32_t g = 0;
-            for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
+            BlockChunks cur{}, nxt{};
+            if (pair < n_tiles) {
+                int m, nb;
+                tile_coords(p, pair, m, nb);
+                block_chunks_range(p, m, cur);
+                block_chunks_first(p, cur);
+            }
+            auto next_slot = [&](uint32_t bytes) -> int {
+                const int s = int(g % kNS);
+                if (g >= kNS)
+                    ok = mbar_wait_bounded(empty0 + 8 * s, ((g / kNS) - 1) & 1, p.status,
+                                           kDevTimeoutPipe);
+                if (ok && leader)
+                    mbar_arrive_expect_tx(full0 + 8 * s, 2u * bytes);
+                return s;
+            };
+            for (int tile = pair; tile < n_tiles && ok; tile += npairs) {
                 int m, nb;
                 tile_coords(p, tile, m, nb);
-                const int n0 = nb * kBN, row0 = m * kBM;
-                const int natoms = min(4, (p.d_out - n0 + 63) / 64);   // 64-column boxes inside d_out
+                const int n0 = nb * kBN + int(crank) * kHN;     // this CTA's columns of B
+                const int row0 = m * kPM + int(crank) * kBM;    // this CTA's rows
+                const bool more = tile + npairs < n_tiles;
+                if (more) {
+                    int mn, nbn;
+                    tile_coords(p, tile + npairs, mn, nbn);
+                    block_chunks_range(p, mn, nxt);
+                }
                 for (int kb = 0; kb < nkb && ok; ++kb, ++g) {
-                    const int s = int(g % kNS);
-                    if (g >= kNS)
-                        ok = mbar_wait_bounded(empty0 + 8 * s, ((g / kNS) - 1) & 1, p.status,
-                                               kDevTimeoutPipe);
+                    if (kb == kpre && more)
+                        block_chunks_first(p, nxt);
+                    const int s = next_slot(kStage);
                     if (!ok)
                         break;
-                    mbar_arrive_expect_tx(full0 + 8 * s, kAStage + uint32_t(natoms) * kBAtom);
-                    tc::tma_load_2d(stage_a(s), &a.xmap, kb * kBK, row0, full0 + 8 * s);
-                    for (int q = 0; q < natoms; ++q)
-                        tc::tma_load_2d(stage_b(s) + uint32_t(q) * kBAtom, &a.wmap, n0 + 64 * q, kb * kBK,
-                                        full0 + 8 * s);
-                    mbar_arrive(full0 + 8 * s);
+                    const uint32_t fb = at_leader(full0 + 8 * s);
+                    tc::tma_load_2d_pair(stage_a(s), &a.xmap, kb * kBK, row0, fb);
+                    tc::tma_load_2d_pair(stage_b(s), &a.wmap, n0, kb * kBK, fb);
+                    tc::tma_load_2d_pair(stage_b(s) + kBAtom, &a.wmap, n0 + 64, kb * kBK, fb);
                 }
-                for_term_stages(p, m, [&](int ti, int, int c, int kc) {
-                    const int s = int(g % kNS);
-                    if (g >= kNS)
-                        ok = mbar_wait_bounded(empty0 + 8 * s, ((g / kNS) - 1) & 1, p.status,
-                                               kDevTimeoutPipe);
+                for_chunk_stages(p, cur, [&](int i, const ProjChunk &ch, int half) {
+                    const int s = next_slot(kAStage + 2u * uint32_t(ch.kc) * 128u);
                     if (!ok)
                         return false;
-                    mbar_arrive(vgo0 + 8 * s);   // the left-operand warps may fill its A half
-                    const int brow = p.terms[ti].b_row + c;
-                    mbar_arrive_expect_tx(full0 + 8 * s, uint32_t(natoms) * uint32_t(kc) * 128u);
-                    for (int q = 0; q < natoms; ++q)
-                        tc::for_row_boxes(kc, [&](int off, int mi) {
-                            tc::tma_load_2d(stage_b(s) + uint32_t(q) * kBAtom + uint32_t(off) * 128u,
-                                            &a.bmap[mi], n0 + 64 * q, brow + off, full0 + 8 * s);
+                    const uint32_t fb = at_leader(full0 + 8 * s);
+                    tc::tma_load_2d_pair(stage_a(s), &a.amap, 0, (2 * i + half) * kPM + int(crank) * kBM, fb);
+                    for (int q = 0; q < 2; ++q)
+                        tc::for_row_boxes(ch.kc, [&](int off, int mi) {
+                            tc::tma_load_2d_pair(stage_b(s) + uint32_t(q) * kBAtom + uint32_t(off) * 128u,
+                                                 &a.bmap[mi], n0 + 64 * q, ch.b_row + off, fb);
                         });
                     ++g;
                     return true;
                 });
+                cur = nxt;
             }
             grid_dep_launch();   // every load issued: the next kernel may start its set-up
-            if (!ok) {
-                // Let the loads already issued land before this CTA can leave.
+            if (!ok && leader) {
+                // Let the loads already issued (both CTAs' bytes complete here) land
+                // before the pair can leave.
                 for (uint32_t q = g > kNS ? g - kNS : 0; q < g; ++q)
                     mbar_wait_bounded(full0 + 8 * (q % kNS), (q / kNS) & 1, nullptr, 0, 20000000ull);
             }
@@ -224,17 +311,28 @@ __global__ void __launch_bounds__(kThreads, 1) k_proj_tc(const __grid_constant__
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            const uint32_t idesc = tc::idesc_bf16(kBM, kBN, 0, 1);
+        if (lane == 0 && leader) {
+            const uint32_t idesc = tc::idesc_bf16(kPM, kBN, 0, 1);
             uint32_t g = 0;
             int lt = 0;
-            for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x, ++lt) {
+            BlockChunks cur{}, nxt{};
+            if (pair < n_tiles) {
                 int m, nb;
-                tile_coords(p, tile, m, nb);
+                tile_coords(p, pair, m, nb);
+                block_chunks_range(p, m, cur);
+                block_chunks_first(p, cur);
+            }
+            for (int tile = pair; tile < n_tiles && ok; tile += npairs, ++lt) {
+                const bool more = tile + npairs < n_tiles;
+                if (more) {
+                    int mn, nbn;
+                    tile_coords(p, tile + npairs, mn, nbn);
+                    block_chunks_range(p, mn, nxt);
+                }
                 const int acc = lt & 1;
                 if (lt >= 2)
-                    ok = mbar_wait_bounded(tempty0 + 8 * acc, ((lt >> 1) - 1) & 1, p.status,
-                                           kDevTimeoutPipe);
+                    ok = mbar_wait_bounded_cluster(tempty0 + 8 * acc, ((lt >> 1) - 1) & 1, p.status,
+                                                   kDevTimeoutPipe);
                 if (!ok)
                     break;
                 tc::fence_after_sync();
@@ -249,35 +347,39 @@ __global__ void __launch_bounds__(kThreads, 1) k_proj_tc(const __grid_constant__
                     for (int kk = 0; kk < kc / 16; ++kk) {
                         const uint64_t da = tc::smem_desc_sw128(stage_a(s) + 32u * uint32_t(kk), 16u, 1024u);
                         const uint64_t db = tc::smem_desc_sw128(stage_b(s) + 2048u * uint32_t(kk), kBAtom, 1024u);
-                        tc::mma_bf16(d, da, db, idesc, (st > 0 || kk > 0) ? 1u : 0u);
+                        tc::mma_bf16_pair(d, da, db, idesc, (st > 0 || kk > 0) ? 1u : 0u);
                     }
-                    tc::mma_commit(empty0 + 8 * s);
+                    tc::mma_commit_pair_both(empty0 + 8 * s);
                     ++st;
                     ++g;
                     return true;
                 };
-                for (int kb = 0; kb < nkb && ok; ++kb)
+                for (int kb = 0; kb < nkb && ok; ++kb) {
+                    if (kb == kpre && more)
+                        block_chunks_first(p, nxt);
                     stage(kBK);
+                }
                 if (ok)
-                    for_term_stages(p, m, [&](int, int, int, int kc) { return stage(kc); });
+                    for_chunk_stages(p, cur, [&](int, const ProjChunk &ch, int) { return stage(ch.kc); });
                 if (!ok)
                     break;
-                tc::mma_commit(tfull0 + 8 * acc);
+                tc::mma_commit_pair_both(tfull0 + 8 * acc);
+                cur = nxt;
             }
             // Every MMA issued so far has completed once this arrives.
-            tc::mma_commit(done);
+            tc::mma_commit_pair(done);
             mbar_wait_bounded(done, 0, nullptr, 0);
         }
         __syncwarp();
-    } else if (warp >= kEpiWarp0 && warp < kLeftWarp0) {
+    } else {
         // ------------------------------------------------------------ epilogue
         const int q4 = warp & 3;                       // TMEM lanes 32*q4 .. 32*q4+31
-        const int r_in = 32 * q4 + lane;               // this thread's row of the tile
+        const int r_in = 32 * q4 + lane;               // this thread's row of the CTA's half
         int lt = 0;
-        for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++lt) {
+        for (int tile = pair; tile < n_tiles; tile += npairs, ++lt) {
             int m, nb;
             tile_coords(p, tile, m, nb);
-            const int n0 = nb * kBN, row0 = m * kBM;
+            const int n0 = nb * kBN, row0 = m * kPM + int(crank) * kBM;
             const int acc = lt & 1;
             if (ok)
                 ok = mbar_wait_bounded(tfull0 + 8 * acc, (lt >> 1) & 1, p.status, kDevTimeoutMma);
@@ -297,8 +399,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_proj_tc(const __grid_constant__
                     // the whole accumulator is in registers: it may take the next tile
                     tc::fence_before_sync();
                     __syncwarp();
-                    if (lane == 0)
-                        mbar_arrive(tempty0 + 8 * acc);
+                    if (lane == 0) {
+                        if (leader)
+                            mbar_arrive(tempty0 + 8 * acc);
+                        else
+                            mbar_arrive_remote(at_leader(tempty0 + 8 * acc));
+                    }
                 }
 #pragma unroll
                 for (int h = 0; h < 2; ++h)
@@ -314,74 +420,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_proj_tc(const __grid_constant__
                     }
             }
         }
-    } else {
-        // ------------------------------------------------------------ left operand
-        // Thread vr writes row vr of every adapter stage's A half: s_k v[row, c..c+kc)
-        // as bf16 hi or lo (zero for rows of other adapters, released rows and rows
-        // past n), in the K-major 128-byte-swizzled layout of the x blocks.
-        // The four warps agree on every decision (named_bar_and), so that they all run
-        // the same sequence of named barriers whatever happens.
-        const int vr = tid - 32 * kLeftWarp0;
-        uint32_t g = 0;
-        uint32_t uses[kNS] = {0, 0, 0, 0};   // adapter stages this thread has filled, per slot
-        for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
-            int m, nb;
-            tile_coords(p, tile, m, nb);
-            const int row0 = m * kBM;
-            const int row = row0 + vr;
-            const int id = (p.ids && row < p.n) ? __ldg(p.ids + row) : -1;
-            g += uint32_t(nkb);
-            for_term_stages(p, m, [&](int ti, int half, int c, int kc) {
-                const int s = int(g % kNS);
-                // The producer arrives on vgo[s] once per adapter stage in slot s, and
-                // the next such arrival needs this stage consumed first: never more
-                // than one phase ahead, so the parity of this slot's count is exact.
-                uint32_t u = 0;
-#pragma unroll
-                for (int q = 0; q < kNS; ++q)
-                    if (q == s)
-                        u = uses[q]++;
-                ok = mbar_wait_bounded(vgo0 + 8 * s, u & 1, p.status, kDevTimeoutPipe);
-                ok = named_bar_and(1, 128, ok);
-                if (ok) {
-                    const ProjTerm tm = p.terms[ti];
-                    const bool mine = id == tm.adapter;
-                    const float* vrow = p.v + int64_t(row) * p.ldv;
-                    uint8_t *dst = gbase + (stage_a(s) - base);
-                    for (int q = 0; q < kc / 8; ++q) {
-                        float f[8];
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            const int j = c + 8 * q + e;
-                            f[e] = (mine && j < tm.rank) ? tm.scale * __ldg(vrow + j) : 0.f;
-                        }
-                        uint4 out = pack8(f);
-                        if (half) {
-                            float back[8];
-                            unpack8(out, back);
-#pragma unroll
-                            for (int e = 0; e < 8; ++e)
-                                f[e] -= back[e];
-                            out = pack8(f);
-                        }
-                        *reinterpret_cast<uint4 *>(dst + tc::sw128(uint32_t(vr), uint32_t(q))) = out;
-                    }
-                    tc::fence_proxy_async_smem();
-                    named_bar_sync(2, 128);
-                    if (vr == 0)
-                        mbar_arrive(full0 + 8 * s);
-                }
-                ++g;
-                return ok;
-            });
-        }
     }
     tc::fence_before_sync();
     __syncthreads();
+    // The pair's MMAs have completed (rank 0 waited for them above) and no arrival or
+    // copy is still addressed to the other CTA: TMEM may go, and the CTAs may leave.
+    cluster_sync();
     if (warp == 1) {
         __syncwarp();
         tc::fence_after_sync();
-        tc::tmem_dealloc(tmem, kTmemCols);
+        tc::tmem_dealloc_pair(tmem, kTmemCols);
     }
 }
 
@@ -400,6 +448,20 @@ int device_sms_proj()
 
 }  // namespace
 
+cudaError_t launch_proj_prep(const ProjParams &p, cudaStream_t stream)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(p.n_chunks));
+    cfg.blockDim = dim3(kPM);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k_proj_prep, p);
+}
+
 cudaError_t launch_proj_tc(const ProjParams &p, cudaStream_t stream)
 {
     ProjArgs a;
@@ -409,12 +471,15 @@ cudaError_t launch_proj_tc(const ProjParams &p, cudaStream_t stream)
         !encode_bf16_2d(&a.wmap, p.W, uint64_t(p.d_out), uint64_t(p.d_in), uint64_t(p.ldw) * 2u, 64,
                         kBK, true))
         return cudaErrorInvalidValue;
-    if (p.b_rows) {
-        if (!encode_row_maps(a.bmap, p.b_rows, uint64_t(p.d_out), p.b_nrows, p.b_ld))
+    if (p.n_chunks > 0) {
+        if (!encode_row_maps(a.bmap, p.b_rows, uint64_t(p.d_out), p.b_nrows, p.b_ld) ||
+            !encode_bf16_2d(&a.amap, p.a_prep, uint64_t(kBK), uint64_t(p.n_chunks) * 2u * kPM,
+                            uint64_t(kBK) * 2u, kBK, kBM, true))
             return cudaErrorInvalidValue;
     } else {
         for (auto &m : a.bmap)
             m = CUtensorMap{};
+        a.amap = CUtensorMap{};
     }
     static bool configured = false;
     if (!configured) {
@@ -424,12 +489,24 @@ cudaError_t launch_proj_tc(const ProjParams &p, cudaStream_t stream)
             return e;
         configured = true;
     }
-    const int n_tiles = p.n_mblk * p.n_nblk;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(unsigned(n_tiles < device_sms_proj() ? n_tiles : device_sms_proj()));
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = proj_smem_bytes();
     cfg.stream = stream;
+    // As many pairs as can be resident at once (a pair waits on nothing outside
+    // itself, so a larger grid would only run in a second wave).
+    static int max_pairs = 0;
+    if (!max_pairs) {
+        cfg.gridDim = dim3(2u * unsigned(device_sms_proj() / 2));
+        int nc = 0;
+        if (cudaOccupancyMaxActiveClusters(&nc, k_proj_tc, &cfg) != cudaSuccess || nc <= 0) {
+            cudaGetLastError();
+            nc = device_sms_proj() / 2;
+        }
+        max_pairs = nc;
+    }
+    const int n_tiles = p.n_mblk * p.n_nblk;
+    cfg.gridDim = dim3(2u * unsigned(n_tiles < max_pairs ? n_tiles : max_pairs));
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -438,7 +515,8 @@ cudaError_t launch_proj_tc(const ProjParams &p, cudaStream_t stream)
     return cudaLaunchKernelEx(&cfg, k_proj_tc, a);
 }
 
-int proj_block_rows() { return kBM; }
+int proj_block_rows() { return kPM; }
 int proj_block_cols() { return kBN; }
+int proj_chunk_cols() { return kBK; }
 
 }  // namespace lora

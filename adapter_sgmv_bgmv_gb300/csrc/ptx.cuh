@@ -63,6 +63,35 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
     return ok != 0;
 }
 
+// `count` arrivals at once.
+__device__ __forceinline__ void mbar_arrive_n(uint32_t bar, uint32_t count)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+// Arrive on an mbarrier of another CTA of the cluster (its cluster address, from
+// map_cluster), releasing this thread's prior writes at cluster scope.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_bar)
+{
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
+                 : "memory");
+}
+
+// try_wait with acquire at cluster scope: pairs with arrivals made from other CTAs
+// of the cluster (mbar_arrive_remote).
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait for phase `parity` of an mbarrier for at most `limit_ns` nanoseconds.  On
 // expiry the status word records `code` and false is returned; the caller keeps
 // the barrier structure of its CTA/cluster intact and skips its stores.
@@ -75,6 +104,24 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
     const uint64_t t0 = globaltimer_ns();
     while (true) {
         if (mbar_try_wait(bar, parity))
+            return true;
+        if (globaltimer_ns() - t0 > limit_ns) {
+            raise_status(status, code);
+            return false;
+        }
+    }
+}
+
+// mbar_wait_bounded with cluster-scope acquire.
+__device__ __forceinline__ bool mbar_wait_bounded_cluster(uint32_t bar, uint32_t parity,
+                                                          unsigned *status, unsigned code,
+                                                          uint64_t limit_ns = kWaitLimitNs)
+{
+    if (mbar_try_wait_cluster(bar, parity))
+        return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        if (mbar_try_wait_cluster(bar, parity))
             return true;
         if (globaltimer_ns() - t0 > limit_ns) {
             raise_status(status, code);

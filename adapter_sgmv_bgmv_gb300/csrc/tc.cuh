@@ -169,6 +169,69 @@ __device__ __forceinline__ void mma_commit(uint32_t bar)
         : "memory");
 }
 
+// ---------------------------------------------------------------- CTA pairs
+// The cta_group::2 forms: the two CTAs of a cluster of two share one MMA of M = 256
+// (A's rows 0-127 and D's lanes in CTA rank 0, rows 128-255 in rank 1; B's first
+// N/2 columns in rank 0, the rest in rank 1), issued by rank 0 with descriptors
+// that address the same shared-memory offsets in both CTAs.  Every tcgen05
+// instruction of such a kernel takes cta_group::2.
+
+// One warp of each CTA of the pair: the same `ncols` TMEM columns in both.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst, uint32_t ncols)
+{
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols)
+{
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mma_bf16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                              uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.u32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive once on this CTA's `bar` when the pair MMAs issued so far have completed.
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar)
+{
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        : "memory");
+}
+
+// The same, arriving on the mbarrier at offset `bar` in both CTAs of the pair.
+__device__ __forceinline__ void mma_commit_pair_both(uint32_t bar)
+{
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
+        "[%0], %1;" ::"r"(bar),
+        "h"(uint16_t(3))
+        : "memory");
+}
+
+// Tiled load into this CTA's shared memory whose bytes complete on an mbarrier of
+// either CTA of the pair (`bar`: its cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap *map, int x, int y,
+                                                 uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
 // ---------------------------------------------------------------- tiled TMA
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y,

@@ -172,10 +172,11 @@ int lora_fused(lora_ctx *ctx, const lora_table *table, const int32_t *ids_host,
  * base weight, row-major d_in x d_out, as for lora_merge), y [n, ldy] bf16 written
  * (never read: every row of y is overwritten, released rows included).  The
  * shrink kernels first write v = x_i A_k (fp32) into context scratch; then one
- * tensor-core GEMM over 128 x 256 tiles accumulates x W and, in the same
- * accumulator, the adapter terms of the tile's rows (s_k v as a pair of bf16
- * operands, hi + lo, about 16 significant bits, times B_k).  Errors (nothing
- * launched): as lora_fused, and LORA_E_INVAL for W. */
+ * tensor-core GEMM over 256 x 256 tiles (each computed by a pair of CTAs on two
+ * SMs) accumulates x W and, in the same accumulator, the adapter terms of the
+ * tile's rows (s_k v as a pair of bf16 operands, hi + lo, about 16 significant
+ * bits, times B_k).  Errors (nothing launched): as lora_fused, and LORA_E_INVAL
+ * for W. */
 int lora_base_fused(lora_ctx *ctx, const lora_table *table, const int32_t *ids_host,
                     int64_t n, const void *x, int64_t ldx, int d_in, const void *W, int64_t ldw,
                     void *y, int64_t ldy, int d_out, void *stream);

@@ -49,23 +49,31 @@ def _report(stats):
 
 
 SMALL = {
-    # three 128-row blocks (the last one 44 rows), d_in not a multiple of the 64-wide
-    # K block, d_out = 256 + 136 (a ragged second column block), mixed ranks with a
-    # padded one, paged adapters, released rows, blocks holding several adapters
+    # two 256-row pair blocks (the second one 44 rows, so its second CTA's half lies
+    # wholly past n), d_in not a multiple of the 64-wide K block, d_out = 256 + 136
+    # (a ragged second column block whose second CTA holds 8 valid columns), mixed
+    # ranks with a padded one, paged adapters, released rows, blocks holding several
+    # adapters
     "ragged_mixed": dict(seed=201, n=300, d_in=200, d_out=392, n_adapters=4,
                          ranks=[8, 24, 64, 128], paged=True, release_frac=0.15),
     # long runs of one adapter: blocks with a single term (no masked rows)
     "runs": dict(seed=202, n=512, d_in=256, d_out=512, n_adapters=2, ranks=[64, 16],
                  ids=np.repeat(np.array([1, 0, -1, 1], np.int32), 128)),
-    # 32 x 10 = 320 tiles over at most 152 CTAs, so a CTA runs two or three tiles in a
-    # row (both accumulators, the stage ring wrapping across tiles), with 16 K blocks
-    # per tile -- more than the ring holds -- before each block's adapter stages;
-    # runs of several lengths, released rows, blocks with one to three adapters
+    # 16 x 10 = 160 tiles over at most 76 CTA pairs, so a pair runs two or three tiles
+    # in a row (both accumulators, the stage ring wrapping across tiles), with 16 K
+    # blocks per tile -- more than the ring holds -- before each block's adapter
+    # stages; runs of several lengths, released rows, blocks with one to three
+    # adapters, and blocks whose two halves hold different adapters
     "multi_tile": dict(seed=206, n=4096, d_in=1024, d_out=2560, n_adapters=3,
                        ranks=[16, 64, 32], paged=True,
                        ids=np.repeat(np.array([0, 1, -1, 2, 1, 0, 2, -1, 1, 2], np.int32),
                                      [700, 300, 57, 900, 441, 128, 1000, 3, 300, 267])),
-    # one row per adapter (a decode-like block with many terms)
+    # the first CTA's half of the pair released, the second's all one adapter: the
+    # term's stages carry rows in one half only
+    "second_half_only": dict(seed=207, n=256, d_in=192, d_out=512, n_adapters=2, ranks=[32, 16],
+                             ids=np.repeat(np.array([-1, 1], np.int32), 128)),
+    # one row per adapter (a decode-like block with many terms, all in the first
+    # CTA's half of the pair)
     "many_terms": dict(seed=203, n=40, d_in=128, d_out=256, n_adapters=40, ranks=[16] * 40,
                        ids=np.arange(40, dtype=np.int32)),
 }
