@@ -21,10 +21,12 @@ __all__ = ["LoraError", "Context", "AdapterTable", "lora_plan_build", "lora_shri
            "lora_expand", "lora_fused", "lora_fused_noalloc", "lora_base_fused", "PreparedFused", "lora_merge", "lora_unmerge", "lora_page_in", "lora_fused_device_ids", "lora_tune_shape",
            "KIND_ROWS_FUSED", "KIND_SHRINK", "KIND_EXPAND", "KIND_TILE_FUSED", "KIND_MERGE",
            "OPT_TILE_PATH", "OPT_MERGE_KERNEL", "OPT_TILE_MIN_RUN", "OPT_EARLY_PAGES", "OPT_DEVICE_PLAN",
+           "OPT_EARLY_INPUT",
            "library_path"]
 
 KIND_ROWS_FUSED, KIND_SHRINK, KIND_EXPAND, KIND_TILE_FUSED, KIND_MERGE = range(5)
 OPT_TILE_PATH, OPT_MERGE_KERNEL, OPT_TILE_MIN_RUN, OPT_EARLY_PAGES, OPT_DEVICE_PLAN = 1, 2, 3, 4, 5
+OPT_EARLY_INPUT = 6
 ERROR_NAMES = {0: "LORA_OK", -1: "LORA_E_INVAL", -2: "LORA_E_RANK", -3: "LORA_E_ADAPTER",
                -4: "LORA_E_NOT_RESIDENT", -5: "LORA_E_PAGE", -6: "LORA_E_CUDA",
                -7: "LORA_E_TIMEOUT", -8: "LORA_E_NOMEM", -9: "LORA_E_CAPACITY",
@@ -158,7 +160,7 @@ class Context:
 
     def set_option(self, option: int, value: int):
         """LORA_OPT_* (see include/lora.h): OPT_TILE_PATH, OPT_MERGE_KERNEL,
-        OPT_TILE_MIN_RUN, OPT_EARLY_PAGES, OPT_DEVICE_PLAN."""
+        OPT_TILE_MIN_RUN, OPT_EARLY_PAGES, OPT_DEVICE_PLAN, OPT_EARLY_INPUT."""
         _check(_L.lora_ctx_set_option(self.handle, int(option), int(value)), self)
 
     def profile_begin(self, every: int = 1):

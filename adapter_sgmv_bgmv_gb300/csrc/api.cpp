@@ -103,6 +103,8 @@ struct lora_ctx {
     int tile_path = 1;              // 1: long same-adapter runs use the tensor-core tiles
     int tile_min_run_override = 0;  // > 0: fixed minimum run for the tile path
     int early_pages = 0;            // LORA_OPT_EARLY_PAGES
+    int early_input = 0;            // LORA_OPT_EARLY_INPUT
+    bool call_early_x = false;      // this call's shrink may load x before its wait
     int call_early = 0;             // early page copies for the call in progress
     int device_plan = 0;            // LORA_OPT_DEVICE_PLAN
     cudaStream_t pool_write_stream = nullptr;   // stream of the last page-in ...
@@ -194,6 +196,7 @@ void begin_call(lora_ctx *ctx, cudaStream_t stream)
 {
     ctx->untuned = false;
     ctx->call_early = ctx->early_pages && !(ctx->pool_write_pending && ctx->pool_write_stream == stream);
+    ctx->call_early_x = ctx->early_input && !(ctx->pool_write_pending && ctx->pool_write_stream == stream);
 }
 
 // A launch of a delta / merge call: after it, the stream's previous kernel is no
@@ -812,6 +815,10 @@ int run_tiles(lora_ctx *ctx, const lora_table *t, int mode, const void *x, int64
     p.n_items = int(pl.tile_items.size());
     p.vmode = mode == kFused ? 0 : 1;
     p.max_tile_rank = pl.tile_max_rank;
+    // x ahead of the wait when the caller allows it and no copy into the row matrix
+    // runs just before; y ahead of the expand's wait when the shrink runs just before.
+    p.early_x = (ctx->call_early_x && !mats.staged) ? 1 : 0;
+    p.early_tiles = mode == kFused ? 1 : 0;
     // The dense copy (if any) is timed with the kernel that first reads it.
     if (mode != kExpand) {
         const long ev = prof_start(ctx, 1, stream);
@@ -1892,6 +1899,7 @@ int lora_ctx_set_option(lora_ctx *ctx, int option, int value)
         ctx->tile_min_run_override = value;
         return LORA_OK;
     case LORA_OPT_EARLY_PAGES: ctx->early_pages = value ? 1 : 0; return LORA_OK;
+    case LORA_OPT_EARLY_INPUT: ctx->early_input = value ? 1 : 0; return LORA_OK;
     case LORA_OPT_DEVICE_PLAN: ctx->device_plan = value ? 1 : 0; return LORA_OK;
     default: return LORA_E_INVAL;
     }

@@ -128,6 +128,8 @@ struct TileParams {
     int vmode;                // 0: V tiles (fused), 1: fp32 v rows
     int max_tile_rank;        // largest rank among the items (sizes shared memory)
     int ksplit;               // fused: K-split of the shrink (1..8)
+    int early_x;              // shrink: x and A loads and MMAs before the dependency wait
+    int early_tiles;          // expand right after its shrink: y and B loads before it
     int items_inline;         // 1: the list is inl[0 .. n_items)
     TileItem inl[kInlineTiles];
 };

@@ -22,7 +22,7 @@
 // one into its own shared memory, and its TMEM holds those 128 rows of the 256 x 256
 // fp32 accumulator.  Against one CTA per 128 x 256 tile, every SM fills a third less
 // shared memory per MMA flop (32 KB per K block of 64 instead of 48 KB), and the
-// ring holds six stages.  Tiles go in groups of 8 row blocks (row blocks fastest
+// ring holds six stages.  Tiles go in groups of 16 row blocks (row blocks fastest
 // within a group, so that a 256-column slice of W is fetched once per group and the
 // group's x blocks stay in L2).  Per tile the accumulator (two of them, so that one
 // tile's epilogue overlaps the next tile's MMAs) takes
@@ -87,7 +87,7 @@ __host__ __device__ inline uint32_t proj_smem_bytes()
 // column block with its row blocks fastest, so that the pairs running at one time
 // share a few x blocks and each 256-column slice of W is fetched from DRAM once per
 // group (x, W and y stay streaming; W is not assumed to stay in L2).
-constexpr int kGroupM = 8;
+constexpr int kGroupM = 16;
 __device__ __forceinline__ void tile_coords(const ProjParams &p, int t, int &m, int &nb)
 {
     const int gsize = kGroupM * p.n_nblk;

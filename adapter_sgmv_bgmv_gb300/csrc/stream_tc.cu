@@ -280,8 +280,13 @@ __global__ void __launch_bounds__(kThreads) k_stream_tc(const __grid_constant__ 
     tc::fence_after_sync();
     const uint32_t tmem = *reinterpret_cast<const uint32_t *>(gbase + (tmem_slot - base));
     // Launched as a programmatic dependent: everything above overlapped the previous
-    // kernel; y / W, V and the row matrices may be its to write.
-    grid_dep_wait();
+    // kernel; y / W, V and the row matrices may be its to write.  Right after the
+    // shrink of the same call (early_tiles) that kernel writes only the partials, and
+    // it let this one start only once the kernel before it had completed: the
+    // producer's y and B loads and the MMA warp (shared memory and TMEM only) go
+    // ahead, and the warps that read the partials or write global memory wait.
+    if (!(a.left == kLeftVParts && a.p.early_tiles) || warp >= 2)
+        grid_dep_wait();
     bool ok = true;
 
     if (warp == 0) {

@@ -36,22 +36,24 @@ namespace lora {
 namespace {
 
 constexpr int kTM = 128;                       // rows per tile
-constexpr int kKB = 64;                        // K elements per stage (one 128-byte row)
+constexpr int kKB = 64;                        // K elements per box (one 128-byte row)
+constexpr int kSub = 2;                        // boxes per stage: 256 bytes of each x row
 constexpr int kMaxStages = 8;
-constexpr uint32_t kXStage = kTM * 128;        // 16 KB
+constexpr uint32_t kXBox = kTM * 128;          // 16 KB
+constexpr uint32_t kXStage = kSub * kXBox;
 constexpr uint32_t kRingBudget = 100u * 1024u; // two CTAs per SM
 
 // Stage ring of the launch, sized by its largest padded rank: X block + A block.
 struct ShrinkRing {
-    uint32_t a_stage, stage;
+    uint32_t a_box, stage;
     int stages;
 };
 __host__ __device__ inline ShrinkRing shrink_ring(int max_rank)
 {
     ShrinkRing g;
     const int rpm = (max_rank + 15) & ~15;
-    g.a_stage = uint32_t(rpm) * 128u;
-    g.stage = (kXStage + g.a_stage + 1023u) & ~1023u;
+    g.a_box = uint32_t(rpm) * 128u;
+    g.stage = (kXStage + kSub * g.a_box + 1023u) & ~1023u;
     g.stages = int(kRingBudget / g.stage);
     if (g.stages > kMaxStages)
         g.stages = kMaxStages;
@@ -95,7 +97,7 @@ __global__ void __launch_bounds__(kShrinkThreads, 2) k_shrink_tc(const __grid_co
     const int tile = blockIdx.x / KS, ks = blockIdx.x - (blockIdx.x / KS) * KS;
     const TileItem it = tile_item(p, tile);
     const int r = it.rank, rp = rank_pad16(r);
-    const int nkb_all = (p.d_in + kKB - 1) / kKB;
+    const int nkb_all = (p.d_in + kSub * kKB - 1) / (kSub * kKB);   // stages of kSub boxes
     const int per = (nkb_all + KS - 1) / KS;
     const int kb0 = ks * per;
     const int nkb = max(0, min(nkb_all, kb0 + per) - kb0);
@@ -117,7 +119,11 @@ __global__ void __launch_bounds__(kShrinkThreads, 2) k_shrink_tc(const __grid_co
     const uint32_t tmem = *reinterpret_cast<const uint32_t *>(gbase + (tmem_slot - base));
     // Launched as a programmatic dependent: everything above overlapped the previous
     // kernel; x, the row matrix and the partial slots may be its to write or read.
-    grid_dep_wait();
+    // With early_x the caller guarantees that it writes neither x nor the row matrix:
+    // the loads and the MMAs (shared memory and TMEM only) then go ahead, and only
+    // the epilogue, which writes global memory, waits.
+    if (!p.early_x)
+        grid_dep_wait();
 
     bool ok = true;
     if (warp == 0) {
@@ -129,13 +135,15 @@ __global__ void __launch_bounds__(kShrinkThreads, 2) k_shrink_tc(const __grid_co
                 if (!ok)
                     break;
                 const uint32_t xs = base + uint32_t(s) * kStage, as = xs + kXStage;
-                const int k0 = (kb0 + kb) * kKB;
-                mbar_arrive_expect_tx(full0 + 8 * s, kXStage + uint32_t(rp) * 128u);
-                tc::tma_load_2d(xs, &args.map, k0, it.row0, full0 + 8 * s);
-                tc::for_row_boxes(rp, [&](int off, int m) {
-                    tc::tma_load_2d(as + uint32_t(off) * 128u, &args.amap[m], k0, it.a_row + off,
-                                    full0 + 8 * s);
-                });
+                const int k0 = (kb0 + kb) * kSub * kKB;
+                mbar_arrive_expect_tx(full0 + 8 * s, kXStage + kSub * uint32_t(rp) * 128u);
+                for (int h = 0; h < kSub; ++h) {
+                    tc::tma_load_2d(xs + h * kXBox, &args.map, k0 + h * kKB, it.row0, full0 + 8 * s);
+                    tc::for_row_boxes(rp, [&](int off, int m) {
+                        tc::tma_load_2d(as + uint32_t(h * rp + off) * 128u, &args.amap[m], k0 + h * kKB,
+                                        it.a_row + off, full0 + 8 * s);
+                    });
+                }
             }
         }
         __syncwarp();
@@ -150,11 +158,14 @@ __global__ void __launch_bounds__(kShrinkThreads, 2) k_shrink_tc(const __grid_co
                 tc::fence_after_sync();
                 const uint32_t xs = base + uint32_t(s) * kStage, as = xs + kXStage;
 #pragma unroll
-                for (int k4 = 0; k4 < kKB / 16; ++k4) {
-                    const uint64_t da = tc::smem_desc_sw128(xs + 32u * k4, 16u, 1024u);
-                    const uint64_t db = tc::smem_desc_sw128(as + 32u * k4, 16u, 1024u);
-                    tc::mma_bf16(tmem, da, db, idesc, (kb > 0 || k4 > 0) ? 1u : 0u);
-                }
+                for (int h = 0; h < kSub; ++h)
+#pragma unroll
+                    for (int k4 = 0; k4 < kKB / 16; ++k4) {
+                        const uint64_t da = tc::smem_desc_sw128(xs + h * kXBox + 32u * k4, 16u, 1024u);
+                        const uint64_t db =
+                            tc::smem_desc_sw128(as + uint32_t(h * rp) * 128u + 32u * k4, 16u, 1024u);
+                        tc::mma_bf16(tmem, da, db, idesc, (kb > 0 || h > 0 || k4 > 0) ? 1u : 0u);
+                    }
                 tc::mma_commit(empty0 + 8 * s);
             }
             tc::mma_commit(done);
@@ -163,8 +174,12 @@ __global__ void __launch_bounds__(kShrinkThreads, 2) k_shrink_tc(const __grid_co
     } else {
         // Epilogue: this warp reads TMEM lanes 32*(warp%4) .. +31.
         ok = mbar_wait_bounded(done, 0, p.status, kDevTimeoutMma);
+        if (p.early_x)
+            grid_dep_wait();
+        // The expand may start on freed SMs (and load y ahead of its own wait): the
+        // kernel before this one has completed by now.
         if (tid == 64)
-            grid_dep_launch();   // the expand may start its set-up on freed SMs
+            grid_dep_launch();
         ok = __all_sync(0xffffffffu, ok);   // warp converged and agreed before tcgen05.ld
         tc::fence_after_sync();
         const int row = 32 * (warp & 3) + lane;

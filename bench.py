@@ -84,17 +84,19 @@ FAMILY_SOURCES = {
 }
 KERNEL_NAMES = {"rows": "k_rows_inline<fused>", "shrink": "k_shrink_tc (+ k_stage_rows)",
                 "expand": "k_stream_tc(expand)", "merge": "k_stream_tc(merge)",
-                "proj": "k_proj_tc (base GEMM + adapter term)"}
+                "proj": "k_proj_tc (base GEMM + adapter term, + k_proj_prep)"}
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
 
 
-def config_for(name: str, early_pages: bool = True, device_ids: bool = False) -> dict:
+def config_for(name: str, early_pages: bool = True, device_ids: bool = False,
+               early_input: bool = True) -> dict:
     """The line's `config` (the same dict for both arms: a function of the workload)."""
     return {"workload": WORKLOAD_DESC[name], "name": name,
             "l2": "inputs rotate over device copies; one pass touches more than 3 x the "
                   "129 MB L2 (no flush needed)",
             "parallelism": "single GPU (replicas under torchrun)",
-            "early_pages": bool(early_pages), "device_ids": bool(device_ids)}
+            "early_pages": bool(early_pages), "early_input": bool(early_input),
+            "device_ids": bool(device_ids)}
 
 
 # --------------------------------------------------------------------------- peaks
@@ -986,7 +988,7 @@ def headline_line(name, m, args, world):
             "steps": m["steps"], "warmup": m["warmup"], "ms_per_step": m["ms_per_step"],
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
-            "config": config_for(name, not args.no_early_pages, args.device_ids)}
+            "config": config_for(name, not args.no_early_pages, args.device_ids, not args.no_early_input)}
     for k in ("us_per_call", "roofline", "gpu_launches", "clocks", "e2e", "cpu_baseline",
               "l2_sets", "n_act_curve"):
         if k in m:
@@ -995,7 +997,7 @@ def headline_line(name, m, args, world):
 
 
 def entry(name, m, args):
-    e = {"config": config_for(name, not args.no_early_pages, args.device_ids)}
+    e = {"config": config_for(name, not args.no_early_pages, args.device_ids, not args.no_early_input)}
     e.update({k: v for k, v in m.items()})
     return e
 
@@ -1021,6 +1023,8 @@ def main():
                     help="host threads for the oracle (0: every core)")
     ap.add_argument("--no-early-pages", action="store_true",
                     help="keep the adapter-page copies behind the dependency wait")
+    ap.add_argument("--no-early-input", action="store_true",
+                    help="keep the tensor-core shrink's x loads behind the dependency wait")
     ap.add_argument("--profile-every", type=int, default=8,
                     help="bracket one kernel launch in N with CUDA events (roofline timing)")
     ap.add_argument("--tiles", default=os.path.join(ROOT, "adapter_sgmv_bgmv_gb300", "tiles.tbl"))
@@ -1052,8 +1056,10 @@ def main():
     if os.path.exists(args.tiles):
         ctx.tiles_load(args.tiles)
     # Every kernel the timed loop launches is this library's, none of which writes
-    # the adapter pools: the row-gather kernel may copy pages before its wait.
+    # the adapter pools or x: the row-gather kernel may copy pages, and the
+    # tensor-core shrink load x, before their waits.
     ctx.set_option(L.OPT_EARLY_PAGES, 0 if args.no_early_pages else 1)
+    ctx.set_option(L.OPT_EARLY_INPUT, 0 if args.no_early_input else 1)
     clocks = ClockSampler(torch, local)
     W = max(3, args.warmup)
     if args.all:
@@ -1189,7 +1195,7 @@ def run_reference(args):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": unit, "n_gpus": 1,
             "steps": K, "warmup": W, "ms_per_step": 1e3 * tot / K, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": config_for(name, not args.no_early_pages, args.device_ids),
+            "config": config_for(name, not args.no_early_pages, args.device_ids, not args.no_early_input),
             "cpu_baseline": {"value": value, "unit": unit, "cores": nthreads, "kind": "oracle",
                              "sample": f"each step: about {per_step:.2f} s of the oracle on "
                                        f"the workload's rows ({desc.split(',')[0]} in the last)"},

@@ -344,13 +344,25 @@ int lora_sync_status(lora_ctx *ctx, void *stream);
  *                          For lora_fused_device_ids in its default mode the guarantee
  *                          covers the device ids as well: with 1 the kernel reads them
  *                          (and copies the pages they select) before the wait.
+ *   LORA_OPT_EARLY_INPUT   0 (default) / 1.  With 1 the tensor-core shrink of a delta
+ *                          call loads x and the A rows, and runs its MMAs, before
+ *                          waiting for the kernel launched immediately before it (only
+ *                          its writes of v or of the partial sums wait), so that its
+ *                          reads overlap that kernel's tail.  The caller then
+ *                          guarantees that no kernel launched immediately before a
+ *                          delta call in the same stream writes x or the pools (a
+ *                          kernel that writes y, such as the base projection or the
+ *                          previous call's expand, is fine; a copy or a host-side wait
+ *                          in between is enough).  Not applied to a call whose own
+ *                          dense copy of scattered adapters runs just before its
+ *                          shrink, nor after a page-in on the same stream.
  *   LORA_OPT_DEVICE_PLAN   lora_fused_device_ids: 0 (default) one row per row-gather
  *                          cluster, its adapter read from the device ids by the kernel
  *                          itself (one launch); 1 a plan kernel first groups the rows by
  *                          adapter into items of several rows (two launches, fewer
  *                          re-reads of a shared adapter). */
 enum { LORA_OPT_TILE_PATH = 1, LORA_OPT_MERGE_KERNEL = 2, LORA_OPT_TILE_MIN_RUN = 3,
-       LORA_OPT_EARLY_PAGES = 4, LORA_OPT_DEVICE_PLAN = 5 };
+       LORA_OPT_EARLY_PAGES = 4, LORA_OPT_DEVICE_PLAN = 5, LORA_OPT_EARLY_INPUT = 6 };
 int lora_ctx_set_option(lora_ctx *ctx, int option, int value);
 
 /* Per-launch timing: between lora_profile_begin and lora_profile_end every
