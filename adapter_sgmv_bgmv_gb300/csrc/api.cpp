@@ -437,6 +437,7 @@ int run_rows(lora_ctx *ctx, const lora_table *t, int mode, RowsCfg cfg, const vo
     p.d_out = d_out;
     p.n_items = int(pl.row_items.size());
     p.early_pages = ctx->call_early;
+    p.early_x = ctx->call_early_x;
     const long ev = prof_start(ctx, 0, stream);
     ctx->rows_last_inline = in_params;
     ctx->rows_last_smem = smem;
@@ -901,6 +902,7 @@ int delta_call(lora_ctx *ctx, const lora_table *t, int mode, const int32_t *ids,
                 q.rank = t->d_rank;
                 q.scale = t->d_scale;
                 q.early_pages = ctx->call_early;
+                q.early_x = ctx->call_early_x;
             };
             if (e->small) {
                 patch(e->small_args.p);
@@ -1715,6 +1717,7 @@ int lora_fused_device_ids(lora_ctx *ctx, const lora_table *t, const int32_t *ids
     p.early_pages = 0;   // planned: the plan is the previous kernel's output
     if (!ctx->device_plan) {
         p.early_pages = ctx->call_early;   // ids and pages read ahead of the wait
+        p.early_x = ctx->call_early_x;
         p.ids_dev = ids_dev;
         p.ok = t->d_ok;
         p.n_adapters = t->n_adapters;

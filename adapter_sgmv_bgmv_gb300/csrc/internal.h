@@ -61,6 +61,7 @@ struct RowsParams {
     int slice_out;            // elements of d_out per CTA (multiple of 8)
     int rows_alloc;           // shared-memory rows per item (>= every item's nrows)
     int early_pages;          // 1: adapter page copies issued before the dependency wait
+    int early_x;              // 1: x, the shrink and the exchange before it as well
     int rank_alloc;           // shared-memory rank slots (>= every item's rank)
     const int32_t *n_items_dev;   // device-side plan: the item count (items past it idle),
                                   // read after the wait for the kernel that wrote the plan

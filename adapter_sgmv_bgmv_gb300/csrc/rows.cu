@@ -159,6 +159,18 @@ __device__ __forceinline__ void rows_body(const RowsParams &pin, const RowItem *
 
     // The partials exchanged per CTA: nrows x RA floats, sent in 16-byte pieces.
     const int xchunks = (nrows * RA + 3) >> 2;
+    // Ahead of the wait for the previous kernel: the adapter pages (early_pages, or
+    // early_x, whose guarantee covers the pools too), and with early_x also x, the
+    // shrink and the cluster exchange.  A fused call whose every thread has at most one
+    // output vector (y_late) then computes its expand term before the wait as well
+    // and afterwards only reads its y vectors, adds and stores.  Either way the next
+    // kernel may start as soon as this one's copies are out: whatever it reads of y or
+    // v waits for this kernel, and this kernel for the one before it.
+    const bool pages_early = p.early_pages || p.early_x;
+    const bool x_early = p.early_x && MODE != kExpand;
+    const int nvo_all = out_len >> 3;
+    const int ngroups = nrows == 1 ? 1 : (nrows + 1) >> 1;
+    const bool y_late = x_early && MODE == kFused && nvo_all * ngroups <= kThreads;
     if (tid == 0) {
         mbar_init(bar0, 1);
         mbar_init(bar1, 1);
@@ -213,32 +225,43 @@ __device__ __forceinline__ void rows_body(const RowsParams &pin, const RowItem *
                          p.b_pool + int64_t(qb) * p.b_pw + out0, out_bytes, bar1);
         }
     };
+    auto issue_x = [&]() {
+        for (int q = lane; q < nrows; q += 32)
+            if (MODE != kExpand && in_bytes)
+                bulk_g2s(smem_u32(sX + size_t(q) * p.slice_in),
+                         p.x + int64_t(s_rows[q]) * p.ldx + in0, in_bytes, bar0);
+    };
+    auto issue_y = [&]() {
+        for (int q = lane; q < nrows; q += 32)
+            if (MODE != kShrink && out_bytes)
+                bulk_g2s(smem_u32(sY + size_t(q) * p.slice_out),
+                         p.y + int64_t(s_rows[q]) * p.ldy + out0, out_bytes, bar1);
+    };
     if (warp == 0) {
         if (lane == 0) {
             if (MODE != kExpand)
                 mbar_arrive_expect_tx(bar0, uint32_t(r + nrows) * in_bytes);
             if (MODE != kShrink)
-                mbar_arrive_expect_tx(bar1, uint32_t(r + nrows) * out_bytes);
+                mbar_arrive_expect_tx(bar1, uint32_t(y_late ? r : r + nrows) * out_bytes);
         }
         __syncwarp();
-        if (p.early_pages)
+        if (pages_early)
             issue_pages();
+        if (x_early)
+            issue_x();
     }
-    grid_dep_wait();
-    if (warp == 0) {
-        if (!p.early_pages)
-            issue_pages();
-        for (int q = lane; q < nrows; q += 32) {
-            const int row = s_rows[q];
-            if (MODE != kExpand && in_bytes)
-                bulk_g2s(smem_u32(sX + size_t(q) * p.slice_in), p.x + int64_t(row) * p.ldx + in0,
-                         in_bytes, bar0);
-            if (MODE != kShrink && out_bytes)
-                bulk_g2s(smem_u32(sY + size_t(q) * p.slice_out), p.y + int64_t(row) * p.ldy + out0,
-                         out_bytes, bar1);
+    if (x_early) {
+        grid_dep_launch();
+    } else {
+        grid_dep_wait();
+        if (warp == 0) {
+            if (!pages_early)
+                issue_pages();
+            issue_x();
+            issue_y();
         }
+        grid_dep_launch();
     }
-    grid_dep_launch();
 
     bool ok = true;
 
@@ -308,6 +331,12 @@ __device__ __forceinline__ void rows_body(const RowsParams &pin, const RowItem *
             }
         }
         __syncthreads();
+        if (x_early && !y_late) {
+            // Everything past here reads y or writes global memory.
+            grid_dep_wait();
+            if (warp == 0)
+                issue_y();
+        }
         if (MODE == kShrink && ok && crank == 0) {
             for (int q = tid; q < nrows * r; q += kThreads) {
                 const int i = q / r, j = q - (q / r) * r;
@@ -324,7 +353,51 @@ __device__ __forceinline__ void rows_body(const RowsParams &pin, const RowItem *
     }
 
     // ---- 4. expand into the CTA's d_out slice
-    if (MODE != kShrink) {
+    if (MODE != kShrink && y_late) {
+        // Thread w holds output vector q = w % nvo of rows 2 (w / nvo) and + 1 (one
+        // row when nrows == 1): the term is computed from B in shared memory before
+        // the wait, y is read straight from global memory after it.
+        ok = mbar_wait_bounded(bar1, 0, p.status, kDevTimeoutLoad) && ok;
+        const int nvo = nvo_all;
+        const int w = tid, q = nvo > 0 ? w % nvo : 0;
+        const int i0 = nvo > 0 ? (w / nvo) * 2 : 0;
+        const bool act = w < nvo * ngroups;
+        const int nr = nrows == 1 ? 1 : min(2, nrows - i0);
+        float acc[2][8];
+        if (act) {
+            if (nr == 2) {
+                expand_vec<2>(sB, p.slice_out, vsum, RA, r, i0, q, acc);
+            } else {
+                float a1[1][8];
+                expand_vec<1>(sB, p.slice_out, vsum, RA, r, i0, q, a1);
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    acc[0][e] = a1[0][e];
+            }
+        }
+        grid_dep_wait();
+        if (act) {
+            uint4 yv[2];
+            uint16_t *yp[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u)
+                if (u < nr) {
+                    yp[u] = p.y + int64_t(s_rows[i0 + u]) * p.ldy + out0 + 8 * q;
+                    yv[u] = *reinterpret_cast<const uint4 *>(yp[u]);
+                }
+#pragma unroll
+            for (int u = 0; u < 2; ++u)
+                if (u < nr) {
+                    float yf[8];
+                    unpack8(yv[u], yf);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        yf[e] = fmaf(s, acc[u][e], yf[e]);
+                    if (ok)
+                        *reinterpret_cast<uint4 *>(yp[u]) = pack8(yf);
+                }
+        }
+    } else if (MODE != kShrink) {
         ok = mbar_wait_bounded(bar1, 0, p.status, kDevTimeoutLoad) && ok;
         const int nvo = out_len >> 3;
         if (nrows == 1) {

@@ -344,18 +344,24 @@ int lora_sync_status(lora_ctx *ctx, void *stream);
  *                          For lora_fused_device_ids in its default mode the guarantee
  *                          covers the device ids as well: with 1 the kernel reads them
  *                          (and copies the pages they select) before the wait.
- *   LORA_OPT_EARLY_INPUT   0 (default) / 1.  With 1 the tensor-core shrink of a delta
- *                          call loads x and the A rows, and runs its MMAs, before
- *                          waiting for the kernel launched immediately before it (only
- *                          its writes of v or of the partial sums wait), so that its
- *                          reads overlap that kernel's tail.  The caller then
- *                          guarantees that no kernel launched immediately before a
- *                          delta call in the same stream writes x or the pools (a
- *                          kernel that writes y, such as the base projection or the
- *                          previous call's expand, is fine; a copy or a host-side wait
- *                          in between is enough).  Not applied to a call whose own
- *                          dense copy of scattered adapters runs just before its
- *                          shrink, nor after a page-in on the same stream.
+ *   LORA_OPT_EARLY_INPUT   0 (default) / 1.  With 1 a delta call reads x and the
+ *                          adapters before waiting for the kernels before it in the
+ *                          stream: the tensor-core shrink loads x and the A rows and
+ *                          runs its MMAs, the row-gather kernel also computes its
+ *                          cluster's v and (when each thread has one output vector)
+ *                          its term s_k v B_k; only the reads of y and the writes of
+ *                          y, v and the partial sums wait.  Consecutive row-gather
+ *                          calls then overlap almost whole.  The caller guarantees
+ *                          that x and the pools are written neither by the kernel
+ *                          launched immediately before a delta call in the same stream
+ *                          nor by an earlier call of this library on that stream since
+ *                          the last kernel that is not this library's (a kernel that
+ *                          writes y, such as the base projection, is fine; so is a
+ *                          chain of delta calls on one x; a copy or a host-side wait
+ *                          in between is enough; one call's y passed as the next
+ *                          call's x is not).  Not applied to a call whose own dense
+ *                          copy of scattered adapters runs just before its shrink, nor
+ *                          after a page-in on the same stream.
  *   LORA_OPT_DEVICE_PLAN   lora_fused_device_ids: 0 (default) one row per row-gather
  *                          cluster, its adapter read from the device ids by the kernel
  *                          itself (one launch); 1 a plan kernel first groups the rows by

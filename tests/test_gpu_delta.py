@@ -336,43 +336,59 @@ def test_early_staging_changes_nothing(ctx):
     assert_parity(got[1][0], ref, REL_FROB, MAX_ABS_RMS, "early staging")
 
 
-@pytest.mark.parametrize("name", ["valora_prefill", "runs_with_releases"])
+@pytest.mark.parametrize("name", ["valora_prefill", "runs_with_releases", "llama7b_decode_het",
+                                  "llama7b_decode_hom", "lorazor_decode", "llama7b_decode_het:dev"])
 def test_early_input_changes_nothing(ctx, name):
     """LORA_OPT_EARLY_INPUT lets the tensor-core shrink load x and run its MMAs before
-    the previous kernel ends, and the expand of a fused call loads its first y tiles
-    before its shrink ends.  Four calls back to back that accumulate into the same y
-    (each call's expand reads what the previous one wrote) give bit-identical results
-    with the options off, and one call is within the bar of the oracle."""
-    c = (workloads.make(name, seed=3) if name == "valora_prefill"
-         else workloads.small(**TILE_CASES[name]))
+    the previous kernel ends (the expand of a fused call loads its first y tiles
+    before its shrink ends), and the row-gather kernel load x, shrink, exchange and
+    compute its expand term before the wait, reading y only after it.  Four calls back
+    to back that accumulate into the same y (each call reads what the previous one
+    wrote) give bit-identical results with the options off, and one call is within
+    the bar of the oracle."""
+    wl, _, mode = name.partition(":")
+    if wl in TILE_CASES:
+        c = workloads.small(**TILE_CASES[wl])
+    else:
+        c = workloads.make(wl, seed=3)
+    ids = workloads.lorazor_ids(c, 0) if wl == "lorazor_decode" else c["ids"]
     table = upload_table(ctx, c)
     x = to_dev(c["x"])
+    ids_dev = torch.from_numpy(np.ascontiguousarray(ids, np.int32)).cuda()
+
+    def call(y):
+        if mode == "dev":
+            L.lora_fused_device_ids(ctx, table, ids_dev, x, y)
+        else:
+            L.lora_fused(ctx, table, ids, x, y)
+
+    tile = wl in ("valora_prefill",) or wl in TILE_CASES
     got = {}
     for early in (0, 1):
         ctx.set_option(L.OPT_EARLY_PAGES, early)
         ctx.set_option(L.OPT_EARLY_INPUT, early)
         try:
             y = to_dev(c["y"])
-            L.lora_fused(ctx, table, c["ids"], x, y)
+            call(y)
             ctx.sync_status()
-            assert ctx.last_path()[0] & 2
+            assert bool(ctx.last_path()[0] & 2) == tile
             first = from_dev(y)
             for _ in range(4):
-                L.lora_fused(ctx, table, c["ids"], x, y)
+                call(y)
             ctx.sync_status()
             got[early] = (first, from_dev(y))
         finally:
             ctx.set_option(L.OPT_EARLY_PAGES, 0)
             ctx.set_option(L.OPT_EARLY_INPUT, 0)
-    for a, b in zip(got[1], got[0]):
-        np.testing.assert_array_equal(a, b)
-    if name == "valora_prefill":
+    for a_, b_ in zip(got[1], got[0]):
+        np.testing.assert_array_equal(a_, b_)
+    if wl == "valora_prefill":
         rows = sample_rows(c, k=48)
         ref = oracle.fused_rows(oracle.Table.from_case(c), c["ids"], c["x"], c["y"], rows,
                                 nthreads=8)
         assert_parity(got[1][0][rows], ref, REL_FROB, MAX_ABS_RMS, name)
     else:
-        ref = oracle.fused(oracle.Table.from_case(c), c["ids"], c["x"], c["y"], nthreads=8)
+        ref = oracle.fused(oracle.Table.from_case(c), ids, c["x"], c["y"], nthreads=8)
         assert_parity(got[1][0], ref, REL_FROB, MAX_ABS_RMS, name)
 
 
