@@ -14,6 +14,9 @@ workloads this library is measured on is used.  Two objectives:
               inputs larger than L2, as a decode loop runs them: consecutive calls
               overlap (programmatic dependent launch), which the call-by-call timing
               cannot see.
+The search runs with LORA_OPT_EARLY_PAGES and LORA_OPT_EARLY_INPUT on (the way a
+decode loop of this library's calls runs, and the way bench.py measures); --no-early
+tunes with both off.
 """
 from __future__ import annotations
 
@@ -21,7 +24,7 @@ import argparse
 import os
 import tempfile
 
-from . import Context
+from . import OPT_EARLY_INPUT, OPT_EARLY_PAGES, Context
 
 DEFAULT_SHAPES = """\
 # kind   n      d_in  d_out  rank adapters run objective
@@ -40,8 +43,13 @@ def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--shapes", default=None, help="shape file (default: built-in list)")
     ap.add_argument("--out", required=True)
+    ap.add_argument("--no-early", action="store_true",
+                    help="tune with LORA_OPT_EARLY_PAGES and LORA_OPT_EARLY_INPUT off")
     args = ap.parse_args()
     ctx = Context(0, max_rows=1 << 15, max_rank=128)
+    early = 0 if args.no_early else 1
+    ctx.set_option(OPT_EARLY_PAGES, early)
+    ctx.set_option(OPT_EARLY_INPUT, early)
     path = args.shapes
     tmp = None
     if path is None:
