@@ -820,6 +820,8 @@ int run_tiles(lora_ctx *ctx, const lora_table *t, int mode, const void *x, int64
     // runs just before; y ahead of the expand's wait when the shrink runs just before.
     p.early_x = (ctx->call_early_x && !mats.staged) ? 1 : 0;
     p.early_tiles = mode == kFused ? 1 : 0;
+    // A shrink-only grid (one CTA per tile) that fits one CTA per SM gets the deeper ring.
+    p.wide_ring = (mode == kShrink && int64_t(pl.tile_items.size()) <= kSms) ? 1 : 0;
     // The dense copy (if any) is timed with the kernel that first reads it.
     if (mode != kExpand) {
         const long ev = prof_start(ctx, 1, stream);
@@ -1594,6 +1596,7 @@ int lora_base_fused(lora_ctx *ctx, const lora_table *t, const int32_t *ids, int6
     p.n_mblk = n_mblk;
     p.n_nblk = n_nblk;
     p.n_chunks = n_chunks;
+    p.early = n_chunks > 0 ? 1 : 0;   // the prep kernel runs just before the GEMM
     if (n_chunks > 0) {
         CUDA_TRY(ctx, launch_proj_prep(p, stream));
         count_launch(ctx, stream);

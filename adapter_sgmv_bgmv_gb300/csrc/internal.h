@@ -131,6 +131,7 @@ struct TileParams {
     int ksplit;               // fused: K-split of the shrink (1..8)
     int early_x;              // shrink: x and A loads and MMAs before the dependency wait
     int early_tiles;          // expand right after its shrink: y and B loads before it
+    int wide_ring;            // shrink: one CTA per SM, a ring of 200 KB instead of 100 KB
     int items_inline;         // 1: the list is inl[0 .. n_items)
     TileItem inl[kInlineTiles];
 };
@@ -249,6 +250,7 @@ struct ProjParams {
     int n_mblk;               // 256-row blocks (one per CTA pair)
     int n_nblk;               // 256-column blocks
     int n_chunks;
+    int early;                // launched right after k_proj_prep: x and W loads go ahead of the wait
 };
 cudaError_t launch_proj_prep(const ProjParams &p, cudaStream_t stream);
 cudaError_t launch_proj_tc(const ProjParams &p, cudaStream_t stream);

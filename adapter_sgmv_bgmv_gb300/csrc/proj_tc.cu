@@ -152,8 +152,11 @@ __global__ void __launch_bounds__(kPM) k_proj_prep(const __grid_constant__ ProjP
     const int i = blockIdx.x, t = threadIdx.x;
     const ProjChunk ch = load_chunk(p, i);
     const int row = ch.m * kPM + t;
-    // v and the ids are the shrink's and the host copy's: wait for the kernel before.
+    // v is the shrink's: wait for the kernels before.  Then the GEMM may start: before
+    // its own wait it reads only x and W, and every kernel before this one has
+    // completed by now.
     grid_dep_wait();
+    grid_dep_launch();
     const bool mine = row < p.n && __ldg(p.ids + row) == ch.adapter;
     float4 v[16];
     const float *vrow = p.v + int64_t(row) * p.ldv + ch.c;   // ldv: a multiple of 4
@@ -161,7 +164,6 @@ __global__ void __launch_bounds__(kPM) k_proj_prep(const __grid_constant__ ProjP
     for (int q = 0; q < 16; ++q)
         v[q] = (mine && ch.c + 4 * q < ch.rank) ? __ldg(reinterpret_cast<const float4 *>(vrow) + q)
                                                 : make_float4(0.f, 0.f, 0.f, 0.f);
-    grid_dep_launch();
     uint4 *hi = reinterpret_cast<uint4 *>(p.a_prep + (int64_t(2 * i) * kPM + t) * kBK);
     uint4 *lo = reinterpret_cast<uint4 *>(p.a_prep + (int64_t(2 * i + 1) * kPM + t) * kBK);
 #pragma unroll
@@ -231,9 +233,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     cluster_sync();
     tc::fence_after_sync();
     const uint32_t tmem = *reinterpret_cast<const uint32_t *>(gbase + (tmem_slot - base));
-    // Launched as a programmatic dependent of the prep kernel: everything above
-    // overlapped its tail.
-    grid_dep_wait();
+    // Launched as a programmatic dependent of the prep kernel (early), which lets it
+    // start once every kernel before the prep has completed: the base stages' x and W
+    // loads and the MMAs (shared memory and TMEM only) go ahead while the prep runs;
+    // the producer waits before its first adapter stage (the prepared operands, the
+    // B rows), the epilogue before its first store.  Without a prep kernel before
+    // it, everything waits here.
+    if (!p.early)
+        grid_dep_wait();
 
     const int n_tiles = p.n_mblk * p.n_nblk;
     const int nkb = (p.d_in + kBK - 1) / kBK;
@@ -246,6 +253,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // fill, full byte count), so that both CTAs' byte counts are fixed per stage.
         if (lane == 0) {
             uint32_t g = 0;
+            bool waited = !p.early;
             BlockChunks cur{}, nxt{};
             if (pair < n_tiles) {
                 int m, nb;
@@ -285,6 +293,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     tc::tma_load_2d_pair(stage_b(s) + kBAtom, &a.wmap, n0 + 64, kb * kBK, fb);
                 }
                 for_chunk_stages(p, cur, [&](int i, const ProjChunk &ch, int half) {
+                    if (!waited) {
+                        grid_dep_wait();
+                        waited = true;
+                    }
                     const int s = next_slot(kAStage + 2u * uint32_t(ch.kc) * 128u);
                     if (!ok)
                         return false;
@@ -300,6 +312,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 });
                 cur = nxt;
             }
+            if (!waited)
+                grid_dep_wait();
             grid_dep_launch();   // every load issued: the next kernel may start its set-up
             if (!ok && leader) {
                 // Let the loads already issued (both CTAs' bytes complete here) land
@@ -375,6 +389,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------ epilogue
         const int q4 = warp & 3;                       // TMEM lanes 32*q4 .. 32*q4+31
         const int r_in = 32 * q4 + lane;               // this thread's row of the CTA's half
+        if (p.early)
+            grid_dep_wait();
         int lt = 0;
         for (int tile = pair; tile < n_tiles; tile += npairs, ++lt) {
             int m, nb;

@@ -18,7 +18,8 @@
 //            rank-padding columns written as zeros) or into the caller's v rows
 //            (shrink-only call, one CTA per tile).
 // Shared memory is sized for two CTAs per SM, so the ksplit x tiles grid (at most
-// two per SM by construction) is resident in one wave.  The kernel is launched as
+// two per SM by construction) is resident in one wave; a grid of at most one CTA per
+// SM (a shrink-only call with few tiles) takes a ring twice as deep instead.  The kernel is launched as
 // a programmatic dependent of the one before it: barrier set-up and the TMEM
 // allocation overlap that kernel's tail, and the expand is released to start its
 // own set-up once every CTA has issued its last MMA.
@@ -42,19 +43,20 @@ constexpr int kMaxStages = 8;
 constexpr uint32_t kXBox = kTM * 128;          // 16 KB
 constexpr uint32_t kXStage = kSub * kXBox;
 constexpr uint32_t kRingBudget = 100u * 1024u; // two CTAs per SM
+constexpr uint32_t kRingBudgetWide = 200u * 1024u;   // one CTA per SM (a grid of at most one per SM)
 
 // Stage ring of the launch, sized by its largest padded rank: X block + A block.
 struct ShrinkRing {
     uint32_t a_box, stage;
     int stages;
 };
-__host__ __device__ inline ShrinkRing shrink_ring(int max_rank)
+__host__ __device__ inline ShrinkRing shrink_ring(int max_rank, bool wide)
 {
     ShrinkRing g;
     const int rpm = (max_rank + 15) & ~15;
     g.a_box = uint32_t(rpm) * 128u;
     g.stage = (kXStage + kSub * g.a_box + 1023u) & ~1023u;
-    g.stages = int(kRingBudget / g.stage);
+    g.stages = int((wide ? kRingBudgetWide : kRingBudget) / g.stage);
     if (g.stages > kMaxStages)
         g.stages = kMaxStages;
     return g;
@@ -69,9 +71,9 @@ struct TileArgs {
 
 __host__ __device__ inline int rank_pad16(int r) { return (r + 15) & ~15; }
 
-__host__ __device__ inline uint32_t shrink_smem_bytes(int max_rank)
+__host__ __device__ inline uint32_t shrink_smem_bytes(int max_rank, bool wide)
 {
-    const ShrinkRing g = shrink_ring(max_rank);
+    const ShrinkRing g = shrink_ring(max_rank, wide);
     return 1024u + uint32_t(g.stages) * g.stage + 2u * kMaxStages * 8u + 64u;
 }
 
@@ -84,7 +86,7 @@ __global__ void __launch_bounds__(kShrinkThreads, 2) k_shrink_tc(const __grid_co
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t *gbase = smem_raw + (base - raw);
-    const ShrinkRing ring = shrink_ring(p.max_tile_rank);
+    const ShrinkRing ring = shrink_ring(p.max_tile_rank, p.wide_ring != 0);
     const int kStages = ring.stages;
     const uint32_t kStage = ring.stage;
     const uint32_t full0 = base + uint32_t(kStages) * kStage;
@@ -245,7 +247,7 @@ cudaError_t launch_shrink_tc(const TileParams &p, cudaStream_t stream)
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(unsigned(p.n_items) * unsigned(p.vmode == 0 ? p.ksplit : 1));
     cfg.blockDim = dim3(kShrinkThreads);
-    cfg.dynamicSmemBytes = shrink_smem_bytes(p.max_tile_rank);
+    cfg.dynamicSmemBytes = shrink_smem_bytes(p.max_tile_rank, p.wide_ring != 0);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

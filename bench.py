@@ -1114,6 +1114,7 @@ def run_probe(name: str) -> int:
     if os.path.exists(tiles):
         ctx.tiles_load(tiles)
     ctx.set_option(L.OPT_EARLY_PAGES, 1)
+    ctx.set_option(L.OPT_EARLY_INPUT, 1)
 
     def n_sets(step_bytes):
         # copies enough that a pass over them is more than 3 x L2: the call a profiler
