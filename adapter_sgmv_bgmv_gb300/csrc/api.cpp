@@ -758,13 +758,14 @@ int run_tiles(lora_ctx *ctx, const lora_table *t, int mode, const void *x, int64
                                       stream));
         d_items = reinterpret_cast<const TileItem *>(slot->dev);
     }
-    // K-split of the fused shrink: about two CTAs per SM over all tiles, each CTA
-    // keeping at least 4 K blocks of 64.
+    // K-split of the fused shrink: at most one CTA per SM over all tiles (each with
+    // the deeper ring; fewer shares also leave the expand fewer partials to sum),
+    // each CTA keeping at least 4 K blocks of 64.
     int ksplit = 1;
     if (mode == kFused) {
         const int64_t tiles = int64_t(pl.tile_items.size());
         const int nkb = (d_in + 63) / 64;
-        while (ksplit < 8 && tiles * ksplit * 2 <= 2 * kSms && nkb / (ksplit * 2) >= 4 &&
+        while (ksplit < 8 && tiles * ksplit * 2 <= kSms && nkb / (ksplit * 2) >= 4 &&
                (!fixed || tiles * ksplit * 2 <= kNoAllocSlots))
             ksplit *= 2;
         const size_t need = size_t(tiles) * size_t(ksplit) * size_t(kVPartBytes);
@@ -820,8 +821,8 @@ int run_tiles(lora_ctx *ctx, const lora_table *t, int mode, const void *x, int64
     // runs just before; y ahead of the expand's wait when the shrink runs just before.
     p.early_x = (ctx->call_early_x && !mats.staged) ? 1 : 0;
     p.early_tiles = mode == kFused ? 1 : 0;
-    // A shrink-only grid (one CTA per tile) that fits one CTA per SM gets the deeper ring.
-    p.wide_ring = (mode == kShrink && int64_t(pl.tile_items.size()) <= kSms) ? 1 : 0;
+    // A grid that fits one CTA per SM gets the deeper ring.
+    p.wide_ring = (int64_t(pl.tile_items.size()) * ksplit <= kSms) ? 1 : 0;
     // The dense copy (if any) is timed with the kernel that first reads it.
     if (mode != kExpand) {
         const long ev = prof_start(ctx, 1, stream);

@@ -17,9 +17,8 @@
 //            CTA's partial slot (fused call; the expand sums the slots in order;
 //            rank-padding columns written as zeros) or into the caller's v rows
 //            (shrink-only call, one CTA per tile).
-// Shared memory is sized for two CTAs per SM, so the ksplit x tiles grid (at most
-// two per SM by construction) is resident in one wave; a grid of at most one CTA per
-// SM (a shrink-only call with few tiles) takes a ring twice as deep instead.  The kernel is launched as
+// A grid of at most one CTA per SM (the host picks the K-split so, where the tiles
+// allow) takes a 200 KB ring; a larger grid is sized for two CTAs per SM (100 KB).  The kernel is launched as
 // a programmatic dependent of the one before it: barrier set-up and the TMEM
 // allocation overlap that kernel's tail, and the expand is released to start its
 // own set-up once every CTA has issued its last MMA.

@@ -229,7 +229,7 @@ def test_tile_kernels_rank_128():
 
 def test_tile_kernels_eight_way_k_split(ctx):
     # nine tiles at d_in = 4096: the fused shrink splits K eight ways (the launcher
-    # doubles the split while tiles x split stays within two CTAs per SM and each CTA
+    # doubles the split while tiles x split stays within one CTA per SM and each CTA
     # keeps at least four 64-wide K blocks), so the expand sums eight partials per
     # tile, two batches of four shares; ragged last tiles (88 and 16 rows) and a
     # ragged last column chunk (d_out = 384 + 72)
