@@ -375,16 +375,24 @@ __device__ __forceinline__ void rows_body(const RowsParams &pin, const RowItem *
                     acc[0][e] = a1[0][e];
             }
         }
-        grid_dep_wait();
+        uint16_t *yp[2];
         if (act) {
-            uint4 yv[2];
-            uint16_t *yp[2];
+            // Bring the y vectors into L2 ahead of the wait (a hint: L2 stays coherent
+            // with the previous kernel's writes), so that the read after it hits L2.
 #pragma unroll
             for (int u = 0; u < 2; ++u)
                 if (u < nr) {
                     yp[u] = p.y + int64_t(s_rows[i0 + u]) * p.ldy + out0 + 8 * q;
-                    yv[u] = *reinterpret_cast<const uint4 *>(yp[u]);
+                    asm volatile("prefetch.global.L2 [%0];" ::"l"(yp[u]));
                 }
+        }
+        grid_dep_wait();
+        if (act) {
+            uint4 yv[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u)
+                if (u < nr)
+                    yv[u] = *reinterpret_cast<const uint4 *>(yp[u]);
 #pragma unroll
             for (int u = 0; u < 2; ++u)
                 if (u < nr) {
