@@ -38,9 +38,12 @@
 //   1      rank 0 only, MMA issuer: tcgen05.mma M = 256, N = 256, K = 16; a commit
 //          multicast to both CTAs frees each stage, and another hands each finished
 //          accumulator to both CTAs' epilogues;
-//   2-5    epilogue (both CTAs): TMEM -> registers -> bf16 -> y rows (16-byte
-//          stores); the accumulator goes back to rank 0's MMA warp once all eight
-//          warps of the pair have read it.
+//   2-5    epilogue (both CTAs): TMEM -> registers -> bf16 -> the warp's 32 x 64
+//          slab of y in shared memory (two slabs per warp, in turn) -> one TMA store
+//          per slab; the accumulator goes back to rank 0's MMA warp once all eight
+//          warps of the pair have read it.  (Per-thread 16-byte stores to 32
+//          different rows cost the producer and MMA warps, which share the SM's
+//          schedulers with the epilogue warps, ≈ 6 % of the kernel.)
 // The producer and the MMA warp read a block's chunk list for the next tile while
 // the current tile's base stages run, so that at a tile's end they go straight on.
 // Every wait is bounded (1 s); on expiry the status word records it, the stores are
@@ -69,18 +72,21 @@ constexpr uint32_t kBStage = 2 * kBAtom;            // 16 KB: this CTA's 128 col
 constexpr uint32_t kStage = kAStage + kBStage;      // 32 KB
 constexpr int kThreads = 192;
 constexpr uint32_t kTmemCols = 2 * kBN;             // two 256-column accumulators
+constexpr uint32_t kSlab = 32 * 128;                // 4 KB: 32 rows x 64 columns of y (bf16)
+constexpr uint32_t kEpiBytes = 4 * 2 * kSlab;       // two slabs per epilogue warp
 
 struct ProjArgs {
     CUtensorMap xmap;                               // x [n, d_in], 64 x 128 boxes
     CUtensorMap wmap;                               // W [d_in, d_out], 64 x 64 boxes
     CUtensorMap amap;                               // prepared left operands, 64 x 128 boxes
+    CUtensorMap ymap;                               // y [n, d_out], 64 x 32 boxes (stores)
     CUtensorMap bmap[3];                            // B row matrix, 64 x 16 / 32 / 64 boxes
     ProjParams p;
 };
 
 __host__ __device__ inline uint32_t proj_smem_bytes()
 {
-    return 1024u + uint32_t(kNS) * kStage + 256u;   // + barriers (2 x 6 x 8 B + 5 x 8 B + 4 B)
+    return 1024u + uint32_t(kNS) * kStage + kEpiBytes + 256u;   // + barriers (2 x 6 x 8 B + 5 x 8 B + 4 B)
 }
 
 // Tile t of the launch: groups of kGroupM row blocks, each group swept over every
@@ -200,7 +206,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const bool leader = crank == 0;
     const int pair = int(blockIdx.x >> 1), npairs = int(gridDim.x >> 1);
 
-    const uint32_t sBar = base + uint32_t(kNS) * kStage;
+    const uint32_t sEpi = base + uint32_t(kNS) * kStage;   // the epilogue warps' y slabs
+    const uint32_t sBar = sEpi + kEpiBytes;
     // barriers: full[6], empty[6], tfull[2], tempty[2], done; then the TMEM address.
     // full (rank 0's) counts both CTAs' bytes; empty and tfull get rank 0's commits
     // in both CTAs; tempty (rank 0's) one arrival per epilogue warp of the pair.
@@ -388,7 +395,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     } else {
         // ------------------------------------------------------------ epilogue
         const int q4 = warp & 3;                       // TMEM lanes 32*q4 .. 32*q4+31
-        const int r_in = 32 * q4 + lane;               // this thread's row of the CTA's half
+        const uint32_t my_slabs = sEpi + uint32_t(warp - 2) * 2u * kSlab;
+        int slab_use = 0;
         if (p.early)
             grid_dep_wait();
         int lt = 0;
@@ -403,10 +411,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             if (!ok)
                 break;
             tc::fence_after_sync();
-            const bool row_ok = row0 + r_in < p.n;
-            uint16_t *yrow = p.y + int64_t(row0 + r_in) * p.ldy + n0;
             const uint32_t ta = tmem + (uint32_t(32 * q4) << 16) + uint32_t(acc * kBN);
-            for (int c0 = 0; c0 < kBN; c0 += 64) {
+            for (int c0 = 0; c0 < kBN; c0 += 64, ++slab_use) {
                 uint32_t v[2][32];
                 tc::tmem_ld32_nowait(ta + uint32_t(c0), v[0]);
                 tc::tmem_ld32_nowait(ta + uint32_t(c0 + 32), v[1]);
@@ -422,20 +428,39 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                             mbar_arrive_remote(at_leader(tempty0 + 8 * acc));
                     }
                 }
+                // Row `lane` of the warp's 32 x 64 slab (128-byte swizzle), once the
+                // store issued from it two slabs ago has read it; then one TMA store
+                // of the slab (rows past n and columns past d_out are clipped).
+                const uint32_t slab = my_slabs + uint32_t(slab_use & 1) * kSlab;
+                if (lane == 0)
+                    tc::bulk_wait_read1();
+                __syncwarp();
+                uint8_t *sp = gbase + (slab - base);
 #pragma unroll
                 for (int h = 0; h < 2; ++h)
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
-                        const int col = c0 + 32 * h + 8 * u;
                         float f[8];
 #pragma unroll
                         for (int e = 0; e < 8; ++e)
                             f[e] = __uint_as_float(v[h][8 * u + e]);
-                        if (row_ok && n0 + col < p.d_out)
-                            *reinterpret_cast<uint4 *>(yrow + col) = pack8(f);
+                        *reinterpret_cast<uint4 *>(sp + tc::sw128(uint32_t(lane), uint32_t(4 * h + u))) =
+                            pack8(f);
                     }
+                tc::fence_proxy_async_smem();
+                __syncwarp();
+                // (a box wholly past n or d_out is not stored at all)
+                if (lane == 0) {
+                    if (row0 + 32 * q4 < p.n && n0 + c0 < p.d_out)
+                        tc::tma_store_2d(&a.ymap, n0 + c0, row0 + 32 * q4, slab);
+                    tc::bulk_commit();
+                }
             }
         }
+        // Every store has finished before the slabs (and the kernel) go away.
+        if (lane == 0)
+            tc::bulk_wait0();
+        __syncwarp();
     }
     tc::fence_before_sync();
     __syncthreads();
@@ -485,7 +510,9 @@ cudaError_t launch_proj_tc(const ProjParams &p, cudaStream_t stream)
     if (!encode_bf16_2d(&a.xmap, p.x, uint64_t(p.d_in), uint64_t(p.n), uint64_t(p.ldx) * 2u, kBK, kBM,
                         true) ||
         !encode_bf16_2d(&a.wmap, p.W, uint64_t(p.d_out), uint64_t(p.d_in), uint64_t(p.ldw) * 2u, 64,
-                        kBK, true))
+                        kBK, true) ||
+        !encode_bf16_2d(&a.ymap, p.y, uint64_t(p.d_out), uint64_t(p.n), uint64_t(p.ldy) * 2u, 64, 32,
+                        true))
         return cudaErrorInvalidValue;
     if (p.n_chunks > 0) {
         if (!encode_row_maps(a.bmap, p.b_rows, uint64_t(p.d_out), p.b_nrows, p.b_ld) ||
