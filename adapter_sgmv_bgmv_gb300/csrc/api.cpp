@@ -320,8 +320,8 @@ RowsCfg default_rows_cfg(int mode, int64_t n_act, int64_t n_seg, int d_in, int d
     return c;
 }
 
-int rows_launch_params(int mode, RowsCfg cfg, int d_in, int d_out, int rank_alloc, RowsParams &p,
-                       size_t &smem)
+int rows_launch_params(int mode, RowsCfg cfg, int d_in, int d_out, int rank_alloc, bool early_x,
+                       RowsParams &p, size_t &smem)
 {
     for (;; cfg.cluster <<= 1) {
         if (cfg.cluster > rows_max_cluster())
@@ -331,8 +331,9 @@ int rows_launch_params(int mode, RowsCfg cfg, int d_in, int d_out, int rank_allo
         p.slice_out = std::max(8, round_up8(ceil_div(d_out, cfg.cluster)));
         p.rows_alloc = cfg.rows;
         p.rank_alloc = rank_alloc;
+        p.no_y_smem = rows_y_late(mode, early_x, p.slice_out, p.rows_alloc) ? 1 : 0;
         smem = rows_smem_bytes(mode, p.slice_in, p.slice_out, p.rows_alloc, p.rank_alloc,
-                               p.cluster);
+                               p.cluster, p.no_y_smem != 0);
         if (smem <= size_t(rows_max_smem()))
             return LORA_OK;
     }
@@ -396,7 +397,7 @@ int run_rows(lora_ctx *ctx, const lora_table *t, int mode, RowsCfg cfg, const vo
     cfg.rows = std::max(1, pl.row_max_rows);
     RowsParams p{};
     size_t smem = 0;
-    int rc = rows_launch_params(mode, cfg, d_in, d_out, pl.row_max_rank, p, smem);
+    int rc = rows_launch_params(mode, cfg, d_in, d_out, pl.row_max_rank, ctx->call_early_x, p, smem);
     if (rc != LORA_OK)
         return rc;
 
@@ -886,6 +887,10 @@ int delta_call(lora_ctx *ctx, const lora_table *t, int mode, const int32_t *ids,
     }
     if (mode == kFused && ctx && t && t->ctx == ctx && n > 0 && ids && ctx->device >= 0) {
         lora_ctx::RowCacheEntry *e = rcache_find(ctx, t, ids, n, d_in, d_out);
+        // A launch laid out without y rows in shared memory needs early input.
+        if (e && (e->small ? e->small_args.p.no_y_smem : e->big_args->p.no_y_smem) &&
+            !ctx->call_early_x)
+            e = nullptr;
         if (e) {
             if (!stride_ok(x, ldx, d_in) || !stride_ok(y, ldy, d_out))
                 return LORA_E_INVAL;
@@ -1698,7 +1703,8 @@ int lora_fused_device_ids(lora_ctx *ctx, const lora_table *t, const int32_t *ids
         cfg.rows = 1;
     RowsParams p{};
     size_t smem = 0;
-    rc = rows_launch_params(kFused, cfg, d_in, d_out, t->rank_max_ok, p, smem);
+    rc = rows_launch_params(kFused, cfg, d_in, d_out, t->rank_max_ok,
+                            !ctx->device_plan && ctx->call_early_x, p, smem);
     if (rc != LORA_OK)
         return rc;
     p.x = static_cast<const uint16_t *>(x);

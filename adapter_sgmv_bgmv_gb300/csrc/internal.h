@@ -62,6 +62,9 @@ struct RowsParams {
     int rows_alloc;           // shared-memory rows per item (>= every item's nrows)
     int early_pages;          // 1: adapter page copies issued before the dependency wait
     int early_x;              // 1: x, the shrink and the exchange before it as well
+    int no_y_smem;            // 1: every CTA reads y after the wait, straight from memory
+                              //    (fused, early_x, one output vector per thread): no y rows
+                              //    in shared memory
     int rank_alloc;           // shared-memory rank slots (>= every item's rank)
     const int32_t *n_items_dev;   // device-side plan: the item count (items past it idle),
                                   // read after the wait for the kernel that wrote the plan
@@ -85,7 +88,10 @@ using RowsParamsInline = RowsParamsInlineT<kInlineItems, kInlinePerm>;
 using RowsParamsInlineSmall = RowsParamsInlineT<64, 128>;
 
 size_t rows_smem_bytes(int mode, int slice_in, int slice_out, int rows_alloc, int rank_alloc,
-                       int cluster);
+                       int cluster, bool no_y = false);
+// Whether a launch with these parameters has every CTA read y after the dependency
+// wait (then its shared memory holds no y rows).
+bool rows_y_late(int mode, bool early_x, int slice_out, int rows_alloc);
 int rows_max_cluster();
 cudaError_t launch_rows(int mode, const RowsParams &p, size_t smem, cudaStream_t stream);
 cudaError_t launch_rows_inline(int mode, const RowsParamsInline &a, size_t smem,

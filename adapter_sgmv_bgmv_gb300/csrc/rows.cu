@@ -39,15 +39,17 @@ constexpr int kMaxCluster = 16;
 
 __host__ __device__ inline size_t align16(size_t v) { return (v + 15) & ~size_t(15); }
 
+// no_y: a fused launch whose threads read y straight from global memory after the
+// dependency wait (see y_late below) has no y rows in shared memory.
 __host__ __device__ inline size_t carve(int mode, int si, int so, int rows, int ranks,
-                                        int cluster, size_t off[8])
+                                        int cluster, bool no_y, size_t off[8])
 {
     size_t o = 0;
     const bool has_in = mode != kExpand, has_out = mode != kShrink;
     off[0] = o; o += has_in ? align16(size_t(ranks) * si * 2) : 0;          // A slice
     off[1] = o; o += has_in ? align16(size_t(rows) * si * 2) : 0;           // x rows
     off[2] = o; o += has_out ? align16(size_t(ranks) * so * 2) : 0;         // B slice
-    off[3] = o; o += has_out ? align16(size_t(rows) * so * 2) : 0;          // y rows
+    off[3] = o; o += (has_out && !no_y) ? align16(size_t(rows) * so * 2) : 0;   // y rows
     // own partial, then the C partials of the cluster (rank c at c * rows * ranks)
     off[4] = o; o += (has_in && cluster > 1) ? align16(size_t(rows) * ranks * 4) * (1 + cluster) : 0;
     off[5] = o; o += align16(size_t(rows) * ranks * 4);                     // v
@@ -94,7 +96,7 @@ __device__ __forceinline__ void rows_body(const RowsParams &pin, const RowItem *
     extern __shared__ __align__(128) uint8_t smem[];
     const int C = p.cluster;
     size_t off[8];
-    carve(MODE, p.slice_in, p.slice_out, p.rows_alloc, p.rank_alloc, C, off);
+    carve(MODE, p.slice_in, p.slice_out, p.rows_alloc, p.rank_alloc, C, p.no_y_smem != 0, off);
     uint16_t *sA = reinterpret_cast<uint16_t *>(smem + off[0]);
     uint16_t *sX = reinterpret_cast<uint16_t *>(smem + off[1]);
     uint16_t *sB = reinterpret_cast<uint16_t *>(smem + off[2]);
@@ -170,7 +172,8 @@ __device__ __forceinline__ void rows_body(const RowsParams &pin, const RowItem *
     const bool x_early = p.early_x && MODE != kExpand;
     const int nvo_all = out_len >> 3;
     const int ngroups = nrows == 1 ? 1 : (nrows + 1) >> 1;
-    const bool y_late = x_early && MODE == kFused && nvo_all * ngroups <= kThreads;
+    // (no_y_smem: the host found that every CTA of the launch qualifies)
+    const bool y_late = x_early && MODE == kFused && (p.no_y_smem || nvo_all * ngroups <= kThreads);
     if (tid == 0) {
         mbar_init(bar0, 1);
         mbar_init(bar1, 1);
@@ -465,18 +468,25 @@ __device__ __forceinline__ void rows_body(const RowsParams &pin, const RowItem *
     }
 }
 
-template <int MODE, bool DIRECT>
-__global__ void __launch_bounds__(kThreads) k_rows(const __grid_constant__ RowsParams p)
+// OCC: CTAs per SM the registers must allow.  A launch whose shared memory fits six
+// CTAs per SM takes the OCC = 6 instance (40 registers, so that six are resident:
+// more of consecutive calls' CTAs overlap); a larger one, which fits fewer CTAs
+// anyway, takes the unconstrained instance.
+template <int MODE, bool DIRECT, int OCC>
+__global__ void __launch_bounds__(kThreads, OCC) k_rows(const __grid_constant__ RowsParams p)
 {
     rows_body<MODE, DIRECT>(p, p.items, p.perm);
 }
 
 // Same kernel with the plan (items and permutation) in the parameter block.
-template <int MODE, typename Inline>
-__global__ void __launch_bounds__(kThreads) k_rows_inline(const __grid_constant__ Inline a)
+template <int MODE, typename Inline, int OCC>
+__global__ void __launch_bounds__(kThreads, OCC) k_rows_inline(const __grid_constant__ Inline a)
 {
     rows_body<MODE, false>(a.p, a.items, a.perm);
 }
+
+// Shared memory per SM on sm_100-family GPUs, and what the runtime reserves per CTA.
+constexpr size_t kSmemPerSm = 228 * 1024, kSmemReservedPerCta = 1024;
 
 template <typename Kernel>
 cudaError_t configure(Kernel k)
@@ -488,16 +498,16 @@ cudaError_t configure(Kernel k)
     return cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
 }
 
-template <int MODE, bool INLINE, typename Arg, bool DIRECT = false>
-cudaError_t launch_mode(const RowsParams &p, const Arg &arg, size_t smem, cudaStream_t stream)
+template <int MODE, bool INLINE, typename Arg, bool DIRECT, int OCC>
+cudaError_t launch_occ(const RowsParams &p, const Arg &arg, size_t smem, cudaStream_t stream)
 {
     static bool configured = false;
     if (!configured) {
         cudaError_t e;
         if constexpr (INLINE)
-            e = configure(k_rows_inline<MODE, Arg>);
+            e = configure(k_rows_inline<MODE, Arg, OCC>);
         else
-            e = configure(k_rows<MODE, DIRECT>);
+            e = configure(k_rows<MODE, DIRECT, OCC>);
         if (e != cudaSuccess)
             return e;
         configured = true;
@@ -518,9 +528,17 @@ cudaError_t launch_mode(const RowsParams &p, const Arg &arg, size_t smem, cudaSt
     cfg.attrs = attr;
     cfg.numAttrs = 2;
     if constexpr (INLINE)
-        return cudaLaunchKernelEx(&cfg, k_rows_inline<MODE, Arg>, arg);
+        return cudaLaunchKernelEx(&cfg, k_rows_inline<MODE, Arg, OCC>, arg);
     else
-        return cudaLaunchKernelEx(&cfg, k_rows<MODE, DIRECT>, arg);
+        return cudaLaunchKernelEx(&cfg, k_rows<MODE, DIRECT, OCC>, arg);
+}
+
+template <int MODE, bool INLINE, typename Arg, bool DIRECT = false>
+cudaError_t launch_mode(const RowsParams &p, const Arg &arg, size_t smem, cudaStream_t stream)
+{
+    if (kSmemPerSm / (smem + kSmemReservedPerCta) >= 6)
+        return launch_occ<MODE, INLINE, Arg, DIRECT, 6>(p, arg, smem, stream);
+    return launch_occ<MODE, INLINE, Arg, DIRECT, 1>(p, arg, smem, stream);
 }
 
 }  // namespace
@@ -529,10 +547,16 @@ int rows_max_smem() { return 227 * 1024; }
 int rows_max_cluster() { return kMaxCluster; }
 
 size_t rows_smem_bytes(int mode, int slice_in, int slice_out, int rows_alloc, int rank_alloc,
-                       int cluster)
+                       int cluster, bool no_y)
 {
     size_t off[8];
-    return carve(mode, slice_in, slice_out, rows_alloc, rank_alloc, cluster, off);
+    return carve(mode, slice_in, slice_out, rows_alloc, rank_alloc, cluster, no_y, off);
+}
+
+bool rows_y_late(int mode, bool early_x, int slice_out, int rows_alloc)
+{
+    const int ngroups = rows_alloc <= 1 ? 1 : (rows_alloc + 1) / 2;
+    return early_x && mode == kFused && (slice_out / 8) * ngroups <= kThreads;
 }
 
 cudaError_t launch_rows(int mode, const RowsParams &p, size_t smem, cudaStream_t stream)
