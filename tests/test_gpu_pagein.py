@@ -136,6 +136,46 @@ def test_page_in_then_delta_on_the_same_stream_with_early_page_copies(ctx):
         assert_parity(from_dev(y), refs[v], REL_FROB, MAX_ABS_RMS, f"version {v}")
 
 
+def test_cached_decode_launch_is_not_reused_right_after_a_page_in(ctx):
+    """With early pages and early input on, a decode-only call is kept in the launch
+    cache laid out for early input (y read after the wait, no y rows in shared
+    memory).  A page-in just before a call turns early input off for that call, so
+    the cached launch must not be reused then.  Alternating two versions of every
+    adapter (a page-in before the first of two calls), each call sees the version
+    paged in before it."""
+    c1 = _case(seed=66, n=64)
+    c1["ids"] = (np.arange(64) % 4).astype(np.int32)          # runs of one row: row-gather only
+    c2 = dict(c1)
+    rng = np.random.default_rng(67)
+    pool2 = c1["a_pool"].copy()
+    used = np.concatenate([c1["a_pages"][c1["a_pages"] >= 0], c1["b_pages"][c1["b_pages"] >= 0]])
+    pool2[used] = workloads._normal(rng, (used.size, pool2.shape[1]), 0.05)
+    c2["a_pool"] = c2["b_pool"] = pool2
+    t, _ = _empty_table(ctx, c1)
+    hosts = {v: [_host_rows(cv, k) for k in range(4)] for v, cv in ((1, c1), (2, c2))}
+    x = to_dev(c1["x"])
+    ctx.set_option(L.OPT_EARLY_PAGES, 1)
+    ctx.set_option(L.OPT_EARLY_INPUT, 1)
+    try:
+        outs = []
+        for v in (1, 2, 1, 2):
+            for k in range(4):
+                L.lora_page_in(ctx, t, k, *hosts[v][k])
+            for _ in range(2):
+                y = to_dev(c1["y"])
+                L.lora_fused(ctx, t, c1["ids"], x, y)
+                assert ctx.last_path()[0] == 1
+                outs.append((v, y))
+        ctx.sync_status()
+    finally:
+        ctx.set_option(L.OPT_EARLY_PAGES, 0)
+        ctx.set_option(L.OPT_EARLY_INPUT, 0)
+    refs = {v: oracle.fused(oracle.Table.from_case(cv), cv["ids"], cv["x"], cv["y"], nthreads=8)
+            for v, cv in ((1, c1), (2, c2))}
+    for v, y in outs:
+        assert_parity(from_dev(y), refs[v], REL_FROB, MAX_ABS_RMS, f"version {v}")
+
+
 def test_page_in_refuses_bad_buffers_and_arguments(ctx):
     c = _case(seed=65)
     t, pool = _empty_table(ctx, c)
