@@ -392,6 +392,53 @@ def test_early_input_changes_nothing(ctx, name):
         assert_parity(got[1][0], ref, REL_FROB, MAX_ABS_RMS, name)
 
 
+def test_early_options_keep_a_mixed_chain_of_calls_in_order(ctx):
+    """With early pages and early input on, one stream runs, back to back: a tile-path
+    delta (y1), the base projection (writes y2), a row-gather delta (y3), a merge (W2),
+    a tile-path delta on y2 (reads what the base projection wrote, two calls back), a
+    shrink into v and an expand of v (y4).  Every result matches the oracle applied
+    in the same order, so no early read crosses a dependency between calls."""
+    t = workloads.small(seed=81, n=700, d_in=256, d_out=384, n_adapters=3, ranks=[16, 32, 64],
+                        ids=np.repeat(np.array([0, 2, 1], np.int32), [300, 260, 140]))
+    d = workloads.small(seed=82, n=48, d_in=256, d_out=384, n_adapters=3, ranks=[16, 32, 64])
+    W = workloads.make_W(256, 384, seed=3)
+    W2 = workloads.make_W(256, 384, seed=4)
+    tab_t, tab_d = upload_table(ctx, t), upload_table(ctx, d)
+    xt, xd = to_dev(t["x"]), to_dev(d["x"])
+    y1, y3, y4 = to_dev(t["y"]), to_dev(d["y"]), to_dev(t["y"])
+    y2 = to_dev(np.zeros((t["n"], 384), np.uint16))
+    Wd, W2d = to_dev(W), to_dev(W2)
+    v = torch.zeros((t["n"], 64), dtype=torch.float32, device="cuda")
+    ctx.set_option(L.OPT_EARLY_PAGES, 1)
+    ctx.set_option(L.OPT_EARLY_INPUT, 1)
+    try:
+        L.lora_fused(ctx, tab_t, t["ids"], xt, y1)
+        assert ctx.last_path()[0] & 2
+        L.lora_base_fused(ctx, tab_t, t["ids"], xt, Wd, y2)
+        L.lora_fused(ctx, tab_d, d["ids"], xd, y3)
+        assert ctx.last_path()[0] == 1
+        L.lora_merge(ctx, tab_d, 1, W2d)
+        L.lora_fused(ctx, tab_t, t["ids"], xt, y2)
+        L.lora_shrink(ctx, tab_t, t["ids"], xt, v)
+        L.lora_expand(ctx, tab_t, t["ids"], v, y4)
+        ctx.sync_status()
+    finally:
+        ctx.set_option(L.OPT_EARLY_PAGES, 0)
+        ctx.set_option(L.OPT_EARLY_INPUT, 0)
+    T, D = oracle.Table.from_case(t), oracle.Table.from_case(d)
+    assert_parity(from_dev(y1), oracle.fused(T, t["ids"], t["x"], t["y"], nthreads=8),
+                  REL_FROB, MAX_ABS_RMS, "tile delta")
+    base = oracle.base_fused(T, t["ids"], t["x"], W, nthreads=8)
+    assert_parity(from_dev(y2), oracle.fused(T, t["ids"], t["x"], from_dev(
+        to_dev(base)), nthreads=8), REL_FROB, MAX_ABS_RMS, "delta on the base projection")
+    assert_parity(from_dev(y3), oracle.fused(D, d["ids"], d["x"], d["y"], nthreads=8),
+                  REL_FROB, MAX_ABS_RMS, "row-gather delta")
+    assert_parity(from_dev(W2d), oracle.merge(D, 1, W2, +1), REL_FROB, MAX_ABS_RMS, "merge")
+    vh = v.cpu().numpy()
+    assert_parity(from_dev(y4), oracle.expand(T, t["ids"], vh, t["y"], nthreads=8),
+                  REL_FROB, MAX_ABS_RMS, "expand of the shrink's v")
+
+
 def test_a_wait_that_runs_out_is_reported_and_the_context_stays_usable(ctx):
     """Failure detection without a fault: a bounded wait on a barrier nothing arrives
     on gives up after 10 ms, the status word records it, sync_status reports
