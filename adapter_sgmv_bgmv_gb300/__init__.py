@@ -18,15 +18,16 @@ import torch
 from . import _lib
 
 __all__ = ["LoraError", "Context", "AdapterTable", "lora_plan_build", "lora_shrink",
-           "lora_expand", "lora_fused", "lora_fused_noalloc", "lora_base_fused", "PreparedFused", "lora_merge", "lora_unmerge", "lora_page_in", "lora_fused_device_ids", "lora_tune_shape",
+           "lora_expand", "lora_fused", "lora_fused_noalloc", "lora_base_fused", "PreparedFused", "PreparedFusedDeviceIds", "lora_merge", "lora_unmerge", "lora_page_in", "lora_fused_device_ids", "lora_tune_shape",
            "KIND_ROWS_FUSED", "KIND_SHRINK", "KIND_EXPAND", "KIND_TILE_FUSED", "KIND_MERGE",
            "OPT_TILE_PATH", "OPT_MERGE_KERNEL", "OPT_TILE_MIN_RUN", "OPT_EARLY_PAGES", "OPT_DEVICE_PLAN",
-           "OPT_EARLY_INPUT",
+           "OPT_EARLY_INPUT", "OPT_ROWS_B_OVER_A",
            "library_path"]
 
 KIND_ROWS_FUSED, KIND_SHRINK, KIND_EXPAND, KIND_TILE_FUSED, KIND_MERGE = range(5)
 OPT_TILE_PATH, OPT_MERGE_KERNEL, OPT_TILE_MIN_RUN, OPT_EARLY_PAGES, OPT_DEVICE_PLAN = 1, 2, 3, 4, 5
 OPT_EARLY_INPUT = 6
+OPT_ROWS_B_OVER_A = 7
 ERROR_NAMES = {0: "LORA_OK", -1: "LORA_E_INVAL", -2: "LORA_E_RANK", -3: "LORA_E_ADAPTER",
                -4: "LORA_E_NOT_RESIDENT", -5: "LORA_E_PAGE", -6: "LORA_E_CUDA",
                -7: "LORA_E_TIMEOUT", -8: "LORA_E_NOMEM", -9: "LORA_E_CAPACITY",
@@ -160,7 +161,8 @@ class Context:
 
     def set_option(self, option: int, value: int):
         """LORA_OPT_* (see include/lora.h): OPT_TILE_PATH, OPT_MERGE_KERNEL,
-        OPT_TILE_MIN_RUN, OPT_EARLY_PAGES, OPT_DEVICE_PLAN, OPT_EARLY_INPUT."""
+        OPT_TILE_MIN_RUN, OPT_EARLY_PAGES, OPT_DEVICE_PLAN, OPT_EARLY_INPUT,
+        OPT_ROWS_B_OVER_A."""
         _check(_L.lora_ctx_set_option(self.handle, int(option), int(value)), self)
 
     def profile_begin(self, every: int = 1):
@@ -335,9 +337,13 @@ def lora_fused_noalloc(ctx: Context, table: AdapterTable, ids, x: torch.Tensor, 
 class PreparedFused:
     """lora_fused with fixed x, y, table and stream (a decode loop's persistent
     buffers): the pointer / stride / stream marshalling happens once.  Each call
-    converts the ids; called again with the same int32 array object (a persistent
-    ids buffer rewritten in place between steps) it reuses the converted arguments
-    too, so the call costs little more than the C function itself."""
+    converts the ids; called again with an int32 array object it has seen among the
+    last 256 (a persistent ids buffer rewritten in place between steps, or a ring of
+    them) it reuses the converted arguments too, so the call costs little more than
+    the C function itself.  Only the object is recognised, never its contents: the
+    library reads the ids on every call."""
+
+    _KEEP = 256
 
     def __init__(self, ctx: Context, table: AdapterTable, x: torch.Tensor, y: torch.Tensor,
                  stream=None):
@@ -350,25 +356,77 @@ class PreparedFused:
         self._tail = (ctypes.c_void_p(px), ctypes.c_int64(ldx), ctypes.c_int(d_in),
                       ctypes.c_void_p(py), ctypes.c_int64(ldy), ctypes.c_int(d_out),
                       ctypes.c_void_p(_stream(stream, ctx.device)))
-        self._last = None          # (ids object, its argument tuple)
+        # id(ids object) -> (the object, kept alive so its id stays its own; its
+        # argument tuple), for int32 arrays used as they are (no converted copy)
+        self._seen = {}
+
+    def _args(self, ids):
+        arr, pid, n = _ids(ids)
+        args = self._head + (ctypes.c_void_p(pid), ctypes.c_int64(n)) + self._tail
+        if arr is ids:             # no converted copy: the object itself is the buffer
+            if len(self._seen) >= self._KEEP:
+                self._seen.pop(next(iter(self._seen)))
+            self._seen[id(ids)] = (ids, args)
+        return args
 
     def bind(self, ids):
         """Convert and keep the arguments for this ids array without launching, so
         that the first call with it costs no more than the later ones."""
-        arr, pid, n = _ids(ids)
-        if arr is ids:
-            self._last = (ids, self._head + (ctypes.c_void_p(pid), ctypes.c_int64(n)) + self._tail)
+        self._args(ids)
 
     def __call__(self, ids):
-        last = self._last
-        if last is not None and last[0] is ids:
-            rc = self._fn(*last[1])
+        hit = self._seen.get(id(ids))
+        if hit is not None and hit[0] is ids:
+            rc = self._fn(*hit[1])
         else:
-            arr, pid, n = _ids(ids)
-            args = self._head + (ctypes.c_void_p(pid), ctypes.c_int64(n)) + self._tail
-            if arr is ids:         # no converted copy: the object itself is the buffer
-                self._last = (ids, args)
-            rc = self._fn(*args)
+            rc = self._fn(*self._args(ids))
+        if rc:
+            _check(rc, self._ctx)
+
+
+class PreparedFusedDeviceIds:
+    """lora_fused_device_ids with fixed x, y, table and stream: the marshalling
+    happens once, and the checked argument tuple of each ids tensor object seen among
+    the last 256 is kept, so a call costs little more than the C function itself.
+    Only the object is recognised (its data pointer and length are taken when it is
+    first seen): the kernel reads the ids on every call."""
+
+    _KEEP = 256
+
+    def __init__(self, ctx: Context, table: AdapterTable, x: torch.Tensor, y: torch.Tensor,
+                 stream=None):
+        px, ldx, d_in = _rows(x, "x")
+        py, ldy, d_out = _rows(y, "y")
+        self._keep = (ctx, table, x, y)
+        self._ctx = ctx
+        self._fn = _lib.untyped("lora_fused_device_ids")
+        self._head = (ctypes.c_void_p(ctx.handle), ctypes.c_void_p(table.handle))
+        self._tail = (ctypes.c_void_p(px), ctypes.c_int64(ldx), ctypes.c_int(d_in),
+                      ctypes.c_void_p(py), ctypes.c_int64(ldy), ctypes.c_int(d_out),
+                      ctypes.c_void_p(_stream(stream, ctx.device)))
+        self._seen = {}
+
+    def _args(self, ids):
+        if not isinstance(ids, torch.Tensor) or not ids.is_cuda or ids.dtype != torch.int32 or \
+                ids.dim() != 1 or not ids.is_contiguous():
+            raise ValueError("ids must be a contiguous 1-D int32 CUDA tensor")
+        args = self._head + (ctypes.c_void_p(ids.data_ptr()), ctypes.c_int64(ids.shape[0])) + \
+            self._tail
+        if len(self._seen) >= self._KEEP:
+            self._seen.pop(next(iter(self._seen)))
+        self._seen[id(ids)] = (ids, args)
+        return args
+
+    def bind(self, ids):
+        """Check and keep the arguments for this ids tensor without launching."""
+        self._args(ids)
+
+    def __call__(self, ids):
+        hit = self._seen.get(id(ids))
+        if hit is not None and hit[0] is ids:
+            rc = self._fn(*hit[1])
+        else:
+            rc = self._fn(*self._args(ids))
         if rc:
             _check(rc, self._ctx)
 

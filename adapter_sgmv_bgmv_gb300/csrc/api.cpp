@@ -107,6 +107,7 @@ struct lora_ctx {
     bool call_early_x = false;      // this call's shrink may load x before its wait
     int call_early = 0;             // early page copies for the call in progress
     int device_plan = 0;            // LORA_OPT_DEVICE_PLAN
+    int b_over_a = 0;               // LORA_OPT_ROWS_B_OVER_A: 0 auto, 1 always, -1 never
     cudaStream_t pool_write_stream = nullptr;   // stream of the last page-in ...
     bool pool_write_pending = false;            // ... and no delta / merge launch after it yet
     int force_cluster = 0;          // > 0 while tuning: row-kernel cluster width
@@ -320,8 +321,15 @@ RowsCfg default_rows_cfg(int mode, int64_t n_act, int64_t n_seg, int d_in, int d
     return c;
 }
 
-int rows_launch_params(int mode, RowsCfg cfg, int d_in, int d_out, int rank_alloc, bool early_x,
-                       RowsParams &p, size_t &smem)
+// n_items: the launch's items (clusters).  A fused launch copies B's slices into A's
+// space after the shrink (LORA_OPT_ROWS_B_OVER_A) by default when it reads x before
+// its wait (consecutive calls overlap, and the A copies no longer share the memory
+// system with B's: measured faster on every decode batch), and otherwise when it has
+// more CTAs than the GPU holds at once and that layout lets more be resident (a lone
+// call's chain is one B copy longer, which only pays when it saves a wave).
+int rows_launch_params(const lora_ctx *ctx, int mode, RowsCfg cfg, int d_in, int d_out,
+                       int rank_alloc, bool early_x, int64_t n_items, RowsParams &p,
+                       size_t &smem)
 {
     for (;; cfg.cluster <<= 1) {
         if (cfg.cluster > rows_max_cluster())
@@ -332,8 +340,20 @@ int rows_launch_params(int mode, RowsCfg cfg, int d_in, int d_out, int rank_allo
         p.rows_alloc = cfg.rows;
         p.rank_alloc = rank_alloc;
         p.no_y_smem = rows_y_late(mode, early_x, p.slice_out, p.rows_alloc) ? 1 : 0;
+        p.b_over_a = 0;
         smem = rows_smem_bytes(mode, p.slice_in, p.slice_out, p.rows_alloc, p.rank_alloc,
                                p.cluster, p.no_y_smem != 0);
+        if (mode == kFused && ctx->b_over_a >= 0) {
+            const size_t over = rows_smem_bytes(mode, p.slice_in, p.slice_out, p.rows_alloc,
+                                                p.rank_alloc, p.cluster, p.no_y_smem != 0, true);
+            const int64_t ctas = n_items * p.cluster;
+            const int per_sm = rows_ctas_per_sm(mode, smem);
+            if (ctx->b_over_a > 0 || early_x ||
+                (ctas > int64_t(kSms) * per_sm && rows_ctas_per_sm(mode, over) > per_sm)) {
+                p.b_over_a = 1;
+                smem = over;
+            }
+        }
         if (smem <= size_t(rows_max_smem()))
             return LORA_OK;
     }
@@ -397,7 +417,8 @@ int run_rows(lora_ctx *ctx, const lora_table *t, int mode, RowsCfg cfg, const vo
     cfg.rows = std::max(1, pl.row_max_rows);
     RowsParams p{};
     size_t smem = 0;
-    int rc = rows_launch_params(mode, cfg, d_in, d_out, pl.row_max_rank, ctx->call_early_x, p, smem);
+    int rc = rows_launch_params(ctx, mode, cfg, d_in, d_out, pl.row_max_rank, ctx->call_early_x,
+                                int64_t(pl.row_items.size()), p, smem);
     if (rc != LORA_OK)
         return rc;
 
@@ -1281,10 +1302,7 @@ int lora_table_create(lora_ctx *ctx, const void *a_pool, int64_t a_n_pages, int 
     t->a_pages.assign(a_pages_host, a_pages_host + np);
     t->b_pages.assign(b_pages_host, b_pages_host + np);
     t->status.resize(size_t(n_adapters));
-    if (ctx->plan.count.capacity() < size_t(n_adapters)) {
-        ctx->plan.count.reserve(size_t(n_adapters));
-        ctx->plan.cursor.reserve(size_t(n_adapters));
-    }
+    plan_reserve(ctx->plan, n_adapters);
     t->a_contig.assign(size_t(n_adapters), 0);
     t->b_contig.assign(size_t(n_adapters), 0);
     for (int k = 0; k < n_adapters; ++k) {
@@ -1703,8 +1721,8 @@ int lora_fused_device_ids(lora_ctx *ctx, const lora_table *t, const int32_t *ids
         cfg.rows = 1;
     RowsParams p{};
     size_t smem = 0;
-    rc = rows_launch_params(kFused, cfg, d_in, d_out, t->rank_max_ok,
-                            !ctx->device_plan && ctx->call_early_x, p, smem);
+    rc = rows_launch_params(ctx, kFused, cfg, d_in, d_out, t->rank_max_ok,
+                            !ctx->device_plan && ctx->call_early_x, n, p, smem);
     if (rc != LORA_OK)
         return rc;
     p.x = static_cast<const uint16_t *>(x);
@@ -1914,6 +1932,11 @@ int lora_ctx_set_option(lora_ctx *ctx, int option, int value)
     case LORA_OPT_EARLY_PAGES: ctx->early_pages = value ? 1 : 0; return LORA_OK;
     case LORA_OPT_EARLY_INPUT: ctx->early_input = value ? 1 : 0; return LORA_OK;
     case LORA_OPT_DEVICE_PLAN: ctx->device_plan = value ? 1 : 0; return LORA_OK;
+    case LORA_OPT_ROWS_B_OVER_A:
+        if (value < -1 || value > 1)
+            return LORA_E_INVAL;
+        ctx->b_over_a = value;
+        return LORA_OK;
     default: return LORA_E_INVAL;
     }
 }

@@ -65,6 +65,9 @@ struct RowsParams {
     int no_y_smem;            // 1: every CTA reads y after the wait, straight from memory
                               //    (fused, early_x, one output vector per thread): no y rows
                               //    in shared memory
+    int b_over_a;             // 1 (fused): B's page slices are copied into A's shared
+                              //    memory once the shrink has read it (half the footprint,
+                              //    so more CTAs are resident at once)
     int rank_alloc;           // shared-memory rank slots (>= every item's rank)
     const int32_t *n_items_dev;   // device-side plan: the item count (items past it idle),
                                   // read after the wait for the kernel that wrote the plan
@@ -88,7 +91,10 @@ using RowsParamsInline = RowsParamsInlineT<kInlineItems, kInlinePerm>;
 using RowsParamsInlineSmall = RowsParamsInlineT<64, 128>;
 
 size_t rows_smem_bytes(int mode, int slice_in, int slice_out, int rows_alloc, int rank_alloc,
-                       int cluster, bool no_y = false);
+                       int cluster, bool no_y = false, bool b_over_a = false);
+// CTAs of a row-gather launch with this much dynamic shared memory that one SM holds
+// at once (shared memory and the kernel instance's register budget).
+int rows_ctas_per_sm(int mode, size_t smem);
 // Whether a launch with these parameters has every CTA read y after the dependency
 // wait (then its shared memory holds no y rows).
 bool rows_y_late(int mode, bool early_x, int slice_out, int rows_alloc);

@@ -11,39 +11,86 @@
 
 namespace lora {
 
+// count and seen are indexed by adapter + 1: slot 0 takes the released rows (and,
+// until the check after the loop, ids out of range), so the counting loop has no
+// data-dependent branch (half-released decode batches would mispredict on every row).
+void plan_reserve(Plan &pl, int n_adapters)
+{
+    const size_t slots = size_t(std::max(n_adapters, 0)) + 1;
+    if (pl.count.size() < slots)
+        pl.count.resize(slots, 0);
+    if (pl.cursor.size() < slots)
+        pl.cursor.resize(slots, 0);
+    if (pl.seen.size() < (slots + 63) / 64)
+        pl.seen.resize((slots + 63) / 64, 0);
+}
+
 int plan_group(Plan &pl, const int32_t *ids, int64_t n, int n_adapters)
 {
-    pl.active.clear();
-    pl.perm.clear();
     pl.seg_offsets.clear();
     pl.seg_adapter.clear();
     pl.max_seg_len = 0;
-    pl.count.assign(size_t(n_adapters), 0);
+    plan_reserve(pl, n_adapters);
+    pl.active.resize(size_t(n));
+    int32_t *active = pl.active.data();
+    int32_t *count = pl.count.data();
+    uint64_t *seen = pl.seen.data();
+    // Count the rows of each adapter, mark the adapters in use and list the active
+    // rows (every row is written, the length advances only for an active one).
+    int64_t n_act = 0;
+    bool bad = false;
     for (int64_t i = 0; i < n; ++i) {
         const int32_t k = ids[i];
-        if (k < -1 || k >= n_adapters)
-            return LORA_E_ADAPTER;
-        if (k >= 0) {
-            pl.active.push_back(int32_t(i));
-            pl.count[size_t(k)] += 1;
-        }
+        const bool in_range = k >= -1 && k < n_adapters;
+        bad |= !in_range;
+        const int32_t slot = in_range ? k + 1 : 0;
+        active[n_act] = int32_t(i);
+        n_act += slot > 0;
+        count[slot] += 1;
+        seen[slot >> 6] |= uint64_t(1) << (slot & 63);
     }
-    pl.cursor.resize(size_t(n_adapters));
-    int32_t run = 0;
-    for (int k = 0; k < n_adapters; ++k) {
-        pl.cursor[size_t(k)] = run;
-        const int32_t c = pl.count[size_t(k)];
-        if (c > 0) {
-            pl.seg_offsets.push_back(run);
-            pl.seg_adapter.push_back(k);
-            pl.max_seg_len = std::max(pl.max_seg_len, c);
+    const size_t words = (size_t(n_adapters) + 1 + 63) / 64;
+    if (bad) {   // leave the scratch all zero
+        for (int64_t i = 0; i < n; ++i) {
+            const int32_t k = ids[i];
+            count[(k >= -1 && k < n_adapters) ? k + 1 : 0] = 0;
         }
-        run += c;
+        std::fill(seen, seen + words, uint64_t(0));
+        pl.active.clear();
+        pl.perm.clear();
+        return LORA_E_ADAPTER;
+    }
+    pl.active.resize(size_t(n_act));
+    count[0] = 0;
+    seen[0] &= ~uint64_t(1);
+    // Segments in ascending adapter order: the set bits, word by word.
+    int32_t run = 0;
+    for (size_t w = 0; w < words; ++w) {
+        uint64_t m = seen[w];
+        if (m == 0)
+            continue;
+        seen[w] = 0;
+        while (m != 0) {
+            const int32_t slot = int32_t(w * 64 + size_t(__builtin_ctzll(m)));
+            m &= m - 1;
+            const int32_t c = count[slot];
+            count[slot] = 0;
+            pl.cursor[size_t(slot)] = run;
+            pl.seg_offsets.push_back(run);
+            pl.seg_adapter.push_back(slot - 1);
+            pl.max_seg_len = std::max(pl.max_seg_len, c);
+            run += c;
+        }
     }
     pl.seg_offsets.push_back(run);
-    pl.perm.resize(pl.active.size());
-    for (int32_t row : pl.active)
-        pl.perm[size_t(pl.cursor[size_t(ids[row])]++)] = row;
+    // Stable placement: rows in ascending order, each at its adapter's cursor.
+    pl.perm.resize(size_t(n_act));
+    int32_t *cursor = pl.cursor.data();
+    int32_t *perm = pl.perm.data();
+    for (int64_t q = 0; q < n_act; ++q) {
+        const int32_t row = active[q];
+        perm[cursor[ids[row] + 1]++] = row;
+    }
     return LORA_OK;
 }
 
@@ -76,7 +123,7 @@ void plan_items(Plan &pl, const int32_t *rank, const float *scale, int rows_per_
             if (to > from)
                 pl.row_max_rank = std::max(pl.row_max_rank, r);
         };
-        if (tile_min_run > 0) {
+        if (tile_min_run > 0 && e - b >= tile_min_run) {   // else no run can reach a tile
             int32_t q = b;
             while (q < e) {
                 // maximal run of consecutive row indices starting at perm[q]

@@ -19,8 +19,10 @@ struct Plan {
     std::vector<int32_t> slot_adapter; // the tile items' adapters, in order of first tile
     std::vector<int32_t> slot_a_base;  // first row of each slot in the A / B row matrices
     std::vector<int32_t> slot_b_base;
-    std::vector<int32_t> count;        // scratch, [n_adapters]
-    std::vector<int32_t> cursor;       // scratch, [n_adapters]
+    std::vector<int32_t> count;        // scratch, [>= n_adapters], all zero between calls
+    std::vector<int32_t> cursor;       // scratch, [>= n_adapters]
+    std::vector<uint64_t> seen;        // scratch bitmap of the adapters in use, all zero
+                                       // between calls
     int32_t max_seg_len = 0;
     int32_t max_rank = 0;              // largest rank referenced
     int32_t tile_max_rank = 0;
@@ -31,7 +33,12 @@ struct Plan {
 };
 
 // Group rows.  Returns LORA_OK or LORA_E_ADAPTER (an id outside [-1, n_adapters)).
+// O(n + n_adapters / 64): only the adapters in use are visited.
 int plan_group(Plan &pl, const int32_t *ids, int64_t n, int n_adapters);
+
+// Size the per-adapter scratch for tables of up to n_adapters adapters (so that a
+// call allocates nothing for it).
+void plan_reserve(Plan &pl, int n_adapters);
 
 // Cut segments into work items.  Runs of consecutive rows of at least
 // `tile_min_run` rows go to 128-row tiles (tile_min_run <= 0: none do); everything

@@ -25,6 +25,8 @@
 // Released rows (id -1) are in no item, so they cost no CTA and are never touched
 // (LoRazor page: the launch follows the active rows).  Modes: shrink-only writes v
 // (fp32) and skips 4; expand-only reads v, skips 1-3 for x/A and needs no cluster.
+#include <algorithm>
+
 #include <cuda_runtime.h>
 
 #include "internal.h"
@@ -40,15 +42,20 @@ constexpr int kMaxCluster = 16;
 __host__ __device__ inline size_t align16(size_t v) { return (v + 15) & ~size_t(15); }
 
 // no_y: a fused launch whose threads read y straight from global memory after the
-// dependency wait (see y_late below) has no y rows in shared memory.
+// dependency wait (see y_late below) has no y rows in shared memory.  b_over_a: a
+// fused launch copies B's slice into A's space after the shrink (one region, the
+// larger of the two).
 __host__ __device__ inline size_t carve(int mode, int si, int so, int rows, int ranks,
-                                        int cluster, bool no_y, size_t off[8])
+                                        int cluster, bool no_y, bool b_over_a, size_t off[8])
 {
     size_t o = 0;
     const bool has_in = mode != kExpand, has_out = mode != kShrink;
-    off[0] = o; o += has_in ? align16(size_t(ranks) * si * 2) : 0;          // A slice
+    const bool over = b_over_a && has_in && has_out;
+    const size_t a_sz = has_in ? align16(size_t(ranks) * si * 2) : 0;
+    const size_t b_sz = has_out ? align16(size_t(ranks) * so * 2) : 0;
+    off[0] = o; o += over ? (a_sz > b_sz ? a_sz : b_sz) : a_sz;             // A slice
     off[1] = o; o += has_in ? align16(size_t(rows) * si * 2) : 0;           // x rows
-    off[2] = o; o += has_out ? align16(size_t(ranks) * so * 2) : 0;         // B slice
+    off[2] = over ? off[0] : o; o += over ? 0 : b_sz;                       // B slice
     off[3] = o; o += (has_out && !no_y) ? align16(size_t(rows) * so * 2) : 0;   // y rows
     // own partial, then the C partials of the cluster (rank c at c * rows * ranks)
     off[4] = o; o += (has_in && cluster > 1) ? align16(size_t(rows) * ranks * 4) * (1 + cluster) : 0;
@@ -96,7 +103,9 @@ __device__ __forceinline__ void rows_body(const RowsParams &pin, const RowItem *
     extern __shared__ __align__(128) uint8_t smem[];
     const int C = p.cluster;
     size_t off[8];
-    carve(MODE, p.slice_in, p.slice_out, p.rows_alloc, p.rank_alloc, C, p.no_y_smem != 0, off);
+    const bool b_late = MODE == kFused && p.b_over_a != 0;
+    carve(MODE, p.slice_in, p.slice_out, p.rows_alloc, p.rank_alloc, C, p.no_y_smem != 0, b_late,
+          off);
     uint16_t *sA = reinterpret_cast<uint16_t *>(smem + off[0]);
     uint16_t *sX = reinterpret_cast<uint16_t *>(smem + off[1]);
     uint16_t *sB = reinterpret_cast<uint16_t *>(smem + off[2]);
@@ -215,17 +224,31 @@ __device__ __forceinline__ void rows_body(const RowsParams &pin, const RowItem *
     }
     // Adapter pages first (by lane j < r), then the rows (lane i < nrows); with
     // early_pages the page copies go out before waiting for the preceding kernel
-    // (the pools are not that kernel's to write), overlapping its tail.
-    auto issue_pages = [&]() {
+    // (the pools are not that kernel's to write), overlapping its tail.  With b_late
+    // B's pages land in A's space, so they go out once the shrink is done with it.
+    auto issue_b = [&]() {
         for (int q = lane; q < r; q += 32) {
-            const int32_t qa = q < 32 ? pa0 : q < 64 ? pa1 : (MODE != kExpand ? ap[q] : 0);
             const int32_t qb = q < 32 ? pb0 : q < 64 ? pb1 : (MODE != kShrink ? bp[q] : 0);
-            if (MODE != kExpand && in_bytes)
-                bulk_g2s(smem_u32(sA + size_t(q) * p.slice_in),
-                         p.a_pool + int64_t(qa) * p.a_pw + in0, in_bytes, bar0);
             if (MODE != kShrink && out_bytes)
                 bulk_g2s(smem_u32(sB + size_t(q) * p.slice_out),
                          p.b_pool + int64_t(qb) * p.b_pw + out0, out_bytes, bar1);
+        }
+    };
+    auto issue_pages = [&]() {
+        for (int q = lane; q < r; q += 32) {
+            const int32_t qa = q < 32 ? pa0 : q < 64 ? pa1 : (MODE != kExpand ? ap[q] : 0);
+            if (MODE != kExpand && in_bytes)
+                bulk_g2s(smem_u32(sA + size_t(q) * p.slice_in),
+                         p.a_pool + int64_t(qa) * p.a_pw + in0, in_bytes, bar0);
+        }
+        if (!b_late)
+            issue_b();
+    };
+    // Called by every thread once all reads of A are done (after a block barrier).
+    auto issue_b_late = [&]() {
+        if (b_late && warp == 0) {
+            fence_proxy_async_smem();   // the shrink's reads of A before the copies' writes
+            issue_b();
         }
     };
     auto issue_x = [&]() {
@@ -309,7 +332,8 @@ __device__ __forceinline__ void rows_body(const RowsParams &pin, const RowItem *
             // own slot); then wait for the C - 1 partials addressed to this CTA and sum
             // all C in cluster-rank order, so that every CTA holds the same v.
             float *vall = vin + align16(size_t(p.rows_alloc) * RA * 4) / 4;
-            __syncthreads();                       // vin complete
+            __syncthreads();                       // vin complete, A read
+            issue_b_late();
             cluster_wait_acquire();
             const uint32_t dst0 = smem_u32(vall) + uint32_t(crank) * uint32_t(xchunks) * 16u;
             for (int q = tid; q < C * xchunks; q += kThreads) {
@@ -334,6 +358,8 @@ __device__ __forceinline__ void rows_body(const RowsParams &pin, const RowItem *
             }
         }
         __syncthreads();
+        if (!clustered)
+            issue_b_late();
         if (x_early && !y_late) {
             // Everything past here reads y or writes global memory.
             grid_dep_wait();
@@ -533,11 +559,28 @@ cudaError_t launch_occ(const RowsParams &p, const Arg &arg, size_t smem, cudaStr
         return cudaLaunchKernelEx(&cfg, k_rows<MODE, DIRECT, OCC>, arg);
 }
 
+// The instance a launch takes: the register budget that lets as many CTAs be
+// resident as its shared memory allows, from six down to five (fused only); the
+// unconstrained instance below that.
+int occ_instance(int mode, size_t smem)
+{
+    const size_t fit = kSmemPerSm / (smem + kSmemReservedPerCta);
+    if (fit >= 6)
+        return 6;
+    if (fit == 5 && mode == kFused)
+        return 5;
+    return 1;
+}
+
 template <int MODE, bool INLINE, typename Arg, bool DIRECT = false>
 cudaError_t launch_mode(const RowsParams &p, const Arg &arg, size_t smem, cudaStream_t stream)
 {
-    if (kSmemPerSm / (smem + kSmemReservedPerCta) >= 6)
+    const int occ = occ_instance(MODE, smem);
+    if (occ == 6)
         return launch_occ<MODE, INLINE, Arg, DIRECT, 6>(p, arg, smem, stream);
+    if constexpr (MODE == kFused)
+        if (occ == 5)
+            return launch_occ<MODE, INLINE, Arg, DIRECT, 5>(p, arg, smem, stream);
     return launch_occ<MODE, INLINE, Arg, DIRECT, 1>(p, arg, smem, stream);
 }
 
@@ -547,10 +590,18 @@ int rows_max_smem() { return 227 * 1024; }
 int rows_max_cluster() { return kMaxCluster; }
 
 size_t rows_smem_bytes(int mode, int slice_in, int slice_out, int rows_alloc, int rank_alloc,
-                       int cluster, bool no_y)
+                       int cluster, bool no_y, bool b_over_a)
 {
     size_t off[8];
-    return carve(mode, slice_in, slice_out, rows_alloc, rank_alloc, cluster, no_y, off);
+    return carve(mode, slice_in, slice_out, rows_alloc, rank_alloc, cluster, no_y, b_over_a, off);
+}
+
+int rows_ctas_per_sm(int mode, size_t smem)
+{
+    // The unconstrained instances take 72 to 82 registers a thread: three CTAs.
+    const int fit = int(kSmemPerSm / (smem + kSmemReservedPerCta));
+    const int occ = occ_instance(mode, smem);
+    return std::min(fit, occ == 1 ? 3 : occ);
 }
 
 bool rows_y_late(int mode, bool early_x, int slice_out, int rows_alloc)

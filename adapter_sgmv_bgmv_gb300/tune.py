@@ -32,6 +32,10 @@ rows     64     4096  4096   16   64       0   throughput
 rows     64     4096  4096   16   1        0   throughput
 rows     16     256   256    8    4        0   throughput
 rows     128    8192  8192   16   72       0   throughput
+rows     100    8192  8192   16   50       0   throughput
+rows     64     8192  8192   16   40       0   throughput
+rows     56     8192  8192   16   28       0   throughput
+rows     32     8192  8192   16   24       0   throughput
 rows     200    8192  8192   16   100      0   throughput
 tiles    5353   4096  4096   64   8        670
 tiles    16896  4096  11008  64   4        1056

@@ -408,8 +408,9 @@ class Bench:
                 d["table"] = L.AdapterTable(self.ctx, d["a_pool"], d["b_pool"], c["rank"],
                                             c["scale"], c["a_pages"], c["b_pages"])
                 if not self.is_merge and not self.is_proj:
-                    d["call"] = L.PreparedFused(self.ctx, d["table"], d["x"], d["y"],
-                                                torch.cuda.current_stream())
+                    prep = L.PreparedFusedDeviceIds if self.device_ids else L.PreparedFused
+                    d["call"] = prep(self.ctx, d["table"], d["x"], d["y"],
+                                     torch.cuda.current_stream())
                 st[key] = d
             if self.device_ids:
                 for t, calls in enumerate(self.steps_ids):
@@ -418,13 +419,13 @@ class Bench:
                             np.ascontiguousarray(ids, np.int32)).cuda()
             st["_blk"] = blk
             self.sets.append(st)
-        # every set's call holds its arguments before the first step, so that no
-        # first call (argument conversion) falls inside a timed region
-        if not self.is_merge and not self.is_proj and not self.device_ids:
+        # every set's call holds the arguments of every step before the first one, so
+        # that no argument conversion falls inside a timed region
+        if not self.is_merge and not self.is_proj:
             for st in self.sets:
-                for calls in self.steps_ids[:1]:
+                for t, calls in enumerate(self.steps_ids):
                     for key, ids in calls:
-                        st[key]["call"].bind(ids)
+                        st[key]["call"].bind(st[("ids", t, key)] if self.device_ids else ids)
         torch.cuda.synchronize()
 
     # ---- one step
@@ -452,9 +453,7 @@ class Bench:
             d = st[key]
             self.L.lora_base_fused(self.ctx, d["table"], ids, d["x"], d["W"], d["y"], stream)
         elif self.device_ids:
-            d = st[key]
-            self.L.lora_fused_device_ids(self.ctx, d["table"], st[("ids", t, key)], d["x"], d["y"],
-                                         stream)
+            st[key]["call"](st[("ids", t, key)])
         else:
             st[key]["call"](ids)
 
@@ -1025,6 +1024,8 @@ def main():
                     help="keep the adapter-page copies behind the dependency wait")
     ap.add_argument("--no-early-input", action="store_true",
                     help="keep the tensor-core shrink's x loads behind the dependency wait")
+    ap.add_argument("--rows-b-over-a", type=int, choices=(-1, 0, 1), default=0,
+                    help="LORA_OPT_ROWS_B_OVER_A for the row-gather kernel (0: the library's choice)")
     ap.add_argument("--profile-every", type=int, default=8,
                     help="bracket one kernel launch in N with CUDA events (roofline timing)")
     ap.add_argument("--tiles", default=os.path.join(ROOT, "adapter_sgmv_bgmv_gb300", "tiles.tbl"))
@@ -1060,6 +1061,7 @@ def main():
     # tensor-core shrink load x, before their waits.
     ctx.set_option(L.OPT_EARLY_PAGES, 0 if args.no_early_pages else 1)
     ctx.set_option(L.OPT_EARLY_INPUT, 0 if args.no_early_input else 1)
+    ctx.set_option(L.OPT_ROWS_B_OVER_A, args.rows_b_over_a)
     clocks = ClockSampler(torch, local)
     W = max(3, args.warmup)
     if args.all:

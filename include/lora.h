@@ -366,9 +366,17 @@ int lora_sync_status(lora_ctx *ctx, void *stream);
  *                          cluster, its adapter read from the device ids by the kernel
  *                          itself (one launch); 1 a plan kernel first groups the rows by
  *                          adapter into items of several rows (two launches, fewer
- *                          re-reads of a shared adapter). */
+ *                          re-reads of a shared adapter).
+ *   LORA_OPT_ROWS_B_OVER_A 0 (default) a fused row-gather launch copies each CTA's
+ *                          slice of B into the shared memory its slice of A used, once
+ *                          the shrink has read it, when the call runs with
+ *                          LORA_OPT_EARLY_INPUT, or when the launch has more CTAs than
+ *                          the GPU holds at once and the smaller footprint lets more
+ *                          be resident; 1 does so in every fused row-gather launch; -1
+ *                          in none.  The results are the same bits either way. */
 enum { LORA_OPT_TILE_PATH = 1, LORA_OPT_MERGE_KERNEL = 2, LORA_OPT_TILE_MIN_RUN = 3,
-       LORA_OPT_EARLY_PAGES = 4, LORA_OPT_DEVICE_PLAN = 5, LORA_OPT_EARLY_INPUT = 6 };
+       LORA_OPT_EARLY_PAGES = 4, LORA_OPT_DEVICE_PLAN = 5, LORA_OPT_EARLY_INPUT = 6,
+       LORA_OPT_ROWS_B_OVER_A = 7 };
 int lora_ctx_set_option(lora_ctx *ctx, int option, int value);
 
 /* Per-launch timing: between lora_profile_begin and lora_profile_end every

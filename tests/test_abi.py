@@ -177,6 +177,32 @@ def test_library_plan_errors_on_host():
         L.lora_fused(ctx, t, np.zeros(4, np.int32), x, x)   # host-only: no launches
 
 
+def test_library_plan_over_many_adapters_and_after_a_refused_call():
+    """The plan visits only the adapters in use (a bitmap, 64 adapters a word): ids
+    at the word boundaries, a half-released batch and a call refused for an id out of
+    range (which must leave no count behind) all give the numpy grouping."""
+    import adapter_sgmv_bgmv_gb300 as L
+    na = 300
+    ctx, t = _host_table(na, (8,) * na, pw=16)
+    rng = np.random.default_rng(7)
+    edges = np.array([0, 62, 63, 64, 65, 127, 128, 191, 192, 255, 256, 299], np.int32)
+    for trial in range(6):
+        ids = rng.choice(np.concatenate([edges, rng.integers(0, na, 40)]), 700).astype(np.int32)
+        ids[rng.random(700) < 0.5] = -1
+        if trial % 2:
+            bad = ids.copy()
+            bad[rng.integers(0, 700)] = na if trial % 4 == 1 else -2
+            with pytest.raises(L.LoraError) as e:
+                L.lora_plan_build(ctx, t, bad)
+            assert e.value.name == "LORA_E_ADAPTER"
+        p = L.lora_plan_build(ctx, t, ids)
+        a, pm, so, sa = _numpy_plan(ids, na)
+        np.testing.assert_array_equal(p["active_rows"], a)
+        np.testing.assert_array_equal(p["perm"], pm)
+        np.testing.assert_array_equal(p["seg_offsets"], so)
+        np.testing.assert_array_equal(p["seg_adapter"], sa)
+
+
 def test_tile_table_file_round_trip(tmp_path):
     import adapter_sgmv_bgmv_gb300 as L
     ctx, _ = _host_table()

@@ -392,6 +392,74 @@ def test_early_input_changes_nothing(ctx, name):
         assert_parity(got[1][0], ref, REL_FROB, MAX_ABS_RMS, name)
 
 
+B_OVER_A_CASES = {
+    # cluster 1 (no wider split of d = 136), A's slice larger than B's, released rows
+    "ragged_c1": dict(seed=91, n=37, d_in=200, d_out=136, n_adapters=3, ranks=[8, 16, 24],
+                      release_frac=0.25),
+    # cluster 2, B's slice larger than A's, ranks past one warp of page lanes
+    "wide_out_rank96": dict(seed=92, n=40, d_in=256, d_out=1032, n_adapters=3,
+                            ranks=[96, 40, 16], paged=True, page_width=1040),
+}
+
+
+@pytest.mark.parametrize("name", ["lorazor_decode", "lorazor_decode:dev", "llama7b_decode_het",
+                                  "ragged_c1", "wide_out_rank96"])
+def test_b_over_a_changes_nothing(ctx, name):
+    """LORA_OPT_ROWS_B_OVER_A has the row-gather kernel copy B's page slices into the
+    shared memory A's slices used, once the shrink has read them.  Forced on, forced
+    off and left to the library (which takes it for the LoRazor step-0 batch: 752 CTAs,
+    more than the GPU holds with both slices staged), with early input off and on (y
+    rows staged, or read after the wait), four calls accumulating into one y give the
+    same bits, and the first call is within the bar of the oracle."""
+    wl, _, mode = name.partition(":")
+    big = None
+    if wl in B_OVER_A_CASES:
+        c = workloads.small(**B_OVER_A_CASES[wl])
+        big = L.Context(0, max_rows=1024, max_rank=128)
+        cx = big
+    else:
+        c = workloads.make(wl, seed=5)
+        cx = ctx
+    ids = workloads.lorazor_ids(c, 0) if wl == "lorazor_decode" else c["ids"]
+    try:
+        table = upload_table(cx, c)
+        x = to_dev(c["x"])
+        ids_dev = torch.from_numpy(np.ascontiguousarray(ids, np.int32)).cuda()
+        got = {}
+        for early in (0, 1):
+            for over in (-1, 0, 1):
+                cx.set_option(L.OPT_EARLY_PAGES, early)
+                cx.set_option(L.OPT_EARLY_INPUT, early)
+                cx.set_option(L.OPT_ROWS_B_OVER_A, over)
+                try:
+                    y = to_dev(c["y"])
+                    for it in range(5):
+                        if mode == "dev":
+                            L.lora_fused_device_ids(cx, table, ids_dev, x, y)
+                        else:
+                            L.lora_fused(cx, table, ids, x, y)
+                        if it == 0:
+                            cx.sync_status()
+                            assert cx.last_path()[0] == 1
+                            first = from_dev(y)
+                    cx.sync_status()
+                    got[(early, over)] = (first, from_dev(y))
+                finally:
+                    cx.set_option(L.OPT_EARLY_PAGES, 0)
+                    cx.set_option(L.OPT_EARLY_INPUT, 0)
+                    cx.set_option(L.OPT_ROWS_B_OVER_A, 0)
+        for key, val in got.items():
+            for a_, b_ in zip(val, got[(0, -1)]):
+                np.testing.assert_array_equal(a_, b_, err_msg=str(key))
+        ref = oracle.fused(oracle.Table.from_case(c), ids, c["x"], c["y"], nthreads=8)
+        assert_parity(got[(1, 1)][0], ref, REL_FROB, MAX_ABS_RMS, name)
+        rel = np.asarray(ids) < 0
+        np.testing.assert_array_equal(got[(1, 1)][1][rel], c["y"][rel])
+    finally:
+        if big is not None:
+            big.close()
+
+
 def test_early_options_keep_a_mixed_chain_of_calls_in_order(ctx):
     """With early pages and early input on, one stream runs, back to back: a tile-path
     delta (y1), the base projection (writes y2), a row-gather delta (y3), a merge (W2),
