@@ -94,6 +94,41 @@ int plan_group(Plan &pl, const int32_t *ids, int64_t n, int n_adapters)
     return LORA_OK;
 }
 
+// Row items only (no run can reach a tile): one pass over the active rows, an item
+// starting at every rows_per_item-th row of a segment.  Written without
+// data-dependent branches, since decode segments of one to a few rows would make a
+// per-segment loop mispredict on almost every segment.
+static void plan_row_items_only(Plan &pl, const int32_t *rank, const float *scale,
+                                int rows_per_item)
+{
+    const int32_t n_act = int32_t(pl.perm.size());
+    pl.row_perm.assign(pl.perm.begin(), pl.perm.end());
+    pl.row_items.resize(size_t(n_act));
+    RowItem *items = pl.row_items.data();
+    const int32_t *offs = pl.seg_offsets.data();
+    const int32_t *seg_adapter = pl.seg_adapter.data();
+    int32_t s = 0, end = offs[1], cnt = 0, n_items = 0, max_rows = 0;
+    for (int32_t q = 0; q < n_act; ++q) {
+        const bool next = q == end;               // first row of the next segment
+        s += next ? 1 : 0;
+        end = next ? offs[s + 1] : end;
+        cnt = next ? 0 : cnt;
+        const int32_t k = seg_adapter[s];
+        const int32_t m = std::min(rows_per_item, end - q);
+        items[n_items] = RowItem{k, q, int16_t(m), int16_t(rank[k]), scale[k]};
+        n_items += cnt == 0 ? 1 : 0;
+        max_rows = std::max(max_rows, cnt == 0 ? m : 0);
+        cnt = cnt + 1 == rows_per_item ? 0 : cnt + 1;
+    }
+    pl.row_items.resize(size_t(n_items));
+    int32_t max_rank = 0;
+    for (const int32_t k : pl.seg_adapter)
+        max_rank = std::max(max_rank, rank[k]);
+    pl.max_rank = pl.row_max_rank = max_rank;
+    pl.row_max_rows = max_rows;
+    pl.row_active = n_act;
+}
+
 void plan_items(Plan &pl, const int32_t *rank, const float *scale, int rows_per_item,
                 int tile_min_run)
 {
@@ -103,6 +138,10 @@ void plan_items(Plan &pl, const int32_t *rank, const float *scale, int rows_per_
     pl.max_rank = pl.tile_max_rank = pl.row_max_rank = pl.row_max_rows = 0;
     pl.row_active = pl.tile_active = 0;
     const size_t nseg = pl.seg_adapter.size();
+    if (nseg > 0 && (tile_min_run <= 0 || pl.max_seg_len < tile_min_run)) {
+        plan_row_items_only(pl, rank, scale, rows_per_item);
+        return;
+    }
     for (size_t s = 0; s < nseg; ++s) {
         const int32_t k = pl.seg_adapter[s];
         const int32_t r = rank[k];
