@@ -13,13 +13,6 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p)
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-// Orders this thread's earlier generic-proxy accesses of shared memory before the
-// async-proxy (bulk copy) accesses it issues next, and the reverse.
-__device__ __forceinline__ void fence_proxy_async_smem()
-{
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
 __device__ __forceinline__ uint64_t globaltimer_ns()
 {
     uint64_t t;

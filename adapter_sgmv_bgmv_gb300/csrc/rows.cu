@@ -247,7 +247,8 @@ __device__ __forceinline__ void rows_body(const RowsParams &pin, const RowItem *
     // Called by every thread once all reads of A are done (after a block barrier).
     auto issue_b_late = [&]() {
         if (b_late && warp == 0) {
-            fence_proxy_async_smem();   // the shrink's reads of A before the copies' writes
+            // the shrink's reads of A (generic proxy) before the copies' writes (async proxy)
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             issue_b();
         }
     };

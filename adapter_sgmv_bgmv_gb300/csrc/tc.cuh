@@ -10,7 +10,10 @@ namespace tc {
 
 // ---------------------------------------------------------------- proxies / fences
 
-using ::lora::fence_proxy_async_smem;
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
 
 __device__ __forceinline__ void fence_before_sync()
 {
