@@ -25,6 +25,12 @@ void plan_reserve(Plan &pl, int n_adapters)
         pl.seen.resize((slots + 63) / 64, 0);
 }
 
+// Batches up to this long are grouped row by row without data-dependent branches
+// (decode: short runs, many released rows); longer ones run by run (prefill: a
+// request's rows sit together, so a run costs one count update and one block of
+// consecutive row indices instead of a read-modify-write per row).
+constexpr int64_t kRowByRowMax = 1024;
+
 int plan_group(Plan &pl, const int32_t *ids, int64_t n, int n_adapters)
 {
     pl.seg_offsets.clear();
@@ -32,28 +38,65 @@ int plan_group(Plan &pl, const int32_t *ids, int64_t n, int n_adapters)
     pl.max_seg_len = 0;
     plan_reserve(pl, n_adapters);
     pl.active.resize(size_t(n));
-    int32_t *active = pl.active.data();
-    int32_t *count = pl.count.data();
-    uint64_t *seen = pl.seen.data();
-    // Count the rows of each adapter, mark the adapters in use and list the active
-    // rows (every row is written, the length advances only for an active one).
+    int32_t *__restrict active = pl.active.data();
+    int32_t *__restrict count = pl.count.data();
+    uint64_t *__restrict seen = pl.seen.data();
+    const size_t words = (size_t(n_adapters) + 1 + 63) / 64;
+    const bool by_row = n <= kRowByRowMax;
+    // Count the rows of each adapter, mark the adapters in use and list the active rows.
     int64_t n_act = 0;
     bool bad = false;
-    for (int64_t i = 0; i < n; ++i) {
-        const int32_t k = ids[i];
-        const bool in_range = k >= -1 && k < n_adapters;
-        bad |= !in_range;
-        const int32_t slot = in_range ? k + 1 : 0;
-        active[n_act] = int32_t(i);
-        n_act += slot > 0;
-        count[slot] += 1;
-        seen[slot >> 6] |= uint64_t(1) << (slot & 63);
-    }
-    const size_t words = (size_t(n_adapters) + 1 + 63) / 64;
-    if (bad) {   // leave the scratch all zero
+    if (by_row) {
+        // every row is written, the length advances only for an active one
         for (int64_t i = 0; i < n; ++i) {
             const int32_t k = ids[i];
-            count[(k >= -1 && k < n_adapters) ? k + 1 : 0] = 0;
+            const bool in_range = k >= -1 && k < n_adapters;
+            bad |= !in_range;
+            const int32_t slot = in_range ? k + 1 : 0;
+            active[n_act] = int32_t(i);
+            n_act += slot > 0;
+            count[slot] += 1;
+            seen[slot >> 6] |= uint64_t(1) << (slot & 63);
+        }
+    } else {
+        pl.runs.clear();
+        for (int64_t i = 0; i < n;) {
+            const int32_t k = ids[i];
+            int64_t j = i + 1;
+            for (; j + 16 <= n; j += 16) {   // whole blocks of 16 first (vector compares)
+                int32_t diff = 0;
+                for (int u = 0; u < 16; ++u)
+                    diff |= ids[j + u] ^ k;
+                if (diff != 0)
+                    break;
+            }
+            while (j < n && ids[j] == k)
+                ++j;
+            if (k < -1 || k >= n_adapters) {
+                bad = true;
+                break;
+            }
+            if (k >= 0) {
+                const int32_t len = int32_t(j - i), row0 = int32_t(i);
+                for (int32_t t = 0; t < len; ++t)
+                    active[n_act + t] = row0 + t;
+                n_act += len;
+                count[k + 1] += len;
+                seen[(k + 1) >> 6] |= uint64_t(1) << ((k + 1) & 63);
+                pl.runs.push_back(Plan::Run{row0, len, k + 1});
+            }
+            i = j;
+        }
+    }
+    if (bad) {   // leave the scratch all zero
+        if (by_row) {
+            for (int64_t i = 0; i < n; ++i) {
+                const int32_t k = ids[i];
+                count[(k >= -1 && k < n_adapters) ? k + 1 : 0] = 0;
+            }
+        } else {
+            for (const Plan::Run &r : pl.runs)
+                count[r.slot] = 0;
         }
         std::fill(seen, seen + words, uint64_t(0));
         pl.active.clear();
@@ -85,11 +128,20 @@ int plan_group(Plan &pl, const int32_t *ids, int64_t n, int n_adapters)
     pl.seg_offsets.push_back(run);
     // Stable placement: rows in ascending order, each at its adapter's cursor.
     pl.perm.resize(size_t(n_act));
-    int32_t *cursor = pl.cursor.data();
-    int32_t *perm = pl.perm.data();
-    for (int64_t q = 0; q < n_act; ++q) {
-        const int32_t row = active[q];
-        perm[cursor[ids[row] + 1]++] = row;
+    int32_t *__restrict cursor = pl.cursor.data();
+    int32_t *__restrict perm = pl.perm.data();
+    if (by_row) {
+        for (int64_t q = 0; q < n_act; ++q) {
+            const int32_t row = active[q];
+            perm[cursor[ids[row] + 1]++] = row;
+        }
+    } else {
+        for (const Plan::Run &r : pl.runs) {
+            const int32_t c = cursor[r.slot];
+            for (int32_t t = 0; t < r.len; ++t)
+                perm[c + t] = r.row0 + t;
+            cursor[r.slot] = c + r.len;
+        }
     }
     return LORA_OK;
 }
@@ -129,6 +181,34 @@ static void plan_row_items_only(Plan &pl, const int32_t *rank, const float *scal
     pl.row_active = n_act;
 }
 
+// End of the maximal run of consecutive row indices that starts at perm[q], within a
+// segment [.., e).  The segment's rows ascend, so [q, t) is one run exactly when
+// perm[t - 1] - perm[q] == t - 1 - q, a property that holds up to the run's end and
+// fails after it: found by doubling the step, then bisecting (a prefill request's
+// thousand rows take about twenty probes, not a thousand).
+static int32_t consecutive_end(const int32_t *perm, int32_t q, int32_t e)
+{
+    auto whole = [&](int32_t t) { return perm[t - 1] - perm[q] == t - 1 - q; };
+    int32_t lo = q + 1, step = 1;   // [q, lo) is known to be one run
+    while (lo < e) {
+        const int32_t hi = std::min(e, lo + step);
+        if (!whole(hi)) {
+            int32_t a = lo, b = hi - 1;   // the end lies in [lo, hi - 1]
+            while (a < b) {
+                const int32_t m = a + (b - a + 1) / 2;
+                if (whole(m))
+                    a = m;
+                else
+                    b = m - 1;
+            }
+            return a;
+        }
+        lo = hi;
+        step *= 2;
+    }
+    return e;
+}
+
 void plan_items(Plan &pl, const int32_t *rank, const float *scale, int rows_per_item,
                 int tile_min_run)
 {
@@ -165,10 +245,7 @@ void plan_items(Plan &pl, const int32_t *rank, const float *scale, int rows_per_
         if (tile_min_run > 0 && e - b >= tile_min_run) {   // else no run can reach a tile
             int32_t q = b;
             while (q < e) {
-                // maximal run of consecutive row indices starting at perm[q]
-                int32_t t = q + 1;
-                while (t < e && pl.perm[size_t(t)] == pl.perm[size_t(t - 1)] + 1)
-                    ++t;
+                const int32_t t = consecutive_end(pl.perm.data(), q, e);
                 if (t - q >= tile_min_run) {
                     flush_rows(pend, q);
                     for (int32_t p = q; p < t; p += 128) {

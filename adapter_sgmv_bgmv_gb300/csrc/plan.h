@@ -23,6 +23,10 @@ struct Plan {
     std::vector<int32_t> cursor;       // scratch, [>= n_adapters]
     std::vector<uint64_t> seen;        // scratch bitmap of the adapters in use, all zero
                                        // between calls
+    struct Run {
+        int32_t row0, len, slot;       // rows [row0, row0 + len) all of adapter slot - 1
+    };
+    std::vector<Run> runs;             // scratch: the runs of equal active ids (long batches)
     int32_t max_seg_len = 0;
     int32_t max_rank = 0;              // largest rank referenced
     int32_t tile_max_rank = 0;

@@ -179,19 +179,24 @@ def test_library_plan_errors_on_host():
 
 def test_library_plan_over_many_adapters_and_after_a_refused_call():
     """The plan visits only the adapters in use (a bitmap, 64 adapters a word): ids
-    at the word boundaries, a half-released batch and a call refused for an id out of
-    range (which must leave no count behind) all give the numpy grouping."""
+    at the word boundaries, half-released batches (short ones grouped row by row,
+    long ones run by run) and a call refused for an id out of range (which must leave
+    no count behind) all give the numpy grouping."""
     import adapter_sgmv_bgmv_gb300 as L
     na = 300
     ctx, t = _host_table(na, (8,) * na, pw=16)
     rng = np.random.default_rng(7)
     edges = np.array([0, 62, 63, 64, 65, 127, 128, 191, 192, 255, 256, 299], np.int32)
-    for trial in range(6):
-        ids = rng.choice(np.concatenate([edges, rng.integers(0, na, 40)]), 700).astype(np.int32)
-        ids[rng.random(700) < 0.5] = -1
+    for trial in range(12):
+        # row by row up to 1024 rows, run by run beyond (runs of one id)
+        n = 700 if trial < 6 else 3000
+        ids = rng.choice(np.concatenate([edges, rng.integers(0, na, 40)]), n).astype(np.int32)
+        if n > 1024:
+            ids = np.repeat(ids[: n // 25], 25)[:n]
+        ids[rng.random(n) < 0.5] = -1
         if trial % 2:
             bad = ids.copy()
-            bad[rng.integers(0, 700)] = na if trial % 4 == 1 else -2
+            bad[rng.integers(0, n)] = na if trial % 4 == 1 else -2
             with pytest.raises(L.LoraError) as e:
                 L.lora_plan_build(ctx, t, bad)
             assert e.value.name == "LORA_E_ADAPTER"
