@@ -334,16 +334,15 @@ def lora_fused_noalloc(ctx: Context, table: AdapterTable, ids, x: torch.Tensor, 
                                  _stream(stream, ctx.device)), ctx)
 
 
-class PreparedFused:
-    """lora_fused with fixed x, y, table and stream (a decode loop's persistent
-    buffers): the pointer / stride / stream marshalling happens once.  Each call
-    converts the ids; called again with an int32 array object it has seen among the
-    last 256 (a persistent ids buffer rewritten in place between steps, or a ring of
-    them) it reuses the converted arguments too, so the call costs little more than
-    the C function itself.  Only the object is recognised, never its contents: the
+class _PreparedCall:
+    """A fused call with fixed x, y, table and stream (a decode loop's persistent
+    buffers).  The marshalling happens once: for each ids object among the last 256
+    it was handed, a filled lora_fused_args block is kept, and a call passes only
+    that block's address.  Only the object is recognised, never its contents: the
     library reads the ids on every call."""
 
     _KEEP = 256
+    _ENTRY = ""
 
     def __init__(self, ctx: Context, table: AdapterTable, x: torch.Tensor, y: torch.Tensor,
                  stream=None):
@@ -351,84 +350,67 @@ class PreparedFused:
         py, ldy, d_out = _rows(y, "y")
         self._keep = (ctx, table, x, y)
         self._ctx = ctx
-        self._fn = _lib.untyped("lora_fused")
-        self._head = (ctypes.c_void_p(ctx.handle), ctypes.c_void_p(table.handle))
-        self._tail = (ctypes.c_void_p(px), ctypes.c_int64(ldx), ctypes.c_int(d_in),
-                      ctypes.c_void_p(py), ctypes.c_int64(ldy), ctypes.c_int(d_out),
-                      ctypes.c_void_p(_stream(stream, ctx.device)))
+        self._fn = _lib.untyped(self._ENTRY)
+        self._fields = dict(ctx=ctx.handle, table=table.handle, x=px, ldx=ldx, d_in=d_in, y=py,
+                            ldy=ldy, d_out=d_out, stream=_stream(stream, ctx.device))
         # id(ids object) -> (the object, kept alive so its id stays its own; its
-        # argument tuple), for int32 arrays used as they are (no converted copy)
+        # argument block; the block's address)
         self._seen = {}
 
-    def _args(self, ids):
-        arr, pid, n = _ids(ids)
-        args = self._head + (ctypes.c_void_p(pid), ctypes.c_int64(n)) + self._tail
-        if arr is ids:             # no converted copy: the object itself is the buffer
+    def _ids_ptr(self, ids):
+        raise NotImplementedError
+
+    def _block(self, ids):
+        ptr, n, keep = self._ids_ptr(ids)
+        blk = _lib.FusedArgs(ids=ptr, n=n, **self._fields)
+        ref = ctypes.byref(blk)
+        if keep:
             if len(self._seen) >= self._KEEP:
                 self._seen.pop(next(iter(self._seen)))
-            self._seen[id(ids)] = (ids, args)
-        return args
+            self._seen[id(ids)] = (ids, blk, ref)
+        return blk, ref
 
     def bind(self, ids):
-        """Convert and keep the arguments for this ids array without launching, so
+        """Convert and keep the arguments for this ids object without launching, so
         that the first call with it costs no more than the later ones."""
-        self._args(ids)
+        self._block(ids)
 
     def __call__(self, ids):
         hit = self._seen.get(id(ids))
         if hit is not None and hit[0] is ids:
-            rc = self._fn(*hit[1])
+            rc = self._fn(hit[2])
         else:
-            rc = self._fn(*self._args(ids))
+            blk, ref = self._block(ids)
+            rc = self._fn(ref)
         if rc:
             _check(rc, self._ctx)
 
 
-class PreparedFusedDeviceIds:
-    """lora_fused_device_ids with fixed x, y, table and stream: the marshalling
-    happens once, and the checked argument tuple of each ids tensor object seen among
-    the last 256 is kept, so a call costs little more than the C function itself.
-    Only the object is recognised (its data pointer and length are taken when it is
-    first seen): the kernel reads the ids on every call."""
+class PreparedFused(_PreparedCall):
+    """lora_fused with fixed x, y, table and stream; call it with the host ids
+    (int32 array, -1 = released).  An array used as it is (int32, contiguous) is
+    remembered, so a persistent ids buffer rewritten in place between steps, or a
+    ring of them, costs little more than the C function itself."""
 
-    _KEEP = 256
+    _ENTRY = "lora_fused_args_call"
 
-    def __init__(self, ctx: Context, table: AdapterTable, x: torch.Tensor, y: torch.Tensor,
-                 stream=None):
-        px, ldx, d_in = _rows(x, "x")
-        py, ldy, d_out = _rows(y, "y")
-        self._keep = (ctx, table, x, y)
-        self._ctx = ctx
-        self._fn = _lib.untyped("lora_fused_device_ids")
-        self._head = (ctypes.c_void_p(ctx.handle), ctypes.c_void_p(table.handle))
-        self._tail = (ctypes.c_void_p(px), ctypes.c_int64(ldx), ctypes.c_int(d_in),
-                      ctypes.c_void_p(py), ctypes.c_int64(ldy), ctypes.c_int(d_out),
-                      ctypes.c_void_p(_stream(stream, ctx.device)))
-        self._seen = {}
+    def _ids_ptr(self, ids):
+        arr, pid, n = _ids(ids)
+        return pid, n, arr is ids
 
-    def _args(self, ids):
+
+class PreparedFusedDeviceIds(_PreparedCall):
+    """lora_fused_device_ids with fixed x, y, table and stream; call it with the ids
+    as a contiguous 1-D int32 CUDA tensor (its data pointer and length are taken when
+    the tensor is first seen)."""
+
+    _ENTRY = "lora_fused_device_ids_args_call"
+
+    def _ids_ptr(self, ids):
         if not isinstance(ids, torch.Tensor) or not ids.is_cuda or ids.dtype != torch.int32 or \
                 ids.dim() != 1 or not ids.is_contiguous():
             raise ValueError("ids must be a contiguous 1-D int32 CUDA tensor")
-        args = self._head + (ctypes.c_void_p(ids.data_ptr()), ctypes.c_int64(ids.shape[0])) + \
-            self._tail
-        if len(self._seen) >= self._KEEP:
-            self._seen.pop(next(iter(self._seen)))
-        self._seen[id(ids)] = (ids, args)
-        return args
-
-    def bind(self, ids):
-        """Check and keep the arguments for this ids tensor without launching."""
-        self._args(ids)
-
-    def __call__(self, ids):
-        hit = self._seen.get(id(ids))
-        if hit is not None and hit[0] is ids:
-            rc = self._fn(*hit[1])
-        else:
-            rc = self._fn(*self._args(ids))
-        if rc:
-            _check(rc, self._ctx)
+        return ids.data_ptr(), ids.shape[0], True
 
 
 def lora_merge(ctx: Context, table: AdapterTable, adapter: int, W: torch.Tensor, stream=None):

@@ -22,6 +22,12 @@ class PlanView(ctypes.Structure):
                 ("tile_min_run", I64)]
 
 
+class FusedArgs(ctypes.Structure):
+    """lora_fused_args (include/lora.h)."""
+    _fields_ = [("ctx", P), ("table", P), ("ids", P), ("n", I64), ("x", P), ("ldx", I64),
+                ("y", P), ("ldy", I64), ("d_in", I), ("d_out", I), ("stream", P)]
+
+
 SIGNATURES = {
     "lora_version": ([], I),
     "lora_strerror": ([I], ctypes.c_char_p),
@@ -41,6 +47,8 @@ SIGNATURES = {
     "lora_unmerge": ([P, P, I, P, I64, I, I, P], I),
     "lora_page_in": ([P, P, I, P, I, P, I, P], I),
     "lora_fused_device_ids": ([P, P, P, I64, P, I64, I, P, I64, I, P], I),
+    "lora_fused_args_call": ([ctypes.POINTER(FusedArgs)], I),
+    "lora_fused_device_ids_args_call": ([ctypes.POINTER(FusedArgs)], I),
     "lora_selftest_timeout": ([P, I64, P], I),
     "lora_tiles_load": ([P, ctypes.c_char_p], I),
     "lora_tiles_save": ([P, ctypes.c_char_p], I),

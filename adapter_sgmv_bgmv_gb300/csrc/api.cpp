@@ -1685,6 +1685,22 @@ int lora_fused_noalloc(lora_ctx *ctx, const lora_table *t, const int32_t *ids, i
     return rc;
 }
 
+int lora_fused_args_call(const lora_fused_args *a)
+{
+    if (!a)
+        return LORA_E_INVAL;
+    return delta_call(a->ctx, a->table, kFused, a->ids, a->n, a->x, a->ldx, a->d_in, nullptr, 0,
+                      a->y, a->ldy, a->d_out, static_cast<cudaStream_t>(a->stream));
+}
+
+int lora_fused_device_ids_args_call(const lora_fused_args *a)
+{
+    if (!a)
+        return LORA_E_INVAL;
+    return lora_fused_device_ids(a->ctx, a->table, a->ids, a->n, a->x, a->ldx, a->d_in, a->y,
+                                 a->ldy, a->d_out, a->stream);
+}
+
 int lora_fused_device_ids(lora_ctx *ctx, const lora_table *t, const int32_t *ids_dev, int64_t n,
                           const void *x, int64_t ldx, int d_in, void *y, int64_t ldy, int d_out,
                           void *stream_ptr)

@@ -233,6 +233,34 @@ int lora_fused_device_ids(lora_ctx *ctx, const lora_table *table, const int32_t 
                           int64_t n, const void *x, int64_t ldx, int d_in, void *y,
                           int64_t ldy, int d_out, void *stream);
 
+/* The arguments of lora_fused / lora_fused_device_ids in one block, for callers that
+ * issue the same call shape many times (a decode loop): a binding fills the block
+ * once per ids buffer and passes one pointer, instead of marshalling eleven
+ * arguments on every call.  ids is host memory for lora_fused_args_call and device
+ * memory for lora_fused_device_ids_args_call.  The block is read during the call
+ * only and is never kept; every field is checked as in the call it stands for. */
+typedef struct lora_fused_args {
+    lora_ctx *ctx;
+    const lora_table *table;
+    const int32_t *ids;
+    int64_t n;
+    const void *x;
+    int64_t ldx;
+    void *y;
+    int64_t ldy;
+    int d_in;
+    int d_out;
+    void *stream;
+} lora_fused_args;
+
+/* lora_fused(a->ctx, a->table, a->ids, a->n, a->x, a->ldx, a->d_in, a->y, a->ldy,
+ * a->d_out, a->stream); LORA_E_INVAL for a null block. */
+int lora_fused_args_call(const lora_fused_args *a);
+
+/* lora_fused_device_ids with the same fields (ids in device memory); LORA_E_INVAL
+ * for a null block. */
+int lora_fused_device_ids_args_call(const lora_fused_args *a);
+
 /* Merge / unmerge (mode switch): W[c, o] = bf16(W[c, o] +/- s_k sum_j A_k[c, j]
  * B_k[j, o]) in place, W [d_in, ldw] bf16 row-major.  Unmerge after merge restores
  * W to within two bf16 rounding steps (not bit-exactly). */

@@ -279,6 +279,39 @@ def test_prepared_fused_matches_lora_fused_and_reads_a_rewritten_ids_buffer(ctx)
         np.testing.assert_array_equal(from_dev(y_got), from_dev(y_ref))
 
 
+def test_prepared_calls_over_a_ring_of_ids_objects(ctx):
+    """PreparedFused and PreparedFusedDeviceIds keep the arguments of the last 256
+    ids objects they were handed: a ring of three arrays (one rewritten in place
+    between its turns) and then 300 fresh ones (past the 256 kept, so the oldest are
+    dropped) give what lora_fused / lora_fused_device_ids give, call for call."""
+    c = workloads.small(seed=83, n=40, d_in=128, d_out=256, n_adapters=4, ranks=[8, 16, 8, 32])
+    table = upload_table(ctx, c)
+    x = to_dev(c["x"])
+    rng = np.random.default_rng(5)
+    ring = [rng.integers(-1, 4, 40).astype(np.int32) for _ in range(3)]
+    y_ref, y_got = to_dev(c["y"]), to_dev(c["y"])
+    yd_ref, yd_got = to_dev(c["y"]), to_dev(c["y"])
+    call = L.PreparedFused(ctx, table, x, y_got)
+    call_d = L.PreparedFusedDeviceIds(ctx, table, x, yd_got)
+    ring_d = [torch.from_numpy(r.copy()).cuda() for r in ring]
+    for step in range(9):
+        k = step % 3
+        if step == 6:
+            ring[k][::2] = -1                   # rewritten in place, host and device
+            ring_d[k].copy_(torch.from_numpy(ring[k]))
+        L.lora_fused(ctx, table, ring[k].copy(), x, y_ref)
+        call(ring[k])
+        L.lora_fused_device_ids(ctx, table, ring_d[k].clone(), x, yd_ref)
+        call_d(ring_d[k])
+    fresh = [rng.integers(-1, 4, 40).astype(np.int32) for _ in range(300)]
+    for ids in fresh + fresh[:5]:
+        L.lora_fused(ctx, table, ids.copy(), x, y_ref)
+        call(ids)
+    ctx.sync_status()
+    np.testing.assert_array_equal(from_dev(y_got), from_dev(y_ref))
+    np.testing.assert_array_equal(from_dev(yd_got), from_dev(yd_ref))
+
+
 @pytest.mark.parametrize("name", ["llama7b_decode_het", "llama7b_decode_hom"])
 def test_early_page_copies_change_nothing(ctx, name):
     """LORA_OPT_EARLY_PAGES only moves the adapter-page copies ahead of the wait for
