@@ -7,7 +7,9 @@ that some reach the tensor-core tiles) and y_in (N(0,1) or zero), then runs with
 drawn options (early page copies and early input, B copied over A or not, the
 tile path on or off, a fixed minimum run).  Checked: lora_fused under the bar with
 released rows bit-exact, and on every third case lora_shrink (the same cells
-written, within fp32 rounding of the oracle) and lora_expand of the oracle's v."""
+written, within fp32 rounding of the oracle) and lora_expand of the oracle's v.
+Drawn cases also go through lora_base_fused, lora_merge / lora_unmerge on both
+merge kernels, and lora_fused_device_ids in both modes."""
 import numpy as np
 import pytest
 import torch
@@ -107,3 +109,70 @@ def test_random_case_matches_oracle(ctx, seed):
         ctx.set_option(L.OPT_ROWS_B_OVER_A, 0)
         ctx.set_option(L.OPT_TILE_PATH, 1)
         ctx.set_option(L.OPT_TILE_MIN_RUN, 0)
+
+
+N_OTHER = 40
+
+
+@pytest.mark.parametrize("seed", range(N_OTHER))
+def test_random_base_projection_matches_oracle(ctx, seed):
+    """lora_base_fused on a drawn case: y = bf16(x W + s (x A) B), x W alone for
+    released rows, every element against the oracle."""
+    c, _ = draw(10_000 + seed)
+    table = upload_table(ctx, c)
+    W = workloads.make_W(c["d_in"], c["d_out"], seed=seed)
+    y = torch.empty((c["n"], c["d_out"]), dtype=torch.bfloat16, device="cuda")
+    L.lora_base_fused(ctx, table, c["ids"], to_dev(c["x"]), to_dev(W), y)
+    ctx.sync_status()
+    ref = oracle.base_fused(oracle.Table.from_case(c), c["ids"], c["x"], W, nthreads=4)
+    assert_parity(from_dev(y), ref, REL_FROB, MAX_ABS_RMS,
+                  f"seed {seed}: n={c['n']} d_in={c['d_in']} d_out={c['d_out']}")
+
+
+@pytest.mark.parametrize("seed", range(N_OTHER))
+def test_random_merge_and_unmerge_match_oracle(ctx, seed):
+    """lora_merge then lora_unmerge of a drawn adapter on a drawn W, on the kernel the
+    library picks and on the CUDA-core one, every element against the oracle."""
+    c, _ = draw(20_000 + seed)
+    table = upload_table(ctx, c)
+    t = oracle.Table.from_case(c)
+    k = seed % len(c["rank"])
+    W = workloads.make_W(c["d_in"], c["d_out"], seed=seed)
+    for path in (0, 1):
+        ctx.set_option(L.OPT_MERGE_KERNEL, path)
+        try:
+            Wd = to_dev(W)
+            L.lora_merge(ctx, table, k, Wd)
+            ctx.sync_status()
+            merged = from_dev(Wd)
+            ref = oracle.merge(t, k, W, +1)
+            assert_parity(merged, ref, REL_FROB, MAX_ABS_RMS, f"seed {seed} merge path {path}")
+            L.lora_unmerge(ctx, table, k, Wd)
+            ctx.sync_status()
+            assert_parity(from_dev(Wd), oracle.merge(t, k, merged, -1), REL_FROB, MAX_ABS_RMS,
+                          f"seed {seed} unmerge path {path}")
+        finally:
+            ctx.set_option(L.OPT_MERGE_KERNEL, 0)
+
+
+@pytest.mark.parametrize("seed", range(N_OTHER))
+def test_random_device_ids_match_host_planned(ctx, seed):
+    """lora_fused_device_ids on a drawn case, in both modes, against the oracle."""
+    c, opts = draw(30_000 + seed)
+    table = upload_table(ctx, c)
+    x = to_dev(c["x"])
+    ids_dev = torch.from_numpy(np.ascontiguousarray(c["ids"], np.int32)).cuda()
+    try:
+        for mode in (0, 1):
+            ctx.set_option(L.OPT_DEVICE_PLAN, mode)
+            ctx.set_option(L.OPT_EARLY_INPUT, opts[L.OPT_EARLY_INPUT])
+            y = to_dev(c["y"])
+            L.lora_fused_device_ids(ctx, table, ids_dev, x, y)
+            ctx.sync_status()
+            ref = oracle.fused(oracle.Table.from_case(c), c["ids"], c["x"], c["y"], nthreads=4)
+            assert_parity(from_dev(y), ref, REL_FROB, MAX_ABS_RMS, f"seed {seed} mode {mode}")
+            rel = c["ids"] < 0
+            np.testing.assert_array_equal(from_dev(y)[rel], c["y"][rel])
+    finally:
+        ctx.set_option(L.OPT_DEVICE_PLAN, 0)
+        ctx.set_option(L.OPT_EARLY_INPUT, 0)
