@@ -807,19 +807,28 @@ def measure(name, K, W, args, L, torch, ctx, dist, world, local, clocks, cpu_bud
     tc_peak = pk["bf16_tflops_sustained"] if sec >= 0.25 else pk["bf16_tflops"]
     tc_src = "bf16_tflops_sustained" if sec >= 0.25 else "bf16_tflops"
     bracketed = sum(m for (m, n) in prof.values() if n)
+    n_fams = sum(1 for (m, n) in prof.values() if n and m > 0)
     per_family = {}
     for f, (m, n) in prof.items():
         if n and m > 0:
             share_s = sec * (m / bracketed)
-            gbs = fam_bytes.get(f, 0) / share_s / 1e9
+            # A launch's duration.  One kernel family: the region over its launches
+            # (consecutive launches overlap, and that is the rate they sustain).
+            # Several: each launch as timed alone by the events around it.  The
+            # families' launches overlap one another by an amount nothing measures, so
+            # the region is not divided between them; the bracketed time is the
+            # conservative figure (it includes the launch's own ramp, unhidden).
+            dur_s = share_s / n if n_fams == 1 else m / 1e3 / n
+            gbs = fam_bytes.get(f, 0) / n / dur_s / 1e9
             e = {"kernel": KERNEL_NAMES[f], "launches": n,
-                 "us_per_launch": round(1e6 * share_s / n, 3),
+                 "us_per_launch": round(1e6 * dur_s, 3),
                  "us_per_launch_bracketed": round(1e3 * m / n, 3),
+                 "us_per_launch_share_of_region": round(1e6 * share_s / n, 3),
                  "alg_bytes_per_launch": fam_bytes.get(f, 0) / n,
                  "GB/s": round(gbs, 1), "frac": round(gbs / pk["hbm_gbs"], 4), "bound": "hbm",
                  "traffic": None if b.device_ids else measured_traffic(name, f)}
             if f == "proj":
-                tf = fam_flops.get(f, 0) / share_s / 1e12
+                tf = fam_flops.get(f, 0) / n / dur_s / 1e12
                 e.update({"bound": "tensor", "alg_flops_per_launch": fam_flops.get(f, 0) / n,
                           "TFLOP/s": round(tf, 1), "frac": round(tf / tc_peak, 4),
                           "frac_of_hbm": round(gbs / pk["hbm_gbs"], 4)})
@@ -835,6 +844,7 @@ def measure(name, K, W, args, L, torch, ctx, dist, world, local, clocks, cpu_bud
         peak_src = ("measured (MEASURED_PEAKS.json hbm_gbs, STREAM-style copy)"
                     if pk["source"] == "measured" else "fallback 6.8 TB/s")
     flops_total = sum(b.flops_step(W + i) for i in range(K))
+    bytes_total = sum(fam_bytes.values())
     if b.is_merge:
         value, unit = 2 * K * world / sec, "merge+unmerge calls/s"
     else:
@@ -852,6 +862,10 @@ def measure(name, K, W, args, L, torch, ctx, dist, world, local, clocks, cpu_bud
                      "bytes_per_launch": per_family[dominant]["alg_bytes_per_launch"],
                      "us_per_launch": per_family[dominant]["us_per_launch"],
                      "per_family": per_family,
+                     # the whole call: every family's algorithmic bytes over the region
+                     "path": {"bytes_per_step": bytes_total / K,
+                              "GB/s": round(bytes_total / sec / 1e9, 1),
+                              "frac_of_hbm": round(bytes_total / sec / 1e9 / pk["hbm_gbs"], 4)},
                      "tflops": flops_total / max(1e-12, sec) / 1e12},
         "gpu_launches": n_launched,
         "clocks": clk,
