@@ -91,3 +91,34 @@ def test_noalloc_rejects_more_scattered_rows_than_its_parameter_plan():
     _refused(ctx, workloads.small(seed=75, n=ids.size, d_in=64, d_out=64, n_adapters=2,
                                   ranks=[8, 8], ids=ids))
     ctx.close()
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_noalloc_on_drawn_cases_matches_the_oracle(seed):
+    """lora_fused_noalloc on drawn cases within its limits (the sweep's shapes,
+    storage, releases, id layouts and options): the oracle's result, released rows
+    bit-exact."""
+    from tests.test_gpu_sweep import draw
+    c, opts = draw(40_000 + seed)
+    ctx = L.Context(0, max_rows=1024, max_rank=64)
+    try:
+        for k, v in opts.items():
+            if k != L.OPT_TILE_MIN_RUN:
+                ctx.set_option(k, v)
+        table = upload_table(ctx, c)
+        y = to_dev(c["y"])
+        try:
+            L.lora_fused_noalloc(ctx, table, c["ids"], to_dev(c["x"]), y)
+        except L.LoraError as e:
+            # past a fixed limit: refused before any launch, y untouched
+            assert e.name == "LORA_E_CAPACITY"
+            np.testing.assert_array_equal(from_dev(y), c["y"])
+            return
+        ctx.sync_status()
+        got = from_dev(y)
+        ref = oracle.fused(oracle.Table.from_case(c), c["ids"], c["x"], c["y"], nthreads=4)
+        assert_parity(got, ref, REL_FROB, MAX_ABS_RMS, f"seed {seed}")
+        rel = c["ids"] < 0
+        np.testing.assert_array_equal(got[rel], c["y"][rel])
+    finally:
+        ctx.close()
