@@ -163,6 +163,33 @@ def test_device_ids_call_checks_its_arguments_on_the_host():
     assert L.ERROR_NAMES[L._L.lora_selftest_timeout(ctx.handle, 10, None)] == "LORA_E_UNSUPPORTED"
 
 
+def test_argument_block_calls_check_like_the_calls_they_stand_for():
+    """lora_fused_args_call / lora_fused_device_ids_args_call: a null block is
+    refused, and a filled block gives the codes of the eleven-argument calls (here on
+    a host-only context: argument errors first, then no device)."""
+    import ctypes
+
+    import adapter_sgmv_bgmv_gb300 as L
+    from adapter_sgmv_bgmv_gb300 import _lib
+    ctx, t = _host_table()
+    ids = np.zeros(4, np.int32)
+    x = np.zeros((4, 64), np.uint16)
+    y = np.zeros((4, 64), np.uint16)
+    for name, plain in (("lora_fused_args_call", "lora_fused"),
+                        ("lora_fused_device_ids_args_call", "lora_fused_device_ids")):
+        fn = getattr(L._L, name)
+        assert L.ERROR_NAMES[fn(None)] == "LORA_E_INVAL"
+        for n, d in ((4, 64), (5000, 64), (4, 72), (0, 64), (4, 64)):
+            blk = _lib.FusedArgs(ctx=ctx.handle, table=t.handle, ids=ids.ctypes.data, n=n,
+                                 x=x.ctypes.data, ldx=64, y=y.ctypes.data, ldy=64, d_in=d,
+                                 d_out=d, stream=None)
+            a = L.ERROR_NAMES[fn(ctypes.byref(blk))]
+            b = L.ERROR_NAMES[getattr(L._L, plain)(ctx.handle, t.handle, ids.ctypes.data, n,
+                                                   x.ctypes.data, 64, d, y.ctypes.data, 64, d,
+                                                   None)]
+            assert a == b, (name, n, d, a, b)
+
+
 def test_library_plan_errors_on_host():
     import adapter_sgmv_bgmv_gb300 as L
     ctx, t = _host_table()
